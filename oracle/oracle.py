@@ -1,0 +1,254 @@
+"""ctypes front end of the CPU oracle (``mpm_oracle.c``).
+
+TEST INFRASTRUCTURE: imported only by the test suite, ``__graft_entry__`` (its
+smoke check and its build step) and ``bench.py``'s CPU-baseline leg.  It shares
+no code with the CUDA library and never loads it.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mpm_oracle.c")
+_OUT = os.path.join(_HERE, "_build", "libmpm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fno-strict-aliasing",
+          "-std=gnu11", "-Wall", "-shared", "-fPIC"]
+
+
+def build(force: bool = False) -> str:
+    """Compiles the oracle with gcc (contraction off) into ``oracle/_build``."""
+    os.makedirs(os.path.dirname(_OUT), exist_ok=True)
+    if force or not os.path.exists(_OUT) or os.path.getmtime(_OUT) < os.path.getmtime(_SRC):
+        tmp = _OUT + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _OUT)
+    return _OUT
+
+
+class Desc(ct.Structure):
+    _fields_ = [("dim", ct.c_int32), ("n", ct.c_int32 * 3), ("dx", ct.c_float),
+                ("inv_dx", ct.c_float), ("order", ct.c_int32), ("acc_mode", ct.c_int32),
+                ("scale_log2", ct.c_int32), ("tile", ct.c_int32), ("boundary_nodes", ct.c_int32)]
+
+
+def desc_from(grid: dict) -> Desc:
+    d = Desc()
+    d.dim = grid["dim"]
+    for i in range(3):
+        d.n[i] = grid["n"][i] if i < len(grid["n"]) else 1
+    d.dx = grid["dx"]
+    d.inv_dx = grid["inv_dx"]
+    d.order = grid["order"]
+    d.acc_mode = grid["acc_mode"]
+    d.scale_log2 = grid["scale_log2"]
+    d.tile = grid["tile"]
+    d.boundary_nodes = grid["boundary_nodes"]
+    return d
+
+
+_P = ct.c_void_p
+_PP = ct.POINTER(ct.c_void_p)
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ct.CDLL(build())
+            L.orc_nodes.argtypes = [ct.POINTER(Desc)]
+            L.orc_nodes.restype = ct.c_int64
+            L.orc_num_tiles.argtypes = [ct.POINTER(Desc)]
+            L.orc_num_tiles.restype = ct.c_int64
+            L.orc_quadratic_weights.argtypes = [ct.c_float, _P]
+            L.orc_quadratic_weights.restype = None
+            L.orc_quadratic_weights_many.argtypes = [ct.c_int64, _P, _P]
+            L.orc_quadratic_weights_many.restype = None
+            L.orc_bin.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _P, _P, _P]
+            L.orc_bin.restype = ct.c_int64
+            L.orc_p2g_fixed.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _PP, _PP, _P, _P, _P]
+            L.orc_p2g_fixed.restype = ct.c_uint32
+            L.orc_p2g_float.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _PP, _PP, _P, _P, _P]
+            L.orc_p2g_float.restype = ct.c_uint32
+            L.orc_grid_update_fixed.argtypes = [ct.POINTER(Desc), _P, _P, _P]
+            L.orc_grid_update_fixed.restype = None
+            L.orc_grid_update_float.argtypes = [ct.POINTER(Desc), _P, _P, _P]
+            L.orc_grid_update_float.restype = None
+            L.orc_g2p.argtypes = [ct.POINTER(Desc), _P, ct.c_int64, _PP, _PP, _PP, ct.c_float]
+            L.orc_g2p.restype = ct.c_int64
+            L.orc_rdiv.argtypes = [ct.c_int64, ct.c_int64]
+            L.orc_rdiv.restype = ct.c_int64
+            L.orc_cic_int_bound.argtypes = [ct.c_int, _P, ct.c_int64, _PP, _P, _PP]
+            L.orc_cic_int_bound.restype = ct.c_int
+            L.orc_cic_int_p2g.argtypes = [ct.c_int, _P, ct.c_int64, _PP, _P, _PP, _P, _P]
+            L.orc_cic_int_p2g.restype = ct.c_int
+            L.orc_cic_int_gather.argtypes = [ct.c_int, _P, ct.c_int64, _PP, _P, _PP]
+            L.orc_cic_int_gather.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ct.c_void_p(a.ctypes.data)
+
+
+def _rows(a: np.ndarray):
+    """Pointer array to the rows of a C-contiguous 2-D array (keeps ``a`` alive via caller)."""
+    arr = (ct.c_void_p * a.shape[0])()
+    for i in range(a.shape[0]):
+        arr[i] = a[i].ctypes.data
+    return arr
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def grid_nodes(grid: dict) -> int:
+    return int(lib().orc_nodes(ct.byref(desc_from(grid))))
+
+
+def num_tiles(grid: dict) -> int:
+    return int(lib().orc_num_tiles(ct.byref(desc_from(grid))))
+
+
+def quadratic_weights(f: float) -> np.ndarray:
+    w = np.zeros(3, dtype=np.float32)
+    lib().orc_quadratic_weights(ct.c_float(f), _ptr(w))
+    return w
+
+
+def quadratic_weights_many(f: np.ndarray) -> np.ndarray:
+    f = _f32(f)
+    w = np.zeros((f.shape[0], 3), dtype=np.float32)
+    lib().orc_quadratic_weights_many(f.shape[0], _ptr(f), _ptr(w))
+    return w
+
+
+def bin_particles(grid: dict, x: np.ndarray):
+    """Returns (key u32 [n], perm u32 [n], tile_count u32 [ntiles], n_valid)."""
+    x = _f32(x)
+    n = x.shape[1]
+    d = desc_from(grid)
+    key = np.zeros(n, dtype=np.uint32)
+    perm = np.zeros(n, dtype=np.uint32)
+    cnt = np.zeros(num_tiles(grid), dtype=np.uint32)
+    valid = lib().orc_bin(ct.byref(d), n, _rows(x), _ptr(key), _ptr(perm), _ptr(cnt))
+    return key, perm, cnt, int(valid)
+
+
+def p2g_fixed(grid: dict, x, v, C, m):
+    """Fixed-point P2G: returns (acc int64 [(dim+1), nodes], status bits, counts[2])."""
+    x, v, C, m = _f32(x), _f32(v), _f32(C), _f32(m)
+    d = desc_from(grid)
+    nodes = grid_nodes(grid)
+    acc = np.zeros((grid["dim"] + 1, nodes), dtype=np.int64)
+    counts = np.zeros(2, dtype=np.int64)
+    st = lib().orc_p2g_fixed(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m),
+                             _ptr(acc), _ptr(counts))
+    return acc, int(st), counts
+
+
+def p2g_float(grid: dict, x, v, C, m):
+    """Float-atomic P2G with fp64 sums: returns (acc float64 [(dim+1), nodes], status, counts)."""
+    x, v, C, m = _f32(x), _f32(v), _f32(C), _f32(m)
+    d = desc_from(grid)
+    nodes = grid_nodes(grid)
+    acc = np.zeros((grid["dim"] + 1, nodes), dtype=np.float64)
+    counts = np.zeros(2, dtype=np.int64)
+    st = lib().orc_p2g_float(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m),
+                             _ptr(acc), _ptr(counts))
+    return acc, int(st), counts
+
+
+def dtg_of(grid: dict) -> np.ndarray:
+    """dt * g, each product rounded to fp32 (the grid update adds this vector)."""
+    dt = np.float32(grid["dt"])
+    return np.array([dt * np.float32(c) for c in (list(grid["g"]) + [0.0] * 3)[:3]], dtype=np.float32)
+
+
+def grid_update_fixed(grid: dict, acc: np.ndarray) -> np.ndarray:
+    acc = np.ascontiguousarray(acc, dtype=np.int64)
+    vel = np.zeros((grid["dim"], grid_nodes(grid)), dtype=np.float32)
+    dtg = dtg_of(grid)
+    lib().orc_grid_update_fixed(ct.byref(desc_from(grid)), _ptr(acc), _ptr(dtg), _ptr(vel))
+    return vel
+
+
+def grid_update_float(grid: dict, acc: np.ndarray) -> np.ndarray:
+    acc = np.ascontiguousarray(acc, dtype=np.float64)
+    vel = np.zeros((grid["dim"], grid_nodes(grid)), dtype=np.float32)
+    dtg = dtg_of(grid)
+    lib().orc_grid_update_float(ct.byref(desc_from(grid)), _ptr(acc), _ptr(dtg), _ptr(vel))
+    return vel
+
+
+def g2p(grid: dict, vel: np.ndarray, x, v=None, C=None):
+    """G2P: returns (x', v', C', moved) as new fp32 arrays.  Particles outside
+    the domain keep their inputs (zeros where ``v``/``C`` are not given)."""
+    vel = _f32(vel)
+    x = _f32(x).copy()
+    dim = grid["dim"]
+    n = x.shape[1]
+    v = _f32(v).copy() if v is not None else np.zeros((dim, n), dtype=np.float32)
+    C = _f32(C).copy() if C is not None else np.zeros((dim * dim, n), dtype=np.float32)
+    moved = lib().orc_g2p(ct.byref(desc_from(grid)), _ptr(vel), n, _rows(x), _rows(v), _rows(C),
+                          ct.c_float(grid["dt"]))
+    return x, v, C, int(moved)
+
+
+def rdiv(a: int, b: int) -> int:
+    return int(lib().orc_rdiv(a, b))
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _i64(a):
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def cic_int_bound(grid: dict, X, m, v) -> bool:
+    X, m, v = _i32(X), _i64(m), _i64(v)
+    n = np.array(grid["n"][:3], dtype=np.int32)
+    return bool(lib().orc_cic_int_bound(grid["dim"], _ptr(n), X.shape[1], _rows(X), _ptr(m), _rows(v)))
+
+
+def cic_int_p2g(grid: dict, X, m, v, order=None):
+    """Integer CIC scatter in the given particle order; returns (acc, ok)."""
+    X, m, v = _i32(X), _i64(m), _i64(v)
+    dim = grid["dim"]
+    n = np.array(grid["n"][:3], dtype=np.int32)
+    nodes = int(np.prod(n[:dim]))
+    acc = np.zeros((dim + 1, nodes), dtype=np.int64)
+    o = _i64(order) if order is not None else None
+    ok = lib().orc_cic_int_p2g(dim, _ptr(n), X.shape[1], _rows(X), _ptr(m), _rows(v),
+                               _ptr(o) if o is not None else None, _ptr(acc))
+    return acc, bool(ok)
+
+
+def cic_int_gather(grid: dict, X, acc):
+    X, acc = _i32(X), _i64(acc)
+    dim = grid["dim"]
+    n = np.array(grid["n"][:3], dtype=np.int32)
+    out = np.zeros((dim, X.shape[1]), dtype=np.int64)
+    lib().orc_cic_int_gather(dim, _ptr(n), X.shape[1], _rows(X), _ptr(acc), _rows(out))
+    return out
+
+
+def step_fixed(grid: dict, x, v, C, m):
+    """One full oracle step in a fixed-point mode: bin, P2G, grid update, G2P."""
+    key, perm, cnt, valid = bin_particles(grid, x)
+    acc, st, counts = p2g_fixed(grid, x, v, C, m)
+    vel = grid_update_fixed(grid, acc)
+    x2, v2, C2, moved = g2p(grid, vel, x, v, C)
+    return dict(key=key, perm=perm, tile_count=cnt, n_valid=valid, acc=acc, status=st,
+                counts=counts, vel=vel, x=x2, v=v2, C=C2)

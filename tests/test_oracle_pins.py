@@ -1,0 +1,423 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Every check here is independent of the oracle's own arithmetic: closed forms
+(the quadratic B-spline, its moments), exact rational arithmetic (Python
+``Fraction`` with round-half-even), brute-force all-nodes loops in fp64 with
+the B-spline written as a function of distance, library routines (numpy's
+stable argsort), invariants (conservation, order independence, APIC's
+reproduction of affine fields) and the values the integer-transfer page prints.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from material_point_particle_gb300 import workloads as W
+from oracle import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# independent helpers
+
+def phi2(r):
+    """Cardinal quadratic B-spline of the distance r (in cells), fp64."""
+    r = np.abs(np.asarray(r, dtype=np.float64))
+    return np.where(r < 0.5, 0.75 - r * r, np.where(r < 1.5, 0.5 * (1.5 - r) ** 2, 0.0))
+
+
+def node_coords(grid):
+    dim = grid["dim"]
+    axes = [np.arange(grid["n"][l]) for l in range(dim)]
+    mesh = np.meshgrid(*axes[::-1], indexing="ij")[::-1]  # node index (k*n1 + j)*n0 + i
+    return np.stack([m.ravel() for m in mesh]).astype(np.float64)  # [dim, nodes]
+
+
+def brute_force_p2g(grid, x, v, C, m):
+    """All nodes x all particles in fp64: mass and APIC momentum m w (v + C (x_i - x_p))."""
+    dim = grid["dim"]
+    X = node_coords(grid)
+    dx = float(grid["dx"])
+    xi = x.astype(np.float64) * float(grid["inv_dx"])
+    nodes = X.shape[1]
+    mass = np.zeros(nodes)
+    mom = np.zeros((dim, nodes))
+    absterm = np.zeros(nodes)
+    for p in range(x.shape[1]):
+        w = np.ones(nodes)
+        for l in range(dim):
+            w *= phi2(X[l] - xi[l, p])
+        dvec = (X - xi[:, p:p + 1]) * dx
+        Cp = C[:, p].astype(np.float64).reshape(dim, dim)
+        vel = v[:, p:p + 1].astype(np.float64) + Cp @ dvec
+        mass += m[p] * w
+        mom += m[p] * w * vel
+        absterm += np.abs(m[p] * w) * (1.0 + np.abs(vel).sum(axis=0))
+    return mass, mom, absterm
+
+
+def rne_fraction(fr: Fraction) -> int:
+    return round(fr)  # Fraction.__round__ rounds half to even
+
+
+# --------------------------------------------------------------------------
+# B-spline weights (tensor-core PIC page, shape functions Eq. 12: non-negative,
+# partition of unity; the quadratic moments are textbook identities)
+
+def test_weights_closed_form_and_moments():
+    s = W.Stream(12345, 1)
+    f = (0.5 + s.uniform24(1_000_000)).astype(np.float32)
+    f = np.concatenate([f, np.float32([0.5, 1.0, np.nextafter(np.float32(1.5), np.float32(0))])])
+    w = O.quadratic_weights_many(f).astype(np.float64)
+    fd = f.astype(np.float64)
+    a = np.arange(3, dtype=np.float64)[None, :]
+    e = a - fd[:, None]
+    assert np.all(w >= 0.0)
+    assert np.max(np.abs(w.sum(axis=1) - 1.0)) <= 1e-6
+    assert np.max(np.abs((w * e).sum(axis=1))) <= 1e-6
+    assert np.max(np.abs((w * e * e).sum(axis=1) - 0.25)) <= 1e-6
+    ref = phi2(e)
+    assert np.max(np.abs(w - ref)) <= 2e-7
+
+
+# --------------------------------------------------------------------------
+# binning: keys name the stencil base cell; perm is the stable sort of keys
+# ("Particle Worlds, part 3", Step 3: counting sort)
+
+@pytest.mark.parametrize("dim,n,tile", [(2, 40, 8), (3, 24, 4), (3, 21, 4)])
+def test_bin_is_stable_sort_of_base_cells(dim, n, tile):
+    cloud = W.small_cloud(dim, 3000, n, seed=11 + dim + n, lo=-0.05, hi=1.05, tile=tile)
+    grid, x = cloud["grid"], cloud["x"]
+    key, perm, cnt, valid = O.bin_particles(grid, x)
+    xi = x.astype(np.float64) * float(np.float32(grid["inv_dx"]))
+    inside = np.all((xi >= 0.5) & (xi < np.array(grid["n"][:dim])[:, None] - 1.5), axis=0)
+    assert valid == int(inside.sum())
+    assert np.all(key[~inside] == 0xFFFFFFFF)
+    # decode key -> base cell and check that the particle lies in [b+0.5, b+1.5)
+    T = tile
+    ntl = [(grid["n"][l] - 2 + T - 1) // T for l in range(dim)]
+    k = key[inside].astype(np.int64)
+    local, tid = k % (T ** dim), k // (T ** dim)
+    b = np.zeros((dim, k.size), dtype=np.int64)
+    for l in range(dim):
+        b[l] = (tid % ntl[l]) * T + (local % T)
+        tid //= ntl[l]
+        local //= T
+    fr = xi[:, inside] - b
+    assert np.all((fr >= 0.5) & (fr < 1.5))
+    assert np.all((b >= 0) & (b <= np.array(grid["n"][:dim])[:, None] - 3))
+    # perm: numpy's stable argsort over the in-domain keys, then the rest in order
+    idx = np.nonzero(inside)[0]
+    expect = np.concatenate([idx[np.argsort(key[idx], kind="stable")], np.nonzero(~inside)[0]])
+    assert np.array_equal(perm.astype(np.int64), expect)
+    assert np.array_equal(cnt.astype(np.int64),
+                          np.bincount(key[idx] // (T ** dim), minlength=cnt.size))
+
+
+# --------------------------------------------------------------------------
+# fixed-point P2G against brute force, conservation and order independence
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_p2g_fixed_matches_brute_force(dim):
+    n = 8
+    cloud = W.small_cloud(dim, 48, n, seed=100 + dim, lo=0.2, hi=0.8, vsig=1.0, csig=3.0,
+                          scale_log2=18, mass_lo=0.5, mass_hi=2.0)
+    grid = cloud["grid"]
+    acc, st, counts = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert st == 0 and counts.sum() == 0
+    S = 2.0 ** grid["scale_log2"]
+    mass, mom, absterm = brute_force_p2g(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    touched = np.zeros(mass.size)
+    xi = cloud["x"].astype(np.float64) * grid["inv_dx"]
+    X = node_coords(grid)
+    for p in range(xi.shape[1]):
+        inside = np.ones(mass.size, dtype=bool)
+        for l in range(dim):
+            inside &= np.abs(X[l] - xi[l, p]) < 1.5
+        touched += inside
+    tol = (13.5 * touched + 1.0) / S + 2e-6 * absterm
+    assert np.all(np.abs(acc[0] / S - mass) <= tol)
+    for k in range(dim):
+        assert np.all(np.abs(acc[1 + k] / S - mom[k]) <= tol)
+    # the affine term is large here: dropping it would fail the bound by far
+    assert np.max(np.abs(mom)) > 0 and np.max(absterm) > 0
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_p2g_float_matches_brute_force(dim):
+    n = 8
+    cloud = W.small_cloud(dim, 48, n, seed=200 + dim, lo=0.2, hi=0.8, vsig=1.0, csig=3.0,
+                          acc_mode=W.ACC_F32, scale_log2=0, mass_lo=0.5, mass_hi=2.0)
+    grid = cloud["grid"]
+    acc, st, counts = O.p2g_float(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    mass, mom, absterm = brute_force_p2g(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    tol = 2e-6 * absterm + 1e-12
+    assert np.all(np.abs(acc[0] - mass) <= tol)
+    for k in range(dim):
+        assert np.all(np.abs(acc[1 + k] - mom[k]) <= tol)
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_grid_totals_equal_particle_totals(dim):
+    cloud = W.small_cloud(dim, 4000, 32, seed=300 + dim, vsig=2.0, csig=1.0, scale_log2=17,
+                          mass_lo=0.25, mass_hi=3.0)
+    grid = cloud["grid"]
+    acc, st, counts = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert st == 0
+    S = np.float32(2.0 ** grid["scale_log2"])
+    Mt = cloud["m"].astype(np.float32) * S
+    # particle totals Q: rint of the fp32 scaled mass and of its fp32 product with v
+    Qm = sum(int(q) for q in np.rint(Mt.astype(np.float64)))
+    assert int(acc[0].sum()) == Qm
+    for k in range(dim):
+        Qk = (Mt * cloud["v"][k].astype(np.float32)).astype(np.float32)
+        assert int(acc[1 + k].sum()) == sum(int(q) for q in np.rint(Qk.astype(np.float64)))
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_scrambled_orders_give_identical_grids(dim):
+    cloud = W.small_cloud(dim, 2048, 24, seed=400 + dim, scale_log2=19)
+    grid = cloud["grid"]
+    base, _, _ = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    for a, b in [(97, 13), (1, 13), (1023, 5), (3, 2047)]:
+        pi = W.scrambled_order(2048, a, b)
+        acc, _, _ = O.p2g_fixed(grid, cloud["x"][:, pi], cloud["v"][:, pi], cloud["C"][:, pi],
+                                cloud["m"][pi])
+        assert np.array_equal(acc, base)
+
+
+def test_out_of_domain_and_out_of_range_particles_are_counted_not_scattered():
+    cloud = W.small_cloud(3, 64, 16, seed=501, scale_log2=19)
+    grid = cloud["grid"]
+    x, v, C, m = cloud["x"].copy(), cloud["v"].copy(), cloud["C"].copy(), cloud["m"].copy()
+    x[0, 3] = 0.0            # below the lowest stencil
+    x[1, 7] = 1.0            # above the highest
+    x[2, 9] = np.nan
+    m[11] = 1e6              # shares would not fit
+    v[1, 12] = np.inf
+    acc, st, counts = O.p2g_fixed(grid, x, v, C, m)
+    assert st == 3 and counts[0] == 3 and counts[1] == 2
+    keep = np.ones(64, dtype=bool)
+    keep[[3, 7, 9, 11, 12]] = False
+    ref, st2, _ = O.p2g_fixed(grid, x[:, keep], v[:, keep], C[:, keep], m[keep])
+    assert st2 == 0 and np.array_equal(acc, ref)
+
+
+# --------------------------------------------------------------------------
+# grid update: hand-made nodes (implementation guide 2.1 / 3.3.2 sign test)
+
+def test_grid_update_cases():
+    grid = W.small_cloud(3, 1, 10, seed=1)["grid"]
+    grid["dt"] = float(np.float32(0.5))
+    grid["g"] = [0.0, -2.0, 0.0]
+    nodes = 1000
+    acc = np.zeros((4, nodes), dtype=np.int64)
+
+    def idx(i, j, k):
+        return (k * 10 + j) * 10 + i
+
+    acc[:, idx(5, 5, 5)] = [4, 8, -4, 2]      # v = (2, -1, 0.5) + (0, -1, 0)
+    acc[:, idx(1, 5, 5)] = [2, -2, 0, 0]      # x < 3 and v_x < 0: stopped
+    acc[:, idx(1, 6, 5)] = [2, 2, 0, 0]       # moving away from the wall: kept
+    acc[:, idx(8, 5, 5)] = [2, 2, 0, 0]       # x > n-1-3 and v_x > 0: stopped
+    acc[:, idx(4, 2, 4)] = [2, 0, 0, 0]       # y near floor, gravity pulls down: stopped
+    acc[:, idx(4, 4, 4)] = [0, 5, 5, 5]       # empty node: zero
+    vel = O.grid_update_fixed(grid, acc)
+    assert list(vel[:, idx(5, 5, 5)]) == [2.0, -2.0, 0.5]
+    assert list(vel[:, idx(1, 5, 5)]) == [0.0, -1.0, 0.0]
+    assert list(vel[:, idx(1, 6, 5)]) == [1.0, -1.0, 0.0]
+    assert list(vel[:, idx(8, 5, 5)]) == [0.0, -1.0, 0.0]
+    assert list(vel[:, idx(4, 2, 4)]) == [0.0, 0.0, 0.0]
+    assert list(vel[:, idx(4, 4, 4)]) == [0.0, 0.0, 0.0]
+    assert np.count_nonzero(vel) == 7
+
+
+# --------------------------------------------------------------------------
+# G2P: quadratic B-splines reproduce affine fields; APIC recovers the gradient
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_g2p_reproduces_affine_velocity_field(dim):
+    n = 16
+    cloud = W.small_cloud(dim, 500, n, seed=600 + dim, lo=0.15, hi=0.85)
+    grid = cloud["grid"]
+    s = W.Stream(77, dim)
+    A = s.normal(dim * dim, 1.0).reshape(dim, dim)
+    c = s.normal(dim, 1.0)
+    X = node_coords(grid) * grid["dx"]
+    vel = (A @ X + c[:, None]).astype(np.float32)
+    grid["dt"] = float(np.float32(1e-3))
+    x2, v2, C2, moved = O.g2p(grid, vel, cloud["x"])
+    assert moved == 500
+    xp = cloud["x"].astype(np.float64)
+    vexp = A @ xp + c[:, None]
+    assert np.max(np.abs(v2 - vexp)) <= 2e-5
+    assert np.max(np.abs(C2 - A.reshape(dim * dim, 1))) <= 2e-3
+    assert np.max(np.abs(x2 - (xp + grid["dt"] * v2.astype(np.float64)))) <= 1e-6
+
+
+@pytest.mark.parametrize("mode", ["fixed", "float"])
+def test_single_particle_apic_round_trip(mode):
+    """P2G -> grid update -> G2P of one particle returns its v and C (APIC is
+    exact for affine velocity fields; no gravity, no walls nearby)."""
+    dim = 3
+    grid = W.small_cloud(3, 1, 32, seed=1, scale_log2=20)["grid"]
+    grid["g"] = [0.0, 0.0, 0.0]
+    if mode == "float":
+        grid["acc_mode"] = W.ACC_F32
+    s = W.Stream(99, 3)
+    for trial in range(20):
+        x = (0.3 + 0.4 * s.uniform24(3)).astype(np.float32).reshape(3, 1)
+        v = s.normal(3, 1.0).astype(np.float32).reshape(3, 1)
+        C = s.normal(9, 2.0).astype(np.float32).reshape(9, 1)
+        m = np.float32([1.0])
+        if mode == "fixed":
+            acc, st, _ = O.p2g_fixed(grid, x, v, C, m)
+            vel = O.grid_update_fixed(grid, acc)
+            tol_v, tol_c = 1e-4, 2e-2
+        else:
+            acc, st, _ = O.p2g_float(grid, x, v, C, m)
+            vel = O.grid_update_float(grid, acc)
+            tol_v, tol_c = 1e-5, 2e-3
+        assert st == 0
+        x2, v2, C2, moved = O.g2p(grid, vel, x)
+        assert moved == 1
+        assert np.max(np.abs(v2 - v)) <= tol_v * (1 + np.abs(v).max())
+        assert np.max(np.abs(C2 - C)) <= tol_c * (1 + np.abs(C).max())
+
+
+def test_step_conserves_momentum_without_gravity_or_walls():
+    cloud = W.small_cloud(3, 3000, 32, seed=701, lo=0.3, hi=0.7, scale_log2=19)
+    grid = cloud["grid"]
+    out = O.step_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    p0 = (cloud["m"][None, :].astype(np.float64) * cloud["v"]).sum(axis=1)
+    p1 = (cloud["m"][None, :].astype(np.float64) * out["v"]).sum(axis=1)
+    assert np.max(np.abs(p1 - p0)) <= 1e-3 * np.abs(cloud["v"]).sum() / 3000 * 10
+
+
+# --------------------------------------------------------------------------
+# the integer CIC transfer page
+
+def test_rdiv_is_round_half_even_division():
+    s = W.Stream(2024, 9)
+    raw = s.bits(4000)
+    qs = (raw[:2000].astype(np.int64) >> np.int64(20)) - (1 << 42)
+    Fs = (raw[2000:] % np.uint64(65536)).astype(np.int64)
+    cases = list(zip(qs.tolist(), Fs.tolist()))
+    cases += [(1, 32768), (3, 32768), (-1, 32768), (-3, 32768), (5, 0), (-7, 65535), (0, 12345),
+              (2**46, 65535), (-(2**46), 65535)]
+    for q, F in cases:
+        far = O.rdiv(q * F, 65536)
+        assert far == rne_fraction(Fraction(q * F, 65536))
+        assert far + (q - far) == q
+    for a, b in [(7, 2), (5, 2), (-5, 2), (-7, 2), (9, -4), (-9, -4), (10, 4), (100, 7)]:
+        assert O.rdiv(a, b) == rne_fraction(Fraction(a, b))
+
+
+def _cic_setup():
+    cfg = W.cic_int()
+    return cfg["grid"], cfg["X"], cfg["m"], cfg["v"]
+
+
+def test_cic_int_totals_are_an_identity():
+    grid, X, m, v = _cic_setup()
+    acc, ok = O.cic_int_p2g(grid, X, m, v)
+    assert ok
+    mom = [int(sum(int(a) * int(b) for a, b in zip(m, v[k]))) for k in range(2)]
+    assert int(acc[0].sum()) == int(m.sum())
+    assert [int(acc[1].sum()), int(acc[2].sum())] == mom
+    # each particle's four mass shares: Fraction check of the two-stage split
+    Xq = X.astype(np.int64)
+    for p in range(0, 256, 17):
+        one, _ = O.cic_int_p2g(grid, X[:, p:p + 1], m[p:p + 1], v[:, p:p + 1])
+        cx, fx = Xq[0, p] >> 16, Xq[0, p] & 0xFFFF
+        cy, fy = Xq[1, p] >> 16, Xq[1, p] & 0xFFFF
+        far_x = rne_fraction(Fraction(int(m[p]) * int(fx), 65536))
+        parts = {cx: int(m[p]) - far_x, cx + 1: far_x}
+        for col, q in parts.items():
+            far_y = rne_fraction(Fraction(q * int(fy), 65536))
+            assert one[0, cy * 9 + col] == q - far_y
+            assert one[0, (cy + 1) * 9 + col] == far_y
+
+
+def test_cic_int_every_scrambled_order_matches():
+    grid, X, m, v = _cic_setup()
+    base, ok = O.cic_int_p2g(grid, X, m, v)
+    assert ok
+    rows = [tuple(int(t) for t in ln.split()) for ln in open(os.path.join(GOLDEN, "p4_scrambled_orders.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    assert [r[0] for r in rows] == list(range(1, 256, 2))
+    for a, float_diff, int_diff in rows:
+        acc, ok = O.cic_int_p2g(grid, X, m, v, W.scrambled_order(256, a, 13))
+        differing = int(np.any(acc != base, axis=0).sum())
+        assert differing == int_diff == 0
+        assert float_diff > 0   # the page's float scatter differs in every order
+
+
+def test_cic_int_gather_is_rounded_cell_mean():
+    grid, X, m, v = _cic_setup()
+    acc, ok = O.cic_int_p2g(grid, X, m, v)
+    out = O.cic_int_gather(grid, X, acc)
+    Xq = X.astype(np.int64)
+    for p in range(256):
+        cx, cy = Xq[0, p] >> 16, Xq[1, p] >> 16
+        nodes = [cy * 9 + cx, cy * 9 + cx + 1, (cy + 1) * 9 + cx, (cy + 1) * 9 + cx + 1]
+        M = int(acc[0, nodes].sum())
+        for k in range(2):
+            assert out[k, p] == rne_fraction(Fraction(int(acc[1 + k, nodes].sum()), M))
+
+
+def test_cic_int_bounds_line_stops_before_any_scatter():
+    grid, X, m, v = _cic_setup()
+    m2 = m.copy()
+    m2[5] = 2**40                      # 256 * 2^40 * 1000 > 2^63
+    acc, ok = O.cic_int_p2g(grid, X, m2, v)
+    assert not ok and not acc.any()
+    X2 = X.copy()
+    X2[0, 9] = 8 * 65536               # a stencil past the last node
+    acc, ok = O.cic_int_p2g(grid, X2, m, v)
+    assert not ok and not acc.any()
+
+
+def test_float_and_double_order_table_qualitatively():
+    """The page's arithmetic table: exact arithmetic (integer, double with
+    dyadic positions) matches in all 128 orders; float, and double with
+    positions in 1/65,535, do not.  Plain numpy scatter, independent of the
+    oracle."""
+    grid, X, m, v = _cic_setup()
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "p4_arithmetic_table.txt"))
+            if ln.strip() and not ln.startswith("#")]
+
+    def scatter(dtype, denom, order):
+        g = np.zeros((3, 81), dtype=dtype)
+        for p in order:
+            fx = dtype(X[0, p] % 65536) / dtype(denom) if denom == 65536 else dtype(X[0, p]) / dtype(denom)
+            fy = dtype(X[1, p] % 65536) / dtype(denom) if denom == 65536 else dtype(X[1, p]) / dtype(denom)
+            if denom != 65536:
+                cx, cy = int(np.floor(fx)), int(np.floor(fy))
+                fx, fy = fx - dtype(cx), fy - dtype(cy)
+            else:
+                cx, cy = int(X[0, p] >> 16), int(X[1, p] >> 16)
+            q = [dtype(m[p]), dtype(m[p]) * dtype(v[0, p]), dtype(m[p]) * dtype(v[1, p])]
+            for (i, j, w) in [(cx, cy, (dtype(1) - fx) * (dtype(1) - fy)), (cx + 1, cy, fx * (dtype(1) - fy)),
+                              (cx, cy + 1, (dtype(1) - fx) * fy), (cx + 1, cy + 1, fx * fy)]:
+                if 0 <= i < 9 and 0 <= j < 9:
+                    for c in range(3):
+                        g[c, j * 9 + i] = dtype(g[c, j * 9 + i] + dtype(q[c] * w))
+        return g
+
+    for name, denom, _, matching in rows:
+        if name == "integer":
+            continue
+        dt = np.float32 if name == "float" else np.float64
+        denom = int(denom)
+        base = scatter(dt, denom, range(256))
+        same = 0
+        for a in range(1, 256, 2):
+            g = scatter(dt, denom, W.scrambled_order(256, a, 13))
+            same += int(np.array_equal(g, base))
+        if int(matching) == 128:
+            assert same == 128
+        else:
+            assert same < 128
