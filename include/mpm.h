@@ -1,0 +1,233 @@
+/*
+ * mpm.h -- C ABI of the GB300 (sm_103a) Material Point Method transfer library.
+ *
+ * One explicit MPM transfer step, in the four phases "reset -> particle-to-grid
+ * (P2G) -> grid update -> grid-to-particle (G2P)" of "Implementation -- GPU
+ * Optimization & Reference Codebases", section 1, plus the cell-key binning
+ * that feeds P2G (section 2.1, "spatial sorting + tiling"; "Particle Worlds,
+ * part 3", Step 3, the counting sort):
+ *
+ *   mpm_bin          cell keys, tile histogram, exclusive scan, stable scatter
+ *   mpm_p2g          scatter of mass and APIC/MLS affine momentum, fixed point
+ *                    (int32/int64) or float atomics
+ *   mpm_grid_update  momentum -> velocity, gravity, boundary; clears the
+ *                    accumulators it reads
+ *   mpm_g2p          gather of velocity and affine matrix, advection
+ *
+ * Conventions shared by every call:
+ *  - All pointers inside the structs are DEVICE pointers unless a call says
+ *    otherwise.  The caller owns all memory; the library allocates nothing.
+ *  - Calls are asynchronous and stream ordered on the stream passed in (a
+ *    cudaStream_t given as void*; NULL is the legacy default stream).
+ *  - Argument errors are found on the host, returned at once, and launch
+ *    nothing.  Data errors (particles outside the domain, shares out of range,
+ *    a failed accumulator bound) are recorded in the device status words of
+ *    mpm_bins; read them with mpm_read_status (asynchronous copy).
+ *  - Particle arrays are structure-of-arrays, one array per component.  The
+ *    affine matrix is C[k*dim + l] = d v_k / d x_l.
+ *  - Grid arrays are planar: channel c of node (i, j, k) is at
+ *    c*nodes + (k*n[1] + j)*n[0] + i.  Accumulator channels: mass, then
+ *    momentum along each axis.  Velocity channels: one per axis.
+ *  - Node i sits at position i*dx; the domain holds particles whose whole
+ *    quadratic stencil lies on the grid, 0.5 <= x*inv_dx < n - 1.5 per axis.
+ */
+#ifndef MPM_GB300_H
+#define MPM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mpm_status {
+    MPM_OK = 0,
+    MPM_E_ARG = 1,        /* bad descriptor, null pointer, unsupported combination */
+    MPM_E_WORKSPACE = 2,  /* workspace too small */
+    MPM_E_DOMAIN = 3,     /* (status bit) particles outside the domain were skipped */
+    MPM_E_BOUND = 4,      /* (status bit) shares or accumulators would not fit */
+    MPM_E_CUDA = 5,       /* a CUDA call failed (launch or copy) */
+    MPM_E_TIMEOUT = 6,    /* reserved: a bounded device wait gave up */
+    MPM_E_NO_DEVICE = 7   /* no usable CUDA device */
+} mpm_status;
+
+typedef enum mpm_acc_mode {
+    MPM_ACC_I32 = 0,       /* fixed point, int32 node accumulators */
+    MPM_ACC_I64 = 1,       /* fixed point, int64 node accumulators */
+    MPM_ACC_F32 = 2,       /* fp32 atomics (order dependent; for comparison) */
+    MPM_ACC_EXACT_INT = 3  /* integer particles, integer CIC split (see mpm_p2g) */
+} mpm_acc_mode;
+
+/* Dense grid descriptor. */
+typedef struct mpm_grid_desc {
+    int32_t dim;            /* 2 or 3 */
+    int32_t n[3];           /* nodes per axis; n[2] ignored (1) in 2D */
+    float dx;               /* node spacing (fp32; the same bits the oracle uses) */
+    float inv_dx;           /* 1/dx, supplied by the caller (fp32) */
+    int32_t order;          /* 2 = quadratic B-spline; 1 = linear (MPM_ACC_EXACT_INT only) */
+    int32_t acc_mode;       /* mpm_acc_mode */
+    int32_t scale_log2;     /* fixed-point scale S = 2^scale_log2, 0..40 */
+    int32_t tile;           /* cells per tile edge: 4 (3D) or 8 (2D) */
+    int32_t boundary_nodes; /* velocity boundary band width in nodes (e.g. 3) */
+} mpm_grid_desc;
+
+/* Particle state (device SoA).  fp32 everywhere, except MPM_ACC_EXACT_INT:
+ * x = int32 positions in 1/65,536 of a cell, v = int64, m = int64, C unused. */
+typedef struct mpm_particles {
+    int64_t n;
+    void *x[3];
+    void *v[3];
+    void *C[9];
+    const void *m;
+} mpm_particles;
+
+/* Status words (device, uint32), in mpm_bins.status. */
+enum {
+    MPM_ST_FLAGS = 0,        /* bit (1 << MPM_E_DOMAIN) | (1 << MPM_E_BOUND) | ... */
+    MPM_ST_N_OUTSIDE = 1,    /* particles outside the domain */
+    MPM_ST_N_OUT_OF_RANGE = 2, /* particles whose shares would not fit (skipped by P2G) */
+    MPM_ST_N_VALID = 3,      /* in-domain particles (length of the sorted part of perm) */
+    MPM_ST_N_SLICES = 4,     /* P2G work items */
+    MPM_ST_N_ACTIVE = 5,     /* tiles holding at least one particle */
+    MPM_ST_MAX_NEIGHBOURS = 6, /* int32 mode: most particles whose stencil covers one node */
+    MPM_ST_N_BIG_TILES = 7,  /* tiles sorted by the large-tile path */
+    MPM_STATUS_WORDS = 16
+};
+
+/* Binning state: device arrays carved out of one caller workspace by
+ * mpm_bins_init.  All read-only for the caller. */
+typedef struct mpm_bins {
+    int64_t n;               /* particle count the workspace was sized for */
+    int64_t ntiles;          /* tiles of tile^dim base cells */
+    int64_t max_slices;
+    uint32_t *key;           /* [n] tile-major base-cell key; 0xFFFFFFFF outside the domain */
+    uint32_t *perm;          /* [n] particle indices in (key, index) order; the
+                                in-domain ones first, then the others in index order */
+    uint32_t *tile_count;    /* [ntiles] particles per tile */
+    uint32_t *tile_start;    /* [ntiles + 1] exclusive prefix of tile_count */
+    uint32_t *slices;        /* [2 * max_slices] P2G work items (tile, first) */
+    uint32_t *active;        /* [ntiles] tiles with particles, ascending */
+    uint32_t *status;        /* [MPM_STATUS_WORDS] */
+    void *scratch;           /* internal */
+    size_t scratch_bytes;
+} mpm_bins;
+
+/* Bytes of workspace mpm_bins_init needs for n particles on this grid. */
+size_t mpm_workspace_bytes(const mpm_grid_desc *desc, int64_t n);
+
+/* Carves `ws` (device, 256-byte aligned, at least mpm_workspace_bytes) into
+ * `out`.  Host only; launches nothing.  MPM_E_WORKSPACE if too small. */
+mpm_status mpm_bins_init(const mpm_grid_desc *desc, int64_t n, void *ws, size_t ws_bytes, mpm_bins *out);
+
+/* Bytes of the accumulator grid ((dim+1) channels of int32/int64/fp32) and of
+ * the velocity grid (dim channels of fp32). */
+size_t mpm_grid_acc_bytes(const mpm_grid_desc *desc);
+size_t mpm_grid_vel_bytes(const mpm_grid_desc *desc);
+
+/* Flags of mpm_bin. */
+enum { MPM_BIN_DEFAULT = 0 };
+
+/*
+ * mpm_bin -- cell keys and a stable counting sort of the particles.
+ * ("Particle Worlds, part 3", Step 3: histogram, exclusive prefix sum, scatter;
+ *  implementation guide section 2.1: bin into tiles, sort an index buffer,
+ *  particles never move; rule 2: index stability.)
+ * key = tile-major id of the particle's stencil base cell b = floor(x*inv_dx - 1/2);
+ * perm = stable order by key (ties by particle index), so the order is a
+ * deterministic function of the keys.  Also builds the active-tile list and
+ * the P2G work list, resets the status words, counts out-of-domain particles,
+ * and in MPM_ACC_I32 mode checks the accumulator bound before any scatter:
+ * every node must be covered by at most 511 particle stencils (511 shares of
+ * magnitude below 2^22 fit int32); otherwise MPM_E_BOUND is set and mpm_p2g
+ * scatters nothing.
+ */
+mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, int flags,
+                   void *stream);
+
+/*
+ * mpm_p2g -- particle-to-grid scatter into `grid_acc` (must be zero on entry;
+ * mpm_grid_update leaves it zero).  Fixed-point modes compute, per particle,
+ *   Mt = m*S, Wt(a) = ((wx[a0]*Mt)*wy[a1])*wz[a2],
+ *   vel_k(a) = fma(C_k2, d_2, fma(C_k1, d_1, fma(C_k0, d_0, v_k))),  d_l = (a_l - f_l)*dx,
+ *   share s_m(a) = rint(Wt(a)), s_k(a) = rint(Wt(a) * vel_k(a)) (exact product,
+ *   one rounding, ties to even), and gives the centre node (1,1,1) the
+ *   remainder Q - sum of the others, with Q_m = rint(Mt), Q_k = rint(Mt*v_k),
+ * so grid totals equal particle totals exactly ("particle to grid transfer in
+ * checked integer arithmetic": split rather than weight; implementation guide
+ * 2.1 and 3.3.1: fixed-point atomics, round rather than truncate).  The result
+ * is bit-identical for every particle order.  A particle whose shares could
+ * reach 2^22 in magnitude (wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) > 2^22 - 4096,
+ * wmax = 0.75^dim) is not scattered and is counted in MPM_ST_N_OUT_OF_RANGE.
+ * MPM_ACC_F32 adds the fp32 values Wt*vel with float atomics instead.
+ * MPM_ACC_EXACT_INT (2D or 3D, order 1): integer positions X (1/65,536 cell),
+ * int64 m and v; the far node's share of q is q*F/65,536 rounded to nearest
+ * (ties to even), the near node gets the rest, split along x then y (then z);
+ * the page's bounds line (count * max m * max |v| must fit int64, positions on
+ * the grid) runs before any scatter and on failure nothing is scattered
+ * (MPM_E_BOUND / MPM_E_DOMAIN in the status).  That mode needs no mpm_bin:
+ * `bins` (from mpm_bins_init for this descriptor) only carries the status words.
+ */
+mpm_status mpm_p2g(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, void *grid_acc,
+                   void *stream);
+
+/*
+ * mpm_grid_update -- for each node of the tiles that hold particles (and their
+ * neighbours): v = (float)P / (float)M (zero where M == 0), v += dtg, then the
+ * velocity-form boundary sign test: within `boundary_nodes` of a wall a
+ * component pointing into the wall becomes zero (implementation guide 2.1 and
+ * 3.3.2).  dtg = dt*g rounded to fp32 per component, computed by the caller.
+ * Reads each accumulator once and writes it back to zero (consume-and-zero,
+ * implementation guide section 2.1 and rule 4).  `grid_vel`: dim fp32 planes.
+ */
+mpm_status mpm_grid_update(const mpm_grid_desc *desc, void *grid_acc, float *grid_vel, const float dtg[3],
+                           mpm_bins *bins, void *stream);
+
+/*
+ * mpm_g2p -- grid-to-particle gather for the in-domain particles:
+ * v' = sum_a w v(a);  C'_kl = (sum_a w v_k(a) (a_l - f_l)) * (4*inv_dx)
+ * (APIC, "gather d and D (= B*4)" in cell units); x' = fma(dt, v', x).
+ * The stencil sums run axis by axis, innermost axis first, each three-term
+ * sum as fma(w2,t2, fma(w1,t1, w0*t0)), the same order the oracle uses.
+ * Particles outside the domain are left unchanged.
+ * MPM_ACC_EXACT_INT: `grid` is the int64 accumulator; each on-grid particle's v is set
+ * to its cell's momentum over its cell's mass, rounded to nearest (ties to even).
+ */
+mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *parts, mpm_bins *bins,
+                   float dt, void *stream);
+
+/*
+ * mpm_step -- mpm_bin, mpm_p2g, mpm_grid_update and mpm_g2p in sequence on one
+ * stream (device pointers throughout).
+ */
+mpm_status mpm_step(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *bins, void *grid_acc,
+                    float *grid_vel, float dt, const float dtg[3], void *stream);
+
+/*
+ * mpm_step_host -- one step from and back to HOST particle arrays: copies the
+ * host SoA (`host`, fp32; pinned memory gives full copy bandwidth) into the
+ * device arrays of `dev`, runs mpm_step, and copies x, v, C back into `host`.
+ * Asynchronous on `stream`; the host arrays must stay valid until it completes.
+ */
+mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev, mpm_bins *bins,
+                         void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream);
+
+/* Reorders a particle SoA by bins->perm: out[j] = in[perm[j]] for every
+ * component, all n entries.  `in` and `out` must not overlap. */
+mpm_status mpm_permute(const mpm_grid_desc *desc, const mpm_particles *in, mpm_particles *out,
+                       const mpm_bins *bins, void *stream);
+
+/* Asynchronous copy of the MPM_STATUS_WORDS status words to host memory. */
+mpm_status mpm_read_status(const mpm_bins *bins, uint32_t *host_out, void *stream);
+
+/* Static text for a status code. */
+const char *mpm_strerror(mpm_status s);
+
+/* Library version, (major << 16) | minor. */
+int32_t mpm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MPM_GB300_H */

@@ -1,0 +1,209 @@
+"""ctypes binding of the C ABI in ``include/mpm.h`` (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: particles, grids and workspaces are torch tensors
+whose device pointers are handed to the library.  The CUDA library must be
+present (it is built in-tree by ``build.py``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import threading
+
+import torch
+
+from . import build as _build
+
+MPM_OK, MPM_E_ARG, MPM_E_WORKSPACE, MPM_E_DOMAIN, MPM_E_BOUND, MPM_E_CUDA, MPM_E_TIMEOUT, MPM_E_NO_DEVICE = range(8)
+MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
+(ST_FLAGS, ST_N_OUTSIDE, ST_N_OUT_OF_RANGE, ST_N_VALID, ST_N_SLICES, ST_N_ACTIVE, ST_MAX_NEIGHBOURS,
+ ST_N_BIG_TILES) = range(8)
+MPM_STATUS_WORDS = 16
+
+
+class MPMError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+        self.code = code
+
+
+class GridDesc(ct.Structure):
+    _fields_ = [("dim", ct.c_int32), ("n", ct.c_int32 * 3), ("dx", ct.c_float), ("inv_dx", ct.c_float),
+                ("order", ct.c_int32), ("acc_mode", ct.c_int32), ("scale_log2", ct.c_int32),
+                ("tile", ct.c_int32), ("boundary_nodes", ct.c_int32)]
+
+
+class Particles(ct.Structure):
+    _fields_ = [("n", ct.c_int64), ("x", ct.c_void_p * 3), ("v", ct.c_void_p * 3), ("C", ct.c_void_p * 9),
+                ("m", ct.c_void_p)]
+
+
+class Bins(ct.Structure):
+    _fields_ = [("n", ct.c_int64), ("ntiles", ct.c_int64), ("max_slices", ct.c_int64),
+                ("key", ct.c_void_p), ("perm", ct.c_void_p), ("tile_count", ct.c_void_p),
+                ("tile_start", ct.c_void_p), ("slices", ct.c_void_p), ("active", ct.c_void_p),
+                ("status", ct.c_void_p), ("scratch", ct.c_void_p), ("scratch_bytes", ct.c_size_t)]
+
+
+_lock = threading.Lock()
+_L = None
+
+
+def library() -> ct.CDLL:
+    """Loads (building first if needed) the in-tree CUDA library."""
+    global _L
+    with _lock:
+        if _L is None:
+            path = _build.build()
+            L = ct.CDLL(path)
+            P, VP = ct.POINTER, ct.c_void_p
+            L.mpm_version.restype = ct.c_int32
+            L.mpm_strerror.argtypes = [ct.c_int]
+            L.mpm_strerror.restype = ct.c_char_p
+            L.mpm_workspace_bytes.argtypes = [P(GridDesc), ct.c_int64]
+            L.mpm_workspace_bytes.restype = ct.c_size_t
+            L.mpm_bins_init.argtypes = [P(GridDesc), ct.c_int64, VP, ct.c_size_t, P(Bins)]
+            L.mpm_grid_acc_bytes.argtypes = [P(GridDesc)]
+            L.mpm_grid_acc_bytes.restype = ct.c_size_t
+            L.mpm_grid_vel_bytes.argtypes = [P(GridDesc)]
+            L.mpm_grid_vel_bytes.restype = ct.c_size_t
+            L.mpm_bin.argtypes = [P(GridDesc), P(Particles), P(Bins), ct.c_int, VP]
+            L.mpm_p2g.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, VP]
+            L.mpm_grid_update.argtypes = [P(GridDesc), VP, VP, P(ct.c_float), P(Bins), VP]
+            L.mpm_g2p.argtypes = [P(GridDesc), VP, P(Particles), P(Bins), ct.c_float, VP]
+            L.mpm_step.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, VP, ct.c_float, P(ct.c_float), VP]
+            L.mpm_step_host.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
+                                        P(ct.c_float), VP]
+            L.mpm_permute.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP]
+            L.mpm_read_status.argtypes = [P(Bins), VP, VP]
+            for name in ("mpm_bins_init", "mpm_bin", "mpm_p2g", "mpm_grid_update", "mpm_g2p", "mpm_step",
+                         "mpm_step_host", "mpm_permute", "mpm_read_status"):
+                getattr(L, name).restype = ct.c_int
+            _L = L
+    return _L
+
+
+def strerror(code: int) -> str:
+    return library().mpm_strerror(code).decode()
+
+
+def _check(code: int, where: str):
+    if code != MPM_OK:
+        raise MPMError(code, where)
+
+
+def _stream(stream) -> ct.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ct.c_void_p(stream.cuda_stream)
+
+
+def grid_desc(grid: dict) -> GridDesc:
+    d = GridDesc()
+    d.dim = grid["dim"]
+    for i in range(3):
+        d.n[i] = grid["n"][i] if i < len(grid["n"]) else 1
+    d.dx = grid["dx"]
+    d.inv_dx = grid["inv_dx"]
+    d.order = grid["order"]
+    d.acc_mode = grid["acc_mode"]
+    d.scale_log2 = grid["scale_log2"]
+    d.tile = grid["tile"]
+    d.boundary_nodes = grid["boundary_nodes"]
+    return d
+
+
+def particles(x: torch.Tensor, v: torch.Tensor, C: torch.Tensor | None, m: torch.Tensor) -> Particles:
+    """SoA view of [dim, n] / [dim*dim, n] / [n] tensors (rows must be contiguous)."""
+    p = Particles()
+    p.n = int(x.shape[1])
+    for rows, field in ((x, p.x), (v, p.v), (C, p.C)):
+        if rows is None:
+            continue
+        assert rows.is_contiguous()
+        for i in range(rows.shape[0]):
+            field[i] = rows[i].data_ptr()
+    assert m.is_contiguous()
+    p.m = m.data_ptr()
+    return p
+
+
+def mpm_version() -> int:
+    return int(library().mpm_version())
+
+
+def mpm_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def mpm_workspace_bytes(desc: GridDesc, n: int) -> int:
+    return int(library().mpm_workspace_bytes(ct.byref(desc), n))
+
+
+def mpm_grid_acc_bytes(desc: GridDesc) -> int:
+    return int(library().mpm_grid_acc_bytes(ct.byref(desc)))
+
+
+def mpm_grid_vel_bytes(desc: GridDesc) -> int:
+    return int(library().mpm_grid_vel_bytes(ct.byref(desc)))
+
+
+def mpm_bins_init(desc: GridDesc, n: int, ws: torch.Tensor) -> Bins:
+    b = Bins()
+    _check(library().mpm_bins_init(ct.byref(desc), n, ct.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+                                   ct.byref(b)), "mpm_bins_init")
+    return b
+
+
+def mpm_bin(desc: GridDesc, parts: Particles, bins: Bins, flags: int = 0, stream=None):
+    _check(library().mpm_bin(ct.byref(desc), ct.byref(parts), ct.byref(bins), flags, _stream(stream)), "mpm_bin")
+
+
+def mpm_p2g(desc: GridDesc, parts: Particles, bins: Bins, grid_acc: torch.Tensor, stream=None):
+    _check(library().mpm_p2g(ct.byref(desc), ct.byref(parts), ct.byref(bins), ct.c_void_p(grid_acc.data_ptr()),
+                             _stream(stream)), "mpm_p2g")
+
+
+def _f3(vals) -> ct.Array:
+    arr = (ct.c_float * 3)()
+    for i, v in enumerate(list(vals)[:3]):
+        arr[i] = float(v)
+    return arr
+
+
+def mpm_grid_update(desc: GridDesc, grid_acc: torch.Tensor, grid_vel: torch.Tensor, dtg, bins: Bins, stream=None):
+    _check(library().mpm_grid_update(ct.byref(desc), ct.c_void_p(grid_acc.data_ptr()),
+                                     ct.c_void_p(grid_vel.data_ptr()), _f3(dtg), ct.byref(bins), _stream(stream)),
+           "mpm_grid_update")
+
+
+def mpm_g2p(desc: GridDesc, grid: torch.Tensor, parts: Particles, bins: Bins | None, dt: float, stream=None):
+    _check(library().mpm_g2p(ct.byref(desc), ct.c_void_p(grid.data_ptr()), ct.byref(parts),
+                             ct.byref(bins) if bins is not None else None, ct.c_float(dt), _stream(stream)),
+           "mpm_g2p")
+
+
+def mpm_step(desc: GridDesc, parts: Particles, bins: Bins, grid_acc: torch.Tensor, grid_vel: torch.Tensor,
+             dt: float, dtg, stream=None):
+    _check(library().mpm_step(ct.byref(desc), ct.byref(parts), ct.byref(bins), ct.c_void_p(grid_acc.data_ptr()),
+                              ct.c_void_p(grid_vel.data_ptr()), ct.c_float(dt), _f3(dtg), _stream(stream)),
+           "mpm_step")
+
+
+def mpm_step_host(desc: GridDesc, host: Particles, dev: Particles, bins: Bins, grid_acc: torch.Tensor,
+                  grid_vel: torch.Tensor, dt: float, dtg, stream=None):
+    _check(library().mpm_step_host(ct.byref(desc), ct.byref(host), ct.byref(dev), ct.byref(bins),
+                                   ct.c_void_p(grid_acc.data_ptr()), ct.c_void_p(grid_vel.data_ptr()),
+                                   ct.c_float(dt), _f3(dtg), _stream(stream)), "mpm_step_host")
+
+
+def mpm_permute(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, stream=None):
+    _check(library().mpm_permute(ct.byref(desc), ct.byref(src), ct.byref(dst), ct.byref(bins), _stream(stream)),
+           "mpm_permute")
+
+
+def mpm_read_status(bins: Bins, out: torch.Tensor, stream=None):
+    """Asynchronous copy of the status words into ``out`` (uint32-sized int32 CPU tensor, 16 entries)."""
+    assert out.numel() >= MPM_STATUS_WORDS and out.element_size() == 4 and out.device.type == "cpu"
+    _check(library().mpm_read_status(ct.byref(bins), ct.c_void_p(out.data_ptr()), _stream(stream)),
+           "mpm_read_status")

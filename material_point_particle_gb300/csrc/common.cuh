@@ -1,0 +1,121 @@
+// common.cuh -- device-side parameters and helpers shared by the CUDA kernels
+// of the MPM transfer library (binning, P2G, grid update, G2P).  Internal to
+// the library: nothing here is part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mpm.h"
+
+namespace mpm {
+
+constexpr uint32_t kKeyInvalid = 0xFFFFFFFFu;
+// Particles per P2G work item (a slice of one tile's sorted particles).
+constexpr int kSliceParticles = 256;
+// Largest tile the shared-memory sort handles (32-bit / 64-bit composites).
+constexpr int kSortCap32 = 16384;
+constexpr int kSortCap64 = 8192;
+// 1.5 * 2^23: adding it to |t| < 2^22 leaves rint(t) in the low mantissa bits.
+constexpr float kMagic = 12582912.0f;
+constexpr int32_t kMagicBits = 0x4B400000;
+// A share must stay below 2^22 in magnitude; the range test keeps this margin.
+constexpr float kShareLimit = 4190208.0f;  // 2^22 - 4096
+// Status flag set by a check that runs before P2G: P2G then scatters nothing.
+constexpr uint32_t kFlagNoScatter = 1u << 16;
+// int32 accumulators: at most this many stencils may cover one node.
+constexpr uint32_t kI32MaxContributions = 511;
+
+// Everything a kernel needs to know about the grid, derived once on the host.
+struct GridP {
+    int dim;
+    int n[3];
+    float dx, inv_dx;
+    int acc_mode;
+    float S;             // 2^scale_log2 as fp32
+    int T;               // tile edge in cells
+    int T_log2;
+    int nt[3];           // tiles per axis (1 on unused axes)
+    int cpt_log2;        // log2(cells per tile) = dim * T_log2
+    int64_t ntiles;      // product of nt
+    int64_t nodes;       // product of n (n[2] = 1 in 2D)
+    int H;               // halo edge T + 2
+    int halo_nodes;      // H^dim
+    int nb[3];           // node blocks (T^dim nodes) per axis
+    int64_t nblocks;
+    int boundary;        // boundary_nodes
+    float wmax;          // 0.75^dim
+};
+
+// Particle SoA as raw typed pointers.
+struct PartsF {
+    float *x[3];
+    float *v[3];
+    float *C[9];
+    const float *m;
+    int64_t n;
+};
+
+__device__ __forceinline__ uint32_t lane_id() {
+    uint32_t l;
+    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
+    return l;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Status word helpers: flags are bit (1 << mpm_status).
+__device__ __forceinline__ void set_flag(uint32_t *status, int code) {
+    atomicOr(&status[MPM_ST_FLAGS], 1u << code);
+}
+
+// Stencil base and fraction along one axis; false outside the domain
+// (0.5 <= xi < n - 1.5).  Every operation is one IEEE fp32 rounding.
+__device__ __forceinline__ bool base_frac(float x, float inv_dx, int n, int &b, float &f) {
+    float xi = __fmul_rn(x, inv_dx);
+    if (!(xi >= 0.5f && xi < __fsub_rn((float)n, 1.5f))) return false;
+    b = (int)floorf(__fsub_rn(xi, 0.5f));
+    f = __fsub_rn(xi, (float)b);
+    return true;
+}
+
+// Quadratic B-spline weights at distances f, f-1, f-2 from the stencil's
+// first node (f in [0.5, 1.5)).
+__device__ __forceinline__ void quad_weights(float f, float w[3]) {
+    float t0 = __fsub_rn(1.5f, f);
+    float t1 = __fsub_rn(f, 1.0f);
+    float t2 = __fsub_rn(f, 0.5f);
+    w[0] = __fmul_rn(0.5f, __fmul_rn(t0, t0));
+    w[1] = __fsub_rn(0.75f, __fmul_rn(t1, t1));
+    w[2] = __fmul_rn(0.5f, __fmul_rn(t2, t2));
+}
+
+// Tile-major key of base cell b (tile id * T^dim + cell within tile).
+__device__ __forceinline__ uint32_t cell_key(const GridP &g, const int b[3]) {
+    uint32_t tile = 0, local = 0;
+    const uint32_t mask = (uint32_t)g.T - 1;
+#pragma unroll
+    for (int l = 2; l >= 0; --l) {
+        if (l >= g.dim) continue;
+        tile = tile * (uint32_t)g.nt[l] + ((uint32_t)b[l] >> g.T_log2);
+        local = (local << g.T_log2) | ((uint32_t)b[l] & mask);
+    }
+    return (tile << g.cpt_log2) | local;
+}
+
+__device__ __forceinline__ void tile_origin(const GridP &g, uint32_t tile, int o[3]) {
+    o[0] = (int)(tile % (uint32_t)g.nt[0]) * g.T;
+    uint32_t r = tile / (uint32_t)g.nt[0];
+    o[1] = (int)(r % (uint32_t)g.nt[1]) * g.T;
+    o[2] = g.dim == 3 ? (int)(r / (uint32_t)g.nt[1]) * g.T : 0;
+}
+
+__device__ __forceinline__ int64_t node_index(const GridP &g, int i, int j, int k) {
+    return ((int64_t)k * g.n[1] + j) * g.n[0] + i;
+}
+
+}  // namespace mpm

@@ -1,0 +1,278 @@
+// grid_g2p.cu -- grid update and grid-to-particle gather.
+//
+// Grid update (implementation guide, section 2.1 item 1 and section 3.3.2):
+// mass-normalise, add gravity (rule 7: a solver parameter), apply the
+// velocity-form boundary sign test; each accumulator is read once and written
+// back to zero (section 2.1, "the grid clear can ride along"; rule 4).  Only
+// node blocks next to a tile that holds particles are visited.
+//
+// G2P (section 1: a gather, every particle writes only itself; section 3.1
+// Part 1 and 3.3.2 "gather d and D (= B*4)"): new velocity, APIC affine matrix
+// C = B * 4/dx^2 in cell units, advection x += dt v.
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mpm {
+
+template <typename AccT>
+__device__ __forceinline__ float acc_to_float(AccT v) {
+    if constexpr (sizeof(AccT) == 8)
+        return __ll2float_rn((long long)v);
+    else if constexpr (std::is_same<AccT, float>::value)
+        return v;
+    else
+        return __int2float_rn((int)v);
+}
+
+template <int DIM, int T, typename AccT>
+__global__ void k_grid_update(GridP g, AccT *__restrict__ acc, float *__restrict__ vel, float dtg0, float dtg1,
+                              float dtg2, const uint32_t *__restrict__ count) {
+    constexpr int NB = DIM == 3 ? T * T * T : T * T;
+    const uint32_t lane = lane_id();
+    const float dtg[3] = {dtg0, dtg1, dtg2};
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < g.nblocks; blk += warps) {
+        const int bx = (int)(blk % g.nb[0]);
+        const int by = (int)((blk / g.nb[0]) % g.nb[1]);
+        const int bz = DIM == 3 ? (int)(blk / ((int64_t)g.nb[0] * g.nb[1])) : 0;
+        // the block's nodes receive shares only from tiles (b - delta), delta in {0,1}^dim
+        bool act = false;
+        if (lane < (1u << DIM)) {
+            const int tx = bx - (int)(lane & 1), ty = by - (int)((lane >> 1) & 1), tz = bz - (int)((lane >> 2) & 1);
+            if (tx >= 0 && ty >= 0 && tz >= 0 && tx < g.nt[0] && ty < g.nt[1] && (DIM == 2 || tz < g.nt[2]))
+                act = count[((int64_t)tz * g.nt[1] + ty) * g.nt[0] + tx] > 0;
+        }
+        if (!__any_sync(0xFFFFFFFFu, act)) continue;
+        for (int r = lane; r < NB; r += 32) {
+            const int gx = bx * T + r % T, gy = by * T + (r / T) % T, gz = DIM == 3 ? bz * T + r / (T * T) : 0;
+            if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
+            const int64_t node = node_index(g, gx, gy, gz);
+            AccT a[DIM + 1];
+            bool any = false;
+#pragma unroll
+            for (int c = 0; c <= DIM; ++c) {
+                a[c] = acc[c * g.nodes + node];
+                any = any || a[c] != (AccT)0;
+            }
+            const int idx[3] = {gx, gy, gz};
+            const float M = acc_to_float(a[0]);
+#pragma unroll
+            for (int l = 0; l < DIM; ++l) {
+                float v = 0.f;
+                if (M != 0.f) {
+                    v = __fadd_rn(__fdiv_rn(acc_to_float(a[1 + l]), M), dtg[l]);
+                    if ((idx[l] < g.boundary && v < 0.f) || (idx[l] > g.n[l] - 1 - g.boundary && v > 0.f)) v = 0.f;
+                }
+                vel[l * g.nodes + node] = v;
+            }
+            if (any) {
+#pragma unroll
+                for (int c = 0; c <= DIM; ++c) acc[c * g.nodes + node] = (AccT)0;
+            }
+        }
+    }
+}
+
+mpm_status launch_grid_update(const GridP &g, void *grid_acc, float *vel, const float dtg[3], const WsView &w,
+                              const DeviceInfo &dev, cudaStream_t st) {
+    const int blocks = dev.sms * 8, threads = 256;
+    if (g.dim == 3 && g.T == 4) {
+        if (g.acc_mode == MPM_ACC_I64)
+            k_grid_update<3, 4, long long><<<blocks, threads, 0, st>>>(g, (long long *)grid_acc, vel, dtg[0], dtg[1],
+                                                                      dtg[2], w.count);
+        else if (g.acc_mode == MPM_ACC_I32)
+            k_grid_update<3, 4, int><<<blocks, threads, 0, st>>>(g, (int *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
+                                                                w.count);
+        else
+            k_grid_update<3, 4, float><<<blocks, threads, 0, st>>>(g, (float *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
+                                                                  w.count);
+    } else if (g.dim == 2 && g.T == 8) {
+        if (g.acc_mode == MPM_ACC_I64)
+            k_grid_update<2, 8, long long><<<blocks, threads, 0, st>>>(g, (long long *)grid_acc, vel, dtg[0], dtg[1],
+                                                                      dtg[2], w.count);
+        else if (g.acc_mode == MPM_ACC_I32)
+            k_grid_update<2, 8, int><<<blocks, threads, 0, st>>>(g, (int *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
+                                                                w.count);
+        else
+            k_grid_update<2, 8, float><<<blocks, threads, 0, st>>>(g, (float *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
+                                                                  w.count);
+    } else {
+        return MPM_E_ARG;
+    }
+    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+}
+
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float sum3(const float w[3], const float t[3]) {
+    return __fmaf_rn(w[2], t[2], __fmaf_rn(w[1], t[1], __fmul_rn(w[0], t[0])));
+}
+
+template <int DIM>
+__global__ void __launch_bounds__(256) k_g2p(GridP g, PartsF p, const float *__restrict__ vel,
+                                             const uint32_t *__restrict__ perm, const uint32_t *__restrict__ status,
+                                             float dt, float c4) {
+    const uint32_t n_valid = status[MPM_ST_N_VALID];
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n_valid; j += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t pid = perm[j];
+        float x[DIM], f[3] = {0.f, 0.f, 0.f};
+        int b[3] = {0, 0, 0};
+        bool ok = true;
+#pragma unroll
+        for (int l = 0; l < DIM; ++l) {
+            x[l] = p.x[l][pid];
+            ok = ok && base_frac(x[l], g.inv_dx, g.n[l], b[l], f[l]);
+        }
+        if (!ok) continue;
+        float w[3][3], we[3][3];
+#pragma unroll
+        for (int l = 0; l < DIM; ++l) {
+            quad_weights(f[l], w[l]);
+#pragma unroll
+            for (int a = 0; a < 3; ++a) we[l][a] = __fmul_rn(w[l][a], __fsub_rn((float)a, f[l]));
+        }
+        const int64_t base = node_index(g, b[0], b[1], b[2]);
+        const int64_t sy = g.n[0], sz = (int64_t)g.n[0] * g.n[1];
+        float vn[DIM], Bm[DIM][DIM];
+#pragma unroll
+        for (int k = 0; k < DIM; ++k) {
+            const float *vk = vel + k * g.nodes + base;
+            if constexpr (DIM == 3) {
+                float Y[3], Ye[3], Yq[3];
+#pragma unroll
+                for (int a0 = 0; a0 < 3; ++a0) {
+                    float Z[3], Zq[3];
+#pragma unroll
+                    for (int a1 = 0; a1 < 3; ++a1) {
+                        float t[3];
+#pragma unroll
+                        for (int a2 = 0; a2 < 3; ++a2) t[a2] = vk[a0 + a1 * sy + a2 * sz];
+                        Z[a1] = sum3(w[2], t);
+                        Zq[a1] = sum3(we[2], t);
+                    }
+                    Y[a0] = sum3(w[1], Z);
+                    Ye[a0] = sum3(we[1], Z);
+                    Yq[a0] = sum3(w[1], Zq);
+                }
+                vn[k] = sum3(w[0], Y);
+                Bm[k][0] = sum3(we[0], Y);
+                Bm[k][1] = sum3(w[0], Ye);
+                Bm[k][DIM - 1] = sum3(w[0], Yq);
+            } else {
+                float Y[3], Ye[3];
+#pragma unroll
+                for (int a0 = 0; a0 < 3; ++a0) {
+                    float t[3];
+#pragma unroll
+                    for (int a1 = 0; a1 < 3; ++a1) t[a1] = vk[a0 + a1 * sy];
+                    Y[a0] = sum3(w[1], t);
+                    Ye[a0] = sum3(we[1], t);
+                }
+                vn[k] = sum3(w[0], Y);
+                Bm[k][0] = sum3(we[0], Y);
+                Bm[k][1] = sum3(w[0], Ye);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < DIM; ++k) {
+            p.v[k][pid] = vn[k];
+#pragma unroll
+            for (int l = 0; l < DIM; ++l) p.C[k * DIM + l][pid] = __fmul_rn(Bm[k][l], c4);
+        }
+#pragma unroll
+        for (int l = 0; l < DIM; ++l) p.x[l][pid] = __fmaf_rn(dt, vn[l], x[l]);
+    }
+}
+
+mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
+                      const DeviceInfo &dev, cudaStream_t st) {
+    const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
+    const int blocks = dev.sms * 8;
+    if (g.dim == 3)
+        k_g2p<3><<<blocks, 256, 0, st>>>(g, p, vel, w.perm, w.status, dt, c4);
+    else
+        k_g2p<2><<<blocks, 256, 0, st>>>(g, p, vel, w.perm, w.status, dt, c4);
+    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+}
+
+// --------------------------------------------------------------------------
+__global__ void k_permute(int ncomp, PartsF in, PartsF out, const uint32_t *__restrict__ perm, int64_t n) {
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t src = perm[j];
+        for (int c = 0; c < ncomp; ++c) {
+            const float *s;
+            float *d;
+            if (c < 3) {
+                s = in.x[c];
+                d = out.x[c];
+            } else if (c < 6) {
+                s = in.v[c - 3];
+                d = out.v[c - 3];
+            } else if (c < 15) {
+                s = in.C[c - 6];
+                d = out.C[c - 6];
+            } else {
+                s = in.m;
+                d = const_cast<float *>(out.m);
+            }
+            if (s && d) d[j] = s[src];
+        }
+    }
+}
+
+mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
+                          const DeviceInfo &dev, cudaStream_t st) {
+    const int blocks = dev.sms * 8;
+    k_permute<<<blocks, 256, 0, st>>>(16, in, out, perm, in.n);
+    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+}
+
+// --------------------------------------------------------------------------
+__device__ __forceinline__ long long div_rne_g(long long a, long long b) {
+    long long q = a / b, r = a % b;
+    unsigned long long ar = r < 0 ? 0ull - (unsigned long long)r : (unsigned long long)r;
+    unsigned long long br = b < 0 ? 0ull - (unsigned long long)b : (unsigned long long)b;
+    unsigned long long other = br - ar;
+    if (ar > other || (ar == other && (q & 1))) q += ((a < 0) != (b < 0)) ? -1 : 1;
+    return q;
+}
+
+template <int DIM>
+__global__ void k_cic_gather(GridP g, PartsI p, const int64_t *__restrict__ acc) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += (int64_t)gridDim.x * blockDim.x) {
+        int c[3] = {0, 0, 0};
+        bool on_grid = true;
+#pragma unroll
+        for (int l = 0; l < DIM; ++l) {
+            const int32_t X = p.X[l][i];
+            c[l] = X >> 16;
+            on_grid = on_grid && X >= 0 && c[l] <= g.n[l] - 2;
+        }
+        if (!on_grid) continue;  // positions off the grid: left unchanged
+        long long M = 0, P[DIM];
+#pragma unroll
+        for (int k = 0; k < DIM; ++k) P[k] = 0;
+#pragma unroll
+        for (int s = 0; s < (1 << DIM); ++s) {
+            const int64_t node = node_index(g, c[0] + (s & 1), c[1] + ((s >> 1) & 1), DIM == 3 ? c[2] + ((s >> 2) & 1) : 0);
+            M += acc[node];
+#pragma unroll
+            for (int k = 0; k < DIM; ++k) P[k] += acc[(1 + k) * g.nodes + node];
+        }
+#pragma unroll
+        for (int k = 0; k < DIM; ++k) p.v[k][i] = M != 0 ? div_rne_g(P[k], M) : 0;
+    }
+}
+
+mpm_status launch_cic_int_gather(const GridP &g, const PartsI &p, const int64_t *acc, const DeviceInfo &dev,
+                                 cudaStream_t st) {
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((p.n + 255) / 256, dev.sms * 4));
+    if (g.dim == 3)
+        k_cic_gather<3><<<blocks, 256, 0, st>>>(g, p, acc);
+    else
+        k_cic_gather<2><<<blocks, 256, 0, st>>>(g, p, acc);
+    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+}
+
+}  // namespace mpm

@@ -1,0 +1,60 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (workspace view, device facts, kernel launchers).  Not part of the ABI.
+#pragma once
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mpm.h"
+
+namespace mpm {
+
+struct GridP;
+struct PartsF;
+
+// Device arrays carved from the caller's workspace (see mpm_bins_init).
+struct WsView {
+    uint32_t *key, *perm, *tmp;
+    uint32_t *count;      // [ntiles + 1] particles per bucket (last: outside the domain)
+    uint32_t *start;      // [ntiles + 2] exclusive prefix of count
+    uint32_t *cursor;     // [ntiles + 1]
+    uint32_t *active;     // [ntiles]
+    uint32_t *slices;     // [2 * max_slices]
+    uint32_t *big;        // [ntiles + 1] buckets above the shared-memory sort capacity
+    uint32_t *partial;    // scan block totals, 3 words per 1024 buckets
+    uint32_t *status;     // [MPM_STATUS_WORDS]
+    uint32_t *cellcount;  // int32 mode only: [ntiles * T^dim], else null
+};
+
+struct DeviceInfo {
+    int device;
+    int sms;
+};
+
+mpm_status device_info(DeviceInfo &out);
+
+mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const DeviceInfo &dev,
+                      cudaStream_t st);
+mpm_status launch_grid_update(const GridP &g, void *grid_acc, float *vel, const float dtg[3], const WsView &w,
+                              const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
+                      const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
+                          const DeviceInfo &dev, cudaStream_t st);
+
+// Integer cloud-in-cell transfer (integer particles, int64 grid).
+struct PartsI {
+    const int32_t *X[3];
+    int64_t *v[3];
+    const int64_t *m;
+    int64_t n;
+};
+mpm_status launch_cic_int_p2g(const GridP &g, const PartsI &p, int64_t *acc, uint32_t *status,
+                              uint64_t *scratch, const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_cic_int_gather(const GridP &g, const PartsI &p, const int64_t *acc, const DeviceInfo &dev,
+                                 cudaStream_t st);
+
+}  // namespace mpm

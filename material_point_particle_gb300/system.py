@@ -1,0 +1,107 @@
+"""Device-resident particle set, grid and workspace for one grid descriptor.
+
+A convenience holder over the C ABI (``_lib``): it allocates torch tensors for
+the particle SoA, the accumulator and velocity grids and the binning
+workspace, and calls the library's entry points on them.  It computes nothing
+of the method itself.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def dt_times_g(grid: dict) -> list[float]:
+    """dt*g per component, each product rounded to fp32 (the grid update adds it)."""
+    dt = np.float32(grid["dt"])
+    g = (list(grid["g"]) + [0.0, 0.0, 0.0])[:3]
+    return [float(dt * np.float32(c)) for c in g]
+
+
+class MPMSystem:
+    def __init__(self, grid: dict, n: int, device: str | torch.device = "cuda"):
+        self.grid = dict(grid)
+        self.desc = L.grid_desc(grid)
+        self.dim = grid["dim"]
+        self.n = int(n)
+        self.device = torch.device(device)
+        dim = self.dim
+        ws_bytes = L.mpm_workspace_bytes(self.desc, self.n)
+        if ws_bytes == 0:
+            raise L.MPMError(L.MPM_E_ARG, "mpm_workspace_bytes")
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
+        self.bins = L.mpm_bins_init(self.desc, self.n, self.ws)
+        acc_bytes = L.mpm_grid_acc_bytes(self.desc)
+        self.nodes = int(np.prod(grid["n"][:dim]))
+        mode = grid["acc_mode"]
+        acc_dtype = {L.MPM_ACC_I32: torch.int32, L.MPM_ACC_I64: torch.int64, L.MPM_ACC_F32: torch.float32,
+                     L.MPM_ACC_EXACT_INT: torch.int64}[mode]
+        self.acc = torch.zeros((dim + 1, self.nodes), dtype=acc_dtype, device=self.device)
+        assert self.acc.numel() * self.acc.element_size() == acc_bytes
+        self.vel = torch.zeros((dim, self.nodes), dtype=torch.float32, device=self.device)
+        self.status_host = torch.zeros(L.MPM_STATUS_WORDS, dtype=torch.int32).pin_memory() \
+            if torch.cuda.is_available() else torch.zeros(L.MPM_STATUS_WORDS, dtype=torch.int32)
+        self.dt = float(grid.get("dt", 0.0))
+        self.dtg = dt_times_g(grid) if "g" in grid else [0.0, 0.0, 0.0]
+        self.x = self.v = self.C = self.m = None
+        self.parts = None
+
+    # -- particle state -------------------------------------------------------
+    def load(self, x, v, C, m):
+        """Copies host arrays ([dim, n], [dim, n], [dim*dim, n], [n]) to the device."""
+        mode = self.grid["acc_mode"]
+        if mode == L.MPM_ACC_EXACT_INT:
+            self.x = torch.as_tensor(np.ascontiguousarray(x, dtype=np.int32)).to(self.device)
+            self.v = torch.as_tensor(np.ascontiguousarray(v, dtype=np.int64)).to(self.device)
+            self.C = None
+            self.m = torch.as_tensor(np.ascontiguousarray(m, dtype=np.int64)).to(self.device)
+        else:
+            f32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.float32)).to(self.device)
+            self.x, self.v, self.C, self.m = f32(x), f32(v), f32(C), f32(m)
+        assert self.x.shape[1] <= self.n
+        self.parts = L.particles(self.x, self.v, self.C, self.m)
+        return self
+
+    def state(self):
+        """(x, v, C) as numpy arrays."""
+        torch.cuda.synchronize(self.device)
+        C = self.C.cpu().numpy() if self.C is not None else None
+        return self.x.cpu().numpy(), self.v.cpu().numpy(), C
+
+    # -- the library calls ----------------------------------------------------
+    def bin(self, stream=None):
+        L.mpm_bin(self.desc, self.parts, self.bins, 0, stream)
+
+    def p2g(self, stream=None):
+        L.mpm_p2g(self.desc, self.parts, self.bins, self.acc, stream)
+
+    def grid_update(self, stream=None):
+        L.mpm_grid_update(self.desc, self.acc, self.vel, self.dtg, self.bins, stream)
+
+    def g2p(self, stream=None):
+        grid = self.acc if self.grid["acc_mode"] == L.MPM_ACC_EXACT_INT else self.vel
+        L.mpm_g2p(self.desc, grid, self.parts, self.bins, self.dt, stream)
+
+    def step(self, stream=None):
+        L.mpm_step(self.desc, self.parts, self.bins, self.acc, self.vel, self.dt, self.dtg, stream)
+
+    def status(self) -> np.ndarray:
+        L.mpm_read_status(self.bins, self.status_host)
+        torch.cuda.synchronize(self.device)
+        return self.status_host.numpy().astype(np.uint32).copy()
+
+    def ws_view(self, ptr: int, count: int) -> torch.Tensor:
+        """uint32 words of the workspace at device address ``ptr`` (as int32)."""
+        off = int(ptr) - self.ws.data_ptr()
+        assert 0 <= off and off + 4 * count <= self.ws.numel() and off % 4 == 0
+        return self.ws[off:off + 4 * count].view(torch.int32)
+
+    def bins_arrays(self):
+        """(key, perm, tile_count) copied to the host as uint32."""
+        torch.cuda.synchronize(self.device)
+        n = self.x.shape[1]
+        nt = int(self.bins.ntiles)
+        grab = lambda ptr, cnt: self.ws_view(ptr, cnt).cpu().numpy().view(np.uint32)
+        return grab(self.bins.key, n), grab(self.bins.perm, n), grab(self.bins.tile_count, nt)

@@ -71,21 +71,41 @@ class Stream:
         self.pos += count
         return out
 
+    CHUNK = 1 << 20
+
+    def _uniform(self, count: int, shift: int, scale: float) -> np.ndarray:
+        out = np.empty(count, dtype=np.float64)
+        for lo in range(0, count, self.CHUNK):
+            hi = min(count, lo + self.CHUNK)
+            out[lo:hi] = (self.bits(hi - lo) >> np.uint64(shift)).astype(np.float64)
+        out *= scale
+        return out
+
     def uniform24(self, count: int) -> np.ndarray:
         """fp32-exact uniforms on [0, 1): multiples of 2^-24."""
-        return (self.bits(count) >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
+        return self._uniform(count, 40, 2.0 ** -24)
 
     def uniform53(self, count: int) -> np.ndarray:
-        return (self.bits(count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        return self._uniform(count, 11, 2.0 ** -53)
 
     def normal(self, count: int, sigma: float = 1.0) -> np.ndarray:
+        """Box-Muller on consecutive draw pairs (2i, 2i+1): pair i gives r cos(th)
+        at output i and r sin(th) at output half + i."""
         half = (count + 1) // 2
-        u1 = 1.0 - self.uniform53(half)          # (0, 1]
-        u2 = self.uniform53(half)
-        r = np.sqrt(-2.0 * np.log(u1))
-        th = 2.0 * math.pi * u2
-        z = np.concatenate([r * np.cos(th), r * np.sin(th)])[:count]
-        return z * sigma
+        z = np.empty(2 * half, dtype=np.float64)
+        for lo in range(0, half, self.CHUNK):
+            hi = min(half, lo + self.CHUNK)
+            k = hi - lo
+            d = (self.bits(2 * k) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+            u1 = 1.0 - d[0::2]    # (0, 1]
+            u2 = d[1::2]
+            r = np.sqrt(-2.0 * np.log(u1))
+            th = 2.0 * math.pi * u2
+            z[lo:hi] = r * np.cos(th)
+            z[half + lo:half + hi] = r * np.sin(th)
+        z = z[:count]
+        z *= sigma
+        return z
 
 
 def scrambled_order(n: int, a: int, b: int) -> np.ndarray:

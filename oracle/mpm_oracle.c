@@ -545,10 +545,11 @@ int orc_cic_int_bound(int dim, const int32_t *n, int64_t np, const int32_t *cons
             if (X[l][p] < 0 || (X[l][p] >> 16) > n[l] - 2)
                 return 0;
     }
-    __int128 top = (__int128)np * mmax * (vmax > 1 ? vmax : 1);
-    if (top > (__int128)INT64_MAX)
+    /* q = largest |m|*|v| (or |m|); each factor is below 2^64, so q fits 128 bits */
+    __int128 q = mmax * (vmax > 1 ? vmax : 1);
+    if (q > (__int128)INT64_MAX / 65536)
         return 0;
-    if (mmax * (vmax > 1 ? vmax : 1) * 65536 > (__int128)INT64_MAX)
+    if (q * (__int128)np > (__int128)INT64_MAX)
         return 0;
     return 1;
 }

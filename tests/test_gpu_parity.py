@@ -1,0 +1,345 @@
+"""CUDA path (through the C ABI) against the CPU oracle, on the same seeded inputs.
+
+Fixed-point modes must match bit for bit: keys, permutation, tile counts,
+accumulator grids, velocity grids and the particle state after G2P.  The
+float-atomic mode must match within |g - o| <= max(1e-5 |o|, 1e-6 max|o|) per
+node and channel.
+"""
+import numpy as np
+import pytest
+import torch
+
+from material_point_particle_gb300 import _lib as L
+from material_point_particle_gb300 import workloads as W
+from material_point_particle_gb300.system import MPMSystem
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def make(cloud, n=None):
+    n = cloud["x"].shape[1] if n is None else n
+    return MPMSystem(cloud["grid"], max(n, 1)).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+
+
+def acc_np(sys):
+    torch.cuda.synchronize()
+    return sys.acc.cpu().numpy()
+
+
+def float_close(g, o):
+    g = np.asarray(g, dtype=np.float64)
+    o = np.asarray(o, dtype=np.float64)
+    scale = np.abs(o).max(axis=-1, keepdims=True) if o.size else 0.0
+    return np.all(np.abs(g - o) <= np.maximum(1e-5 * np.abs(o), 1e-6 * scale))
+
+
+def with_outliers(cloud, k=11):
+    x = cloud["x"].copy()
+    n = x.shape[1]
+    s = W.Stream(5, 5)
+    idx = (s.bits(k) % np.uint64(n)).astype(np.int64)
+    x[0, idx[: k // 2]] = -0.1
+    x[-1, idx[k // 2:]] = 2.0
+    cloud = dict(cloud)
+    cloud["x"] = x
+    return cloud
+
+
+# --------------------------------------------------------------------------
+# binning
+
+@pytest.mark.parametrize("dim,n,count", [(2, 64, 5003), (3, 40, 4099), (3, 24, 257), (2, 130, 31)])
+def test_bin_matches_oracle(dim, n, count):
+    cloud = with_outliers(W.small_cloud(dim, count, n, seed=10 * dim + n, lo=0.02, hi=0.98))
+    sys = make(cloud)
+    sys.bin()
+    key, perm, cnt = sys.bins_arrays()
+    okey, operm, ocnt, valid = O.bin_particles(cloud["grid"], cloud["x"])
+    st = sys.status()
+    assert np.array_equal(key, okey)
+    assert np.array_equal(perm, operm)
+    assert np.array_equal(cnt, ocnt)
+    assert st[L.ST_N_VALID] == valid and st[L.ST_N_OUTSIDE] == count - valid
+
+
+@pytest.mark.parametrize("where", ["tile", "outside"])
+def test_bin_bucket_larger_than_shared_memory(where):
+    """A bucket of 20,000 particles exceeds the shared-memory sort and takes
+    the large-bucket path; the permutation is still the stable sort."""
+    s = W.Stream(77, 1)
+    cnt = 20000
+    if where == "tile":
+        x = (0.5 + (s.uniform24(3 * cnt) * 3.9) / 32.0).reshape(3, cnt)  # one 4^3 tile of a 32^3 grid
+    else:
+        x = np.concatenate([np.full((3, cnt), 5.0), 0.5 + 0.2 * s.uniform24(3 * 999).reshape(3, 999)], axis=1)
+    n = x.shape[1]
+    cloud = dict(x=x.astype(np.float32), v=np.zeros((3, n), np.float32), C=np.zeros((9, n), np.float32),
+                 m=np.ones(n, np.float32), grid=W.small_cloud(3, 1, 32, seed=1)["grid"])
+    sys = make(cloud)
+    sys.bin()
+    key, perm, cnt_t = sys.bins_arrays()
+    okey, operm, ocnt, valid = O.bin_particles(cloud["grid"], cloud["x"])
+    assert sys.status()[L.ST_N_BIG_TILES] >= 1
+    assert np.array_equal(key, okey) and np.array_equal(perm, operm) and np.array_equal(cnt_t, ocnt)
+
+
+def test_bin_tiny_and_empty():
+    for count in (0, 1, 2, 33):
+        cloud = W.small_cloud(3, count, 16, seed=3 + count)
+        sys = make(cloud)
+        sys.step()
+        st = sys.status()
+        assert st[L.ST_N_VALID] == count
+        if count:
+            key, perm, cnt = sys.bins_arrays()
+            okey, operm, ocnt, valid = O.bin_particles(cloud["grid"], cloud["x"])
+            assert np.array_equal(perm, operm)
+
+
+# --------------------------------------------------------------------------
+# P2G, grid update, G2P
+
+FIXED_CASES = [
+    (2, W.ACC_I32, 20, 64, 6000),
+    (2, W.ACC_I64, 20, 48, 3001),
+    (3, W.ACC_I64, 19, 32, 6007),
+    (3, W.ACC_I32, 19, 24, 2500),
+]
+
+
+@pytest.mark.parametrize("dim,mode,scale,n,count", FIXED_CASES)
+def test_step_fixed_bit_exact(dim, mode, scale, n, count):
+    cloud = with_outliers(W.small_cloud(dim, count, n, seed=100 + dim * 7 + n, acc_mode=mode, scale_log2=scale,
+                                        lo=0.05, hi=0.95, vsig=1.0, csig=2.0, mass_lo=0.5, mass_hi=1.5))
+    cloud["grid"]["g"] = [0.0, -9.8, 0.0]
+    sys = make(cloud)
+    sys.bin()
+    sys.p2g()
+    acc = acc_np(sys)
+    oacc, ost, ocounts = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert np.array_equal(acc.astype(np.int64), oacc)
+    st = sys.status()
+    assert st[L.ST_N_OUT_OF_RANGE] == ocounts[1]
+    sys.grid_update()
+    vel = sys.vel.cpu().numpy()
+    ovel = O.grid_update_fixed(cloud["grid"], oacc)
+    assert np.array_equal(vel.view(np.uint32), ovel.view(np.uint32))
+    assert not acc_np(sys).any(), "grid update must leave the accumulators zero"
+    sys.g2p()
+    x, v, C = sys.state()
+    ox, ov, oC, moved = O.g2p(cloud["grid"], ovel, cloud["x"], cloud["v"], cloud["C"])
+    assert np.array_equal(x.view(np.uint32), ox.view(np.uint32))
+    assert np.array_equal(v.view(np.uint32), ov.view(np.uint32))
+    assert np.array_equal(C.view(np.uint32), oC.view(np.uint32))
+
+
+@pytest.mark.parametrize("dim,n,count", [(2, 64, 6000), (3, 32, 6007)])
+def test_step_float_within_tolerance(dim, n, count):
+    cloud = W.small_cloud(dim, count, n, seed=200 + dim, acc_mode=W.ACC_F32, scale_log2=0, lo=0.05, hi=0.95,
+                          csig=2.0)
+    sys = make(cloud)
+    sys.bin()
+    sys.p2g()
+    acc = acc_np(sys)
+    oacc, _, _ = O.p2g_float(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert float_close(acc, oacc)
+    sys.grid_update()
+    sys.g2p()
+    x, v, C = sys.state()
+    ovel = O.grid_update_float(cloud["grid"], oacc)
+    ox, ov, oC, _ = O.g2p(cloud["grid"], ovel, cloud["x"], cloud["v"], cloud["C"])
+    # particle state from an order-dependent grid: tolerance scaled by the field
+    assert np.max(np.abs(v - ov)) <= 1e-4 * (1 + np.abs(ov).max())
+    assert np.max(np.abs(C - oC)) <= 1e-3 * n * (1 + np.abs(ov).max())
+    assert np.max(np.abs(x - ox)) <= 1e-6
+
+
+def test_scrambled_input_order_gives_identical_results():
+    cloud = W.small_cloud(3, 8192, 32, seed=301, scale_log2=19, lo=0.2, hi=0.8)
+    a = make(cloud)
+    a.step()
+    base_acc = None
+    xa, va, Ca = a.state()
+    for (mul, add) in [(97, 13), (1, 4095), (5, 1)]:
+        pi = W.scrambled_order(8192, mul, add)
+        c2 = dict(cloud, x=cloud["x"][:, pi], v=cloud["v"][:, pi], C=cloud["C"][:, pi], m=cloud["m"][pi])
+        b = make(c2)
+        b.bin()
+        b.p2g()
+        acc_b = acc_np(b)
+        if base_acc is None:
+            a2 = make(cloud)
+            a2.bin()
+            a2.p2g()
+            base_acc = acc_np(a2)
+        assert np.array_equal(acc_b, base_acc)
+        b.grid_update()
+        b.g2p()
+        xb, vb, Cb = b.state()
+        assert np.array_equal(xb, xa[:, pi]) and np.array_equal(vb, va[:, pi]) and np.array_equal(Cb, Ca[:, pi])
+
+
+def test_dense_single_cell_uses_warp_reduction_and_matches():
+    s = W.Stream(9, 9)
+    cnt = 5000
+    x = np.full((3, cnt), 0.5 + 0.3 / 16, dtype=np.float64) + 0.2 / 16 * s.uniform24(3 * cnt).reshape(3, cnt)
+    cloud = dict(x=x.astype(np.float32), v=s.normal(3 * cnt, 1.0).reshape(3, cnt).astype(np.float32),
+                 C=s.normal(9 * cnt, 1.0).reshape(9, cnt).astype(np.float32), m=np.ones(cnt, np.float32),
+                 grid=W.small_cloud(3, 1, 16, seed=1, scale_log2=19)["grid"])
+    sys = make(cloud)
+    sys.bin()
+    sys.p2g()
+    oacc, _, _ = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert np.array_equal(acc_np(sys), oacc)
+
+
+def test_out_of_range_particles_are_skipped_and_flagged():
+    cloud = W.small_cloud(3, 3000, 24, seed=401, scale_log2=19)
+    cloud["m"][[5, 77, 2999]] = 1e5
+    cloud["v"][1, 100] = np.nan
+    sys = make(cloud)
+    sys.bin()
+    sys.p2g()
+    oacc, ost, ocounts = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    st = sys.status()
+    assert st[L.ST_N_OUT_OF_RANGE] == 4 == ocounts[1]
+    assert st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
+    assert np.array_equal(acc_np(sys), oacc)
+
+
+def test_int32_accumulator_bound_stops_before_any_scatter():
+    cnt = 600  # 600 stencils over one node > 511
+    s = W.Stream(4, 4)
+    x = (0.5 + 0.01 * s.uniform24(2 * cnt)).reshape(2, cnt)
+    cloud = W.small_cloud(2, cnt, 64, seed=1, acc_mode=W.ACC_I32, scale_log2=10)
+    cloud["x"] = x.astype(np.float32)
+    sys = make(cloud)
+    sys.bin()
+    sys.p2g()
+    st = sys.status()
+    assert st[L.ST_MAX_NEIGHBOURS] == cnt
+    assert st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
+    assert not acc_np(sys).any()
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("mls2d", {}),
+    ("dambreak3d", dict(n_particles=32768)),
+    ("dambreak3d_float", dict(n_particles=32768, acc_mode=W.ACC_F32)),
+    ("blobs3d", dict(n_particles=262144)),
+    ("sphere3d", dict(n_particles=100000, n=128)),
+])
+def test_workload_step_matches_oracle(name, kw):
+    builder = {"mls2d": W.mls2d, "dambreak3d": W.dambreak3d, "dambreak3d_float": W.dambreak3d,
+               "blobs3d": W.blobs3d, "sphere3d": W.sphere3d}[name]
+    cloud = builder(**kw)
+    grid = cloud["grid"]
+    sys = make(cloud)
+    sys.bin()
+    key, perm, cnt = sys.bins_arrays()
+    okey, operm, ocnt, valid = O.bin_particles(grid, cloud["x"])
+    assert np.array_equal(perm, operm)
+    sys.p2g()
+    acc = acc_np(sys)
+    fixed = grid["acc_mode"] != W.ACC_F32
+    if fixed:
+        oacc, _, ocounts = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+        assert ocounts.sum() == 0
+        assert np.array_equal(acc.astype(np.int64), oacc)
+        ovel = O.grid_update_fixed(grid, oacc)
+    else:
+        oacc, _, _ = O.p2g_float(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+        assert float_close(acc, oacc)
+        ovel = O.grid_update_float(grid, oacc)
+    sys.grid_update()
+    sys.g2p()
+    x, v, C = sys.state()
+    ox, ov, oC, _ = O.g2p(grid, ovel, cloud["x"], cloud["v"], cloud["C"])
+    if fixed:
+        assert np.array_equal(sys.vel.cpu().numpy().view(np.uint32), ovel.view(np.uint32))
+        assert np.array_equal(x.view(np.uint32), ox.view(np.uint32))
+        assert np.array_equal(v.view(np.uint32), ov.view(np.uint32))
+        assert np.array_equal(C.view(np.uint32), oC.view(np.uint32))
+    else:
+        assert np.max(np.abs(v - ov)) <= 1e-4 * (1 + np.abs(ov).max())
+        assert np.max(np.abs(x - ox)) <= 1e-6
+
+
+def test_step_host_equals_device_step():
+    cloud = W.small_cloud(3, 20000, 32, seed=501, scale_log2=19)
+    a = make(cloud)
+    a.step()
+    xa, va, Ca = a.state()
+    b = make(cloud)
+    hx = torch.from_numpy(cloud["x"].copy()).pin_memory()
+    hv = torch.from_numpy(cloud["v"].copy()).pin_memory()
+    hC = torch.from_numpy(cloud["C"].copy()).pin_memory()
+    hm = torch.from_numpy(cloud["m"].copy()).pin_memory()
+    b.x.zero_()
+    b.v.zero_()
+    host = L.particles(hx, hv, hC, hm)
+    L.mpm_step_host(b.desc, host, b.parts, b.bins, b.acc, b.vel, b.dt, b.dtg)
+    torch.cuda.synchronize()
+    assert np.array_equal(hx.numpy(), xa) and np.array_equal(hv.numpy(), va) and np.array_equal(hC.numpy(), Ca)
+
+
+def test_permute_reorders_by_perm():
+    cloud = W.small_cloud(3, 5000, 32, seed=601)
+    a = make(cloud)
+    a.bin()
+    _, perm, _ = a.bins_arrays()
+    out = make(cloud)
+    L.mpm_permute(a.desc, a.parts, out.parts, a.bins)
+    x, v, C = out.state()
+    assert np.array_equal(x, cloud["x"][:, perm]) and np.array_equal(C, cloud["C"][:, perm])
+    assert np.array_equal(out.m.cpu().numpy(), cloud["m"][perm])
+
+
+# --------------------------------------------------------------------------
+# the integer CIC transfer page
+
+def _cic_sys(cfg):
+    return MPMSystem(cfg["grid"], cfg["X"].shape[1]).load(cfg["X"], cfg["v"], None, cfg["m"])
+
+
+def test_cic_int_grid_and_gather_match_oracle():
+    cfg = W.cic_int()
+    sys = _cic_sys(cfg)
+    sys.p2g()
+    acc = acc_np(sys)
+    oacc, ok = O.cic_int_p2g(cfg["grid"], cfg["X"], cfg["m"], cfg["v"])
+    assert ok and np.array_equal(acc, oacc)
+    st = sys.status()
+    assert st[L.ST_FLAGS] == 0
+    sys.g2p()
+    torch.cuda.synchronize()
+    assert np.array_equal(sys.v.cpu().numpy(), O.cic_int_gather(cfg["grid"], cfg["X"], oacc))
+
+
+def test_cic_int_all_scrambled_orders_identical_on_gpu():
+    cfg = W.cic_int()
+    oacc, _ = O.cic_int_p2g(cfg["grid"], cfg["X"], cfg["m"], cfg["v"])
+    for a in range(1, 256, 2):
+        pi = W.scrambled_order(256, a, 13)
+        sys = MPMSystem(cfg["grid"], 256).load(cfg["X"][:, pi], cfg["v"][:, pi], None, cfg["m"][pi])
+        sys.p2g()
+        assert np.array_equal(acc_np(sys), oacc), a
+
+
+def test_cic_int_bounds_line_scatters_nothing():
+    cfg = W.cic_int()
+    m = cfg["m"].copy()
+    m[3] = 2 ** 40
+    sys = MPMSystem(cfg["grid"], 256).load(cfg["X"], cfg["v"], None, m)
+    sys.p2g()
+    st = sys.status()
+    assert st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
+    assert not acc_np(sys).any()
+    X = cfg["X"].copy()
+    X[1, 7] = 8 * 65536
+    sys = MPMSystem(cfg["grid"], 256).load(X, cfg["v"], None, cfg["m"])
+    sys.p2g()
+    st = sys.status()
+    assert st[L.ST_FLAGS] & (1 << L.MPM_E_DOMAIN) and st[L.ST_N_OUTSIDE] == 1
+    assert not acc_np(sys).any()
