@@ -178,7 +178,7 @@ def dambreak3d(n_particles: int = 2097152, seed: int = SEED_BASE + 3, n: int = 1
 
 
 def blobs3d(n_particles: int = 16777216, seed: int = SEED_BASE + 4, n: int = 256,
-            n_blobs: int = 64, sigma: float = 0.02, scale_log2: int = 20):
+            n_blobs: int = 64, sigma: float = 0.02, scale_log2: int = 19):
     """Gaussian blobs, stored blob-major; samples outside [2dx, 1-2dx] are redrawn."""
     s = Stream(seed, 4)
     centres = 0.1 + 0.8 * s.uniform53(3 * n_blobs).reshape(n_blobs, 3)

@@ -70,7 +70,8 @@ def test_bin_bucket_larger_than_shared_memory(where):
     s = W.Stream(77, 1)
     cnt = 20000
     if where == "tile":
-        x = (0.5 + (s.uniform24(3 * cnt) * 3.9) / 32.0).reshape(3, cnt)  # one 4^3 tile of a 32^3 grid
+        # base cells 16..19 on every axis: one 4^3 tile of a 32^3 grid
+        x = ((16.5 + 3.99 * s.uniform24(3 * cnt)) / 32.0).reshape(3, cnt)
     else:
         x = np.concatenate([np.full((3, cnt), 5.0), 0.5 + 0.2 * s.uniform24(3 * 999).reshape(3, 999)], axis=1)
     n = x.shape[1]

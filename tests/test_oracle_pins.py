@@ -108,9 +108,17 @@ def test_bin_is_stable_sort_of_base_cells(dim, n, tile):
     fr = xi[:, inside] - b
     assert np.all((fr >= 0.5) & (fr < 1.5))
     assert np.all((b >= 0) & (b <= np.array(grid["n"][:dim])[:, None] - 3))
-    # perm: numpy's stable argsort over the in-domain keys, then the rest in order
+    # perm: numpy's stable argsort over the in-domain keys gives each cell's
+    # particles in index order (their rank); inside a tile, each group of 32
+    # cells lists rank 0 of its cells, then rank 1, ...; out-of-domain last
     idx = np.nonzero(inside)[0]
-    expect = np.concatenate([idx[np.argsort(key[idx], kind="stable")], np.nonzero(~inside)[0]])
+    cellmajor = idx[np.argsort(key[idx], kind="stable")]
+    k_sorted = key[cellmajor].astype(np.int64)
+    first = np.searchsorted(k_sorted, k_sorted, side="left")
+    rank = np.arange(k_sorted.size) - first
+    tile_of, cell_of = k_sorted // (T ** dim), k_sorted % (T ** dim)
+    order = np.lexsort((cell_of, rank, cell_of // 32, tile_of))
+    expect = np.concatenate([cellmajor[order], np.nonzero(~inside)[0]])
     assert np.array_equal(perm.astype(np.int64), expect)
     assert np.array_equal(cnt.astype(np.int64),
                           np.bincount(key[idx] // (T ** dim), minlength=cnt.size))
