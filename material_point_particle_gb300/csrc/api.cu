@@ -72,7 +72,7 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
 }
 
 struct Layout {
-    size_t key, perm, tmp, count, start, cursor, active, slices, big, partial, status, cellcount, scratch, total;
+    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, partial, status, cellcount, scratch, total;
     int64_t max_slices;
 };
 
@@ -100,7 +100,8 @@ Layout layout_of(const GridP &g, int64_t n) {
     L.cursor = take(nb * sizeof(uint32_t));
     L.active = take(g.ntiles * sizeof(uint32_t));
     L.slices = take(2 * L.max_slices * sizeof(uint32_t));
-    L.big = take(nb * sizeof(uint32_t));
+    L.gH = take((n + g.ntiles + 2) * sizeof(uint32_t));
+    L.gCW = take(2 * n * sizeof(uint64_t));
     L.partial = take(3 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
     L.status = take(MPM_STATUS_WORDS * sizeof(uint32_t));
     L.cellcount = g.acc_mode == MPM_ACC_I32 ? take((size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t)) : 0;
@@ -123,7 +124,8 @@ WsView view_of(const GridP &g, const mpm_bins &b) {
     w.cursor = reinterpret_cast<uint32_t *>(base + L.cursor);
     w.active = reinterpret_cast<uint32_t *>(base + L.active);
     w.slices = reinterpret_cast<uint32_t *>(base + L.slices);
-    w.big = reinterpret_cast<uint32_t *>(base + L.big);
+    w.gH = reinterpret_cast<uint32_t *>(base + L.gH);
+    w.gCW = base + L.gCW;
     w.partial = reinterpret_cast<uint32_t *>(base + L.partial);
     w.cellcount = g.acc_mode == MPM_ACC_I32 ? reinterpret_cast<uint32_t *>(base + L.cellcount) : nullptr;
     return w;

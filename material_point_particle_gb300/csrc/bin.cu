@@ -19,9 +19,8 @@
 //                   exclusive scans of (count, P2G slices, active flag) over
 //                   the buckets; active-tile list, P2G work list, cursors
 //   k_scatter       warp-aggregated atomic scatter of indices into buckets
-//   k_tile_sort     per-bucket sort by (cell, index) in shared memory
-//   k_big_sort      buckets too large for shared memory: a stable counting
-//                   sort over the key array in index order
+//   k_tile_order    per-tile order: claims sorted back into index order, a
+//                   stable counting sort by cell, the rank-major write-out
 //   k_nbr_bound     int32 mode: most stencils covering one node (the
 //                   accumulator bound, checked before any scatter)
 #include "common.cuh"
@@ -139,7 +138,7 @@ __global__ void k_scan_top(Tri *__restrict__ partial, int64_t nblocks, const uin
 __global__ void k_scan_final(GridP g, const uint32_t *__restrict__ count, int64_t nb, const Tri *__restrict__ partial,
                              uint32_t *__restrict__ start, uint32_t *__restrict__ cursor,
                              uint32_t *__restrict__ active, uint32_t *__restrict__ slices,
-                             uint32_t *__restrict__ big, uint32_t *__restrict__ status, int sort_cap) {
+                             uint32_t *__restrict__ status) {
     const int64_t b0 = (int64_t)blockIdx.x * kScanBlock + threadIdx.x * kScanItems;
     Tri v[kScanItems];
     Tri s = {0, 0, 0};
@@ -160,7 +159,6 @@ __global__ void k_scan_final(GridP g, const uint32_t *__restrict__ count, int64_
             slices[2 * (int64_t)(run.b + s2)] = (uint32_t)b;
             slices[2 * (int64_t)(run.b + s2) + 1] = s2 * kSliceParticles;
         }
-        if (v[j].a > (uint32_t)sort_cap) big[atomicAdd(&status[MPM_ST_N_BIG_TILES], 1u)] = (uint32_t)b;
         run = tri_add(run, v[j]);
         if (b == nb - 1) start[nb] = run.a;
     }
@@ -191,18 +189,51 @@ __global__ void k_scatter(GridP g, const uint32_t *__restrict__ key, int64_t n, 
 }
 
 // --------------------------------------------------------------------------
-// Per-bucket sort by (cell within tile, particle index).  Composite keys are
-// distinct, so any correct sort gives the stable order; a bitonic network in
-// shared memory, padded to a power of two with all-ones sentinels.
-template <typename K>
-__device__ void bitonic_sort_smem(K *s, int n_pow2) {
-    for (int k = 2; k <= n_pow2; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int t = threadIdx.x; t < (n_pow2 >> 1); t += blockDim.x) {
-                const int i = (t / j) * 2 * j + (t % j);
-                const int pr = i + j;
+// The order inside each tile.  The atomic scatter filled each bucket with
+// "claims": one per warp and bucket, holding that warp's lanes of the bucket
+// in lane (= index) order, and all sharing idx >> 5 (a warp covers 32
+// consecutive indices per round).  So sorting the claims by idx >> 5 puts the
+// bucket in index order.  In steady state a tile has few claims; from a cold
+// order every entry is its own claim and this is a plain sort.  A stable
+// counting sort by cell follows (cell-major, each cell in index order), then
+// the rank-major write-out: each group of 32 cells lists rank 0 of its cells,
+// then rank 1, and so on.  Buckets above kOrderCap entries use global scratch
+// instead of shared memory (same code, generic pointers).
+constexpr int kOrderThreads = 256;
+constexpr int kOrderCap = 4096;
+constexpr int kOrderWarps = kOrderThreads / 32;
+
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t &total, uint32_t *sh) {
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if ((int)lane >= d) inc += t;
+    }
+    if (lane == 31) sh[warp] = inc;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kOrderWarps; ++w) {
+        const uint32_t t = sh[w];
+        before += (w < (int)warp) ? t : 0u;
+        tot += t;
+    }
+    __syncthreads();
+    total = tot;
+    return before + inc - v;
+}
+
+// Ascending bitonic sort of n_pow2 keys, block-wide (shared or global memory).
+__device__ void block_bitonic(unsigned long long *s, uint32_t n_pow2) {
+    for (uint32_t k = 2; k <= n_pow2; k <<= 1) {
+        for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+            for (uint32_t t = threadIdx.x; t < (n_pow2 >> 1); t += blockDim.x) {
+                const uint32_t i = (t / j) * 2 * j + (t % j);
+                const uint32_t pr = i + j;
                 const bool up = (i & k) == 0;
-                K a = s[i], b = s[pr];
+                const unsigned long long a = s[i], b = s[pr];
                 if ((a > b) == up) {
                     s[i] = b;
                     s[pr] = a;
@@ -213,113 +244,145 @@ __device__ void bitonic_sort_smem(K *s, int n_pow2) {
     }
 }
 
-template <typename K>
-__global__ void k_tile_sort(GridP g, const uint32_t *__restrict__ key, const uint32_t *__restrict__ tmp,
-                            const uint32_t *__restrict__ start, const uint32_t *__restrict__ count,
-                            const uint32_t *__restrict__ active, int64_t nb, uint32_t *__restrict__ perm,
-                            const uint32_t *__restrict__ status, int idx_bits, int cap) {
+__global__ void __launch_bounds__(kOrderThreads)
+k_tile_order(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const uint32_t *__restrict__ start,
+             const uint32_t *__restrict__ count, const uint32_t *__restrict__ active, int64_t nb, uint32_t *perm,
+             uint32_t *gH, unsigned long long *gCW, uint32_t *__restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    K *s = reinterpret_cast<K *>(smem_raw);
+    unsigned long long *sCW = reinterpret_cast<unsigned long long *>(smem_raw);
+    uint32_t *sA = reinterpret_cast<uint32_t *>(sCW + kOrderCap);
+    uint32_t *sS = sA + kOrderCap;
+    uint32_t *sH = sS + kOrderCap;
+    __shared__ uint32_t cnt64[64], cs64[65], run64[64];
+    __shared__ uint32_t wcnt[kOrderWarps][64], woff[kOrderWarps][64];
+    __shared__ uint32_t scan_sh[kOrderWarps];
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     const uint32_t n_active = status[MPM_ST_N_ACTIVE];
-    const uint32_t local_mask = (1u << g.cpt_log2) - 1;
-    // items: the active tiles, then the outside-the-domain bucket
+    const uint32_t cmask = (1u << g.cpt_log2) - 1;
     for (uint32_t item = blockIdx.x; item <= n_active; item += gridDim.x) {
-        const uint32_t b = item < n_active ? active[item] : (uint32_t)(nb - 1);
-        const uint32_t beg = start[b];
-        const uint32_t cnt = count[b];
-        if (cnt == 0 || cnt > (uint32_t)cap) continue;  // empty, or sorted by k_big_sort
+        const bool outside = item == n_active;
+        const uint32_t b = outside ? (uint32_t)(nb - 1) : active[item];
+        const uint32_t beg = start[b], cnt = count[b];
+        if (cnt == 0) continue;
         if (cnt == 1) {
             if (threadIdx.x == 0) perm[beg] = tmp[beg];
             continue;
         }
-        int n_pow2 = 1;
-        while (n_pow2 < (int)cnt) n_pow2 <<= 1;
-        for (int r = threadIdx.x; r < n_pow2; r += blockDim.x) {
-            K c = ~(K)0;
-            if (r < (int)cnt) {
-                const uint32_t idx = tmp[beg + r];
-                const uint32_t k = key[idx];
-                const K local = k == kKeyInvalid ? (K)0 : (K)(k & local_mask);
-                c = (local << idx_bits) | (K)idx;
+        const bool small = cnt <= (uint32_t)kOrderCap;
+        if (!small && threadIdx.x == 0) atomicAdd(&status[MPM_ST_N_BIG_TILES], 1u);
+        uint32_t *A = small ? sA : tmp + beg;
+        uint32_t *S = small ? sS : perm + beg;
+        uint32_t *H = small ? sH : gH + (size_t)beg + item;
+        unsigned long long *CW = small ? sCW : gCW + 2 * (size_t)beg;
+        if (small)
+            for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) A[i] = tmp[beg + i];
+        __syncthreads();
+        // claims: heads where idx >> 5 changes
+        uint32_t nclaims = 0;
+        for (uint32_t base = 0; base < cnt; base += blockDim.x) {
+            const uint32_t i = base + threadIdx.x;
+            uint32_t head = 0, w = 0;
+            if (i < cnt) {
+                w = A[i] >> 5;
+                head = (i == 0 || w != (A[i - 1] >> 5)) ? 1u : 0u;
             }
-            s[r] = c;
+            uint32_t tot;
+            const uint32_t ex = block_excl_scan(head, tot, scan_sh);
+            if (head) {
+                const uint32_t k = nclaims + ex;
+                H[k] = i;
+                CW[k] = ((unsigned long long)w << 32) | k;
+            }
+            nclaims += tot;
+        }
+        uint32_t np2 = 1;
+        while (np2 < nclaims) np2 <<= 1;
+        for (uint32_t k = nclaims + threadIdx.x; k < np2; k += blockDim.x) CW[k] = ~0ull;
+        if (threadIdx.x == 0) H[nclaims] = cnt;
+        __syncthreads();
+        if (nclaims > 1) block_bitonic(CW, np2);
+        // claims in index order: copy each claim to its destination
+        uint32_t done = 0;
+        for (uint32_t base = 0; base < nclaims; base += blockDim.x) {
+            const uint32_t j = base + threadIdx.x;
+            uint32_t len = 0, k = 0;
+            if (j < nclaims) {
+                k = (uint32_t)(CW[j] & 0xFFFFFFFFu);
+                len = H[k + 1] - H[k];
+            }
+            uint32_t tot;
+            const uint32_t ex = block_excl_scan(len, tot, scan_sh);
+            if (j < nclaims) {
+                const uint32_t d = done + ex, src = H[k];
+                for (uint32_t e = 0; e < len; ++e) S[d + e] = A[src + e];
+            }
+            done += tot;
         }
         __syncthreads();
-        bitonic_sort_smem(s, n_pow2);
-        const K idx_mask = (idx_bits >= (int)(8 * sizeof(K))) ? ~(K)0 : (((K)1 << idx_bits) - 1);
-        for (int r = threadIdx.x; r < (int)cnt; r += blockDim.x) perm[beg + r] = (uint32_t)(s[r] & idx_mask);
+        if (outside) {
+            if (small)
+                for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) perm[beg + i] = S[i];
+            __syncthreads();
+            continue;
+        }
+        // stable counting sort by cell: S (index order) -> A (cell-major)
+        if (threadIdx.x < 64) cnt64[threadIdx.x] = 0;
         __syncthreads();
-    }
-}
-
-// Buckets above the shared-memory capacity: one CTA per bucket reads the key
-// array in index order twice (cell histogram, then stable placement).  Slow
-// (O(n) per bucket) and only reached by very dense inputs.
-constexpr int kBigThreads = 256;
-constexpr int kMaxCells = 4096;
-
-__global__ void k_big_sort(GridP g, const uint32_t *__restrict__ key, int64_t n, const uint32_t *__restrict__ start,
-                           const uint32_t *__restrict__ big, int64_t nb, uint32_t *__restrict__ perm,
-                           const uint32_t *__restrict__ status) {
-    __shared__ uint32_t cell_off[kMaxCells];
-    __shared__ uint32_t warp_cnt[kBigThreads / 32][64];
-    __shared__ uint32_t warp_off[kBigThreads / 32][64];
-    const uint32_t nbig = status[MPM_ST_N_BIG_TILES];
-    const uint32_t ncell = 1u << g.cpt_log2;
-    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-    for (uint32_t item = blockIdx.x; item < nbig; item += gridDim.x) {
-        const uint32_t b = big[item];
-        const bool outside = b == (uint32_t)(nb - 1);
-        const uint32_t cells = outside ? 1u : ncell;
-        for (uint32_t c = threadIdx.x; c < cells; c += blockDim.x) cell_off[c] = 0;
-        __syncthreads();
-        // pass 1: cell histogram of this bucket
-        for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-            const uint32_t k = key[i];
-            const uint32_t kb = k == kKeyInvalid ? (uint32_t)(nb - 1) : (k >> g.cpt_log2);
-            if (kb == b) atomicAdd(&cell_off[outside ? 0u : (k & (ncell - 1))], 1u);
+        for (uint32_t base = 0; base < cnt; base += blockDim.x) {
+            const uint32_t i = base + threadIdx.x;
+            const uint32_t c = i < cnt ? (key[S[i]] & cmask) : 64u;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
+            if (i < cnt && (peers & lanemask_lt()) == 0) atomicAdd(&cnt64[c], (uint32_t)__popc(peers));
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t run = start[b];
-            for (uint32_t c = 0; c < cells; ++c) {
-                uint32_t t = cell_off[c];
-                cell_off[c] = run;
-                run += t;
+        if (threadIdx.x < 32) {
+            const uint32_t a0 = cnt64[2 * lane], a1 = cnt64[2 * lane + 1];
+            uint32_t inc = a0 + a1;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+                if ((int)lane >= d) inc += t;
             }
+            const uint32_t ex = inc - a0 - a1;
+            cs64[2 * lane] = ex;
+            cs64[2 * lane + 1] = ex + a0;
+            run64[2 * lane] = ex;
+            run64[2 * lane + 1] = ex + a0;
+            if (lane == 31) cs64[64] = inc;
         }
         __syncthreads();
-        // pass 2: stable placement, 256 indices per round, cells in groups of 64
-        for (int64_t base = 0; base < n; base += blockDim.x) {
-            const int64_t i = base + threadIdx.x;
-            uint32_t c = 0xFFFFFFFFu;
-            if (i < n) {
-                const uint32_t k = key[i];
-                const uint32_t kb = k == kKeyInvalid ? (uint32_t)(nb - 1) : (k >> g.cpt_log2);
-                if (kb == b) c = outside ? 0u : (k & (ncell - 1));
-            }
-            for (uint32_t group = 0; group < cells; group += 64) {
-                const bool mine = c != 0xFFFFFFFFu && c >= group && c < group + 64;
-                const uint32_t cg = mine ? c - group : 64u;
-                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, cg);
-                if (lane < 64 / 2) {
-                    warp_cnt[warp][lane] = 0;
-                    warp_cnt[warp][lane + 32] = 0;
+        for (uint32_t base = 0; base < cnt; base += blockDim.x) {
+            const uint32_t i = base + threadIdx.x;
+            const uint32_t c = i < cnt ? (key[S[i]] & cmask) : 64u;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
+            const uint32_t rank = __popc(peers & lanemask_lt());
+            wcnt[warp][lane] = 0;
+            wcnt[warp][lane + 32] = 0;
+            __syncwarp();
+            if (i < cnt && rank == 0) wcnt[warp][c] = __popc(peers);
+            __syncthreads();
+            if (threadIdx.x < 64) {
+                uint32_t r = run64[threadIdx.x];
+                for (int w2 = 0; w2 < kOrderWarps; ++w2) {
+                    woff[w2][threadIdx.x] = r;
+                    r += wcnt[w2][threadIdx.x];
                 }
-                __syncwarp();
-                if (mine && (peers & lanemask_lt()) == 0) warp_cnt[warp][cg] = __popc(peers);
-                __syncthreads();
-                if (threadIdx.x < 64 && group + threadIdx.x < cells) {
-                    uint32_t run = cell_off[group + threadIdx.x];
-                    for (int w = 0; w < kBigThreads / 32; ++w) {
-                        warp_off[w][threadIdx.x] = run;
-                        run += warp_cnt[w][threadIdx.x];
-                    }
-                    cell_off[group + threadIdx.x] = run;
-                }
-                __syncthreads();
-                if (mine) perm[warp_off[warp][cg] + __popc(peers & lanemask_lt())] = (uint32_t)i;
-                __syncthreads();
+                run64[threadIdx.x] = r;
+            }
+            __syncthreads();
+            if (i < cnt) A[woff[warp][c] + rank] = S[i];
+            __syncthreads();
+        }
+        // rank-major write-out, one warp per group of 32 cells
+        if (warp < 2) {
+            const uint32_t c = warp * 32 + lane;
+            const uint32_t nc = cnt64[c], first = cs64[c];
+            uint32_t seg = warp == 0 ? 0u : cs64[32];
+            for (uint32_t r = 0;; ++r) {
+                const uint32_t m = __ballot_sync(0xFFFFFFFFu, nc > r);
+                if (m == 0) break;
+                if (nc > r) perm[beg + seg + __popc(m & lanemask_lt())] = A[first + r];
+                seg += __popc(m);
             }
         }
         __syncthreads();
@@ -369,27 +432,14 @@ mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const De
     const int64_t nblk = (nb + kScanBlock - 1) / kScanBlock;
     k_scan_reduce<<<(unsigned)nblk, kScanThreads, 0, st>>>(g, w.count, nb, (Tri *)w.partial);
     k_scan_top<<<1, kScanThreads, 0, st>>>((Tri *)w.partial, nblk, w.count, nb, w.status);
-    const bool narrow = n <= (int64_t(1) << (32 - g.cpt_log2));
-    const int cap = narrow ? kSortCap32 : kSortCap64;
     k_scan_final<<<(unsigned)nblk, kScanThreads, 0, st>>>(g, w.count, nb, (const Tri *)w.partial, w.start,
-                                                          w.cursor, w.active, w.slices, w.big, w.status, cap);
+                                                          w.cursor, w.active, w.slices, w.status);
     if (n > 0) {
         k_scatter<<<grid_p, threads, 0, st>>>(g, w.key, n, w.cursor, w.tmp);
-        const int sort_blocks = dev.sms * 2;
-        // the sort buffers are 64 KB of dynamic shared memory (above the 48 KB default)
-        cudaFuncSetAttribute(k_tile_sort<uint32_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSortCap32 * (int)sizeof(uint32_t));
-        cudaFuncSetAttribute(k_tile_sort<uint64_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSortCap64 * (int)sizeof(uint64_t));
-        if (narrow) {
-            int idx_bits = 32 - g.cpt_log2;
-            k_tile_sort<uint32_t><<<sort_blocks, 512, kSortCap32 * sizeof(uint32_t), st>>>(
-                g, w.key, w.tmp, w.start, w.count, w.active, nb, w.perm, w.status, idx_bits, cap);
-        } else {
-            k_tile_sort<uint64_t><<<sort_blocks, 512, kSortCap64 * sizeof(uint64_t), st>>>(
-                g, w.key, w.tmp, w.start, w.count, w.active, nb, w.perm, w.status, 32, cap);
-        }
-        k_big_sort<<<dev.sms, kBigThreads, 0, st>>>(g, w.key, n, w.start, w.big, nb, w.perm, w.status);
+        const int smem = kOrderCap * (8 + 4 + 4 + 4) + 16;
+        cudaFuncSetAttribute(k_tile_order, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        k_tile_order<<<dev.sms * 2, kOrderThreads, smem, st>>>(g, w.key, w.tmp, w.start, w.count, w.active, nb, w.perm,
+                                                             w.gH, (unsigned long long *)w.gCW, w.status);
     }
     if (w.cellcount) k_nbr_bound<<<dev.sms * 4, 256, 0, st>>>(g, w.cellcount, w.status);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;

@@ -11,11 +11,10 @@
 namespace mpm {
 
 constexpr uint32_t kKeyInvalid = 0xFFFFFFFFu;
-// Particles per P2G work item (a slice of one tile's sorted particles).
-constexpr int kSliceParticles = 256;
-// Largest tile the shared-memory sort handles (32-bit / 64-bit composites).
-constexpr int kSortCap32 = 16384;
-constexpr int kSortCap64 = 8192;
+// Particles per P2G/G2P work item (a slice of one tile's sorted particles),
+// and the threads of the CTA that processes it.
+constexpr int kSliceParticles = 1024;
+constexpr int kP2GThreads = 256;
 // 1.5 * 2^23: adding it to |t| < 2^22 leaves rint(t) in the low mantissa bits.
 constexpr float kMagic = 12582912.0f;
 constexpr int32_t kMagicBits = 0x4B400000;
@@ -117,5 +116,36 @@ __device__ __forceinline__ void tile_origin(const GridP &g, uint32_t tile, int o
 __device__ __forceinline__ int64_t node_index(const GridP &g, int i, int j, int k) {
     return ((int64_t)k * g.n[1] + j) * g.n[0] + i;
 }
+
+template <int DIM>
+struct Stencil {
+    static constexpr int NA = DIM == 3 ? 27 : 9;
+    static constexpr int NC = DIM + 1;
+    static constexpr int CENTRE = DIM == 3 ? 13 : 4;  // a = (1,1,1) / (1,1)
+};
+
+// Shared-memory halo of one tile: (T+2)^dim nodes, x fastest, rows and planes
+// padded so that the 32 cells of one rank-major group (a 4x4x2 or 8x4 block)
+// fall in 32 different banks: row pitch 36 = 4 (mod 32), plane pitch
+// 240 = 16 (mod 32) in 3D; row pitch 40 = 8 (mod 32) in 2D.
+template <int DIM, int T>
+struct Halo {
+    static constexpr int H = T + 2;
+    static constexpr int SY = DIM == 3 ? 36 : 40;
+    static constexpr int SZ = DIM == 3 ? 240 : 0;
+    static constexpr int SIZE = DIM == 3 ? (H - 1) * SZ + (H - 1) * SY + H : (H - 1) * SY + H;
+    static constexpr int NODES = DIM == 3 ? H * H * H : H * H;
+    // padded offset of stencil node a = a0*9 + a1*3 + a2 (3D) or a0*3 + a1 (2D)
+    __device__ static constexpr int off(int a) {
+        return DIM == 3 ? (a / 9) + (a / 3 % 3) * SY + (a % 3) * SZ : (a / 3) + (a % 3) * SY;
+    }
+    // padded index and grid coordinates of halo node h (x fastest)
+    __device__ static void node(int h, int &hx, int &hy, int &hz, int &idx) {
+        hx = h % H;
+        hy = (h / H) % H;
+        hz = DIM == 3 ? h / (H * H) : 0;
+        idx = hx + hy * SY + hz * SZ;
+    }
+};
 
 }  // namespace mpm

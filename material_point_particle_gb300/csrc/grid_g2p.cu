@@ -109,90 +109,120 @@ __device__ __forceinline__ float sum3(const float w[3], const float t[3]) {
     return __fmaf_rn(w[2], t[2], __fmaf_rn(w[1], t[1], __fmul_rn(w[0], t[0])));
 }
 
-template <int DIM>
-__global__ void __launch_bounds__(256) k_g2p(GridP g, PartsF p, const float *__restrict__ vel,
-                                             const uint32_t *__restrict__ perm, const uint32_t *__restrict__ status,
-                                             float dt, float c4) {
-    const uint32_t n_valid = status[MPM_ST_N_VALID];
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n_valid; j += (int64_t)gridDim.x * blockDim.x) {
-        const uint32_t pid = perm[j];
-        float x[DIM], f[3] = {0.f, 0.f, 0.f};
-        int b[3] = {0, 0, 0};
-        bool ok = true;
+// One particle's gather from the tile's velocity halo in shared memory.
+template <int DIM, int T>
+__device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, uint32_t pid, const int o[3],
+                                           const float *sv, float dt, float c4) {
+    using Hl = Halo<DIM, T>;
+    float x[DIM], f[3] = {0.f, 0.f, 0.f};
+    int b[3] = {0, 0, 0};
 #pragma unroll
-        for (int l = 0; l < DIM; ++l) {
-            x[l] = p.x[l][pid];
-            ok = ok && base_frac(x[l], g.inv_dx, g.n[l], b[l], f[l]);
-        }
-        if (!ok) continue;
-        float w[3][3], we[3][3];
+    for (int l = 0; l < DIM; ++l) {
+        x[l] = p.x[l][pid];
+        base_frac(x[l], g.inv_dx, g.n[l], b[l], f[l]);
+    }
+    float w[3][3], we[3][3];
 #pragma unroll
-        for (int l = 0; l < DIM; ++l) {
-            quad_weights(f[l], w[l]);
+    for (int l = 0; l < DIM; ++l) {
+        quad_weights(f[l], w[l]);
 #pragma unroll
-            for (int a = 0; a < 3; ++a) we[l][a] = __fmul_rn(w[l][a], __fsub_rn((float)a, f[l]));
-        }
-        const int64_t base = node_index(g, b[0], b[1], b[2]);
-        const int64_t sy = g.n[0], sz = (int64_t)g.n[0] * g.n[1];
-        float vn[DIM], Bm[DIM][DIM];
+        for (int a = 0; a < 3; ++a) we[l][a] = __fmul_rn(w[l][a], __fsub_rn((float)a, f[l]));
+    }
+    const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
+                            : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
+    float vn[DIM], Bm[DIM][DIM];
 #pragma unroll
-        for (int k = 0; k < DIM; ++k) {
-            const float *vk = vel + k * g.nodes + base;
-            if constexpr (DIM == 3) {
-                float Y[3], Ye[3], Yq[3];
+    for (int k = 0; k < DIM; ++k) {
+        const float *vk = sv + k * Hl::SIZE + hb;
+        if constexpr (DIM == 3) {
+            float Y[3], Ye[3], Yq[3];
 #pragma unroll
-                for (int a0 = 0; a0 < 3; ++a0) {
-                    float Z[3], Zq[3];
+            for (int a0 = 0; a0 < 3; ++a0) {
+                float Z[3], Zq[3];
 #pragma unroll
-                    for (int a1 = 0; a1 < 3; ++a1) {
-                        float t[3];
-#pragma unroll
-                        for (int a2 = 0; a2 < 3; ++a2) t[a2] = vk[a0 + a1 * sy + a2 * sz];
-                        Z[a1] = sum3(w[2], t);
-                        Zq[a1] = sum3(we[2], t);
-                    }
-                    Y[a0] = sum3(w[1], Z);
-                    Ye[a0] = sum3(we[1], Z);
-                    Yq[a0] = sum3(w[1], Zq);
-                }
-                vn[k] = sum3(w[0], Y);
-                Bm[k][0] = sum3(we[0], Y);
-                Bm[k][1] = sum3(w[0], Ye);
-                Bm[k][DIM - 1] = sum3(w[0], Yq);
-            } else {
-                float Y[3], Ye[3];
-#pragma unroll
-                for (int a0 = 0; a0 < 3; ++a0) {
+                for (int a1 = 0; a1 < 3; ++a1) {
                     float t[3];
 #pragma unroll
-                    for (int a1 = 0; a1 < 3; ++a1) t[a1] = vk[a0 + a1 * sy];
-                    Y[a0] = sum3(w[1], t);
-                    Ye[a0] = sum3(we[1], t);
+                    for (int a2 = 0; a2 < 3; ++a2) t[a2] = vk[a0 + a1 * Hl::SY + a2 * Hl::SZ];
+                    Z[a1] = sum3(w[2], t);
+                    Zq[a1] = sum3(we[2], t);
                 }
-                vn[k] = sum3(w[0], Y);
-                Bm[k][0] = sum3(we[0], Y);
-                Bm[k][1] = sum3(w[0], Ye);
+                Y[a0] = sum3(w[1], Z);
+                Ye[a0] = sum3(we[1], Z);
+                Yq[a0] = sum3(w[1], Zq);
             }
+            vn[k] = sum3(w[0], Y);
+            Bm[k][0] = sum3(we[0], Y);
+            Bm[k][1] = sum3(w[0], Ye);
+            Bm[k][DIM - 1] = sum3(w[0], Yq);
+        } else {
+            float Y[3], Ye[3];
+#pragma unroll
+            for (int a0 = 0; a0 < 3; ++a0) {
+                float t[3];
+#pragma unroll
+                for (int a1 = 0; a1 < 3; ++a1) t[a1] = vk[a0 + a1 * Hl::SY];
+                Y[a0] = sum3(w[1], t);
+                Ye[a0] = sum3(we[1], t);
+            }
+            vn[k] = sum3(w[0], Y);
+            Bm[k][0] = sum3(we[0], Y);
+            Bm[k][1] = sum3(w[0], Ye);
         }
+    }
 #pragma unroll
-        for (int k = 0; k < DIM; ++k) {
-            p.v[k][pid] = vn[k];
+    for (int k = 0; k < DIM; ++k) {
+        p.v[k][pid] = vn[k];
 #pragma unroll
-            for (int l = 0; l < DIM; ++l) p.C[k * DIM + l][pid] = __fmul_rn(Bm[k][l], c4);
+        for (int l = 0; l < DIM; ++l) p.C[k * DIM + l][pid] = __fmul_rn(Bm[k][l], c4);
+    }
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) p.x[l][pid] = __fmaf_rn(dt, vn[l], x[l]);
+}
+
+// Work item as in P2G: one slice of a tile.  The CTA stages the tile's halo
+// of node velocities in shared memory (padded as the P2G accumulators), then
+// every thread gathers its particles from it.
+template <int DIM, int T>
+__global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, const float *__restrict__ vel,
+                                                     const uint32_t *__restrict__ perm,
+                                                     const uint32_t *__restrict__ slices,
+                                                     const uint32_t *__restrict__ start,
+                                                     const uint32_t *__restrict__ status, float dt, float c4) {
+    using Hl = Halo<DIM, T>;
+    __shared__ float sv[DIM * Hl::SIZE];
+    const uint32_t nslices = status[MPM_ST_N_SLICES];
+    for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
+        const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
+        const uint32_t beg = start[t] + first;
+        const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
+        int o[3];
+        tile_origin(g, t, o);
+        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
+            int hx, hy, hz, idx;
+            Hl::node(h, hx, hy, hz, idx);
+            const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
+            const bool in = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
+            const int64_t node = in ? node_index(g, gx, gy, gz) : 0;
+#pragma unroll
+            for (int k = 0; k < DIM; ++k) sv[k * Hl::SIZE + idx] = in ? vel[k * g.nodes + node] : 0.f;
         }
-#pragma unroll
-        for (int l = 0; l < DIM; ++l) p.x[l][pid] = __fmaf_rn(dt, vn[l], x[l]);
+        __syncthreads();
+        for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x) gather_one<DIM, T>(g, p, perm[beg + r], o, sv, dt, c4);
+        __syncthreads();
     }
 }
 
 mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
                       const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
-    const int blocks = dev.sms * 8;
-    if (g.dim == 3)
-        k_g2p<3><<<blocks, 256, 0, st>>>(g, p, vel, w.perm, w.status, dt, c4);
+    const int blocks = dev.sms * 4;
+    if (g.dim == 3 && g.T == 4)
+        k_g2p<3, 4><<<blocks, kP2GThreads, 0, st>>>(g, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
+    else if (g.dim == 2 && g.T == 8)
+        k_g2p<2, 8><<<blocks, kP2GThreads, 0, st>>>(g, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
     else
-        k_g2p<2><<<blocks, 256, 0, st>>>(g, p, vel, w.perm, w.status, dt, c4);
+        return MPM_E_ARG;
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }
 

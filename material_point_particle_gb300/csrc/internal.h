@@ -22,7 +22,8 @@ struct WsView {
     uint32_t *cursor;     // [ntiles + 1]
     uint32_t *active;     // [ntiles]
     uint32_t *slices;     // [2 * max_slices]
-    uint32_t *big;        // [ntiles + 1] buckets above the shared-memory sort capacity
+    uint32_t *gH;         // [n + ntiles + 2] claim heads of buckets above the shared-memory capacity
+    void *gCW;            // [2 n] uint64 claim keys of those buckets
     uint32_t *partial;    // scan block totals, 3 words per 1024 buckets
     uint32_t *status;     // [MPM_STATUS_WORDS]
     uint32_t *cellcount;  // int32 mode only: [ntiles * T^dim], else null

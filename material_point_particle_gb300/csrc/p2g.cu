@@ -26,32 +26,27 @@ __device__ __forceinline__ int32_t rint_mul(float a, float b) {
 }
 __device__ __forceinline__ int32_t rint_f(float a) { return __float_as_int(__fadd_rn(a, kMagic)) - kMagicBits; }
 
-template <int DIM>
-struct Stencil {
-    static constexpr int NA = DIM == 3 ? 27 : 9;
-    static constexpr int NC = DIM + 1;
-    static constexpr int CENTRE = DIM == 3 ? 13 : 4;  // a = (1,1,1) / (1,1)
-};
 
-// Loads particle `pid`, checks the domain and the share range, and computes
-// its NC x NA integer shares (fixed point) -- the arithmetic the oracle states.
-// Returns 0 = ok, 1 = outside the domain, 2 = out of range.
-template <int DIM>
-__device__ __forceinline__ int particle_shares(const GridP &g, const PartsF &p, uint32_t pid, int b[3],
-                                               int32_t sh[Stencil<DIM>::NC][Stencil<DIM>::NA]) {
+
+// One particle's fixed-point shares, added to the tile accumulator as they
+// are formed (the arithmetic the oracle states).  Returns false (and adds
+// nothing) when the particle is out of range.
+template <int DIM, int T>
+__device__ __forceinline__ bool scatter_fixed(const GridP &g, const PartsF &p, uint32_t pid, const int o[3],
+                                              int32_t *sacc) {
     using St = Stencil<DIM>;
+    using Hl = Halo<DIM, T>;
     float f[3] = {0.f, 0.f, 0.f};
-    b[2] = 0;
+    int b[3] = {0, 0, 0};
 #pragma unroll
-    for (int l = 0; l < DIM; ++l)
-        if (!base_frac(p.x[l][pid], g.inv_dx, g.n[l], b[l], f[l])) return 1;
+    for (int l = 0; l < DIM; ++l) base_frac(p.x[l][pid], g.inv_dx, g.n[l], b[l], f[l]);
     float v[DIM], C[DIM * DIM];
 #pragma unroll
     for (int k = 0; k < DIM; ++k) v[k] = p.v[k][pid];
 #pragma unroll
     for (int j = 0; j < DIM * DIM; ++j) C[j] = p.C[j][pid];
     const float Mt = __fmul_rn(p.m[pid], g.S);
-    // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) below 2^22 - 4096
+    // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) at most 2^22 - 4096
     const float h = __fmul_rn(1.5f, g.dx);
     const float aM = fabsf(Mt);
     bool ok = __fmul_rn(g.wmax, aM) <= kShareLimit;
@@ -62,7 +57,7 @@ __device__ __forceinline__ int particle_shares(const GridP &g, const PartsF &p, 
         const float R = __fmul_rn(aM, __fadd_rn(fabsf(v[k]), __fmul_rn(h, sc)));
         ok = ok && (__fmul_rn(g.wmax, R) <= kShareLimit);
     }
-    if (!ok) return 2;
+    if (!ok) return false;
     float w[3][3], dd[3][3];
 #pragma unroll
     for (int l = 0; l < DIM; ++l) {
@@ -70,13 +65,12 @@ __device__ __forceinline__ int particle_shares(const GridP &g, const PartsF &p, 
 #pragma unroll
         for (int a = 0; a < 3; ++a) dd[l][a] = __fmul_rn(__fsub_rn((float)a, f[l]), g.dx);
     }
-    int32_t Q[St::NC];
-    Q[0] = __float2int_rn(Mt);
-#pragma unroll
-    for (int k = 0; k < DIM; ++k) Q[1 + k] = __float2int_rn(__fmul_rn(Mt, v[k]));
+    const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
+                            : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
     int32_t rest[St::NC];
+    rest[0] = __float2int_rn(Mt);
 #pragma unroll
-    for (int c = 0; c < St::NC; ++c) rest[c] = Q[c];
+    for (int k = 0; k < DIM; ++k) rest[1 + k] = __float2int_rn(__fmul_rn(Mt, v[k]));
 #pragma unroll
     for (int a0 = 0; a0 < 3; ++a0) {
         const float Wx = __fmul_rn(w[0][a0], Mt);
@@ -94,89 +88,121 @@ __device__ __forceinline__ int particle_shares(const GridP &g, const PartsF &p, 
                 const int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
                 if (a == St::CENTRE) continue;
                 const float Wt = DIM == 3 ? __fmul_rn(Wxy, w[2][a2]) : Wxy;
+                const int at = hb + Hl::off(a);
                 const int32_t sm = rint_f(Wt);
-                sh[0][a] = sm;
                 rest[0] -= sm;
+                atomicAdd(&sacc[at], sm);
 #pragma unroll
                 for (int k = 0; k < DIM; ++k) {
                     const float vel = DIM == 3 ? __fmaf_rn(C[k * DIM + 2], dd[2][a2], h1[k]) : h1[k];
-                    const int32_t s = rint_mul(Wt, vel);
-                    sh[1 + k][a] = s;
-                    rest[1 + k] -= s;
+                    const int32_t sk = rint_mul(Wt, vel);
+                    rest[1 + k] -= sk;
+                    atomicAdd(&sacc[(1 + k) * Hl::SIZE + at], sk);
                 }
             }
         }
     }
+    const int ac = hb + Hl::off(St::CENTRE);
 #pragma unroll
-    for (int c = 0; c < St::NC; ++c) sh[c][St::CENTRE] = rest[c];
-    return 0;
+    for (int c = 0; c < St::NC; ++c) atomicAdd(&sacc[c * Hl::SIZE + ac], rest[c]);
+    return true;
 }
 
-// Shared-memory halo offset of stencil node a relative to the base node.
-template <int DIM, int H>
-__device__ __forceinline__ constexpr int halo_off(int a) {
-    return DIM == 3 ? ((a / 9) + (a / 3 % 3) * H + (a % 3) * H * H) : ((a / 3) + (a % 3) * H);
+template <int DIM, int T>
+__device__ __forceinline__ void scatter_float(const GridP &g, const PartsF &p, uint32_t pid, const int o[3],
+                                              float *sacc) {
+    using Hl = Halo<DIM, T>;
+    float f[3] = {0.f, 0.f, 0.f};
+    int b[3] = {0, 0, 0};
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) base_frac(p.x[l][pid], g.inv_dx, g.n[l], b[l], f[l]);
+    float v[DIM], C[DIM * DIM], w[3][3], dd[3][3];
+#pragma unroll
+    for (int k = 0; k < DIM; ++k) v[k] = p.v[k][pid];
+#pragma unroll
+    for (int j = 0; j < DIM * DIM; ++j) C[j] = p.C[j][pid];
+    const float m = p.m[pid];
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) {
+        quad_weights(f[l], w[l]);
+#pragma unroll
+        for (int a = 0; a < 3; ++a) dd[l][a] = __fmul_rn(__fsub_rn((float)a, f[l]), g.dx);
+    }
+    const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
+                            : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
+#pragma unroll
+    for (int a0 = 0; a0 < 3; ++a0) {
+        const float Wx = __fmul_rn(w[0][a0], m);
+        float h0[DIM];
+#pragma unroll
+        for (int k = 0; k < DIM; ++k) h0[k] = __fmaf_rn(C[k * DIM + 0], dd[0][a0], v[k]);
+#pragma unroll
+        for (int a1 = 0; a1 < 3; ++a1) {
+            const float Wxy = __fmul_rn(Wx, w[1][a1]);
+            float h1[DIM];
+#pragma unroll
+            for (int k = 0; k < DIM; ++k) h1[k] = __fmaf_rn(C[k * DIM + 1], dd[1][a1], h0[k]);
+#pragma unroll
+            for (int a2 = 0; a2 < (DIM == 3 ? 3 : 1); ++a2) {
+                const int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
+                const float W = DIM == 3 ? __fmul_rn(Wxy, w[2][a2]) : Wxy;
+                const int at = hb + Hl::off(a);
+                atomicAdd(&sacc[at], W);
+#pragma unroll
+                for (int k = 0; k < DIM; ++k) {
+                    const float vel = DIM == 3 ? __fmaf_rn(C[k * DIM + 2], dd[2][a2], h1[k]) : h1[k];
+                    atomicAdd(&sacc[(1 + k) * Hl::SIZE + at], __fmul_rn(W, vel));
+                }
+            }
+        }
+    }
 }
 
+// Work item: up to kSliceParticles consecutive sorted particles of one tile
+// (rank-major inside the tile, so a warp's 32 lanes sit in distinct cells).
+// The CTA zeroes the tile's halo accumulators, every thread scatters its
+// particles with shared atomics, and the CTA adds each nonzero node to the
+// grid once (neighbouring tiles overlap on the halo, so the flush adds).
 template <int DIM, int T, typename AccT>
-__global__ void __launch_bounds__(kSliceParticles) k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm,
-                                                               const uint32_t *__restrict__ slices,
-                                                               const uint32_t *__restrict__ start,
-                                                               uint32_t *__restrict__ status, AccT *__restrict__ acc) {
+__global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm,
+                                                           const uint32_t *__restrict__ slices,
+                                                           const uint32_t *__restrict__ start,
+                                                           uint32_t *__restrict__ status, AccT *__restrict__ acc) {
     using St = Stencil<DIM>;
-    constexpr int H = T + 2;
-    constexpr int HN = DIM == 3 ? H * H * H : H * H;
-    __shared__ int32_t sacc[St::NC * HN];
+    using Hl = Halo<DIM, T>;
+    __shared__ int32_t sacc[St::NC * Hl::SIZE];
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
     const uint32_t nslices = status[MPM_ST_N_SLICES];
-    const uint32_t lane = lane_id();
     for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
         const uint32_t beg = start[t] + first;
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
         int o[3];
         tile_origin(g, t, o);
-        for (int i = threadIdx.x; i < St::NC * HN; i += blockDim.x) sacc[i] = 0;
+        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
+            int hx, hy, hz, idx;
+            Hl::node(h, hx, hy, hz, idx);
+#pragma unroll
+            for (int c = 0; c < St::NC; ++c) sacc[c * Hl::SIZE + idx] = 0;
+        }
         __syncthreads();
-
-        int32_t sh[St::NC][St::NA];
-        int b[3] = {0, 0, 0};
-        int res = 1;
-        if (threadIdx.x < cnt) res = particle_shares<DIM>(g, p, perm[beg + threadIdx.x], b, sh);
-        if (threadIdx.x < cnt && res == 2) {
-            atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], 1u);
+        uint32_t bad = 0;
+        for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x)
+            if (!scatter_fixed<DIM, T>(g, p, perm[beg + r], o, sacc)) ++bad;
+        if (bad) {
+            atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
             set_flag(status, MPM_E_BOUND);
         }
-        const bool ok = res == 0;
-        const int hb = DIM == 3 ? ((b[2] - o[2]) * H + (b[1] - o[1])) * H + (b[0] - o[0])
-                                : (b[1] - o[1]) * H + (b[0] - o[0]);
-        const int hb0 = __shfl_sync(0xFFFFFFFFu, hb, 0);
-        const bool uniform = __all_sync(0xFFFFFFFFu, ok && hb == hb0);
-        if (uniform) {
-            // one base cell for the whole warp: reduce each share across lanes
-#pragma unroll
-            for (int c = 0; c < St::NC; ++c)
-#pragma unroll
-                for (int a = 0; a < St::NA; ++a) {
-                    const uint32_t r = __reduce_add_sync(0xFFFFFFFFu, (uint32_t)sh[c][a]);
-                    if (lane == (uint32_t)((c * St::NA + a) & 31))
-                        atomicAdd(&sacc[c * HN + hb0 + halo_off<DIM, H>(a)], (int32_t)r);
-                }
-        } else if (ok) {
-#pragma unroll
-            for (int c = 0; c < St::NC; ++c)
-#pragma unroll
-                for (int a = 0; a < St::NA; ++a) atomicAdd(&sacc[c * HN + hb + halo_off<DIM, H>(a)], sh[c][a]);
-        }
         __syncthreads();
-        for (int h = threadIdx.x; h < HN; h += blockDim.x) {
-            const int hx = h % H, hy = (h / H) % H, hz = DIM == 3 ? h / (H * H) : 0;
+        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
+            int hx, hy, hz, idx;
+            Hl::node(h, hx, hy, hz, idx);
             const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
             if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
             const int64_t node = node_index(g, gx, gy, gz);
 #pragma unroll
             for (int c = 0; c < St::NC; ++c) {
-                const int32_t val = sacc[c * HN + h];
+                const int32_t val = sacc[c * Hl::SIZE + idx];
                 if (val == 0) continue;
                 if constexpr (sizeof(AccT) == 8)
                     atomicAdd(reinterpret_cast<unsigned long long *>(acc + c * g.nodes + node),
@@ -191,15 +217,14 @@ __global__ void __launch_bounds__(kSliceParticles) k_p2g_fixed(GridP g, PartsF p
 
 // Float-atomic P2G (comparison variant: fp32 adds, order dependent).
 template <int DIM, int T>
-__global__ void __launch_bounds__(kSliceParticles) k_p2g_float(GridP g, PartsF p, const uint32_t *__restrict__ perm,
-                                                               const uint32_t *__restrict__ slices,
-                                                               const uint32_t *__restrict__ start,
-                                                               const uint32_t *__restrict__ status,
-                                                               float *__restrict__ acc) {
+__global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, const uint32_t *__restrict__ perm,
+                                                           const uint32_t *__restrict__ slices,
+                                                           const uint32_t *__restrict__ start,
+                                                           const uint32_t *__restrict__ status,
+                                                           float *__restrict__ acc) {
     using St = Stencil<DIM>;
-    constexpr int H = T + 2;
-    constexpr int HN = DIM == 3 ? H * H * H : H * H;
-    __shared__ float sacc[St::NC * HN];
+    using Hl = Halo<DIM, T>;
+    __shared__ float sacc[St::NC * Hl::SIZE];
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
@@ -207,67 +232,24 @@ __global__ void __launch_bounds__(kSliceParticles) k_p2g_float(GridP g, PartsF p
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
         int o[3];
         tile_origin(g, t, o);
-        for (int i = threadIdx.x; i < St::NC * HN; i += blockDim.x) sacc[i] = 0.f;
-        __syncthreads();
-        if (threadIdx.x < cnt) {
-            const uint32_t pid = perm[beg + threadIdx.x];
-            int b[3] = {0, 0, 0};
-            float f[3] = {0.f, 0.f, 0.f};
-            bool ok = true;
+        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
+            int hx, hy, hz, idx;
+            Hl::node(h, hx, hy, hz, idx);
 #pragma unroll
-            for (int l = 0; l < DIM; ++l) ok = ok && base_frac(p.x[l][pid], g.inv_dx, g.n[l], b[l], f[l]);
-            if (ok) {
-                float v[DIM], C[DIM * DIM], w[3][3], dd[3][3];
-#pragma unroll
-                for (int k = 0; k < DIM; ++k) v[k] = p.v[k][pid];
-#pragma unroll
-                for (int j = 0; j < DIM * DIM; ++j) C[j] = p.C[j][pid];
-                const float m = p.m[pid];
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) {
-                    quad_weights(f[l], w[l]);
-#pragma unroll
-                    for (int a = 0; a < 3; ++a) dd[l][a] = __fmul_rn(__fsub_rn((float)a, f[l]), g.dx);
-                }
-                const int hb = DIM == 3 ? ((b[2] - o[2]) * H + (b[1] - o[1])) * H + (b[0] - o[0])
-                                        : (b[1] - o[1]) * H + (b[0] - o[0]);
-#pragma unroll
-                for (int a0 = 0; a0 < 3; ++a0) {
-                    const float Wx = __fmul_rn(w[0][a0], m);
-                    float h0[DIM];
-#pragma unroll
-                    for (int k = 0; k < DIM; ++k) h0[k] = __fmaf_rn(C[k * DIM + 0], dd[0][a0], v[k]);
-#pragma unroll
-                    for (int a1 = 0; a1 < 3; ++a1) {
-                        const float Wxy = __fmul_rn(Wx, w[1][a1]);
-                        float h1[DIM];
-#pragma unroll
-                        for (int k = 0; k < DIM; ++k) h1[k] = __fmaf_rn(C[k * DIM + 1], dd[1][a1], h0[k]);
-#pragma unroll
-                        for (int a2 = 0; a2 < (DIM == 3 ? 3 : 1); ++a2) {
-                            const int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
-                            const float W = DIM == 3 ? __fmul_rn(Wxy, w[2][a2]) : Wxy;
-                            const int off = hb + halo_off<DIM, H>(a);
-                            atomicAdd(&sacc[off], W);
-#pragma unroll
-                            for (int k = 0; k < DIM; ++k) {
-                                const float vel = DIM == 3 ? __fmaf_rn(C[k * DIM + 2], dd[2][a2], h1[k]) : h1[k];
-                                atomicAdd(&sacc[(1 + k) * HN + off], __fmul_rn(W, vel));
-                            }
-                        }
-                    }
-                }
-            }
+            for (int c = 0; c < St::NC; ++c) sacc[c * Hl::SIZE + idx] = 0.f;
         }
         __syncthreads();
-        for (int h = threadIdx.x; h < HN; h += blockDim.x) {
-            const int hx = h % H, hy = (h / H) % H, hz = DIM == 3 ? h / (H * H) : 0;
+        for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x) scatter_float<DIM, T>(g, p, perm[beg + r], o, sacc);
+        __syncthreads();
+        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
+            int hx, hy, hz, idx;
+            Hl::node(h, hx, hy, hz, idx);
             const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
             if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
             const int64_t node = node_index(g, gx, gy, gz);
 #pragma unroll
             for (int c = 0; c < St::NC; ++c) {
-                const float val = sacc[c * HN + h];
+                const float val = sacc[c * Hl::SIZE + idx];
                 if (val != 0.f) atomicAdd(acc + c * g.nodes + node, val);
             }
         }
@@ -280,23 +262,23 @@ mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *gr
     const int blocks = dev.sms * 4;
     if (g.dim == 3 && g.T == 4) {
         if (g.acc_mode == MPM_ACC_I64)
-            k_p2g_fixed<3, 4, int64_t><<<blocks, kSliceParticles, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+            k_p2g_fixed<3, 4, int64_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
                                                                           (int64_t *)grid_acc);
         else if (g.acc_mode == MPM_ACC_I32)
-            k_p2g_fixed<3, 4, int32_t><<<blocks, kSliceParticles, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+            k_p2g_fixed<3, 4, int32_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
                                                                           (int32_t *)grid_acc);
         else
-            k_p2g_float<3, 4><<<blocks, kSliceParticles, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+            k_p2g_float<3, 4><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
                                                                  (float *)grid_acc);
     } else if (g.dim == 2 && g.T == 8) {
         if (g.acc_mode == MPM_ACC_I64)
-            k_p2g_fixed<2, 8, int64_t><<<blocks, kSliceParticles, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+            k_p2g_fixed<2, 8, int64_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
                                                                           (int64_t *)grid_acc);
         else if (g.acc_mode == MPM_ACC_I32)
-            k_p2g_fixed<2, 8, int32_t><<<blocks, kSliceParticles, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+            k_p2g_fixed<2, 8, int32_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
                                                                           (int32_t *)grid_acc);
         else
-            k_p2g_float<2, 8><<<blocks, kSliceParticles, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+            k_p2g_float<2, 8><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
                                                                  (float *)grid_acc);
     } else {
         return MPM_E_ARG;
