@@ -1,9 +1,11 @@
 """Benchmark of the MPM transfer step (bin + P2G + grid update + G2P).
 
 Default workload: 3D quadratic B-spline, 256^3 nodes, 16,777,216 particles in
-64 Gaussian blobs (sigma 0.02), int64 fixed point.  Particles start in the
-order of their initial binning (the caller keeps them sorted by cell, as a
-production simulation does) and every timed step recomputes the binning.
+64 Gaussian blobs (sigma 0.02), int64 fixed point.  Every step bins the
+particles, scatters, updates the grid and gathers with the sorted G2P, which
+writes the new state in bin order into the second particle buffer (ping-pong),
+so each step starts from the previous step's order (the steady state of a
+simulation that keeps its particles sorted).
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle on a bounded
 sample of the same workload instead.  Under torchrun (N > 1) every rank runs an
@@ -29,7 +31,7 @@ METRIC = "P2G+G2P particles/sec (3D 256^3, 16M clustered); % of HBM roofline"
 UNIT = "particles/s"
 WORKLOAD = "blobs3d: 3D quadratic B-spline MPM step, 256^3 nodes, 16,777,216 particles in 64 Gaussian blobs " \
            "(sigma 0.02), int64 fixed point"
-LAUNCHES_PER_STEP = 10  # bin: keys, 3 scans, scatter, tile sort, large-bucket sort; p2g; grid update; g2p
+LAUNCHES_PER_STEP = 11  # bin: keys, 3 scans, scatter, small/large tile order; p2g; grid update; g2p + copy
 
 
 def dist_env():
@@ -119,9 +121,8 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def sorted_workload(W, n_particles):
-    cloud = W.blobs3d(n_particles=n_particles)
-    return cloud
+def workload(W, n_particles, n_blobs=64):
+    return W.blobs3d(n_particles=n_particles, n_blobs=n_blobs)
 
 
 def run_ours(args, rank, world, local):
@@ -132,21 +133,10 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cloud = sorted_workload(W, args.particles)
+    cloud = workload(W, args.particles, args.blobs)
     grid = cloud["grid"]
     n = cloud["x"].shape[1]
-    sys_ = MPMSystem(grid, n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"])
-    # caller-side renumbering: particles stored in their initial bin order (steady state)
-    sys_.bin()
-    tmp = MPMSystem(grid, n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"])
-    L.mpm_permute(sys_.desc, sys_.parts, tmp.parts, sys_.bins)
-    torch.cuda.synchronize()
-    sys_.x.copy_(tmp.x)
-    sys_.v.copy_(tmp.v)
-    sys_.C.copy_(tmp.C)
-    sys_.m.copy_(tmp.m)
-    del tmp
-    torch.cuda.empty_cache()
+    sys_ = MPMSystem(grid, n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted()
     # touched nodes of the initial state (algorithmic grid bytes)
     sys_.bin()
     sys_.p2g()
@@ -156,8 +146,10 @@ def run_ours(args, rank, world, local):
     st = sys_.status()
     assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
     stream = torch.cuda.current_stream(dev)
+    # warm-up steps: the sorted step also moves the particles into bin order,
+    # so the timed steps start from (and stay in) the steady state
     for _ in range(args.warmup):
-        sys_.step(stream)
+        sys_.step_sorted(stream)
     torch.cuda.synchronize()
     # timed region
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
@@ -177,7 +169,7 @@ def run_ours(args, rank, world, local):
         e[2].record(stream)
         sys_.grid_update(stream)
         e[3].record(stream)
-        sys_.g2p(stream)
+        sys_.g2p_sorted(stream)
         e[4].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -197,7 +189,7 @@ def run_ours(args, rank, world, local):
         "bin": n * 24.0,
         "p2g": n * 64.0 + touched * 4 * 8.0,
         "grid_update": touched * 4 * 8.0,
-        "g2p": n * 72.0,
+        "g2p": n * 72.0,  # read x, write x v C (the m and id copies of the sorted output are extra)
     }
     dom = names[int(np.argmax(mean_ms))]
     peak, peak_kind = load_peaks()
@@ -210,25 +202,25 @@ def run_ours(args, rank, world, local):
     # end to end through the host entry point (pinned host SoA, copies inside the timed region)
     e2e = None
     if not args.no_e2e:
-        hx = torch.from_numpy(sys_.x.cpu().numpy()).pin_memory()
-        hv = torch.from_numpy(sys_.v.cpu().numpy()).pin_memory()
-        hC = torch.from_numpy(sys_.C.cpu().numpy()).pin_memory()
-        hm = torch.from_numpy(sys_.m.cpu().numpy()).pin_memory()
-        host = L.particles(hx, hv, hC, hm)
+        pin = lambda t: torch.from_numpy(t.cpu().numpy()).pin_memory()
+        hx, hv, hC, hm, hid = pin(sys_.x), pin(sys_.v), pin(sys_.C), pin(sys_.m), pin(sys_.id)
+        host = L.particles(hx, hv, hC, hm, hid)
         for _ in range(max(1, args.warmup)):
-            L.mpm_step_host(sys_.desc, host, sys_.parts, sys_.bins, sys_.acc, sys_.vel, sys_.dt, sys_.dtg, stream)
+            L.mpm_step_host(sys_.desc, host, sys_.parts, sys_.parts2, sys_.bins, sys_.acc, sys_.vel, sys_.dt,
+                            sys_.dtg, stream)
         torch.cuda.synchronize()
         barrier(world, dev)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(args.steps):
-            L.mpm_step_host(sys_.desc, host, sys_.parts, sys_.bins, sys_.acc, sys_.vel, sys_.dt, sys_.dtg, stream)
+            L.mpm_step_host(sys_.desc, host, sys_.parts, sys_.parts2, sys_.bins, sys_.acc, sys_.vel, sys_.dt,
+                            sys_.dtg, stream)
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = aggregate_max(a.elapsed_time(b) / args.steps, world, dev)
         e2e = {"value": round(n * world / (e2e_ms * 1e-3), 1), "unit": UNIT,
-               "h2d_bytes_per_step": n * 16 * 4, "d2h_bytes_per_step": n * 15 * 4,
+               "h2d_bytes_per_step": n * 17 * 4, "d2h_bytes_per_step": n * 17 * 4,
                "ms_per_step": round(e2e_ms, 4)}
 
     cpu = None
@@ -241,7 +233,7 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "f32+i64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "particles": n, "grid": grid["n"], "acc": "int64",
                    "scale_log2": grid["scale_log2"], "tile": grid["tile"], "touched_nodes": touched,
-                   "particle_order": "initial bin order (steady state)",
+                   "particle_order": "kept in bin order: each step's G2P writes the new state sorted (ping-pong)",
                    "l2": "inputs larger than L2 (1.07 GB of particle state per step)",
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, mean_ms)},
@@ -304,6 +296,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--particles", type=int, default=16777216)
+    ap.add_argument("--blobs", type=int, default=64, help="blobs (64 = the workload; fewer keeps the density "
+                    "of a smaller sample, for profiling)")
     ap.add_argument("--cpu-sample", type=int, default=2097152)
     ap.add_argument("--ref-sample", type=int, default=262144)
     ap.add_argument("--no-e2e", action="store_true")

@@ -73,13 +73,17 @@ typedef struct mpm_grid_desc {
 } mpm_grid_desc;
 
 /* Particle state (device SoA).  fp32 everywhere, except MPM_ACC_EXACT_INT:
- * x = int32 positions in 1/65,536 of a cell, v = int64, m = int64, C unused. */
+ * x = int32 positions in 1/65,536 of a cell, v = int64, m = int64, C unused.
+ * id: optional uint32 particle identities (NULL if unused); only the calls
+ * that move particles (mpm_permute, mpm_g2p_sorted, mpm_step_sorted,
+ * mpm_step_host) touch it, carrying it along with the particle. */
 typedef struct mpm_particles {
     int64_t n;
     void *x[3];
     void *v[3];
     void *C[9];
     const void *m;
+    void *id;
 } mpm_particles;
 
 /* Status words (device, uint32), in mpm_bins.status. */
@@ -91,7 +95,9 @@ enum {
     MPM_ST_N_SLICES = 4,     /* P2G work items */
     MPM_ST_N_ACTIVE = 5,     /* tiles holding at least one particle */
     MPM_ST_MAX_NEIGHBOURS = 6, /* int32 mode: most particles whose stencil covers one node */
-    MPM_ST_N_BIG_TILES = 7,  /* tiles sorted by the large-tile path */
+    MPM_ST_N_BIG_TILES = 7,  /* buckets ordered in global scratch (above the shared-memory capacity) */
+    MPM_ST_N_SMALL_BUCKETS = 8, /* buckets of at most 256 particles (ordered by one warp each) */
+    MPM_ST_N_LARGE_BUCKETS = 9, /* larger buckets (ordered by one block each) */
     MPM_STATUS_WORDS = 16
 };
 
@@ -197,23 +203,48 @@ mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *p
                    float dt, void *stream);
 
 /*
+ * mpm_g2p_sorted -- mpm_g2p that also moves the particles into bin order:
+ * out[j] is the gathered new state of particle in[perm[j]] for the in-domain
+ * particles (j below MPM_ST_N_VALID) and an unchanged copy of in[perm[j]] for
+ * the rest; m and id are carried along.  This is the ping-pong buffer of
+ * "Particle Worlds, part 3", Step 4 ("the sort writes into a second buffer"):
+ * the next step's binning then starts from almost sorted particles, so its
+ * permutation is close to the identity and every particle pass reads and
+ * writes contiguous memory.  The bits of every particle's new state are those
+ * of mpm_g2p.  `in` and `out` must not overlap.
+ */
+mpm_status mpm_g2p_sorted(const mpm_grid_desc *desc, const float *grid_vel, const mpm_particles *in,
+                          mpm_particles *out, mpm_bins *bins, float dt, void *stream);
+
+/*
  * mpm_step -- mpm_bin, mpm_p2g, mpm_grid_update and mpm_g2p in sequence on one
- * stream (device pointers throughout).
+ * stream (device pointers throughout; particles keep their index).
  */
 mpm_status mpm_step(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *bins, void *grid_acc,
                     float *grid_vel, float dt, const float dtg[3], void *stream);
 
 /*
- * mpm_step_host -- one step from and back to HOST particle arrays: copies the
- * host SoA (`host`, fp32; pinned memory gives full copy bandwidth) into the
- * device arrays of `dev`, runs mpm_step, and copies x, v, C back into `host`.
- * Asynchronous on `stream`; the host arrays must stay valid until it completes.
+ * mpm_step_sorted -- mpm_bin, mpm_p2g and mpm_grid_update on `in`, then
+ * mpm_g2p_sorted from `in` into `out` (the caller swaps the two between steps).
  */
-mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev, mpm_bins *bins,
-                         void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream);
+mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
+                           void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream);
+
+/*
+ * mpm_step_host -- one step from and back to HOST particle arrays: copies the
+ * host SoA (`host`: x, v, C, m and id if given; pinned memory gives full copy
+ * bandwidth) into the device arrays `dev_in`, runs mpm_step_sorted into
+ * `dev_out`, and copies x, v, C, m (and id) of `dev_out` back into `host`, so
+ * the host arrays hold the new state in bin order.  Asynchronous on `stream`;
+ * the host arrays must stay valid until it completes.
+ */
+mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev_in,
+                         mpm_particles *dev_out, mpm_bins *bins, void *grid_acc, float *grid_vel, float dt,
+                         const float dtg[3], void *stream);
 
 /* Reorders a particle SoA by bins->perm: out[j] = in[perm[j]] for every
- * component, all n entries.  `in` and `out` must not overlap. */
+ * component (and id if both are non-NULL), all n entries.  `in` and `out`
+ * must not overlap. */
 mpm_status mpm_permute(const mpm_grid_desc *desc, const mpm_particles *in, mpm_particles *out,
                        const mpm_bins *bins, void *stream);
 

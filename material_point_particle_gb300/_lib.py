@@ -17,7 +17,7 @@ from . import build as _build
 MPM_OK, MPM_E_ARG, MPM_E_WORKSPACE, MPM_E_DOMAIN, MPM_E_BOUND, MPM_E_CUDA, MPM_E_TIMEOUT, MPM_E_NO_DEVICE = range(8)
 MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
 (ST_FLAGS, ST_N_OUTSIDE, ST_N_OUT_OF_RANGE, ST_N_VALID, ST_N_SLICES, ST_N_ACTIVE, ST_MAX_NEIGHBOURS,
- ST_N_BIG_TILES) = range(8)
+ ST_N_BIG_TILES, ST_N_SMALL_BUCKETS, ST_N_LARGE_BUCKETS) = range(10)
 MPM_STATUS_WORDS = 16
 
 
@@ -35,7 +35,7 @@ class GridDesc(ct.Structure):
 
 class Particles(ct.Structure):
     _fields_ = [("n", ct.c_int64), ("x", ct.c_void_p * 3), ("v", ct.c_void_p * 3), ("C", ct.c_void_p * 9),
-                ("m", ct.c_void_p)]
+                ("m", ct.c_void_p), ("id", ct.c_void_p)]
 
 
 class Bins(ct.Structure):
@@ -72,12 +72,15 @@ def library() -> ct.CDLL:
             L.mpm_grid_update.argtypes = [P(GridDesc), VP, VP, P(ct.c_float), P(Bins), VP]
             L.mpm_g2p.argtypes = [P(GridDesc), VP, P(Particles), P(Bins), ct.c_float, VP]
             L.mpm_step.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, VP, ct.c_float, P(ct.c_float), VP]
-            L.mpm_step_host.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
-                                        P(ct.c_float), VP]
+            L.mpm_g2p_sorted.argtypes = [P(GridDesc), VP, P(Particles), P(Particles), P(Bins), ct.c_float, VP]
+            L.mpm_step_sorted.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
+                                          P(ct.c_float), VP]
+            L.mpm_step_host.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Particles), P(Bins), VP, VP,
+                                        ct.c_float, P(ct.c_float), VP]
             L.mpm_permute.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP]
             L.mpm_read_status.argtypes = [P(Bins), VP, VP]
             for name in ("mpm_bins_init", "mpm_bin", "mpm_p2g", "mpm_grid_update", "mpm_g2p", "mpm_step",
-                         "mpm_step_host", "mpm_permute", "mpm_read_status"):
+                         "mpm_g2p_sorted", "mpm_step_sorted", "mpm_step_host", "mpm_permute", "mpm_read_status"):
                 getattr(L, name).restype = ct.c_int
             _L = L
     return _L
@@ -113,9 +116,14 @@ def grid_desc(grid: dict) -> GridDesc:
     return d
 
 
-def particles(x: torch.Tensor, v: torch.Tensor, C: torch.Tensor | None, m: torch.Tensor) -> Particles:
-    """SoA view of [dim, n] / [dim*dim, n] / [n] tensors (rows must be contiguous)."""
+def particles(x: torch.Tensor, v: torch.Tensor, C: torch.Tensor | None, m: torch.Tensor,
+              id: torch.Tensor | None = None) -> Particles:
+    """SoA view of [dim, n] / [dim*dim, n] / [n] tensors (rows must be contiguous),
+    with optional uint32-sized [n] particle ids."""
     p = Particles()
+    if id is not None:
+        assert id.is_contiguous() and id.element_size() == 4
+        p.id = id.data_ptr()
     p.n = int(x.shape[1])
     for rows, field in ((x, p.x), (v, p.v), (C, p.C)):
         if rows is None:
@@ -190,10 +198,23 @@ def mpm_step(desc: GridDesc, parts: Particles, bins: Bins, grid_acc: torch.Tenso
            "mpm_step")
 
 
-def mpm_step_host(desc: GridDesc, host: Particles, dev: Particles, bins: Bins, grid_acc: torch.Tensor,
-                  grid_vel: torch.Tensor, dt: float, dtg, stream=None):
-    _check(library().mpm_step_host(ct.byref(desc), ct.byref(host), ct.byref(dev), ct.byref(bins),
-                                   ct.c_void_p(grid_acc.data_ptr()), ct.c_void_p(grid_vel.data_ptr()),
+def mpm_g2p_sorted(desc: GridDesc, grid_vel: torch.Tensor, src: Particles, dst: Particles, bins: Bins, dt: float,
+                   stream=None):
+    _check(library().mpm_g2p_sorted(ct.byref(desc), ct.c_void_p(grid_vel.data_ptr()), ct.byref(src), ct.byref(dst),
+                                    ct.byref(bins), ct.c_float(dt), _stream(stream)), "mpm_g2p_sorted")
+
+
+def mpm_step_sorted(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, grid_acc: torch.Tensor,
+                    grid_vel: torch.Tensor, dt: float, dtg, stream=None):
+    _check(library().mpm_step_sorted(ct.byref(desc), ct.byref(src), ct.byref(dst), ct.byref(bins),
+                                     ct.c_void_p(grid_acc.data_ptr()), ct.c_void_p(grid_vel.data_ptr()),
+                                     ct.c_float(dt), _f3(dtg), _stream(stream)), "mpm_step_sorted")
+
+
+def mpm_step_host(desc: GridDesc, host: Particles, dev_in: Particles, dev_out: Particles, bins: Bins,
+                  grid_acc: torch.Tensor, grid_vel: torch.Tensor, dt: float, dtg, stream=None):
+    _check(library().mpm_step_host(ct.byref(desc), ct.byref(host), ct.byref(dev_in), ct.byref(dev_out),
+                                   ct.byref(bins), ct.c_void_p(grid_acc.data_ptr()), ct.c_void_p(grid_vel.data_ptr()),
                                    ct.c_float(dt), _f3(dtg), _stream(stream)), "mpm_step_host")
 
 

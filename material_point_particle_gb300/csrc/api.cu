@@ -72,7 +72,9 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
 }
 
 struct Layout {
-    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, partial, status, cellcount, scratch, total;
+    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, gCA, gCS, small_list, large_list, partial,
+        status,
+        cellcount, scratch, total;
     int64_t max_slices;
 };
 
@@ -102,7 +104,11 @@ Layout layout_of(const GridP &g, int64_t n) {
     L.slices = take(2 * L.max_slices * sizeof(uint32_t));
     L.gH = take((n + g.ntiles + 2) * sizeof(uint32_t));
     L.gCW = take(2 * n * sizeof(uint64_t));
-    L.partial = take(3 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
+    L.gCA = take(n);
+    L.gCS = take(n);
+    L.small_list = take(nb * sizeof(uint32_t));
+    L.large_list = take(nb * sizeof(uint32_t));
+    L.partial = take(5 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
     L.status = take(MPM_STATUS_WORDS * sizeof(uint32_t));
     L.cellcount = g.acc_mode == MPM_ACC_I32 ? take((size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t)) : 0;
     L.scratch = take(2 * sizeof(uint64_t));
@@ -126,6 +132,10 @@ WsView view_of(const GridP &g, const mpm_bins &b) {
     w.slices = reinterpret_cast<uint32_t *>(base + L.slices);
     w.gH = reinterpret_cast<uint32_t *>(base + L.gH);
     w.gCW = base + L.gCW;
+    w.gCA = reinterpret_cast<uint8_t *>(base + L.gCA);
+    w.gCS = reinterpret_cast<uint8_t *>(base + L.gCS);
+    w.small_list = reinterpret_cast<uint32_t *>(base + L.small_list);
+    w.large_list = reinterpret_cast<uint32_t *>(base + L.large_list);
     w.partial = reinterpret_cast<uint32_t *>(base + L.partial);
     w.cellcount = g.acc_mode == MPM_ACC_I32 ? reinterpret_cast<uint32_t *>(base + L.cellcount) : nullptr;
     return w;
@@ -159,6 +169,7 @@ mpm_status parts_f(const GridP &g, const mpm_particles *p, bool need_state, Part
     }
     out.m = static_cast<const float *>(p->m);
     if (!out.m && p->n) return MPM_E_ARG;
+    out.id = static_cast<uint32_t *>(p->id);
     return MPM_OK;
 }
 
@@ -343,34 +354,64 @@ mpm_status mpm_step(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *b
     return mpm_g2p(desc, grid_vel, parts, bins, dt, stream);
 }
 
-mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev, mpm_bins *bins,
-                         void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream) {
+mpm_status mpm_g2p_sorted(const mpm_grid_desc *desc, const float *grid_vel, const mpm_particles *in,
+                          mpm_particles *out, mpm_bins *bins, float dt, void *stream) {
     GridP g;
     MPM_TRY(make_grid(desc, g));
-    if (g.acc_mode == MPM_ACC_EXACT_INT || !host || !dev || host->n != dev->n) return MPM_E_ARG;
-    PartsF ph, pd;
+    if (g.acc_mode == MPM_ACC_EXACT_INT || !grid_vel) return MPM_E_ARG;
+    PartsF pi, po;
+    MPM_TRY(parts_f(g, in, true, pi));
+    MPM_TRY(parts_f(g, out, true, po));
+    if (pi.n != po.n || (!pi.id) != (!po.id)) return MPM_E_ARG;
+    MPM_TRY(check_bins(g, bins, pi.n));
+    DeviceInfo dev;
+    MPM_TRY(device_info(dev));
+    return launch_g2p_sorted(g, grid_vel, pi, po, view_of(g, *bins), dt, dev, static_cast<cudaStream_t>(stream));
+}
+
+mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
+                           void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream) {
+    MPM_TRY(mpm_bin(desc, in, bins, 0, stream));
+    MPM_TRY(mpm_p2g(desc, in, bins, grid_acc, stream));
+    MPM_TRY(mpm_grid_update(desc, grid_acc, grid_vel, dtg, bins, stream));
+    return mpm_g2p_sorted(desc, grid_vel, in, out, bins, dt, stream);
+}
+
+mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev_in,
+                         mpm_particles *dev_out, mpm_bins *bins, void *grid_acc, float *grid_vel, float dt,
+                         const float dtg[3], void *stream) {
+    GridP g;
+    MPM_TRY(make_grid(desc, g));
+    if (g.acc_mode == MPM_ACC_EXACT_INT || !host || !dev_in || !dev_out) return MPM_E_ARG;
+    PartsF ph, pa, pb;
     MPM_TRY(parts_f(g, host, true, ph));
-    MPM_TRY(parts_f(g, dev, true, pd));
+    MPM_TRY(parts_f(g, dev_in, true, pa));
+    MPM_TRY(parts_f(g, dev_out, true, pb));
+    if (ph.n != pa.n || ph.n != pb.n) return MPM_E_ARG;
+    if ((!ph.id) != (!pa.id) || (!ph.id) != (!pb.id)) return MPM_E_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)ph.n * sizeof(float);
+    auto copy = [&](void *dst, const void *src, cudaMemcpyKind kind) {
+        return cudaMemcpyAsync(dst, src, bytes, kind, st) == cudaSuccess;
+    };
     if (bytes) {
-        for (int l = 0; l < g.dim; ++l) {
-            if (cudaMemcpyAsync(pd.x[l], ph.x[l], bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return MPM_E_CUDA;
-            if (cudaMemcpyAsync(pd.v[l], ph.v[l], bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return MPM_E_CUDA;
-        }
-        for (int j = 0; j < g.dim * g.dim; ++j)
-            if (cudaMemcpyAsync(pd.C[j], ph.C[j], bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return MPM_E_CUDA;
-        if (cudaMemcpyAsync(const_cast<float *>(pd.m), ph.m, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-            return MPM_E_CUDA;
+        bool ok = true;
+        for (int l = 0; l < g.dim; ++l) ok = ok && copy(pa.x[l], ph.x[l], cudaMemcpyHostToDevice);
+        for (int l = 0; l < g.dim; ++l) ok = ok && copy(pa.v[l], ph.v[l], cudaMemcpyHostToDevice);
+        for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(pa.C[j], ph.C[j], cudaMemcpyHostToDevice);
+        ok = ok && copy(const_cast<float *>(pa.m), ph.m, cudaMemcpyHostToDevice);
+        if (ph.id) ok = ok && copy(pa.id, ph.id, cudaMemcpyHostToDevice);
+        if (!ok) return MPM_E_CUDA;
     }
-    MPM_TRY(mpm_step(desc, dev, bins, grid_acc, grid_vel, dt, dtg, stream));
+    MPM_TRY(mpm_step_sorted(desc, dev_in, dev_out, bins, grid_acc, grid_vel, dt, dtg, stream));
     if (bytes) {
-        for (int l = 0; l < g.dim; ++l) {
-            if (cudaMemcpyAsync(ph.x[l], pd.x[l], bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MPM_E_CUDA;
-            if (cudaMemcpyAsync(ph.v[l], pd.v[l], bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MPM_E_CUDA;
-        }
-        for (int j = 0; j < g.dim * g.dim; ++j)
-            if (cudaMemcpyAsync(ph.C[j], pd.C[j], bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MPM_E_CUDA;
+        bool ok = true;
+        for (int l = 0; l < g.dim; ++l) ok = ok && copy(ph.x[l], pb.x[l], cudaMemcpyDeviceToHost);
+        for (int l = 0; l < g.dim; ++l) ok = ok && copy(ph.v[l], pb.v[l], cudaMemcpyDeviceToHost);
+        for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(ph.C[j], pb.C[j], cudaMemcpyDeviceToHost);
+        ok = ok && copy(const_cast<float *>(ph.m), pb.m, cudaMemcpyDeviceToHost);
+        if (ph.id) ok = ok && copy(ph.id, pb.id, cudaMemcpyDeviceToHost);
+        if (!ok) return MPM_E_CUDA;
     }
     return MPM_OK;
 }

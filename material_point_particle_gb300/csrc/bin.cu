@@ -19,8 +19,10 @@
 //                   exclusive scans of (count, P2G slices, active flag) over
 //                   the buckets; active-tile list, P2G work list, cursors
 //   k_scatter       warp-aggregated atomic scatter of indices into buckets
-//   k_tile_order    per-tile order: claims sorted back into index order, a
-//                   stable counting sort by cell, the rank-major write-out
+//   k_order_small   per-tile order for buckets up to 256 entries (one warp)
+//   k_order_large   per-tile order for larger buckets (one block): claims put
+//                   back into index order, a stable counting sort by cell,
+//                   the rank-major write-out
 //   k_nbr_bound     int32 mode: most stencils covering one node (the
 //                   accumulator bound, checked before any scatter)
 #include "common.cuh"
@@ -66,101 +68,122 @@ __global__ void k_keys(GridP g, PartsF p, uint32_t *__restrict__ key, uint32_t *
 // --------------------------------------------------------------------------
 // Scans over the nb = ntiles + 1 buckets (the last bucket holds the particles
 // outside the domain).  Each thread of a 256-thread block owns 4 buckets.
+// Five running totals: particles, P2G slices, active tiles, and the buckets
+// ordered by the warp kernel (small) and by the block kernel (large).
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 4;
 constexpr int kScanBlock = kScanThreads * kScanItems;
+constexpr uint32_t kSmallBucket = 256;   // buckets up to this size are ordered by one warp
 
-struct Tri {
-    uint32_t a, b, c;
+struct Tot5 {
+    uint32_t v[5];
 };
 
-__device__ __forceinline__ Tri tri_add(Tri x, Tri y) { return {x.a + y.a, x.b + y.b, x.c + y.c}; }
-
-__device__ __forceinline__ Tri bucket_values(const GridP &g, const uint32_t *count, int64_t nb, int64_t b) {
-    if (b >= nb) return {0, 0, 0};
-    uint32_t c = count[b];
-    if (b == nb - 1) return {c, 0, 0};  // outside-the-domain bucket: no P2G work
-    return {c, (c + kSliceParticles - 1) / kSliceParticles, c > 0 ? 1u : 0u};
+__device__ __forceinline__ Tot5 tot_add(const Tot5 &x, const Tot5 &y) {
+    Tot5 r;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) r.v[i] = x.v[i] + y.v[i];
+    return r;
 }
 
-// Block-wide exclusive scan of one Tri per thread; returns the block total.
-__device__ Tri block_exclusive_scan(Tri v, Tri &excl) {
-    __shared__ Tri warp_tot[kScanThreads / 32];
+__device__ __forceinline__ Tot5 tot_zero() { return Tot5{{0, 0, 0, 0, 0}}; }
+
+__device__ __forceinline__ Tot5 bucket_values(const uint32_t *count, int64_t nb, int64_t b) {
+    if (b >= nb) return tot_zero();
+    const uint32_t c = count[b];
+    const bool outside = b == nb - 1;
+    Tot5 r;
+    r.v[0] = c;
+    r.v[1] = outside ? 0u : (c + kSliceParticles - 1) / kSliceParticles;  // no P2G work outside
+    r.v[2] = (!outside && c > 0) ? 1u : 0u;
+    r.v[3] = (c > 0 && c <= kSmallBucket) ? 1u : 0u;
+    r.v[4] = c > kSmallBucket ? 1u : 0u;
+    return r;
+}
+
+// Block-wide exclusive scan of one Tot5 per thread; returns the block total.
+__device__ Tot5 block_exclusive_scan(const Tot5 &v, Tot5 &excl) {
+    __shared__ Tot5 warp_tot[kScanThreads / 32];
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-    Tri inc = v;
+    Tot5 inc = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        uint32_t a = __shfl_up_sync(0xFFFFFFFFu, inc.a, d);
-        uint32_t b = __shfl_up_sync(0xFFFFFFFFu, inc.b, d);
-        uint32_t c = __shfl_up_sync(0xFFFFFFFFu, inc.c, d);
-        if ((int)lane >= d) inc = tri_add(inc, {a, b, c});
+        Tot5 t;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) t.v[i] = __shfl_up_sync(0xFFFFFFFFu, inc.v[i], d);
+        if ((int)lane >= d) inc = tot_add(inc, t);
     }
     if (lane == 31) warp_tot[warp] = inc;
     __syncthreads();
-    Tri before = {0, 0, 0}, total = {0, 0, 0};
+    Tot5 before = tot_zero(), total = tot_zero();
     for (int w = 0; w < kScanThreads / 32; ++w) {
-        if (w < (int)warp) before = tri_add(before, warp_tot[w]);
-        total = tri_add(total, warp_tot[w]);
+        if (w < (int)warp) before = tot_add(before, warp_tot[w]);
+        total = tot_add(total, warp_tot[w]);
     }
-    excl = {before.a + inc.a - v.a, before.b + inc.b - v.b, before.c + inc.c - v.c};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) excl.v[i] = before.v[i] + inc.v[i] - v.v[i];
     __syncthreads();
     return total;
 }
 
-__global__ void k_scan_reduce(GridP g, const uint32_t *__restrict__ count, int64_t nb, Tri *__restrict__ partial) {
+__global__ void k_scan_reduce(const uint32_t *__restrict__ count, int64_t nb, Tot5 *__restrict__ partial) {
     const int64_t b0 = (int64_t)blockIdx.x * kScanBlock + threadIdx.x * kScanItems;
-    Tri s = {0, 0, 0};
-    for (int j = 0; j < kScanItems; ++j) s = tri_add(s, bucket_values(g, count, nb, b0 + j));
-    Tri excl;
-    Tri tot = block_exclusive_scan(s, excl);
+    Tot5 s = tot_zero();
+    for (int j = 0; j < kScanItems; ++j) s = tot_add(s, bucket_values(count, nb, b0 + j));
+    Tot5 excl;
+    Tot5 tot = block_exclusive_scan(s, excl);
     if (threadIdx.x == 0) partial[blockIdx.x] = tot;
 }
 
 // One block: exclusive scan of the block totals (in place) and the grand totals.
-__global__ void k_scan_top(Tri *__restrict__ partial, int64_t nblocks, const uint32_t *__restrict__ count,
+__global__ void k_scan_top(Tot5 *__restrict__ partial, int64_t nblocks, const uint32_t *__restrict__ count,
                            int64_t nb, uint32_t *__restrict__ status) {
-    Tri carry = {0, 0, 0};
+    Tot5 carry = tot_zero();
     for (int64_t base = 0; base < nblocks; base += kScanThreads) {
-        int64_t i = base + threadIdx.x;
-        Tri v = i < nblocks ? partial[i] : Tri{0, 0, 0};
-        Tri excl;
-        Tri tot = block_exclusive_scan(v, excl);
-        if (i < nblocks) partial[i] = tri_add(carry, excl);
-        carry = tri_add(carry, tot);
+        const int64_t i = base + threadIdx.x;
+        const Tot5 v = i < nblocks ? partial[i] : tot_zero();
+        Tot5 excl;
+        const Tot5 tot = block_exclusive_scan(v, excl);
+        if (i < nblocks) partial[i] = tot_add(carry, excl);
+        carry = tot_add(carry, tot);
     }
     if (threadIdx.x == 0) {
-        status[MPM_ST_N_VALID] = carry.a - count[nb - 1];
-        status[MPM_ST_N_SLICES] = carry.b;
-        status[MPM_ST_N_ACTIVE] = carry.c;
+        status[MPM_ST_N_VALID] = carry.v[0] - count[nb - 1];
+        status[MPM_ST_N_SLICES] = carry.v[1];
+        status[MPM_ST_N_ACTIVE] = carry.v[2];
+        status[MPM_ST_N_SMALL_BUCKETS] = carry.v[3];
+        status[MPM_ST_N_LARGE_BUCKETS] = carry.v[4];
     }
 }
 
-__global__ void k_scan_final(GridP g, const uint32_t *__restrict__ count, int64_t nb, const Tri *__restrict__ partial,
+__global__ void k_scan_final(const uint32_t *__restrict__ count, int64_t nb, const Tot5 *__restrict__ partial,
                              uint32_t *__restrict__ start, uint32_t *__restrict__ cursor,
                              uint32_t *__restrict__ active, uint32_t *__restrict__ slices,
-                             uint32_t *__restrict__ status) {
+                             uint32_t *__restrict__ small_list, uint32_t *__restrict__ large_list) {
     const int64_t b0 = (int64_t)blockIdx.x * kScanBlock + threadIdx.x * kScanItems;
-    Tri v[kScanItems];
-    Tri s = {0, 0, 0};
+    Tot5 v[kScanItems];
+    Tot5 s = tot_zero();
     for (int j = 0; j < kScanItems; ++j) {
-        v[j] = bucket_values(g, count, nb, b0 + j);
-        s = tri_add(s, v[j]);
+        v[j] = bucket_values(count, nb, b0 + j);
+        s = tot_add(s, v[j]);
     }
-    Tri excl;
+    Tot5 excl;
     block_exclusive_scan(s, excl);
-    Tri run = tri_add(partial[blockIdx.x], excl);
+    Tot5 run = tot_add(partial[blockIdx.x], excl);
     for (int j = 0; j < kScanItems; ++j) {
         const int64_t b = b0 + j;
         if (b >= nb) break;
-        start[b] = run.a;
-        cursor[b] = run.a;
-        if (v[j].c) active[run.c] = (uint32_t)b;
-        for (uint32_t s2 = 0; s2 < v[j].b; ++s2) {
-            slices[2 * (int64_t)(run.b + s2)] = (uint32_t)b;
-            slices[2 * (int64_t)(run.b + s2) + 1] = s2 * kSliceParticles;
+        start[b] = run.v[0];
+        cursor[b] = run.v[0];
+        if (v[j].v[2]) active[run.v[2]] = (uint32_t)b;
+        for (uint32_t s2 = 0; s2 < v[j].v[1]; ++s2) {
+            slices[2 * (int64_t)(run.v[1] + s2)] = (uint32_t)b;
+            slices[2 * (int64_t)(run.v[1] + s2) + 1] = s2 * kSliceParticles;
         }
-        run = tri_add(run, v[j]);
-        if (b == nb - 1) start[nb] = run.a;
+        if (v[j].v[3]) small_list[run.v[3]] = (uint32_t)b;
+        if (v[j].v[4]) large_list[run.v[4]] = (uint32_t)b;
+        run = tot_add(run, v[j]);
+        if (b == nb - 1) start[nb] = run.v[0];
     }
 }
 
@@ -189,19 +212,159 @@ __global__ void k_scatter(GridP g, const uint32_t *__restrict__ key, int64_t n, 
 }
 
 // --------------------------------------------------------------------------
-// The order inside each tile.  The atomic scatter filled each bucket with
-// "claims": one per warp and bucket, holding that warp's lanes of the bucket
-// in lane (= index) order, and all sharing idx >> 5 (a warp covers 32
-// consecutive indices per round).  So sorting the claims by idx >> 5 puts the
-// bucket in index order.  In steady state a tile has few claims; from a cold
-// order every entry is its own claim and this is a plain sort.  A stable
-// counting sort by cell follows (cell-major, each cell in index order), then
-// the rank-major write-out: each group of 32 cells lists rank 0 of its cells,
-// then rank 1, and so on.  Buckets above kOrderCap entries use global scratch
-// instead of shared memory (same code, generic pointers).
+// The order inside each tile.  The atomic scatter leaves each bucket as a set
+// of "claims": one per warp-round and bucket, holding that warp's lanes of the
+// bucket in lane (= index) order, all sharing w = idx >> 5 (a warp covers 32
+// consecutive indices per round).  The stable order wanted is cell-major with
+// each cell in index order; the output lists, for each group of 32 cells,
+// rank 0 of its cells, then rank 1, and so on.
+//
+// Small buckets (at most 256 entries): one warp sorts (cell, index) keys in
+// registers with a bitonic network.
+// Large buckets: one block.  Claims are put in index order by a table over a
+// window of 2048 values of w around the bucket's median entry (in steady
+// state almost every claim falls there); the few claims outside the window
+// are sorted and placed before or after it.  Then a stable counting sort by
+// cell and the rank-major write-out.  Buckets above kOrderCap entries keep
+// their working arrays in global scratch instead of shared memory.
 constexpr int kOrderThreads = 256;
-constexpr int kOrderCap = 4096;
 constexpr int kOrderWarps = kOrderThreads / 32;
+constexpr int kOrderCap = 8192;
+constexpr int kWindow = 2048;
+constexpr int kFarCap = 256;  // far claims kept in shared memory (and sorted by one warp)
+constexpr int kHeadCap = kOrderCap / 4;  // claim heads kept in shared memory
+
+template <int E>
+__device__ __forceinline__ void warp_bitonic(unsigned long long (&v)[E]) {
+    const uint32_t lane = lane_id();
+#pragma unroll
+    for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= 32) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int e2 = e ^ (j >> 5);
+                    if (e < e2) {
+                        const bool asc = (((uint32_t)e * 32u + lane) & (uint32_t)k) == 0;
+                        const unsigned long long a = v[e], b = v[e2];
+                        if ((a > b) == asc) {
+                            v[e] = b;
+                            v[e2] = a;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const bool asc = (((uint32_t)e * 32u + lane) & (uint32_t)k) == 0;
+                    const unsigned long long p = __shfl_xor_sync(0xFFFFFFFFu, v[e], j);
+                    const bool lower = (lane & (uint32_t)j) == 0;
+                    v[e] = (lower == asc) ? (v[e] < p ? v[e] : p) : (v[e] < p ? p : v[e]);
+                }
+            }
+        }
+    }
+}
+
+// Rank-major write-out of a cell-major run cm[0, cnt) with per-cell counts and
+// starts (64 cells), by one warp per group (warp index `grp`).
+__device__ __forceinline__ void write_rank_major(uint32_t grp, const uint32_t *cnt64, const uint32_t *cs64,
+                                                 const uint32_t *cm, uint32_t *out) {
+    const uint32_t lane = lane_id();
+    const uint32_t c = grp * 32 + lane;
+    const uint32_t nc = cnt64[c], first = cs64[c];
+    uint32_t seg = cs64[grp * 32];
+    for (uint32_t r = 0;; ++r) {
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, nc > r);
+        if (m == 0) break;
+        if (nc > r) out[seg + __popc(m & lanemask_lt())] = cm[first + r];
+        seg += __popc(m);
+    }
+}
+
+template <int E>
+__device__ void order_small(const GridP &g, const uint32_t *key, const uint32_t *tmp, uint32_t beg, uint32_t cnt,
+                            bool outside, uint32_t *perm, uint32_t *sbuf, uint32_t *scnt, uint32_t *sfirst) {
+    const uint32_t lane = lane_id();
+    const uint32_t cmask = (1u << g.cpt_log2) - 1;
+    unsigned long long v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const uint32_t i = (uint32_t)e * 32u + lane;
+        if (i < cnt) {
+            const uint32_t idx = tmp[beg + i];
+            const uint32_t c = outside ? 0u : (key[idx] & cmask);
+            v[e] = ((unsigned long long)c << 32) | idx;
+        } else {
+            v[e] = ~0ull;
+        }
+    }
+    warp_bitonic<E>(v);
+    if (outside) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const uint32_t i = (uint32_t)e * 32u + lane;
+            if (i < cnt) perm[beg + i] = (uint32_t)v[e];
+        }
+        return;
+    }
+    scnt[lane] = 0;
+    scnt[lane + 32] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const uint32_t i = (uint32_t)e * 32u + lane;
+        if (i < cnt) {
+            sbuf[i] = (uint32_t)v[e];
+            atomicAdd(&scnt[(uint32_t)(v[e] >> 32)], 1u);
+        }
+    }
+    __syncwarp();
+    const uint32_t a0 = scnt[2 * lane], a1 = scnt[2 * lane + 1];
+    uint32_t inc = a0 + a1;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if ((int)lane >= d) inc += t;
+    }
+    sfirst[2 * lane] = inc - a0 - a1;
+    sfirst[2 * lane + 1] = inc - a1;
+    __syncwarp();
+    write_rank_major(0, scnt, sfirst, sbuf, perm + beg);
+    write_rank_major(1, scnt, sfirst, sbuf, perm + beg);
+    __syncwarp();
+}
+
+__global__ void __launch_bounds__(256) k_order_small(GridP g, const uint32_t *__restrict__ key,
+                                                     const uint32_t *__restrict__ tmp,
+                                                     const uint32_t *__restrict__ start,
+                                                     const uint32_t *__restrict__ count,
+                                                     const uint32_t *__restrict__ list, int64_t nb,
+                                                     uint32_t *__restrict__ perm, const uint32_t *__restrict__ status) {
+    __shared__ uint32_t sbuf[8][kSmallBucket];
+    __shared__ uint32_t scnt[8][64];
+    __shared__ uint32_t sfirst[8][64];
+    const uint32_t nitems = status[MPM_ST_N_SMALL_BUCKETS];
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    const uint32_t nw = gridDim.x * 8;
+    for (uint32_t it = blockIdx.x * 8 + warp; it < nitems; it += nw) {
+        const uint32_t b = list[it];
+        const uint32_t beg = start[b], cnt = count[b];
+        const bool outside = b == (uint32_t)(nb - 1);
+        if (cnt == 1) {
+            if (lane == 0) perm[beg] = tmp[beg];
+        } else if (cnt <= 32) {
+            order_small<1>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+        } else if (cnt <= 64) {
+            order_small<2>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+        } else if (cnt <= 128) {
+            order_small<4>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+        } else {
+            order_small<8>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+        }
+    }
+}
 
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t &total, uint32_t *sh) {
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -245,78 +408,179 @@ __device__ void block_bitonic(unsigned long long *s, uint32_t n_pow2) {
 }
 
 __global__ void __launch_bounds__(kOrderThreads)
-k_tile_order(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const uint32_t *__restrict__ start,
-             const uint32_t *__restrict__ count, const uint32_t *__restrict__ active, int64_t nb, uint32_t *perm,
-             uint32_t *gH, unsigned long long *gCW, uint32_t *__restrict__ status) {
+k_order_large(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const uint32_t *__restrict__ start,
+              const uint32_t *__restrict__ count, const uint32_t *__restrict__ list, int64_t nb, uint32_t *perm,
+              uint32_t *gH, unsigned long long *gF, uint8_t *gCA, uint8_t *gCS, uint32_t *__restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    unsigned long long *sCW = reinterpret_cast<unsigned long long *>(smem_raw);
-    uint32_t *sA = reinterpret_cast<uint32_t *>(sCW + kOrderCap);
+    uint32_t *sA = reinterpret_cast<uint32_t *>(smem_raw);
     uint32_t *sS = sA + kOrderCap;
-    uint32_t *sH = sS + kOrderCap;
-    __shared__ uint32_t cnt64[64], cs64[65], run64[64];
-    __shared__ uint32_t wcnt[kOrderWarps][64], woff[kOrderWarps][64];
+    uint32_t *sH = sS + kOrderCap;                                  // kHeadCap + 1 entries
+    uint8_t *sCA = reinterpret_cast<uint8_t *>(sH + kHeadCap + 4);  // cell of each entry of A
+    uint8_t *sCS = sCA + kOrderCap;                                 // cell of each entry of S
+    __shared__ uint32_t table[kWindow];
+    __shared__ unsigned long long sF[kFarCap];
+    __shared__ uint32_t cnt64[64], cs64[64];
+    __shared__ uint32_t wcnt[kOrderWarps][64];
     __shared__ uint32_t scan_sh[kOrderWarps];
+    __shared__ uint32_t nfar_sh, nlow_sh;
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-    const uint32_t n_active = status[MPM_ST_N_ACTIVE];
+    const uint32_t nitems = status[MPM_ST_N_LARGE_BUCKETS];
     const uint32_t cmask = (1u << g.cpt_log2) - 1;
-    for (uint32_t item = blockIdx.x; item <= n_active; item += gridDim.x) {
-        const bool outside = item == n_active;
-        const uint32_t b = outside ? (uint32_t)(nb - 1) : active[item];
+    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
+        const uint32_t b = list[it];
         const uint32_t beg = start[b], cnt = count[b];
-        if (cnt == 0) continue;
-        if (cnt == 1) {
-            if (threadIdx.x == 0) perm[beg] = tmp[beg];
-            continue;
-        }
+        const bool outside = b == (uint32_t)(nb - 1);
         const bool small = cnt <= (uint32_t)kOrderCap;
         if (!small && threadIdx.x == 0) atomicAdd(&status[MPM_ST_N_BIG_TILES], 1u);
         uint32_t *A = small ? sA : tmp + beg;
         uint32_t *S = small ? sS : perm + beg;
-        uint32_t *H = small ? sH : gH + (size_t)beg + item;
-        unsigned long long *CW = small ? sCW : gCW + 2 * (size_t)beg;
-        if (small)
-            for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) A[i] = tmp[beg + i];
-        __syncthreads();
-        // claims: heads where idx >> 5 changes
-        uint32_t nclaims = 0;
-        for (uint32_t base = 0; base < cnt; base += blockDim.x) {
-            const uint32_t i = base + threadIdx.x;
-            uint32_t head = 0, w = 0;
-            if (i < cnt) {
-                w = A[i] >> 5;
-                head = (i == 0 || w != (A[i - 1] >> 5)) ? 1u : 0u;
-            }
-            uint32_t tot;
-            const uint32_t ex = block_excl_scan(head, tot, scan_sh);
-            if (head) {
-                const uint32_t k = nclaims + ex;
-                H[k] = i;
-                CW[k] = ((unsigned long long)w << 32) | k;
-            }
-            nclaims += tot;
+        uint8_t *CA = small ? sCA : gCA + beg;
+        uint8_t *CS = small ? sCS : gCS + beg;
+        // load the entries and gather each one's cell once (independent loads)
+        for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) {
+            const uint32_t idx = tmp[beg + i];
+            if (small) A[i] = idx;
+            CA[i] = outside ? (uint8_t)0 : (uint8_t)(key[idx] & cmask);
         }
-        uint32_t np2 = 1;
-        while (np2 < nclaims) np2 <<= 1;
-        for (uint32_t k = nclaims + threadIdx.x; k < np2; k += blockDim.x) CW[k] = ~0ull;
+        if (threadIdx.x == 0) nfar_sh = 0;
+        for (uint32_t d = threadIdx.x; d < (uint32_t)kWindow; d += blockDim.x) table[d] = 0;
+        __syncthreads();
+        // claim heads: warp w scans the contiguous segment [w*hseg, (w+1)*hseg)
+        // 32 entries at a time, counts its heads, then writes their positions
+        const uint32_t hseg = (cnt + kOrderWarps - 1) / kOrderWarps;
+        const uint32_t h0 = min(cnt, warp * hseg), h1 = min(cnt, h0 + hseg);
+        uint32_t myheads = 0;
+        for (uint32_t base = h0; base < h1; base += 32) {
+            const uint32_t i = base + lane;
+            const bool head = i < h1 && (i == 0 || (A[i] >> 5) != (A[i - 1] >> 5));
+            myheads += __popc(__ballot_sync(0xFFFFFFFFu, head));
+        }
+        uint32_t nclaims;
+        uint32_t k = block_excl_scan(lane == 0 ? myheads : 0u, nclaims, scan_sh);
+        k = __shfl_sync(0xFFFFFFFFu, k, 0);
+        uint32_t *H = (small && nclaims <= (uint32_t)kHeadCap) ? sH : gH + (size_t)beg + b;
+        for (uint32_t base = h0; base < h1; base += 32) {
+            const uint32_t i = base + lane;
+            const bool head = i < h1 && (i == 0 || (A[i] >> 5) != (A[i - 1] >> 5));
+            const uint32_t m = __ballot_sync(0xFFFFFFFFu, head);
+            if (head) H[k + __popc(m & lanemask_lt())] = i;
+            k += __popc(m);
+        }
         if (threadIdx.x == 0) H[nclaims] = cnt;
         __syncthreads();
-        if (nclaims > 1) block_bitonic(CW, np2);
-        // claims in index order: copy each claim to its destination
-        uint32_t done = 0;
-        for (uint32_t base = 0; base < nclaims; base += blockDim.x) {
-            const uint32_t j = base + threadIdx.x;
-            uint32_t len = 0, k = 0;
-            if (j < nclaims) {
-                k = (uint32_t)(CW[j] & 0xFFFFFFFFu);
-                len = H[k + 1] - H[k];
+        // window around the median entry; claims inside go to the table by w,
+        // the others ("far") to a list sorted below
+        const long long w_lo = (long long)(A[cnt / 2] >> 5) - kWindow / 2;
+        for (uint32_t c = threadIdx.x; c < nclaims; c += blockDim.x) {
+            const long long d = (long long)(A[H[c]] >> 5) - w_lo;
+            if (d >= 0 && d < kWindow) table[d] = H[c + 1] - H[c];
+            else atomicAdd(&nfar_sh, 1u);
+        }
+        __syncthreads();
+        const uint32_t nfar = nfar_sh;
+        unsigned long long *F = nfar <= (uint32_t)kFarCap ? sF : gF + 2 * (size_t)beg;
+        __syncthreads();
+        if (threadIdx.x == 0) nfar_sh = 0;
+        __syncthreads();
+        for (uint32_t c = threadIdx.x; c < nclaims; c += blockDim.x) {
+            const uint32_t w = A[H[c]] >> 5;
+            const long long d = (long long)w - w_lo;
+            if (!(d >= 0 && d < kWindow)) F[atomicAdd(&nfar_sh, 1u)] = ((unsigned long long)w << 32) | c;
+        }
+        __syncthreads();
+        if (nfar > 1 && nfar <= (uint32_t)kFarCap) {
+            // one warp sorts in registers
+            if (warp == 0) {
+                unsigned long long v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t f = (uint32_t)e * 32u + lane;
+                    v[e] = f < nfar ? F[f] : ~0ull;
+                }
+                warp_bitonic<8>(v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t f = (uint32_t)e * 32u + lane;
+                    if (f < nfar) F[f] = v[e];
+                }
+            }
+            __syncthreads();
+        } else if (nfar > (uint32_t)kFarCap) {
+            uint32_t np2 = 1;
+            while (np2 < nfar) np2 <<= 1;
+            for (uint32_t f = nfar + threadIdx.x; f < np2; f += blockDim.x) F[f] = ~0ull;
+            __syncthreads();
+            block_bitonic(F, np2);
+        }
+        // far claims below the window come first: count them (binary search in
+        // the sorted keys) and add up their lengths
+        if (threadIdx.x == 0) {
+            uint32_t lo2 = 0, hi2 = nfar;
+            while (lo2 < hi2) {
+                const uint32_t mid = (lo2 + hi2) / 2;
+                if ((long long)(F[mid] >> 32) < w_lo) lo2 = mid + 1;
+                else hi2 = mid;
+            }
+            nlow_sh = lo2;
+        }
+        __syncthreads();
+        const uint32_t nlow = nlow_sh;
+        uint32_t mylow = 0;
+        for (uint32_t f = threadIdx.x; f < nlow; f += blockDim.x) {
+            const uint32_t c = (uint32_t)(F[f] & 0xFFFFFFFFu);
+            mylow += H[c + 1] - H[c];
+        }
+        uint32_t lowlen;
+        block_excl_scan(mylow, lowlen, scan_sh);
+        // table prefix (blocked, 8 slots per thread) -> destinations of the window claims
+        constexpr int kPer = kWindow / kOrderThreads;
+        uint32_t tv[kPer], tsum = 0;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            tv[q] = table[threadIdx.x * kPer + q];
+            tsum += tv[q];
+        }
+        uint32_t wintotal;
+        uint32_t toff = block_excl_scan(tsum, wintotal, scan_sh);
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const uint32_t t = tv[q];
+            table[threadIdx.x * kPer + q] = lowlen + toff;
+            toff += t;
+        }
+        __syncthreads();
+        // copy window claims
+        for (uint32_t c = threadIdx.x; c < nclaims; c += blockDim.x) {
+            const uint32_t src = H[c], len = H[c + 1] - H[c];
+            const long long d = (long long)(A[src] >> 5) - w_lo;
+            if (d >= 0 && d < kWindow) {
+                const uint32_t dst = table[d];
+                for (uint32_t e = 0; e < len; ++e) {
+                    S[dst + e] = A[src + e];
+                    CS[dst + e] = CA[src + e];
+                }
+            }
+        }
+        // copy far claims in sorted order (block-wide prefix of their lengths)
+        uint32_t run = 0;
+        for (uint32_t base = 0; base < nfar; base += blockDim.x) {
+            const uint32_t f = base + threadIdx.x;
+            uint32_t len = 0, c = 0;
+            if (f < nfar) {
+                c = (uint32_t)(F[f] & 0xFFFFFFFFu);
+                len = H[c + 1] - H[c];
             }
             uint32_t tot;
-            const uint32_t ex = block_excl_scan(len, tot, scan_sh);
-            if (j < nclaims) {
-                const uint32_t d = done + ex, src = H[k];
-                for (uint32_t e = 0; e < len; ++e) S[d + e] = A[src + e];
+            const uint32_t ex = run + block_excl_scan(len, tot, scan_sh);
+            if (f < nfar) {
+                const uint32_t dst = f < nlow ? ex : ex + wintotal;
+                const uint32_t src = H[c];
+                for (uint32_t e = 0; e < len; ++e) {
+                    S[dst + e] = A[src + e];
+                    CS[dst + e] = CA[src + e];
+                }
             }
-            done += tot;
+            run += tot;
         }
         __syncthreads();
         if (outside) {
@@ -325,17 +589,28 @@ k_tile_order(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const uin
             __syncthreads();
             continue;
         }
-        // stable counting sort by cell: S (index order) -> A (cell-major)
-        if (threadIdx.x < 64) cnt64[threadIdx.x] = 0;
-        __syncthreads();
-        for (uint32_t base = 0; base < cnt; base += blockDim.x) {
-            const uint32_t i = base + threadIdx.x;
-            const uint32_t c = i < cnt ? (key[S[i]] & cmask) : 64u;
+        // stable counting sort by cell, S (index order) -> A (cell-major).
+        // Warp w owns the contiguous segment [w*seg, (w+1)*seg) of S.
+        const uint32_t seg = (cnt + kOrderWarps - 1) / kOrderWarps;
+        const uint32_t s0 = min(cnt, warp * seg), s1 = min(cnt, s0 + seg);
+        wcnt[warp][lane] = 0;
+        wcnt[warp][lane + 32] = 0;
+        __syncwarp();
+        for (uint32_t base = s0; base < s1; base += 32) {
+            const uint32_t i = base + lane;
+            const uint32_t c = i < s1 ? (uint32_t)CS[i] : 64u;
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
-            if (i < cnt && (peers & lanemask_lt()) == 0) atomicAdd(&cnt64[c], (uint32_t)__popc(peers));
+            if (i < s1 && (peers & lanemask_lt()) == 0) wcnt[warp][c] += __popc(peers);
+            __syncwarp();
         }
         __syncthreads();
-        if (threadIdx.x < 32) {
+        if (threadIdx.x < 64) {
+            uint32_t tot = 0;
+            for (int w2 = 0; w2 < kOrderWarps; ++w2) tot += wcnt[w2][threadIdx.x];
+            cnt64[threadIdx.x] = tot;
+        }
+        __syncthreads();
+        if (warp == 0) {
             const uint32_t a0 = cnt64[2 * lane], a1 = cnt64[2 * lane + 1];
             uint32_t inc = a0 + a1;
 #pragma unroll
@@ -343,48 +618,31 @@ k_tile_order(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const uin
                 const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
                 if ((int)lane >= d) inc += t;
             }
-            const uint32_t ex = inc - a0 - a1;
-            cs64[2 * lane] = ex;
-            cs64[2 * lane + 1] = ex + a0;
-            run64[2 * lane] = ex;
-            run64[2 * lane + 1] = ex + a0;
-            if (lane == 31) cs64[64] = inc;
+            cs64[2 * lane] = inc - a0 - a1;
+            cs64[2 * lane + 1] = inc - a1;
         }
         __syncthreads();
-        for (uint32_t base = 0; base < cnt; base += blockDim.x) {
-            const uint32_t i = base + threadIdx.x;
-            const uint32_t c = i < cnt ? (key[S[i]] & cmask) : 64u;
+        if (threadIdx.x < 64) {
+            // per-warp starting offset of each cell: cell start + counts of earlier warps
+            uint32_t r = cs64[threadIdx.x];
+            for (int w2 = 0; w2 < kOrderWarps; ++w2) {
+                const uint32_t t = wcnt[w2][threadIdx.x];
+                wcnt[w2][threadIdx.x] = r;
+                r += t;
+            }
+        }
+        __syncthreads();
+        for (uint32_t base = s0; base < s1; base += 32) {
+            const uint32_t i = base + lane;
+            const uint32_t c = i < s1 ? (uint32_t)CS[i] : 64u;
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
-            const uint32_t rank = __popc(peers & lanemask_lt());
-            wcnt[warp][lane] = 0;
-            wcnt[warp][lane + 32] = 0;
+            if (i < s1) A[wcnt[warp][c] + __popc(peers & lanemask_lt())] = S[i];
             __syncwarp();
-            if (i < cnt && rank == 0) wcnt[warp][c] = __popc(peers);
-            __syncthreads();
-            if (threadIdx.x < 64) {
-                uint32_t r = run64[threadIdx.x];
-                for (int w2 = 0; w2 < kOrderWarps; ++w2) {
-                    woff[w2][threadIdx.x] = r;
-                    r += wcnt[w2][threadIdx.x];
-                }
-                run64[threadIdx.x] = r;
-            }
-            __syncthreads();
-            if (i < cnt) A[woff[warp][c] + rank] = S[i];
-            __syncthreads();
+            if (i < s1 && (peers & lanemask_lt()) == 0) wcnt[warp][c] += __popc(peers);
+            __syncwarp();
         }
-        // rank-major write-out, one warp per group of 32 cells
-        if (warp < 2) {
-            const uint32_t c = warp * 32 + lane;
-            const uint32_t nc = cnt64[c], first = cs64[c];
-            uint32_t seg = warp == 0 ? 0u : cs64[32];
-            for (uint32_t r = 0;; ++r) {
-                const uint32_t m = __ballot_sync(0xFFFFFFFFu, nc > r);
-                if (m == 0) break;
-                if (nc > r) perm[beg + seg + __popc(m & lanemask_lt())] = A[first + r];
-                seg += __popc(m);
-            }
-        }
+        __syncthreads();
+        if (warp < 2) write_rank_major(warp, cnt64, cs64, A, perm + beg);
         __syncthreads();
     }
 }
@@ -430,16 +688,19 @@ mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const De
     const int grid_p = (int)std::max<int64_t>(1, std::min<int64_t>((n + threads - 1) / threads, dev.sms * 8));
     if (n > 0) k_keys<<<grid_p, threads, 0, st>>>(g, p, w.key, w.count, w.cellcount, w.status);
     const int64_t nblk = (nb + kScanBlock - 1) / kScanBlock;
-    k_scan_reduce<<<(unsigned)nblk, kScanThreads, 0, st>>>(g, w.count, nb, (Tri *)w.partial);
-    k_scan_top<<<1, kScanThreads, 0, st>>>((Tri *)w.partial, nblk, w.count, nb, w.status);
-    k_scan_final<<<(unsigned)nblk, kScanThreads, 0, st>>>(g, w.count, nb, (const Tri *)w.partial, w.start,
-                                                          w.cursor, w.active, w.slices, w.status);
+    k_scan_reduce<<<(unsigned)nblk, kScanThreads, 0, st>>>(w.count, nb, (Tot5 *)w.partial);
+    k_scan_top<<<1, kScanThreads, 0, st>>>((Tot5 *)w.partial, nblk, w.count, nb, w.status);
+    k_scan_final<<<(unsigned)nblk, kScanThreads, 0, st>>>(w.count, nb, (const Tot5 *)w.partial, w.start, w.cursor,
+                                                          w.active, w.slices, w.small_list, w.large_list);
     if (n > 0) {
         k_scatter<<<grid_p, threads, 0, st>>>(g, w.key, n, w.cursor, w.tmp);
-        const int smem = kOrderCap * (8 + 4 + 4 + 4) + 16;
-        cudaFuncSetAttribute(k_tile_order, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        k_tile_order<<<dev.sms * 2, kOrderThreads, smem, st>>>(g, w.key, w.tmp, w.start, w.count, w.active, nb, w.perm,
-                                                             w.gH, (unsigned long long *)w.gCW, w.status);
+        k_order_small<<<dev.sms * 4, 256, 0, st>>>(g, w.key, w.tmp, w.start, w.count, w.small_list, nb, w.perm,
+                                                   w.status);
+        const int smem = (2 * kOrderCap + kHeadCap + 4) * (int)sizeof(uint32_t) + 2 * kOrderCap;
+        cudaFuncSetAttribute(k_order_large, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        k_order_large<<<dev.sms * 2, kOrderThreads, smem, st>>>(g, w.key, w.tmp, w.start, w.count, w.large_list, nb,
+                                                               w.perm, w.gH, (unsigned long long *)w.gCW, w.gCA,
+                                                               w.gCS, w.status);
     }
     if (w.cellcount) k_nbr_bound<<<dev.sms * 4, 256, 0, st>>>(g, w.cellcount, w.status);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;

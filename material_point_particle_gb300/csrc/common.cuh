@@ -52,6 +52,7 @@ struct PartsF {
     float *v[3];
     float *C[9];
     const float *m;
+    uint32_t *id;
     int64_t n;
 };
 
@@ -112,6 +113,63 @@ __device__ __forceinline__ void tile_origin(const GridP &g, uint32_t tile, int o
     o[1] = (int)(r % (uint32_t)g.nt[1]) * g.T;
     o[2] = g.dim == 3 ? (int)(r / (uint32_t)g.nt[1]) * g.T : 0;
 }
+
+// Base cell and fraction of particle pid, and whether that base cell lies in
+// the tile at origin o (it does for every particle binned into the tile from
+// the same positions; the test keeps shared-memory indices in range if the
+// positions changed after binning).
+template <int DIM>
+__device__ __forceinline__ bool in_tile(const GridP &g, const PartsF &p, uint32_t pid, const int o[3], int b[3],
+                                        float f[3]) {
+    bool ok = true;
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) {
+        ok = ok && base_frac(p.x[l][pid], g.inv_dx, g.n[l], b[l], f[l]);
+        ok = ok && b[l] >= o[l] && b[l] < o[l] + g.T;
+    }
+    return ok;
+}
+
+// The same test on positions already loaded.
+template <int DIM>
+__device__ __forceinline__ bool in_tile_x(const GridP &g, const float *x, const int o[3], int b[3], float f[3]) {
+    bool ok = true;
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) {
+        ok = ok && base_frac(x[l], g.inv_dx, g.n[l], b[l], f[l]);
+        ok = ok && b[l] >= o[l] && b[l] < o[l] + g.T;
+    }
+    return ok;
+}
+
+// Asynchronous 4-byte global -> shared copies (cp.async), grouped per thread.
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Per-thread double buffer in shared memory for the NF fields of one
+// particle: field f of stage s of thread t at buf[(s * NF + f) * NT + t]
+// (consecutive threads, consecutive words).
+template <int NF, int NT>
+struct Prefetch {
+    float *buf;
+    __device__ float *at(int stage, int f) const { return buf + (stage * NF + f) * NT + threadIdx.x; }
+};
+
+// The particle record of P2G: x[dim], v[dim], C[dim*dim], m.
+template <int DIM>
+struct P2GFields {
+    static constexpr int NF = DIM + DIM + DIM * DIM + 1;
+    __device__ static const float *src(const PartsF &p, int f) {
+        return f < DIM ? p.x[f] : f < 2 * DIM ? p.v[f - DIM] : f < 2 * DIM + DIM * DIM ? p.C[f - 2 * DIM] : p.m;
+    }
+};
 
 __device__ __forceinline__ int64_t node_index(const GridP &g, int i, int j, int k) {
     return ((int64_t)k * g.n[1] + j) * g.n[0] + i;

@@ -109,17 +109,37 @@ __device__ __forceinline__ float sum3(const float w[3], const float t[3]) {
     return __fmaf_rn(w[2], t[2], __fmaf_rn(w[1], t[1], __fmul_rn(w[0], t[0])));
 }
 
-// One particle's gather from the tile's velocity halo in shared memory.
-template <int DIM, int T>
-__device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, uint32_t pid, const int o[3],
-                                           const float *sv, float dt, float c4) {
+// Whole-state copy of particle `src` of p to entry `dst` of q.
+template <int DIM>
+__device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, uint32_t src, uint32_t dst) {
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) {
+        q.x[l][dst] = p.x[l][src];
+        q.v[l][dst] = p.v[l][src];
+    }
+#pragma unroll
+    for (int j = 0; j < DIM * DIM; ++j) q.C[j][dst] = p.C[j][src];
+    const_cast<float *>(q.m)[dst] = p.m[src];
+    if (q.id && p.id) q.id[dst] = p.id[src];
+}
+
+// One particle's gather from the tile's velocity halo in shared memory.  The
+// new state of particle `pid` of `p` goes to entry `dst` of `q` (the same
+// arrays and index in place; the sorted output otherwise, m and id with it).
+// rec(f): the particle's prefetched fields x[dim], then (sorted output) m and
+// the id bits.
+template <int DIM, int T, bool SORTED, typename Rec>
+__device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
+                                           uint32_t dst, const Rec &rec, const int o[3], const float *sv, float dt,
+                                           float c4) {
     using Hl = Halo<DIM, T>;
     float x[DIM], f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
 #pragma unroll
-    for (int l = 0; l < DIM; ++l) {
-        x[l] = p.x[l][pid];
-        base_frac(x[l], g.inv_dx, g.n[l], b[l], f[l]);
+    for (int l = 0; l < DIM; ++l) x[l] = rec(l);
+    if (!in_tile_x<DIM>(g, x, o, b, f)) {
+        if constexpr (SORTED) copy_particle<DIM>(p, q, pid, dst);
+        return;
     }
     float w[3][3], we[3][3];
 #pragma unroll
@@ -172,25 +192,32 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, uint
     }
 #pragma unroll
     for (int k = 0; k < DIM; ++k) {
-        p.v[k][pid] = vn[k];
+        q.v[k][dst] = vn[k];
 #pragma unroll
-        for (int l = 0; l < DIM; ++l) p.C[k * DIM + l][pid] = __fmul_rn(Bm[k][l], c4);
+        for (int l = 0; l < DIM; ++l) q.C[k * DIM + l][dst] = __fmul_rn(Bm[k][l], c4);
     }
 #pragma unroll
-    for (int l = 0; l < DIM; ++l) p.x[l][pid] = __fmaf_rn(dt, vn[l], x[l]);
+    for (int l = 0; l < DIM; ++l) q.x[l][dst] = __fmaf_rn(dt, vn[l], x[l]);
+    if constexpr (SORTED) {
+        const_cast<float *>(q.m)[dst] = rec(DIM);
+        if (q.id) q.id[dst] = __float_as_uint(rec(DIM + 1));
+    }
 }
 
 // Work item as in P2G: one slice of a tile.  The CTA stages the tile's halo
 // of node velocities in shared memory (padded as the P2G accumulators), then
 // every thread gathers its particles from it.
-template <int DIM, int T>
-__global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, const float *__restrict__ vel,
+template <int DIM, int T, bool SORTED>
+__global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                      const uint32_t *__restrict__ perm,
                                                      const uint32_t *__restrict__ slices,
                                                      const uint32_t *__restrict__ start,
                                                      const uint32_t *__restrict__ status, float dt, float c4) {
     using Hl = Halo<DIM, T>;
+    constexpr int NF = DIM + (SORTED ? 2 : 0);
     __shared__ float sv[DIM * Hl::SIZE];
+    __shared__ float sbuf[2 * NF * kP2GThreads];
+    const Prefetch<NF, kP2GThreads> pf{sbuf};
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
@@ -208,9 +235,47 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, const fl
             for (int k = 0; k < DIM; ++k) sv[k * Hl::SIZE + idx] = in ? vel[k * g.nodes + node] : 0.f;
         }
         __syncthreads();
-        for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x) gather_one<DIM, T>(g, p, perm[beg + r], o, sv, dt, c4);
+        // each thread's particles r, r + 256, ...: the next one's fields are
+        // copied into shared memory (cp.async) while the current one gathers
+        constexpr int NQ = kSliceParticles / kP2GThreads;
+        uint32_t pids[NQ];
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+            const uint32_t r = threadIdx.x + qi * kP2GThreads;
+            pids[qi] = r < cnt ? perm[beg + r] : 0u;
+        }
+        auto issue = [&](int stage, uint32_t pid) {
+#pragma unroll
+            for (int f = 0; f < DIM; ++f) cp_async4(pf.at(stage, f), p.x[f] + pid);
+            if constexpr (SORTED) {
+                cp_async4(pf.at(stage, DIM), p.m + pid);
+                if (p.id) cp_async4(pf.at(stage, DIM + 1), p.id + pid);
+            }
+        };
+        if (threadIdx.x < cnt) issue(0, pids[0]);
+        cp_async_commit();
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+            const uint32_t r = threadIdx.x + qi * kP2GThreads;
+            if (qi + 1 < NQ && r + kP2GThreads < cnt) issue((qi + 1) & 1, pids[qi + 1]);
+            cp_async_commit();
+            cp_async_wait<1>();
+            if (r < cnt) {
+                const int stage = qi & 1;
+                auto rec = [&](int f) { return *pf.at(stage, f); };
+                gather_one<DIM, T, SORTED>(g, p, q, pids[qi], SORTED ? beg + r : pids[qi], rec, o, sv, dt, c4);
+            }
+        }
         __syncthreads();
     }
+}
+
+// Particles past the sorted in-domain part (outside the domain): copied.
+template <int DIM>
+__global__ void k_copy_rest(PartsF p, PartsF q, const uint32_t *__restrict__ perm, const uint32_t *__restrict__ status) {
+    for (int64_t j = (int64_t)status[MPM_ST_N_VALID] + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < p.n;
+         j += (int64_t)gridDim.x * blockDim.x)
+        copy_particle<DIM>(p, q, perm[j], (uint32_t)j);
 }
 
 mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
@@ -218,11 +283,29 @@ mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const W
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
     const int blocks = dev.sms * 4;
     if (g.dim == 3 && g.T == 4)
-        k_g2p<3, 4><<<blocks, kP2GThreads, 0, st>>>(g, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
+        k_g2p<3, 4, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
     else if (g.dim == 2 && g.T == 8)
-        k_g2p<2, 8><<<blocks, kP2GThreads, 0, st>>>(g, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
+        k_g2p<2, 8, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
     else
         return MPM_E_ARG;
+    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+}
+
+mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
+                             float dt, const DeviceInfo &dev, cudaStream_t st) {
+    const float c4 = 4.0f * g.inv_dx;
+    const int blocks = dev.sms * 4;
+    if (g.dim == 3 && g.T == 4) {
+        k_g2p<3, 4, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.slices, w.start, w.status, dt,
+                                                          c4);
+        k_copy_rest<3><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+    } else if (g.dim == 2 && g.T == 8) {
+        k_g2p<2, 8, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.slices, w.start, w.status, dt,
+                                                          c4);
+        k_copy_rest<2><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+    } else {
+        return MPM_E_ARG;
+    }
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }
 
@@ -248,6 +331,7 @@ __global__ void k_permute(int ncomp, PartsF in, PartsF out, const uint32_t *__re
             }
             if (s && d) d[j] = s[src];
         }
+        if (in.id && out.id) out.id[j] = in.id[src];
     }
 }
 

@@ -24,7 +24,10 @@ struct WsView {
     uint32_t *slices;     // [2 * max_slices]
     uint32_t *gH;         // [n + ntiles + 2] claim heads of buckets above the shared-memory capacity
     void *gCW;            // [2 n] uint64 claim keys of those buckets
-    uint32_t *partial;    // scan block totals, 3 words per 1024 buckets
+    uint8_t *gCA, *gCS;   // [n] cells of the entries of those buckets
+    uint32_t *small_list; // [ntiles + 1] buckets of at most 256 particles
+    uint32_t *large_list; // [ntiles + 1] larger buckets
+    uint32_t *partial;    // scan block totals, 5 words per 1024 buckets
     uint32_t *status;     // [MPM_STATUS_WORDS]
     uint32_t *cellcount;  // int32 mode only: [ntiles * T^dim], else null
 };
@@ -43,6 +46,8 @@ mpm_status launch_grid_update(const GridP &g, void *grid_acc, float *vel, const 
                               const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
                       const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
+                             float dt, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
                           const DeviceInfo &dev, cudaStream_t st);
 

@@ -31,21 +31,23 @@ __device__ __forceinline__ int32_t rint_f(float a) { return __float_as_int(__fad
 // One particle's fixed-point shares, added to the tile accumulator as they
 // are formed (the arithmetic the oracle states).  Returns false (and adds
 // nothing) when the particle is out of range.
-template <int DIM, int T>
-__device__ __forceinline__ bool scatter_fixed(const GridP &g, const PartsF &p, uint32_t pid, const int o[3],
-                                              int32_t *sacc) {
+// rec(f) reads field f of the particle (x[dim], v[dim], C[dim*dim], m).
+template <int DIM, int T, typename Rec>
+__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], int32_t *sacc) {
     using St = Stencil<DIM>;
     using Hl = Halo<DIM, T>;
     float f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
+    float xs[DIM];
 #pragma unroll
-    for (int l = 0; l < DIM; ++l) base_frac(p.x[l][pid], g.inv_dx, g.n[l], b[l], f[l]);
+    for (int l = 0; l < DIM; ++l) xs[l] = rec(l);
+    if (!in_tile_x<DIM>(g, xs, o, b, f)) return false;
     float v[DIM], C[DIM * DIM];
 #pragma unroll
-    for (int k = 0; k < DIM; ++k) v[k] = p.v[k][pid];
+    for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
 #pragma unroll
-    for (int j = 0; j < DIM * DIM; ++j) C[j] = p.C[j][pid];
-    const float Mt = __fmul_rn(p.m[pid], g.S);
+    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
+    const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
     // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) at most 2^22 - 4096
     const float h = __fmul_rn(1.5f, g.dx);
     const float aM = fabsf(Mt);
@@ -108,20 +110,21 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const PartsF &p, u
     return true;
 }
 
-template <int DIM, int T>
-__device__ __forceinline__ void scatter_float(const GridP &g, const PartsF &p, uint32_t pid, const int o[3],
-                                              float *sacc) {
+template <int DIM, int T, typename Rec>
+__device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, const int o[3], float *sacc) {
     using Hl = Halo<DIM, T>;
     float f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
+    float xs[DIM];
 #pragma unroll
-    for (int l = 0; l < DIM; ++l) base_frac(p.x[l][pid], g.inv_dx, g.n[l], b[l], f[l]);
+    for (int l = 0; l < DIM; ++l) xs[l] = rec(l);
+    if (!in_tile_x<DIM>(g, xs, o, b, f)) return;
     float v[DIM], C[DIM * DIM], w[3][3], dd[3][3];
 #pragma unroll
-    for (int k = 0; k < DIM; ++k) v[k] = p.v[k][pid];
+    for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
 #pragma unroll
-    for (int j = 0; j < DIM * DIM; ++j) C[j] = p.C[j][pid];
-    const float m = p.m[pid];
+    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
+    const float m = rec(2 * DIM + DIM * DIM);
 #pragma unroll
     for (int l = 0; l < DIM; ++l) {
         quad_weights(f[l], w[l]);
@@ -170,7 +173,10 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
                                                            uint32_t *__restrict__ status, AccT *__restrict__ acc) {
     using St = Stencil<DIM>;
     using Hl = Halo<DIM, T>;
+    using Fl = P2GFields<DIM>;
     __shared__ int32_t sacc[St::NC * Hl::SIZE];
+    __shared__ float sbuf[2 * Fl::NF * kP2GThreads];
+    const Prefetch<Fl::NF, kP2GThreads> pf{sbuf};
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
@@ -187,8 +193,32 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
         }
         __syncthreads();
         uint32_t bad = 0;
-        for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x)
-            if (!scatter_fixed<DIM, T>(g, p, perm[beg + r], o, sacc)) ++bad;
+        // each thread's particles r, r + 256, ...: the next one's record is
+        // copied into shared memory (cp.async) while the current one scatters
+        uint32_t pids[kSliceParticles / kP2GThreads];
+#pragma unroll
+        for (int q = 0; q < kSliceParticles / kP2GThreads; ++q) {
+            const uint32_t r = threadIdx.x + q * kP2GThreads;
+            pids[q] = r < cnt ? perm[beg + r] : 0u;
+        }
+        auto issue = [&](int stage, uint32_t pid) {
+#pragma unroll
+            for (int f = 0; f < Fl::NF; ++f) cp_async4(pf.at(stage, f), Fl::src(p, f) + pid);
+        };
+        if (threadIdx.x < cnt) issue(0, pids[0]);
+        cp_async_commit();
+#pragma unroll
+        for (int q = 0; q < kSliceParticles / kP2GThreads; ++q) {
+            const uint32_t r = threadIdx.x + q * kP2GThreads;
+            if (q + 1 < kSliceParticles / kP2GThreads && r + kP2GThreads < cnt) issue((q + 1) & 1, pids[q + 1]);
+            cp_async_commit();
+            cp_async_wait<1>();
+            if (r < cnt) {
+                const int stage = q & 1;
+                auto rec = [&](int f) { return *pf.at(stage, f); };
+                if (!scatter_fixed<DIM, T>(g, rec, o, sacc)) ++bad;
+            }
+        }
         if (bad) {
             atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
             set_flag(status, MPM_E_BOUND);
@@ -224,6 +254,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
                                                            float *__restrict__ acc) {
     using St = Stencil<DIM>;
     using Hl = Halo<DIM, T>;
+    using Fl = P2GFields<DIM>;
     __shared__ float sacc[St::NC * Hl::SIZE];
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
@@ -239,7 +270,11 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
             for (int c = 0; c < St::NC; ++c) sacc[c * Hl::SIZE + idx] = 0.f;
         }
         __syncthreads();
-        for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x) scatter_float<DIM, T>(g, p, perm[beg + r], o, sacc);
+        for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x) {
+            const uint32_t pid = perm[beg + r];
+            auto rec = [&](int f) { return Fl::src(p, f)[pid]; };
+            scatter_float<DIM, T>(g, rec, o, sacc);
+        }
         __syncthreads();
         for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
             int hx, hy, hz, idx;

@@ -87,6 +87,37 @@ class MPMSystem:
     def step(self, stream=None):
         L.mpm_step(self.desc, self.parts, self.bins, self.acc, self.vel, self.dt, self.dtg, stream)
 
+    # -- steps that keep the particles in bin order (ping-pong buffers) --------
+    def enable_sorted(self, with_ids: bool = True):
+        """Allocates the second particle buffer and (optionally) particle ids 0..n-1."""
+        n = self.x.shape[1]
+        if with_ids:
+            self.id = torch.arange(n, dtype=torch.int32, device=self.device)
+            self.id2 = torch.empty_like(self.id)
+        else:
+            self.id = self.id2 = None
+        self.x2, self.v2, self.C2, self.m2 = (torch.empty_like(t) for t in (self.x, self.v, self.C, self.m))
+        self.parts = L.particles(self.x, self.v, self.C, self.m, self.id)
+        self.parts2 = L.particles(self.x2, self.v2, self.C2, self.m2, self.id2)
+        return self
+
+    def swap(self):
+        self.x, self.x2 = self.x2, self.x
+        self.v, self.v2 = self.v2, self.v
+        self.C, self.C2 = self.C2, self.C
+        self.m, self.m2 = self.m2, self.m
+        self.id, self.id2 = self.id2, self.id
+        self.parts, self.parts2 = self.parts2, self.parts
+
+    def g2p_sorted(self, stream=None):
+        L.mpm_g2p_sorted(self.desc, self.vel, self.parts, self.parts2, self.bins, self.dt, stream)
+        self.swap()
+
+    def step_sorted(self, stream=None):
+        L.mpm_step_sorted(self.desc, self.parts, self.parts2, self.bins, self.acc, self.vel, self.dt, self.dtg,
+                          stream)
+        self.swap()
+
     def status(self) -> np.ndarray:
         L.mpm_read_status(self.bins, self.status_host)
         torch.cuda.synchronize(self.device)

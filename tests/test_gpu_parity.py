@@ -267,22 +267,60 @@ def test_workload_step_matches_oracle(name, kw):
         assert np.max(np.abs(x - ox)) <= 1e-6
 
 
-def test_step_host_equals_device_step():
+def test_g2p_sorted_moves_particles_into_bin_order():
+    cloud = with_outliers(W.small_cloud(3, 7001, 32, seed=502, scale_log2=19, lo=0.05, hi=0.95))
+    sys = make(cloud).enable_sorted()
+    sys.bin()
+    _, perm, _ = sys.bins_arrays()
+    valid = int(sys.status()[L.ST_N_VALID])
+    sys.p2g()
+    sys.grid_update()
+    sys.g2p_sorted()
+    x, v, C = sys.state()
+    m, ids = sys.m.cpu().numpy(), sys.id.cpu().numpy()
+    oacc, _, _ = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    ovel = O.grid_update_fixed(cloud["grid"], oacc)
+    ox, ov, oC, moved = O.g2p(cloud["grid"], ovel, cloud["x"], cloud["v"], cloud["C"])
+    assert moved == valid
+    p = perm.astype(np.int64)
+    assert np.array_equal(ids, p)
+    assert np.array_equal(x.view(np.uint32), ox[:, p].view(np.uint32))
+    assert np.array_equal(v.view(np.uint32), ov[:, p].view(np.uint32))
+    assert np.array_equal(C.view(np.uint32), oC[:, p].view(np.uint32))
+    assert np.array_equal(m, cloud["m"][p])
+
+
+def test_step_host_equals_device_sorted_step():
     cloud = W.small_cloud(3, 20000, 32, seed=501, scale_log2=19)
-    a = make(cloud)
-    a.step()
+    a = make(cloud).enable_sorted()
+    a.step_sorted()
     xa, va, Ca = a.state()
-    b = make(cloud)
-    hx = torch.from_numpy(cloud["x"].copy()).pin_memory()
-    hv = torch.from_numpy(cloud["v"].copy()).pin_memory()
-    hC = torch.from_numpy(cloud["C"].copy()).pin_memory()
-    hm = torch.from_numpy(cloud["m"].copy()).pin_memory()
+    ida = a.id.cpu().numpy()
+    b = make(cloud).enable_sorted()
+    pin = lambda arr: torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
+    hx, hv, hC, hm = pin(cloud["x"]), pin(cloud["v"]), pin(cloud["C"]), pin(cloud["m"])
+    hid = pin(np.arange(20000, dtype=np.int32))
     b.x.zero_()
-    b.v.zero_()
-    host = L.particles(hx, hv, hC, hm)
-    L.mpm_step_host(b.desc, host, b.parts, b.bins, b.acc, b.vel, b.dt, b.dtg)
+    host = L.particles(hx, hv, hC, hm, hid)
+    L.mpm_step_host(b.desc, host, b.parts, b.parts2, b.bins, b.acc, b.vel, b.dt, b.dtg)
     torch.cuda.synchronize()
+    assert np.array_equal(hid.numpy(), ida)
     assert np.array_equal(hx.numpy(), xa) and np.array_equal(hv.numpy(), va) and np.array_equal(hC.numpy(), Ca)
+
+
+def test_sorted_steps_track_the_in_place_steps():
+    """Three sorted steps give, particle by particle (through the ids), the
+    same state as three in-place steps."""
+    cloud = W.small_cloud(3, 30000, 48, seed=503, scale_log2=19, lo=0.2, hi=0.8)
+    a = make(cloud)
+    b = make(cloud).enable_sorted()
+    for _ in range(3):
+        a.step()
+        b.step_sorted()
+    xa, va, Ca = a.state()
+    xb, vb, Cb = b.state()
+    ids = b.id.cpu().numpy().astype(np.int64)
+    assert np.array_equal(xb, xa[:, ids]) and np.array_equal(vb, va[:, ids]) and np.array_equal(Cb, Ca[:, ids])
 
 
 def test_permute_reorders_by_perm():
