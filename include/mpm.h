@@ -108,7 +108,7 @@ typedef struct mpm_bins {
     int64_t ntiles;          /* tiles of tile^dim base cells */
     int64_t max_slices;
     uint32_t *key;           /* [n] tile-major base-cell key; 0xFFFFFFFF outside the domain */
-    uint32_t *perm;          /* [n] particle indices in (key, index) order; the
+    uint32_t *perm;          /* [n] particle indices in (tile, index) order; the
                                 in-domain ones first, then the others in index order */
     uint32_t *tile_count;    /* [ntiles] particles per tile */
     uint32_t *tile_start;    /* [ntiles + 1] exclusive prefix of tile_count */
@@ -135,13 +135,14 @@ size_t mpm_grid_vel_bytes(const mpm_grid_desc *desc);
 enum { MPM_BIN_DEFAULT = 0 };
 
 /*
- * mpm_bin -- cell keys and a stable counting sort of the particles.
+ * mpm_bin -- cell keys and a stable counting sort of the particles into tiles.
  * ("Particle Worlds, part 3", Step 3: histogram, exclusive prefix sum, scatter;
- *  implementation guide section 2.1: bin into tiles, sort an index buffer,
- *  particles never move; rule 2: index stability.)
+ *  implementation guide section 2.1: bin into tiles, sort an index buffer.)
  * key = tile-major id of the particle's stencil base cell b = floor(x*inv_dx - 1/2);
- * perm = stable order by key (ties by particle index), so the order is a
- * deterministic function of the keys.  Also builds the active-tile list and
+ * the tile is key >> log2(tile^dim).  perm = the in-domain particles in
+ * ascending tile order, each tile in particle-index order (the stable counting
+ * sort with the tile as bucket), then the out-of-domain particles in index
+ * order, so the order is a deterministic function of the keys.  Also builds the active-tile list and
  * the P2G work list, resets the status words, counts out-of-domain particles,
  * and in MPM_ACC_I32 mode checks the accumulator bound before any scatter:
  * every node must be covered by at most 511 particle stencils (511 shares of

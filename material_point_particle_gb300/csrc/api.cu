@@ -72,8 +72,7 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
 }
 
 struct Layout {
-    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, gCA, gCS, small_list, large_list, partial,
-        status,
+    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, small_list, large_list, partial, status,
         cellcount, scratch, total;
     int64_t max_slices;
 };
@@ -104,8 +103,6 @@ Layout layout_of(const GridP &g, int64_t n) {
     L.slices = take(2 * L.max_slices * sizeof(uint32_t));
     L.gH = take((n + g.ntiles + 2) * sizeof(uint32_t));
     L.gCW = take(2 * n * sizeof(uint64_t));
-    L.gCA = take(n);
-    L.gCS = take(n);
     L.small_list = take(nb * sizeof(uint32_t));
     L.large_list = take(nb * sizeof(uint32_t));
     L.partial = take(5 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
@@ -132,8 +129,6 @@ WsView view_of(const GridP &g, const mpm_bins &b) {
     w.slices = reinterpret_cast<uint32_t *>(base + L.slices);
     w.gH = reinterpret_cast<uint32_t *>(base + L.gH);
     w.gCW = base + L.gCW;
-    w.gCA = reinterpret_cast<uint8_t *>(base + L.gCA);
-    w.gCS = reinterpret_cast<uint8_t *>(base + L.gCS);
     w.small_list = reinterpret_cast<uint32_t *>(base + L.small_list);
     w.large_list = reinterpret_cast<uint32_t *>(base + L.large_list);
     w.partial = reinterpret_cast<uint32_t *>(base + L.partial);

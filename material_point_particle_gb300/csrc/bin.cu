@@ -7,10 +7,10 @@
 // unspecified; the implementation guide (section 2.1, caveat (b), and rule 3)
 // asks for every such race to be neutralised by a sort on a stable key.
 // Here the buckets are tiles of T^dim base cells (section 2.1: bin into
-// tiles, sort an index buffer, particles never move), the atomic scatter
-// fills each tile's range, and one CTA per tile then sorts the range by
-// (cell, particle index) in shared memory, which makes the permutation the
-// stable sort of the keys -- a deterministic function of the keys.
+// tiles, sort an index buffer), the atomic scatter fills each tile's range,
+// and a warp or block per tile puts the range back in particle-index order,
+// which makes the permutation the stable counting sort by tile -- a
+// deterministic function of the keys.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
 //   k_keys          key per particle, warp-aggregated tile histogram,
@@ -19,10 +19,9 @@
 //                   exclusive scans of (count, P2G slices, active flag) over
 //                   the buckets; active-tile list, P2G work list, cursors
 //   k_scatter       warp-aggregated atomic scatter of indices into buckets
-//   k_order_small   per-tile order for buckets up to 256 entries (one warp)
-//   k_order_large   per-tile order for larger buckets (one block): claims put
-//                   back into index order, a stable counting sort by cell,
-//                   the rank-major write-out
+//   k_order_small   index order inside buckets of up to 256 entries (one warp)
+//   k_order_large   index order inside larger buckets (one block): the
+//                   atomic scatter's claims put back in order
 //   k_nbr_bound     int32 mode: most stencils covering one node (the
 //                   accumulator bound, checked before any scatter)
 #include "common.cuh"
@@ -212,26 +211,25 @@ __global__ void k_scatter(GridP g, const uint32_t *__restrict__ key, int64_t n, 
 }
 
 // --------------------------------------------------------------------------
-// The order inside each tile.  The atomic scatter leaves each bucket as a set
-// of "claims": one per warp-round and bucket, holding that warp's lanes of the
+// The order inside each tile: particle-index order (the stable counting sort
+// with the tile as bucket).  The atomic scatter leaves each bucket as a set of
+// "claims": one per warp-round and bucket, holding that warp's lanes of the
 // bucket in lane (= index) order, all sharing w = idx >> 5 (a warp covers 32
-// consecutive indices per round).  The stable order wanted is cell-major with
-// each cell in index order; the output lists, for each group of 32 cells,
-// rank 0 of its cells, then rank 1, and so on.
+// consecutive indices per round).  So ordering the claims by w puts the
+// bucket in index order.
 //
-// Small buckets (at most 256 entries): one warp sorts (cell, index) keys in
+// Small buckets (at most 256 entries): one warp sorts the indices in
 // registers with a bitonic network.
-// Large buckets: one block.  Claims are put in index order by a table over a
-// window of 2048 values of w around the bucket's median entry (in steady
-// state almost every claim falls there); the few claims outside the window
-// are sorted and placed before or after it.  Then a stable counting sort by
-// cell and the rank-major write-out.  Buckets above kOrderCap entries keep
-// their working arrays in global scratch instead of shared memory.
+// Large buckets: one block.  Claims are placed by a table over a window of
+// 2048 values of w around the bucket's median entry (in steady state almost
+// every claim falls in it); the few claims outside are sorted and go before or
+// after it.  Buckets above kOrderCap entries keep their working arrays in
+// global scratch instead of shared memory.
 constexpr int kOrderThreads = 256;
 constexpr int kOrderWarps = kOrderThreads / 32;
 constexpr int kOrderCap = 8192;
 constexpr int kWindow = 2048;
-constexpr int kFarCap = 256;  // far claims kept in shared memory (and sorted by one warp)
+constexpr int kFarCap = 256;             // far claims kept in shared memory (and sorted by one warp)
 constexpr int kHeadCap = kOrderCap / 4;  // claim heads kept in shared memory
 
 template <int E>
@@ -267,101 +265,44 @@ __device__ __forceinline__ void warp_bitonic(unsigned long long (&v)[E]) {
     }
 }
 
-// Rank-major write-out of a cell-major run cm[0, cnt) with per-cell counts and
-// starts (64 cells), by one warp per group (warp index `grp`).
-__device__ __forceinline__ void write_rank_major(uint32_t grp, const uint32_t *cnt64, const uint32_t *cs64,
-                                                 const uint32_t *cm, uint32_t *out) {
-    const uint32_t lane = lane_id();
-    const uint32_t c = grp * 32 + lane;
-    const uint32_t nc = cnt64[c], first = cs64[c];
-    uint32_t seg = cs64[grp * 32];
-    for (uint32_t r = 0;; ++r) {
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, nc > r);
-        if (m == 0) break;
-        if (nc > r) out[seg + __popc(m & lanemask_lt())] = cm[first + r];
-        seg += __popc(m);
-    }
-}
-
 template <int E>
-__device__ void order_small(const GridP &g, const uint32_t *key, const uint32_t *tmp, uint32_t beg, uint32_t cnt,
-                            bool outside, uint32_t *perm, uint32_t *sbuf, uint32_t *scnt, uint32_t *sfirst) {
+__device__ __forceinline__ void order_small(const uint32_t *tmp, uint32_t beg, uint32_t cnt, uint32_t *perm) {
     const uint32_t lane = lane_id();
-    const uint32_t cmask = (1u << g.cpt_log2) - 1;
     unsigned long long v[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const uint32_t i = (uint32_t)e * 32u + lane;
-        if (i < cnt) {
-            const uint32_t idx = tmp[beg + i];
-            const uint32_t c = outside ? 0u : (key[idx] & cmask);
-            v[e] = ((unsigned long long)c << 32) | idx;
-        } else {
-            v[e] = ~0ull;
-        }
+        v[e] = i < cnt ? (unsigned long long)tmp[beg + i] : ~0ull;
     }
     warp_bitonic<E>(v);
-    if (outside) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const uint32_t i = (uint32_t)e * 32u + lane;
-            if (i < cnt) perm[beg + i] = (uint32_t)v[e];
-        }
-        return;
-    }
-    scnt[lane] = 0;
-    scnt[lane + 32] = 0;
-    __syncwarp();
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const uint32_t i = (uint32_t)e * 32u + lane;
-        if (i < cnt) {
-            sbuf[i] = (uint32_t)v[e];
-            atomicAdd(&scnt[(uint32_t)(v[e] >> 32)], 1u);
-        }
+        if (i < cnt) perm[beg + i] = (uint32_t)v[e];
     }
-    __syncwarp();
-    const uint32_t a0 = scnt[2 * lane], a1 = scnt[2 * lane + 1];
-    uint32_t inc = a0 + a1;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-        if ((int)lane >= d) inc += t;
-    }
-    sfirst[2 * lane] = inc - a0 - a1;
-    sfirst[2 * lane + 1] = inc - a1;
-    __syncwarp();
-    write_rank_major(0, scnt, sfirst, sbuf, perm + beg);
-    write_rank_major(1, scnt, sfirst, sbuf, perm + beg);
-    __syncwarp();
 }
 
-__global__ void __launch_bounds__(256) k_order_small(GridP g, const uint32_t *__restrict__ key,
-                                                     const uint32_t *__restrict__ tmp,
+__global__ void __launch_bounds__(256) k_order_small(const uint32_t *__restrict__ tmp,
                                                      const uint32_t *__restrict__ start,
                                                      const uint32_t *__restrict__ count,
-                                                     const uint32_t *__restrict__ list, int64_t nb,
-                                                     uint32_t *__restrict__ perm, const uint32_t *__restrict__ status) {
-    __shared__ uint32_t sbuf[8][kSmallBucket];
-    __shared__ uint32_t scnt[8][64];
-    __shared__ uint32_t sfirst[8][64];
+                                                     const uint32_t *__restrict__ list, uint32_t *__restrict__ perm,
+                                                     const uint32_t *__restrict__ status) {
     const uint32_t nitems = status[MPM_ST_N_SMALL_BUCKETS];
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-    const uint32_t nw = gridDim.x * 8;
-    for (uint32_t it = blockIdx.x * 8 + warp; it < nitems; it += nw) {
+    const uint32_t nw = gridDim.x * (blockDim.x >> 5);
+    for (uint32_t it = blockIdx.x * (blockDim.x >> 5) + warp; it < nitems; it += nw) {
         const uint32_t b = list[it];
         const uint32_t beg = start[b], cnt = count[b];
-        const bool outside = b == (uint32_t)(nb - 1);
         if (cnt == 1) {
             if (lane == 0) perm[beg] = tmp[beg];
         } else if (cnt <= 32) {
-            order_small<1>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+            order_small<1>(tmp, beg, cnt, perm);
         } else if (cnt <= 64) {
-            order_small<2>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+            order_small<2>(tmp, beg, cnt, perm);
         } else if (cnt <= 128) {
-            order_small<4>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+            order_small<4>(tmp, beg, cnt, perm);
         } else {
-            order_small<8>(g, key, tmp, beg, cnt, outside, perm, sbuf[warp], scnt[warp], sfirst[warp]);
+            order_small<8>(tmp, beg, cnt, perm);
         }
     }
 }
@@ -408,40 +349,27 @@ __device__ void block_bitonic(unsigned long long *s, uint32_t n_pow2) {
 }
 
 __global__ void __launch_bounds__(kOrderThreads)
-k_order_large(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const uint32_t *__restrict__ start,
-              const uint32_t *__restrict__ count, const uint32_t *__restrict__ list, int64_t nb, uint32_t *perm,
-              uint32_t *gH, unsigned long long *gF, uint8_t *gCA, uint8_t *gCS, uint32_t *__restrict__ status) {
+k_order_large(const uint32_t *__restrict__ tmp, const uint32_t *__restrict__ start,
+              const uint32_t *__restrict__ count, const uint32_t *__restrict__ list, uint32_t *perm, uint32_t *gH,
+              unsigned long long *gF, uint32_t *__restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint32_t *sA = reinterpret_cast<uint32_t *>(smem_raw);
-    uint32_t *sS = sA + kOrderCap;
-    uint32_t *sH = sS + kOrderCap;                                  // kHeadCap + 1 entries
-    uint8_t *sCA = reinterpret_cast<uint8_t *>(sH + kHeadCap + 4);  // cell of each entry of A
-    uint8_t *sCS = sCA + kOrderCap;                                 // cell of each entry of S
+    uint32_t *sH = sA + kOrderCap;  // kHeadCap + 1 entries
     __shared__ uint32_t table[kWindow];
     __shared__ unsigned long long sF[kFarCap];
-    __shared__ uint32_t cnt64[64], cs64[64];
-    __shared__ uint32_t wcnt[kOrderWarps][64];
     __shared__ uint32_t scan_sh[kOrderWarps];
     __shared__ uint32_t nfar_sh, nlow_sh;
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     const uint32_t nitems = status[MPM_ST_N_LARGE_BUCKETS];
-    const uint32_t cmask = (1u << g.cpt_log2) - 1;
     for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
         const uint32_t b = list[it];
         const uint32_t beg = start[b], cnt = count[b];
-        const bool outside = b == (uint32_t)(nb - 1);
         const bool small = cnt <= (uint32_t)kOrderCap;
         if (!small && threadIdx.x == 0) atomicAdd(&status[MPM_ST_N_BIG_TILES], 1u);
-        uint32_t *A = small ? sA : tmp + beg;
-        uint32_t *S = small ? sS : perm + beg;
-        uint8_t *CA = small ? sCA : gCA + beg;
-        uint8_t *CS = small ? sCS : gCS + beg;
-        // load the entries and gather each one's cell once (independent loads)
-        for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) {
-            const uint32_t idx = tmp[beg + i];
-            if (small) A[i] = idx;
-            CA[i] = outside ? (uint8_t)0 : (uint8_t)(key[idx] & cmask);
-        }
+        const uint32_t *A = small ? sA : tmp + beg;
+        uint32_t *S = perm + beg;
+        if (small)
+            for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) sA[i] = tmp[beg + i];
         if (threadIdx.x == 0) nfar_sh = 0;
         for (uint32_t d = threadIdx.x; d < (uint32_t)kWindow; d += blockDim.x) table[d] = 0;
         __syncthreads();
@@ -482,15 +410,16 @@ k_order_large(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const ui
         __syncthreads();
         if (threadIdx.x == 0) nfar_sh = 0;
         __syncthreads();
-        for (uint32_t c = threadIdx.x; c < nclaims; c += blockDim.x) {
-            const uint32_t w = A[H[c]] >> 5;
-            const long long d = (long long)w - w_lo;
-            if (!(d >= 0 && d < kWindow)) F[atomicAdd(&nfar_sh, 1u)] = ((unsigned long long)w << 32) | c;
+        if (nfar > 0) {
+            for (uint32_t c = threadIdx.x; c < nclaims; c += blockDim.x) {
+                const uint32_t w = A[H[c]] >> 5;
+                const long long d = (long long)w - w_lo;
+                if (!(d >= 0 && d < kWindow)) F[atomicAdd(&nfar_sh, 1u)] = ((unsigned long long)w << 32) | c;
+            }
+            __syncthreads();
         }
-        __syncthreads();
         if (nfar > 1 && nfar <= (uint32_t)kFarCap) {
-            // one warp sorts in registers
-            if (warp == 0) {
+            if (warp == 0) {  // one warp sorts in registers
                 unsigned long long v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -514,24 +443,26 @@ k_order_large(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const ui
         }
         // far claims below the window come first: count them (binary search in
         // the sorted keys) and add up their lengths
-        if (threadIdx.x == 0) {
-            uint32_t lo2 = 0, hi2 = nfar;
-            while (lo2 < hi2) {
-                const uint32_t mid = (lo2 + hi2) / 2;
-                if ((long long)(F[mid] >> 32) < w_lo) lo2 = mid + 1;
-                else hi2 = mid;
+        uint32_t nlow = 0, lowlen = 0;
+        if (nfar > 0) {
+            if (threadIdx.x == 0) {
+                uint32_t lo2 = 0, hi2 = nfar;
+                while (lo2 < hi2) {
+                    const uint32_t mid = (lo2 + hi2) / 2;
+                    if ((long long)(F[mid] >> 32) < w_lo) lo2 = mid + 1;
+                    else hi2 = mid;
+                }
+                nlow_sh = lo2;
             }
-            nlow_sh = lo2;
+            __syncthreads();
+            nlow = nlow_sh;
+            uint32_t mylow = 0;
+            for (uint32_t f = threadIdx.x; f < nlow; f += blockDim.x) {
+                const uint32_t c = (uint32_t)(F[f] & 0xFFFFFFFFu);
+                mylow += H[c + 1] - H[c];
+            }
+            block_excl_scan(mylow, lowlen, scan_sh);
         }
-        __syncthreads();
-        const uint32_t nlow = nlow_sh;
-        uint32_t mylow = 0;
-        for (uint32_t f = threadIdx.x; f < nlow; f += blockDim.x) {
-            const uint32_t c = (uint32_t)(F[f] & 0xFFFFFFFFu);
-            mylow += H[c + 1] - H[c];
-        }
-        uint32_t lowlen;
-        block_excl_scan(mylow, lowlen, scan_sh);
         // table prefix (blocked, 8 slots per thread) -> destinations of the window claims
         constexpr int kPer = kWindow / kOrderThreads;
         uint32_t tv[kPer], tsum = 0;
@@ -549,17 +480,11 @@ k_order_large(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const ui
             toff += t;
         }
         __syncthreads();
-        // copy window claims
-        for (uint32_t c = threadIdx.x; c < nclaims; c += blockDim.x) {
+        // copy window claims: one warp per claim, lanes copy its entries
+        for (uint32_t c = warp; c < nclaims; c += kOrderWarps) {
             const uint32_t src = H[c], len = H[c + 1] - H[c];
             const long long d = (long long)(A[src] >> 5) - w_lo;
-            if (d >= 0 && d < kWindow) {
-                const uint32_t dst = table[d];
-                for (uint32_t e = 0; e < len; ++e) {
-                    S[dst + e] = A[src + e];
-                    CS[dst + e] = CA[src + e];
-                }
-            }
+            if (d >= 0 && d < kWindow && lane < len) S[table[d] + lane] = A[src + lane];
         }
         // copy far claims in sorted order (block-wide prefix of their lengths)
         uint32_t run = 0;
@@ -575,74 +500,10 @@ k_order_large(GridP g, const uint32_t *__restrict__ key, uint32_t *tmp, const ui
             if (f < nfar) {
                 const uint32_t dst = f < nlow ? ex : ex + wintotal;
                 const uint32_t src = H[c];
-                for (uint32_t e = 0; e < len; ++e) {
-                    S[dst + e] = A[src + e];
-                    CS[dst + e] = CA[src + e];
-                }
+                for (uint32_t e = 0; e < len; ++e) S[dst + e] = A[src + e];
             }
             run += tot;
         }
-        __syncthreads();
-        if (outside) {
-            if (small)
-                for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) perm[beg + i] = S[i];
-            __syncthreads();
-            continue;
-        }
-        // stable counting sort by cell, S (index order) -> A (cell-major).
-        // Warp w owns the contiguous segment [w*seg, (w+1)*seg) of S.
-        const uint32_t seg = (cnt + kOrderWarps - 1) / kOrderWarps;
-        const uint32_t s0 = min(cnt, warp * seg), s1 = min(cnt, s0 + seg);
-        wcnt[warp][lane] = 0;
-        wcnt[warp][lane + 32] = 0;
-        __syncwarp();
-        for (uint32_t base = s0; base < s1; base += 32) {
-            const uint32_t i = base + lane;
-            const uint32_t c = i < s1 ? (uint32_t)CS[i] : 64u;
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
-            if (i < s1 && (peers & lanemask_lt()) == 0) wcnt[warp][c] += __popc(peers);
-            __syncwarp();
-        }
-        __syncthreads();
-        if (threadIdx.x < 64) {
-            uint32_t tot = 0;
-            for (int w2 = 0; w2 < kOrderWarps; ++w2) tot += wcnt[w2][threadIdx.x];
-            cnt64[threadIdx.x] = tot;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            const uint32_t a0 = cnt64[2 * lane], a1 = cnt64[2 * lane + 1];
-            uint32_t inc = a0 + a1;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-                if ((int)lane >= d) inc += t;
-            }
-            cs64[2 * lane] = inc - a0 - a1;
-            cs64[2 * lane + 1] = inc - a1;
-        }
-        __syncthreads();
-        if (threadIdx.x < 64) {
-            // per-warp starting offset of each cell: cell start + counts of earlier warps
-            uint32_t r = cs64[threadIdx.x];
-            for (int w2 = 0; w2 < kOrderWarps; ++w2) {
-                const uint32_t t = wcnt[w2][threadIdx.x];
-                wcnt[w2][threadIdx.x] = r;
-                r += t;
-            }
-        }
-        __syncthreads();
-        for (uint32_t base = s0; base < s1; base += 32) {
-            const uint32_t i = base + lane;
-            const uint32_t c = i < s1 ? (uint32_t)CS[i] : 64u;
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
-            if (i < s1) A[wcnt[warp][c] + __popc(peers & lanemask_lt())] = S[i];
-            __syncwarp();
-            if (i < s1 && (peers & lanemask_lt()) == 0) wcnt[warp][c] += __popc(peers);
-            __syncwarp();
-        }
-        __syncthreads();
-        if (warp < 2) write_rank_major(warp, cnt64, cs64, A, perm + beg);
         __syncthreads();
     }
 }
@@ -694,13 +555,11 @@ mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const De
                                                           w.active, w.slices, w.small_list, w.large_list);
     if (n > 0) {
         k_scatter<<<grid_p, threads, 0, st>>>(g, w.key, n, w.cursor, w.tmp);
-        k_order_small<<<dev.sms * 4, 256, 0, st>>>(g, w.key, w.tmp, w.start, w.count, w.small_list, nb, w.perm,
-                                                   w.status);
-        const int smem = (2 * kOrderCap + kHeadCap + 4) * (int)sizeof(uint32_t) + 2 * kOrderCap;
+        k_order_small<<<dev.sms * 4, 256, 0, st>>>(w.tmp, w.start, w.count, w.small_list, w.perm, w.status);
+        const int smem = (kOrderCap + kHeadCap + 4) * (int)sizeof(uint32_t);
         cudaFuncSetAttribute(k_order_large, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        k_order_large<<<dev.sms * 2, kOrderThreads, smem, st>>>(g, w.key, w.tmp, w.start, w.count, w.large_list, nb,
-                                                               w.perm, w.gH, (unsigned long long *)w.gCW, w.gCA,
-                                                               w.gCS, w.status);
+        k_order_large<<<dev.sms * 4, kOrderThreads, smem, st>>>(w.tmp, w.start, w.count, w.large_list, w.perm, w.gH,
+                                                               (unsigned long long *)w.gCW, w.status);
     }
     if (w.cellcount) k_nbr_bound<<<dev.sms * 4, 256, 0, st>>>(g, w.cellcount, w.status);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;

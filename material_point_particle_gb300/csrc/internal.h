@@ -24,7 +24,6 @@ struct WsView {
     uint32_t *slices;     // [2 * max_slices]
     uint32_t *gH;         // [n + ntiles + 2] claim heads of buckets above the shared-memory capacity
     void *gCW;            // [2 n] uint64 claim keys of those buckets
-    uint8_t *gCA, *gCS;   // [n] cells of the entries of those buckets
     uint32_t *small_list; // [ntiles + 1] buckets of at most 256 particles
     uint32_t *large_list; // [ntiles + 1] larger buckets
     uint32_t *partial;    // scan block totals, 5 words per 1024 buckets

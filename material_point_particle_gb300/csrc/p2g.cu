@@ -161,8 +161,7 @@ __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, co
     }
 }
 
-// Work item: up to kSliceParticles consecutive sorted particles of one tile
-// (rank-major inside the tile, so a warp's 32 lanes sit in distinct cells).
+// Work item: up to kSliceParticles consecutive binned particles of one tile.
 // The CTA zeroes the tile's halo accumulators, every thread scatters its
 // particles with shared atomics, and the CTA adds each nonzero node to the
 // grid once (neighbouring tiles overlap on the halo, so the flush adds).

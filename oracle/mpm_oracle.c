@@ -154,48 +154,15 @@ static int cmp_u64(const void *a, const void *b)
     return (x > y) - (x < y);
 }
 
-/* The order inside a tile.  The pages leave it open (page 2's atomic scatter
- * "doesn't put the particles in any particular order within a cell"; the
- * implementation guide, section 2.1, only asks that it be neutralised by a
- * stable key).  Here it is fixed as follows.  A tile's T^dim cells, in
- * tile-local order, form groups of 32 consecutive cells.  Inside each cell
- * the particles are ranked by particle index (the stable counting sort).
- * Each group lists all particles of rank 0 (its cells in ascending order),
- * then all of rank 1, and so on.  So consecutive particles are in different
- * cells.                                                                    */
-static void rank_major_tile(const uint32_t *cellmajor, const uint32_t *cells, int64_t count,
-                            uint32_t cells_per_tile, uint32_t *out)
-{
-    uint32_t cnt[4096], first[4096];
-    memset(cnt, 0, sizeof(uint32_t) * cells_per_tile);
-    for (int64_t j = 0; j < count; ++j)
-        cnt[cells[j]] += 1;
-    uint32_t run = 0;
-    for (uint32_t c = 0; c < cells_per_tile; ++c) {
-        first[c] = run;
-        run += cnt[c];
-    }
-    int64_t pos = 0;
-    for (uint32_t g = 0; g < cells_per_tile; g += 32) {
-        uint32_t end = g + 32 < cells_per_tile ? g + 32 : cells_per_tile;
-        for (uint32_t r = 0;; ++r) {
-            int any = 0;
-            for (uint32_t c = g; c < end; ++c)
-                if (cnt[c] > r) {
-                    out[pos++] = cellmajor[first[c] + r];
-                    any = 1;
-                }
-            if (!any)
-                break;
-        }
-    }
-}
-
 /* key[i] for every particle (ORC_KEY_INVALID outside the domain); perm = the
- * in-domain particles tile by tile in ascending tile order, each tile in the
- * rank-major order above, followed by the out-of-domain ones in index order;
- * tile_count[t] = particles whose base cell lies in tile t.  Returns the
- * number of in-domain particles.                                            */
+ * in-domain particles ordered by (tile, index) -- the stable counting sort
+ * with the tile as bucket -- followed by the out-of-domain ones in index
+ * order; tile_count[t] = particles whose base cell lies in tile t.  Returns
+ * the number of in-domain particles.  (The pages leave the order inside a
+ * bucket open: page 2's atomic scatter "doesn't put the particles in any
+ * particular order within a cell"; the implementation guide, section 2.1,
+ * asks that such a race be neutralised by sorting on a stable key.  Here the
+ * key is the tile and ties keep particle-index order.)                      */
 int64_t orc_bin(const orc_desc *d, int64_t np, const float *const *x,
                 uint32_t *key, uint32_t *perm, uint32_t *tile_count)
 {
@@ -212,30 +179,15 @@ int64_t orc_bin(const orc_desc *d, int64_t np, const float *const *x,
         if (base_frac(d, x, p, b, f)) {
             key[p] = key_of(d, b);
             tile_count[key[p] / cells_per_tile] += 1;
-            pairs[valid++] = ((uint64_t)key[p] << 32) | (uint64_t)p;
+            pairs[valid++] = ((uint64_t)(key[p] / cells_per_tile) << 32) | (uint64_t)p;
         } else {
             key[p] = ORC_KEY_INVALID;
         }
     }
-    /* stable counting sort by key: (key, index) order, cell-major */
+    /* stable counting sort by tile: (tile, index) order */
     qsort(pairs, (size_t)valid, sizeof(uint64_t), cmp_u64);
-    uint32_t *cm = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(valid > 0 ? valid : 1));
-    uint32_t *cl = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(valid > 0 ? valid : 1));
-    for (int64_t j = 0; j < valid; ++j) {
-        cm[j] = (uint32_t)(pairs[j] & 0xFFFFFFFFu);
-        cl[j] = (uint32_t)(pairs[j] >> 32) % cells_per_tile;
-    }
-    /* then each tile's run rearranged rank-major */
-    for (int64_t j = 0; j < valid;) {
-        uint32_t t = (uint32_t)(pairs[j] >> 32) / cells_per_tile;
-        int64_t e = j;
-        while (e < valid && (uint32_t)(pairs[e] >> 32) / cells_per_tile == t)
-            ++e;
-        rank_major_tile(cm + j, cl + j, e - j, cells_per_tile, perm + j);
-        j = e;
-    }
-    free(cm);
-    free(cl);
+    for (int64_t j = 0; j < valid; ++j)
+        perm[j] = (uint32_t)(pairs[j] & 0xFFFFFFFFu);
     for (int64_t p = 0; p < np; ++p)
         if (key[p] == ORC_KEY_INVALID)
             perm[valid + invalid++] = (uint32_t)p;

@@ -83,8 +83,8 @@ def test_weights_closed_form_and_moments():
 
 
 # --------------------------------------------------------------------------
-# binning: keys name the stencil base cell; perm is the stable sort of keys
-# ("Particle Worlds, part 3", Step 3: counting sort)
+# binning: keys name the stencil base cell; perm is the stable counting sort
+# by tile ("Particle Worlds, part 3", Step 3: counting sort)
 
 @pytest.mark.parametrize("dim,n,tile", [(2, 40, 8), (3, 24, 4), (3, 21, 4)])
 def test_bin_is_stable_sort_of_base_cells(dim, n, tile):
@@ -108,17 +108,11 @@ def test_bin_is_stable_sort_of_base_cells(dim, n, tile):
     fr = xi[:, inside] - b
     assert np.all((fr >= 0.5) & (fr < 1.5))
     assert np.all((b >= 0) & (b <= np.array(grid["n"][:dim])[:, None] - 3))
-    # perm: numpy's stable argsort over the in-domain keys gives each cell's
-    # particles in index order (their rank); inside a tile, each group of 32
-    # cells lists rank 0 of its cells, then rank 1, ...; out-of-domain last
+    # perm: numpy's stable argsort of the tile ids of the in-domain particles
+    # (ties in index order), then the out-of-domain ones in index order
     idx = np.nonzero(inside)[0]
-    cellmajor = idx[np.argsort(key[idx], kind="stable")]
-    k_sorted = key[cellmajor].astype(np.int64)
-    first = np.searchsorted(k_sorted, k_sorted, side="left")
-    rank = np.arange(k_sorted.size) - first
-    tile_of, cell_of = k_sorted // (T ** dim), k_sorted % (T ** dim)
-    order = np.lexsort((cell_of, rank, cell_of // 32, tile_of))
-    expect = np.concatenate([cellmajor[order], np.nonzero(~inside)[0]])
+    tile_of = key[idx].astype(np.int64) // (T ** dim)
+    expect = np.concatenate([idx[np.argsort(tile_of, kind="stable")], np.nonzero(~inside)[0]])
     assert np.array_equal(perm.astype(np.int64), expect)
     assert np.array_equal(cnt.astype(np.int64),
                           np.bincount(key[idx] // (T ** dim), minlength=cnt.size))
