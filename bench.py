@@ -31,7 +31,7 @@ METRIC = "P2G+G2P particles/sec (3D 256^3, 16M clustered); % of HBM roofline"
 UNIT = "particles/s"
 WORKLOAD = "blobs3d: 3D quadratic B-spline MPM step, 256^3 nodes, 16,777,216 particles in 64 Gaussian blobs " \
            "(sigma 0.02), int64 fixed point"
-LAUNCHES_PER_STEP = 11  # bin: keys, 3 scans, scatter, small/large tile order; p2g; grid update; g2p + copy
+LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2g; grid update; g2p + copy
 
 
 def dist_env():

@@ -72,7 +72,8 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
 }
 
 struct Layout {
-    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, small_list, large_list, partial, status,
+    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, small_list, large_list, fallback, partial,
+        status,
         cellcount, scratch, total;
     int64_t max_slices;
 };
@@ -105,6 +106,7 @@ Layout layout_of(const GridP &g, int64_t n) {
     L.gCW = take(2 * n * sizeof(uint64_t));
     L.small_list = take(nb * sizeof(uint32_t));
     L.large_list = take(nb * sizeof(uint32_t));
+    L.fallback = take(nb * sizeof(uint32_t));
     L.partial = take(5 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
     L.status = take(MPM_STATUS_WORDS * sizeof(uint32_t));
     L.cellcount = g.acc_mode == MPM_ACC_I32 ? take((size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t)) : 0;
@@ -131,6 +133,7 @@ WsView view_of(const GridP &g, const mpm_bins &b) {
     w.gCW = base + L.gCW;
     w.small_list = reinterpret_cast<uint32_t *>(base + L.small_list);
     w.large_list = reinterpret_cast<uint32_t *>(base + L.large_list);
+    w.fallback = reinterpret_cast<uint32_t *>(base + L.fallback);
     w.partial = reinterpret_cast<uint32_t *>(base + L.partial);
     w.cellcount = g.acc_mode == MPM_ACC_I32 ? reinterpret_cast<uint32_t *>(base + L.cellcount) : nullptr;
     return w;

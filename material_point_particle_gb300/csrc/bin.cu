@@ -20,8 +20,9 @@
 //                   the buckets; active-tile list, P2G work list, cursors
 //   k_scatter       warp-aggregated atomic scatter of indices into buckets
 //   k_order_small   index order inside buckets of up to 256 entries (one warp)
-//   k_order_large   index order inside larger buckets (one block): the
-//                   atomic scatter's claims put back in order
+//   k_order_claims  index order inside larger buckets (one warp): the
+//                   atomic scatter's claims sorted and copied back in order
+//   k_order_large   the same for buckets with too many claims (one block)
 //   k_nbr_bound     int32 mode: most stencils covering one node (the
 //                   accumulator bound, checked before any scatter)
 #include "common.cuh"
@@ -307,6 +308,110 @@ __global__ void __launch_bounds__(256) k_order_small(const uint32_t *__restrict_
     }
 }
 
+// Larger buckets whose claims number at most kClaimCap: one warp per bucket.
+// Pass 1 records each claim head as a key (w << 37 | position << 6 | length-1)
+// in the warp's shared slot, the warp sorts the keys in registers, scans the
+// lengths in sorted order and copies each claim from tmp to its place in perm
+// (one lane per entry).  Buckets with more claims (a cold particle order) or
+// above 2^26 entries go to `fallback` for the block kernel.
+constexpr int kClaimCap = 512;
+constexpr int kClaimWarps = 8;
+
+__global__ void __launch_bounds__(kClaimWarps * 32) k_order_claims(const uint32_t *__restrict__ tmp,
+                                                                   const uint32_t *__restrict__ start,
+                                                                   const uint32_t *__restrict__ count,
+                                                                   const uint32_t *__restrict__ list,
+                                                                   uint32_t *__restrict__ perm,
+                                                                   uint32_t *__restrict__ fallback,
+                                                                   uint32_t *__restrict__ status) {
+    __shared__ unsigned long long keys[kClaimWarps][kClaimCap];
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    unsigned long long *kw = keys[warp];
+    const uint32_t nitems = status[MPM_ST_N_LARGE_BUCKETS];
+    const uint32_t nw = gridDim.x * kClaimWarps;
+    for (uint32_t it = blockIdx.x * kClaimWarps + warp; it < nitems; it += nw) {
+        const uint32_t b = list[it];
+        const uint32_t beg = start[b], cnt = count[b];
+        // pass 1: claim heads (where idx >> 5 changes)
+        uint32_t nclaims = 0, wlast = 0xFFFFFFFFu;
+        for (uint32_t base = 0; base < cnt; base += 32) {
+            const uint32_t i = base + lane;
+            const uint32_t w = i < cnt ? (tmp[beg + i] >> 5) : 0xFFFFFFFFu;
+            uint32_t wprev = __shfl_up_sync(0xFFFFFFFFu, w, 1);
+            if (lane == 0) wprev = wlast;
+            const bool head = i < cnt && w != wprev;
+            const uint32_t m = __ballot_sync(0xFFFFFFFFu, head);
+            const uint32_t k = nclaims + __popc(m & lanemask_lt());
+            if (head && k < (uint32_t)kClaimCap) kw[k] = ((unsigned long long)w << 37) | ((unsigned long long)i << 6);
+            nclaims += __popc(m);
+            wlast = __shfl_sync(0xFFFFFFFFu, w, 31);
+        }
+        if (nclaims > (uint32_t)kClaimCap || cnt >= (1u << 26)) {
+            if (lane == 0) fallback[atomicAdd(&status[MPM_ST_N_FALLBACK], 1u)] = b;
+            continue;
+        }
+        __syncwarp();
+        // lengths (from the next head in bucket order), then sort by w
+        unsigned long long v[kClaimCap / 32];
+#pragma unroll
+        for (int e = 0; e < kClaimCap / 32; ++e) {
+            const uint32_t k = (uint32_t)e * 32u + lane;
+            if (k < nclaims) {
+                const unsigned long long key = kw[k];
+                const uint32_t pos = (uint32_t)(key >> 6) & ((1u << 26) - 1);
+                const uint32_t next = k + 1 < nclaims ? (uint32_t)(kw[k + 1] >> 6) & ((1u << 26) - 1) : cnt;
+                v[e] = key | (unsigned long long)(next - pos - 1);
+            } else {
+                v[e] = ~0ull;
+            }
+        }
+        __syncwarp();
+        warp_bitonic<kClaimCap / 32>(v);
+        // destinations: running sum of lengths in sorted order; claims back to shared memory
+        uint32_t run = 0;
+#pragma unroll
+        for (int e = 0; e < kClaimCap / 32; ++e) {
+            const uint32_t k = (uint32_t)e * 32u + lane;
+            const uint32_t len = k < nclaims ? (uint32_t)(v[e] & 63u) + 1u : 0u;
+            uint32_t inc = len;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+                if ((int)lane >= d) inc += t;
+            }
+            if (k < nclaims) {
+                const uint32_t pos = (uint32_t)(v[e] >> 6) & ((1u << 26) - 1);
+                kw[k] = ((unsigned long long)(run + inc - len) << 32) | ((unsigned long long)pos << 6) | (len - 1);
+            }
+            run += __shfl_sync(0xFFFFFFFFu, inc, 31);
+        }
+        __syncwarp();
+        // copy claim by claim (independent iterations, unrolled for memory parallelism)
+        uint32_t j = 0;
+        for (; j + 4 <= nclaims; j += 4) {
+            uint32_t val[4], dst[4];
+            bool on[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const unsigned long long c = kw[j + u];
+                const uint32_t pos = (uint32_t)(c >> 6) & ((1u << 26) - 1), len = (uint32_t)(c & 63u) + 1u;
+                dst[u] = (uint32_t)(c >> 32);
+                on[u] = lane < len;
+                val[u] = on[u] ? tmp[beg + pos + lane] : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (on[u]) perm[beg + dst[u] + lane] = val[u];
+        }
+        for (; j < nclaims; ++j) {
+            const unsigned long long c = kw[j];
+            const uint32_t pos = (uint32_t)(c >> 6) & ((1u << 26) - 1), len = (uint32_t)(c & 63u) + 1u;
+            if (lane < len) perm[beg + (uint32_t)(c >> 32) + lane] = tmp[beg + pos + lane];
+        }
+        __syncwarp();
+    }
+}
+
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t &total, uint32_t *sh) {
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     uint32_t inc = v;
@@ -360,7 +465,7 @@ k_order_large(const uint32_t *__restrict__ tmp, const uint32_t *__restrict__ sta
     __shared__ uint32_t scan_sh[kOrderWarps];
     __shared__ uint32_t nfar_sh, nlow_sh;
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-    const uint32_t nitems = status[MPM_ST_N_LARGE_BUCKETS];
+    const uint32_t nitems = status[MPM_ST_N_FALLBACK];
     for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
         const uint32_t b = list[it];
         const uint32_t beg = start[b], cnt = count[b];
@@ -556,9 +661,11 @@ mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const De
     if (n > 0) {
         k_scatter<<<grid_p, threads, 0, st>>>(g, w.key, n, w.cursor, w.tmp);
         k_order_small<<<dev.sms * 4, 256, 0, st>>>(w.tmp, w.start, w.count, w.small_list, w.perm, w.status);
+        k_order_claims<<<dev.sms * 4, kClaimWarps * 32, 0, st>>>(w.tmp, w.start, w.count, w.large_list, w.perm,
+                                                                  w.fallback, w.status);
         const int smem = (kOrderCap + kHeadCap + 4) * (int)sizeof(uint32_t);
         cudaFuncSetAttribute(k_order_large, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        k_order_large<<<dev.sms * 4, kOrderThreads, smem, st>>>(w.tmp, w.start, w.count, w.large_list, w.perm, w.gH,
+        k_order_large<<<dev.sms * 2, kOrderThreads, smem, st>>>(w.tmp, w.start, w.count, w.fallback, w.perm, w.gH,
                                                                (unsigned long long *)w.gCW, w.status);
     }
     if (w.cellcount) k_nbr_bound<<<dev.sms * 4, 256, 0, st>>>(g, w.cellcount, w.status);

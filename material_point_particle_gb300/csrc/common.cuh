@@ -142,6 +142,14 @@ __device__ __forceinline__ bool in_tile_x(const GridP &g, const float *x, const 
     return ok;
 }
 
+// Dynamic work distribution: the CTA's next work item from a global counter.
+__device__ __forceinline__ uint32_t grab_item(uint32_t *counter, uint32_t *sh) {
+    __syncthreads();
+    if (threadIdx.x == 0) *sh = atomicAdd(counter, 1u);
+    __syncthreads();
+    return *sh;
+}
+
 // Asynchronous 4-byte global -> shared copies (cp.async), grouped per thread.
 __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
     const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);

@@ -212,14 +212,15 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                                                      const uint32_t *__restrict__ perm,
                                                      const uint32_t *__restrict__ slices,
                                                      const uint32_t *__restrict__ start,
-                                                     const uint32_t *__restrict__ status, float dt, float c4) {
+                                                     uint32_t *__restrict__ status, float dt, float c4) {
     using Hl = Halo<DIM, T>;
     constexpr int NF = DIM + (SORTED ? 2 : 0);
     __shared__ float sv[DIM * Hl::SIZE];
     __shared__ float sbuf[2 * NF * kP2GThreads];
     const Prefetch<NF, kP2GThreads> pf{sbuf};
     const uint32_t nslices = status[MPM_ST_N_SLICES];
-    for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
+    __shared__ uint32_t item_sh;
+    for (uint32_t s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh); s < nslices; s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh)) {
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
         const uint32_t beg = start[t] + first;
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
@@ -282,6 +283,7 @@ mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const W
                       const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
     const int blocks = dev.sms * 4;
+    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4)
         k_g2p<3, 4, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
     else if (g.dim == 2 && g.T == 8)
@@ -295,6 +297,7 @@ mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in,
                              float dt, const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;
     const int blocks = dev.sms * 4;
+    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4) {
         k_g2p<3, 4, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.slices, w.start, w.status, dt,
                                                           c4);

@@ -26,6 +26,7 @@ struct WsView {
     void *gCW;            // [2 n] uint64 claim keys of those buckets
     uint32_t *small_list; // [ntiles + 1] buckets of at most 256 particles
     uint32_t *large_list; // [ntiles + 1] larger buckets
+    uint32_t *fallback;   // [ntiles + 1] larger buckets left to the block kernel
     uint32_t *partial;    // scan block totals, 5 words per 1024 buckets
     uint32_t *status;     // [MPM_STATUS_WORDS]
     uint32_t *cellcount;  // int32 mode only: [ntiles * T^dim], else null

@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
     const Prefetch<Fl::NF, kP2GThreads> pf{sbuf};
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
     const uint32_t nslices = status[MPM_ST_N_SLICES];
-    for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
+    __shared__ uint32_t item_sh;
+    for (uint32_t s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh); s < nslices; s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh)) {
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
         const uint32_t beg = start[t] + first;
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
@@ -249,14 +250,15 @@ template <int DIM, int T>
 __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, const uint32_t *__restrict__ perm,
                                                            const uint32_t *__restrict__ slices,
                                                            const uint32_t *__restrict__ start,
-                                                           const uint32_t *__restrict__ status,
+                                                           uint32_t *__restrict__ status,
                                                            float *__restrict__ acc) {
     using St = Stencil<DIM>;
     using Hl = Halo<DIM, T>;
     using Fl = P2GFields<DIM>;
     __shared__ float sacc[St::NC * Hl::SIZE];
     const uint32_t nslices = status[MPM_ST_N_SLICES];
-    for (uint32_t s = blockIdx.x; s < nslices; s += gridDim.x) {
+    __shared__ uint32_t item_sh;
+    for (uint32_t s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh); s < nslices; s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh)) {
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
         const uint32_t beg = start[t] + first;
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
@@ -294,6 +296,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
 mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const DeviceInfo &dev,
                       cudaStream_t st) {
     const int blocks = dev.sms * 4;
+    cudaMemsetAsync(&w.status[MPM_ST_WORK_P2G], 0, sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4) {
         if (g.acc_mode == MPM_ACC_I64)
             k_p2g_fixed<3, 4, int64_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
