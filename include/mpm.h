@@ -252,6 +252,44 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
 mpm_status mpm_permute(const mpm_grid_desc *desc, const mpm_particles *in, mpm_particles *out,
                        const mpm_bins *bins, void *stream);
 
+/*
+ * mpm_bin_static -- mpm_bin for callers that cannot give the library a
+ * workspace.  The method's pages have no counterpart of this call; it is a
+ * convenience of this library.
+ *
+ * Some callers cannot allocate device memory at the point where they bin:
+ * code embedded in a host application that owns every device allocation
+ * under its own budget, or a loop that must not call cudaMalloc because it
+ * may synchronise the device and stall work already in flight.  This call
+ * bins into a workspace the library holds itself: a file-scope device array
+ * of MPM_STATIC_WORKSPACE_BYTES (16 MiB) per device, created when the
+ * library's device code is loaded.  It calls no allocator (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *
+ * Arguments and results are those of mpm_bin with bins = `out`: the call
+ * fills `out` (host struct) as mpm_bins_init would, with every device array
+ * pointing into the static workspace, then runs mpm_bin.  `out` may then be
+ * passed to mpm_p2g, mpm_grid_update, mpm_g2p, mpm_g2p_sorted, mpm_permute
+ * and mpm_read_status like any other bins.
+ *  - Size limit: mpm_workspace_bytes(desc, parts->n) must be at most
+ *    MPM_STATIC_WORKSPACE_BYTES; a larger problem returns MPM_E_WORKSPACE at
+ *    once and launches nothing.  Use mpm_bins_init with your own memory then.
+ *  - Zero state: nothing in the static workspace has to be zero beforehand
+ *    (every call clears the counters it uses).  The accumulator grid given to
+ *    a later mpm_p2g must still be zero, as always.
+ *  - Setup: the first call on each device looks up the array's device
+ *    address with that device current (this may load the library's device
+ *    code); make that first call before any stream capture begins.
+ *  - Sharing: there is ONE static workspace per device and process.  A call
+ *    overwrites what the previous call left there, so calls (and the P2G,
+ *    grid update and G2P calls that read their `out`) must not overlap in
+ *    time: two calls in flight at once on different streams or host threads
+ *    race on the same memory.  Order them on one stream.
+ */
+#define MPM_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+mpm_status mpm_bin_static(const mpm_grid_desc *desc, const mpm_particles *parts, int flags, mpm_bins *out,
+                          void *stream);
+
 /* Asynchronous copy of the MPM_STATUS_WORDS status words to host memory. */
 mpm_status mpm_read_status(const mpm_bins *bins, uint32_t *host_out, void *stream);
 

@@ -19,6 +19,7 @@ MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
 (ST_FLAGS, ST_N_OUTSIDE, ST_N_OUT_OF_RANGE, ST_N_VALID, ST_N_SLICES, ST_N_ACTIVE, ST_MAX_NEIGHBOURS,
  ST_N_BIG_TILES, ST_N_SMALL_BUCKETS, ST_N_LARGE_BUCKETS, ST_N_FALLBACK) = range(11)
 MPM_STATUS_WORDS = 16
+MPM_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class MPMError(RuntimeError):
@@ -79,8 +80,10 @@ def library() -> ct.CDLL:
                                         ct.c_float, P(ct.c_float), VP]
             L.mpm_permute.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP]
             L.mpm_read_status.argtypes = [P(Bins), VP, VP]
+            L.mpm_bin_static.argtypes = [P(GridDesc), P(Particles), ct.c_int, P(Bins), VP]
             for name in ("mpm_bins_init", "mpm_bin", "mpm_p2g", "mpm_grid_update", "mpm_g2p", "mpm_step",
-                         "mpm_g2p_sorted", "mpm_step_sorted", "mpm_step_host", "mpm_permute", "mpm_read_status"):
+                         "mpm_g2p_sorted", "mpm_step_sorted", "mpm_step_host", "mpm_permute", "mpm_read_status",
+                         "mpm_bin_static"):
                 getattr(L, name).restype = ct.c_int
             _L = L
     return _L
@@ -228,3 +231,23 @@ def mpm_read_status(bins: Bins, out: torch.Tensor, stream=None):
     assert out.numel() >= MPM_STATUS_WORDS and out.element_size() == 4 and out.device.type == "cpu"
     _check(library().mpm_read_status(ct.byref(bins), ct.c_void_p(out.data_ptr()), _stream(stream)),
            "mpm_read_status")
+
+
+def mpm_bin_static(desc: GridDesc, parts: Particles, flags: int = 0, stream=None) -> Bins:
+    """Bins into the library's own fixed-size device workspace (no allocation
+    by anyone) and returns the bins, whose arrays point into that workspace.
+
+    For callers that cannot allocate device memory where they bin.  One such
+    workspace exists per device and process: the next call overwrites it, so
+    calls (and the steps that read the returned bins) must not overlap; keep
+    them on one stream.  The first call on a device sets the workspace up, so
+    make it before any stream capture begins.
+    """
+    b = Bins()
+    code = library().mpm_bin_static(ct.byref(desc), ct.byref(parts), flags, ct.byref(b), _stream(stream))
+    if code == MPM_E_WORKSPACE:
+        need = mpm_workspace_bytes(desc, int(parts.n))
+        raise MPMError(code, f"mpm_bin_static: {int(parts.n)} particles need {need} bytes of workspace, the static "
+                             f"workspace holds {MPM_STATIC_WORKSPACE_BYTES}; use mpm_bins_init with your own memory")
+    _check(code, "mpm_bin_static")
+    return b
