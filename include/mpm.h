@@ -95,10 +95,9 @@ enum {
     MPM_ST_N_SLICES = 4,     /* P2G work items */
     MPM_ST_N_ACTIVE = 5,     /* tiles holding at least one particle */
     MPM_ST_MAX_NEIGHBOURS = 6, /* int32 mode: most particles whose stencil covers one node */
-    MPM_ST_N_BIG_TILES = 7,  /* buckets ordered in global scratch (above the shared-memory capacity) */
-    MPM_ST_N_SMALL_BUCKETS = 8, /* buckets of at most 256 particles (ordered by one warp each) */
-    MPM_ST_N_LARGE_BUCKETS = 9, /* larger buckets */
-    MPM_ST_N_FALLBACK = 10,  /* larger buckets ordered by the block kernel (many claims) */
+    MPM_ST_N_BIG_TILES = 7,  /* buckets whose runs were sorted in global memory (cold, huge buckets) */
+    MPM_ST_N_RUNS = 8,       /* runs: maximal index ranges of one bucket (= buckets when already sorted) */
+    MPM_ST_N_LARGE_BUCKETS = 9, /* buckets of more than 512 runs (sorted by one block each) */
     MPM_ST_WORK_P2G = 11,    /* internal: work counter of the P2G launch */
     MPM_ST_WORK_G2P = 12,    /* internal: work counter of the G2P launch */
     MPM_STATUS_WORDS = 16

@@ -17,7 +17,8 @@ from . import build as _build
 MPM_OK, MPM_E_ARG, MPM_E_WORKSPACE, MPM_E_DOMAIN, MPM_E_BOUND, MPM_E_CUDA, MPM_E_TIMEOUT, MPM_E_NO_DEVICE = range(8)
 MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
 (ST_FLAGS, ST_N_OUTSIDE, ST_N_OUT_OF_RANGE, ST_N_VALID, ST_N_SLICES, ST_N_ACTIVE, ST_MAX_NEIGHBOURS,
- ST_N_BIG_TILES, ST_N_SMALL_BUCKETS, ST_N_LARGE_BUCKETS, ST_N_FALLBACK) = range(11)
+ ST_N_BIG_TILES, ST_N_RUNS, ST_N_LARGE_BUCKETS) = range(10)
+ST_BIN_WORDS = 10   # status words 0..9 are written by mpm_bin
 MPM_STATUS_WORDS = 16
 MPM_STATIC_WORKSPACE_BYTES = 16 << 20
 

@@ -72,9 +72,8 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
 }
 
 struct Layout {
-    size_t key, perm, tmp, count, start, cursor, active, slices, gH, gCW, small_list, large_list, fallback, partial,
-        status,
-        cellcount, scratch, total;
+    size_t key, perm, heads, tails, count, start, hcnt, tcnt, active, slices, large_list, partial, status, cellcount,
+        scratch, total;
     int64_t max_slices;
 };
 
@@ -96,18 +95,16 @@ Layout layout_of(const GridP &g, int64_t n) {
     L.max_slices = (n + kSliceParticles - 1) / kSliceParticles + std::min<int64_t>(g.ntiles, n) + 1;
     L.key = take(n * sizeof(uint32_t));
     L.perm = take(n * sizeof(uint32_t));
-    L.tmp = take(n * sizeof(uint32_t));
+    L.heads = take(n * sizeof(uint32_t));
+    L.tails = take(n * sizeof(uint32_t));
     L.count = take(nb * sizeof(uint32_t));
     L.start = take((nb + 1) * sizeof(uint32_t));
-    L.cursor = take(nb * sizeof(uint32_t));
+    L.hcnt = take(nb * sizeof(uint32_t));
+    L.tcnt = take(nb * sizeof(uint32_t));
     L.active = take(g.ntiles * sizeof(uint32_t));
     L.slices = take(2 * L.max_slices * sizeof(uint32_t));
-    L.gH = take((n + g.ntiles + 2) * sizeof(uint32_t));
-    L.gCW = take(2 * n * sizeof(uint64_t));
-    L.small_list = take(nb * sizeof(uint32_t));
     L.large_list = take(nb * sizeof(uint32_t));
-    L.fallback = take(nb * sizeof(uint32_t));
-    L.partial = take(5 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
+    L.partial = take(3 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
     L.status = take(MPM_STATUS_WORDS * sizeof(uint32_t));
     L.cellcount = g.acc_mode == MPM_ACC_I32 ? take((size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t)) : 0;
     L.scratch = take(2 * sizeof(uint64_t));
@@ -123,17 +120,15 @@ WsView view_of(const GridP &g, const mpm_bins &b) {
     if (g.acc_mode == MPM_ACC_EXACT_INT) return w;
     w.key = reinterpret_cast<uint32_t *>(base + L.key);
     w.perm = reinterpret_cast<uint32_t *>(base + L.perm);
-    w.tmp = reinterpret_cast<uint32_t *>(base + L.tmp);
+    w.heads = reinterpret_cast<uint32_t *>(base + L.heads);
+    w.tails = reinterpret_cast<uint32_t *>(base + L.tails);
     w.count = reinterpret_cast<uint32_t *>(base + L.count);
     w.start = reinterpret_cast<uint32_t *>(base + L.start);
-    w.cursor = reinterpret_cast<uint32_t *>(base + L.cursor);
+    w.hcnt = reinterpret_cast<uint32_t *>(base + L.hcnt);
+    w.tcnt = reinterpret_cast<uint32_t *>(base + L.tcnt);
     w.active = reinterpret_cast<uint32_t *>(base + L.active);
     w.slices = reinterpret_cast<uint32_t *>(base + L.slices);
-    w.gH = reinterpret_cast<uint32_t *>(base + L.gH);
-    w.gCW = base + L.gCW;
-    w.small_list = reinterpret_cast<uint32_t *>(base + L.small_list);
     w.large_list = reinterpret_cast<uint32_t *>(base + L.large_list);
-    w.fallback = reinterpret_cast<uint32_t *>(base + L.fallback);
     w.partial = reinterpret_cast<uint32_t *>(base + L.partial);
     w.cellcount = g.acc_mode == MPM_ACC_I32 ? reinterpret_cast<uint32_t *>(base + L.cellcount) : nullptr;
     return w;

@@ -16,18 +16,17 @@ struct PartsF;
 
 // Device arrays carved from the caller's workspace (see mpm_bins_init).
 struct WsView {
-    uint32_t *key, *perm, *tmp;
+    uint32_t *key, *perm;
+    uint32_t *heads;      // [n] run heads, each bucket's in its range [start, start + count); then sorted
+    uint32_t *tails;      // [n] run tails, likewise; then the runs' offsets inside the bucket
     uint32_t *count;      // [ntiles + 1] particles per bucket (last: outside the domain)
     uint32_t *start;      // [ntiles + 2] exclusive prefix of count
-    uint32_t *cursor;     // [ntiles + 1]
+    uint32_t *hcnt;       // [ntiles + 1] runs per bucket (heads appended)
+    uint32_t *tcnt;       // [ntiles + 1] tails appended
     uint32_t *active;     // [ntiles]
     uint32_t *slices;     // [2 * max_slices]
-    uint32_t *gH;         // [n + ntiles + 2] claim heads of buckets above the shared-memory capacity
-    void *gCW;            // [2 n] uint64 claim keys of those buckets
-    uint32_t *small_list; // [ntiles + 1] buckets of at most 256 particles
-    uint32_t *large_list; // [ntiles + 1] larger buckets
-    uint32_t *fallback;   // [ntiles + 1] larger buckets left to the block kernel
-    uint32_t *partial;    // scan block totals, 5 words per 1024 buckets
+    uint32_t *large_list; // [ntiles + 1] buckets of more than 512 runs
+    uint32_t *partial;    // scan block totals, 3 words per 1024 buckets
     uint32_t *status;     // [MPM_STATUS_WORDS]
     uint32_t *cellcount;  // int32 mode only: [ntiles * T^dim], else null
 };

@@ -8,17 +8,23 @@
 // integer arithmetic": split rather than weight, so each particle's shares
 // sum exactly to its quantity and the grid is the same in every order.
 //
-// Work item: a slice of at most 256 consecutive sorted particles of one tile
-// (T^dim base cells).  A CTA zeroes the tile's (T+2)^dim x (dim+1) int32
-// accumulators in shared memory, each thread computes its particle's shares,
-// warps whose 32 particles share one base cell add each share with one
-// redux.sync and one shared atomic, the others add lane by lane, and the CTA
-// flushes every nonzero node once with a global atomic add (neighbouring
-// slices and tiles overlap on halo nodes, so the flush must add).
+// Work item: a slice of at most 1024 consecutive binned particles of one
+// tile (T^dim base cells), taken from a global work counter.  A CTA zeroes
+// the tile's (T+2)^dim x (dim+1) int32 accumulators in shared memory, each
+// thread computes its particles' shares and adds each one with a shared
+// atomic as soon as it is formed, and the CTA flushes every nonzero node with
+// one global atomic add (neighbouring slices and tiles overlap on halo nodes,
+// so the flush must add).  The int32 halo is flushed after every 512
+// particles, so no halo sum can overflow.
 #include "common.cuh"
 #include "internal.h"
 
 namespace mpm {
+
+// Particles whose shares may meet in one int32 halo accumulator: 512 shares
+// of magnitude below 2^22 sum to less than 2^31.
+constexpr int kFlushParticles = 512;
+static_assert(kFlushParticles % kP2GThreads == 0, "flush point on a round boundary");
 
 // Share encode: rint(a * b) for |a*b| < 2^22, exact product rounded once (RNE).
 __device__ __forceinline__ int32_t rint_mul(float a, float b) {
@@ -205,6 +211,28 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
 #pragma unroll
             for (int f = 0; f < Fl::NF; ++f) cp_async4(pf.at(stage, f), Fl::src(p, f) + pid);
         };
+        // every nonzero halo node added to the grid once (and, if `clear`,
+        // reset to zero for the rest of the slice)
+        auto flush = [&](bool clear) {
+            for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
+                int hx, hy, hz, idx;
+                Hl::node(h, hx, hy, hz, idx);
+                const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
+                if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
+                const int64_t node = node_index(g, gx, gy, gz);
+#pragma unroll
+                for (int c = 0; c < St::NC; ++c) {
+                    const int32_t val = sacc[c * Hl::SIZE + idx];
+                    if (val == 0) continue;
+                    if (clear) sacc[c * Hl::SIZE + idx] = 0;
+                    if constexpr (sizeof(AccT) == 8)
+                        atomicAdd(reinterpret_cast<unsigned long long *>(acc + c * g.nodes + node),
+                                  (unsigned long long)(long long)val);
+                    else
+                        atomicAdd(reinterpret_cast<int *>(acc + c * g.nodes + node), val);
+                }
+            }
+        };
         if (threadIdx.x < cnt) issue(0, pids[0]);
         cp_async_commit();
 #pragma unroll
@@ -218,29 +246,20 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
                 auto rec = [&](int f) { return *pf.at(stage, f); };
                 if (!scatter_fixed<DIM, T>(g, rec, o, sacc)) ++bad;
             }
+            // int32 halo accumulators: at most kFlushParticles shares of
+            // magnitude below 2^22 reach one node between two flushes
+            if ((q + 1) * kP2GThreads == kFlushParticles && cnt > (uint32_t)kFlushParticles) {
+                __syncthreads();
+                flush(true);
+                __syncthreads();
+            }
         }
         if (bad) {
             atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
             set_flag(status, MPM_E_BOUND);
         }
         __syncthreads();
-        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
-            int hx, hy, hz, idx;
-            Hl::node(h, hx, hy, hz, idx);
-            const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
-            if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
-            const int64_t node = node_index(g, gx, gy, gz);
-#pragma unroll
-            for (int c = 0; c < St::NC; ++c) {
-                const int32_t val = sacc[c * Hl::SIZE + idx];
-                if (val == 0) continue;
-                if constexpr (sizeof(AccT) == 8)
-                    atomicAdd(reinterpret_cast<unsigned long long *>(acc + c * g.nodes + node),
-                              (unsigned long long)(long long)val);
-                else
-                    atomicAdd(reinterpret_cast<int *>(acc + c * g.nodes + node), val);
-            }
-        }
+        flush(false);
         __syncthreads();
     }
 }

@@ -61,19 +61,36 @@ def test_bin_matches_oracle(dim, n, count):
     assert np.array_equal(perm, operm)
     assert np.array_equal(cnt, ocnt)
     assert st[L.ST_N_VALID] == valid and st[L.ST_N_OUTSIDE] == count - valid
+    assert st[L.ST_N_RUNS] == n_runs(cloud["grid"], okey)
+
+
+def n_runs(grid, key):
+    """Maximal ranges of consecutive indices whose particles share a bucket."""
+    key = np.asarray(key, dtype=np.uint64)
+    if key.size == 0:
+        return 0
+    cpt_log2 = grid["dim"] * int(np.log2(grid["tile"]))
+    b = np.where(key == 0xFFFFFFFF, np.uint64(1 << 40), key >> np.uint64(cpt_log2))   # outside: one bucket
+    return 1 + int(np.count_nonzero(b[1:] != b[:-1]))
 
 
 @pytest.mark.parametrize("where", ["tile", "outside"])
-def test_bin_bucket_larger_than_shared_memory(where):
-    """A bucket of 20,000 particles exceeds the shared-memory sort and takes
-    the large-bucket path; the permutation is still the stable sort."""
+@pytest.mark.parametrize("cnt", [2000, 20000])
+def test_bin_bucket_with_many_runs(where, cnt):
+    """One bucket whose particles alternate with another bucket's, so every
+    particle is a run of its own: 1,000 runs take the block sort in shared
+    memory, 10,000 the block sort in global memory.  The permutation is
+    still the stable sort."""
     s = W.Stream(77, 1)
-    cnt = 20000
+    # base cells 16..19 on every axis: one 4^3 tile of a 32^3 grid
+    a = ((16.5 + 3.99 * s.uniform24(3 * cnt)) / 32.0).reshape(3, cnt)
     if where == "tile":
-        # base cells 16..19 on every axis: one 4^3 tile of a 32^3 grid
-        x = ((16.5 + 3.99 * s.uniform24(3 * cnt)) / 32.0).reshape(3, cnt)
+        other = ((8.5 + 3.99 * s.uniform24(3 * cnt)) / 32.0).reshape(3, cnt)   # tile at cells 8..11
     else:
-        x = np.concatenate([np.full((3, cnt), 5.0), 0.5 + 0.2 * s.uniform24(3 * 999).reshape(3, 999)], axis=1)
+        other = np.full((3, cnt), 5.0)
+    x = np.empty((3, 2 * cnt))
+    x[:, 0::2] = a
+    x[:, 1::2] = other
     n = x.shape[1]
     cloud = dict(x=x.astype(np.float32), v=np.zeros((3, n), np.float32), C=np.zeros((9, n), np.float32),
                  m=np.ones(n, np.float32), grid=W.small_cloud(3, 1, 32, seed=1)["grid"])
@@ -81,8 +98,44 @@ def test_bin_bucket_larger_than_shared_memory(where):
     sys.bin()
     key, perm, cnt_t = sys.bins_arrays()
     okey, operm, ocnt, valid = O.bin_particles(cloud["grid"], cloud["x"])
-    assert sys.status()[L.ST_N_BIG_TILES] >= 1
+    st = sys.status()
+    assert st[L.ST_N_RUNS] == n_runs(cloud["grid"], okey) == n
+    assert st[L.ST_N_LARGE_BUCKETS] == 2
+    assert st[L.ST_N_BIG_TILES] == (2 if cnt > 8192 else 0)
     assert np.array_equal(key, okey) and np.array_equal(perm, operm) and np.array_equal(cnt_t, ocnt)
+
+
+def test_bin_sorted_input_has_one_run_per_bucket():
+    """Particles already in bin order: each bucket is one run."""
+    cloud = W.small_cloud(3, 30000, 64, seed=5, lo=0.05, hi=0.95)
+    okey, operm, ocnt, valid = O.bin_particles(cloud["grid"], cloud["x"])
+    srt = {k: (v[..., operm] if k in ("x", "v", "C", "m") else v) for k, v in cloud.items()}
+    sys = make(srt)
+    sys.bin()
+    key, perm, cnt_t = sys.bins_arrays()
+    st = sys.status()
+    assert np.array_equal(perm, np.arange(perm.size, dtype=np.uint32))
+    assert st[L.ST_N_RUNS] == st[L.ST_N_ACTIVE] + (1 if st[L.ST_N_OUTSIDE] else 0)
+
+
+@pytest.mark.parametrize("frac", [0.002, 0.03, 0.3])
+def test_bin_nearly_sorted_input(frac):
+    """Bin order with a fraction of the particles moved elsewhere (as after a
+    step): buckets of a few long runs, some of more than 32."""
+    cloud = W.small_cloud(3, 60000, 16, seed=6, lo=0.05, hi=0.95)   # 64 tiles, ~900 particles each
+    okey, operm, _, _ = O.bin_particles(cloud["grid"], cloud["x"])
+    srt = {k: (v[..., operm] if k in ("x", "v", "C", "m") else v) for k, v in cloud.items()}
+    s = W.Stream(8, 8)
+    n = srt["x"].shape[1]
+    moved = (s.bits(int(frac * n)) % np.uint64(n)).astype(np.int64)
+    srt["x"][:, moved] = (0.05 + 0.9 * s.uniform24(3 * moved.size)).reshape(3, -1).astype(np.float32)
+    sys = make(srt)
+    sys.bin()
+    key, perm, cnt_t = sys.bins_arrays()
+    okey, operm, ocnt, valid = O.bin_particles(srt["grid"], srt["x"])
+    st = sys.status()
+    assert np.array_equal(key, okey) and np.array_equal(perm, operm) and np.array_equal(cnt_t, ocnt)
+    assert st[L.ST_N_RUNS] == n_runs(srt["grid"], okey)
 
 
 def test_bin_tiny_and_empty():
@@ -192,6 +245,23 @@ def test_dense_single_cell_uses_warp_reduction_and_matches():
     sys.bin()
     sys.p2g()
     oacc, _, _ = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert np.array_equal(acc_np(sys), oacc)
+
+
+def test_full_slice_of_largest_shares():
+    """1,024 particles on one point, each with the largest mass the share
+    range allows: their centre-node shares sum past 2^31, so a halo kept in
+    int32 must be flushed part-way through the slice."""
+    cnt = 1024
+    grid = W.small_cloud(3, 1, 32, seed=1, scale_log2=20)["grid"]
+    x = np.full((3, cnt), 10.0 / 32.0, dtype=np.float32)   # base cell 9, f = 1: centre weight 0.75^3
+    m = np.full(cnt, 9.4, dtype=np.float32)                # 0.421875 * 9.4 * 2^20 just under 2^22 - 4096
+    cloud = dict(x=x, v=np.zeros((3, cnt), np.float32), C=np.zeros((9, cnt), np.float32), m=m, grid=grid)
+    sys = make(cloud)
+    sys.bin()
+    sys.p2g()
+    oacc, ost, ocounts = O.p2g_fixed(grid, x, cloud["v"], cloud["C"], m)
+    assert ocounts[1] == 0 and oacc[0].max() > 2 ** 31
     assert np.array_equal(acc_np(sys), oacc)
 
 

@@ -16,7 +16,7 @@ from material_point_particle_gb300.system import MPMSystem
 
 pytestmark = pytest.mark.gpu
 
-BIN_WORDS = L.ST_N_FALLBACK + 1   # the status words mpm_bin writes
+BIN_WORDS = L.ST_BIN_WORDS   # the status words mpm_bin writes
 
 
 def _status(bins):
