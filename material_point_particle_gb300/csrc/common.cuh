@@ -142,10 +142,22 @@ __device__ __forceinline__ bool in_tile_x(const GridP &g, const float *x, const 
     return ok;
 }
 
-// Dynamic work distribution: the CTA's next work item from a global counter.
+// Dynamic work distribution from a global counter.  A CTA takes its first
+// item with grab_item; inside the loop, thread 0 asks for the next item at
+// the top (ask_item: the atomic's latency overlaps the item's work) and
+// publish_item hands it to the whole CTA at the bottom.
 __device__ __forceinline__ uint32_t grab_item(uint32_t *counter, uint32_t *sh) {
     __syncthreads();
     if (threadIdx.x == 0) *sh = atomicAdd(counter, 1u);
+    __syncthreads();
+    return *sh;
+}
+__device__ __forceinline__ uint32_t ask_item(uint32_t *counter) {
+    return threadIdx.x == 0 ? atomicAdd(counter, 1u) : 0u;
+}
+__device__ __forceinline__ uint32_t publish_item(uint32_t next, uint32_t *sh) {
+    __syncthreads();
+    if (threadIdx.x == 0) *sh = next;
     __syncthreads();
     return *sh;
 }

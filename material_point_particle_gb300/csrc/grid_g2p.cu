@@ -204,28 +204,90 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     }
 }
 
+// Interleaved slices.  The sorted output keeps each slice in its place but
+// orders it by the bank class of the particles' base cells (the low five bits
+// of the cell key: x + 4y + 16(z mod 2) in a 4^3 tile, x + 8(y mod 4) in an
+// 8^2 tile), stable in bin order, then deals the class-sorted entries out
+// column by column over rounds of 32: with R = ceil(cnt / 32) rounds and
+// L = cnt - 32 (R - 1) lanes in the last one, lane l holds sorted entries
+// [cum(l), cum(l + 1)), cum(l) = l R - max(0, l - L), and entry
+// cum(l) + rho sits at rho * 32 + l.  So the 32 entries of a round come from
+// classes spread over the whole range.  Cells of different classes put a
+// given stencil node in different shared-memory banks, and particles move a
+// small fraction of a cell per step, so P2G and G2P, which take particles 32
+// at a time in storage order, meet few bank conflicts.
+
+// Sorted entry held by place pos of an interleaved slice of cnt entries.
+__device__ __forceinline__ uint32_t interleave_entry(uint32_t pos, uint32_t cnt) {
+    const uint32_t R = (cnt + 31) / 32, L = cnt - 32 * (R - 1);
+    const uint32_t l = pos & 31u, rho = pos >> 5;
+    return l * R - (l > L ? l - L : 0u) + rho;
+}
+
 // Work item as in P2G: one slice of a tile.  The CTA stages the tile's halo
 // of node velocities in shared memory (padded as the P2G accumulators), then
 // every thread gathers its particles from it.
+//
+// In place: thread t takes slice entries t, t + 256, ...; the next one's
+// fields are copied into shared memory (cp.async) while the current one
+// gathers.  Sorted: the slice's x, m and id are copied into shared memory in
+// bin order, the slice is counting-sorted by bank class, and thread t
+// computes the particles that go to places t, t + 256, ... of the
+// interleaved slice, so that its writes are coalesced and its reads of the
+// velocity halo meet few bank conflicts.
 template <int DIM, int T, bool SORTED>
 __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                      const uint32_t *__restrict__ perm,
+                                                     const uint32_t *__restrict__ key,
                                                      const uint32_t *__restrict__ slices,
                                                      const uint32_t *__restrict__ start,
                                                      uint32_t *__restrict__ status, float dt, float c4) {
     using Hl = Halo<DIM, T>;
-    constexpr int NF = DIM + (SORTED ? 2 : 0);
+    constexpr int NQ = kSliceParticles / kP2GThreads;
+    constexpr int NWARP = kP2GThreads / 32;
+    static_assert(NQ * NWARP == 32, "one warp-scan lane per (round, warp)");
+    // in place: per-thread double buffer of x; sorted: x, m, id of the whole slice
+    constexpr int NF = SORTED ? DIM + 2 : DIM;
+    constexpr int BUF = SORTED ? NF * kSliceParticles : 2 * NF * kP2GThreads;
     __shared__ float sv[DIM * Hl::SIZE];
-    __shared__ float sbuf[2 * NF * kP2GThreads];
-    const Prefetch<NF, kP2GThreads> pf{sbuf};
+    __shared__ float sbuf[BUF];
+    // [(qi, warp)][class], rows padded to 33 words: the scan reads a column
+    __shared__ uint32_t hist[SORTED ? NQ * NWARP * 33 : 1];
+    __shared__ uint32_t cstart[SORTED ? 32 : 1];
+    // sorted entry e -> bin-order entry, at e + e / 32: the interleaved reads
+    // take entries R apart
+    __shared__ uint32_t order[SORTED ? kSliceParticles + kSliceParticles / 32 : 1];
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
-    for (uint32_t s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh); s < nslices; s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh)) {
+    uint32_t next = 0;
+    for (uint32_t s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
+        next = ask_item(&status[MPM_ST_WORK_G2P]);
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
         const uint32_t beg = start[t] + first;
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
         int o[3];
         tile_origin(g, t, o);
+        uint32_t pids[NQ];
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+            const uint32_t r = threadIdx.x + qi * kP2GThreads;
+            pids[qi] = r < cnt ? perm[beg + r] : 0u;
+        }
+        if constexpr (SORTED) {
+            // the slice's x, m, id in bin order
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                const uint32_t r = threadIdx.x + qi * kP2GThreads;
+                if (r < cnt) {
+#pragma unroll
+                    for (int f = 0; f < DIM; ++f) cp_async4(&sbuf[f * kSliceParticles + r], p.x[f] + pids[qi]);
+                    cp_async4(&sbuf[DIM * kSliceParticles + r], p.m + pids[qi]);
+                    if (p.id) cp_async4(&sbuf[(DIM + 1) * kSliceParticles + r], p.id + pids[qi]);
+                }
+            }
+            cp_async_commit();
+        }
         for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
             int hx, hy, hz, idx;
             Hl::node(h, hx, hy, hz, idx);
@@ -235,39 +297,89 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
 #pragma unroll
             for (int k = 0; k < DIM; ++k) sv[k * Hl::SIZE + idx] = in ? vel[k * g.nodes + node] : 0.f;
         }
-        __syncthreads();
-        // each thread's particles r, r + 256, ...: the next one's fields are
-        // copied into shared memory (cp.async) while the current one gathers
-        constexpr int NQ = kSliceParticles / kP2GThreads;
-        uint32_t pids[NQ];
+        if constexpr (SORTED) {
+            // stable counting sort of the slice by bank class: counts per
+            // (round, warp, class), scanned class-major
+            uint32_t cls[NQ], below[NQ];
 #pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-            const uint32_t r = threadIdx.x + qi * kP2GThreads;
-            pids[qi] = r < cnt ? perm[beg + r] : 0u;
-        }
-        auto issue = [&](int stage, uint32_t pid) {
-#pragma unroll
-            for (int f = 0; f < DIM; ++f) cp_async4(pf.at(stage, f), p.x[f] + pid);
-            if constexpr (SORTED) {
-                cp_async4(pf.at(stage, DIM), p.m + pid);
-                if (p.id) cp_async4(pf.at(stage, DIM + 1), p.id + pid);
+            for (int qi = 0; qi < NQ; ++qi) {
+                const uint32_t r = threadIdx.x + qi * kP2GThreads;
+                cls[qi] = r < cnt ? (key[pids[qi]] & 31u) : 32u;
             }
-        };
-        if (threadIdx.x < cnt) issue(0, pids[0]);
-        cp_async_commit();
+            for (int i = threadIdx.x; i < NQ * NWARP * 33; i += blockDim.x) hist[i] = 0;
+            __syncthreads();
 #pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-            const uint32_t r = threadIdx.x + qi * kP2GThreads;
-            if (qi + 1 < NQ && r + kP2GThreads < cnt) issue((qi + 1) & 1, pids[qi + 1]);
+            for (int qi = 0; qi < NQ; ++qi) {
+                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, cls[qi]);
+                below[qi] = (uint32_t)__popc(peers & lanemask_lt());
+                if (cls[qi] < 32u && below[qi] == 0) hist[(qi * NWARP + warp) * 33 + cls[qi]] = (uint32_t)__popc(peers);
+            }
+            __syncthreads();
+            for (uint32_t c = warp; c < 32; c += NWARP) {
+                const uint32_t v = hist[lane * 33 + c];
+                uint32_t inc = v;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+                    if ((int)lane >= d) inc += t2;
+                }
+                hist[lane * 33 + c] = inc - v;
+                if (lane == 31) cstart[c] = inc;
+            }
+            __syncthreads();
+            if (warp == 0) {
+                const uint32_t v = cstart[lane];
+                uint32_t inc = v;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+                    if ((int)lane >= d) inc += t2;
+                }
+                cstart[lane] = inc - v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                const uint32_t r = threadIdx.x + qi * kP2GThreads;
+                if (cls[qi] < 32u) {
+                    const uint32_t e = cstart[cls[qi]] + hist[(qi * NWARP + warp) * 33 + cls[qi]] + below[qi];
+                    order[e + (e >> 5)] = r;
+                }
+            }
+            cp_async_wait<0>();
+            __syncthreads();
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                const uint32_t pos = threadIdx.x + qi * kP2GThreads;
+                if (pos < cnt) {
+                    const uint32_t e = interleave_entry(pos, cnt);
+                    const uint32_t r = order[e + (e >> 5)];
+                    auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
+                    gather_one<DIM, T, true>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4);
+                }
+            }
+        } else {
+            const Prefetch<NF, kP2GThreads> pf{sbuf};
+            __syncthreads();
+            auto issue = [&](int stage, uint32_t pid) {
+#pragma unroll
+                for (int f = 0; f < DIM; ++f) cp_async4(pf.at(stage, f), p.x[f] + pid);
+            };
+            if (threadIdx.x < cnt) issue(0, pids[0]);
             cp_async_commit();
-            cp_async_wait<1>();
-            if (r < cnt) {
-                const int stage = qi & 1;
-                auto rec = [&](int f) { return *pf.at(stage, f); };
-                gather_one<DIM, T, SORTED>(g, p, q, pids[qi], SORTED ? beg + r : pids[qi], rec, o, sv, dt, c4);
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                const uint32_t r = threadIdx.x + qi * kP2GThreads;
+                if (qi + 1 < NQ && r + kP2GThreads < cnt) issue((qi + 1) & 1, pids[qi + 1]);
+                cp_async_commit();
+                cp_async_wait<1>();
+                if (r < cnt) {
+                    const int stage = qi & 1;
+                    auto rec = [&](int f) { return *pf.at(stage, f); };
+                    gather_one<DIM, T, false>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4);
+                }
             }
         }
-        __syncthreads();
     }
 }
 
@@ -285,9 +397,9 @@ mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const W
     const int blocks = dev.sms * 4;
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4)
-        k_g2p<3, 4, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
+        k_g2p<3, 4, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
     else if (g.dim == 2 && g.T == 8)
-        k_g2p<2, 8, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.slices, w.start, w.status, dt, c4);
+        k_g2p<2, 8, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
     else
         return MPM_E_ARG;
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
@@ -299,11 +411,11 @@ mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in,
     const int blocks = dev.sms * 4;
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4) {
-        k_g2p<3, 4, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.slices, w.start, w.status, dt,
+        k_g2p<3, 4, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start, w.status, dt,
                                                           c4);
         k_copy_rest<3><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
     } else if (g.dim == 2 && g.T == 8) {
-        k_g2p<2, 8, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.slices, w.start, w.status, dt,
+        k_g2p<2, 8, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start, w.status, dt,
                                                           c4);
         k_copy_rest<2><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
     } else {

@@ -185,7 +185,9 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
-    for (uint32_t s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh); s < nslices; s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh)) {
+    uint32_t next = 0;
+    for (uint32_t s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
+        next = ask_item(&status[MPM_ST_WORK_P2G]);
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
         const uint32_t beg = start[t] + first;
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
@@ -277,7 +279,9 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
     __shared__ float sacc[St::NC * Hl::SIZE];
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
-    for (uint32_t s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh); s < nslices; s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh)) {
+    uint32_t next = 0;
+    for (uint32_t s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
+        next = ask_item(&status[MPM_ST_WORK_P2G]);
         const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
         const uint32_t beg = start[t] + first;
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);

@@ -337,11 +337,38 @@ def test_workload_step_matches_oracle(name, kw):
         assert np.max(np.abs(x - ox)) <= 1e-6
 
 
+SLICE = 1024   # particles per work item (a slice of one tile)
+
+
+def sorted_output_order(key, perm, tile_count, n_valid):
+    """Where mpm_g2p_sorted puts each particle: slice by slice in bin order,
+    each slice stably sorted by bank class (key & 31) and dealt out column by
+    column over rounds of 32."""
+    out = perm.astype(np.int64).copy()
+    start = np.concatenate([[0], np.cumsum(tile_count.astype(np.int64))])
+    for t in np.nonzero(tile_count)[0]:
+        for first in range(0, int(tile_count[t]), SLICE):
+            beg = int(start[t]) + first
+            cnt = min(SLICE, int(tile_count[t]) - first)
+            idx = perm[beg:beg + cnt].astype(np.int64)
+            srt = np.empty(cnt, np.int64)
+            srt[np.argsort(key[idx] & 31, kind="stable")] = np.arange(cnt)
+            R = -(-cnt // 32)
+            Lf = cnt - 32 * (R - 1)
+            lane = np.where(srt < Lf * R, srt // R, Lf + (srt - Lf * R) // max(R - 1, 1))
+            rho = np.where(srt < Lf * R, srt % R, (srt - Lf * R) % max(R - 1, 1))
+            pos = rho * 32 + lane
+            assert np.array_equal(np.sort(pos), np.arange(cnt))
+            out[beg + pos] = idx
+    assert int(start[-1]) == n_valid
+    return out
+
+
 def test_g2p_sorted_moves_particles_into_bin_order():
     cloud = with_outliers(W.small_cloud(3, 7001, 32, seed=502, scale_log2=19, lo=0.05, hi=0.95))
     sys = make(cloud).enable_sorted()
     sys.bin()
-    _, perm, _ = sys.bins_arrays()
+    key, perm, cnt = sys.bins_arrays()
     valid = int(sys.status()[L.ST_N_VALID])
     sys.p2g()
     sys.grid_update()
@@ -352,7 +379,7 @@ def test_g2p_sorted_moves_particles_into_bin_order():
     ovel = O.grid_update_fixed(cloud["grid"], oacc)
     ox, ov, oC, moved = O.g2p(cloud["grid"], ovel, cloud["x"], cloud["v"], cloud["C"])
     assert moved == valid
-    p = perm.astype(np.int64)
+    p = sorted_output_order(key, perm, cnt, valid)
     assert np.array_equal(ids, p)
     assert np.array_equal(x.view(np.uint32), ox[:, p].view(np.uint32))
     assert np.array_equal(v.view(np.uint32), ov[:, p].view(np.uint32))
