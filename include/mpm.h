@@ -206,13 +206,21 @@ mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *p
                    float dt, void *stream);
 
 /*
- * mpm_g2p_sorted -- mpm_g2p that also moves the particles into bin order:
- * out[j] is the gathered new state of particle in[perm[j]] for the in-domain
- * particles (j below MPM_ST_N_VALID) and an unchanged copy of in[perm[j]] for
- * the rest; m and id are carried along.  This is the ping-pong buffer of
- * "Particle Worlds, part 3", Step 4 ("the sort writes into a second buffer"):
- * the next step's binning then starts from almost sorted particles, so its
- * permutation is close to the identity and every particle pass reads and
+ * mpm_g2p_sorted -- mpm_g2p that also moves the particles into bin order.
+ * The in-domain particles (perm entries below MPM_ST_N_VALID) are written
+ * tile by tile in bin order, each P2G work item (a slice of up to 1024
+ * consecutive perm entries of one tile) to the same range of out, but with
+ * the slice reordered: stably sorted by the bank class of the particle's base
+ * cell (key & 31), then dealt out column by column over rounds of 32 (lane l
+ * of R = ceil(cnt/32) rounds holds sorted entries cum(l) .. cum(l+1) - 1 with
+ * cum(l) = l*R - max(0, l - L), L = cnt - 32*(R - 1), and entry cum(l) + rho
+ * goes to slice place rho*32 + l).  Particles 32 apart in a round then sit in
+ * cells that use different shared-memory banks, which the next step's P2G
+ * and G2P exploit.  The remaining particles (outside the domain) are copied
+ * unchanged to out[j] = in[perm[j]].  m and id are carried along.  This is
+ * the ping-pong buffer of "Particle Worlds, part 3", Step 4 ("the sort writes
+ * into a second buffer"): the next step's binning then starts from almost
+ * sorted particles, so its runs are long and every particle pass reads and
  * writes contiguous memory.  The bits of every particle's new state are those
  * of mpm_g2p.  `in` and `out` must not overlap.
  */
@@ -238,7 +246,7 @@ mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_par
  * host SoA (`host`: x, v, C, m and id if given; pinned memory gives full copy
  * bandwidth) into the device arrays `dev_in`, runs mpm_step_sorted into
  * `dev_out`, and copies x, v, C, m (and id) of `dev_out` back into `host`, so
- * the host arrays hold the new state in bin order.  Asynchronous on `stream`;
+ * the host arrays hold the new state in the order mpm_g2p_sorted writes.  Asynchronous on `stream`;
  * the host arrays must stay valid until it completes.
  */
 mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev_in,
