@@ -123,15 +123,33 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
     if (q.id && p.id) q.id[dst] = p.id[src];
 }
 
+// Velocity halo of one tile in shared memory, padded as the P2G accumulators:
+// the x and y components side by side (one 64-bit word per node, so that one
+// load feeds a packed fp32x2 fma), z (3D) in its own array.
+template <int DIM, int T>
+struct VelHalo {
+    using Hl = Halo<DIM, T>;
+    float2 *xy;
+    float *z;
+};
+
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+// sum3 on two independent lanes (each lane exactly the scalar sum3)
+__device__ __forceinline__ float2 sum3x2(const float2 w[3], const float2 t[3]) {
+    return __ffma2_rn(w[2], t[2], __ffma2_rn(w[1], t[1], __fmul2_rn(w[0], t[0])));
+}
+
 // One particle's gather from the tile's velocity halo in shared memory.  The
 // new state of particle `pid` of `p` goes to entry `dst` of `q` (the same
 // arrays and index in place; the sorted output otherwise, m and id with it).
-// rec(f): the particle's prefetched fields x[dim], then (sorted output) m and
-// the id bits.
+// rec(f): the particle's staged fields x[dim], then (sorted output) m and the
+// id bits.  The x and y components go through packed fp32x2 arithmetic, which
+// rounds each lane exactly as the scalar operation.
 template <int DIM, int T, bool SORTED, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
-                                           uint32_t dst, const Rec &rec, const int o[3], const float *sv, float dt,
-                                           float c4) {
+                                           uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
+                                           float dt, float c4) {
     using Hl = Halo<DIM, T>;
     float x[DIM], f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
@@ -150,45 +168,82 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     }
     const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
                             : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
+    float2 W[3][3], WE[3][3];
+#pragma unroll
+    for (int l = 0; l < DIM; ++l)
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            W[l][a] = f2(w[l][a]);
+            WE[l][a] = f2(we[l][a]);
+        }
     float vn[DIM], Bm[DIM][DIM];
+    const float2 *vxy = sv.xy + hb;
+    if constexpr (DIM == 3) {
+        // x and y packed
+        float2 Y[3], Ye[3], Yq[3];
 #pragma unroll
-    for (int k = 0; k < DIM; ++k) {
-        const float *vk = sv + k * Hl::SIZE + hb;
-        if constexpr (DIM == 3) {
-            float Y[3], Ye[3], Yq[3];
+        for (int a0 = 0; a0 < 3; ++a0) {
+            float2 Z[3], Zq[3];
 #pragma unroll
-            for (int a0 = 0; a0 < 3; ++a0) {
-                float Z[3], Zq[3];
+            for (int a1 = 0; a1 < 3; ++a1) {
+                float2 t[3];
 #pragma unroll
-                for (int a1 = 0; a1 < 3; ++a1) {
-                    float t[3];
-#pragma unroll
-                    for (int a2 = 0; a2 < 3; ++a2) t[a2] = vk[a0 + a1 * Hl::SY + a2 * Hl::SZ];
-                    Z[a1] = sum3(w[2], t);
-                    Zq[a1] = sum3(we[2], t);
-                }
-                Y[a0] = sum3(w[1], Z);
-                Ye[a0] = sum3(we[1], Z);
-                Yq[a0] = sum3(w[1], Zq);
+                for (int a2 = 0; a2 < 3; ++a2) t[a2] = vxy[a0 + a1 * Hl::SY + a2 * Hl::SZ];
+                Z[a1] = sum3x2(W[2], t);
+                Zq[a1] = sum3x2(WE[2], t);
             }
-            vn[k] = sum3(w[0], Y);
-            Bm[k][0] = sum3(we[0], Y);
-            Bm[k][1] = sum3(w[0], Ye);
-            Bm[k][DIM - 1] = sum3(w[0], Yq);
-        } else {
-            float Y[3], Ye[3];
+            Y[a0] = sum3x2(W[1], Z);
+            Ye[a0] = sum3x2(WE[1], Z);
+            Yq[a0] = sum3x2(W[1], Zq);
+        }
+        const float2 v2 = sum3x2(W[0], Y), b0 = sum3x2(WE[0], Y), b1 = sum3x2(W[0], Ye), b2 = sum3x2(W[0], Yq);
+        vn[0] = v2.x;
+        vn[1] = v2.y;
+        Bm[0][0] = b0.x;
+        Bm[1][0] = b0.y;
+        Bm[0][1] = b1.x;
+        Bm[1][1] = b1.y;
+        Bm[0][2] = b2.x;
+        Bm[1][2] = b2.y;
+        // z alone
+        const float *vz = sv.z + hb;
+        float Ys[3], Yes[3], Yqs[3];
 #pragma unroll
-            for (int a0 = 0; a0 < 3; ++a0) {
+        for (int a0 = 0; a0 < 3; ++a0) {
+            float Z[3], Zq[3];
+#pragma unroll
+            for (int a1 = 0; a1 < 3; ++a1) {
                 float t[3];
 #pragma unroll
-                for (int a1 = 0; a1 < 3; ++a1) t[a1] = vk[a0 + a1 * Hl::SY];
-                Y[a0] = sum3(w[1], t);
-                Ye[a0] = sum3(we[1], t);
+                for (int a2 = 0; a2 < 3; ++a2) t[a2] = vz[a0 + a1 * Hl::SY + a2 * Hl::SZ];
+                Z[a1] = sum3(w[2], t);
+                Zq[a1] = sum3(we[2], t);
             }
-            vn[k] = sum3(w[0], Y);
-            Bm[k][0] = sum3(we[0], Y);
-            Bm[k][1] = sum3(w[0], Ye);
+            Ys[a0] = sum3(w[1], Z);
+            Yes[a0] = sum3(we[1], Z);
+            Yqs[a0] = sum3(w[1], Zq);
         }
+        vn[2] = sum3(w[0], Ys);
+        Bm[2][0] = sum3(we[0], Ys);
+        Bm[2][1] = sum3(w[0], Yes);
+        Bm[2][2] = sum3(w[0], Yqs);
+    } else {
+        float2 Y[3], Ye[3];
+#pragma unroll
+        for (int a0 = 0; a0 < 3; ++a0) {
+            float2 t[3];
+#pragma unroll
+            for (int a1 = 0; a1 < 3; ++a1) t[a1] = vxy[a0 + a1 * Hl::SY];
+            Y[a0] = sum3x2(W[1], t);
+            Ye[a0] = sum3x2(WE[1], t);
+        }
+        const float2 v2 = sum3x2(W[0], Y), b0 = sum3x2(WE[0], Y), b1 = sum3x2(W[0], Ye);
+        vn[0] = v2.x;
+        vn[1] = v2.y;
+        Bm[0][0] = b0.x;
+        Bm[1][0] = b0.y;
+        Bm[0][1] = b1.x;
+        Bm[1][1] = b1.y;
     }
 #pragma unroll
     for (int k = 0; k < DIM; ++k) {
@@ -249,7 +304,9 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
     // in place: per-thread double buffer of x; sorted: x, m, id of the whole slice
     constexpr int NF = SORTED ? DIM + 2 : DIM;
     constexpr int BUF = SORTED ? NF * kSliceParticles : 2 * NF * kP2GThreads;
-    __shared__ float sv[DIM * Hl::SIZE];
+    __shared__ float2 sv_xy[Hl::SIZE];
+    __shared__ float sv_z[DIM == 3 ? Hl::SIZE : 1];
+    const VelHalo<DIM, T> sv{sv_xy, sv_z};
     __shared__ float sbuf[BUF];
     // [(qi, warp)][class], rows padded to 33 words: the scan reads a column
     __shared__ uint32_t hist[SORTED ? NQ * NWARP * 33 : 1];
@@ -294,8 +351,8 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
             const bool in = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
             const int64_t node = in ? node_index(g, gx, gy, gz) : 0;
-#pragma unroll
-            for (int k = 0; k < DIM; ++k) sv[k * Hl::SIZE + idx] = in ? vel[k * g.nodes + node] : 0.f;
+            sv_xy[idx] = in ? make_float2(vel[node], vel[g.nodes + node]) : make_float2(0.f, 0.f);
+            if (DIM == 3) sv_z[idx] = in ? vel[2 * g.nodes + node] : 0.f;
         }
         if constexpr (SORTED) {
             // stable counting sort of the slice by bank class: counts per

@@ -79,33 +79,44 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     rest[0] = __float2int_rn(Mt);
 #pragma unroll
     for (int k = 0; k < DIM; ++k) rest[1 + k] = __float2int_rn(__fmul_rn(Mt, v[k]));
+    // the x and y momentum channels go through packed fp32x2 arithmetic,
+    // which rounds each lane exactly as the scalar operation
+    const float2 magic2 = make_float2(kMagic, kMagic);
+    float2 Cxy[3] = {make_float2(C[0], C[DIM + 0]), make_float2(C[1], C[DIM + 1]), make_float2(0.f, 0.f)};
+    if constexpr (DIM == 3) Cxy[2] = make_float2(C[2], C[5]);
 #pragma unroll
     for (int a0 = 0; a0 < 3; ++a0) {
         const float Wx = __fmul_rn(w[0][a0], Mt);
-        float h0[DIM];
-#pragma unroll
-        for (int k = 0; k < DIM; ++k) h0[k] = __fmaf_rn(C[k * DIM + 0], dd[0][a0], v[k]);
+        const float2 h0xy = __ffma2_rn(Cxy[0], make_float2(dd[0][a0], dd[0][a0]), make_float2(v[0], v[1]));
+        float h0z = 0.f;
+        if constexpr (DIM == 3) h0z = __fmaf_rn(C[6], dd[0][a0], v[2]);
 #pragma unroll
         for (int a1 = 0; a1 < 3; ++a1) {
-            const float Wxy = __fmul_rn(Wx, w[1][a1]);
-            float h1[DIM];
-#pragma unroll
-            for (int k = 0; k < DIM; ++k) h1[k] = __fmaf_rn(C[k * DIM + 1], dd[1][a1], h0[k]);
+            const float2 Wxy = __fmul2_rn(make_float2(Wx, Wx), make_float2(w[1][a1], w[1][a1]));
+            const float2 h1xy = __ffma2_rn(Cxy[1], make_float2(dd[1][a1], dd[1][a1]), h0xy);
+            float h1z = 0.f;
+            if constexpr (DIM == 3) h1z = __fmaf_rn(C[7], dd[1][a1], h0z);
 #pragma unroll
             for (int a2 = 0; a2 < (DIM == 3 ? 3 : 1); ++a2) {
                 const int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
                 if (a == St::CENTRE) continue;
-                const float Wt = DIM == 3 ? __fmul_rn(Wxy, w[2][a2]) : Wxy;
+                const float2 Wt = DIM == 3 ? __fmul2_rn(Wxy, make_float2(w[2][a2], w[2][a2])) : Wxy;
                 const int at = hb + Hl::off(a);
-                const int32_t sm = rint_f(Wt);
+                const int32_t sm = rint_f(Wt.x);
                 rest[0] -= sm;
                 atomicAdd(&sacc[at], sm);
-#pragma unroll
-                for (int k = 0; k < DIM; ++k) {
-                    const float vel = DIM == 3 ? __fmaf_rn(C[k * DIM + 2], dd[2][a2], h1[k]) : h1[k];
-                    const int32_t sk = rint_mul(Wt, vel);
-                    rest[1 + k] -= sk;
-                    atomicAdd(&sacc[(1 + k) * Hl::SIZE + at], sk);
+                const float2 velxy = DIM == 3 ? __ffma2_rn(Cxy[2], make_float2(dd[2][a2], dd[2][a2]), h1xy) : h1xy;
+                const float2 bxy = __ffma2_rn(Wt, velxy, magic2);
+                const int32_t sx = __float_as_int(bxy.x) - kMagicBits, sy = __float_as_int(bxy.y) - kMagicBits;
+                rest[1] -= sx;
+                rest[2] -= sy;
+                atomicAdd(&sacc[1 * Hl::SIZE + at], sx);
+                atomicAdd(&sacc[2 * Hl::SIZE + at], sy);
+                if constexpr (DIM == 3) {
+                    const float velz = __fmaf_rn(C[8], dd[2][a2], h1z);
+                    const int32_t sz = rint_mul(Wt.x, velz);
+                    rest[3] -= sz;
+                    atomicAdd(&sacc[3 * Hl::SIZE + at], sz);
                 }
             }
         }
