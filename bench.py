@@ -34,6 +34,31 @@ WORKLOAD = "blobs3d: 3D quadratic B-spline MPM step, 256^3 nodes, 16,777,216 par
 LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2g; grid update; g2p + copy
 
 
+# DRAM traffic per particle (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by the
+# particles it processed) from the ncu capture summarised in profiles/p2g_g2p_full_blobs3d_2M.md, taken on
+# the 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
+# Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
+MEASURED_TRAFFIC = {
+    "p2g": {"bytes_per_particle": 79.3, "files": ("p2g.cu", "common.cuh"),
+            "sha256": "a06af81c541373b3322fee9409a914292f3d969a333be188eb2955e15d5a12b6"
+                      "621333145496c650c4107b3e7b4d5f602d54992a0e5932e19969ad1a16504ed2"},
+    "g2p": {"bytes_per_particle": 77.2, "files": ("grid_g2p.cu", "common.cuh"),
+            "sha256": "1e7ec50beadeaa05265a5b418bc1c6229a28ba3a8d235415d0875e424b3f7995"
+                      "621333145496c650c4107b3e7b4d5f602d54992a0e5932e19969ad1a16504ed2"},
+}
+
+
+def measured_traffic(kernel: str, n: int):
+    """Bytes per launch of `kernel` for n particles, or None if not measured on these sources."""
+    rec = MEASURED_TRAFFIC.get(kernel)
+    if rec is None:
+        return None
+    import hashlib
+    csrc = os.path.join(ROOT, "material_point_particle_gb300", "csrc")
+    digest = "".join(hashlib.sha256(open(os.path.join(csrc, f), "rb").read()).hexdigest() for f in rec["files"])
+    return round(rec["bytes_per_particle"] * n) if digest == rec["sha256"] else None
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -203,7 +228,7 @@ def run_ours(args, rank, world, local):
     achieved = alg_bytes[dom] / (mean_ms[names.index(dom)] * 1e-3) / 1e9
     step_bytes = n * 160.0 + touched * 64.0
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(dom, n), "peak_kind": peak_kind,
                 "step_frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4)}
     # the transfer alone (P2G + grid update + G2P, binning reported apart):
     # 136 B per particle and 64 B per touched node must move
