@@ -182,28 +182,66 @@ __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, co
 // The CTA zeroes the tile's halo accumulators, every thread scatters its
 // particles with shared atomics, and the CTA adds each nonzero node to the
 // grid once (neighbouring tiles overlap on the halo, so the flush adds).
+// Where one work item's particles sit in perm.
+struct SliceMeta {
+    uint32_t tile, beg, cnt;
+};
+
+__device__ __forceinline__ SliceMeta slice_meta(const uint32_t *slices, const uint32_t *start, uint32_t s) {
+    SliceMeta m;
+    m.tile = slices[2 * (size_t)s];
+    m.beg = start[m.tile] + slices[2 * (size_t)s + 1];
+    m.cnt = min((uint32_t)kSliceParticles, start[m.tile + 1] - m.beg);
+    return m;
+}
+
 template <int DIM, int T, typename AccT>
-__global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm,
-                                                           const uint32_t *__restrict__ slices,
-                                                           const uint32_t *__restrict__ start,
-                                                           uint32_t *__restrict__ status, AccT *__restrict__ acc) {
+__global__ void __launch_bounds__(kP2GThreads, 3) k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm,
+                                                              const uint32_t *__restrict__ slices,
+                                                              const uint32_t *__restrict__ start,
+                                                              uint32_t *__restrict__ status, AccT *__restrict__ acc) {
     using St = Stencil<DIM>;
     using Hl = Halo<DIM, T>;
     using Fl = P2GFields<DIM>;
+    constexpr int NQ = kSliceParticles / kP2GThreads;
     __shared__ int32_t sacc[St::NC * Hl::SIZE];
     __shared__ float sbuf[2 * Fl::NF * kP2GThreads];
     const Prefetch<Fl::NF, kP2GThreads> pf{sbuf};
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
     const uint32_t nslices = status[MPM_ST_N_SLICES];
+    uint32_t *work = &status[MPM_ST_WORK_P2G];
     __shared__ uint32_t item_sh;
-    uint32_t next = 0;
-    for (uint32_t s = grab_item(&status[MPM_ST_WORK_P2G], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
-        next = ask_item(&status[MPM_ST_WORK_P2G]);
-        const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
-        const uint32_t beg = start[t] + first;
-        const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
+    auto issue = [&](int stage, uint32_t pid) {
+#pragma unroll
+        for (int f = 0; f < Fl::NF; ++f) cp_async4(pf.at(stage, f), Fl::src(p, f) + pid);
+    };
+    // Items are taken two ahead: while slice s is scattered, the next one's
+    // place in perm, its first perm entries and its first records are
+    // already on their way (the record copies go to the other stage of the
+    // per-thread double buffer during s's last round).
+    uint32_t s = grab_item(work, &item_sh);
+    uint32_t s_next = grab_item(work, &item_sh);
+    SliceMeta cur{0, 0, 0};
+    if (s < nslices) cur = slice_meta(slices, start, s);
+    int stage = 0;
+    if (s < nslices && threadIdx.x < cur.cnt) issue(0, perm[cur.beg + threadIdx.x]);
+    cp_async_commit();
+    while (s < nslices) {
+        const uint32_t s_after = ask_item(work);
+        SliceMeta nx{0, 0, 0};
+        uint32_t pid_nx = 0;
+        if (s_next < nslices) {
+            nx = slice_meta(slices, start, s_next);
+            if (threadIdx.x < nx.cnt) pid_nx = perm[nx.beg + threadIdx.x];
+        }
+        uint32_t pids[NQ];
+#pragma unroll
+        for (int q = 1; q < NQ; ++q) {
+            const uint32_t r = threadIdx.x + q * kP2GThreads;
+            pids[q] = r < cur.cnt ? perm[cur.beg + r] : 0u;
+        }
         int o[3];
-        tile_origin(g, t, o);
+        tile_origin(g, cur.tile, o);
         for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
             int hx, hy, hz, idx;
             Hl::node(h, hx, hy, hz, idx);
@@ -212,18 +250,6 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
         }
         __syncthreads();
         uint32_t bad = 0;
-        // each thread's particles r, r + 256, ...: the next one's record is
-        // copied into shared memory (cp.async) while the current one scatters
-        uint32_t pids[kSliceParticles / kP2GThreads];
-#pragma unroll
-        for (int q = 0; q < kSliceParticles / kP2GThreads; ++q) {
-            const uint32_t r = threadIdx.x + q * kP2GThreads;
-            pids[q] = r < cnt ? perm[beg + r] : 0u;
-        }
-        auto issue = [&](int stage, uint32_t pid) {
-#pragma unroll
-            for (int f = 0; f < Fl::NF; ++f) cp_async4(pf.at(stage, f), Fl::src(p, f) + pid);
-        };
         // every nonzero halo node added to the grid once (and, if `clear`,
         // reset to zero for the rest of the slice)
         auto flush = [&](bool clear) {
@@ -246,22 +272,27 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
                 }
             }
         };
-        if (threadIdx.x < cnt) issue(0, pids[0]);
-        cp_async_commit();
+        const uint32_t rounds = (cur.cnt + kP2GThreads - 1) / kP2GThreads;
 #pragma unroll
-        for (int q = 0; q < kSliceParticles / kP2GThreads; ++q) {
+        for (int q = 0; q < NQ; ++q) {
+            if ((uint32_t)q >= rounds) break;
             const uint32_t r = threadIdx.x + q * kP2GThreads;
-            if (q + 1 < kSliceParticles / kP2GThreads && r + kP2GThreads < cnt) issue((q + 1) & 1, pids[q + 1]);
+            if ((uint32_t)q + 1 < rounds) {
+                if (r + kP2GThreads < cur.cnt) issue(stage ^ 1, pids[q + 1]);
+            } else if (s_next < nslices && threadIdx.x < nx.cnt) {
+                issue(stage ^ 1, pid_nx);
+            }
             cp_async_commit();
             cp_async_wait<1>();
-            if (r < cnt) {
-                const int stage = q & 1;
-                auto rec = [&](int f) { return *pf.at(stage, f); };
+            if (r < cur.cnt) {
+                const int st = stage;
+                auto rec = [&](int f) { return *pf.at(st, f); };
                 if (!scatter_fixed<DIM, T>(g, rec, o, sacc)) ++bad;
             }
+            stage ^= 1;
             // int32 halo accumulators: at most kFlushParticles shares of
             // magnitude below 2^22 reach one node between two flushes
-            if ((q + 1) * kP2GThreads == kFlushParticles && cnt > (uint32_t)kFlushParticles) {
+            if ((q + 1) * kP2GThreads == kFlushParticles && cur.cnt > (uint32_t)kFlushParticles) {
                 __syncthreads();
                 flush(true);
                 __syncthreads();
@@ -273,8 +304,11 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_fixed(GridP g, PartsF p, co
         }
         __syncthreads();
         flush(false);
-        __syncthreads();
+        s = s_next;
+        cur = nx;
+        s_next = publish_item(s_after, &item_sh);
     }
+    cp_async_wait<0>();
 }
 
 // Float-atomic P2G (comparison variant: fp32 adds, order dependent).
