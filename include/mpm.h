@@ -211,7 +211,9 @@ mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *p
  * tile by tile in bin order, each P2G work item (a slice of up to 1024
  * consecutive perm entries of one tile) to the same range of out, but with
  * the slice reordered: stably sorted by the bank class of the particle's base
- * cell (key & 31), then dealt out column by column over rounds of 32 (lane l
+ * cell (with in-tile cell coordinates lx, ly, lz from the key and H = tile + 2,
+ * class = (lx + H*ly + H*H*lz) mod 32), then dealt out column by column over
+ * rounds of 32 (lane l
  * of R = ceil(cnt/32) rounds holds sorted entries cum(l) .. cum(l+1) - 1 with
  * cum(l) = l*R - max(0, l - L), L = cnt - 32*(R - 1), and entry cum(l) + rho
  * goes to slice place rho*32 + l).  Particles 32 apart in a round then sit in

@@ -4,6 +4,8 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/mpm.h"
@@ -162,6 +164,23 @@ __device__ __forceinline__ uint32_t publish_item(uint32_t next, uint32_t *sh) {
     return *sh;
 }
 
+// Compile-time loop: f(std::integral_constant<int, i>) for i = 0 .. N-1.
+template <typename F, int... I>
+__device__ __forceinline__ void static_for_impl(F &f, std::integer_sequence<int, I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+    static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
+
+// Shared-memory add without a result, at a constant byte offset from a
+// shared address.
+template <int OFF>
+__device__ __forceinline__ void red_shared_add(uint32_t base, int32_t v) {
+    asm volatile("red.shared.add.s32 [%0+%1], %2;" ::"r"(base), "n"(OFF), "r"(v));
+}
+
 // Asynchronous 4-byte global -> shared copies (cp.async), grouped per thread.
 __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
     const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);
@@ -225,5 +244,39 @@ struct Halo {
         idx = hx + hy * SY + hz * SZ;
     }
 };
+
+// Compact shared-memory halo of one tile: (T+2)^dim nodes, x fastest, no
+// padding (row pitch H, plane pitch H^2), channel c at c * NODES.  Node
+// (hx, hy, hz) sits in bank (hx + H hy + H^2 hz) mod 32, so particles whose
+// base cells have different bank classes (cell_class) add to, or read, a given
+// stencil node in different banks.
+template <int DIM, int T>
+struct HaloU {
+    static constexpr int H = T + 2;
+    static constexpr int SY = H;
+    static constexpr int SZ = DIM == 3 ? H * H : 0;
+    static constexpr int NODES = DIM == 3 ? H * H * H : H * H;
+    static constexpr int SIZE = NODES;
+    // offset of stencil node a = a0*9 + a1*3 + a2 (3D) or a0*3 + a1 (2D)
+    __device__ static constexpr int off(int a) {
+        return DIM == 3 ? (a / 9) + (a / 3 % 3) * SY + (a % 3) * SZ : (a / 3) + (a % 3) * SY;
+    }
+    __device__ static void node(int h, int &hx, int &hy, int &hz) {
+        hx = h % H;
+        hy = (h / H) % H;
+        hz = DIM == 3 ? h / (H * H) : 0;
+    }
+};
+
+// Bank class of a base cell from the in-tile bits of its key
+// (local = lx + T ly + T^2 lz): its compact-halo offset modulo 32.
+template <int DIM, int T>
+__device__ __forceinline__ uint32_t cell_class(uint32_t key) {
+    constexpr int H = T + 2;
+    constexpr int LOG = T == 4 ? 2 : 3;
+    const uint32_t lx = key & (T - 1), ly = (key >> LOG) & (T - 1);
+    const uint32_t lz = DIM == 3 ? (key >> (2 * LOG)) & (T - 1) : 0u;
+    return (lx + H * ly + H * H * lz) & 31u;
+}
 
 }  // namespace mpm

@@ -123,14 +123,11 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
     if (q.id && p.id) q.id[dst] = p.id[src];
 }
 
-// Velocity halo of one tile in shared memory, padded as the P2G accumulators:
-// the x and y components side by side (one 64-bit word per node, so that one
-// load feeds a packed fp32x2 fma), z (3D) in its own array.
+// Velocity halo of one tile in shared memory, in the compact layout of the
+// P2G accumulators (HaloU), one array per component.
 template <int DIM, int T>
 struct VelHalo {
-    using Hl = Halo<DIM, T>;
-    float2 *xy;
-    float *z;
+    float *x, *y, *z;
 };
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
@@ -150,7 +147,7 @@ template <int DIM, int T, bool SORTED, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
                                            uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
                                            float dt, float c4) {
-    using Hl = Halo<DIM, T>;
+    using Hl = HaloU<DIM, T>;
     float x[DIM], f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
 #pragma unroll
@@ -177,7 +174,7 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
             WE[l][a] = f2(we[l][a]);
         }
     float vn[DIM], Bm[DIM][DIM];
-    const float2 *vxy = sv.xy + hb;
+    const float *vx = sv.x + hb, *vy = sv.y + hb;
     if constexpr (DIM == 3) {
         // x and y packed
         float2 Y[3], Ye[3], Yq[3];
@@ -188,7 +185,10 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
             for (int a1 = 0; a1 < 3; ++a1) {
                 float2 t[3];
 #pragma unroll
-                for (int a2 = 0; a2 < 3; ++a2) t[a2] = vxy[a0 + a1 * Hl::SY + a2 * Hl::SZ];
+                for (int a2 = 0; a2 < 3; ++a2) {
+                    const int i = a0 + a1 * Hl::SY + a2 * Hl::SZ;
+                    t[a2] = make_float2(vx[i], vy[i]);
+                }
                 Z[a1] = sum3x2(W[2], t);
                 Zq[a1] = sum3x2(WE[2], t);
             }
@@ -233,7 +233,7 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
         for (int a0 = 0; a0 < 3; ++a0) {
             float2 t[3];
 #pragma unroll
-            for (int a1 = 0; a1 < 3; ++a1) t[a1] = vxy[a0 + a1 * Hl::SY];
+            for (int a1 = 0; a1 < 3; ++a1) t[a1] = make_float2(vx[a0 + a1 * Hl::SY], vy[a0 + a1 * Hl::SY]);
             Y[a0] = sum3x2(W[1], t);
             Ye[a0] = sum3x2(WE[1], t);
         }
@@ -260,9 +260,9 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
 }
 
 // Interleaved slices.  The sorted output keeps each slice in its place but
-// orders it by the bank class of the particles' base cells (the low five bits
-// of the cell key: x + 4y + 16(z mod 2) in a 4^3 tile, x + 8(y mod 4) in an
-// 8^2 tile), stable in bin order, then deals the class-sorted entries out
+// orders it by the bank class of the particles' base cells (cell_class: the
+// cell's offset in the compact halo modulo 32, x + 6y + 36z in a 4^3 tile,
+// x + 10y in an 8^2 tile), stable in bin order, then deals the class-sorted entries out
 // column by column over rounds of 32: with R = ceil(cnt / 32) rounds and
 // L = cnt - 32 (R - 1) lanes in the last one, lane l holds sorted entries
 // [cum(l), cum(l + 1)), cum(l) = l R - max(0, l - L), and entry
@@ -297,16 +297,15 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                                                      const uint32_t *__restrict__ slices,
                                                      const uint32_t *__restrict__ start,
                                                      uint32_t *__restrict__ status, float dt, float c4) {
-    using Hl = Halo<DIM, T>;
+    using Hl = HaloU<DIM, T>;
     constexpr int NQ = kSliceParticles / kP2GThreads;
     constexpr int NWARP = kP2GThreads / 32;
     static_assert(NQ * NWARP == 32, "one warp-scan lane per (round, warp)");
     // in place: per-thread double buffer of x; sorted: x, m, id of the whole slice
     constexpr int NF = SORTED ? DIM + 2 : DIM;
     constexpr int BUF = SORTED ? NF * kSliceParticles : 2 * NF * kP2GThreads;
-    __shared__ float2 sv_xy[Hl::SIZE];
-    __shared__ float sv_z[DIM == 3 ? Hl::SIZE : 1];
-    const VelHalo<DIM, T> sv{sv_xy, sv_z};
+    __shared__ float sv_x[Hl::SIZE], sv_y[Hl::SIZE], sv_z[DIM == 3 ? Hl::SIZE : 1];
+    const VelHalo<DIM, T> sv{sv_x, sv_y, sv_z};
     __shared__ float sbuf[BUF];
     // [(qi, warp)][class], rows padded to 33 words: the scan reads a column
     __shared__ uint32_t hist[SORTED ? NQ * NWARP * 33 : 1];
@@ -346,13 +345,14 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             cp_async_commit();
         }
         for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
-            int hx, hy, hz, idx;
-            Hl::node(h, hx, hy, hz, idx);
+            int hx, hy, hz;
+            Hl::node(h, hx, hy, hz);
             const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
             const bool in = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
             const int64_t node = in ? node_index(g, gx, gy, gz) : 0;
-            sv_xy[idx] = in ? make_float2(vel[node], vel[g.nodes + node]) : make_float2(0.f, 0.f);
-            if (DIM == 3) sv_z[idx] = in ? vel[2 * g.nodes + node] : 0.f;
+            sv_x[h] = in ? vel[node] : 0.f;
+            sv_y[h] = in ? vel[g.nodes + node] : 0.f;
+            if (DIM == 3) sv_z[h] = in ? vel[2 * g.nodes + node] : 0.f;
         }
         if constexpr (SORTED) {
             // stable counting sort of the slice by bank class: counts per
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
 #pragma unroll
             for (int qi = 0; qi < NQ; ++qi) {
                 const uint32_t r = threadIdx.x + qi * kP2GThreads;
-                cls[qi] = r < cnt ? (key[pids[qi]] & 31u) : 32u;
+                cls[qi] = r < cnt ? cell_class<DIM, T>(key[pids[qi]]) : 32u;
             }
             for (int i = threadIdx.x; i < NQ * NWARP * 33; i += blockDim.x) hist[i] = 0;
             __syncthreads();

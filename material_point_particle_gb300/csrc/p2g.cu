@@ -21,11 +21,6 @@
 
 namespace mpm {
 
-// Particles whose shares may meet in one int32 halo accumulator: 512 shares
-// of magnitude below 2^22 sum to less than 2^31.
-constexpr int kFlushParticles = 512;
-static_assert(kFlushParticles % kP2GThreads == 0, "flush point on a round boundary");
-
 // Share encode: rint(a * b) for |a*b| < 2^22, exact product rounded once (RNE).
 __device__ __forceinline__ int32_t rint_mul(float a, float b) {
     return __float_as_int(__fmaf_rn(a, b, kMagic)) - kMagicBits;
@@ -38,10 +33,9 @@ __device__ __forceinline__ int32_t rint_f(float a) { return __float_as_int(__fad
 // are formed (the arithmetic the oracle states).  Returns false (and adds
 // nothing) when the particle is out of range.
 // rec(f) reads field f of the particle (x[dim], v[dim], C[dim*dim], m).
-template <int DIM, int T, typename Rec>
-__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], int32_t *sacc) {
+template <int DIM, int T, typename Hl, typename Rec>
+__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo) {
     using St = Stencil<DIM>;
-    using Hl = Halo<DIM, T>;
     float f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
     float xs[DIM];
@@ -84,46 +78,52 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     const float2 magic2 = make_float2(kMagic, kMagic);
     float2 Cxy[3] = {make_float2(C[0], C[DIM + 0]), make_float2(C[1], C[DIM + 1]), make_float2(0.f, 0.f)};
     if constexpr (DIM == 3) Cxy[2] = make_float2(C[2], C[5]);
-#pragma unroll
-    for (int a0 = 0; a0 < 3; ++a0) {
+    // the shared atomics address the halo from one base with constant offsets
+    const uint32_t base = halo + 4u * (uint32_t)hb;
+    static_for<3>([&](auto A0) {
+        constexpr int a0 = decltype(A0)::value;
         const float Wx = __fmul_rn(w[0][a0], Mt);
         const float2 h0xy = __ffma2_rn(Cxy[0], make_float2(dd[0][a0], dd[0][a0]), make_float2(v[0], v[1]));
         float h0z = 0.f;
         if constexpr (DIM == 3) h0z = __fmaf_rn(C[6], dd[0][a0], v[2]);
-#pragma unroll
-        for (int a1 = 0; a1 < 3; ++a1) {
+        static_for<3>([&](auto A1) {
+            constexpr int a1 = decltype(A1)::value;
             const float2 Wxy = __fmul2_rn(make_float2(Wx, Wx), make_float2(w[1][a1], w[1][a1]));
             const float2 h1xy = __ffma2_rn(Cxy[1], make_float2(dd[1][a1], dd[1][a1]), h0xy);
             float h1z = 0.f;
             if constexpr (DIM == 3) h1z = __fmaf_rn(C[7], dd[1][a1], h0z);
-#pragma unroll
-            for (int a2 = 0; a2 < (DIM == 3 ? 3 : 1); ++a2) {
-                const int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
-                if (a == St::CENTRE) continue;
-                const float2 Wt = DIM == 3 ? __fmul2_rn(Wxy, make_float2(w[2][a2], w[2][a2])) : Wxy;
-                const int at = hb + Hl::off(a);
-                const int32_t sm = rint_f(Wt.x);
-                rest[0] -= sm;
-                atomicAdd(&sacc[at], sm);
-                const float2 velxy = DIM == 3 ? __ffma2_rn(Cxy[2], make_float2(dd[2][a2], dd[2][a2]), h1xy) : h1xy;
-                const float2 bxy = __ffma2_rn(Wt, velxy, magic2);
-                const int32_t sx = __float_as_int(bxy.x) - kMagicBits, sy = __float_as_int(bxy.y) - kMagicBits;
-                rest[1] -= sx;
-                rest[2] -= sy;
-                atomicAdd(&sacc[1 * Hl::SIZE + at], sx);
-                atomicAdd(&sacc[2 * Hl::SIZE + at], sy);
-                if constexpr (DIM == 3) {
-                    const float velz = __fmaf_rn(C[8], dd[2][a2], h1z);
-                    const int32_t sz = rint_mul(Wt.x, velz);
-                    rest[3] -= sz;
-                    atomicAdd(&sacc[3 * Hl::SIZE + at], sz);
+            static_for<(DIM == 3 ? 3 : 1)>([&](auto A2) {
+                constexpr int a2 = decltype(A2)::value;
+                constexpr int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
+                if constexpr (a != St::CENTRE) {
+                    constexpr int off = 4 * Hl::off(a);
+                    const float2 Wt = DIM == 3 ? __fmul2_rn(Wxy, make_float2(w[2][a2], w[2][a2])) : Wxy;
+                    const int32_t sm = rint_f(Wt.x);
+                    rest[0] -= sm;
+                    red_shared_add<off>(base, sm);
+                    const float2 velxy =
+                        DIM == 3 ? __ffma2_rn(Cxy[2], make_float2(dd[2][a2], dd[2][a2]), h1xy) : h1xy;
+                    const float2 bxy = __ffma2_rn(Wt, velxy, magic2);
+                    const int32_t sx = __float_as_int(bxy.x) - kMagicBits, sy = __float_as_int(bxy.y) - kMagicBits;
+                    rest[1] -= sx;
+                    rest[2] -= sy;
+                    red_shared_add<off + 4 * Hl::SIZE>(base, sx);
+                    red_shared_add<off + 8 * Hl::SIZE>(base, sy);
+                    if constexpr (DIM == 3) {
+                        const float velz = __fmaf_rn(C[8], dd[2][a2], h1z);
+                        const int32_t sz = rint_mul(Wt.x, velz);
+                        rest[3] -= sz;
+                        red_shared_add<off + 12 * Hl::SIZE>(base, sz);
+                    }
                 }
-            }
-        }
-    }
-    const int ac = hb + Hl::off(St::CENTRE);
-#pragma unroll
-    for (int c = 0; c < St::NC; ++c) atomicAdd(&sacc[c * Hl::SIZE + ac], rest[c]);
+            });
+        });
+    });
+    constexpr int offc = 4 * Hl::off(St::CENTRE);
+    red_shared_add<offc>(base, rest[0]);
+    red_shared_add<offc + 4 * Hl::SIZE>(base, rest[1]);
+    red_shared_add<offc + 8 * Hl::SIZE>(base, rest[2]);
+    if constexpr (DIM == 3) red_shared_add<offc + 12 * Hl::SIZE>(base, rest[3]);
     return true;
 }
 
@@ -195,75 +195,68 @@ __device__ __forceinline__ SliceMeta slice_meta(const uint32_t *slices, const ui
     return m;
 }
 
+// One warp per work item (a slice of at most 1024 binned particles of one
+// tile), so no CTA barrier couples the warps: each warp owns a compact halo
+// of the tile's (T+2)^dim nodes x (dim+1) int32 accumulators and a double
+// buffer for its lanes' particle records.  Per item: 32 particles a round,
+// the next round's records copied into shared memory (cp.async) while the
+// current one scatters; every 512 particles and at the end the warp adds each
+// nonzero halo entry to the grid with one global atomic and clears it
+// (neighbouring tiles overlap on the halo, so the flush adds).  Particles
+// stored in bank-class interleaved order (the sorted G2P) put the 32 lanes of
+// a round in different banks.
+constexpr int kP2GWarps = kP2GThreads / 32;
+
 template <int DIM, int T, typename AccT>
 __global__ void __launch_bounds__(kP2GThreads, 3) k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm,
                                                               const uint32_t *__restrict__ slices,
                                                               const uint32_t *__restrict__ start,
                                                               uint32_t *__restrict__ status, AccT *__restrict__ acc) {
     using St = Stencil<DIM>;
-    using Hl = Halo<DIM, T>;
+    using Hl = HaloU<DIM, T>;
     using Fl = P2GFields<DIM>;
-    constexpr int NQ = kSliceParticles / kP2GThreads;
-    __shared__ int32_t sacc[St::NC * Hl::SIZE];
-    __shared__ float sbuf[2 * Fl::NF * kP2GThreads];
-    const Prefetch<Fl::NF, kP2GThreads> pf{sbuf};
+    constexpr int HW = St::NC * Hl::NODES;  // halo words per warp
+    __shared__ __align__(16) int32_t shalo[kP2GWarps][HW];
+    __shared__ float sbuf[kP2GWarps][2 * Fl::NF * 32];
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    int32_t *wh = shalo[warp];
+    float *wb = sbuf[warp];
+    const uint32_t halo = (uint32_t)__cvta_generic_to_shared(wh);
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     uint32_t *work = &status[MPM_ST_WORK_P2G];
-    __shared__ uint32_t item_sh;
+    for (int i = lane; i < HW; i += 32) wh[i] = 0;
+    __syncwarp();
+    auto at = [&](int stage, int f) { return wb + (stage * Fl::NF + f) * 32 + lane; };
     auto issue = [&](int stage, uint32_t pid) {
 #pragma unroll
-        for (int f = 0; f < Fl::NF; ++f) cp_async4(pf.at(stage, f), Fl::src(p, f) + pid);
+        for (int f = 0; f < Fl::NF; ++f) cp_async4(at(stage, f), Fl::src(p, f) + pid);
     };
-    // Items are taken two ahead: while slice s is scattered, the next one's
-    // place in perm, its first perm entries and its first records are
-    // already on their way (the record copies go to the other stage of the
-    // per-thread double buffer during s's last round).
-    uint32_t s = grab_item(work, &item_sh);
-    uint32_t s_next = grab_item(work, &item_sh);
-    SliceMeta cur{0, 0, 0};
-    if (s < nslices) cur = slice_meta(slices, start, s);
-    int stage = 0;
-    if (s < nslices && threadIdx.x < cur.cnt) issue(0, perm[cur.beg + threadIdx.x]);
-    cp_async_commit();
+    uint32_t s = 0;
+    if (lane == 0) s = atomicAdd(work, 1u);
+    s = __shfl_sync(0xFFFFFFFFu, s, 0);
     while (s < nslices) {
-        const uint32_t s_after = ask_item(work);
-        SliceMeta nx{0, 0, 0};
-        uint32_t pid_nx = 0;
-        if (s_next < nslices) {
-            nx = slice_meta(slices, start, s_next);
-            if (threadIdx.x < nx.cnt) pid_nx = perm[nx.beg + threadIdx.x];
-        }
-        uint32_t pids[NQ];
-#pragma unroll
-        for (int q = 1; q < NQ; ++q) {
-            const uint32_t r = threadIdx.x + q * kP2GThreads;
-            pids[q] = r < cur.cnt ? perm[cur.beg + r] : 0u;
-        }
+        const uint32_t ask = lane == 0 ? atomicAdd(work, 1u) : 0u;  // the next item, used at the end
+        const uint32_t t = slices[2 * (size_t)s];
+        const uint32_t beg = start[t] + slices[2 * (size_t)s + 1];
+        const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
         int o[3];
-        tile_origin(g, cur.tile, o);
-        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
-            int hx, hy, hz, idx;
-            Hl::node(h, hx, hy, hz, idx);
-#pragma unroll
-            for (int c = 0; c < St::NC; ++c) sacc[c * Hl::SIZE + idx] = 0;
-        }
-        __syncthreads();
-        uint32_t bad = 0;
-        // every nonzero halo node added to the grid once (and, if `clear`,
-        // reset to zero for the rest of the slice)
-        auto flush = [&](bool clear) {
-            for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
-                int hx, hy, hz, idx;
-                Hl::node(h, hx, hy, hz, idx);
+        tile_origin(g, t, o);
+        // every nonzero halo entry added to the grid once, and cleared
+        auto flush = [&]() {
+            __syncwarp();
+            for (int h = lane; h < Hl::NODES; h += 32) {
+                int hx, hy, hz;
+                Hl::node(h, hx, hy, hz);
                 const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
-                if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
+                const bool on = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
                 const int64_t node = node_index(g, gx, gy, gz);
 #pragma unroll
                 for (int c = 0; c < St::NC; ++c) {
-                    const int32_t val = sacc[c * Hl::SIZE + idx];
+                    const int32_t val = wh[c * Hl::NODES + h];
                     if (val == 0) continue;
-                    if (clear) sacc[c * Hl::SIZE + idx] = 0;
+                    wh[c * Hl::NODES + h] = 0;
+                    if (!on) continue;
                     if constexpr (sizeof(AccT) == 8)
                         atomicAdd(reinterpret_cast<unsigned long long *>(acc + c * g.nodes + node),
                                   (unsigned long long)(long long)val);
@@ -271,42 +264,35 @@ __global__ void __launch_bounds__(kP2GThreads, 3) k_p2g_fixed(GridP g, PartsF p,
                         atomicAdd(reinterpret_cast<int *>(acc + c * g.nodes + node), val);
                 }
             }
+            __syncwarp();
         };
-        const uint32_t rounds = (cur.cnt + kP2GThreads - 1) / kP2GThreads;
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            if ((uint32_t)q >= rounds) break;
-            const uint32_t r = threadIdx.x + q * kP2GThreads;
-            if ((uint32_t)q + 1 < rounds) {
-                if (r + kP2GThreads < cur.cnt) issue(stage ^ 1, pids[q + 1]);
-            } else if (s_next < nslices && threadIdx.x < nx.cnt) {
-                issue(stage ^ 1, pid_nx);
-            }
+        uint32_t bad = 0;
+        const uint32_t rounds = (cnt + 31) / 32;
+        if (lane < cnt) issue(0, perm[beg + lane]);
+        cp_async_commit();
+        int stage = 0;
+        for (uint32_t q = 0; q < rounds; ++q) {
+            const uint32_t r = q * 32 + lane;
+            if (q + 1 < rounds && r + 32 < cnt) issue(stage ^ 1, perm[beg + r + 32]);
             cp_async_commit();
             cp_async_wait<1>();
-            if (r < cur.cnt) {
+            if (r < cnt) {
                 const int st = stage;
-                auto rec = [&](int f) { return *pf.at(st, f); };
-                if (!scatter_fixed<DIM, T>(g, rec, o, sacc)) ++bad;
+                auto rec = [&](int f) { return *at(st, f); };
+                if (!scatter_fixed<DIM, T, Hl>(g, rec, o, halo)) ++bad;
             }
             stage ^= 1;
-            // int32 halo accumulators: at most kFlushParticles shares of
-            // magnitude below 2^22 reach one node between two flushes
-            if ((q + 1) * kP2GThreads == kFlushParticles && cur.cnt > (uint32_t)kFlushParticles) {
-                __syncthreads();
-                flush(true);
-                __syncthreads();
-            }
+            // int32 halo accumulators: at most 512 shares of magnitude below
+            // 2^22 reach one entry between two flushes
+            if ((q + 1) % 16 == 0 && q + 1 < rounds) flush();
         }
-        if (bad) {
+        flush();
+        bad = __reduce_add_sync(0xFFFFFFFFu, bad);
+        if (bad && lane == 0) {
             atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
             set_flag(status, MPM_E_BOUND);
         }
-        __syncthreads();
-        flush(false);
-        s = s_next;
-        cur = nx;
-        s_next = publish_item(s_after, &item_sh);
+        s = __shfl_sync(0xFFFFFFFFu, ask, 0);
     }
     cp_async_wait<0>();
 }

@@ -340,10 +340,19 @@ def test_workload_step_matches_oracle(name, kw):
 SLICE = 1024   # particles per work item (a slice of one tile)
 
 
-def sorted_output_order(key, perm, tile_count, n_valid):
+def cell_class(key, dim, tile):
+    """Bank class of a base cell: its offset in the compact (tile+2)^dim halo, mod 32."""
+    key = key.astype(np.int64)
+    h, lg = tile + 2, int(np.log2(tile))
+    lx, ly = key & (tile - 1), (key >> lg) & (tile - 1)
+    lz = (key >> (2 * lg)) & (tile - 1) if dim == 3 else 0
+    return (lx + h * ly + h * h * lz) & 31
+
+
+def sorted_output_order(key, perm, tile_count, n_valid, dim=3, tile=4):
     """Where mpm_g2p_sorted puts each particle: slice by slice in bin order,
-    each slice stably sorted by bank class (key & 31) and dealt out column by
-    column over rounds of 32."""
+    each slice stably sorted by bank class and dealt out column by column over
+    rounds of 32."""
     out = perm.astype(np.int64).copy()
     start = np.concatenate([[0], np.cumsum(tile_count.astype(np.int64))])
     for t in np.nonzero(tile_count)[0]:
@@ -352,7 +361,7 @@ def sorted_output_order(key, perm, tile_count, n_valid):
             cnt = min(SLICE, int(tile_count[t]) - first)
             idx = perm[beg:beg + cnt].astype(np.int64)
             srt = np.empty(cnt, np.int64)
-            srt[np.argsort(key[idx] & 31, kind="stable")] = np.arange(cnt)
+            srt[np.argsort(cell_class(key[idx], dim, tile), kind="stable")] = np.arange(cnt)
             R = -(-cnt // 32)
             Lf = cnt - 32 * (R - 1)
             lane = np.where(srt < Lf * R, srt // R, Lf + (srt - Lf * R) // max(R - 1, 1))
