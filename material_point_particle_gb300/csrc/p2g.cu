@@ -84,13 +84,13 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
         constexpr int a0 = decltype(A0)::value;
         const float Wx = __fmul_rn(w[0][a0], Mt);
         const float2 h0xy = __ffma2_rn(Cxy[0], make_float2(dd[0][a0], dd[0][a0]), make_float2(v[0], v[1]));
-        float h0z = 0.f;
+        [[maybe_unused]] float h0z = 0.f;
         if constexpr (DIM == 3) h0z = __fmaf_rn(C[6], dd[0][a0], v[2]);
         static_for<3>([&](auto A1) {
             constexpr int a1 = decltype(A1)::value;
             const float2 Wxy = __fmul2_rn(make_float2(Wx, Wx), make_float2(w[1][a1], w[1][a1]));
             const float2 h1xy = __ffma2_rn(Cxy[1], make_float2(dd[1][a1], dd[1][a1]), h0xy);
-            float h1z = 0.f;
+            [[maybe_unused]] float h1z = 0.f;
             if constexpr (DIM == 3) h1z = __fmaf_rn(C[7], dd[1][a1], h0z);
             static_for<(DIM == 3 ? 3 : 1)>([&](auto A2) {
                 constexpr int a2 = decltype(A2)::value;
