@@ -39,12 +39,12 @@ LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2
 # the 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
-    "p2g": {"bytes_per_particle": 79.3, "files": ("p2g.cu", "common.cuh"),
-            "sha256": "a06af81c541373b3322fee9409a914292f3d969a333be188eb2955e15d5a12b6"
-                      "621333145496c650c4107b3e7b4d5f602d54992a0e5932e19969ad1a16504ed2"},
-    "g2p": {"bytes_per_particle": 77.2, "files": ("grid_g2p.cu", "common.cuh"),
-            "sha256": "1e7ec50beadeaa05265a5b418bc1c6229a28ba3a8d235415d0875e424b3f7995"
-                      "621333145496c650c4107b3e7b4d5f602d54992a0e5932e19969ad1a16504ed2"},
+    "p2g": {"bytes_per_particle": 81.9, "files": ("p2g.cu", "common.cuh"),
+            "sha256": "098a72f38c248480137b7082b87285b56b829b7fc515cb580b41283b0021d3a5"
+                      "caa52acb850be6dfcc10664d1a0528e01c133bee3783931b11469d24af5c1ad8"},
+    "g2p": {"bytes_per_particle": 77.0, "files": ("grid_g2p.cu", "common.cuh"),
+            "sha256": "f80471f52ed8f0239e8d19733c7618c9d41075901ea8243834d5aa49b1d105e7"
+                      "caa52acb850be6dfcc10664d1a0528e01c133bee3783931b11469d24af5c1ad8"},
 }
 
 
