@@ -24,7 +24,7 @@
 // the same code sorts indices.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
-//   k_keys          key per particle, warp-aggregated tile histogram,
+//   k_keys          key per particle, tile histogram aggregated over runs,
 //                   out-of-domain count (int32 mode: per-cell counts)
 //   k_scan_reduce / k_scan_top / k_scan_final
 //                   exclusive scans of (count, P2G slices, active flag) over
@@ -47,9 +47,27 @@ namespace mpm {
 constexpr int kKeysUnroll = 4;   // particles per lane per iteration (loads in flight)
 
 // --------------------------------------------------------------------------
+// Tile-major cell key with the tile shape known at compile time.
+template <int DIM, int T>
+__device__ __forceinline__ uint32_t cell_key_t(const GridP &g, const int b[3]) {
+    constexpr int LOG = T == 4 ? 2 : 3;
+    uint32_t tile = 0, local = 0;
+#pragma unroll
+    for (int l = DIM - 1; l >= 0; --l) {
+        tile = tile * (uint32_t)g.nt[l] + ((uint32_t)b[l] >> LOG);
+        local = (local << LOG) | ((uint32_t)b[l] & (T - 1));
+    }
+    return (tile << (DIM * LOG)) | local;
+}
+
+// Key per particle; tile histogram aggregated over runs of equal buckets
+// among a warp's 32 consecutive particles (one atomic per run: particles
+// kept in bin order come in long runs).
+template <int DIM, int T>
 __global__ void __launch_bounds__(256) k_keys(GridP g, PartsF p, uint32_t *__restrict__ key,
                                               uint32_t *__restrict__ count, uint32_t *__restrict__ cellcount,
                                               uint32_t *__restrict__ status) {
+    constexpr int LOG = T == 4 ? 2 : 3;
     const int64_t n = p.n;
     const uint32_t lane = lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -57,39 +75,39 @@ __global__ void __launch_bounds__(256) k_keys(GridP g, PartsF p, uint32_t *__res
     constexpr int64_t kSpan = 32 * kKeysUnroll;
     for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kSpan; base < n;
          base += warps * kSpan) {
-        float xv[kKeysUnroll][3];
+        float xv[kKeysUnroll][DIM];
 #pragma unroll
         for (int u = 0; u < kKeysUnroll; ++u) {
             const int64_t i = base + u * 32 + lane;
 #pragma unroll
-            for (int l = 0; l < 3; ++l) xv[u][l] = (i < n && l < g.dim) ? p.x[l][i] : 0.f;
+            for (int l = 0; l < DIM; ++l) xv[u][l] = i < n ? p.x[l][i] : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < kKeysUnroll; ++u) {
             const int64_t i = base + u * 32 + lane;
-            uint32_t k = kKeyInvalid, bucket = 0xFFFFFFFFu;
+            uint32_t k = kKeyInvalid, bucket = bucket_invalid;
             if (i < n) {
                 int b[3] = {0, 0, 0};
                 float f;
                 bool ok = true;
 #pragma unroll
-                for (int l = 0; l < 3; ++l)
-                    if (l < g.dim) ok = base_frac(xv[u][l], g.inv_dx, g.n[l], b[l], f) && ok;
+                for (int l = 0; l < DIM; ++l) ok = base_frac(xv[u][l], g.inv_dx, g.n[l], b[l], f) && ok;
                 if (ok) {
-                    k = cell_key(g, b);
-                    bucket = k >> g.cpt_log2;
+                    k = cell_key_t<DIM, T>(g, b);
+                    bucket = k >> (DIM * LOG);
                     if (cellcount) atomicAdd(&cellcount[k], 1u);
-                } else {
-                    bucket = bucket_invalid;
                 }
                 key[i] = k;
             }
-            // warp-aggregated histogram: one atomic per distinct bucket in the warp
+            // runs of equal buckets: the head lane adds the run's length
             const uint32_t live = __ballot_sync(0xFFFFFFFFu, i < n);
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bucket) & live;
-            if (i < n && (peers & lanemask_lt()) == 0) {
-                atomicAdd(&count[bucket], (uint32_t)__popc(peers));
-                if (bucket == bucket_invalid) atomicAdd(&status[MPM_ST_N_OUTSIDE], (uint32_t)__popc(peers));
+            const uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, bucket, 1);
+            const uint32_t heads = __ballot_sync(0xFFFFFFFFu, i < n && (lane == 0 || prev != bucket));
+            if ((heads >> lane) & 1u) {
+                const uint32_t later = heads & ~((2u << lane) - 1u);   // heads after this lane (lane 31: none)
+                const uint32_t stop = later ? (uint32_t)(__ffs(later) - 1) : (uint32_t)(32 - __clz(live));
+                atomicAdd(&count[bucket], stop - lane);
+                if (bucket == bucket_invalid) atomicAdd(&status[MPM_ST_N_OUTSIDE], stop - lane);
             }
         }
     }
@@ -215,6 +233,7 @@ __device__ __forceinline__ uint32_t bucket_of(uint32_t k, int cpt_log2, uint32_t
 // Run heads (first index of a run) and tails (last index), each appended to
 // its bucket's range of `heads` / `tails` (a bucket has at most as many runs
 // as particles, so its range [start, start + count) has room).
+template <int DIM, int T>
 __global__ void __launch_bounds__(256) k_runs(GridP g, const uint32_t *__restrict__ key, int64_t n,
                                               const uint32_t *__restrict__ start, uint32_t *__restrict__ hcnt,
                                               uint32_t *__restrict__ tcnt, uint32_t *__restrict__ heads,
@@ -229,11 +248,11 @@ __global__ void __launch_bounds__(256) k_runs(GridP g, const uint32_t *__restric
 #pragma unroll
         for (int u = 0; u < kKeysUnroll; ++u) {
             const int64_t i = base + u * 32 + lane;
-            bk[u] = bucket_of(i < n ? key[i] : kKeyInvalid, g.cpt_log2, binv);
+            bk[u] = bucket_of(i < n ? key[i] : kKeyInvalid, (DIM * (T == 4 ? 2 : 3)), binv);
         }
         // the buckets just before and just after the span (lane 0 / lane 31 use them)
-        const uint32_t bprev = (lane == 0 && base > 0) ? bucket_of(key[base - 1], g.cpt_log2, binv) : binv;
-        const uint32_t bnext = (lane == 31 && base + kSpan < n) ? bucket_of(key[base + kSpan], g.cpt_log2, binv)
+        const uint32_t bprev = (lane == 0 && base > 0) ? bucket_of(key[base - 1], (DIM * (T == 4 ? 2 : 3)), binv) : binv;
+        const uint32_t bnext = (lane == 31 && base + kSpan < n) ? bucket_of(key[base + kSpan], (DIM * (T == 4 ? 2 : 3)), binv)
                                                                 : binv;
 #pragma unroll
         for (int u = 0; u < kKeysUnroll; ++u) {
@@ -608,22 +627,30 @@ mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const De
     const int threads = 256;
     const int64_t span = (int64_t)threads * kKeysUnroll;
     const int grid_p = (int)std::max<int64_t>(1, std::min<int64_t>((n + span - 1) / span, dev.sms * 8));
-    if (n > 0) k_keys<<<grid_p, threads, 0, st>>>(g, p, w.key, w.count, w.cellcount, w.status);
+    if (n > 0) {
+        if (g.dim == 3)
+            k_keys<3, 4><<<grid_p, threads, 0, st>>>(g, p, w.key, w.count, w.cellcount, w.status);
+        else
+            k_keys<2, 8><<<grid_p, threads, 0, st>>>(g, p, w.key, w.count, w.cellcount, w.status);
+    }
     const int64_t nblk = (nb + kScanBlock - 1) / kScanBlock;
     k_scan_reduce<<<(unsigned)nblk, kScanThreads, 0, st>>>(w.count, nb, (Tot3 *)w.partial);
     k_scan_top<<<1, kScanThreads, 0, st>>>((Tot3 *)w.partial, nblk, w.count, nb, w.status);
     k_scan_final<<<(unsigned)nblk, kScanThreads, 0, st>>>(w.count, nb, (const Tot3 *)w.partial, w.start, w.hcnt,
                                                           w.tcnt, w.active, w.slices);
     if (n > 0) {
-        k_runs<<<grid_p, threads, 0, st>>>(g, w.key, n, w.start, w.hcnt, w.tcnt, w.heads, w.tails);
+        if (g.dim == 3)
+            k_runs<3, 4><<<grid_p, threads, 0, st>>>(g, w.key, n, w.start, w.hcnt, w.tcnt, w.heads, w.tails);
+        else
+            k_runs<2, 8><<<grid_p, threads, 0, st>>>(g, w.key, n, w.start, w.hcnt, w.tcnt, w.heads, w.tails);
         k_sort_runs<<<dev.sms * 4, kSortWarps * 32, 0, st>>>(g, w.start, w.count, w.active, w.hcnt, w.heads,
                                                              w.tails, w.large_list, w.status);
         const int smem = 2 * (int)kSmemRuns * (int)sizeof(uint32_t);
         cudaFuncSetAttribute(k_sort_runs_large, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         k_sort_runs_large<<<dev.sms, kLargeThreads, smem, st>>>(w.start, w.hcnt, w.large_list, w.heads, w.tails,
                                                                 w.status);
-        k_emit<<<dev.sms * 4, 256, 0, st>>>(g, w.start, w.count, w.hcnt, w.heads, w.tails, w.slices, w.status,
-                                            w.perm);
+        k_emit<<<dev.sms * 16, 256, 0, st>>>(g, w.start, w.count, w.hcnt, w.heads, w.tails, w.slices, w.status,
+                                             w.perm);
     }
     if (w.cellcount) k_nbr_bound<<<dev.sms * 4, 256, 0, st>>>(g, w.cellcount, w.status);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
