@@ -218,7 +218,8 @@ mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *p
  * cum(l) = l*R - max(0, l - L), L = cnt - 32*(R - 1), and entry cum(l) + rho
  * goes to slice place rho*32 + l).  Particles 32 apart in a round then sit in
  * cells that use different shared-memory banks, which the next step's P2G
- * and G2P exploit.  The remaining particles (outside the domain) are copied
+ * and G2P exploit.  A slice of at most 32 particles (one round) keeps bin
+ * order.  The remaining particles (outside the domain) are copied
  * unchanged to out[j] = in[perm[j]].  m and id are carried along.  This is
  * the ping-pong buffer of "Particle Worlds, part 3", Step 4 ("the sort writes
  * into a second buffer"): the next step's binning then starts from almost

@@ -289,7 +289,8 @@ __device__ __forceinline__ uint32_t interleave_entry(uint32_t pos, uint32_t cnt)
 // bin order, the slice is counting-sorted by bank class, and thread t
 // computes the particles that go to places t, t + 256, ... of the
 // interleaved slice, so that its writes are coalesced and its reads of the
-// velocity halo meet few bank conflicts.
+// velocity halo meet few bank conflicts.  A slice of at most 32 particles is
+// one round and keeps bin order.
 template <int DIM, int T, bool SORTED>
 __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                      const uint32_t *__restrict__ perm,
@@ -354,7 +355,16 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             sv_y[h] = in ? vel[g.nodes + node] : 0.f;
             if (DIM == 3) sv_z[h] = in ? vel[2 * g.nodes + node] : 0.f;
         }
-        if constexpr (SORTED) {
+        if (SORTED && cnt <= 32u) {
+            // one round: the order inside it does not matter, bin order is kept
+            cp_async_wait<0>();
+            __syncthreads();
+            if (threadIdx.x < cnt) {
+                const uint32_t r = threadIdx.x;
+                auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
+                gather_one<DIM, T, true>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4);
+            }
+        } else if constexpr (SORTED) {
             // stable counting sort of the slice by bank class: counts per
             // (round, warp, class), scanned class-major
             uint32_t cls[NQ], below[NQ];

@@ -351,8 +351,8 @@ def cell_class(key, dim, tile):
 
 def sorted_output_order(key, perm, tile_count, n_valid, dim=3, tile=4):
     """Where mpm_g2p_sorted puts each particle: slice by slice in bin order,
-    each slice stably sorted by bank class and dealt out column by column over
-    rounds of 32."""
+    each slice of more than 32 particles stably sorted by bank class and dealt
+    out column by column over rounds of 32."""
     out = perm.astype(np.int64).copy()
     start = np.concatenate([[0], np.cumsum(tile_count.astype(np.int64))])
     for t in np.nonzero(tile_count)[0]:
@@ -360,6 +360,8 @@ def sorted_output_order(key, perm, tile_count, n_valid, dim=3, tile=4):
             beg = int(start[t]) + first
             cnt = min(SLICE, int(tile_count[t]) - first)
             idx = perm[beg:beg + cnt].astype(np.int64)
+            if cnt <= 32:            # one round: bin order kept
+                continue
             srt = np.empty(cnt, np.int64)
             srt[np.argsort(cell_class(key[idx], dim, tile), kind="stable")] = np.arange(cnt)
             R = -(-cnt // 32)
