@@ -510,6 +510,28 @@ int64_t orc_g2p(const orc_desc *d, const float *vel, int64_t np, float *const *x
     return moved;
 }
 
+/* The advective time-step bound of the implementation guide (section 3.3.2,
+ * rule 6: the step must satisfy dt <= dx / max_p(|v_p| + 1.5 dx |C_p|_F)):
+ * the largest |v_p| + 1.5 dx |C_p|_F over np particles, each term in fp32 as
+ * sqrt((vx*vx + vy*vy) + vz*vz) + (1.5*dx) * sqrt(C0*C0 + C1*C1 + ... ), the
+ * sums taken in index order.  0 for no particle.                            */
+float orc_advective_speed(int dim, float dx, int64_t np, const float *const *v, const float *const *C)
+{
+    float best = 0.0f;
+    float h = 1.5f * dx;
+    for (int64_t p = 0; p < np; ++p) {
+        float sv = 0.0f, sc = 0.0f;
+        for (int k = 0; k < dim; ++k)
+            sv = sv + v[k][p] * v[k][p];
+        for (int j = 0; j < dim * dim; ++j)
+            sc = sc + C[j][p] * C[j][p];
+        float t = sqrtf(sv) + h * sqrtf(sc);
+        if (t > best)
+            best = t;
+    }
+    return best;
+}
+
 /* ------------------------------------------------------------------------ */
 /* The integer cloud-in-cell transfer of "particle to grid transfer in
  * checked integer arithmetic".  Positions are integers in 1/65,536 of a cell;

@@ -83,6 +83,8 @@ def lib():
             L.orc_grid_update_float.restype = None
             L.orc_g2p.argtypes = [ct.POINTER(Desc), _P, ct.c_int64, _PP, _PP, _PP, ct.c_float]
             L.orc_g2p.restype = ct.c_int64
+            L.orc_advective_speed.argtypes = [ct.c_int, ct.c_float, ct.c_int64, _PP, _PP]
+            L.orc_advective_speed.restype = ct.c_float
             L.orc_rdiv.argtypes = [ct.c_int64, ct.c_int64]
             L.orc_rdiv.restype = ct.c_int64
             L.orc_cic_int_bound.argtypes = [ct.c_int, _P, ct.c_int64, _PP, _P, _PP]
@@ -202,6 +204,12 @@ def g2p(grid: dict, vel: np.ndarray, x, v=None, C=None):
     moved = lib().orc_g2p(ct.byref(desc_from(grid)), _ptr(vel), n, _rows(x), _rows(v), _rows(C),
                           ct.c_float(grid["dt"]))
     return x, v, C, int(moved)
+
+
+def advective_speed(dim: int, dx: float, v, C) -> float:
+    """max_p |v_p| + 1.5 dx |C_p|_F in fp32 (the advective step bound is dt <= dx / this)."""
+    v, C = _f32(v), _f32(C)
+    return float(lib().orc_advective_speed(dim, ct.c_float(dx), v.shape[1], _rows(v), _rows(C)))
 
 
 def rdiv(a: int, b: int) -> int:

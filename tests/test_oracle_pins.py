@@ -423,3 +423,38 @@ def test_float_and_double_order_table_qualitatively():
             assert same == 128
         else:
             assert same < 128
+
+
+# --------------------------------------------------------------------------
+# the advective step bound (implementation guide 3.3.2, rule 6)
+
+def test_advective_speed_special_cases():
+    # 3-4-5: |v| = 5 exactly; C = 0
+    v = np.array([[3.0], [4.0], [0.0]], np.float32)
+    C = np.zeros((9, 1), np.float32)
+    assert O.advective_speed(3, 0.25, v, C) == 5.0
+    # v = 0, C with |C|_F = 5 exactly (entries 3 and 4): 1.5 * 0.25 * 5
+    C[0, 0], C[4, 0] = 3.0, 4.0
+    assert O.advective_speed(3, 0.25, np.zeros((3, 1), np.float32), C) == 1.875
+    # both terms add
+    assert O.advective_speed(3, 0.25, v, C) == 6.875
+    # 2D reads two components and four entries
+    assert O.advective_speed(2, 0.5, np.array([[6.0], [8.0]], np.float32), np.zeros((4, 1), np.float32)) == 10.0
+    # no particle
+    assert O.advective_speed(3, 0.25, np.zeros((3, 0), np.float32), np.zeros((9, 0), np.float32)) == 0.0
+
+
+def test_advective_speed_is_the_largest_particle_term():
+    s = W.Stream(41, 41)
+    n = 5000
+    v = s.normal(3 * n, 2.0).reshape(3, n).astype(np.float32)
+    C = s.normal(9 * n, 5.0).reshape(9, n).astype(np.float32)
+    dx = 1.0 / 64
+    got = O.advective_speed(3, dx, v, C)
+    terms = (np.sqrt((v.astype(np.float64) ** 2).sum(axis=0))
+             + 1.5 * dx * np.sqrt((C.astype(np.float64) ** 2).sum(axis=0)))
+    assert got == pytest.approx(terms.max(), rel=1e-6)
+    # attained by one particle, and no particle is larger
+    k = int(np.argmax(terms))
+    assert O.advective_speed(3, dx, v[:, k:k + 1], C[:, k:k + 1]) == got
+    assert O.advective_speed(3, dx, np.delete(v, k, axis=1), np.delete(C, k, axis=1)) <= got
