@@ -39,11 +39,11 @@ LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2
 # the 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
-    "p2g": {"bytes_per_particle": 81.9, "files": ("p2g.cu", "common.cuh"),
+    "p2g": {"bytes_per_particle": 82.1, "files": ("p2g.cu", "common.cuh"),
             "sha256": "098a72f38c248480137b7082b87285b56b829b7fc515cb580b41283b0021d3a5"
                       "caa52acb850be6dfcc10664d1a0528e01c133bee3783931b11469d24af5c1ad8"},
     "g2p": {"bytes_per_particle": 77.0, "files": ("grid_g2p.cu", "common.cuh"),
-            "sha256": "f80471f52ed8f0239e8d19733c7618c9d41075901ea8243834d5aa49b1d105e7"
+            "sha256": "612b6f184ccf40ab83fa3319579f43bbae68baa3bfe4fae71b1d274ca70a74da"
                       "caa52acb850be6dfcc10664d1a0528e01c133bee3783931b11469d24af5c1ad8"},
 }
 
@@ -213,6 +213,9 @@ def run_ours(args, rank, world, local):
     assert st[L.ST_FLAGS] == 0, f"status flags after timing {st[:8]}"
     ms_step = aggregate_max(total_ms / args.steps, world, dev)
     value = n * world / (ms_step * 1e-3)
+    # the advective step bound of the state the last timed G2P wrote
+    speed = float(np.array([st[L.ST_MAX_SPEED]], np.uint32).view(np.float32)[0])
+    advective = {"max_speed": speed, "dt_limit": grid["dx"] / speed if speed > 0 else None, "dt": sys_.dt}
 
     # roofline of the dominant kernel
     mean_ms = parts_ms.mean(axis=0)
@@ -281,6 +284,7 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,
+        "advective_step_bound": advective,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu

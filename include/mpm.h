@@ -100,6 +100,8 @@ enum {
     MPM_ST_N_LARGE_BUCKETS = 9, /* buckets of more than 512 runs (sorted by one block each) */
     MPM_ST_WORK_P2G = 11,    /* internal: work counter of the P2G launch */
     MPM_ST_WORK_G2P = 12,    /* internal: work counter of the G2P launch */
+    MPM_ST_MAX_SPEED = 13,   /* fp32 bits of max over the particles the last G2P moved of
+                                |v'| + 1.5 dx |C'|_F; the advective step bound is dt <= dx / it */
     MPM_STATUS_WORDS = 16
 };
 

@@ -19,6 +19,7 @@ MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
 (ST_FLAGS, ST_N_OUTSIDE, ST_N_OUT_OF_RANGE, ST_N_VALID, ST_N_SLICES, ST_N_ACTIVE, ST_MAX_NEIGHBOURS,
  ST_N_BIG_TILES, ST_N_RUNS, ST_N_LARGE_BUCKETS) = range(10)
 ST_BIN_WORDS = 10   # status words 0..9 are written by mpm_bin
+ST_MAX_SPEED = 13   # fp32 bits of max |v'| + 1.5 dx |C'|_F over the particles the last G2P moved
 MPM_STATUS_WORDS = 16
 MPM_STATIC_WORKSPACE_BYTES = 16 << 20
 

@@ -146,7 +146,7 @@ __device__ __forceinline__ float2 sum3x2(const float2 w[3], const float2 t[3]) {
 template <int DIM, int T, bool SORTED, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
                                            uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
-                                           float dt, float c4) {
+                                           float dt, float c4, float &smax) {
     using Hl = HaloU<DIM, T>;
     float x[DIM], f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
@@ -245,12 +245,20 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
         Bm[0][1] = b1.x;
         Bm[1][1] = b1.y;
     }
+    // the advective bound's term |v'| + 1.5 dx |C'|_F, sums in index order
+    float sv2 = 0.f, sc2 = 0.f;
 #pragma unroll
     for (int k = 0; k < DIM; ++k) {
         q.v[k][dst] = vn[k];
+        sv2 = __fadd_rn(sv2, __fmul_rn(vn[k], vn[k]));
 #pragma unroll
-        for (int l = 0; l < DIM; ++l) q.C[k * DIM + l][dst] = __fmul_rn(Bm[k][l], c4);
+        for (int l = 0; l < DIM; ++l) {
+            const float c = __fmul_rn(Bm[k][l], c4);
+            q.C[k * DIM + l][dst] = c;
+            sc2 = __fadd_rn(sc2, __fmul_rn(c, c));
+        }
     }
+    smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
 #pragma unroll
     for (int l = 0; l < DIM; ++l) q.x[l][dst] = __fmaf_rn(dt, vn[l], x[l]);
     if constexpr (SORTED) {
@@ -317,6 +325,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
+    float smax = 0.f;  // the advective bound's largest term among this thread's particles
     uint32_t next = 0;
     for (uint32_t s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
         next = ask_item(&status[MPM_ST_WORK_G2P]);
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             if (threadIdx.x < cnt) {
                 const uint32_t r = threadIdx.x;
                 auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                gather_one<DIM, T, true>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4);
+                gather_one<DIM, T, true>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
             }
         } else if constexpr (SORTED) {
             // stable counting sort of the slice by bank class: counts per
@@ -422,7 +431,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                     const uint32_t e = interleave_entry(pos, cnt);
                     const uint32_t r = order[e + (e >> 5)];
                     auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                    gather_one<DIM, T, true>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4);
+                    gather_one<DIM, T, true>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax);
                 }
             }
         } else {
@@ -443,11 +452,14 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                 if (r < cnt) {
                     const int stage = qi & 1;
                     auto rec = [&](int f) { return *pf.at(stage, f); };
-                    gather_one<DIM, T, false>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4);
+                    gather_one<DIM, T, false>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4, smax);
                 }
             }
         }
     }
+    // non-negative fp32 values order as their bit patterns
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
+    if (lane == 0 && wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
 }
 
 // Particles past the sorted in-domain part (outside the domain): copied.
@@ -462,7 +474,7 @@ mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const W
                       const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
     const int blocks = dev.sms * 4;
-    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, sizeof(uint32_t), st);
+    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
     if (g.dim == 3 && g.T == 4)
         k_g2p<3, 4, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
     else if (g.dim == 2 && g.T == 8)
@@ -476,7 +488,7 @@ mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in,
                              float dt, const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;
     const int blocks = dev.sms * 4;
-    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, sizeof(uint32_t), st);
+    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
     if (g.dim == 3 && g.T == 4) {
         k_g2p<3, 4, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start, w.status, dt,
                                                           c4);

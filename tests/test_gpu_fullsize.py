@@ -135,6 +135,9 @@ def _check_step(sys, grid, n, n_tiles_sampled=6):
     sys.g2p_sorted()
     x1, v1, C1 = sys.state()
     ids1 = sys.id.cpu().numpy().astype(np.int64)
+    # the advective step bound: the largest term over the moved particles (all in the domain)
+    speed = np.array([sys.status()[L.ST_MAX_SPEED]], np.uint32).view(np.float32)[0]
+    assert speed == O.advective_speed(grid["dim"], grid["dx"], v1[:, :valid], C1[:, :valid])
     where = np.empty(n, dtype=np.int64)
     where[ids1] = np.arange(n)
     samp = inside[(W.Stream(32, 32).bits(20000) % np.uint64(inside.size)).astype(np.int64)]

@@ -186,6 +186,10 @@ def test_step_fixed_bit_exact(dim, mode, scale, n, count):
     assert np.array_equal(x.view(np.uint32), ox.view(np.uint32))
     assert np.array_equal(v.view(np.uint32), ov.view(np.uint32))
     assert np.array_equal(C.view(np.uint32), oC.view(np.uint32))
+    # the advective step bound over the particles G2P moved
+    inside = O.bin_particles(cloud["grid"], cloud["x"])[0] != 0xFFFFFFFF
+    speed = np.array([sys.status()[L.ST_MAX_SPEED]], np.uint32).view(np.float32)[0]
+    assert speed == O.advective_speed(dim, cloud["grid"]["dx"], ov[:, inside], oC[:, inside])
 
 
 @pytest.mark.parametrize("dim,n,count", [(2, 64, 6000), (3, 32, 6007)])
@@ -396,6 +400,8 @@ def test_g2p_sorted_moves_particles_into_bin_order():
     assert np.array_equal(v.view(np.uint32), ov[:, p].view(np.uint32))
     assert np.array_equal(C.view(np.uint32), oC[:, p].view(np.uint32))
     assert np.array_equal(m, cloud["m"][p])
+    speed = np.array([sys.status()[L.ST_MAX_SPEED]], np.uint32).view(np.float32)[0]
+    assert speed == O.advective_speed(3, cloud["grid"]["dx"], ov[:, p], oC[:, p])
 
 
 def test_step_host_equals_device_sorted_step():
