@@ -246,6 +246,25 @@ def small_cloud(dim: int, n_particles: int, n: int, seed: int, acc_mode: int = A
     return out
 
 
+def with_elastic(cloud: dict, seed: int, fsig: float = 0.05, ppc: float = 8.0, mu: float = 1.0e7,
+                 lam: float = 1.0e7) -> dict:
+    """Adds an elastic state to `cloud`: deformation gradients F = I + N(0, fsig) per
+    entry (dim*dim planes, row-major like C), rest volumes V0 = dx^dim / ppc and a
+    Neo-Hookean material {mu, lambda}.  The defaults make the stress term of the
+    affine matrix comparable to C on the small test grids (dt = 1e-4, m ~ 1)."""
+    dim = cloud["grid"]["dim"]
+    n = cloud["x"].shape[1]
+    s = Stream(seed, 11)
+    F = s.normal(dim * dim * n, fsig).reshape(dim * dim, n)
+    for k in range(dim):
+        F[k * dim + k] += 1.0
+    vol = np.full(n, cloud["grid"]["dx"] ** dim / ppc)
+    out = dict(cloud)
+    out.update(F=np.ascontiguousarray(F, dtype=np.float32), vol=np.ascontiguousarray(vol, dtype=np.float32),
+               material={"mu": float(np.float32(mu)), "lambda": float(np.float32(lam))})
+    return out
+
+
 CONFIGS = {
     "cic_int": cic_int,
     "mls2d": mls2d,

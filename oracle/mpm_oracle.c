@@ -3,7 +3,9 @@
  * Point Method particle/grid transfer: cell keys and a stable counting sort,
  * the particle-to-grid (P2G) scatter of mass and APIC/MLS affine momentum in
  * fixed-point integers (and in floating point), the grid update and the
- * grid-to-particle (G2P) gather.  Also the integer cloud-in-cell transfer of
+ * grid-to-particle (G2P) gather, and the MLS-MPM elastic stress folded into
+ * the affine matrix with the deformation-gradient update.  Also the integer
+ * cloud-in-cell transfer of
  * "particle to grid transfer in checked integer arithmetic" exactly as that
  * page states it.
  *
@@ -358,6 +360,135 @@ uint32_t orc_p2g_float(const orc_desc *d, int64_t np, const float *const *x, con
 }
 
 /* ------------------------------------------------------------------------ */
+/* MLS-MPM elastic stress (implementation guide, section 3.1, Part 2: the
+ * Neo-Hookean model with Lame constants mu and lambda,
+ *     J = det F,  P = mu (F - F^-T) + lambda ln(J) F^-T,  sigma = P F^T / J).
+ * In MLS-MPM the stress enters the same affine scatter as the APIC matrix:
+ * node momentum gains -dt V sigma D^-1 w (x_i - x_p), with V = V0 J the
+ * particle's current volume and D^-1 = 4/dx^2 the quadratic B-spline's
+ * inverse inertia (the guide's "D (= B*4)", section 3.3.2).  Dividing by the
+ * particle mass folds it into C:
+ *     C' = C - kappa tau,  kappa = dt V0 (4/dx^2) / m,  tau = J sigma = P F^T
+ * and P F^T = mu (F F^T - I) + lambda ln(J) I, because F^-T F^T = I.  So the
+ * scatter itself is unchanged; only the matrix it reads differs.
+ *
+ * Evaluation order (fp32, round to nearest even, no contraction), the
+ * contract the GPU reproduces bit for bit:
+ *   J (3D)  = (F00*(F11*F22 - F12*F21) - F01*(F10*F22 - F12*F20))
+ *             + F02*(F10*F21 - F11*F20);      J (2D) = F00*F11 - F01*F10
+ *   b_kl    = (F_k0*F_l0 + F_k1*F_l1) + F_k2*F_l2       (F F^T, index order)
+ *   tau_kl  = mu*b_kl (k != l);  tau_kk = mu*(b_kk - 1) + lambda*ln(J)
+ *   kappa   = ((dt*V0) * c4s) / m,  c4s = (4*inv_dx)*inv_dx
+ *   C'_kl   = C_kl - kappa*tau_kl
+ * A particle whose J is not a positive normal finite number (an inverted or
+ * collapsed element; ln J undefined) keeps C' = C and is counted.
+ *
+ * ln is computed here, not taken from the C library, so that both sides
+ * round identically: J = 2^e * r with r in [1/sqrt2, sqrt2), and
+ * ln r = 2 atanh(s), s = (r - 1)/(r + 1), from the series
+ * atanh(s) = s + s^3/3 + s^5/5 + s^7/7 + s^9/9 + ..., |s| <= 0.1716, so the
+ * dropped terms are below 2e-9 relative.  ln 2 is split as
+ * LN2_HI = 45426/65536 (e * LN2_HI exact for |e| < 256) plus LN2_LO.
+ *   z = s*s;  p = ((1/9*z + 1/7)*z + 1/5)*z + 1/3   (each op rounded)
+ *   ln r = 2*(s + s*(z*p));   ln J = e*LN2_HI + (e*LN2_LO + ln r)         */
+
+#define ORC_LN2_HI 0x1.62e4p-1f       /* 45426 / 65536 */
+#define ORC_LN2_LO 0x1.7f7d1cp-20f    /* ln 2 - LN2_HI, rounded to fp32 */
+#define ORC_SQRT2 0x1.6a09e6p+0f      /* sqrt(2) rounded down to fp32 */
+
+/* 1 if J > 0 is a normal finite fp32 number. */
+static int orc_log_domain(float J)
+{
+    return J >= 0x1p-126f && J <= 0x1.fffffep+127f;
+}
+
+/* ln J for J in the log domain (above); 0 outside it. */
+float orc_log(float J)
+{
+    if (!orc_log_domain(J))
+        return 0.0f;
+    uint32_t u;
+    memcpy(&u, &J, sizeof u);
+    int e = (int)(u >> 23) - 127;
+    u = (u & 0x007FFFFFu) | 0x3F800000u;
+    float r;
+    memcpy(&r, &u, sizeof r);
+    if (r > ORC_SQRT2) {
+        r = r * 0.5f;
+        e += 1;
+    }
+    float s = (r - 1.0f) / (r + 1.0f);
+    float z = s * s;
+    float p = (1.0f / 9.0f) * z + (1.0f / 7.0f);
+    p = p * z + (1.0f / 5.0f);
+    p = p * z + (1.0f / 3.0f);
+    float lr = 2.0f * (s + s * (z * p));
+    float fe = (float)e;
+    return fe * ORC_LN2_HI + (fe * ORC_LN2_LO + lr);
+}
+
+/* Kirchhoff stress tau = P F^T of the Neo-Hookean model; F and tau are
+ * dim x dim row-major (F[k*dim + l]).  Returns 0 (tau = 0) when J is
+ * outside the log domain, else 1.                                           */
+int orc_kirchhoff(int dim, float mu, float lambda, const float *F, float *tau)
+{
+    float J;
+    if (dim == 3) {
+        float c0 = F[4] * F[8] - F[5] * F[7];
+        float c1 = F[3] * F[8] - F[5] * F[6];
+        float c2 = F[3] * F[7] - F[4] * F[6];
+        J = (F[0] * c0 - F[1] * c1) + F[2] * c2;
+    } else {
+        J = F[0] * F[3] - F[1] * F[2];
+    }
+    for (int j = 0; j < dim * dim; ++j)
+        tau[j] = 0.0f;
+    if (!orc_log_domain(J))
+        return 0;
+    float lj = lambda * orc_log(J);
+    for (int k = 0; k < dim; ++k)
+        for (int l = 0; l < dim; ++l) {
+            float b = F[k * dim + 0] * F[l * dim + 0] + F[k * dim + 1] * F[l * dim + 1];
+            if (dim == 3)
+                b = b + F[k * dim + 2] * F[l * dim + 2];
+            tau[k * dim + l] = k == l ? mu * (b - 1.0f) + lj : mu * b;
+        }
+    return 1;
+}
+
+/* C' = C - kappa tau for every particle (Cout may alias C).  Returns the
+ * number of in-domain particles whose J is outside the log domain (those
+ * keep C' = C); out-of-domain particles are folded too but not counted,
+ * since P2G never scatters them.                                            */
+int64_t orc_stress_affine(const orc_desc *d, float dt, float mu, float lambda, int64_t np,
+                          const float *const *x, const float *const *C, const float *const *F,
+                          const float *vol, const float *m, float *const *Cout)
+{
+    int dim = d->dim;
+    float c4s = (4.0f * d->inv_dx) * d->inv_dx;
+    int64_t degenerate = 0;
+    for (int64_t p = 0; p < np; ++p) {
+        float Fp[9] = {0}, tau[9];
+        for (int j = 0; j < dim * dim; ++j)
+            Fp[j] = F[j][p];
+        int ok = orc_kirchhoff(dim, mu, lambda, Fp, tau);
+        int b[3];
+        float f[3];
+        if (!ok) {
+            if (base_frac(d, x, p, b, f))
+                degenerate += 1;
+            for (int j = 0; j < dim * dim; ++j)
+                Cout[j][p] = C[j][p];
+            continue;
+        }
+        float kappa = ((dt * vol[p]) * c4s) / m[p];
+        for (int j = 0; j < dim * dim; ++j)
+            Cout[j][p] = C[j][p] - kappa * tau[j];
+    }
+    return degenerate;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Grid update.  Implementation guide section 2.1 (the grid pass:
  * mass-normalise, collide, boundary) and section 3.3.2's note that the
  * velocity-form boundary is a sign test; rule 7: gravity is a solver
@@ -443,9 +574,29 @@ static float sum3(const float w[3], const float t[3])
     return fmaf(w[2], t[2], fmaf(w[1], t[1], w[0] * t[0]));
 }
 
-/* Out-of-domain particles are left unchanged.  Returns how many moved.     */
+/* Out-of-domain particles are left unchanged.  Returns how many moved.
+ * With F (not NULL) the deformation gradient of every moved particle is
+ * advanced with its new C (implementation guide, section 3.3.2: F <- (I + D) F,
+ * where the velocity form's D is dt C):
+ *   F'_kl = fma(D_k2, F_2l, fma(D_k1, F_1l, fma(D_k0, F_0l, F_kl))),
+ *   D_kj = dt * C'_kj        (2D: drop the third term).                   */
+static int64_t g2p_core(const orc_desc *d, const float *vel, int64_t np, float *const *x, float *const *v,
+                        float *const *C, float *const *F, float dt);
+
 int64_t orc_g2p(const orc_desc *d, const float *vel, int64_t np, float *const *x, float *const *v,
                 float *const *C, float dt)
+{
+    return g2p_core(d, vel, np, x, v, C, NULL, dt);
+}
+
+int64_t orc_g2p_elastic(const orc_desc *d, const float *vel, int64_t np, float *const *x, float *const *v,
+                        float *const *C, float *const *F, float dt)
+{
+    return g2p_core(d, vel, np, x, v, C, F, dt);
+}
+
+static int64_t g2p_core(const orc_desc *d, const float *vel, int64_t np, float *const *x, float *const *v,
+                        float *const *C, float *const *F, float dt)
 {
     int dim = d->dim;
     int64_t nodes = nodes_of(d);
@@ -505,6 +656,21 @@ int64_t orc_g2p(const orc_desc *d, const float *vel, int64_t np, float *const *x
         }
         for (int l = 0; l < dim; ++l)
             x[l][p] = fmaf(dt, vnew[l], x[l][p]);
+        if (F) {
+            float D[9], Fo[9];
+            for (int j = 0; j < dim * dim; ++j) {
+                D[j] = dt * C[j][p];
+                Fo[j] = F[j][p];
+            }
+            for (int k = 0; k < dim; ++k)
+                for (int l = 0; l < dim; ++l) {
+                    float t = fmaf(D[k * dim + 0], Fo[0 * dim + l], Fo[k * dim + l]);
+                    t = fmaf(D[k * dim + 1], Fo[1 * dim + l], t);
+                    if (dim == 3)
+                        t = fmaf(D[k * dim + 2], Fo[2 * dim + l], t);
+                    F[k * dim + l][p] = t;
+                }
+        }
         moved += 1;
     }
     return moved;

@@ -83,6 +83,15 @@ def lib():
             L.orc_grid_update_float.restype = None
             L.orc_g2p.argtypes = [ct.POINTER(Desc), _P, ct.c_int64, _PP, _PP, _PP, ct.c_float]
             L.orc_g2p.restype = ct.c_int64
+            L.orc_g2p_elastic.argtypes = [ct.POINTER(Desc), _P, ct.c_int64, _PP, _PP, _PP, _PP, ct.c_float]
+            L.orc_g2p_elastic.restype = ct.c_int64
+            L.orc_log.argtypes = [ct.c_float]
+            L.orc_log.restype = ct.c_float
+            L.orc_kirchhoff.argtypes = [ct.c_int, ct.c_float, ct.c_float, _P, _P]
+            L.orc_kirchhoff.restype = ct.c_int
+            L.orc_stress_affine.argtypes = [ct.POINTER(Desc), ct.c_float, ct.c_float, ct.c_float, ct.c_int64,
+                                            _PP, _PP, _PP, _P, _P, _PP]
+            L.orc_stress_affine.restype = ct.c_int64
             L.orc_advective_speed.argtypes = [ct.c_int, ct.c_float, ct.c_int64, _PP, _PP]
             L.orc_advective_speed.restype = ct.c_float
             L.orc_rdiv.argtypes = [ct.c_int64, ct.c_int64]
@@ -206,6 +215,39 @@ def g2p(grid: dict, vel: np.ndarray, x, v=None, C=None):
     return x, v, C, int(moved)
 
 
+def g2p_elastic(grid: dict, vel: np.ndarray, x, v, C, F):
+    """G2P that also advances the deformation gradient, F' = (I + dt C') F:
+    returns (x', v', C', F', moved)."""
+    vel = _f32(vel)
+    x, v, C, F = (_f32(a).copy() for a in (x, v, C, F))
+    moved = lib().orc_g2p_elastic(ct.byref(desc_from(grid)), _ptr(vel), x.shape[1], _rows(x), _rows(v), _rows(C),
+                                  _rows(F), ct.c_float(grid["dt"]))
+    return x, v, C, F, int(moved)
+
+
+def log(J: float) -> float:
+    """The fp32 natural logarithm both sides use for the Neo-Hookean ln J."""
+    return float(lib().orc_log(ct.c_float(J)))
+
+
+def kirchhoff(dim: int, mu: float, lam: float, F) -> tuple:
+    """Neo-Hookean Kirchhoff stress tau = P F^T (dim x dim, fp32); (tau, ok)."""
+    F = _f32(np.asarray(F).reshape(dim * dim))
+    tau = np.zeros(dim * dim, dtype=np.float32)
+    ok = lib().orc_kirchhoff(dim, ct.c_float(mu), ct.c_float(lam), _ptr(F), _ptr(tau))
+    return tau.reshape(dim, dim), bool(ok)
+
+
+def stress_affine(grid: dict, material: dict, x, C, F, vol, m):
+    """The MLS fold C' = C - kappa tau: returns (C' fp32 [dim*dim, n], degenerate in-domain count)."""
+    x, C, F, vol, m = _f32(x), _f32(C), _f32(F), _f32(vol), _f32(m)
+    out = np.zeros_like(C)
+    bad = lib().orc_stress_affine(ct.byref(desc_from(grid)), ct.c_float(grid["dt"]), ct.c_float(material["mu"]),
+                                  ct.c_float(material["lambda"]), x.shape[1], _rows(x), _rows(C), _rows(F),
+                                  _ptr(vol), _ptr(m), _rows(out))
+    return out, int(bad)
+
+
 def advective_speed(dim: int, dx: float, v, C) -> float:
     """max_p |v_p| + 1.5 dx |C_p|_F in fp32 (the advective step bound is dt <= dx / this)."""
     v, C = _f32(v), _f32(C)
@@ -250,6 +292,21 @@ def cic_int_gather(grid: dict, X, acc):
     out = np.zeros((dim, X.shape[1]), dtype=np.int64)
     lib().orc_cic_int_gather(dim, _ptr(n), X.shape[1], _rows(X), _ptr(acc), _rows(out))
     return out
+
+
+def step_elastic(grid: dict, material: dict, x, v, C, m, F, vol):
+    """One oracle step with the elastic stress: bin, fold, P2G, grid update, G2P with the F update."""
+    key, perm, cnt, valid = bin_particles(grid, x)
+    Cs, degenerate = stress_affine(grid, material, x, C, F, vol, m)
+    if grid["acc_mode"] == 2:
+        acc, st, counts = p2g_float(grid, x, v, Cs, m)
+        vel = grid_update_float(grid, acc)
+    else:
+        acc, st, counts = p2g_fixed(grid, x, v, Cs, m)
+        vel = grid_update_fixed(grid, acc)
+    x2, v2, C2, F2, moved = g2p_elastic(grid, vel, x, v, C, F)
+    return dict(key=key, perm=perm, tile_count=cnt, n_valid=valid, acc=acc, status=st, counts=counts,
+                degenerate=degenerate, vel=vel, x=x2, v=v2, C=C2, F=F2)
 
 
 def step_fixed(grid: dict, x, v, C, m):

@@ -458,3 +458,165 @@ def test_advective_speed_is_the_largest_particle_term():
     k = int(np.argmax(terms))
     assert O.advective_speed(3, dx, v[:, k:k + 1], C[:, k:k + 1]) == got
     assert O.advective_speed(3, dx, np.delete(v, k, axis=1), np.delete(C, k, axis=1)) <= got
+
+
+# --------------------------------------------------------------------------
+# MLS-MPM elastic stress (implementation guide, section 3.1, Part 2: the
+# Neo-Hookean P and sigma; section 3.3.2: F <- (I + D) F)
+
+def _pages_fold_fp64(grid, material, C, F, vol, m):
+    """C - dt V sigma (4/dx^2) / m per particle, the stress written exactly as
+    the guide prints it (F^-T, P, sigma = P F^T / J, V = V0 J), in fp64."""
+    dim = grid["dim"]
+    mu, lam = material["mu"], material["lambda"]
+    out = np.zeros(C.shape, dtype=np.float64)
+    for p in range(C.shape[1]):
+        Fp = F[:, p].astype(np.float64).reshape(dim, dim)
+        J = np.linalg.det(Fp)
+        FinvT = np.linalg.inv(Fp).T
+        P = mu * (Fp - FinvT) + lam * np.log(J) * FinvT
+        sigma = P @ Fp.T / J
+        V = vol[p] * J
+        term = -grid["dt"] * V * sigma * 4.0 / grid["dx"] ** 2 / m[p]
+        out[:, p] = C[:, p] + term.reshape(-1)
+    return out
+
+
+def test_log_series_matches_the_logarithm():
+    s = W.Stream(4242, 1)
+    J = np.exp(s.uniform53(200000) * 80.0 - 40.0).astype(np.float32)
+    near1 = (1.0 + (s.uniform53(20000) - 0.5) * 1e-3).astype(np.float32)
+    J = np.concatenate([J, near1, np.float32([1.0, 2.0, 0.5, 3.0, 2.0 ** -126, 3.4e38])])
+    got = np.array([O.log(float(j)) for j in J], dtype=np.float64)
+    ref = np.log(J.astype(np.float64))
+    ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2.0 * ulp + 1e-45)
+    assert O.log(1.0) == 0.0
+    # outside the domain (not positive, subnormal, infinite, NaN): 0
+    for bad in (0.0, -1.0, 1e-40, float("inf"), float("nan")):
+        assert O.log(bad) == 0.0
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_kirchhoff_vanishes_at_rest_and_under_rotation(dim):
+    tau, ok = O.kirchhoff(dim, 3.0e6, 5.0e6, np.eye(dim))
+    assert ok and np.all(tau == 0.0)
+    s = W.Stream(31, dim)
+    for _ in range(20):
+        q, _ = np.linalg.qr(s.normal(dim * dim, 1.0).reshape(dim, dim))
+        if np.linalg.det(q) < 0:
+            q[:, 0] = -q[:, 0]
+        tau, ok = O.kirchhoff(dim, 3.0e6, 5.0e6, q)
+        assert ok and np.max(np.abs(tau)) <= 3.0e6 * 1e-6
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_kirchhoff_uniform_stretch_closed_form(dim):
+    for sc in (0.5, 0.8, 1.25, 1.5, 2.0):
+        mu, lam = 2.0e3, 7.0e3
+        tau, ok = O.kirchhoff(dim, mu, lam, sc * np.eye(dim))
+        expect = mu * (sc * sc - 1.0) + lam * dim * np.log(sc)
+        assert ok
+        assert np.max(np.abs(tau - expect * np.eye(dim))) <= 1e-6 * (abs(expect) + mu)
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_stress_fold_matches_the_guides_formulas_in_fp64(dim):
+    cloud = W.with_elastic(W.small_cloud(dim, 400, 32, seed=900 + dim, lo=0.1, hi=0.9, csig=1.0,
+                                         mass_lo=0.5, mass_hi=2.0), seed=901 + dim, fsig=0.15)
+    g, mat = cloud["grid"], cloud["material"]
+    Cs, bad = O.stress_affine(g, mat, cloud["x"], cloud["C"], cloud["F"], cloud["vol"], cloud["m"])
+    ref = _pages_fold_fp64(g, mat, cloud["C"], cloud["F"], cloud["vol"], cloud["m"])
+    assert bad == 0
+    # fp32 error model: a few roundings of C, of mu * (F F^T)_kk (mu (F F^T - I) cancels) and of lambda ln J
+    n = cloud["x"].shape[1]
+    kappa = g["dt"] * cloud["vol"].astype(np.float64) * 4.0 / g["dx"] ** 2 / cloud["m"]
+    Fm = cloud["F"].astype(np.float64).T.reshape(n, dim, dim)
+    bnorm = np.einsum("pkj,pkj->p", Fm, Fm)
+    logJ = np.abs(np.log(np.linalg.det(Fm)))
+    scale = np.abs(cloud["C"]).max(axis=0) + kappa * (mat["mu"] * bnorm + mat["lambda"] * logJ)
+    assert np.all(np.abs(Cs - ref) <= 1e-6 * scale[None, :])
+    # the stress term is not small next to C here: dropping it fails by far
+    assert np.median(np.abs(ref - cloud["C"])) > 0.3 * np.median(np.abs(cloud["C"]))
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_stress_scatter_is_the_mls_nodal_force(dim):
+    """With v = 0 and C = 0 the momentum the fold scatters is the MLS force
+    impulse -dt V sigma (4/dx^2) w_i (x_i - x_p), summed in fp64 over all nodes."""
+    cloud = W.with_elastic(W.small_cloud(dim, 24, 8, seed=910 + dim, lo=0.25, hi=0.75, scale_log2=18,
+                                         mass_lo=0.5, mass_hi=2.0), seed=911 + dim, fsig=0.2, mu=2.0e5,
+                           lam=3.0e5)
+    g, mat = cloud["grid"], cloud["material"]
+    n = cloud["x"].shape[1]
+    v0 = np.zeros((dim, n), dtype=np.float32)
+    C0 = np.zeros((dim * dim, n), dtype=np.float32)
+    Cs, bad = O.stress_affine(g, mat, cloud["x"], C0, cloud["F"], cloud["vol"], cloud["m"])
+    acc, st, counts = O.p2g_fixed(g, cloud["x"], v0, Cs, cloud["m"])
+    assert bad == 0 and st == 0
+    ref_C = _pages_fold_fp64(g, mat, C0, cloud["F"], cloud["vol"], cloud["m"])
+    mass, mom, absterm = brute_force_p2g(g, cloud["x"], v0, ref_C, cloud["m"])
+    S = 2.0 ** g["scale_log2"]
+    assert np.max(np.abs(mom)) > 1e3 / S
+    tol = (13.5 * n + 1.0) / S + 2e-6 * absterm
+    for k in range(dim):
+        assert np.all(np.abs(acc[1 + k] / S - mom[k]) <= tol)
+    # momentum is unchanged by the stress: the shares of each particle sum to rint(m S v) = 0
+    assert np.all(acc[1:].sum(axis=1) == 0)
+
+
+def test_degenerate_deformation_is_counted_and_unstressed():
+    cloud = W.with_elastic(W.small_cloud(3, 6, 16, seed=920, lo=0.3, hi=0.7), seed=921)
+    F = cloud["F"].copy()
+    F[:, 0] = [1, 0, 0, 0, 1, 0, 0, 0, -1]          # inverted
+    F[:, 1] = [1, 2, 3, 2, 4, 6, 0, 0, 1]           # singular
+    F[:, 2] = [1e-20, 0, 0, 0, 1e-20, 0, 0, 0, 1]   # J subnormal
+    x = cloud["x"].copy()
+    x[:, 2] = -1.0                                  # ... but outside the domain: not counted
+    Cs, bad = O.stress_affine(cloud["grid"], cloud["material"], x, cloud["C"], F, cloud["vol"], cloud["m"])
+    assert bad == 2
+    assert np.array_equal(Cs[:, :3].view(np.uint32), cloud["C"][:, :3].view(np.uint32))
+    assert not np.array_equal(Cs[:, 3:], cloud["C"][:, 3:])
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_g2p_advances_F_by_the_new_affine_matrix(dim):
+    """In an affine velocity field v = A x + c the gathered C is A, and F becomes
+    (I + dt A) F: A on the left (a transposed or right-multiplied update fails)."""
+    n = 16
+    cloud = W.with_elastic(W.small_cloud(dim, 300, n, seed=930 + dim, lo=0.15, hi=0.85), seed=931 + dim,
+                           fsig=0.3)
+    grid = cloud["grid"]
+    grid["dt"] = float(np.float32(1e-2))
+    s = W.Stream(78, dim)
+    A = s.normal(dim * dim, 1.0).reshape(dim, dim)
+    c = s.normal(dim, 1.0)
+    X = node_coords(grid) * grid["dx"]
+    vel = (A @ X + c[:, None]).astype(np.float32)
+    x2, v2, C2, F2, moved = O.g2p_elastic(grid, vel, cloud["x"], cloud["v"], cloud["C"], cloud["F"])
+    assert moved == 300
+    x3, v3, C3, moved3 = O.g2p(grid, vel, cloud["x"], cloud["v"], cloud["C"])
+    assert np.array_equal(C2, C3) and np.array_equal(v2, v3) and np.array_equal(x2, x3)
+    for p in range(300):
+        Fp = cloud["F"][:, p].astype(np.float64).reshape(dim, dim)
+        Cp = C2[:, p].astype(np.float64).reshape(dim, dim)
+        expect = (np.eye(dim) + grid["dt"] * Cp) @ Fp
+        assert np.max(np.abs(F2[:, p].reshape(dim, dim) - expect)) <= 1e-6 * (1 + np.abs(expect).max())
+        assert np.max(np.abs(Cp - A)) <= 2e-3
+    wrong = np.stack([(cloud["F"][:, p].reshape(dim, dim) @ (np.eye(dim) + grid["dt"] * A)).ravel()
+                      for p in range(300)], axis=1)
+    assert np.max(np.abs(F2 - wrong)) > 1e-3
+
+
+def test_elastic_step_keeps_grid_totals_an_identity():
+    cloud = W.with_elastic(W.small_cloud(3, 2000, 32, seed=940, lo=0.2, hi=0.8, scale_log2=19), seed=941)
+    grid = cloud["grid"]
+    out = O.step_elastic(grid, cloud["material"], cloud["x"], cloud["v"], cloud["C"], cloud["m"], cloud["F"],
+                         cloud["vol"])
+    assert out["status"] == 0 and out["degenerate"] == 0
+    S = np.float32(2.0 ** grid["scale_log2"])
+    Mt = (cloud["m"] * S).astype(np.float32)
+    assert int(out["acc"][0].sum()) == int(np.rint(Mt).astype(np.int64).sum())
+    for k in range(3):
+        Qk = np.rint((Mt * cloud["v"][k]).astype(np.float32)).astype(np.int64)
+        assert int(out["acc"][1 + k].sum()) == int(Qk.sum())
