@@ -76,7 +76,16 @@ typedef struct mpm_grid_desc {
  * x = int32 positions in 1/65,536 of a cell, v = int64, m = int64, C unused.
  * id: optional uint32 particle identities (NULL if unused); only the calls
  * that move particles (mpm_permute, mpm_g2p_sorted, mpm_step_sorted,
- * mpm_step_host) touch it, carrying it along with the particle. */
+ * mpm_step_host) touch it, carrying it along with the particle.
+ *
+ * Elastic state (optional; F[0] == NULL for none, the APIC transfer alone):
+ * F = deformation gradient, dim*dim fp32 planes in the layout of C
+ * (F[k*dim + l]); vol = rest volume V0 per particle (fp32); mu, lambda = the
+ * Lame constants of the particles' Neo-Hookean material.  With it, mpm_p2g
+ * adds the MLS-MPM stress to the affine matrix it scatters and mpm_g2p
+ * advances F (implementation guide, section 3.1, Part 2; section 3.3.2,
+ * F <- (I + D) F); the calls that move particles carry F and vol along.
+ * Not used by MPM_ACC_EXACT_INT. */
 typedef struct mpm_particles {
     int64_t n;
     void *x[3];
@@ -84,6 +93,10 @@ typedef struct mpm_particles {
     void *C[9];
     const void *m;
     void *id;
+    void *F[9];
+    void *vol;
+    float mu;
+    float lambda;
 } mpm_particles;
 
 /* Status words (device, uint32), in mpm_bins.status. */
@@ -98,6 +111,8 @@ enum {
     MPM_ST_N_BIG_TILES = 7,  /* buckets whose runs were sorted in global memory (cold, huge buckets) */
     MPM_ST_N_RUNS = 8,       /* runs: maximal index ranges of one bucket (= buckets when already sorted) */
     MPM_ST_N_LARGE_BUCKETS = 9, /* buckets of more than 512 runs (sorted by one block each) */
+    MPM_ST_N_DEGENERATE = 10, /* elastic particles the last P2G scattered without stress: det F
+                                 not a positive normal fp32 number (inverted or collapsed) */
     MPM_ST_WORK_P2G = 11,    /* internal: work counter of the P2G launch */
     MPM_ST_WORK_G2P = 12,    /* internal: work counter of the G2P launch */
     MPM_ST_MAX_SPEED = 13,   /* fp32 bits of max over the particles the last G2P moved of
@@ -171,6 +186,17 @@ mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
  * reach 2^22 in magnitude (wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) > 2^22 - 4096,
  * wmax = 0.75^dim) is not scattered and is counted in MPM_ST_N_OUT_OF_RANGE.
  * MPM_ACC_F32 adds the fp32 values Wt*vel with float atomics instead.
+ * Elastic particles (parts->F[0] != NULL) scatter with C replaced by the
+ * MLS-MPM affine matrix C' = C - kappa*tau (implementation guide, section
+ * 3.1, Part 2: J = det F, P = mu (F - F^-T) + lambda ln(J) F^-T,
+ * sigma = P F^T / J; the force -dt V sigma (4/dx^2) w (x_i - x_p) with
+ * V = V0 J, divided by m): tau = J sigma = mu (F F^T - I) + lambda ln(J) I,
+ * kappa = ((dt*V0)*c4s)/m, c4s = (4*inv_dx)*inv_dx, each step one fp32
+ * rounding in the order the oracle states, ln computed by the library's own
+ * series (not the CUDA math library) so that it is reproducible.  C' also
+ * enters the range test.  A particle whose det F is not a positive normal
+ * fp32 number keeps C and is counted in MPM_ST_N_DEGENERATE.  `dt` is only
+ * read for elastic particles.
  * MPM_ACC_EXACT_INT (2D or 3D, order 1): integer positions X (1/65,536 cell),
  * int64 m and v; the far node's share of q is q*F/65,536 rounded to nearest
  * (ties to even), the near node gets the rest, split along x then y (then z);
@@ -180,7 +206,7 @@ mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
  * `bins` (from mpm_bins_init for this descriptor) only carries the status words.
  */
 mpm_status mpm_p2g(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, void *grid_acc,
-                   void *stream);
+                   float dt, void *stream);
 
 /*
  * mpm_grid_update -- for each node of the tiles that hold particles (and their
@@ -200,6 +226,8 @@ mpm_status mpm_grid_update(const mpm_grid_desc *desc, void *grid_acc, float *gri
  * (APIC, "gather d and D (= B*4)" in cell units); x' = fma(dt, v', x).
  * The stencil sums run axis by axis, innermost axis first, each three-term
  * sum as fma(w2,t2, fma(w1,t1, w0*t0)), the same order the oracle uses.
+ * Elastic particles also get F' = (I + dt C') F, each entry as
+ * fma(D_k2, F_2l, fma(D_k1, F_1l, fma(D_k0, F_0l, F_kl))) with D = dt*C'.
  * Particles outside the domain are left unchanged.
  * MPM_ACC_EXACT_INT: `grid` is the int64 accumulator; each on-grid particle's v is set
  * to its cell's momentum over its cell's mass, rounded to nearest (ties to even).
@@ -222,12 +250,13 @@ mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *p
  * cells that use different shared-memory banks, which the next step's P2G
  * and G2P exploit.  A slice of at most 32 particles (one round) keeps bin
  * order.  The remaining particles (outside the domain) are copied
- * unchanged to out[j] = in[perm[j]].  m and id are carried along.  This is
+ * unchanged to out[j] = in[perm[j]].  m, id and vol are carried along.  This is
  * the ping-pong buffer of "Particle Worlds, part 3", Step 4 ("the sort writes
  * into a second buffer"): the next step's binning then starts from almost
  * sorted particles, so its runs are long and every particle pass reads and
  * writes contiguous memory.  The bits of every particle's new state are those
- * of mpm_g2p.  `in` and `out` must not overlap.
+ * of mpm_g2p.  `in` and `out` must not overlap, and both or neither carry an
+ * elastic state.
  */
 mpm_status mpm_g2p_sorted(const mpm_grid_desc *desc, const float *grid_vel, const mpm_particles *in,
                           mpm_particles *out, mpm_bins *bins, float dt, void *stream);
@@ -248,9 +277,10 @@ mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_par
 
 /*
  * mpm_step_host -- one step from and back to HOST particle arrays: copies the
- * host SoA (`host`: x, v, C, m and id if given; pinned memory gives full copy
- * bandwidth) into the device arrays `dev_in`, runs mpm_step_sorted into
- * `dev_out`, and copies x, v, C, m (and id) of `dev_out` back into `host`, so
+ * host SoA (`host`: x, v, C, m, and id, F and vol if given; pinned memory
+ * gives full copy bandwidth) into the device arrays `dev_in`, runs
+ * mpm_step_sorted into `dev_out`, and copies the same arrays of `dev_out`
+ * back into `host`, so
  * the host arrays hold the new state in the order mpm_g2p_sorted writes.  Asynchronous on `stream`;
  * the host arrays must stay valid until it completes.
  */

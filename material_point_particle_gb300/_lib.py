@@ -19,6 +19,7 @@ MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
 (ST_FLAGS, ST_N_OUTSIDE, ST_N_OUT_OF_RANGE, ST_N_VALID, ST_N_SLICES, ST_N_ACTIVE, ST_MAX_NEIGHBOURS,
  ST_N_BIG_TILES, ST_N_RUNS, ST_N_LARGE_BUCKETS) = range(10)
 ST_BIN_WORDS = 10   # status words 0..9 are written by mpm_bin
+ST_N_DEGENERATE = 10  # elastic particles the last P2G scattered without stress (det F not positive normal)
 ST_MAX_SPEED = 13   # fp32 bits of max |v'| + 1.5 dx |C'|_F over the particles the last G2P moved
 MPM_STATUS_WORDS = 16
 MPM_STATIC_WORKSPACE_BYTES = 16 << 20
@@ -38,7 +39,8 @@ class GridDesc(ct.Structure):
 
 class Particles(ct.Structure):
     _fields_ = [("n", ct.c_int64), ("x", ct.c_void_p * 3), ("v", ct.c_void_p * 3), ("C", ct.c_void_p * 9),
-                ("m", ct.c_void_p), ("id", ct.c_void_p)]
+                ("m", ct.c_void_p), ("id", ct.c_void_p), ("F", ct.c_void_p * 9), ("vol", ct.c_void_p),
+                ("mu", ct.c_float), ("lambda_", ct.c_float)]
 
 
 class Bins(ct.Structure):
@@ -71,7 +73,7 @@ def library() -> ct.CDLL:
             L.mpm_grid_vel_bytes.argtypes = [P(GridDesc)]
             L.mpm_grid_vel_bytes.restype = ct.c_size_t
             L.mpm_bin.argtypes = [P(GridDesc), P(Particles), P(Bins), ct.c_int, VP]
-            L.mpm_p2g.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, VP]
+            L.mpm_p2g.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, ct.c_float, VP]
             L.mpm_grid_update.argtypes = [P(GridDesc), VP, VP, P(ct.c_float), P(Bins), VP]
             L.mpm_g2p.argtypes = [P(GridDesc), VP, P(Particles), P(Bins), ct.c_float, VP]
             L.mpm_step.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, VP, ct.c_float, P(ct.c_float), VP]
@@ -122,10 +124,19 @@ def grid_desc(grid: dict) -> GridDesc:
 
 
 def particles(x: torch.Tensor, v: torch.Tensor, C: torch.Tensor | None, m: torch.Tensor,
-              id: torch.Tensor | None = None) -> Particles:
+              id: torch.Tensor | None = None, F: torch.Tensor | None = None, vol: torch.Tensor | None = None,
+              mu: float = 0.0, lam: float = 0.0) -> Particles:
     """SoA view of [dim, n] / [dim*dim, n] / [n] tensors (rows must be contiguous),
-    with optional uint32-sized [n] particle ids."""
+    with optional uint32-sized [n] particle ids and an optional elastic state
+    (F [dim*dim, n], vol [n], Lame constants mu and lam)."""
     p = Particles()
+    if F is not None:
+        assert F.is_contiguous() and vol is not None and vol.is_contiguous()
+        for i in range(F.shape[0]):
+            p.F[i] = F[i].data_ptr()
+        p.vol = vol.data_ptr()
+        p.mu = mu
+        p.lambda_ = lam
     if id is not None:
         assert id.is_contiguous() and id.element_size() == 4
         p.id = id.data_ptr()
@@ -172,9 +183,9 @@ def mpm_bin(desc: GridDesc, parts: Particles, bins: Bins, flags: int = 0, stream
     _check(library().mpm_bin(ct.byref(desc), ct.byref(parts), ct.byref(bins), flags, _stream(stream)), "mpm_bin")
 
 
-def mpm_p2g(desc: GridDesc, parts: Particles, bins: Bins, grid_acc: torch.Tensor, stream=None):
+def mpm_p2g(desc: GridDesc, parts: Particles, bins: Bins, grid_acc: torch.Tensor, dt: float = 0.0, stream=None):
     _check(library().mpm_p2g(ct.byref(desc), ct.byref(parts), ct.byref(bins), ct.c_void_p(grid_acc.data_ptr()),
-                             _stream(stream)), "mpm_p2g")
+                             ct.c_float(dt), _stream(stream)), "mpm_p2g")
 
 
 def _f3(vals) -> ct.Array:

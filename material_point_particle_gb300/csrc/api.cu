@@ -163,6 +163,16 @@ mpm_status parts_f(const GridP &g, const mpm_particles *p, bool need_state, Part
     out.m = static_cast<const float *>(p->m);
     if (!out.m && p->n) return MPM_E_ARG;
     out.id = static_cast<uint32_t *>(p->id);
+    if (p->F[0]) {  // elastic state: every F plane and vol
+        for (int j = 0; j < g.dim * g.dim; ++j) {
+            out.F[j] = static_cast<float *>(p->F[j]);
+            if (!out.F[j]) return MPM_E_ARG;
+        }
+        out.vol = static_cast<float *>(p->vol);
+        if (!out.vol) return MPM_E_ARG;
+        out.mu = p->mu;
+        out.lam = p->lambda;
+    }
     return MPM_OK;
 }
 
@@ -285,7 +295,7 @@ mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
 }
 
 mpm_status mpm_p2g(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, void *grid_acc,
-                   void *stream) {
+                   float dt, void *stream) {
     GridP g;
     MPM_TRY(make_grid(desc, g));
     if (!grid_acc) return MPM_E_ARG;
@@ -305,7 +315,7 @@ mpm_status mpm_p2g(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
     MPM_TRY(parts_f(g, parts, true, p));
     MPM_TRY(check_bins(g, bins, p.n));
     MPM_TRY(device_info(dev));
-    return launch_p2g(g, p, view_of(g, *bins), grid_acc, dev, static_cast<cudaStream_t>(stream));
+    return launch_p2g(g, p, view_of(g, *bins), grid_acc, dt, dev, static_cast<cudaStream_t>(stream));
 }
 
 mpm_status mpm_grid_update(const mpm_grid_desc *desc, void *grid_acc, float *grid_vel, const float dtg[3],
@@ -342,7 +352,7 @@ mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *p
 mpm_status mpm_step(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *bins, void *grid_acc, float *grid_vel,
                     float dt, const float dtg[3], void *stream) {
     MPM_TRY(mpm_bin(desc, parts, bins, 0, stream));
-    MPM_TRY(mpm_p2g(desc, parts, bins, grid_acc, stream));
+    MPM_TRY(mpm_p2g(desc, parts, bins, grid_acc, dt, stream));
     MPM_TRY(mpm_grid_update(desc, grid_acc, grid_vel, dtg, bins, stream));
     return mpm_g2p(desc, grid_vel, parts, bins, dt, stream);
 }
@@ -355,7 +365,7 @@ mpm_status mpm_g2p_sorted(const mpm_grid_desc *desc, const float *grid_vel, cons
     PartsF pi, po;
     MPM_TRY(parts_f(g, in, true, pi));
     MPM_TRY(parts_f(g, out, true, po));
-    if (pi.n != po.n || (!pi.id) != (!po.id)) return MPM_E_ARG;
+    if (pi.n != po.n || (!pi.id) != (!po.id) || (!pi.F[0]) != (!po.F[0])) return MPM_E_ARG;
     MPM_TRY(check_bins(g, bins, pi.n));
     DeviceInfo dev;
     MPM_TRY(device_info(dev));
@@ -365,7 +375,7 @@ mpm_status mpm_g2p_sorted(const mpm_grid_desc *desc, const float *grid_vel, cons
 mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
                            void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream) {
     MPM_TRY(mpm_bin(desc, in, bins, 0, stream));
-    MPM_TRY(mpm_p2g(desc, in, bins, grid_acc, stream));
+    MPM_TRY(mpm_p2g(desc, in, bins, grid_acc, dt, stream));
     MPM_TRY(mpm_grid_update(desc, grid_acc, grid_vel, dtg, bins, stream));
     return mpm_g2p_sorted(desc, grid_vel, in, out, bins, dt, stream);
 }
@@ -382,6 +392,7 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
     MPM_TRY(parts_f(g, dev_out, true, pb));
     if (ph.n != pa.n || ph.n != pb.n) return MPM_E_ARG;
     if ((!ph.id) != (!pa.id) || (!ph.id) != (!pb.id)) return MPM_E_ARG;
+    if ((!ph.F[0]) != (!pa.F[0]) || (!ph.F[0]) != (!pb.F[0])) return MPM_E_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)ph.n * sizeof(float);
     auto copy = [&](void *dst, const void *src, cudaMemcpyKind kind) {
@@ -394,6 +405,10 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
         for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(pa.C[j], ph.C[j], cudaMemcpyHostToDevice);
         ok = ok && copy(const_cast<float *>(pa.m), ph.m, cudaMemcpyHostToDevice);
         if (ph.id) ok = ok && copy(pa.id, ph.id, cudaMemcpyHostToDevice);
+        if (ph.F[0]) {
+            for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(pa.F[j], ph.F[j], cudaMemcpyHostToDevice);
+            ok = ok && copy(pa.vol, ph.vol, cudaMemcpyHostToDevice);
+        }
         if (!ok) return MPM_E_CUDA;
     }
     MPM_TRY(mpm_step_sorted(desc, dev_in, dev_out, bins, grid_acc, grid_vel, dt, dtg, stream));
@@ -404,6 +419,10 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
         for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(ph.C[j], pb.C[j], cudaMemcpyDeviceToHost);
         ok = ok && copy(const_cast<float *>(ph.m), pb.m, cudaMemcpyDeviceToHost);
         if (ph.id) ok = ok && copy(ph.id, pb.id, cudaMemcpyDeviceToHost);
+        if (ph.F[0]) {
+            for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(ph.F[j], pb.F[j], cudaMemcpyDeviceToHost);
+            ok = ok && copy(ph.vol, pb.vol, cudaMemcpyDeviceToHost);
+        }
         if (!ok) return MPM_E_CUDA;
     }
     return MPM_OK;

@@ -55,6 +55,9 @@ struct PartsF {
     float *C[9];
     const float *m;
     uint32_t *id;
+    float *F[9];  // elastic state (F[0] null for none): deformation gradient
+    float *vol;   // and rest volume
+    float mu, lam;
     int64_t n;
 };
 
@@ -201,12 +204,19 @@ struct Prefetch {
     __device__ float *at(int stage, int f) const { return buf + (stage * NF + f) * NT + threadIdx.x; }
 };
 
-// The particle record of P2G: x[dim], v[dim], C[dim*dim], m.
-template <int DIM>
+// The particle record of P2G: x[dim], v[dim], C[dim*dim], m, and with the
+// elastic state F[dim*dim], vol.
+template <int DIM, bool EL = false>
 struct P2GFields {
-    static constexpr int NF = DIM + DIM + DIM * DIM + 1;
+    static constexpr int BASE = DIM + DIM + DIM * DIM + 1;  // index of F[0]
+    static constexpr int NF = BASE + (EL ? DIM * DIM + 1 : 0);
     __device__ static const float *src(const PartsF &p, int f) {
-        return f < DIM ? p.x[f] : f < 2 * DIM ? p.v[f - DIM] : f < 2 * DIM + DIM * DIM ? p.C[f - 2 * DIM] : p.m;
+        return f < DIM                    ? p.x[f]
+               : f < 2 * DIM              ? p.v[f - DIM]
+               : f < 2 * DIM + DIM * DIM  ? p.C[f - 2 * DIM]
+               : f < BASE                 ? p.m
+               : f < BASE + DIM * DIM     ? p.F[f - BASE]
+                                          : p.vol;
     }
 };
 

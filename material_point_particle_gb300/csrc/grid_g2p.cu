@@ -8,11 +8,13 @@
 //
 // G2P (section 1: a gather, every particle writes only itself; section 3.1
 // Part 1 and 3.3.2 "gather d and D (= B*4)"): new velocity, APIC affine matrix
-// C = B * 4/dx^2 in cell units, advection x += dt v.
+// C = B * 4/dx^2 in cell units, advection x += dt v; for elastic particles
+// also F <- (I + dt C) F (section 3.3.2; stress.cuh).
 #include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
+#include "stress.cuh"
 
 namespace mpm {
 
@@ -121,6 +123,11 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
     for (int j = 0; j < DIM * DIM; ++j) q.C[j][dst] = p.C[j][src];
     const_cast<float *>(q.m)[dst] = p.m[src];
     if (q.id && p.id) q.id[dst] = p.id[src];
+    if (q.F[0] && p.F[0]) {
+#pragma unroll
+        for (int j = 0; j < DIM * DIM; ++j) q.F[j][dst] = p.F[j][src];
+        q.vol[dst] = p.vol[src];
+    }
 }
 
 // Velocity halo of one tile in shared memory, in the compact layout of the
@@ -142,8 +149,9 @@ __device__ __forceinline__ float2 sum3x2(const float2 w[3], const float2 t[3]) {
 // arrays and index in place; the sorted output otherwise, m and id with it).
 // rec(f): the particle's staged fields x[dim], then (sorted output) m and the
 // id bits.  The x and y components go through packed fp32x2 arithmetic, which
-// rounds each lane exactly as the scalar operation.
-template <int DIM, int T, bool SORTED, typename Rec>
+// rounds each lane exactly as the scalar operation.  Elastic particles (EL)
+// read F (and, sorted, vol) of `pid` from global memory and write F'.
+template <int DIM, int T, bool SORTED, bool EL, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
                                            uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
                                            float dt, float c4, float &smax) {
@@ -155,6 +163,11 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     if (!in_tile_x<DIM>(g, x, o, b, f)) {
         if constexpr (SORTED) copy_particle<DIM>(p, q, pid, dst);
         return;
+    }
+    [[maybe_unused]] float Fo[EL ? DIM * DIM : 1];
+    if constexpr (EL) {
+#pragma unroll
+        for (int j = 0; j < DIM * DIM; ++j) Fo[j] = p.F[j][pid];
     }
     float w[3][3], we[3][3];
 #pragma unroll
@@ -247,6 +260,7 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     }
     // the advective bound's term |v'| + 1.5 dx |C'|_F, sums in index order
     float sv2 = 0.f, sc2 = 0.f;
+    float Cn[DIM * DIM];
 #pragma unroll
     for (int k = 0; k < DIM; ++k) {
         q.v[k][dst] = vn[k];
@@ -254,9 +268,17 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
 #pragma unroll
         for (int l = 0; l < DIM; ++l) {
             const float c = __fmul_rn(Bm[k][l], c4);
+            Cn[k * DIM + l] = c;
             q.C[k * DIM + l][dst] = c;
             sc2 = __fadd_rn(sc2, __fmul_rn(c, c));
         }
+    }
+    if constexpr (EL) {
+        float Fn[DIM * DIM];
+        advance_F<DIM>(dt, Cn, Fo, Fn);
+#pragma unroll
+        for (int j = 0; j < DIM * DIM; ++j) q.F[j][dst] = Fn[j];
+        if constexpr (SORTED) q.vol[dst] = p.vol[pid];
     }
     smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
 #pragma unroll
@@ -299,7 +321,7 @@ __device__ __forceinline__ uint32_t interleave_entry(uint32_t pos, uint32_t cnt)
 // interleaved slice, so that its writes are coalesced and its reads of the
 // velocity halo meet few bank conflicts.  A slice of at most 32 particles is
 // one round and keeps bin order.
-template <int DIM, int T, bool SORTED>
+template <int DIM, int T, bool SORTED, bool EL>
 __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                      const uint32_t *__restrict__ perm,
                                                      const uint32_t *__restrict__ key,
@@ -371,7 +393,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             if (threadIdx.x < cnt) {
                 const uint32_t r = threadIdx.x;
                 auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                gather_one<DIM, T, true>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
+                gather_one<DIM, T, true, EL>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
             }
         } else if constexpr (SORTED) {
             // stable counting sort of the slice by bank class: counts per
@@ -431,7 +453,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                     const uint32_t e = interleave_entry(pos, cnt);
                     const uint32_t r = order[e + (e >> 5)];
                     auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                    gather_one<DIM, T, true>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax);
+                    gather_one<DIM, T, true, EL>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax);
                 }
             }
         } else {
@@ -452,7 +474,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                 if (r < cnt) {
                     const int stage = qi & 1;
                     auto rec = [&](int f) { return *pf.at(stage, f); };
-                    gather_one<DIM, T, false>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4, smax);
+                    gather_one<DIM, T, false, EL>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4, smax);
                 }
             }
         }
@@ -470,37 +492,46 @@ __global__ void k_copy_rest(PartsF p, PartsF q, const uint32_t *__restrict__ per
         copy_particle<DIM>(p, q, perm[j], (uint32_t)j);
 }
 
-mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
-                      const DeviceInfo &dev, cudaStream_t st) {
+template <int DIM, int T, bool SORTED, bool EL>
+void launch_g2p_t(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w, float dt,
+                  const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
     const int blocks = dev.sms * 4;
-    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
-    if (g.dim == 3 && g.T == 4)
-        k_g2p<3, 4, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
-    else if (g.dim == 2 && g.T == 8)
-        k_g2p<2, 8, false><<<blocks, kP2GThreads, 0, st>>>(g, p, p, vel, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
-    else
-        return MPM_E_ARG;
-    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+    k_g2p<DIM, T, SORTED, EL><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start,
+                                                               w.status, dt, c4);
+    if constexpr (SORTED) k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
 }
 
-mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
-                             float dt, const DeviceInfo &dev, cudaStream_t st) {
-    const float c4 = 4.0f * g.inv_dx;
-    const int blocks = dev.sms * 4;
+template <bool SORTED>
+mpm_status launch_g2p_any(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
+                          float dt, const DeviceInfo &dev, cudaStream_t st) {
+    const bool el = in.F[0] != nullptr;
+    static_assert(MPM_ST_MAX_SPEED == MPM_ST_WORK_G2P + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
     if (g.dim == 3 && g.T == 4) {
-        k_g2p<3, 4, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start, w.status, dt,
-                                                          c4);
-        k_copy_rest<3><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+        if (el)
+            launch_g2p_t<3, 4, SORTED, true>(g, vel, in, out, w, dt, dev, st);
+        else
+            launch_g2p_t<3, 4, SORTED, false>(g, vel, in, out, w, dt, dev, st);
     } else if (g.dim == 2 && g.T == 8) {
-        k_g2p<2, 8, true><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start, w.status, dt,
-                                                          c4);
-        k_copy_rest<2><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+        if (el)
+            launch_g2p_t<2, 8, SORTED, true>(g, vel, in, out, w, dt, dev, st);
+        else
+            launch_g2p_t<2, 8, SORTED, false>(g, vel, in, out, w, dt, dev, st);
     } else {
         return MPM_E_ARG;
     }
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+}
+
+mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
+                      const DeviceInfo &dev, cudaStream_t st) {
+    return launch_g2p_any<false>(g, vel, p, p, w, dt, dev, st);
+}
+
+mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
+                             float dt, const DeviceInfo &dev, cudaStream_t st) {
+    return launch_g2p_any<true>(g, vel, in, out, w, dt, dev, st);
 }
 
 // --------------------------------------------------------------------------
@@ -519,9 +550,15 @@ __global__ void k_permute(int ncomp, PartsF in, PartsF out, const uint32_t *__re
             } else if (c < 15) {
                 s = in.C[c - 6];
                 d = out.C[c - 6];
-            } else {
+            } else if (c == 15) {
                 s = in.m;
                 d = const_cast<float *>(out.m);
+            } else if (c < 25) {
+                s = in.F[c - 16];
+                d = out.F[c - 16];
+            } else {
+                s = in.vol;
+                d = out.vol;
             }
             if (s && d) d[j] = s[src];
         }
@@ -532,7 +569,7 @@ __global__ void k_permute(int ncomp, PartsF in, PartsF out, const uint32_t *__re
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
                           const DeviceInfo &dev, cudaStream_t st) {
     const int blocks = dev.sms * 8;
-    k_permute<<<blocks, 256, 0, st>>>(16, in, out, perm, in.n);
+    k_permute<<<blocks, 256, 0, st>>>(26, in, out, perm, in.n);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }
 

@@ -18,6 +18,7 @@
 // particles, so no halo sum can overflow.
 #include "common.cuh"
 #include "internal.h"
+#include "stress.cuh"
 
 namespace mpm {
 
@@ -29,12 +30,31 @@ __device__ __forceinline__ int32_t rint_f(float a) { return __float_as_int(__fad
 
 
 
+// The particle's affine matrix as P2G scatters it: C, and for elastic
+// particles C minus the stress term (stress.cuh); counts the elastic
+// particles whose det F leaves them unstressed.
+template <int DIM, bool EL, typename Rec>
+__device__ __forceinline__ void load_affine(const Rec &rec, const StressP &sp, float (&C)[DIM * DIM],
+                                            uint32_t &degenerate) {
+    using Fl = P2GFields<DIM, EL>;
+#pragma unroll
+    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
+    if constexpr (EL) {
+        float F[DIM * DIM];
+#pragma unroll
+        for (int j = 0; j < DIM * DIM; ++j) F[j] = rec(Fl::BASE + j);
+        if (!fold_stress<DIM>(sp, F, rec(Fl::BASE + DIM * DIM), rec(2 * DIM + DIM * DIM), C)) ++degenerate;
+    }
+}
+
 // One particle's fixed-point shares, added to the tile accumulator as they
 // are formed (the arithmetic the oracle states).  Returns false (and adds
 // nothing) when the particle is out of range.
-// rec(f) reads field f of the particle (x[dim], v[dim], C[dim*dim], m).
-template <int DIM, int T, typename Hl, typename Rec>
-__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo) {
+// rec(f) reads field f of the particle (P2GFields: x[dim], v[dim],
+// C[dim*dim], m, then F[dim*dim] and vol for elastic particles).
+template <int DIM, int T, typename Hl, bool EL, typename Rec>
+__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo,
+                                              const StressP &sp, uint32_t &degenerate) {
     using St = Stencil<DIM>;
     float f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
@@ -45,8 +65,7 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     float v[DIM], C[DIM * DIM];
 #pragma unroll
     for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
-#pragma unroll
-    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
+    load_affine<DIM, EL>(rec, sp, C, degenerate);
     const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
     // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) at most 2^22 - 4096
     const float h = __fmul_rn(1.5f, g.dx);
@@ -127,8 +146,9 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     return true;
 }
 
-template <int DIM, int T, typename Rec>
-__device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, const int o[3], float *sacc) {
+template <int DIM, int T, bool EL, typename Rec>
+__device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, const int o[3], float *sacc,
+                                              const StressP &sp, uint32_t &degenerate) {
     using Hl = Halo<DIM, T>;
     float f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
@@ -139,8 +159,7 @@ __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, co
     float v[DIM], C[DIM * DIM], w[3][3], dd[3][3];
 #pragma unroll
     for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
-#pragma unroll
-    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
+    load_affine<DIM, EL>(rec, sp, C, degenerate);
     const float m = rec(2 * DIM + DIM * DIM);
 #pragma unroll
     for (int l = 0; l < DIM; ++l) {
@@ -207,14 +226,14 @@ __device__ __forceinline__ SliceMeta slice_meta(const uint32_t *slices, const ui
 // a round in different banks.
 constexpr int kP2GWarps = kP2GThreads / 32;
 
-template <int DIM, int T, typename AccT>
-__global__ void __launch_bounds__(kP2GThreads, 3) k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm,
-                                                              const uint32_t *__restrict__ slices,
-                                                              const uint32_t *__restrict__ start,
-                                                              uint32_t *__restrict__ status, AccT *__restrict__ acc) {
+template <int DIM, int T, typename AccT, bool EL>
+__global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
+    k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm, const uint32_t *__restrict__ slices,
+                const uint32_t *__restrict__ start, uint32_t *__restrict__ status, AccT *__restrict__ acc,
+                StressP sp) {
     using St = Stencil<DIM>;
     using Hl = HaloU<DIM, T>;
-    using Fl = P2GFields<DIM>;
+    using Fl = P2GFields<DIM, EL>;
     constexpr int HW = St::NC * Hl::NODES;  // halo words per warp
     __shared__ __align__(16) int32_t shalo[kP2GWarps][HW];
     __shared__ float sbuf[kP2GWarps][2 * Fl::NF * 32];
@@ -232,7 +251,7 @@ __global__ void __launch_bounds__(kP2GThreads, 3) k_p2g_fixed(GridP g, PartsF p,
 #pragma unroll
         for (int f = 0; f < Fl::NF; ++f) cp_async4(at(stage, f), Fl::src(p, f) + pid);
     };
-    uint32_t s = 0;
+    uint32_t s = 0, degenerate = 0;
     if (lane == 0) s = atomicAdd(work, 1u);
     s = __shfl_sync(0xFFFFFFFFu, s, 0);
     while (s < nslices) {
@@ -279,7 +298,7 @@ __global__ void __launch_bounds__(kP2GThreads, 3) k_p2g_fixed(GridP g, PartsF p,
             if (r < cnt) {
                 const int st = stage;
                 auto rec = [&](int f) { return *at(st, f); };
-                if (!scatter_fixed<DIM, T, Hl>(g, rec, o, halo)) ++bad;
+                if (!scatter_fixed<DIM, T, Hl, EL>(g, rec, o, halo, sp, degenerate)) ++bad;
             }
             stage ^= 1;
             // int32 halo accumulators: at most 512 shares of magnitude below
@@ -295,18 +314,23 @@ __global__ void __launch_bounds__(kP2GThreads, 3) k_p2g_fixed(GridP g, PartsF p,
         s = __shfl_sync(0xFFFFFFFFu, ask, 0);
     }
     cp_async_wait<0>();
+    if constexpr (EL) {
+        degenerate = __reduce_add_sync(0xFFFFFFFFu, degenerate);
+        if (degenerate && lane == 0) atomicAdd(&status[MPM_ST_N_DEGENERATE], degenerate);
+    }
 }
 
 // Float-atomic P2G (comparison variant: fp32 adds, order dependent).
-template <int DIM, int T>
+template <int DIM, int T, bool EL>
 __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, const uint32_t *__restrict__ perm,
                                                            const uint32_t *__restrict__ slices,
                                                            const uint32_t *__restrict__ start,
                                                            uint32_t *__restrict__ status,
-                                                           float *__restrict__ acc) {
+                                                           float *__restrict__ acc, StressP sp) {
     using St = Stencil<DIM>;
     using Hl = Halo<DIM, T>;
-    using Fl = P2GFields<DIM>;
+    using Fl = P2GFields<DIM, EL>;
+    uint32_t degenerate = 0;
     __shared__ float sacc[St::NC * Hl::SIZE];
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
@@ -328,7 +352,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
         for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x) {
             const uint32_t pid = perm[beg + r];
             auto rec = [&](int f) { return Fl::src(p, f)[pid]; };
-            scatter_float<DIM, T>(g, rec, o, sacc);
+            scatter_float<DIM, T, EL>(g, rec, o, sacc, sp, degenerate);
         }
         __syncthreads();
         for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
@@ -345,32 +369,44 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
         }
         __syncthreads();
     }
+    if constexpr (EL) {
+        degenerate = __reduce_add_sync(0xFFFFFFFFu, degenerate);
+        if (degenerate && lane_id() == 0) atomicAdd(&status[MPM_ST_N_DEGENERATE], degenerate);
+    }
 }
 
-mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const DeviceInfo &dev,
-                      cudaStream_t st) {
+template <int DIM, int T, bool EL>
+void launch_p2g_t(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const StressP &sp, int blocks,
+                  cudaStream_t st) {
+    if (g.acc_mode == MPM_ACC_I64)
+        k_p2g_fixed<DIM, T, int64_t, EL><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+                                                                        (int64_t *)grid_acc, sp);
+    else if (g.acc_mode == MPM_ACC_I32)
+        k_p2g_fixed<DIM, T, int32_t, EL><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+                                                                        (int32_t *)grid_acc, sp);
+    else
+        k_p2g_float<DIM, T, EL><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+                                                               (float *)grid_acc, sp);
+}
+
+mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt,
+                      const DeviceInfo &dev, cudaStream_t st) {
     const int blocks = dev.sms * 4;
-    cudaMemsetAsync(&w.status[MPM_ST_WORK_P2G], 0, sizeof(uint32_t), st);
+    const bool el = p.F[0] != nullptr;
+    const StressP sp{p.mu, p.lam, dt, (4.0f * g.inv_dx) * g.inv_dx};
+    // degenerate-particle count and work counter
+    static_assert(MPM_ST_WORK_P2G == MPM_ST_N_DEGENERATE + 1, "adjacent status words");
+    cudaMemsetAsync(&w.status[MPM_ST_N_DEGENERATE], 0, 2 * sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4) {
-        if (g.acc_mode == MPM_ACC_I64)
-            k_p2g_fixed<3, 4, int64_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                          (int64_t *)grid_acc);
-        else if (g.acc_mode == MPM_ACC_I32)
-            k_p2g_fixed<3, 4, int32_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                          (int32_t *)grid_acc);
+        if (el)
+            launch_p2g_t<3, 4, true>(g, p, w, grid_acc, sp, blocks, st);
         else
-            k_p2g_float<3, 4><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                 (float *)grid_acc);
+            launch_p2g_t<3, 4, false>(g, p, w, grid_acc, sp, blocks, st);
     } else if (g.dim == 2 && g.T == 8) {
-        if (g.acc_mode == MPM_ACC_I64)
-            k_p2g_fixed<2, 8, int64_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                          (int64_t *)grid_acc);
-        else if (g.acc_mode == MPM_ACC_I32)
-            k_p2g_fixed<2, 8, int32_t><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                          (int32_t *)grid_acc);
+        if (el)
+            launch_p2g_t<2, 8, true>(g, p, w, grid_acc, sp, blocks, st);
         else
-            k_p2g_float<2, 8><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                 (float *)grid_acc);
+            launch_p2g_t<2, 8, false>(g, p, w, grid_acc, sp, blocks, st);
     } else {
         return MPM_E_ARG;
     }

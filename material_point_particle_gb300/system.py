@@ -46,7 +46,10 @@ class MPMSystem:
         self.dt = float(grid.get("dt", 0.0))
         self.dtg = dt_times_g(grid) if "g" in grid else [0.0, 0.0, 0.0]
         self.x = self.v = self.C = self.m = None
-        self.parts = None
+        self.id = self.id2 = None
+        self.F = self.vol = self.F2 = self.vol2 = None
+        self.material = {"mu": 0.0, "lambda": 0.0}
+        self.parts = self.parts2 = None
 
     # -- particle state -------------------------------------------------------
     def load(self, x, v, C, m):
@@ -61,8 +64,25 @@ class MPMSystem:
             f32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.float32)).to(self.device)
             self.x, self.v, self.C, self.m = f32(x), f32(v), f32(C), f32(m)
         assert self.x.shape[1] <= self.n
-        self.parts = L.particles(self.x, self.v, self.C, self.m)
+        self.parts = self._parts(self.x, self.v, self.C, self.m, None, self.F, self.vol)
         return self
+
+    def load_elastic(self, F, vol, material: dict):
+        """Adds the elastic state: deformation gradients F [dim*dim, n], rest
+        volumes vol [n] and the Neo-Hookean constants {"mu", "lambda"}."""
+        f32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.float32)).to(self.device)
+        self.F, self.vol = f32(F), f32(vol)
+        self.material = {"mu": float(material["mu"]), "lambda": float(material["lambda"])}
+        self.parts = self._parts(self.x, self.v, self.C, self.m, self.id, self.F, self.vol)
+        return self
+
+    def _parts(self, x, v, C, m, id, F, vol):
+        return L.particles(x, v, C, m, id, F, vol, self.material["mu"], self.material["lambda"])
+
+    def elastic_state(self):
+        """(F, vol) as numpy arrays."""
+        torch.cuda.synchronize(self.device)
+        return self.F.cpu().numpy(), self.vol.cpu().numpy()
 
     def state(self):
         """(x, v, C) as numpy arrays."""
@@ -75,7 +95,7 @@ class MPMSystem:
         L.mpm_bin(self.desc, self.parts, self.bins, 0, stream)
 
     def p2g(self, stream=None):
-        L.mpm_p2g(self.desc, self.parts, self.bins, self.acc, stream)
+        L.mpm_p2g(self.desc, self.parts, self.bins, self.acc, self.dt, stream)
 
     def grid_update(self, stream=None):
         L.mpm_grid_update(self.desc, self.acc, self.vel, self.dtg, self.bins, stream)
@@ -97,8 +117,10 @@ class MPMSystem:
         else:
             self.id = self.id2 = None
         self.x2, self.v2, self.C2, self.m2 = (torch.empty_like(t) for t in (self.x, self.v, self.C, self.m))
-        self.parts = L.particles(self.x, self.v, self.C, self.m, self.id)
-        self.parts2 = L.particles(self.x2, self.v2, self.C2, self.m2, self.id2)
+        if self.F is not None:
+            self.F2, self.vol2 = torch.empty_like(self.F), torch.empty_like(self.vol)
+        self.parts = self._parts(self.x, self.v, self.C, self.m, self.id, self.F, self.vol)
+        self.parts2 = self._parts(self.x2, self.v2, self.C2, self.m2, self.id2, self.F2, self.vol2)
         return self
 
     def swap(self):
@@ -107,6 +129,8 @@ class MPMSystem:
         self.C, self.C2 = self.C2, self.C
         self.m, self.m2 = self.m2, self.m
         self.id, self.id2 = self.id2, self.id
+        self.F, self.F2 = self.F2, self.F
+        self.vol, self.vol2 = self.vol2, self.vol
         self.parts, self.parts2 = self.parts2, self.parts
 
     def g2p_sorted(self, stream=None):

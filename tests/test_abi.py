@@ -3,6 +3,7 @@ rejects bad arguments on the host before touching a device (no GPU needed)."""
 import ctypes as ct
 import os
 import re
+import subprocess
 
 import pytest
 import torch
@@ -89,7 +90,16 @@ def test_workspace_carving_and_size_checks():
     # null particle arrays are refused
     p, _ = _parts(3, 10)
     p.v[1] = None
-    assert L.library().mpm_p2g(ct.byref(d), ct.byref(p), ct.byref(b), ct.c_void_p(base), None) == L.MPM_E_ARG
+    assert L.library().mpm_p2g(ct.byref(d), ct.byref(p), ct.byref(b), ct.c_void_p(base), 0.0, None) == L.MPM_E_ARG
+    # an elastic state needs every F plane and the rest volumes
+    p, keep = _parts(3, 10)
+    F = torch.zeros((9, 10))
+    for j in range(9):
+        p.F[j] = F[j].data_ptr()
+    assert L.library().mpm_p2g(ct.byref(d), ct.byref(p), ct.byref(b), ct.c_void_p(base), 0.0, None) == L.MPM_E_ARG
+    p.vol = F[0].data_ptr()
+    p.F[8] = None
+    assert L.library().mpm_p2g(ct.byref(d), ct.byref(p), ct.byref(b), ct.c_void_p(base), 0.0, None) == L.MPM_E_ARG
 
 
 def test_grid_byte_counts():
@@ -111,3 +121,25 @@ def test_valid_call_without_device_fails_loudly():
     code = L.library().mpm_bin(ct.byref(d), ct.byref(p), ct.byref(b), 0, None)
     assert code == L.MPM_E_NO_DEVICE
     assert "device" in L.strerror(code)
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of the C structs have the header's sizes and offsets."""
+    src = tmp_path / "layout.c"
+    src.write_text("""
+#include <stddef.h>
+#include <stdio.h>
+#include "mpm.h"
+int main(void) {
+    printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(mpm_grid_desc), sizeof(mpm_particles), sizeof(mpm_bins),
+           offsetof(mpm_particles, id), offsetof(mpm_particles, F), offsetof(mpm_particles, vol),
+           offsetof(mpm_particles, mu), offsetof(mpm_particles, lambda));
+    return 0;
+}
+""")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(t) for t in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    P = L.Particles
+    assert got == [ct.sizeof(L.GridDesc), ct.sizeof(P), ct.sizeof(L.Bins), P.id.offset, P.F.offset,
+                   P.vol.offset, P.mu.offset, P.lambda_.offset]
