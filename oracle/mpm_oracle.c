@@ -241,15 +241,53 @@ static int64_t rint_product(float a, float b)
     return (int64_t)nearbyint((double)a * (double)b);
 }
 
+/* The grid-recovered volume channel (implementation guide, section 3.3.2,
+ * "grid-recovered volume": each particle scatters its rest volume as a
+ * fraction of a cell, 1/ppc for a rest packing, so that a node of a
+ * rest-packed region sums to about one; G2P gathers the node values back).
+ * The quantity is q = V0 * inv_dx^dim (inv_dx^3 = (inv_dx*inv_dx)*inv_dx),
+ * scattered as the mass is: Vt = q*S, share rint(((wx*Vt)*wy)*wz), the centre
+ * node takes rint(Vt) minus the other shares, and the particle's range test
+ * also requires wmax*|Vt| <= 2^22 - 4096.  It is the last plane of acc.     */
+static float cells_of_volume(const orc_desc *d, float V0)
+{
+    float c = d->inv_dx * d->inv_dx;
+    if (d->dim == 3)
+        c = c * d->inv_dx;
+    return V0 * c;
+}
+
+static uint32_t p2g_fixed_core(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                               const float *const *C, const float *m, const float *vol, int64_t *acc,
+                               int64_t counts[2]);
+
 /* acc: (dim+1) planes of nodes_of(d) int64 values (mass, then momentum per
  * axis), zeroed by the caller.  counts[0] = out-of-domain particles,
  * counts[1] = out-of-range particles.  Returns the status bits.            */
 uint32_t orc_p2g_fixed(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
                        const float *const *C, const float *m, int64_t *acc, int64_t counts[2])
 {
+    return p2g_fixed_core(d, np, x, v, C, m, NULL, acc, counts);
+}
+
+/* The same with the volume channel: acc has dim+2 planes, the last one the
+ * rest volume in cells.                                                     */
+uint32_t orc_p2g_fixed_vol(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                           const float *const *C, const float *m, const float *vol, int64_t *acc,
+                           int64_t counts[2])
+{
+    return p2g_fixed_core(d, np, x, v, C, m, vol, acc, counts);
+}
+
+static uint32_t p2g_fixed_core(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                               const float *const *C, const float *m, const float *vol, int64_t *acc,
+                               int64_t counts[2])
+{
     int dim = d->dim;
     int64_t nodes = nodes_of(d);
     float S = ldexpf(1.0f, d->scale_log2);
+    float wmax = dim == 3 ? 0.421875f : 0.5625f;
+    int64_t vplane = (int64_t)(dim + 1) * nodes;
     counts[0] = counts[1] = 0;
     for (int64_t p = 0; p < np; ++p) {
         int b[3];
@@ -259,7 +297,8 @@ uint32_t orc_p2g_fixed(const orc_desc *d, int64_t np, const float *const *x, con
             continue;
         }
         float Mt = m[p] * S;
-        if (!in_range(d, Mt, v, C, p)) {
+        float Vt = vol ? cells_of_volume(d, vol[p]) * S : 0.0f;
+        if (!in_range(d, Mt, v, C, p) || !((wmax * fabsf(Vt)) <= ORC_SHARE_LIMIT)) {
             counts[1] += 1;
             continue;
         }
@@ -279,6 +318,7 @@ uint32_t orc_p2g_fixed(const orc_desc *d, int64_t np, const float *const *x, con
         for (int k = 0; k < dim; ++k)
             Q[1 + k] = (int64_t)rintf(Mt * v[k][p]);
         int64_t rest[4] = {Q[0], Q[1], Q[2], Q[3]};
+        int64_t vrest = (int64_t)rintf(Vt);
         int a2n = dim == 3 ? 3 : 1;
         for (int a0 = 0; a0 < 3; ++a0)
             for (int a1 = 0; a1 < 3; ++a1)
@@ -293,6 +333,14 @@ uint32_t orc_p2g_fixed(const orc_desc *d, int64_t np, const float *const *x, con
                     int64_t sm = (int64_t)rintf(Wt);
                     acc[node] += sm;
                     rest[0] -= sm;
+                    if (vol) {
+                        float Wv = (w[0][a0] * Vt) * w[1][a1];
+                        if (dim == 3)
+                            Wv = Wv * w[2][a2];
+                        int64_t sv = (int64_t)rintf(Wv);
+                        acc[vplane + node] += sv;
+                        vrest -= sv;
+                    }
                     for (int k = 0; k < dim; ++k) {
                         float vel = fmaf(C[k * dim + 0][p], dd[0][a0], v[k][p]);
                         vel = fmaf(C[k * dim + 1][p], dd[1][a1], vel);
@@ -306,6 +354,8 @@ uint32_t orc_p2g_fixed(const orc_desc *d, int64_t np, const float *const *x, con
         int64_t cnode = node_at(d, b[0] + 1, b[1] + 1, dim == 3 ? b[2] + 1 : 0);
         for (int c = 0; c <= dim; ++c)
             acc[(int64_t)c * nodes + cnode] += rest[c];
+        if (vol)
+            acc[vplane + cnode] += vrest;
     }
     return (counts[0] ? ORC_ST_DOMAIN : 0u) | (counts[1] ? ORC_ST_BOUND : 0u);
 }
@@ -314,11 +364,32 @@ uint32_t orc_p2g_fixed(const orc_desc *d, int64_t np, const float *const *x, con
  * float atomics are order-dependent).  The node value is the sum over
  * particles of the fp32 terms u_m(a) = W(a), u_k(a) = W(a) * vel_k(a) with
  * W(a) = ((wx*m)*wy)*wz; the oracle adds them in fp64.                      */
+static uint32_t p2g_float_core(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                               const float *const *C, const float *m, const float *vol, double *acc,
+                               int64_t counts[2]);
+
 uint32_t orc_p2g_float(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
                        const float *const *C, const float *m, double *acc, int64_t counts[2])
 {
+    return p2g_float_core(d, np, x, v, C, m, NULL, acc, counts);
+}
+
+/* With the volume channel (last plane): the fp32 terms ((wx*q)*wy)*wz of
+ * q = V0 * inv_dx^dim, summed in fp64.                                      */
+uint32_t orc_p2g_float_vol(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                           const float *const *C, const float *m, const float *vol, double *acc,
+                           int64_t counts[2])
+{
+    return p2g_float_core(d, np, x, v, C, m, vol, acc, counts);
+}
+
+static uint32_t p2g_float_core(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                               const float *const *C, const float *m, const float *vol, double *acc,
+                               int64_t counts[2])
+{
     int dim = d->dim;
     int64_t nodes = nodes_of(d);
+    int64_t vplane = (int64_t)(dim + 1) * nodes;
     counts[0] = counts[1] = 0;
     for (int64_t p = 0; p < np; ++p) {
         int b[3];
@@ -347,6 +418,12 @@ uint32_t orc_p2g_float(const orc_desc *d, int64_t np, const float *const *x, con
                         W = W * w[2][a2];
                     int64_t node = node_at(d, b[0] + a0, b[1] + a1, dim == 3 ? b[2] + a2 : 0);
                     acc[node] += (double)W;
+                    if (vol) {
+                        float Wv = (w[0][a0] * cells_of_volume(d, vol[p])) * w[1][a1];
+                        if (dim == 3)
+                            Wv = Wv * w[2][a2];
+                        acc[vplane + node] += (double)Wv;
+                    }
                     for (int k = 0; k < dim; ++k) {
                         float vel = fmaf(C[k * dim + 0][p], dd[0][a0], v[k][p]);
                         vel = fmaf(C[k * dim + 1][p], dd[1][a1], vel);
@@ -674,6 +751,64 @@ static int64_t g2p_core(const orc_desc *d, const float *vel, int64_t np, float *
         moved += 1;
     }
     return moved;
+}
+
+/* Grid volume fraction from the volume channel: phi = (float)V * 2^-scale
+ * (fixed point; the int64 sum rounded once, the scale exact), or the fp64 sum
+ * rounded to fp32 (float mode).  vplane: the channel's nodes_of(d) values.  */
+void orc_grid_volume_fixed(const orc_desc *d, const int64_t *vplane, float *phi)
+{
+    int64_t nodes = nodes_of(d);
+    float inv_S = ldexpf(1.0f, -d->scale_log2);
+    for (int64_t i = 0; i < nodes; ++i)
+        phi[i] = (float)vplane[i] * inv_S;
+}
+
+void orc_grid_volume_float(const orc_desc *d, const double *vplane, float *phi)
+{
+    int64_t nodes = nodes_of(d);
+    for (int64_t i = 0; i < nodes; ++i)
+        phi[i] = (float)vplane[i];
+}
+
+/* The particle's grid-recovered volume fraction: sum_a w(a) phi(a), taken in
+ * the G2P's order (innermost axis first, three-term sums as in sum3), from
+ * the positions before advection.  Out-of-domain particles are left as they
+ * are.  Returns how many were written.                                      */
+int64_t orc_g2p_volume(const orc_desc *d, const float *phi, int64_t np, const float *const *x, float *out)
+{
+    int dim = d->dim;
+    int64_t written = 0;
+    for (int64_t p = 0; p < np; ++p) {
+        int b[3];
+        float f[3];
+        if (!base_frac(d, x, p, b, f))
+            continue;
+        float w[3][3];
+        for (int l = 0; l < dim; ++l)
+            orc_quadratic_weights(f[l], w[l]);
+        float Y[3];
+        for (int a0 = 0; a0 < 3; ++a0) {
+            if (dim == 3) {
+                float Z[3];
+                for (int a1 = 0; a1 < 3; ++a1) {
+                    float t[3];
+                    for (int a2 = 0; a2 < 3; ++a2)
+                        t[a2] = phi[node_at(d, b[0] + a0, b[1] + a1, b[2] + a2)];
+                    Z[a1] = sum3(w[2], t);
+                }
+                Y[a0] = sum3(w[1], Z);
+            } else {
+                float t[3];
+                for (int a1 = 0; a1 < 3; ++a1)
+                    t[a1] = phi[node_at(d, b[0] + a0, b[1] + a1, 0)];
+                Y[a0] = sum3(w[1], t);
+            }
+        }
+        out[p] = sum3(w[0], Y);
+        written += 1;
+    }
+    return written;
 }
 
 /* The advective time-step bound of the implementation guide (section 3.3.2,

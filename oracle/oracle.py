@@ -83,6 +83,16 @@ def lib():
             L.orc_grid_update_float.restype = None
             L.orc_g2p.argtypes = [ct.POINTER(Desc), _P, ct.c_int64, _PP, _PP, _PP, ct.c_float]
             L.orc_g2p.restype = ct.c_int64
+            L.orc_p2g_fixed_vol.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _PP, _PP, _P, _P, _P, _P]
+            L.orc_p2g_fixed_vol.restype = ct.c_uint32
+            L.orc_p2g_float_vol.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _PP, _PP, _P, _P, _P, _P]
+            L.orc_p2g_float_vol.restype = ct.c_uint32
+            L.orc_grid_volume_fixed.argtypes = [ct.POINTER(Desc), _P, _P]
+            L.orc_grid_volume_fixed.restype = None
+            L.orc_grid_volume_float.argtypes = [ct.POINTER(Desc), _P, _P]
+            L.orc_grid_volume_float.restype = None
+            L.orc_g2p_volume.argtypes = [ct.POINTER(Desc), _P, ct.c_int64, _PP, _P]
+            L.orc_g2p_volume.restype = ct.c_int64
             L.orc_g2p_elastic.argtypes = [ct.POINTER(Desc), _P, ct.c_int64, _PP, _PP, _PP, _PP, ct.c_float]
             L.orc_g2p_elastic.restype = ct.c_int64
             L.orc_log.argtypes = [ct.c_float]
@@ -155,28 +165,59 @@ def bin_particles(grid: dict, x: np.ndarray):
     return key, perm, cnt, int(valid)
 
 
-def p2g_fixed(grid: dict, x, v, C, m):
-    """Fixed-point P2G: returns (acc int64 [(dim+1), nodes], status bits, counts[2])."""
+def p2g_fixed(grid: dict, x, v, C, m, vol=None):
+    """Fixed-point P2G: returns (acc int64 [(dim+1), nodes], status bits, counts[2]);
+    with rest volumes ``vol`` the volume channel is a last plane (dim+2 planes)."""
     x, v, C, m = _f32(x), _f32(v), _f32(C), _f32(m)
     d = desc_from(grid)
     nodes = grid_nodes(grid)
-    acc = np.zeros((grid["dim"] + 1, nodes), dtype=np.int64)
+    acc = np.zeros((grid["dim"] + (1 if vol is None else 2), nodes), dtype=np.int64)
     counts = np.zeros(2, dtype=np.int64)
-    st = lib().orc_p2g_fixed(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m),
-                             _ptr(acc), _ptr(counts))
+    if vol is None:
+        st = lib().orc_p2g_fixed(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m),
+                                 _ptr(acc), _ptr(counts))
+    else:
+        vol = _f32(vol)
+        st = lib().orc_p2g_fixed_vol(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m), _ptr(vol),
+                                     _ptr(acc), _ptr(counts))
     return acc, int(st), counts
 
 
-def p2g_float(grid: dict, x, v, C, m):
-    """Float-atomic P2G with fp64 sums: returns (acc float64 [(dim+1), nodes], status, counts)."""
+def p2g_float(grid: dict, x, v, C, m, vol=None):
+    """Float-atomic P2G with fp64 sums: returns (acc float64 [(dim+1), nodes], status, counts);
+    with ``vol`` the volume channel is a last plane."""
     x, v, C, m = _f32(x), _f32(v), _f32(C), _f32(m)
     d = desc_from(grid)
     nodes = grid_nodes(grid)
-    acc = np.zeros((grid["dim"] + 1, nodes), dtype=np.float64)
+    acc = np.zeros((grid["dim"] + (1 if vol is None else 2), nodes), dtype=np.float64)
     counts = np.zeros(2, dtype=np.int64)
-    st = lib().orc_p2g_float(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m),
-                             _ptr(acc), _ptr(counts))
+    if vol is None:
+        st = lib().orc_p2g_float(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m),
+                                 _ptr(acc), _ptr(counts))
+    else:
+        vol = _f32(vol)
+        st = lib().orc_p2g_float_vol(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m), _ptr(vol),
+                                     _ptr(acc), _ptr(counts))
     return acc, int(st), counts
+
+
+def grid_volume(grid: dict, plane) -> np.ndarray:
+    """Node volume fractions from the volume channel (int64: fixed point, float64: float mode)."""
+    phi = np.zeros(grid_nodes(grid), dtype=np.float32)
+    if np.asarray(plane).dtype == np.int64:
+        lib().orc_grid_volume_fixed(ct.byref(desc_from(grid)), _ptr(np.ascontiguousarray(plane)), _ptr(phi))
+    else:
+        plane = np.ascontiguousarray(plane, dtype=np.float64)
+        lib().orc_grid_volume_float(ct.byref(desc_from(grid)), _ptr(plane), _ptr(phi))
+    return phi
+
+
+def g2p_volume(grid: dict, phi: np.ndarray, x, out=None):
+    """Grid-recovered volume fraction of each in-domain particle (others keep ``out``'s values, 0 by default)."""
+    phi, x = _f32(phi), _f32(x)
+    res = np.zeros(x.shape[1], dtype=np.float32) if out is None else _f32(out).copy()
+    lib().orc_g2p_volume(ct.byref(desc_from(grid)), _ptr(phi), x.shape[1], _rows(x), _ptr(res))
+    return res
 
 
 def dtg_of(grid: dict) -> np.ndarray:

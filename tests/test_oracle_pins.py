@@ -620,3 +620,79 @@ def test_elastic_step_keeps_grid_totals_an_identity():
     for k in range(3):
         Qk = np.rint((Mt * cloud["v"][k]).astype(np.float32)).astype(np.int64)
         assert int(out["acc"][1 + k].sum()) == int(Qk.sum())
+
+
+# --------------------------------------------------------------------------
+# grid-recovered volume (implementation guide, section 3.3.2: each particle
+# scatters its rest volume as a fraction of a cell, so a rest-packed node sums
+# to about one; G2P gathers it back)
+
+def _lattice(n, per_cell_axis, lo_cell, hi_cell, dim=3):
+    """Particles on a regular lattice, per_cell_axis per cell edge, cells lo..hi-1."""
+    h = 1.0 / per_cell_axis
+    ax = (np.arange(lo_cell * per_cell_axis, hi_cell * per_cell_axis) + 0.5) * h / n
+    mesh = np.meshgrid(*([ax] * dim), indexing="ij")
+    return np.stack([m.ravel() for m in mesh]).astype(np.float32)
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_volume_channel_sums_to_one_on_a_rest_packing(dim):
+    n = 16
+    x = _lattice(n, 2, 3, 13, dim)
+    npart = x.shape[1]
+    grid = W.small_cloud(dim, 1, n, seed=1, scale_log2=20)["grid"]
+    dx = grid["dx"]
+    vol = np.full(npart, dx ** dim / 2 ** dim, dtype=np.float32)   # 1/ppc of a cell each
+    z = np.zeros((dim, npart), np.float32)
+    acc, st, counts = O.p2g_fixed(grid, x, z, np.zeros((dim * dim, npart), np.float32),
+                                  np.ones(npart, np.float32), vol=vol)
+    assert st == 0 and acc.shape[0] == dim + 2
+    S = 2.0 ** grid["scale_log2"]
+    assert int(acc[dim + 1].sum()) == npart * int(np.rint(S / 2 ** dim))      # totals: an identity
+    phi = O.grid_volume(grid, acc[dim + 1])
+    X = node_coords(grid)
+    interior = np.all((X >= 5) & (X <= 10), axis=0)
+    assert np.max(np.abs(phi[interior] - 1.0)) <= 27 * 2 ** dim / S
+    assert np.all(phi[~np.all((X >= 2) & (X <= 14), axis=0)] == 0.0)
+    # gathered back: particles well inside read a rest packing
+    pp = O.g2p_volume(grid, phi, x)
+    inside = np.all((x * n >= 5.5) & (x * n <= 10.5), axis=0)
+    assert np.max(np.abs(pp[inside] - 1.0)) <= 1e-5
+    # compressed: the same particles at twice the density read two
+    acc2, _, _ = O.p2g_fixed(grid, x, z, np.zeros((dim * dim, npart), np.float32),
+                             np.ones(npart, np.float32), vol=vol * 2)
+    pp2 = O.g2p_volume(grid, O.grid_volume(grid, acc2[dim + 1]), x)
+    assert np.max(np.abs(pp2[inside] - 2.0)) <= 2e-5
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_volume_channel_matches_brute_force(dim):
+    n = 8
+    cloud = W.with_elastic(W.small_cloud(dim, 40, n, seed=950 + dim, lo=0.2, hi=0.8, scale_log2=20), seed=951)
+    grid = cloud["grid"]
+    vol = (cloud["vol"] * (0.5 + W.Stream(952, 1).uniform24(40))).astype(np.float32)
+    acc, st, _ = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"], vol=vol)
+    accf, _, _ = O.p2g_float(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"], vol=vol)
+    base, _, _ = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert st == 0 and np.array_equal(acc[: dim + 1], base)      # the other channels are unchanged
+    q = vol.astype(np.float64) / grid["dx"] ** dim
+    ones = np.ones((dim, 40))
+    mass, _, absterm = brute_force_p2g(grid, cloud["x"], 0 * ones, np.zeros((dim * dim, 40)), q)
+    S = 2.0 ** grid["scale_log2"]
+    assert np.all(np.abs(acc[dim + 1] / S - mass) <= 27.0 * 40 / S + 1e-6 * absterm)
+    assert np.all(np.abs(accf[dim + 1] - mass) <= 2e-6 * absterm + 1e-12)
+
+
+@pytest.mark.parametrize("dim", [2, 3])
+def test_volume_gather_reproduces_affine_fields(dim):
+    """The quadratic B-spline reproduces affine functions: gathering phi = a.x + b
+    returns a.x_p + b (a transposed node index or a wrong weight fails)."""
+    n = 16
+    cloud = W.small_cloud(dim, 500, n, seed=960 + dim, lo=0.15, hi=0.85)
+    grid = cloud["grid"]
+    a = np.array([0.7, -1.3, 2.1][:dim])
+    X = node_coords(grid) * grid["dx"]
+    phi = (a @ X + 0.25).astype(np.float32)
+    pp = O.g2p_volume(grid, phi, cloud["x"])
+    expect = a @ cloud["x"].astype(np.float64) + 0.25
+    assert np.max(np.abs(pp - expect)) <= 2e-6
