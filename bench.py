@@ -240,9 +240,10 @@ def run_ours(args, rank, world, local):
                 "frac": round((n * 136.0 + touched * 64.0) / (tr_ms * 1e-3) / 1e9 / peak, 4),
                 "bin_ms": round(float(mean_ms[0]), 4)}
 
-    elastic = None
-    if args.elastic_steps > 0:
-        elastic = measure_elastic(args, cloud, dev, stream, world, peak)
+    elastic = volume = None
+    if args.variant_steps > 0:
+        elastic = measure_variant(args, cloud, dev, stream, world, peak, elastic=True, volume=False)
+        volume = measure_variant(args, cloud, dev, stream, world, peak, elastic=False, volume=True)
 
     # end to end through the host entry point (pinned host SoA, copies inside the timed region)
     e2e = None
@@ -290,6 +291,7 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "advective_step_bound": advective,
         "mls_stress": elastic,
+        "volume_channel": volume,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
@@ -299,30 +301,38 @@ def run_ours(args, rank, world, local):
 ELASTIC = {"fsig": 0.05, "ppc": 1.0, "mu": 1.0e9, "lambda": 1.0e9}
 
 
-def measure_elastic(args, cloud, dev, stream, world, peak):
-    """The same workload with an elastic state (F = I + N(0, 0.05), V0 = dx^3,
-    Neo-Hookean mu = lambda = 1e9): the stress folded into P2G's affine matrix
-    and F advanced in G2P.  Timed like the main region, steady state."""
+def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume: bool):
+    """The same workload with the elastic state (F = I + N(0, 0.05), V0 = dx^3,
+    Neo-Hookean mu = lambda = 1e9: the stress folded into P2G's affine matrix,
+    F advanced in G2P) and/or the grid-recovered volume channel (rest volume
+    V0 = dx^3 scattered and gathered back).  Timed like the main region, in the
+    steady state, per phase."""
     import torch
     from material_point_particle_gb300 import _lib as L
     from material_point_particle_gb300 import workloads as W
     from material_point_particle_gb300.system import MPMSystem
 
+    steps = args.variant_steps
+    grid = dict(cloud["grid"], volume_channel=1 if volume else 0)
     ecloud = W.with_elastic(cloud, seed=77, fsig=ELASTIC["fsig"], ppc=ELASTIC["ppc"], mu=ELASTIC["mu"],
                             lam=ELASTIC["lambda"])
     n = cloud["x"].shape[1]
-    es = (MPMSystem(cloud["grid"], n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"])
-          .load_elastic(ecloud["F"], ecloud["vol"], ecloud["material"]).enable_sorted())
+    es = MPMSystem(grid, n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    if elastic:
+        es.load_elastic(ecloud["F"], ecloud["vol"], ecloud["material"])
+    else:
+        es.load_volume(ecloud["vol"])
+    es.enable_sorted()
     del ecloud
     for _ in range(max(3, args.warmup)):
         es.step_sorted(stream)
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.elastic_steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     barrier(world, dev)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for k in range(args.elastic_steps):
+    for k in range(steps):
         e = ev[k]
         e[0].record(stream)
         es.bin(stream)
@@ -336,27 +346,35 @@ def measure_elastic(args, cloud, dev, stream, world, peak):
     t1.record(stream)
     torch.cuda.synchronize()
     st = es.status()
-    assert st[L.ST_FLAGS] == 0, f"elastic status flags {st[:8]}"
-    ms = aggregate_max(t0.elapsed_time(t1) / args.elastic_steps, world, dev)
+    assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
+    ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
     parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev]).mean(axis=0)
     names = ["bin", "p2g", "grid_update", "g2p"]
-    # algorithmic bytes: P2G reads the record (64 B) plus F and V0 (40 B); G2P reads x and F,
-    # writes x v C F (72 + 72 B); touched grid nodes as in the main region
     es.bin(stream)
     es.p2g(stream)
     touched = int((es.acc[0] != 0).sum().item())
     es.grid_update(stream)
     torch.cuda.synchronize()
-    alg = {"p2g": n * 104.0 + touched * 32.0, "g2p": n * 144.0}
+    # algorithmic bytes: P2G reads the record (64 B) plus F (36 B) and V0 (4 B) as used, and writes
+    # 8 B per channel per touched node; G2P reads x (and F) and writes x v C (and F, and phi)
+    ch = 4 + (1 if volume else 0)
+    alg = {"p2g": n * (64.0 + (36.0 if elastic else 0.0) + 4.0) + touched * 8.0 * ch,
+           "g2p": n * (72.0 + (72.0 if elastic else 0.0) + (4.0 if volume else 0.0))}
     dom = "p2g" if parts[1] >= parts[3] else "g2p"
     achieved = alg[dom] / (parts[names.index(dom)] * 1e-3) / 1e9
-    out = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT,
-           "steps": args.elastic_steps, "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, parts)},
-           "material": {"mu": ELASTIC["mu"], "lambda": ELASTIC["lambda"], "F": "I + N(0, 0.05) per entry",
-                        "V0": "dx^3"},
-           "degenerate": int(st[L.ST_N_DEGENERATE]), "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
+    out = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+           "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, parts)},
+           "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None}}
+    if elastic:
+        out["material"] = {"mu": ELASTIC["mu"], "lambda": ELASTIC["lambda"], "F": "I + N(0, 0.05) per entry",
+                           "V0": "dx^3"}
+        out["degenerate"] = int(st[L.ST_N_DEGENERATE])
+    if volume:
+        phi = es.phi.float()
+        out["volume_fraction"] = {"V0": "dx^3 (one cell)", "mean": round(float(phi.mean().item()), 4),
+                                  "max": round(float(phi.max().item()), 4)}
     del es
     torch.cuda.empty_cache()
     return out
@@ -415,8 +433,9 @@ def main():
                     "of a smaller sample, for profiling)")
     ap.add_argument("--cpu-sample", type=int, default=2097152)
     ap.add_argument("--ref-sample", type=int, default=262144)
-    ap.add_argument("--elastic-steps", type=int, default=50,
-                    help="timed steps of the same workload with the Neo-Hookean stress (0: skip)")
+    ap.add_argument("--variant-steps", type=int, default=50,
+                    help="timed steps of the same workload with the Neo-Hookean stress, and with the "
+                         "volume channel (0: skip both)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -27,7 +27,9 @@
  *    affine matrix is C[k*dim + l] = d v_k / d x_l.
  *  - Grid arrays are planar: channel c of node (i, j, k) is at
  *    c*nodes + (k*n[1] + j)*n[0] + i.  Accumulator channels: mass, then
- *    momentum along each axis.  Velocity channels: one per axis.
+ *    momentum along each axis, then (volume_channel) the rest volume.
+ *    Velocity channels: one per axis, then (volume_channel) the node's
+ *    volume fraction.
  *  - Node i sits at position i*dx; the domain holds particles whose whole
  *    quadratic stencil lies on the grid, 0.5 <= x*inv_dx < n - 1.5 per axis.
  */
@@ -70,6 +72,7 @@ typedef struct mpm_grid_desc {
     int32_t scale_log2;     /* fixed-point scale S = 2^scale_log2, 0..40 */
     int32_t tile;           /* cells per tile edge: 4 (3D) or 8 (2D) */
     int32_t boundary_nodes; /* velocity boundary band width in nodes (e.g. 3) */
+    int32_t volume_channel; /* 1: the grid-recovered volume channel (see mpm_p2g), else 0 */
 } mpm_grid_desc;
 
 /* Particle state (device SoA).  fp32 everywhere, except MPM_ACC_EXACT_INT:
@@ -85,7 +88,11 @@ typedef struct mpm_grid_desc {
  * adds the MLS-MPM stress to the affine matrix it scatters and mpm_g2p
  * advances F (implementation guide, section 3.1, Part 2; section 3.3.2,
  * F <- (I + D) F); the calls that move particles carry F and vol along.
- * Not used by MPM_ACC_EXACT_INT. */
+ * Not used by MPM_ACC_EXACT_INT.
+ *
+ * Grid-recovered volume (descriptors with volume_channel = 1): vol as above
+ * (the rest volume V0, needed then even without F) and phi = fp32 output of
+ * G2P, the particle's grid-recovered volume fraction (see mpm_g2p). */
 typedef struct mpm_particles {
     int64_t n;
     void *x[3];
@@ -97,6 +104,7 @@ typedef struct mpm_particles {
     void *vol;
     float mu;
     float lambda;
+    void *phi;
 } mpm_particles;
 
 /* Status words (device, uint32), in mpm_bins.status. */
@@ -197,6 +205,13 @@ mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
  * enters the range test.  A particle whose det F is not a positive normal
  * fp32 number keeps C and is counted in MPM_ST_N_DEGENERATE.  `dt` is only
  * read for elastic particles.
+ * With volume_channel = 1 a last accumulator channel receives each
+ * particle's rest volume in cells, q = V0 * inv_dx^dim (inv_dx^3 taken as
+ * (inv_dx*inv_dx)*inv_dx), as the mass is scattered: Vt = q*S, shares
+ * rint(((wx*Vt)*wy)*wz), remainder at the centre, and the range test also
+ * requires wmax*|Vt| <= 2^22 - 4096 (implementation guide, section 3.3.2,
+ * "grid-recovered volume": 1/ppc per particle, so a rest-packed node sums to
+ * about one).  MPM_ACC_F32 adds the fp32 terms ((wx*q)*wy)*wz.
  * MPM_ACC_EXACT_INT (2D or 3D, order 1): integer positions X (1/65,536 cell),
  * int64 m and v; the far node's share of q is q*F/65,536 rounded to nearest
  * (ties to even), the near node gets the rest, split along x then y (then z);
@@ -215,7 +230,9 @@ mpm_status mpm_p2g(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
  * component pointing into the wall becomes zero (implementation guide 2.1 and
  * 3.3.2).  dtg = dt*g rounded to fp32 per component, computed by the caller.
  * Reads each accumulator once and writes it back to zero (consume-and-zero,
- * implementation guide section 2.1 and rule 4).  `grid_vel`: dim fp32 planes.
+ * implementation guide section 2.1 and rule 4).  `grid_vel`: dim fp32 planes;
+ * with volume_channel one more, the node volume fraction phi = (float)V * 2^-scale_log2
+ * (fixed point) or the fp32 sum (MPM_ACC_F32).
  */
 mpm_status mpm_grid_update(const mpm_grid_desc *desc, void *grid_acc, float *grid_vel, const float dtg[3],
                            mpm_bins *bins, void *stream);
@@ -226,6 +243,11 @@ mpm_status mpm_grid_update(const mpm_grid_desc *desc, void *grid_acc, float *gri
  * (APIC, "gather d and D (= B*4)" in cell units); x' = fma(dt, v', x).
  * The stencil sums run axis by axis, innermost axis first, each three-term
  * sum as fma(w2,t2, fma(w1,t1, w0*t0)), the same order the oracle uses.
+ * With volume_channel, phi_p = sum_a w phi(a) (the same nested order) is
+ * written to parts->phi: the grid-recovered volume fraction, about one in a
+ * rest packing and above one where the material is compressed (the guide
+ * reciprocates it and blends it into a tracked density where it reads
+ * compressed; that policy is left to the caller).
  * Elastic particles also get F' = (I + dt C') F, each entry as
  * fma(D_k2, F_2l, fma(D_k1, F_1l, fma(D_k0, F_0l, F_kl))) with D = dt*C'.
  * Particles outside the domain are left unchanged.
@@ -250,7 +272,7 @@ mpm_status mpm_g2p(const mpm_grid_desc *desc, const void *grid, mpm_particles *p
  * cells that use different shared-memory banks, which the next step's P2G
  * and G2P exploit.  A slice of at most 32 particles (one round) keeps bin
  * order.  The remaining particles (outside the domain) are copied
- * unchanged to out[j] = in[perm[j]].  m, id and vol are carried along.  This is
+ * unchanged to out[j] = in[perm[j]].  m, id, vol and phi are carried along.  This is
  * the ping-pong buffer of "Particle Worlds, part 3", Step 4 ("the sort writes
  * into a second buffer"): the next step's binning then starts from almost
  * sorted particles, so its runs are long and every particle pass reads and
@@ -277,7 +299,7 @@ mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_par
 
 /*
  * mpm_step_host -- one step from and back to HOST particle arrays: copies the
- * host SoA (`host`: x, v, C, m, and id, F and vol if given; pinned memory
+ * host SoA (`host`: x, v, C, m, and id, F, vol and phi if given; pinned memory
  * gives full copy bandwidth) into the device arrays `dev_in`, runs
  * mpm_step_sorted into `dev_out`, and copies the same arrays of `dev_out`
  * back into `host`, so

@@ -34,13 +34,13 @@ class MPMError(RuntimeError):
 class GridDesc(ct.Structure):
     _fields_ = [("dim", ct.c_int32), ("n", ct.c_int32 * 3), ("dx", ct.c_float), ("inv_dx", ct.c_float),
                 ("order", ct.c_int32), ("acc_mode", ct.c_int32), ("scale_log2", ct.c_int32),
-                ("tile", ct.c_int32), ("boundary_nodes", ct.c_int32)]
+                ("tile", ct.c_int32), ("boundary_nodes", ct.c_int32), ("volume_channel", ct.c_int32)]
 
 
 class Particles(ct.Structure):
     _fields_ = [("n", ct.c_int64), ("x", ct.c_void_p * 3), ("v", ct.c_void_p * 3), ("C", ct.c_void_p * 9),
                 ("m", ct.c_void_p), ("id", ct.c_void_p), ("F", ct.c_void_p * 9), ("vol", ct.c_void_p),
-                ("mu", ct.c_float), ("lambda_", ct.c_float)]
+                ("mu", ct.c_float), ("lambda_", ct.c_float), ("phi", ct.c_void_p)]
 
 
 class Bins(ct.Structure):
@@ -120,23 +120,30 @@ def grid_desc(grid: dict) -> GridDesc:
     d.scale_log2 = grid["scale_log2"]
     d.tile = grid["tile"]
     d.boundary_nodes = grid["boundary_nodes"]
+    d.volume_channel = int(grid.get("volume_channel", 0))
     return d
 
 
 def particles(x: torch.Tensor, v: torch.Tensor, C: torch.Tensor | None, m: torch.Tensor,
               id: torch.Tensor | None = None, F: torch.Tensor | None = None, vol: torch.Tensor | None = None,
-              mu: float = 0.0, lam: float = 0.0) -> Particles:
+              mu: float = 0.0, lam: float = 0.0, phi: torch.Tensor | None = None) -> Particles:
     """SoA view of [dim, n] / [dim*dim, n] / [n] tensors (rows must be contiguous),
-    with optional uint32-sized [n] particle ids and an optional elastic state
-    (F [dim*dim, n], vol [n], Lame constants mu and lam)."""
+    with optional uint32-sized [n] particle ids, an optional elastic state
+    (F [dim*dim, n], Lame constants mu and lam), rest volumes vol [n] and the
+    volume-channel output phi [n]."""
     p = Particles()
     if F is not None:
-        assert F.is_contiguous() and vol is not None and vol.is_contiguous()
+        assert F.is_contiguous()
         for i in range(F.shape[0]):
             p.F[i] = F[i].data_ptr()
-        p.vol = vol.data_ptr()
         p.mu = mu
         p.lambda_ = lam
+    if vol is not None:
+        assert vol.is_contiguous()
+        p.vol = vol.data_ptr()
+    if phi is not None:
+        assert phi.is_contiguous()
+        p.phi = phi.data_ptr()
     if id is not None:
         assert id.is_contiguous() and id.element_size() == 4
         p.id = id.data_ptr()

@@ -27,6 +27,8 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
     if (!d) return MPM_E_ARG;
     if (d->dim != 2 && d->dim != 3) return MPM_E_ARG;
     if (d->acc_mode < MPM_ACC_I32 || d->acc_mode > MPM_ACC_EXACT_INT) return MPM_E_ARG;
+    if (d->volume_channel != 0 && d->volume_channel != 1) return MPM_E_ARG;
+    if (d->volume_channel && d->acc_mode == MPM_ACC_EXACT_INT) return MPM_E_ARG;
     std::memset(&g, 0, sizeof(g));
     g.dim = d->dim;
     g.acc_mode = d->acc_mode;
@@ -68,6 +70,10 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
     g.halo_nodes = d->dim == 3 ? g.H * g.H * g.H : g.H * g.H;
     g.boundary = d->boundary_nodes;
     g.wmax = d->dim == 3 ? 0.421875f : 0.5625f;
+    g.vc = d->volume_channel;
+    g.vcell = d->inv_dx * d->inv_dx;
+    if (d->dim == 3) g.vcell = g.vcell * d->inv_dx;
+    g.inv_S = d->acc_mode == MPM_ACC_F32 ? 1.0f : std::ldexp(1.0f, -d->scale_log2);
     return MPM_OK;
 }
 
@@ -173,6 +179,11 @@ mpm_status parts_f(const GridP &g, const mpm_particles *p, bool need_state, Part
         out.mu = p->mu;
         out.lam = p->lambda;
     }
+    if (g.vc) {  // volume channel: rest volumes in, volume fractions out
+        out.vol = static_cast<float *>(p->vol);
+        out.phi = static_cast<float *>(p->phi);
+        if ((!out.vol || !out.phi) && p->n) return MPM_E_ARG;
+    }
     return MPM_OK;
 }
 
@@ -273,13 +284,13 @@ size_t mpm_grid_acc_bytes(const mpm_grid_desc *desc) {
     GridP g;
     if (make_grid(desc, g) != MPM_OK) return 0;
     const size_t w = (g.acc_mode == MPM_ACC_I64 || g.acc_mode == MPM_ACC_EXACT_INT) ? 8 : 4;
-    return (size_t)(g.dim + 1) * (size_t)g.nodes * w;
+    return (size_t)(g.dim + 1 + g.vc) * (size_t)g.nodes * w;
 }
 
 size_t mpm_grid_vel_bytes(const mpm_grid_desc *desc) {
     GridP g;
     if (make_grid(desc, g) != MPM_OK) return 0;
-    return (size_t)g.dim * (size_t)g.nodes * sizeof(float);
+    return (size_t)(g.dim + g.vc) * (size_t)g.nodes * sizeof(float);
 }
 
 mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, int flags, void *stream) {
@@ -393,6 +404,8 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
     if (ph.n != pa.n || ph.n != pb.n) return MPM_E_ARG;
     if ((!ph.id) != (!pa.id) || (!ph.id) != (!pb.id)) return MPM_E_ARG;
     if ((!ph.F[0]) != (!pa.F[0]) || (!ph.F[0]) != (!pb.F[0])) return MPM_E_ARG;
+    if ((!ph.vol) != (!pa.vol) || (!ph.vol) != (!pb.vol) || (!ph.phi) != (!pa.phi) || (!ph.phi) != (!pb.phi))
+        return MPM_E_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)ph.n * sizeof(float);
     auto copy = [&](void *dst, const void *src, cudaMemcpyKind kind) {
@@ -405,10 +418,10 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
         for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(pa.C[j], ph.C[j], cudaMemcpyHostToDevice);
         ok = ok && copy(const_cast<float *>(pa.m), ph.m, cudaMemcpyHostToDevice);
         if (ph.id) ok = ok && copy(pa.id, ph.id, cudaMemcpyHostToDevice);
-        if (ph.F[0]) {
+        if (ph.F[0])
             for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(pa.F[j], ph.F[j], cudaMemcpyHostToDevice);
-            ok = ok && copy(pa.vol, ph.vol, cudaMemcpyHostToDevice);
-        }
+        if (ph.vol) ok = ok && copy(pa.vol, ph.vol, cudaMemcpyHostToDevice);
+        if (ph.phi) ok = ok && copy(pa.phi, ph.phi, cudaMemcpyHostToDevice);
         if (!ok) return MPM_E_CUDA;
     }
     MPM_TRY(mpm_step_sorted(desc, dev_in, dev_out, bins, grid_acc, grid_vel, dt, dtg, stream));
@@ -419,10 +432,10 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
         for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(ph.C[j], pb.C[j], cudaMemcpyDeviceToHost);
         ok = ok && copy(const_cast<float *>(ph.m), pb.m, cudaMemcpyDeviceToHost);
         if (ph.id) ok = ok && copy(ph.id, pb.id, cudaMemcpyDeviceToHost);
-        if (ph.F[0]) {
+        if (ph.F[0])
             for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(ph.F[j], pb.F[j], cudaMemcpyDeviceToHost);
-            ok = ok && copy(ph.vol, pb.vol, cudaMemcpyDeviceToHost);
-        }
+        if (ph.vol) ok = ok && copy(ph.vol, pb.vol, cudaMemcpyDeviceToHost);
+        if (ph.phi) ok = ok && copy(ph.phi, pb.phi, cudaMemcpyDeviceToHost);
         if (!ok) return MPM_E_CUDA;
     }
     return MPM_OK;

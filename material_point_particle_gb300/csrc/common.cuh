@@ -46,6 +46,9 @@ struct GridP {
     int64_t nblocks;
     int boundary;        // boundary_nodes
     float wmax;          // 0.75^dim
+    int vc;              // 1: grid-recovered volume channel
+    float vcell;         // inv_dx^dim, (inv_dx * inv_dx) [* inv_dx]
+    float inv_S;         // 2^-scale_log2 (1 in float mode)
 };
 
 // Particle SoA as raw typed pointers.
@@ -56,8 +59,9 @@ struct PartsF {
     const float *m;
     uint32_t *id;
     float *F[9];  // elastic state (F[0] null for none): deformation gradient
-    float *vol;   // and rest volume
+    float *vol;   // rest volume (elastic state, volume channel)
     float mu, lam;
+    float *phi;   // volume channel: grid-recovered volume fraction (G2P output)
     int64_t n;
 };
 
@@ -204,18 +208,20 @@ struct Prefetch {
     __device__ float *at(int stage, int f) const { return buf + (stage * NF + f) * NT + threadIdx.x; }
 };
 
-// The particle record of P2G: x[dim], v[dim], C[dim*dim], m, and with the
-// elastic state F[dim*dim], vol.
-template <int DIM, bool EL = false>
+// The particle record of P2G: x[dim], v[dim], C[dim*dim], m, then with the
+// elastic state F[dim*dim], and vol when the elastic state or the volume
+// channel needs it.
+template <int DIM, bool EL = false, bool VC = false>
 struct P2GFields {
     static constexpr int BASE = DIM + DIM + DIM * DIM + 1;  // index of F[0]
-    static constexpr int NF = BASE + (EL ? DIM * DIM + 1 : 0);
+    static constexpr int VOLF = BASE + (EL ? DIM * DIM : 0);  // index of vol
+    static constexpr int NF = VOLF + (EL || VC ? 1 : 0);
     __device__ static const float *src(const PartsF &p, int f) {
         return f < DIM                    ? p.x[f]
                : f < 2 * DIM              ? p.v[f - DIM]
                : f < 2 * DIM + DIM * DIM  ? p.C[f - 2 * DIM]
                : f < BASE                 ? p.m
-               : f < BASE + DIM * DIM     ? p.F[f - BASE]
+               : f < VOLF                 ? p.F[f - BASE]
                                           : p.vol;
     }
 };

@@ -28,9 +28,10 @@ __device__ __forceinline__ float acc_to_float(AccT v) {
         return __int2float_rn((int)v);
 }
 
-template <int DIM, int T, typename AccT>
+template <int DIM, int T, typename AccT, bool VC>
 __global__ void k_grid_update(GridP g, AccT *__restrict__ acc, float *__restrict__ vel, float dtg0, float dtg1,
                               float dtg2, const uint32_t *__restrict__ count) {
+    constexpr int NCH = DIM + 1 + (VC ? 1 : 0);
     constexpr int NB = DIM == 3 ? T * T * T : T * T;
     const uint32_t lane = lane_id();
     const float dtg[3] = {dtg0, dtg1, dtg2};
@@ -51,10 +52,10 @@ __global__ void k_grid_update(GridP g, AccT *__restrict__ acc, float *__restrict
             const int gx = bx * T + r % T, gy = by * T + (r / T) % T, gz = DIM == 3 ? bz * T + r / (T * T) : 0;
             if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
             const int64_t node = node_index(g, gx, gy, gz);
-            AccT a[DIM + 1];
+            AccT a[NCH];
             bool any = false;
 #pragma unroll
-            for (int c = 0; c <= DIM; ++c) {
+            for (int c = 0; c < NCH; ++c) {
                 a[c] = acc[c * g.nodes + node];
                 any = any || a[c] != (AccT)0;
             }
@@ -69,37 +70,44 @@ __global__ void k_grid_update(GridP g, AccT *__restrict__ acc, float *__restrict
                 }
                 vel[l * g.nodes + node] = v;
             }
+            // volume fraction: the sum in cells, the fixed-point scale removed
+            if constexpr (VC) vel[DIM * g.nodes + node] = __fmul_rn(acc_to_float(a[DIM + 1]), g.inv_S);
             if (any) {
 #pragma unroll
-                for (int c = 0; c <= DIM; ++c) acc[c * g.nodes + node] = (AccT)0;
+                for (int c = 0; c < NCH; ++c) acc[c * g.nodes + node] = (AccT)0;
             }
         }
     }
 }
 
+template <int DIM, int T, typename AccT>
+void launch_grid_update_t(const GridP &g, void *grid_acc, float *vel, const float dtg[3], const WsView &w, int blocks,
+                          cudaStream_t st) {
+    if (g.vc)
+        k_grid_update<DIM, T, AccT, true><<<blocks, 256, 0, st>>>(g, (AccT *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
+                                                                  w.count);
+    else
+        k_grid_update<DIM, T, AccT, false><<<blocks, 256, 0, st>>>(g, (AccT *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
+                                                                   w.count);
+}
+
 mpm_status launch_grid_update(const GridP &g, void *grid_acc, float *vel, const float dtg[3], const WsView &w,
                               const DeviceInfo &dev, cudaStream_t st) {
-    const int blocks = dev.sms * 8, threads = 256;
+    const int blocks = dev.sms * 8;
     if (g.dim == 3 && g.T == 4) {
         if (g.acc_mode == MPM_ACC_I64)
-            k_grid_update<3, 4, long long><<<blocks, threads, 0, st>>>(g, (long long *)grid_acc, vel, dtg[0], dtg[1],
-                                                                      dtg[2], w.count);
+            launch_grid_update_t<3, 4, long long>(g, grid_acc, vel, dtg, w, blocks, st);
         else if (g.acc_mode == MPM_ACC_I32)
-            k_grid_update<3, 4, int><<<blocks, threads, 0, st>>>(g, (int *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
-                                                                w.count);
+            launch_grid_update_t<3, 4, int>(g, grid_acc, vel, dtg, w, blocks, st);
         else
-            k_grid_update<3, 4, float><<<blocks, threads, 0, st>>>(g, (float *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
-                                                                  w.count);
+            launch_grid_update_t<3, 4, float>(g, grid_acc, vel, dtg, w, blocks, st);
     } else if (g.dim == 2 && g.T == 8) {
         if (g.acc_mode == MPM_ACC_I64)
-            k_grid_update<2, 8, long long><<<blocks, threads, 0, st>>>(g, (long long *)grid_acc, vel, dtg[0], dtg[1],
-                                                                      dtg[2], w.count);
+            launch_grid_update_t<2, 8, long long>(g, grid_acc, vel, dtg, w, blocks, st);
         else if (g.acc_mode == MPM_ACC_I32)
-            k_grid_update<2, 8, int><<<blocks, threads, 0, st>>>(g, (int *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
-                                                                w.count);
+            launch_grid_update_t<2, 8, int>(g, grid_acc, vel, dtg, w, blocks, st);
         else
-            k_grid_update<2, 8, float><<<blocks, threads, 0, st>>>(g, (float *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
-                                                                  w.count);
+            launch_grid_update_t<2, 8, float>(g, grid_acc, vel, dtg, w, blocks, st);
     } else {
         return MPM_E_ARG;
     }
@@ -126,8 +134,9 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
     if (q.F[0] && p.F[0]) {
 #pragma unroll
         for (int j = 0; j < DIM * DIM; ++j) q.F[j][dst] = p.F[j][src];
-        q.vol[dst] = p.vol[src];
     }
+    if (q.vol && p.vol) q.vol[dst] = p.vol[src];
+    if (q.phi && p.phi) q.phi[dst] = p.phi[src];
 }
 
 // Velocity halo of one tile in shared memory, in the compact layout of the
@@ -135,6 +144,7 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
 template <int DIM, int T>
 struct VelHalo {
     float *x, *y, *z;
+    float *phi;  // node volume fractions (volume channel)
 };
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
@@ -150,8 +160,10 @@ __device__ __forceinline__ float2 sum3x2(const float2 w[3], const float2 t[3]) {
 // rec(f): the particle's staged fields x[dim], then (sorted output) m and the
 // id bits.  The x and y components go through packed fp32x2 arithmetic, which
 // rounds each lane exactly as the scalar operation.  Elastic particles (EL)
-// read F (and, sorted, vol) of `pid` from global memory and write F'.
-template <int DIM, int T, bool SORTED, bool EL, typename Rec>
+// read F (and, sorted, vol) of `pid` from global memory and write F'; with
+// the volume channel (VC) the particle's grid-recovered volume fraction is
+// gathered as v is and written to phi.
+template <int DIM, int T, bool SORTED, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
                                            uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
                                            float dt, float c4, float &smax) {
@@ -278,7 +290,32 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
         advance_F<DIM>(dt, Cn, Fo, Fn);
 #pragma unroll
         for (int j = 0; j < DIM * DIM; ++j) q.F[j][dst] = Fn[j];
-        if constexpr (SORTED) q.vol[dst] = p.vol[pid];
+    }
+    if constexpr (SORTED && (EL || VC)) q.vol[dst] = p.vol[pid];
+    if constexpr (VC) {
+        // sum_a w(a) phi(a), innermost axis first (the order of v)
+        const float *vp = sv.phi + hb;
+        float Yp[3];
+#pragma unroll
+        for (int a0 = 0; a0 < 3; ++a0) {
+            if constexpr (DIM == 3) {
+                float Zp[3];
+#pragma unroll
+                for (int a1 = 0; a1 < 3; ++a1) {
+                    float t[3];
+#pragma unroll
+                    for (int a2 = 0; a2 < 3; ++a2) t[a2] = vp[a0 + a1 * Hl::SY + a2 * Hl::SZ];
+                    Zp[a1] = sum3(w[2], t);
+                }
+                Yp[a0] = sum3(w[1], Zp);
+            } else {
+                float t[3];
+#pragma unroll
+                for (int a1 = 0; a1 < 3; ++a1) t[a1] = vp[a0 + a1 * Hl::SY];
+                Yp[a0] = sum3(w[1], t);
+            }
+        }
+        q.phi[dst] = sum3(w[0], Yp);
     }
     smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
 #pragma unroll
@@ -321,7 +358,7 @@ __device__ __forceinline__ uint32_t interleave_entry(uint32_t pos, uint32_t cnt)
 // interleaved slice, so that its writes are coalesced and its reads of the
 // velocity halo meet few bank conflicts.  A slice of at most 32 particles is
 // one round and keeps bin order.
-template <int DIM, int T, bool SORTED, bool EL>
+template <int DIM, int T, bool SORTED, bool EL, bool VC>
 __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                      const uint32_t *__restrict__ perm,
                                                      const uint32_t *__restrict__ key,
@@ -335,8 +372,8 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
     // in place: per-thread double buffer of x; sorted: x, m, id of the whole slice
     constexpr int NF = SORTED ? DIM + 2 : DIM;
     constexpr int BUF = SORTED ? NF * kSliceParticles : 2 * NF * kP2GThreads;
-    __shared__ float sv_x[Hl::SIZE], sv_y[Hl::SIZE], sv_z[DIM == 3 ? Hl::SIZE : 1];
-    const VelHalo<DIM, T> sv{sv_x, sv_y, sv_z};
+    __shared__ float sv_x[Hl::SIZE], sv_y[Hl::SIZE], sv_z[DIM == 3 ? Hl::SIZE : 1], sv_phi[VC ? Hl::SIZE : 1];
+    const VelHalo<DIM, T> sv{sv_x, sv_y, sv_z, sv_phi};
     __shared__ float sbuf[BUF];
     // [(qi, warp)][class], rows padded to 33 words: the scan reads a column
     __shared__ uint32_t hist[SORTED ? NQ * NWARP * 33 : 1];
@@ -385,6 +422,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             sv_x[h] = in ? vel[node] : 0.f;
             sv_y[h] = in ? vel[g.nodes + node] : 0.f;
             if (DIM == 3) sv_z[h] = in ? vel[2 * g.nodes + node] : 0.f;
+            if (VC) sv_phi[h] = in ? vel[DIM * g.nodes + node] : 0.f;
         }
         if (SORTED && cnt <= 32u) {
             // one round: the order inside it does not matter, bin order is kept
@@ -393,7 +431,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             if (threadIdx.x < cnt) {
                 const uint32_t r = threadIdx.x;
                 auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                gather_one<DIM, T, true, EL>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
+                gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
             }
         } else if constexpr (SORTED) {
             // stable counting sort of the slice by bank class: counts per
@@ -453,7 +491,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                     const uint32_t e = interleave_entry(pos, cnt);
                     const uint32_t r = order[e + (e >> 5)];
                     auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                    gather_one<DIM, T, true, EL>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax);
+                    gather_one<DIM, T, true, EL, VC>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax);
                 }
             }
         } else {
@@ -474,7 +512,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                 if (r < cnt) {
                     const int stage = qi & 1;
                     auto rec = [&](int f) { return *pf.at(stage, f); };
-                    gather_one<DIM, T, false, EL>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4, smax);
+                    gather_one<DIM, T, false, EL, VC>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4, smax);
                 }
             }
         }
@@ -492,35 +530,41 @@ __global__ void k_copy_rest(PartsF p, PartsF q, const uint32_t *__restrict__ per
         copy_particle<DIM>(p, q, perm[j], (uint32_t)j);
 }
 
-template <int DIM, int T, bool SORTED, bool EL>
+template <int DIM, int T, bool SORTED, bool EL, bool VC>
 void launch_g2p_t(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w, float dt,
                   const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
     const int blocks = dev.sms * 4;
-    k_g2p<DIM, T, SORTED, EL><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start,
-                                                               w.status, dt, c4);
+    k_g2p<DIM, T, SORTED, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start,
+                                                                   w.status, dt, c4);
     if constexpr (SORTED) k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+}
+
+template <int DIM, int T, bool SORTED>
+void launch_g2p_dt(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w, float dt,
+                   const DeviceInfo &dev, cudaStream_t st) {
+    const bool el = in.F[0] != nullptr;
+    if (el && g.vc)
+        launch_g2p_t<DIM, T, SORTED, true, true>(g, vel, in, out, w, dt, dev, st);
+    else if (el)
+        launch_g2p_t<DIM, T, SORTED, true, false>(g, vel, in, out, w, dt, dev, st);
+    else if (g.vc)
+        launch_g2p_t<DIM, T, SORTED, false, true>(g, vel, in, out, w, dt, dev, st);
+    else
+        launch_g2p_t<DIM, T, SORTED, false, false>(g, vel, in, out, w, dt, dev, st);
 }
 
 template <bool SORTED>
 mpm_status launch_g2p_any(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
                           float dt, const DeviceInfo &dev, cudaStream_t st) {
-    const bool el = in.F[0] != nullptr;
     static_assert(MPM_ST_MAX_SPEED == MPM_ST_WORK_G2P + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
-    if (g.dim == 3 && g.T == 4) {
-        if (el)
-            launch_g2p_t<3, 4, SORTED, true>(g, vel, in, out, w, dt, dev, st);
-        else
-            launch_g2p_t<3, 4, SORTED, false>(g, vel, in, out, w, dt, dev, st);
-    } else if (g.dim == 2 && g.T == 8) {
-        if (el)
-            launch_g2p_t<2, 8, SORTED, true>(g, vel, in, out, w, dt, dev, st);
-        else
-            launch_g2p_t<2, 8, SORTED, false>(g, vel, in, out, w, dt, dev, st);
-    } else {
+    if (g.dim == 3 && g.T == 4)
+        launch_g2p_dt<3, 4, SORTED>(g, vel, in, out, w, dt, dev, st);
+    else if (g.dim == 2 && g.T == 8)
+        launch_g2p_dt<2, 8, SORTED>(g, vel, in, out, w, dt, dev, st);
+    else
         return MPM_E_ARG;
-    }
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }
 
@@ -556,9 +600,12 @@ __global__ void k_permute(int ncomp, PartsF in, PartsF out, const uint32_t *__re
             } else if (c < 25) {
                 s = in.F[c - 16];
                 d = out.F[c - 16];
-            } else {
+            } else if (c == 25) {
                 s = in.vol;
                 d = out.vol;
+            } else {
+                s = in.phi;
+                d = out.phi;
             }
             if (s && d) d[j] = s[src];
         }
@@ -569,7 +616,7 @@ __global__ void k_permute(int ncomp, PartsF in, PartsF out, const uint32_t *__re
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
                           const DeviceInfo &dev, cudaStream_t st) {
     const int blocks = dev.sms * 8;
-    k_permute<<<blocks, 256, 0, st>>>(26, in, out, perm, in.n);
+    k_permute<<<blocks, 256, 0, st>>>(27, in, out, perm, in.n);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }
 

@@ -33,17 +33,17 @@ __device__ __forceinline__ int32_t rint_f(float a) { return __float_as_int(__fad
 // The particle's affine matrix as P2G scatters it: C, and for elastic
 // particles C minus the stress term (stress.cuh); counts the elastic
 // particles whose det F leaves them unstressed.
-template <int DIM, bool EL, typename Rec>
+template <int DIM, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ void load_affine(const Rec &rec, const StressP &sp, float (&C)[DIM * DIM],
                                             uint32_t &degenerate) {
-    using Fl = P2GFields<DIM, EL>;
+    using Fl = P2GFields<DIM, EL, VC>;
 #pragma unroll
     for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
     if constexpr (EL) {
         float F[DIM * DIM];
 #pragma unroll
         for (int j = 0; j < DIM * DIM; ++j) F[j] = rec(Fl::BASE + j);
-        if (!fold_stress<DIM>(sp, F, rec(Fl::BASE + DIM * DIM), rec(2 * DIM + DIM * DIM), C)) ++degenerate;
+        if (!fold_stress<DIM>(sp, F, rec(Fl::VOLF), rec(2 * DIM + DIM * DIM), C)) ++degenerate;
     }
 }
 
@@ -51,10 +51,13 @@ __device__ __forceinline__ void load_affine(const Rec &rec, const StressP &sp, f
 // are formed (the arithmetic the oracle states).  Returns false (and adds
 // nothing) when the particle is out of range.
 // rec(f) reads field f of the particle (P2GFields: x[dim], v[dim],
-// C[dim*dim], m, then F[dim*dim] and vol for elastic particles).
-template <int DIM, int T, typename Hl, bool EL, typename Rec>
+// C[dim*dim], m, then F[dim*dim] for elastic particles, and vol).  With the
+// volume channel (VC) the rest volume in cells, Vt = (vol * inv_dx^dim) * S,
+// is split over the stencil as the mass is, into channel dim + 1.
+template <int DIM, int T, typename Hl, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo,
                                               const StressP &sp, uint32_t &degenerate) {
+    using Fl = P2GFields<DIM, EL, VC>;
     using St = Stencil<DIM>;
     float f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
@@ -65,12 +68,15 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     float v[DIM], C[DIM * DIM];
 #pragma unroll
     for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
-    load_affine<DIM, EL>(rec, sp, C, degenerate);
+    load_affine<DIM, EL, VC>(rec, sp, C, degenerate);
     const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
-    // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) at most 2^22 - 4096
+    [[maybe_unused]] float Vt = 0.f;
+    if constexpr (VC) Vt = __fmul_rn(__fmul_rn(rec(Fl::VOLF), g.vcell), g.S);
+    // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) (and wmax*|Vt|) at most 2^22 - 4096
     const float h = __fmul_rn(1.5f, g.dx);
     const float aM = fabsf(Mt);
     bool ok = __fmul_rn(g.wmax, aM) <= kShareLimit;
+    if constexpr (VC) ok = ok && __fmul_rn(g.wmax, fabsf(Vt)) <= kShareLimit;
 #pragma unroll
     for (int k = 0; k < DIM; ++k) {
         float sc = __fadd_rn(fabsf(C[k * DIM + 0]), fabsf(C[k * DIM + 1]));
@@ -88,8 +94,9 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     }
     const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
                             : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
-    int32_t rest[St::NC];
+    int32_t rest[St::NC + 1];
     rest[0] = __float2int_rn(Mt);
+    rest[St::NC] = VC ? __float2int_rn(Vt) : 0;
 #pragma unroll
     for (int k = 0; k < DIM; ++k) rest[1 + k] = __float2int_rn(__fmul_rn(Mt, v[k]));
     // the x and y momentum channels go through packed fp32x2 arithmetic,
@@ -102,12 +109,14 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     static_for<3>([&](auto A0) {
         constexpr int a0 = decltype(A0)::value;
         const float Wx = __fmul_rn(w[0][a0], Mt);
+        // lane y carries the volume weight with the volume channel, else the mass weight again
+        const float2 Wx2 = make_float2(Wx, VC ? __fmul_rn(w[0][a0], Vt) : Wx);
         const float2 h0xy = __ffma2_rn(Cxy[0], make_float2(dd[0][a0], dd[0][a0]), make_float2(v[0], v[1]));
         [[maybe_unused]] float h0z = 0.f;
         if constexpr (DIM == 3) h0z = __fmaf_rn(C[6], dd[0][a0], v[2]);
         static_for<3>([&](auto A1) {
             constexpr int a1 = decltype(A1)::value;
-            const float2 Wxy = __fmul2_rn(make_float2(Wx, Wx), make_float2(w[1][a1], w[1][a1]));
+            const float2 Wxy = __fmul2_rn(Wx2, make_float2(w[1][a1], w[1][a1]));
             const float2 h1xy = __ffma2_rn(Cxy[1], make_float2(dd[1][a1], dd[1][a1]), h0xy);
             [[maybe_unused]] float h1z = 0.f;
             if constexpr (DIM == 3) h1z = __fmaf_rn(C[7], dd[1][a1], h0z);
@@ -120,9 +129,15 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
                     const int32_t sm = rint_f(Wt.x);
                     rest[0] -= sm;
                     red_shared_add<off>(base, sm);
+                    if constexpr (VC) {
+                        const int32_t sv = rint_f(Wt.y);
+                        rest[St::NC] -= sv;
+                        red_shared_add<off + 4 * (DIM + 1) * Hl::SIZE>(base, sv);
+                    }
+                    const float2 Wm = VC ? make_float2(Wt.x, Wt.x) : Wt;
                     const float2 velxy =
                         DIM == 3 ? __ffma2_rn(Cxy[2], make_float2(dd[2][a2], dd[2][a2]), h1xy) : h1xy;
-                    const float2 bxy = __ffma2_rn(Wt, velxy, magic2);
+                    const float2 bxy = __ffma2_rn(Wm, velxy, magic2);
                     const int32_t sx = __float_as_int(bxy.x) - kMagicBits, sy = __float_as_int(bxy.y) - kMagicBits;
                     rest[1] -= sx;
                     rest[2] -= sy;
@@ -143,13 +158,15 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     red_shared_add<offc + 4 * Hl::SIZE>(base, rest[1]);
     red_shared_add<offc + 8 * Hl::SIZE>(base, rest[2]);
     if constexpr (DIM == 3) red_shared_add<offc + 12 * Hl::SIZE>(base, rest[3]);
+    if constexpr (VC) red_shared_add<offc + 4 * (DIM + 1) * Hl::SIZE>(base, rest[St::NC]);
     return true;
 }
 
-template <int DIM, int T, bool EL, typename Rec>
+template <int DIM, int T, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, const int o[3], float *sacc,
                                               const StressP &sp, uint32_t &degenerate) {
     using Hl = Halo<DIM, T>;
+    using Fl = P2GFields<DIM, EL, VC>;
     float f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
     float xs[DIM];
@@ -159,8 +176,10 @@ __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, co
     float v[DIM], C[DIM * DIM], w[3][3], dd[3][3];
 #pragma unroll
     for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
-    load_affine<DIM, EL>(rec, sp, C, degenerate);
+    load_affine<DIM, EL, VC>(rec, sp, C, degenerate);
     const float m = rec(2 * DIM + DIM * DIM);
+    [[maybe_unused]] float q = 0.f;
+    if constexpr (VC) q = __fmul_rn(rec(Fl::VOLF), g.vcell);
 #pragma unroll
     for (int l = 0; l < DIM; ++l) {
         quad_weights(f[l], w[l]);
@@ -187,6 +206,10 @@ __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, co
                 const float W = DIM == 3 ? __fmul_rn(Wxy, w[2][a2]) : Wxy;
                 const int at = hb + Hl::off(a);
                 atomicAdd(&sacc[at], W);
+                if constexpr (VC) {
+                    const float Wvxy = __fmul_rn(__fmul_rn(w[0][a0], q), w[1][a1]);
+                    atomicAdd(&sacc[(DIM + 1) * Hl::SIZE + at], DIM == 3 ? __fmul_rn(Wvxy, w[2][a2]) : Wvxy);
+                }
 #pragma unroll
                 for (int k = 0; k < DIM; ++k) {
                     const float vel = DIM == 3 ? __fmaf_rn(C[k * DIM + 2], dd[2][a2], h1[k]) : h1[k];
@@ -226,15 +249,16 @@ __device__ __forceinline__ SliceMeta slice_meta(const uint32_t *slices, const ui
 // a round in different banks.
 constexpr int kP2GWarps = kP2GThreads / 32;
 
-template <int DIM, int T, typename AccT, bool EL>
+template <int DIM, int T, typename AccT, bool EL, bool VC>
 __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
     k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm, const uint32_t *__restrict__ slices,
                 const uint32_t *__restrict__ start, uint32_t *__restrict__ status, AccT *__restrict__ acc,
                 StressP sp) {
     using St = Stencil<DIM>;
     using Hl = HaloU<DIM, T>;
-    using Fl = P2GFields<DIM, EL>;
-    constexpr int HW = St::NC * Hl::NODES;  // halo words per warp
+    using Fl = P2GFields<DIM, EL, VC>;
+    constexpr int NCH = St::NC + (VC ? 1 : 0);  // accumulator channels
+    constexpr int HW = NCH * Hl::NODES;         // halo words per warp
     __shared__ __align__(16) int32_t shalo[kP2GWarps][HW];
     __shared__ float sbuf[kP2GWarps][2 * Fl::NF * 32];
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
@@ -271,7 +295,7 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
                 const bool on = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
                 const int64_t node = node_index(g, gx, gy, gz);
 #pragma unroll
-                for (int c = 0; c < St::NC; ++c) {
+                for (int c = 0; c < NCH; ++c) {
                     const int32_t val = wh[c * Hl::NODES + h];
                     if (val == 0) continue;
                     wh[c * Hl::NODES + h] = 0;
@@ -298,7 +322,7 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
             if (r < cnt) {
                 const int st = stage;
                 auto rec = [&](int f) { return *at(st, f); };
-                if (!scatter_fixed<DIM, T, Hl, EL>(g, rec, o, halo, sp, degenerate)) ++bad;
+                if (!scatter_fixed<DIM, T, Hl, EL, VC>(g, rec, o, halo, sp, degenerate)) ++bad;
             }
             stage ^= 1;
             // int32 halo accumulators: at most 512 shares of magnitude below
@@ -321,7 +345,7 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
 }
 
 // Float-atomic P2G (comparison variant: fp32 adds, order dependent).
-template <int DIM, int T, bool EL>
+template <int DIM, int T, bool EL, bool VC>
 __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, const uint32_t *__restrict__ perm,
                                                            const uint32_t *__restrict__ slices,
                                                            const uint32_t *__restrict__ start,
@@ -329,9 +353,10 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
                                                            float *__restrict__ acc, StressP sp) {
     using St = Stencil<DIM>;
     using Hl = Halo<DIM, T>;
-    using Fl = P2GFields<DIM, EL>;
+    using Fl = P2GFields<DIM, EL, VC>;
+    constexpr int NCH = St::NC + (VC ? 1 : 0);
     uint32_t degenerate = 0;
-    __shared__ float sacc[St::NC * Hl::SIZE];
+    __shared__ float sacc[NCH * Hl::SIZE];
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
     uint32_t next = 0;
@@ -346,13 +371,13 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
             int hx, hy, hz, idx;
             Hl::node(h, hx, hy, hz, idx);
 #pragma unroll
-            for (int c = 0; c < St::NC; ++c) sacc[c * Hl::SIZE + idx] = 0.f;
+            for (int c = 0; c < NCH; ++c) sacc[c * Hl::SIZE + idx] = 0.f;
         }
         __syncthreads();
         for (uint32_t r = threadIdx.x; r < cnt; r += blockDim.x) {
             const uint32_t pid = perm[beg + r];
             auto rec = [&](int f) { return Fl::src(p, f)[pid]; };
-            scatter_float<DIM, T, EL>(g, rec, o, sacc, sp, degenerate);
+            scatter_float<DIM, T, EL, VC>(g, rec, o, sacc, sp, degenerate);
         }
         __syncthreads();
         for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
@@ -362,7 +387,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
             if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
             const int64_t node = node_index(g, gx, gy, gz);
 #pragma unroll
-            for (int c = 0; c < St::NC; ++c) {
+            for (int c = 0; c < NCH; ++c) {
                 const float val = sacc[c * Hl::SIZE + idx];
                 if (val != 0.f) atomicAdd(acc + c * g.nodes + node, val);
             }
@@ -375,41 +400,47 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
     }
 }
 
-template <int DIM, int T, bool EL>
+template <int DIM, int T, bool EL, bool VC>
 void launch_p2g_t(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const StressP &sp, int blocks,
                   cudaStream_t st) {
     if (g.acc_mode == MPM_ACC_I64)
-        k_p2g_fixed<DIM, T, int64_t, EL><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                        (int64_t *)grid_acc, sp);
+        k_p2g_fixed<DIM, T, int64_t, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start,
+                                                                            w.status, (int64_t *)grid_acc, sp);
     else if (g.acc_mode == MPM_ACC_I32)
-        k_p2g_fixed<DIM, T, int32_t, EL><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                        (int32_t *)grid_acc, sp);
+        k_p2g_fixed<DIM, T, int32_t, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start,
+                                                                            w.status, (int32_t *)grid_acc, sp);
     else
-        k_p2g_float<DIM, T, EL><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                               (float *)grid_acc, sp);
+        k_p2g_float<DIM, T, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
+                                                                   (float *)grid_acc, sp);
+}
+
+template <int DIM, int T>
+void launch_p2g_dt(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const StressP &sp, int blocks,
+                   cudaStream_t st) {
+    const bool el = p.F[0] != nullptr;
+    if (el && g.vc)
+        launch_p2g_t<DIM, T, true, true>(g, p, w, grid_acc, sp, blocks, st);
+    else if (el)
+        launch_p2g_t<DIM, T, true, false>(g, p, w, grid_acc, sp, blocks, st);
+    else if (g.vc)
+        launch_p2g_t<DIM, T, false, true>(g, p, w, grid_acc, sp, blocks, st);
+    else
+        launch_p2g_t<DIM, T, false, false>(g, p, w, grid_acc, sp, blocks, st);
 }
 
 mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt,
                       const DeviceInfo &dev, cudaStream_t st) {
     const int blocks = dev.sms * 4;
-    const bool el = p.F[0] != nullptr;
     const StressP sp{p.mu, p.lam, dt, (4.0f * g.inv_dx) * g.inv_dx};
     // degenerate-particle count and work counter
     static_assert(MPM_ST_WORK_P2G == MPM_ST_N_DEGENERATE + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_N_DEGENERATE], 0, 2 * sizeof(uint32_t), st);
-    if (g.dim == 3 && g.T == 4) {
-        if (el)
-            launch_p2g_t<3, 4, true>(g, p, w, grid_acc, sp, blocks, st);
-        else
-            launch_p2g_t<3, 4, false>(g, p, w, grid_acc, sp, blocks, st);
-    } else if (g.dim == 2 && g.T == 8) {
-        if (el)
-            launch_p2g_t<2, 8, true>(g, p, w, grid_acc, sp, blocks, st);
-        else
-            launch_p2g_t<2, 8, false>(g, p, w, grid_acc, sp, blocks, st);
-    } else {
+    if (g.dim == 3 && g.T == 4)
+        launch_p2g_dt<3, 4>(g, p, w, grid_acc, sp, blocks, st);
+    else if (g.dim == 2 && g.T == 8)
+        launch_p2g_dt<2, 8>(g, p, w, grid_acc, sp, blocks, st);
+    else
         return MPM_E_ARG;
-    }
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }
 

@@ -38,9 +38,10 @@ class MPMSystem:
         mode = grid["acc_mode"]
         acc_dtype = {L.MPM_ACC_I32: torch.int32, L.MPM_ACC_I64: torch.int64, L.MPM_ACC_F32: torch.float32,
                      L.MPM_ACC_EXACT_INT: torch.int64}[mode]
-        self.acc = torch.zeros((dim + 1, self.nodes), dtype=acc_dtype, device=self.device)
+        self.vc = int(grid.get("volume_channel", 0))
+        self.acc = torch.zeros((dim + 1 + self.vc, self.nodes), dtype=acc_dtype, device=self.device)
         assert self.acc.numel() * self.acc.element_size() == acc_bytes
-        self.vel = torch.zeros((dim, self.nodes), dtype=torch.float32, device=self.device)
+        self.vel = torch.zeros((dim + self.vc, self.nodes), dtype=torch.float32, device=self.device)
         self.status_host = torch.zeros(L.MPM_STATUS_WORDS, dtype=torch.int32).pin_memory() \
             if torch.cuda.is_available() else torch.zeros(L.MPM_STATUS_WORDS, dtype=torch.int32)
         self.dt = float(grid.get("dt", 0.0))
@@ -48,6 +49,7 @@ class MPMSystem:
         self.x = self.v = self.C = self.m = None
         self.id = self.id2 = None
         self.F = self.vol = self.F2 = self.vol2 = None
+        self.phi = self.phi2 = None
         self.material = {"mu": 0.0, "lambda": 0.0}
         self.parts = self.parts2 = None
 
@@ -64,7 +66,15 @@ class MPMSystem:
             f32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.float32)).to(self.device)
             self.x, self.v, self.C, self.m = f32(x), f32(v), f32(C), f32(m)
         assert self.x.shape[1] <= self.n
-        self.parts = self._parts(self.x, self.v, self.C, self.m, None, self.F, self.vol)
+        self.parts = self._parts(self.x, self.v, self.C, self.m, None, self.F, self.vol, self.phi)
+        return self
+
+    def load_volume(self, vol):
+        """Rest volumes [n] for the volume channel; phi (the gathered volume fraction) starts at zero."""
+        f32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.float32)).to(self.device)
+        self.vol = f32(vol)
+        self.phi = torch.zeros_like(self.vol)
+        self.parts = self._parts(self.x, self.v, self.C, self.m, self.id, self.F, self.vol, self.phi)
         return self
 
     def load_elastic(self, F, vol, material: dict):
@@ -72,12 +82,14 @@ class MPMSystem:
         volumes vol [n] and the Neo-Hookean constants {"mu", "lambda"}."""
         f32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.float32)).to(self.device)
         self.F, self.vol = f32(F), f32(vol)
+        if self.vc and self.phi is None:
+            self.phi = torch.zeros_like(self.vol)
         self.material = {"mu": float(material["mu"]), "lambda": float(material["lambda"])}
-        self.parts = self._parts(self.x, self.v, self.C, self.m, self.id, self.F, self.vol)
+        self.parts = self._parts(self.x, self.v, self.C, self.m, self.id, self.F, self.vol, self.phi)
         return self
 
-    def _parts(self, x, v, C, m, id, F, vol):
-        return L.particles(x, v, C, m, id, F, vol, self.material["mu"], self.material["lambda"])
+    def _parts(self, x, v, C, m, id, F, vol, phi=None):
+        return L.particles(x, v, C, m, id, F, vol, self.material["mu"], self.material["lambda"], phi)
 
     def elastic_state(self):
         """(F, vol) as numpy arrays."""
@@ -118,9 +130,13 @@ class MPMSystem:
             self.id = self.id2 = None
         self.x2, self.v2, self.C2, self.m2 = (torch.empty_like(t) for t in (self.x, self.v, self.C, self.m))
         if self.F is not None:
-            self.F2, self.vol2 = torch.empty_like(self.F), torch.empty_like(self.vol)
-        self.parts = self._parts(self.x, self.v, self.C, self.m, self.id, self.F, self.vol)
-        self.parts2 = self._parts(self.x2, self.v2, self.C2, self.m2, self.id2, self.F2, self.vol2)
+            self.F2 = torch.empty_like(self.F)
+        if self.vol is not None:
+            self.vol2 = torch.empty_like(self.vol)
+        if self.phi is not None:
+            self.phi2 = torch.zeros_like(self.phi)
+        self.parts = self._parts(self.x, self.v, self.C, self.m, self.id, self.F, self.vol, self.phi)
+        self.parts2 = self._parts(self.x2, self.v2, self.C2, self.m2, self.id2, self.F2, self.vol2, self.phi2)
         return self
 
     def swap(self):
@@ -131,6 +147,7 @@ class MPMSystem:
         self.id, self.id2 = self.id2, self.id
         self.F, self.F2 = self.F2, self.F
         self.vol, self.vol2 = self.vol2, self.vol
+        self.phi, self.phi2 = self.phi2, self.phi
         self.parts, self.parts2 = self.parts2, self.parts
 
     def g2p_sorted(self, stream=None):
