@@ -39,12 +39,26 @@ LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2
 # the 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
-    "p2g": {"bytes_per_particle": 82.1, "files": ("p2g.cu", "common.cuh"),
-            "sha256": "098a72f38c248480137b7082b87285b56b829b7fc515cb580b41283b0021d3a5"
-                      "caa52acb850be6dfcc10664d1a0528e01c133bee3783931b11469d24af5c1ad8"},
-    "g2p": {"bytes_per_particle": 77.0, "files": ("grid_g2p.cu", "common.cuh"),
-            "sha256": "612b6f184ccf40ab83fa3319579f43bbae68baa3bfe4fae71b1d274ca70a74da"
-                      "caa52acb850be6dfcc10664d1a0528e01c133bee3783931b11469d24af5c1ad8"},
+    "p2g": {"bytes_per_particle": 82.0, "files": ('p2g.cu', 'common.cuh'),
+            "sha256": "c6dfe51b1f0273472f433146ebc3674e1c64082a7c1e4562caf3dba360d5507c"
+                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
+    "g2p": {"bytes_per_particle": 77.0, "files": ('grid_g2p.cu', 'common.cuh'),
+            "sha256": "651b07b89e4be6450719238e229272fcbb4bfa75c60eb2d9ce821fbc2d668c0b"
+                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
+    "p2g_el": {"bytes_per_particle": 126.3, "files": ('p2g.cu', 'common.cuh', 'stress.cuh'),
+            "sha256": "c6dfe51b1f0273472f433146ebc3674e1c64082a7c1e4562caf3dba360d5507c"
+                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"
+                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
+    "g2p_el": {"bytes_per_particle": 156.5, "files": ('grid_g2p.cu', 'common.cuh', 'stress.cuh'),
+            "sha256": "651b07b89e4be6450719238e229272fcbb4bfa75c60eb2d9ce821fbc2d668c0b"
+                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"
+                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
+    "p2g_vc": {"bytes_per_particle": 89.3, "files": ('p2g.cu', 'common.cuh'),
+            "sha256": "c6dfe51b1f0273472f433146ebc3674e1c64082a7c1e4562caf3dba360d5507c"
+                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
+    "g2p_vc": {"bytes_per_particle": 88.1, "files": ('grid_g2p.cu', 'common.cuh'),
+            "sha256": "651b07b89e4be6450719238e229272fcbb4bfa75c60eb2d9ce821fbc2d668c0b"
+                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
 }
 
 
@@ -366,7 +380,8 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
            "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, parts)},
            "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                        "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None}}
+                        "unit": "GB/s", "frac": round(achieved / peak, 4),
+                        "traffic": measured_traffic(f"{dom}_{'el' if elastic else 'vc'}", n)}}
     if elastic:
         out["material"] = {"mu": ELASTIC["mu"], "lambda": ELASTIC["lambda"], "F": "I + N(0, 0.05) per entry",
                            "V0": "dx^3"}
