@@ -35,8 +35,9 @@ LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2
 
 
 # DRAM traffic per particle (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by the
-# particles it processed) from the ncu capture summarised in profiles/p2g_g2p_full_blobs3d_2M.md, taken on
-# the 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
+# particles it processed) from the ncu captures summarised in profiles/p2g_g2p_full_blobs3d_2M.md and (the
+# "_el" stress and "_vc" volume-channel variants) profiles/stress_volume_full_blobs3d_2M.md, taken on the
+# 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
     "p2g": {"bytes_per_particle": 82.0, "files": ('p2g.cu', 'common.cuh'),
