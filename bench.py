@@ -255,10 +255,11 @@ def run_ours(args, rank, world, local):
                 "frac": round((n * 136.0 + touched * 64.0) / (tr_ms * 1e-3) / 1e9 / peak, 4),
                 "bin_ms": round(float(mean_ms[0]), 4)}
 
-    elastic = volume = None
+    elastic = volume = fused = None
     if args.variant_steps > 0:
         elastic = measure_variant(args, cloud, dev, stream, world, peak, elastic=True, volume=False)
         volume = measure_variant(args, cloud, dev, stream, world, peak, elastic=False, volume=True)
+        fused = measure_fused(args, cloud, dev, stream, world, peak, touched, float(mean_ms[0]))
 
     # end to end through the host entry point (pinned host SoA, copies inside the timed region)
     e2e = None
@@ -307,6 +308,7 @@ def run_ours(args, rank, world, local):
         "advective_step_bound": advective,
         "mls_stress": elastic,
         "volume_channel": volume,
+        "fused_step": fused,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
@@ -392,6 +394,44 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
         out["volume_fraction"] = {"V0": "dx^3 (one cell)", "mean": round(float(phi.mean().item()), 4),
                                   "max": round(float(phi.max().item()), 4)}
     del es
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_fused(args, cloud, dev, stream, world, peak, touched, bin_ms):
+    """The same workload stepped by mpm_step_fused (bin, then one kernel for the grid
+    update, G2P and the next P2G, then the clear of the grid it read), steady state."""
+    import torch
+    from material_point_particle_gb300 import _lib as L
+    from material_point_particle_gb300.system import MPMSystem
+
+    steps = args.variant_steps
+    n = cloud["x"].shape[1]
+    fs = MPMSystem(cloud["grid"], n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted() \
+        .enable_fused()
+    for _ in range(max(3, args.warmup)):
+        fs.step_fused(stream)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        fs.step_fused(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    st = fs.status()
+    assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
+    ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
+    # algorithmic bytes of the fused kernel: read x, m, id (20 B) and write x, v, C, m, id (68 B) per
+    # particle; read the accumulators R and write W (32 B each per touched node)
+    kern_ms = ms - bin_ms
+    achieved = (n * 88.0 + touched * 64.0) / (kern_ms * 1e-3) / 1e9
+    out = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+           "escaped": int(st[L.ST_N_ESCAPED]), "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
+           "roofline": {"bound": "hbm", "kernel": "g2p2g + clear (step minus the main region's bin time)",
+                        "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4), "traffic": None}}
+    del fs
     torch.cuda.empty_cache()
     return out
 

@@ -13,6 +13,7 @@
  *   mpm_grid_update  momentum -> velocity, gravity, boundary; clears the
  *                    accumulators it reads
  *   mpm_g2p          gather of velocity and affine matrix, advection
+ *   mpm_step_fused   grid update, G2P and the next P2G in one kernel
  *
  * Conventions shared by every call:
  *  - All pointers inside the structs are DEVICE pointers unless a call says
@@ -125,6 +126,8 @@ enum {
     MPM_ST_WORK_G2P = 12,    /* internal: work counter of the G2P launch */
     MPM_ST_MAX_SPEED = 13,   /* fp32 bits of max over the particles the last G2P moved of
                                 |v'| + 1.5 dx |C'|_F; the advective step bound is dt <= dx / it */
+    MPM_ST_N_ESCAPED = 14,   /* mpm_step_fused: particles that moved further than one cell, scattered
+                                straight into the global grid */
     MPM_STATUS_WORDS = 16
 };
 
@@ -309,6 +312,28 @@ mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_par
 mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev_in,
                          mpm_particles *dev_out, mpm_bins *bins, void *grid_acc, float *grid_vel, float dt,
                          const float dtg[3], void *stream);
+
+/*
+ * mpm_step_fused -- one step as the fused gather-scatter kernel of the
+ * implementation guide, section 2.1 (one kernel per step: load the tile's
+ * nodes applying the grid update, gather each particle, scatter it back into
+ * shared-memory accumulators, flush them once).  `acc_read` must hold the
+ * accumulators of mpm_p2g at the positions of `in` (the first step: mpm_bin
+ * and mpm_p2g on `in`; later steps: the previous call's `acc_write`);
+ * `acc_write` must be zero.  The call bins `in`, gathers as mpm_grid_update +
+ * mpm_g2p_sorted would into `out` (the same order and bits), scatters the new
+ * state into `acc_write` as mpm_p2g on `out` would (the same integers), and
+ * clears `acc_read`; the caller then swaps in/out and the two grids.
+ * Particles that moved further than one cell in the step are scattered
+ * straight into the global grid and counted in MPM_ST_N_ESCAPED; those
+ * leaving the domain are not scattered; out-of-range ones are counted in
+ * MPM_ST_N_OUT_OF_RANGE as by mpm_p2g.  MPM_ACC_I64 only, without the
+ * elastic state or the volume channel (MPM_E_ARG otherwise): the int32 mode's
+ * bound is checked by the binning of the positions it will scatter, which
+ * this scatter runs ahead of.  No velocity grid is written.
+ */
+mpm_status mpm_step_fused(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
+                          void *acc_read, void *acc_write, float dt, const float dtg[3], void *stream);
 
 /* Reorders a particle SoA by bins->perm: out[j] = in[perm[j]] for every
  * component (and id if both are non-NULL), all n entries.  `in` and `out`

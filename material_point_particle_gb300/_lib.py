@@ -21,6 +21,7 @@ MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
 ST_BIN_WORDS = 10   # status words 0..9 are written by mpm_bin
 ST_N_DEGENERATE = 10  # elastic particles the last P2G scattered without stress (det F not positive normal)
 ST_MAX_SPEED = 13   # fp32 bits of max |v'| + 1.5 dx |C'|_F over the particles the last G2P moved
+ST_N_ESCAPED = 14   # mpm_step_fused: particles that moved more than a cell (scattered into the global grid)
 MPM_STATUS_WORDS = 16
 MPM_STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -82,12 +83,14 @@ def library() -> ct.CDLL:
                                           P(ct.c_float), VP]
             L.mpm_step_host.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Particles), P(Bins), VP, VP,
                                         ct.c_float, P(ct.c_float), VP]
+            L.mpm_step_fused.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
+                                         P(ct.c_float), VP]
             L.mpm_permute.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP]
             L.mpm_read_status.argtypes = [P(Bins), VP, VP]
             L.mpm_bin_static.argtypes = [P(GridDesc), P(Particles), ct.c_int, P(Bins), VP]
             for name in ("mpm_bins_init", "mpm_bin", "mpm_p2g", "mpm_grid_update", "mpm_g2p", "mpm_step",
                          "mpm_g2p_sorted", "mpm_step_sorted", "mpm_step_host", "mpm_permute", "mpm_read_status",
-                         "mpm_bin_static"):
+                         "mpm_bin_static", "mpm_step_fused"):
                 getattr(L, name).restype = ct.c_int
             _L = L
     return _L
@@ -225,6 +228,13 @@ def mpm_g2p_sorted(desc: GridDesc, grid_vel: torch.Tensor, src: Particles, dst: 
                    stream=None):
     _check(library().mpm_g2p_sorted(ct.byref(desc), ct.c_void_p(grid_vel.data_ptr()), ct.byref(src), ct.byref(dst),
                                     ct.byref(bins), ct.c_float(dt), _stream(stream)), "mpm_g2p_sorted")
+
+
+def mpm_step_fused(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, acc_read: torch.Tensor,
+                   acc_write: torch.Tensor, dt: float, dtg, stream=None):
+    _check(library().mpm_step_fused(ct.byref(desc), ct.byref(src), ct.byref(dst), ct.byref(bins),
+                                    ct.c_void_p(acc_read.data_ptr()), ct.c_void_p(acc_write.data_ptr()),
+                                    ct.c_float(dt), _f3(dtg), _stream(stream)), "mpm_step_fused")
 
 
 def mpm_step_sorted(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, grid_acc: torch.Tensor,

@@ -391,6 +391,24 @@ mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_par
     return mpm_g2p_sorted(desc, grid_vel, in, out, bins, dt, stream);
 }
 
+mpm_status mpm_step_fused(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
+                          void *acc_read, void *acc_write, float dt, const float dtg[3], void *stream) {
+    GridP g;
+    MPM_TRY(make_grid(desc, g));
+    if (g.acc_mode != MPM_ACC_I64 || g.vc || !acc_read || !acc_write || acc_read == acc_write || !dtg)
+        return MPM_E_ARG;
+    PartsF pi, po;
+    MPM_TRY(parts_f(g, in, true, pi));
+    MPM_TRY(parts_f(g, out, true, po));
+    if (pi.F[0] || po.F[0]) return MPM_E_ARG;
+    if (pi.n != po.n || (!pi.id) != (!po.id)) return MPM_E_ARG;
+    MPM_TRY(mpm_bin(desc, in, bins, 0, stream));
+    DeviceInfo dev;
+    MPM_TRY(device_info(dev));
+    return launch_g2p2g(g, pi, po, view_of(g, *bins), acc_read, acc_write, dt, dtg, dev,
+                        static_cast<cudaStream_t>(stream));
+}
+
 mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev_in,
                          mpm_particles *dev_out, mpm_bins *bins, void *grid_acc, float *grid_vel, float dt,
                          const float dtg[3], void *stream) {

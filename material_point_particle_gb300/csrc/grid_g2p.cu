@@ -13,6 +13,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "gather.cuh"
 #include "internal.h"
 #include "stress.cuh"
 
@@ -115,10 +116,6 @@ mpm_status launch_grid_update(const GridP &g, void *grid_acc, float *vel, const 
 }
 
 // --------------------------------------------------------------------------
-__device__ __forceinline__ float sum3(const float w[3], const float t[3]) {
-    return __fmaf_rn(w[2], t[2], __fmaf_rn(w[1], t[1], __fmul_rn(w[0], t[0])));
-}
-
 // Whole-state copy of particle `src` of p to entry `dst` of q.
 template <int DIM>
 __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, uint32_t src, uint32_t dst) {
@@ -137,21 +134,6 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
     }
     if (q.vol && p.vol) q.vol[dst] = p.vol[src];
     if (q.phi && p.phi) q.phi[dst] = p.phi[src];
-}
-
-// Velocity halo of one tile in shared memory, in the compact layout of the
-// P2G accumulators (HaloU), one array per component.
-template <int DIM, int T>
-struct VelHalo {
-    float *x, *y, *z;
-    float *phi;  // node volume fractions (volume channel)
-};
-
-__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
-
-// sum3 on two independent lanes (each lane exactly the scalar sum3)
-__device__ __forceinline__ float2 sum3x2(const float2 w[3], const float2 t[3]) {
-    return __ffma2_rn(w[2], t[2], __ffma2_rn(w[1], t[1], __fmul2_rn(w[0], t[0])));
 }
 
 // One particle's gather from the tile's velocity halo in shared memory.  The
@@ -190,86 +172,8 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     }
     const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
                             : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
-    float2 W[3][3], WE[3][3];
-#pragma unroll
-    for (int l = 0; l < DIM; ++l)
-#pragma unroll
-        for (int a = 0; a < 3; ++a) {
-            W[l][a] = f2(w[l][a]);
-            WE[l][a] = f2(we[l][a]);
-        }
     float vn[DIM], Bm[DIM][DIM];
-    const float *vx = sv.x + hb, *vy = sv.y + hb;
-    if constexpr (DIM == 3) {
-        // x and y packed
-        float2 Y[3], Ye[3], Yq[3];
-#pragma unroll
-        for (int a0 = 0; a0 < 3; ++a0) {
-            float2 Z[3], Zq[3];
-#pragma unroll
-            for (int a1 = 0; a1 < 3; ++a1) {
-                float2 t[3];
-#pragma unroll
-                for (int a2 = 0; a2 < 3; ++a2) {
-                    const int i = a0 + a1 * Hl::SY + a2 * Hl::SZ;
-                    t[a2] = make_float2(vx[i], vy[i]);
-                }
-                Z[a1] = sum3x2(W[2], t);
-                Zq[a1] = sum3x2(WE[2], t);
-            }
-            Y[a0] = sum3x2(W[1], Z);
-            Ye[a0] = sum3x2(WE[1], Z);
-            Yq[a0] = sum3x2(W[1], Zq);
-        }
-        const float2 v2 = sum3x2(W[0], Y), b0 = sum3x2(WE[0], Y), b1 = sum3x2(W[0], Ye), b2 = sum3x2(W[0], Yq);
-        vn[0] = v2.x;
-        vn[1] = v2.y;
-        Bm[0][0] = b0.x;
-        Bm[1][0] = b0.y;
-        Bm[0][1] = b1.x;
-        Bm[1][1] = b1.y;
-        Bm[0][2] = b2.x;
-        Bm[1][2] = b2.y;
-        // z alone
-        const float *vz = sv.z + hb;
-        float Ys[3], Yes[3], Yqs[3];
-#pragma unroll
-        for (int a0 = 0; a0 < 3; ++a0) {
-            float Z[3], Zq[3];
-#pragma unroll
-            for (int a1 = 0; a1 < 3; ++a1) {
-                float t[3];
-#pragma unroll
-                for (int a2 = 0; a2 < 3; ++a2) t[a2] = vz[a0 + a1 * Hl::SY + a2 * Hl::SZ];
-                Z[a1] = sum3(w[2], t);
-                Zq[a1] = sum3(we[2], t);
-            }
-            Ys[a0] = sum3(w[1], Z);
-            Yes[a0] = sum3(we[1], Z);
-            Yqs[a0] = sum3(w[1], Zq);
-        }
-        vn[2] = sum3(w[0], Ys);
-        Bm[2][0] = sum3(we[0], Ys);
-        Bm[2][1] = sum3(w[0], Yes);
-        Bm[2][2] = sum3(w[0], Yqs);
-    } else {
-        float2 Y[3], Ye[3];
-#pragma unroll
-        for (int a0 = 0; a0 < 3; ++a0) {
-            float2 t[3];
-#pragma unroll
-            for (int a1 = 0; a1 < 3; ++a1) t[a1] = make_float2(vx[a0 + a1 * Hl::SY], vy[a0 + a1 * Hl::SY]);
-            Y[a0] = sum3x2(W[1], t);
-            Ye[a0] = sum3x2(WE[1], t);
-        }
-        const float2 v2 = sum3x2(W[0], Y), b0 = sum3x2(WE[0], Y), b1 = sum3x2(W[0], Ye);
-        vn[0] = v2.x;
-        vn[1] = v2.y;
-        Bm[0][0] = b0.x;
-        Bm[1][0] = b0.y;
-        Bm[0][1] = b1.x;
-        Bm[1][1] = b1.y;
-    }
+    gather_vB<DIM, T>(sv, hb, w, we, vn, Bm);
     // the advective bound's term |v'| + 1.5 dx |C'|_F, sums in index order
     float sv2 = 0.f, sc2 = 0.f;
     float Cn[DIM * DIM];
@@ -292,31 +196,7 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
         for (int j = 0; j < DIM * DIM; ++j) q.F[j][dst] = Fn[j];
     }
     if constexpr (SORTED && (EL || VC)) q.vol[dst] = p.vol[pid];
-    if constexpr (VC) {
-        // sum_a w(a) phi(a), innermost axis first (the order of v)
-        const float *vp = sv.phi + hb;
-        float Yp[3];
-#pragma unroll
-        for (int a0 = 0; a0 < 3; ++a0) {
-            if constexpr (DIM == 3) {
-                float Zp[3];
-#pragma unroll
-                for (int a1 = 0; a1 < 3; ++a1) {
-                    float t[3];
-#pragma unroll
-                    for (int a2 = 0; a2 < 3; ++a2) t[a2] = vp[a0 + a1 * Hl::SY + a2 * Hl::SZ];
-                    Zp[a1] = sum3(w[2], t);
-                }
-                Yp[a0] = sum3(w[1], Zp);
-            } else {
-                float t[3];
-#pragma unroll
-                for (int a1 = 0; a1 < 3; ++a1) t[a1] = vp[a0 + a1 * Hl::SY];
-                Yp[a0] = sum3(w[1], t);
-            }
-        }
-        q.phi[dst] = sum3(w[0], Yp);
-    }
+    if constexpr (VC) q.phi[dst] = gather_phi<DIM, T>(sv, hb, w);
     smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
 #pragma unroll
     for (int l = 0; l < DIM; ++l) q.x[l][dst] = __fmaf_rn(dt, vn[l], x[l]);
@@ -326,25 +206,6 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     }
 }
 
-// Interleaved slices.  The sorted output keeps each slice in its place but
-// orders it by the bank class of the particles' base cells (cell_class: the
-// cell's offset in the compact halo modulo 32, x + 6y + 36z in a 4^3 tile,
-// x + 10y in an 8^2 tile), stable in bin order, then deals the class-sorted entries out
-// column by column over rounds of 32: with R = ceil(cnt / 32) rounds and
-// L = cnt - 32 (R - 1) lanes in the last one, lane l holds sorted entries
-// [cum(l), cum(l + 1)), cum(l) = l R - max(0, l - L), and entry
-// cum(l) + rho sits at rho * 32 + l.  So the 32 entries of a round come from
-// classes spread over the whole range.  Cells of different classes put a
-// given stencil node in different shared-memory banks, and particles move a
-// small fraction of a cell per step, so P2G and G2P, which take particles 32
-// at a time in storage order, meet few bank conflicts.
-
-// Sorted entry held by place pos of an interleaved slice of cnt entries.
-__device__ __forceinline__ uint32_t interleave_entry(uint32_t pos, uint32_t cnt) {
-    const uint32_t R = (cnt + 31) / 32, L = cnt - 32 * (R - 1);
-    const uint32_t l = pos & 31u, rho = pos >> 5;
-    return l * R - (l > L ? l - L : 0u) + rho;
-}
 
 // Work item as in P2G: one slice of a tile.  The CTA stages the tile's halo
 // of node velocities in shared memory (padded as the P2G accumulators), then
@@ -359,19 +220,19 @@ __device__ __forceinline__ uint32_t interleave_entry(uint32_t pos, uint32_t cnt)
 // velocity halo meet few bank conflicts.  A slice of at most 32 particles is
 // one round and keeps bin order.
 template <int DIM, int T, bool SORTED, bool EL, bool VC>
-__global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
+__global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                      const uint32_t *__restrict__ perm,
                                                      const uint32_t *__restrict__ key,
                                                      const uint32_t *__restrict__ slices,
                                                      const uint32_t *__restrict__ start,
                                                      uint32_t *__restrict__ status, float dt, float c4) {
     using Hl = HaloU<DIM, T>;
-    constexpr int NQ = kSliceParticles / kP2GThreads;
-    constexpr int NWARP = kP2GThreads / 32;
+    constexpr int NQ = kSliceParticles / kG2PThreads;
+    constexpr int NWARP = kG2PThreads / 32;
     static_assert(NQ * NWARP == 32, "one warp-scan lane per (round, warp)");
     // in place: per-thread double buffer of x; sorted: x, m, id of the whole slice
     constexpr int NF = SORTED ? DIM + 2 : DIM;
-    constexpr int BUF = SORTED ? NF * kSliceParticles : 2 * NF * kP2GThreads;
+    constexpr int BUF = SORTED ? NF * kSliceParticles : 2 * NF * kG2PThreads;
     __shared__ float sv_x[Hl::SIZE], sv_y[Hl::SIZE], sv_z[DIM == 3 ? Hl::SIZE : 1], sv_phi[VC ? Hl::SIZE : 1];
     const VelHalo<DIM, T> sv{sv_x, sv_y, sv_z, sv_phi};
     __shared__ float sbuf[BUF];
@@ -381,7 +242,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
     // sorted entry e -> bin-order entry, at e + e / 32: the interleaved reads
     // take entries R apart
     __shared__ uint32_t order[SORTED ? kSliceParticles + kSliceParticles / 32 : 1];
-    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
     float smax = 0.f;  // the advective bound's largest term among this thread's particles
@@ -396,14 +257,14 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
         uint32_t pids[NQ];
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi) {
-            const uint32_t r = threadIdx.x + qi * kP2GThreads;
+            const uint32_t r = threadIdx.x + qi * kG2PThreads;
             pids[qi] = r < cnt ? perm[beg + r] : 0u;
         }
         if constexpr (SORTED) {
             // the slice's x, m, id in bin order
 #pragma unroll
             for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t r = threadIdx.x + qi * kP2GThreads;
+                const uint32_t r = threadIdx.x + qi * kG2PThreads;
                 if (r < cnt) {
 #pragma unroll
                     for (int f = 0; f < DIM; ++f) cp_async4(&sbuf[f * kSliceParticles + r], p.x[f] + pids[qi]);
@@ -434,59 +295,12 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                 gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
             }
         } else if constexpr (SORTED) {
-            // stable counting sort of the slice by bank class: counts per
-            // (round, warp, class), scanned class-major
-            uint32_t cls[NQ], below[NQ];
-#pragma unroll
-            for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t r = threadIdx.x + qi * kP2GThreads;
-                cls[qi] = r < cnt ? cell_class<DIM, T>(key[pids[qi]]) : 32u;
-            }
-            for (int i = threadIdx.x; i < NQ * NWARP * 33; i += blockDim.x) hist[i] = 0;
-            __syncthreads();
-#pragma unroll
-            for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, cls[qi]);
-                below[qi] = (uint32_t)__popc(peers & lanemask_lt());
-                if (cls[qi] < 32u && below[qi] == 0) hist[(qi * NWARP + warp) * 33 + cls[qi]] = (uint32_t)__popc(peers);
-            }
-            __syncthreads();
-            for (uint32_t c = warp; c < 32; c += NWARP) {
-                const uint32_t v = hist[lane * 33 + c];
-                uint32_t inc = v;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-                    if ((int)lane >= d) inc += t2;
-                }
-                hist[lane * 33 + c] = inc - v;
-                if (lane == 31) cstart[c] = inc;
-            }
-            __syncthreads();
-            if (warp == 0) {
-                const uint32_t v = cstart[lane];
-                uint32_t inc = v;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-                    if ((int)lane >= d) inc += t2;
-                }
-                cstart[lane] = inc - v;
-            }
-            __syncthreads();
-#pragma unroll
-            for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t r = threadIdx.x + qi * kP2GThreads;
-                if (cls[qi] < 32u) {
-                    const uint32_t e = cstart[cls[qi]] + hist[(qi * NWARP + warp) * 33 + cls[qi]] + below[qi];
-                    order[e + (e >> 5)] = r;
-                }
-            }
+            class_order<DIM, T, kG2PThreads>(key, pids, cnt, hist, cstart, order);
             cp_async_wait<0>();
             __syncthreads();
 #pragma unroll
             for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t pos = threadIdx.x + qi * kP2GThreads;
+                const uint32_t pos = threadIdx.x + qi * kG2PThreads;
                 if (pos < cnt) {
                     const uint32_t e = interleave_entry(pos, cnt);
                     const uint32_t r = order[e + (e >> 5)];
@@ -495,7 +309,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
                 }
             }
         } else {
-            const Prefetch<NF, kP2GThreads> pf{sbuf};
+            const Prefetch<NF, kG2PThreads> pf{sbuf};
             __syncthreads();
             auto issue = [&](int stage, uint32_t pid) {
 #pragma unroll
@@ -505,8 +319,8 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p(GridP g, PartsF p, PartsF q
             cp_async_commit();
 #pragma unroll
             for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t r = threadIdx.x + qi * kP2GThreads;
-                if (qi + 1 < NQ && r + kP2GThreads < cnt) issue((qi + 1) & 1, pids[qi + 1]);
+                const uint32_t r = threadIdx.x + qi * kG2PThreads;
+                if (qi + 1 < NQ && r + kG2PThreads < cnt) issue((qi + 1) & 1, pids[qi + 1]);
                 cp_async_commit();
                 cp_async_wait<1>();
                 if (r < cnt) {
@@ -530,12 +344,20 @@ __global__ void k_copy_rest(PartsF p, PartsF q, const uint32_t *__restrict__ per
         copy_particle<DIM>(p, q, perm[j], (uint32_t)j);
 }
 
+void launch_copy_rest(const GridP &g, const PartsF &in, const PartsF &out, const WsView &w, const DeviceInfo &dev,
+                      cudaStream_t st) {
+    if (g.dim == 3)
+        k_copy_rest<3><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+    else
+        k_copy_rest<2><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+}
+
 template <int DIM, int T, bool SORTED, bool EL, bool VC>
 void launch_g2p_t(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w, float dt,
                   const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
-    const int blocks = dev.sms * 4;
-    k_g2p<DIM, T, SORTED, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start,
+    const int blocks = dev.sms * (1024 / kG2PThreads);
+    k_g2p<DIM, T, SORTED, EL, VC><<<blocks, kG2PThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start,
                                                                    w.status, dt, c4);
     if constexpr (SORTED) k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
 }

@@ -47,6 +47,10 @@ mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const W
                       const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
                              float dt, const DeviceInfo &dev, cudaStream_t st);
+void launch_copy_rest(const GridP &g, const PartsF &in, const PartsF &out, const WsView &w, const DeviceInfo &dev,
+                      cudaStream_t st);
+mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, const WsView &w, void *acc_read,
+                        void *acc_write, float dt, const float dtg[3], const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
                           const DeviceInfo &dev, cudaStream_t st);
 

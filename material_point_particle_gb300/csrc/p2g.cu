@@ -18,149 +18,10 @@
 // particles, so no halo sum can overflow.
 #include "common.cuh"
 #include "internal.h"
+#include "scatter.cuh"
 #include "stress.cuh"
 
 namespace mpm {
-
-// Share encode: rint(a * b) for |a*b| < 2^22, exact product rounded once (RNE).
-__device__ __forceinline__ int32_t rint_mul(float a, float b) {
-    return __float_as_int(__fmaf_rn(a, b, kMagic)) - kMagicBits;
-}
-__device__ __forceinline__ int32_t rint_f(float a) { return __float_as_int(__fadd_rn(a, kMagic)) - kMagicBits; }
-
-
-
-// The particle's affine matrix as P2G scatters it: C, and for elastic
-// particles C minus the stress term (stress.cuh); counts the elastic
-// particles whose det F leaves them unstressed.
-template <int DIM, bool EL, bool VC, typename Rec>
-__device__ __forceinline__ void load_affine(const Rec &rec, const StressP &sp, float (&C)[DIM * DIM],
-                                            uint32_t &degenerate) {
-    using Fl = P2GFields<DIM, EL, VC>;
-#pragma unroll
-    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
-    if constexpr (EL) {
-        float F[DIM * DIM];
-#pragma unroll
-        for (int j = 0; j < DIM * DIM; ++j) F[j] = rec(Fl::BASE + j);
-        if (!fold_stress<DIM>(sp, F, rec(Fl::VOLF), rec(2 * DIM + DIM * DIM), C)) ++degenerate;
-    }
-}
-
-// One particle's fixed-point shares, added to the tile accumulator as they
-// are formed (the arithmetic the oracle states).  Returns false (and adds
-// nothing) when the particle is out of range.
-// rec(f) reads field f of the particle (P2GFields: x[dim], v[dim],
-// C[dim*dim], m, then F[dim*dim] for elastic particles, and vol).  With the
-// volume channel (VC) the rest volume in cells, Vt = (vol * inv_dx^dim) * S,
-// is split over the stencil as the mass is, into channel dim + 1.
-template <int DIM, int T, typename Hl, bool EL, bool VC, typename Rec>
-__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo,
-                                              const StressP &sp, uint32_t &degenerate) {
-    using Fl = P2GFields<DIM, EL, VC>;
-    using St = Stencil<DIM>;
-    float f[3] = {0.f, 0.f, 0.f};
-    int b[3] = {0, 0, 0};
-    float xs[DIM];
-#pragma unroll
-    for (int l = 0; l < DIM; ++l) xs[l] = rec(l);
-    if (!in_tile_x<DIM>(g, xs, o, b, f)) return false;
-    float v[DIM], C[DIM * DIM];
-#pragma unroll
-    for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
-    load_affine<DIM, EL, VC>(rec, sp, C, degenerate);
-    const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
-    [[maybe_unused]] float Vt = 0.f;
-    if constexpr (VC) Vt = __fmul_rn(__fmul_rn(rec(Fl::VOLF), g.vcell), g.S);
-    // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) (and wmax*|Vt|) at most 2^22 - 4096
-    const float h = __fmul_rn(1.5f, g.dx);
-    const float aM = fabsf(Mt);
-    bool ok = __fmul_rn(g.wmax, aM) <= kShareLimit;
-    if constexpr (VC) ok = ok && __fmul_rn(g.wmax, fabsf(Vt)) <= kShareLimit;
-#pragma unroll
-    for (int k = 0; k < DIM; ++k) {
-        float sc = __fadd_rn(fabsf(C[k * DIM + 0]), fabsf(C[k * DIM + 1]));
-        if (DIM == 3) sc = __fadd_rn(sc, fabsf(C[k * DIM + 2]));
-        const float R = __fmul_rn(aM, __fadd_rn(fabsf(v[k]), __fmul_rn(h, sc)));
-        ok = ok && (__fmul_rn(g.wmax, R) <= kShareLimit);
-    }
-    if (!ok) return false;
-    float w[3][3], dd[3][3];
-#pragma unroll
-    for (int l = 0; l < DIM; ++l) {
-        quad_weights(f[l], w[l]);
-#pragma unroll
-        for (int a = 0; a < 3; ++a) dd[l][a] = __fmul_rn(__fsub_rn((float)a, f[l]), g.dx);
-    }
-    const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
-                            : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
-    int32_t rest[St::NC + 1];
-    rest[0] = __float2int_rn(Mt);
-    rest[St::NC] = VC ? __float2int_rn(Vt) : 0;
-#pragma unroll
-    for (int k = 0; k < DIM; ++k) rest[1 + k] = __float2int_rn(__fmul_rn(Mt, v[k]));
-    // the x and y momentum channels go through packed fp32x2 arithmetic,
-    // which rounds each lane exactly as the scalar operation
-    const float2 magic2 = make_float2(kMagic, kMagic);
-    float2 Cxy[3] = {make_float2(C[0], C[DIM + 0]), make_float2(C[1], C[DIM + 1]), make_float2(0.f, 0.f)};
-    if constexpr (DIM == 3) Cxy[2] = make_float2(C[2], C[5]);
-    // the shared atomics address the halo from one base with constant offsets
-    const uint32_t base = halo + 4u * (uint32_t)hb;
-    static_for<3>([&](auto A0) {
-        constexpr int a0 = decltype(A0)::value;
-        const float Wx = __fmul_rn(w[0][a0], Mt);
-        // lane y carries the volume weight with the volume channel, else the mass weight again
-        const float2 Wx2 = make_float2(Wx, VC ? __fmul_rn(w[0][a0], Vt) : Wx);
-        const float2 h0xy = __ffma2_rn(Cxy[0], make_float2(dd[0][a0], dd[0][a0]), make_float2(v[0], v[1]));
-        [[maybe_unused]] float h0z = 0.f;
-        if constexpr (DIM == 3) h0z = __fmaf_rn(C[6], dd[0][a0], v[2]);
-        static_for<3>([&](auto A1) {
-            constexpr int a1 = decltype(A1)::value;
-            const float2 Wxy = __fmul2_rn(Wx2, make_float2(w[1][a1], w[1][a1]));
-            const float2 h1xy = __ffma2_rn(Cxy[1], make_float2(dd[1][a1], dd[1][a1]), h0xy);
-            [[maybe_unused]] float h1z = 0.f;
-            if constexpr (DIM == 3) h1z = __fmaf_rn(C[7], dd[1][a1], h0z);
-            static_for<(DIM == 3 ? 3 : 1)>([&](auto A2) {
-                constexpr int a2 = decltype(A2)::value;
-                constexpr int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
-                if constexpr (a != St::CENTRE) {
-                    constexpr int off = 4 * Hl::off(a);
-                    const float2 Wt = DIM == 3 ? __fmul2_rn(Wxy, make_float2(w[2][a2], w[2][a2])) : Wxy;
-                    const int32_t sm = rint_f(Wt.x);
-                    rest[0] -= sm;
-                    red_shared_add<off>(base, sm);
-                    if constexpr (VC) {
-                        const int32_t sv = rint_f(Wt.y);
-                        rest[St::NC] -= sv;
-                        red_shared_add<off + 4 * (DIM + 1) * Hl::SIZE>(base, sv);
-                    }
-                    const float2 Wm = VC ? make_float2(Wt.x, Wt.x) : Wt;
-                    const float2 velxy =
-                        DIM == 3 ? __ffma2_rn(Cxy[2], make_float2(dd[2][a2], dd[2][a2]), h1xy) : h1xy;
-                    const float2 bxy = __ffma2_rn(Wm, velxy, magic2);
-                    const int32_t sx = __float_as_int(bxy.x) - kMagicBits, sy = __float_as_int(bxy.y) - kMagicBits;
-                    rest[1] -= sx;
-                    rest[2] -= sy;
-                    red_shared_add<off + 4 * Hl::SIZE>(base, sx);
-                    red_shared_add<off + 8 * Hl::SIZE>(base, sy);
-                    if constexpr (DIM == 3) {
-                        const float velz = __fmaf_rn(C[8], dd[2][a2], h1z);
-                        const int32_t sz = rint_mul(Wt.x, velz);
-                        rest[3] -= sz;
-                        red_shared_add<off + 12 * Hl::SIZE>(base, sz);
-                    }
-                }
-            });
-        });
-    });
-    constexpr int offc = 4 * Hl::off(St::CENTRE);
-    red_shared_add<offc>(base, rest[0]);
-    red_shared_add<offc + 4 * Hl::SIZE>(base, rest[1]);
-    red_shared_add<offc + 8 * Hl::SIZE>(base, rest[2]);
-    if constexpr (DIM == 3) red_shared_add<offc + 12 * Hl::SIZE>(base, rest[3]);
-    if constexpr (VC) red_shared_add<offc + 4 * (DIM + 1) * Hl::SIZE>(base, rest[St::NC]);
-    return true;
-}
 
 template <int DIM, int T, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, const int o[3], float *sacc,

@@ -1,0 +1,202 @@
+// scatter.cuh -- one particle's fixed-point P2G shares into a shared-memory
+// accumulator (used by the P2G kernels and by the fused gather-scatter step).
+//
+// Shares follow "particle to grid transfer in checked integer arithmetic":
+// split rather than weight, so each particle's shares sum exactly to its
+// quantity and the grid is the same in every order.  The momentum is the
+// APIC/MLS affine momentum of the implementation guide, section 3.1; elastic
+// particles scatter the stress-folded affine matrix (stress.cuh).
+#pragma once
+
+#include "common.cuh"
+#include "stress.cuh"
+
+namespace mpm {
+
+// The stencil base cell b and fraction f of position x, true when the
+// particle is in the domain and b lies in the box [o, o + TB) per axis.
+template <int DIM, int TB>
+__device__ __forceinline__ bool in_box_x(const GridP &g, const float *x, const int o[3], int b[3], float f[3]) {
+    bool ok = true;
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) {
+        ok = ok && base_frac(x[l], g.inv_dx, g.n[l], b[l], f[l]);
+        ok = ok && b[l] >= o[l] && b[l] < o[l] + TB;
+    }
+    return ok;
+}
+
+// Share encode: rint(a * b) for |a*b| < 2^22, exact product rounded once (RNE).
+__device__ __forceinline__ int32_t rint_mul(float a, float b) {
+    return __float_as_int(__fmaf_rn(a, b, kMagic)) - kMagicBits;
+}
+__device__ __forceinline__ int32_t rint_f(float a) { return __float_as_int(__fadd_rn(a, kMagic)) - kMagicBits; }
+
+// Where a share goes: add<C, A>(v) adds share v of channel C to stencil node
+// A (A = a0*9 + a1*3 + a2 in 3D, a0*3 + a1 in 2D; a0 along x).
+//
+// SharedAdd: a shared-memory accumulator of layout Hl; `base` is the shared
+// address of the stencil's first node (constant offsets from one base).
+template <typename Hl>
+struct SharedAdd {
+    uint32_t base;
+    template <int C, int A>
+    __device__ __forceinline__ void add(int32_t v) const {
+        red_shared_add<4 * (Hl::off(A) + C * Hl::SIZE)>(base, v);
+    }
+};
+
+// GlobalAdd: the int64 grid itself, node0 = the stencil's first node.
+template <int DIM>
+struct GlobalAdd {
+    long long *acc;
+    int64_t nodes, n0, n01, node0;
+    template <int C, int A>
+    __device__ __forceinline__ void add(int32_t v) const {
+        constexpr int a0 = DIM == 3 ? A / 9 : A / 3;
+        constexpr int a1 = DIM == 3 ? (A / 3) % 3 : A % 3;
+        constexpr int a2 = DIM == 3 ? A % 3 : 0;
+        atomicAdd(reinterpret_cast<unsigned long long *>(acc + C * nodes + node0 + a0 + a1 * n0 + a2 * n01),
+                  (unsigned long long)(long long)v);
+    }
+};
+
+// The particle's affine matrix as P2G scatters it: C, and for elastic
+// particles C minus the stress term (stress.cuh); counts the elastic
+// particles whose det F leaves them unstressed.
+template <int DIM, bool EL, bool VC, typename Rec>
+__device__ __forceinline__ void load_affine(const Rec &rec, const StressP &sp, float (&C)[DIM * DIM],
+                                            uint32_t &degenerate) {
+    using Fl = P2GFields<DIM, EL, VC>;
+#pragma unroll
+    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
+    if constexpr (EL) {
+        float F[DIM * DIM];
+#pragma unroll
+        for (int j = 0; j < DIM * DIM; ++j) F[j] = rec(Fl::BASE + j);
+        if (!fold_stress<DIM>(sp, F, rec(Fl::VOLF), rec(2 * DIM + DIM * DIM), C)) ++degenerate;
+    }
+}
+
+// One particle's fixed-point shares, handed to `ad` as they are formed (the
+// arithmetic the oracle states).  Returns false (and adds nothing) when the
+// particle is out of range.  f: the fractions of its stencil base cell.
+// rec(f) reads field f of the particle (P2GFields: x[dim], v[dim],
+// C[dim*dim], m, then F[dim*dim] for elastic particles, and vol).  With the
+// volume channel (VC) the rest volume in cells, Vt = (vol * inv_dx^dim) * S,
+// is split over the stencil as the mass is, into channel dim + 1.
+template <int DIM, bool EL, bool VC, typename Rec, typename Add>
+__device__ __forceinline__ bool scatter_shares(const GridP &g, const Rec &rec, const float (&f)[3], const Add &ad,
+                                               const StressP &sp, uint32_t &degenerate) {
+    using Fl = P2GFields<DIM, EL, VC>;
+    using St = Stencil<DIM>;
+    float v[DIM], C[DIM * DIM];
+#pragma unroll
+    for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
+    load_affine<DIM, EL, VC>(rec, sp, C, degenerate);
+    const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
+    [[maybe_unused]] float Vt = 0.f;
+    if constexpr (VC) Vt = __fmul_rn(__fmul_rn(rec(Fl::VOLF), g.vcell), g.S);
+    // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) (and wmax*|Vt|) at most 2^22 - 4096
+    const float h = __fmul_rn(1.5f, g.dx);
+    const float aM = fabsf(Mt);
+    bool ok = __fmul_rn(g.wmax, aM) <= kShareLimit;
+    if constexpr (VC) ok = ok && __fmul_rn(g.wmax, fabsf(Vt)) <= kShareLimit;
+#pragma unroll
+    for (int k = 0; k < DIM; ++k) {
+        float sc = __fadd_rn(fabsf(C[k * DIM + 0]), fabsf(C[k * DIM + 1]));
+        if (DIM == 3) sc = __fadd_rn(sc, fabsf(C[k * DIM + 2]));
+        const float R = __fmul_rn(aM, __fadd_rn(fabsf(v[k]), __fmul_rn(h, sc)));
+        ok = ok && (__fmul_rn(g.wmax, R) <= kShareLimit);
+    }
+    if (!ok) return false;
+    float w[3][3], dd[3][3];
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) {
+        quad_weights(f[l], w[l]);
+#pragma unroll
+        for (int a = 0; a < 3; ++a) dd[l][a] = __fmul_rn(__fsub_rn((float)a, f[l]), g.dx);
+    }
+    int32_t rest[St::NC + 1];
+    rest[0] = __float2int_rn(Mt);
+    rest[St::NC] = VC ? __float2int_rn(Vt) : 0;
+#pragma unroll
+    for (int k = 0; k < DIM; ++k) rest[1 + k] = __float2int_rn(__fmul_rn(Mt, v[k]));
+    // the x and y momentum channels go through packed fp32x2 arithmetic,
+    // which rounds each lane exactly as the scalar operation
+    const float2 magic2 = make_float2(kMagic, kMagic);
+    float2 Cxy[3] = {make_float2(C[0], C[DIM + 0]), make_float2(C[1], C[DIM + 1]), make_float2(0.f, 0.f)};
+    if constexpr (DIM == 3) Cxy[2] = make_float2(C[2], C[5]);
+    static_for<3>([&](auto A0) {
+        constexpr int a0 = decltype(A0)::value;
+        const float Wx = __fmul_rn(w[0][a0], Mt);
+        // lane y carries the volume weight with the volume channel, else the mass weight again
+        const float2 Wx2 = make_float2(Wx, VC ? __fmul_rn(w[0][a0], Vt) : Wx);
+        const float2 h0xy = __ffma2_rn(Cxy[0], make_float2(dd[0][a0], dd[0][a0]), make_float2(v[0], v[1]));
+        [[maybe_unused]] float h0z = 0.f;
+        if constexpr (DIM == 3) h0z = __fmaf_rn(C[6], dd[0][a0], v[2]);
+        static_for<3>([&](auto A1) {
+            constexpr int a1 = decltype(A1)::value;
+            const float2 Wxy = __fmul2_rn(Wx2, make_float2(w[1][a1], w[1][a1]));
+            const float2 h1xy = __ffma2_rn(Cxy[1], make_float2(dd[1][a1], dd[1][a1]), h0xy);
+            [[maybe_unused]] float h1z = 0.f;
+            if constexpr (DIM == 3) h1z = __fmaf_rn(C[7], dd[1][a1], h0z);
+            static_for<(DIM == 3 ? 3 : 1)>([&](auto A2) {
+                constexpr int a2 = decltype(A2)::value;
+                constexpr int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
+                if constexpr (a != St::CENTRE) {
+                    const float2 Wt = DIM == 3 ? __fmul2_rn(Wxy, make_float2(w[2][a2], w[2][a2])) : Wxy;
+                    const int32_t sm = rint_f(Wt.x);
+                    rest[0] -= sm;
+                    ad.template add<0, a>(sm);
+                    if constexpr (VC) {
+                        const int32_t sv = rint_f(Wt.y);
+                        rest[St::NC] -= sv;
+                        ad.template add<DIM + 1, a>(sv);
+                    }
+                    const float2 Wm = VC ? make_float2(Wt.x, Wt.x) : Wt;
+                    const float2 velxy =
+                        DIM == 3 ? __ffma2_rn(Cxy[2], make_float2(dd[2][a2], dd[2][a2]), h1xy) : h1xy;
+                    const float2 bxy = __ffma2_rn(Wm, velxy, magic2);
+                    const int32_t sx = __float_as_int(bxy.x) - kMagicBits, sy = __float_as_int(bxy.y) - kMagicBits;
+                    rest[1] -= sx;
+                    rest[2] -= sy;
+                    ad.template add<1, a>(sx);
+                    ad.template add<2, a>(sy);
+                    if constexpr (DIM == 3) {
+                        const float velz = __fmaf_rn(C[8], dd[2][a2], h1z);
+                        const int32_t sz = rint_mul(Wt.x, velz);
+                        rest[3] -= sz;
+                        ad.template add<3, a>(sz);
+                    }
+                }
+            });
+        });
+    });
+    ad.template add<0, St::CENTRE>(rest[0]);
+    ad.template add<1, St::CENTRE>(rest[1]);
+    ad.template add<2, St::CENTRE>(rest[2]);
+    if constexpr (DIM == 3) ad.template add<3, St::CENTRE>(rest[3]);
+    if constexpr (VC) ad.template add<DIM + 1, St::CENTRE>(rest[St::NC]);
+    return true;
+}
+
+// scatter_shares into a shared-memory tile accumulator `halo` (layout Hl)
+// covering the stencils of base cells in the box [o, o + TB) per axis.
+// False when the particle is outside the domain or the box, or out of range.
+template <int DIM, int TB, typename Hl, bool EL, bool VC, typename Rec>
+__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo,
+                                              const StressP &sp, uint32_t &degenerate) {
+    float f[3] = {0.f, 0.f, 0.f};
+    int b[3] = {0, 0, 0};
+    float xs[DIM];
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) xs[l] = rec(l);
+    if (!in_box_x<DIM, TB>(g, xs, o, b, f)) return false;
+    const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
+                            : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
+    const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb};
+    return scatter_shares<DIM, EL, VC>(g, rec, f, ad, sp, degenerate);
+}
+
+}  // namespace mpm

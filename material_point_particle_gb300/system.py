@@ -159,6 +159,21 @@ class MPMSystem:
                           stream)
         self.swap()
 
+    # -- the fused step: the accumulators of the current positions in, the next ones out --
+    def enable_fused(self):
+        """Second accumulator grid for mpm_step_fused; fills the first with the
+        P2G of the current positions (bin + p2g).  Needs enable_sorted()."""
+        self.acc2 = torch.zeros_like(self.acc)
+        self.bin()
+        self.p2g()
+        return self
+
+    def step_fused(self, stream=None):
+        L.mpm_step_fused(self.desc, self.parts, self.parts2, self.bins, self.acc, self.acc2, self.dt, self.dtg,
+                         stream)
+        self.swap()
+        self.acc, self.acc2 = self.acc2, self.acc
+
     def status(self) -> np.ndarray:
         L.mpm_read_status(self.bins, self.status_host)
         torch.cuda.synchronize(self.device)
