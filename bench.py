@@ -255,11 +255,12 @@ def run_ours(args, rank, world, local):
                 "frac": round((n * 136.0 + touched * 64.0) / (tr_ms * 1e-3) / 1e9 / peak, 4),
                 "bin_ms": round(float(mean_ms[0]), 4)}
 
-    elastic = volume = fused = None
+    elastic = volume = fused = loop = None
     if args.variant_steps > 0:
         elastic = measure_variant(args, cloud, dev, stream, world, peak, elastic=True, volume=False)
         volume = measure_variant(args, cloud, dev, stream, world, peak, elastic=False, volume=True)
         fused = measure_fused(args, cloud, dev, stream, world, peak, touched, float(mean_ms[0]))
+        loop = measure_loop(args, cloud, dev, stream, world, peak)
 
     # end to end through the host entry point (pinned host SoA, copies inside the timed region)
     e2e = None
@@ -309,6 +310,7 @@ def run_ours(args, rank, world, local):
         "mls_stress": elastic,
         "volume_channel": volume,
         "fused_step": fused,
+        "transfer_loop": loop,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
@@ -432,6 +434,61 @@ def measure_fused(args, cloud, dev, stream, world, peak, touched, bin_ms):
                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(achieved / peak, 4), "traffic": None}}
     del fs
+    torch.cuda.empty_cache()
+    return out
+
+
+LOOP_ITERATIONS = 5
+
+
+def measure_loop(args, cloud, dev, stream, world, peak):
+    """The position-based solver's transfer loop on the same workload: LOOP_ITERATIONS
+    rounds of P2G -> grid update (no gravity) -> G2P (no advection) at fixed positions,
+    once as mpm_iterate (one fused kernel per iteration) and once as the separate
+    calls; binning and the first P2G are outside both timings."""
+    import torch
+    from material_point_particle_gb300 import _lib as L
+    from material_point_particle_gb300.system import MPMSystem
+
+    grid = dict(cloud["grid"], g=[0.0, 0.0, 0.0], dt=0.0)
+    n = cloud["x"].shape[1]
+    ls = MPMSystem(grid, n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    acc_b = torch.zeros_like(ls.acc)
+    reps = max(1, args.variant_steps // LOOP_ITERATIONS)
+
+    def fused():
+        ls.bin(stream)
+        ls.p2g(stream)
+        a.record(stream)
+        L.mpm_iterate(ls.desc, ls.parts, ls.bins, ls.acc, acc_b, LOOP_ITERATIONS, stream)
+        b.record(stream)
+
+    def separate():
+        ls.bin(stream)
+        ls.p2g(stream)
+        a.record(stream)
+        for it in range(LOOP_ITERATIONS):
+            ls.grid_update(stream)
+            ls.g2p(stream)
+            if it + 1 < LOOP_ITERATIONS:
+                ls.p2g(stream)
+        b.record(stream)
+
+    out = {"iterations": LOOP_ITERATIONS, "unit": "ms per iteration"}
+    for name, fn in (("fused", fused), ("separate", separate)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        total = 0.0
+        for _ in range(reps):
+            fn()
+            torch.cuda.synchronize()
+            total += a.elapsed_time(b)
+        out[name] = round(aggregate_max(total / reps / LOOP_ITERATIONS, world, dev), 4)
+    st = ls.status()
+    assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
+    del ls, acc_b
     torch.cuda.empty_cache()
     return out
 

@@ -14,6 +14,7 @@
  *                    accumulators it reads
  *   mpm_g2p          gather of velocity and affine matrix, advection
  *   mpm_step_fused   grid update, G2P and the next P2G in one kernel
+ *   mpm_iterate      the position-based transfer loop, one kernel per iteration
  *
  * Conventions shared by every call:
  *  - All pointers inside the structs are DEVICE pointers unless a call says
@@ -334,6 +335,26 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
  */
 mpm_status mpm_step_fused(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
                           void *acc_read, void *acc_write, float dt, const float dtg[3], void *stream);
+
+/*
+ * mpm_iterate -- the transfer loop at fixed positions of the implementation
+ * guide's position-based solver (section 3.3.2: P2G -> grid update -> G2P,
+ * iterationCount times per substep, the particles in place; v and C carry the
+ * displacement d and its gradient D, with the same transfer arithmetic), one
+ * fused kernel per iteration (section 2.1): the grid update is applied while
+ * the tile's accumulators are loaded, without gravity (the loop adds none),
+ * each particle's new v and C are gathered and written in place, and -- but
+ * for the last iteration -- scattered at the same position into the other
+ * grid.  `bins` must hold mpm_bin of the current positions and `acc_a` the
+ * mpm_p2g of the current state; `acc_b` must be zero.  Both grids are zero
+ * afterwards; x, m and every particle outside the domain are unchanged.  The
+ * bits equal `iterations` rounds of mpm_grid_update (dtg = 0) + mpm_g2p
+ * (dt = 0) + mpm_p2g.  The material projections the guide runs between the
+ * transfers are not part of this call.  MPM_ACC_I64 only, without the elastic
+ * state or the volume channel.  iterations >= 1.
+ */
+mpm_status mpm_iterate(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *bins, void *acc_a, void *acc_b,
+                       int iterations, void *stream);
 
 /* Reorders a particle SoA by bins->perm: out[j] = in[perm[j]] for every
  * component (and id if both are non-NULL), all n entries.  `in` and `out`

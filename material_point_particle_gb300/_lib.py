@@ -85,12 +85,13 @@ def library() -> ct.CDLL:
                                         ct.c_float, P(ct.c_float), VP]
             L.mpm_step_fused.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
                                          P(ct.c_float), VP]
+            L.mpm_iterate.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, VP, ct.c_int, VP]
             L.mpm_permute.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP]
             L.mpm_read_status.argtypes = [P(Bins), VP, VP]
             L.mpm_bin_static.argtypes = [P(GridDesc), P(Particles), ct.c_int, P(Bins), VP]
             for name in ("mpm_bins_init", "mpm_bin", "mpm_p2g", "mpm_grid_update", "mpm_g2p", "mpm_step",
                          "mpm_g2p_sorted", "mpm_step_sorted", "mpm_step_host", "mpm_permute", "mpm_read_status",
-                         "mpm_bin_static", "mpm_step_fused"):
+                         "mpm_bin_static", "mpm_step_fused", "mpm_iterate"):
                 getattr(L, name).restype = ct.c_int
             _L = L
     return _L
@@ -235,6 +236,12 @@ def mpm_step_fused(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, a
     _check(library().mpm_step_fused(ct.byref(desc), ct.byref(src), ct.byref(dst), ct.byref(bins),
                                     ct.c_void_p(acc_read.data_ptr()), ct.c_void_p(acc_write.data_ptr()),
                                     ct.c_float(dt), _f3(dtg), _stream(stream)), "mpm_step_fused")
+
+
+def mpm_iterate(desc: GridDesc, parts: Particles, bins: Bins, acc_a: torch.Tensor, acc_b: torch.Tensor,
+                iterations: int, stream=None):
+    _check(library().mpm_iterate(ct.byref(desc), ct.byref(parts), ct.byref(bins), ct.c_void_p(acc_a.data_ptr()),
+                                 ct.c_void_p(acc_b.data_ptr()), int(iterations), _stream(stream)), "mpm_iterate")
 
 
 def mpm_step_sorted(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, grid_acc: torch.Tensor,

@@ -409,6 +409,21 @@ mpm_status mpm_step_fused(const mpm_grid_desc *desc, mpm_particles *in, mpm_part
                         static_cast<cudaStream_t>(stream));
 }
 
+mpm_status mpm_iterate(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *bins, void *acc_a, void *acc_b,
+                       int iterations, void *stream) {
+    GridP g;
+    MPM_TRY(make_grid(desc, g));
+    if (g.acc_mode != MPM_ACC_I64 || g.vc || !acc_a || !acc_b || acc_a == acc_b || iterations < 1)
+        return MPM_E_ARG;
+    PartsF p;
+    MPM_TRY(parts_f(g, parts, true, p));
+    if (p.F[0]) return MPM_E_ARG;
+    MPM_TRY(check_bins(g, bins, p.n));
+    DeviceInfo dev;
+    MPM_TRY(device_info(dev));
+    return launch_iterate(g, p, view_of(g, *bins), acc_a, acc_b, iterations, dev, static_cast<cudaStream_t>(stream));
+}
+
 mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev_in,
                          mpm_particles *dev_out, mpm_bins *bins, void *grid_acc, float *grid_vel, float dt,
                          const float dtg[3], void *stream) {

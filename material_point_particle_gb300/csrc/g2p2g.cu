@@ -310,6 +310,13 @@ __global__ void k_clear_blocks(GridP g, long long *__restrict__ acc, const uint3
     }
 }
 
+void launch_clear_blocks(const GridP &g, long long *acc, const WsView &w, const DeviceInfo &dev, cudaStream_t st) {
+    if (g.dim == 3)
+        k_clear_blocks<3, 4><<<dev.sms * 8, 256, 0, st>>>(g, acc, w.count);
+    else
+        k_clear_blocks<2, 8><<<dev.sms * 8, 256, 0, st>>>(g, acc, w.count);
+}
+
 mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, const WsView &w, void *acc_read,
                         void *acc_write, float dt, const float dtg[3], const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;
@@ -323,12 +330,12 @@ mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, con
         k_g2p2g<3, 4><<<blocks, kG2PThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm, w.key,
                                                       w.slices, w.start, w.status, dt, c4);
         launch_copy_rest(g, in, out, w, dev, st);
-        k_clear_blocks<3, 4><<<dev.sms * 8, 256, 0, st>>>(g, Rc, w.count);
+        launch_clear_blocks(g, Rc, w, dev, st);
     } else if (g.dim == 2 && g.T == 8) {
         k_g2p2g<2, 8><<<blocks, kG2PThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm, w.key,
                                                       w.slices, w.start, w.status, dt, c4);
         launch_copy_rest(g, in, out, w, dev, st);
-        k_clear_blocks<2, 8><<<dev.sms * 8, 256, 0, st>>>(g, Rc, w.count);
+        launch_clear_blocks(g, Rc, w, dev, st);
     } else {
         return MPM_E_ARG;
     }
