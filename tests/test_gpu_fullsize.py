@@ -12,6 +12,10 @@
   the whole velocity grid where there is mass against the oracle's grid update
   of the GPU's accumulators; and the sorted G2P on sampled particles (found
   through their ids) against the oracle's G2P.
+- The blobs as the benchmark's elastic row times them (the Neo-Hookean state),
+  checked the same way with the stress fold and the F update.
+- The blobs stepped by the fused kernel: the new state on sampled particles,
+  the next accumulators in total and on sampled tiles, the read grid cleared.
 """
 import numpy as np
 import pytest
@@ -83,10 +87,14 @@ def _quantities(grid, x, v, m):
 
 
 def _check_step(sys, grid, n, n_tiles_sampled=6):
-    """One sorted step of `sys`, checked piece by piece against the oracle."""
+    """One sorted step of `sys`, checked piece by piece against the oracle
+    (with the stress fold and the F update when the particles are elastic)."""
     x0, v0, C0 = sys.state()
     m0 = sys.m.cpu().numpy()
     ids0 = sys.id.cpu().numpy().astype(np.int64)
+    elastic = sys.F is not None
+    if elastic:
+        F0, vol0 = sys.elastic_state()
 
     # binning: the whole permutation
     sys.bin()
@@ -115,7 +123,10 @@ def _check_step(sys, grid, n, n_tiles_sampled=6):
         # nodes of tile t's own block get shares only from base cells in [o - 2, o + T)
         near = np.all((base >= (o - 2)[:, None]) & (base < (o + T)[:, None]), axis=0)
         sub = np.nonzero(near)[0]
-        oacc, _, counts = O.p2g_fixed(grid, x0[:, sub], v0[:, sub], C0[:, sub], m0[sub])
+        Cs = C0[:, sub]
+        if elastic:
+            Cs, _ = O.stress_affine(grid, sys.material, x0[:, sub], C0[:, sub], F0[:, sub], vol0[sub], m0[sub])
+        oacc, _, counts = O.p2g_fixed(grid, x0[:, sub], v0[:, sub], Cs, m0[sub])
         assert counts.sum() == 0
         gx, gy, gz = np.meshgrid(*(np.arange(oi, oi + T) for oi in o), indexing="ij")
         nodes = ((gz * nn + gy) * nn + gx).ravel()
@@ -141,9 +152,15 @@ def _check_step(sys, grid, n, n_tiles_sampled=6):
     where = np.empty(n, dtype=np.int64)
     where[ids1] = np.arange(n)
     samp = inside[(W.Stream(32, 32).bits(20000) % np.uint64(inside.size)).astype(np.int64)]
-    ox, ov, oC, moved = O.g2p(grid, vel, x0[:, samp], v0[:, samp], C0[:, samp])
-    assert moved == samp.size
     at = where[ids0[samp]]
+    if elastic:
+        ox, ov, oC, oF, moved = O.g2p_elastic(grid, vel, x0[:, samp], v0[:, samp], C0[:, samp], F0[:, samp])
+        F1, vol1 = sys.elastic_state()
+        assert np.array_equal(F1[:, at].view(np.uint32), oF.view(np.uint32))
+        assert np.array_equal(vol1[at], vol0[samp])
+    else:
+        ox, ov, oC, moved = O.g2p(grid, vel, x0[:, samp], v0[:, samp], C0[:, samp])
+    assert moved == samp.size
     for a, b in ((x1[:, at], ox), (v1[:, at], ov), (C1[:, at], oC)):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
@@ -169,3 +186,73 @@ def test_sphere_full_size_step():
     sys = _system(cloud).enable_sorted()
     del cloud
     _check_step(sys, grid, n, n_tiles_sampled=3)
+
+
+def test_blobs_full_size_elastic():
+    """The bench's elastic row: the blobs with F = I + N(0, 0.05), V0 = dx^3 and
+    mu = lambda = 1e9, one sorted step checked after three steady-state steps."""
+    cloud = W.blobs3d()
+    grid = cloud["grid"]
+    n = cloud["x"].shape[1]
+    el = W.with_elastic(cloud, seed=77, fsig=0.05, ppc=1.0, mu=1.0e9, lam=1.0e9)
+    sys = _system(cloud).load_elastic(el["F"], el["vol"], el["material"]).enable_sorted()
+    del cloud, el
+    for _ in range(3):
+        sys.step_sorted()
+    _check_step(sys, grid, n, n_tiles_sampled=4)
+    assert sys.status()[L.ST_N_DEGENERATE] == 0
+
+
+def test_blobs_full_size_fused_step():
+    """mpm_step_fused on the blobs in their steady-state order: the new state on
+    sampled particles, the next accumulators on sampled tiles and in total, and
+    the grid it read cleared."""
+    cloud = W.blobs3d()
+    grid = cloud["grid"]
+    n = cloud["x"].shape[1]
+    sys = _system(cloud).enable_sorted()
+    del cloud
+    for _ in range(3):
+        sys.step_sorted()
+    sys.enable_fused()
+    torch.cuda.synchronize()
+    x0, v0, C0 = sys.state()
+    m0 = sys.m.cpu().numpy()
+    ids0 = sys.id.cpu().numpy().astype(np.int64)
+    R = sys.acc.cpu().numpy()
+    vel = O.grid_update_fixed(grid, R)
+    sys.step_fused()
+    torch.cuda.synchronize()
+    st = sys.status()
+    assert st[L.ST_FLAGS] == 0 and st[L.ST_N_ESCAPED] == 0
+    assert not sys.acc2.any().item(), "the grid read must be cleared"
+    x1, v1, C1 = sys.state()
+    ids1 = sys.id.cpu().numpy().astype(np.int64)
+    where = np.empty(n, dtype=np.int64)
+    where[ids1] = np.arange(n)
+    inside = np.nonzero(O.bin_particles(grid, x0)[0] != 0xFFFFFFFF)[0]
+    samp = inside[(W.Stream(33, 33).bits(20000) % np.uint64(inside.size)).astype(np.int64)]
+    ox, ov, oC, moved = O.g2p(grid, vel, x0[:, samp], v0[:, samp], C0[:, samp])
+    at = where[ids0[samp]]
+    for a, b in ((x1[:, at], ox), (v1[:, at], ov), (C1[:, at], oC)):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    # the next accumulators: exact totals and sampled tiles of the new positions
+    Wacc = sys.acc.cpu().numpy()
+    m1 = sys.m.cpu().numpy()
+    key1, _, cnt1, _ = O.bin_particles(grid, x1)
+    inside1 = np.nonzero(key1 != 0xFFFFFFFF)[0]
+    Q = _quantities(grid, x1[:, inside1], v1[:, inside1], m1[inside1])
+    for c in range(4):
+        assert int(Wacc[c].sum()) == int(Q[c].sum()), f"channel {c} not conserved"
+    T, nn = grid["tile"], grid["n"][0]
+    nt = (nn - 2 + T - 1) // T
+    base = np.floor(x1.astype(np.float32) * np.float32(grid["inv_dx"]) - np.float32(0.5)).astype(np.int64)
+    tiles = np.nonzero(cnt1)[0]
+    for t in tiles[(W.Stream(34, 34).bits(4) % np.uint64(tiles.size)).astype(np.int64)]:
+        o = np.array([t % nt, (t // nt) % nt, t // (nt * nt)]) * T
+        near = np.all((base >= (o - 2)[:, None]) & (base < (o + T)[:, None]), axis=0)
+        sub = np.nonzero(near)[0]
+        oacc, _, counts = O.p2g_fixed(grid, x1[:, sub], v1[:, sub], C1[:, sub], m1[sub])
+        gx, gy, gz = np.meshgrid(*(np.arange(oi, oi + T) for oi in o), indexing="ij")
+        nodes = ((gz * nn + gy) * nn + gx).ravel()
+        assert np.array_equal(Wacc[:, nodes], oacc[:, nodes]), f"tile {t}"
