@@ -402,33 +402,38 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
 
 def measure_fused(args, cloud, dev, stream, world, peak, touched, bin_ms):
     """The same workload stepped by mpm_step_fused (bin, then one kernel for the grid
-    update, G2P and the next P2G, then the clear of the grid it read), steady state."""
+    update, G2P and the next P2G, then the clear of the grid it read), after sorted
+    steps have written the bank-class interleave; `steps` fused steps in a row."""
     import torch
     from material_point_particle_gb300 import _lib as L
     from material_point_particle_gb300.system import MPMSystem
 
     steps = args.variant_steps
     n = cloud["x"].shape[1]
-    fs = MPMSystem(cloud["grid"], n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted() \
-        .enable_fused()
+    fs = MPMSystem(cloud["grid"], n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted()
+    # the sorted steps write the bank-class interleave, which the fused steps' bin order keeps
     for _ in range(max(3, args.warmup)):
-        fs.step_fused(stream)
+        fs.step_sorted(stream)
+    fs.enable_fused()
     torch.cuda.synchronize()
     barrier(world, dev)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for k in range(steps):
         fs.step_fused(stream)
-    t1.record(stream)
+        ev[k + 1].record(stream)
     torch.cuda.synchronize()
     st = fs.status()
     assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
-    ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
+    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    ms = aggregate_max(ev[0].elapsed_time(ev[steps]) / steps, world, dev)
     # algorithmic bytes of the fused kernel: read x, m, id (20 B) and write x, v, C, m, id (68 B) per
     # particle; read the accumulators R and write W (32 B each per touched node)
     kern_ms = ms - bin_ms
     achieved = (n * 88.0 + touched * 64.0) / (kern_ms * 1e-3) / 1e9
+    q = max(1, steps // 10)
     out = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+           "first_tenth_ms": round(float(np.mean(per[:q])), 4), "last_tenth_ms": round(float(np.mean(per[-q:])), 4),
            "escaped": int(st[L.ST_N_ESCAPED]), "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
            "roofline": {"bound": "hbm", "kernel": "g2p2g + clear (step minus the main region's bin time)",
                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -127,8 +127,8 @@ enum {
     MPM_ST_WORK_G2P = 12,    /* internal: work counter of the G2P launch */
     MPM_ST_MAX_SPEED = 13,   /* fp32 bits of max over the particles the last G2P moved of
                                 |v'| + 1.5 dx |C'|_F; the advective step bound is dt <= dx / it */
-    MPM_ST_N_ESCAPED = 14,   /* mpm_step_fused: particles that moved further than one cell, scattered
-                                straight into the global grid */
+    MPM_ST_N_ESCAPED = 14,   /* mpm_step_fused: particles whose base cell left their tile in the step,
+                                scattered straight into the global grid */
     MPM_STATUS_WORDS = 16
 };
 
@@ -322,13 +322,18 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
  * accumulators of mpm_p2g at the positions of `in` (the first step: mpm_bin
  * and mpm_p2g on `in`; later steps: the previous call's `acc_write`);
  * `acc_write` must be zero.  The call bins `in`, gathers as mpm_grid_update +
- * mpm_g2p_sorted would into `out` (the same order and bits), scatters the new
- * state into `acc_write` as mpm_p2g on `out` would (the same integers), and
- * clears `acc_read`; the caller then swaps in/out and the two grids.
- * Particles that moved further than one cell in the step are scattered
- * straight into the global grid and counted in MPM_ST_N_ESCAPED; those
- * leaving the domain are not scattered; out-of-range ones are counted in
- * MPM_ST_N_OUT_OF_RANGE as by mpm_p2g.  MPM_ACC_I64 only, without the
+ * mpm_g2p would (the same bits) and writes the new state to `out` in bin
+ * order, out[j] = new state of in[perm[j]]: the order inside a tile is the
+ * input's, so the bank-class interleave mpm_step_sorted writes carries over
+ * (particles drifting between cells wear it down slowly; an occasional
+ * sorted step restores it).  It scatters the new state into `acc_write` as
+ * mpm_p2g on `out` would (the same integers), and clears `acc_read`; the
+ * caller then swaps in/out and the two grids.  One
+ * warp per work item: a particle's new state is scattered into the warp's
+ * tile accumulator while its base cell stays in the tile; a particle whose
+ * base cell left the tile is scattered straight into the global grid and
+ * counted in MPM_ST_N_ESCAPED; those leaving the domain are not scattered;
+ * out-of-range ones are counted in MPM_ST_N_OUT_OF_RANGE as by mpm_p2g.  MPM_ACC_I64 only, without the
  * elastic state or the volume channel (MPM_E_ARG otherwise): the int32 mode's
  * bound is checked by the binning of the positions it will scatter, which
  * this scatter runs ahead of.  No velocity grid is written.

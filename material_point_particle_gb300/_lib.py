@@ -21,7 +21,7 @@ MPM_ACC_I32, MPM_ACC_I64, MPM_ACC_F32, MPM_ACC_EXACT_INT = range(4)
 ST_BIN_WORDS = 10   # status words 0..9 are written by mpm_bin
 ST_N_DEGENERATE = 10  # elastic particles the last P2G scattered without stress (det F not positive normal)
 ST_MAX_SPEED = 13   # fp32 bits of max |v'| + 1.5 dx |C'|_F over the particles the last G2P moved
-ST_N_ESCAPED = 14   # mpm_step_fused: particles that moved more than a cell (scattered into the global grid)
+ST_N_ESCAPED = 14   # mpm_step_fused: particles whose base cell left their tile (scattered into the global grid)
 MPM_STATUS_WORDS = 16
 MPM_STATIC_WORKSPACE_BYTES = 16 << 20
 

@@ -170,10 +170,12 @@ __global__ void __launch_bounds__(kG2PThreads, 2)
                 const float m = sbuf[DIM * kSliceParticles + r];
                 if (!in_box_x<DIM, T>(g, x, o, b, f)) {
                     // not binned into this tile from these positions: carried as it is
+#pragma unroll
                     for (int l = 0; l < DIM; ++l) {
                         q.x[l][dst] = p.x[l][pid];
                         q.v[l][dst] = p.v[l][pid];
                     }
+#pragma unroll
                     for (int j = 0; j < DIM * DIM; ++j) q.C[j][dst] = p.C[j][pid];
                     const_cast<float *>(q.m)[dst] = m;
                     if (q.id) q.id[dst] = __float_as_uint(sbuf[(DIM + 1) * kSliceParticles + r]);
@@ -282,6 +284,229 @@ __global__ void __launch_bounds__(kG2PThreads, 2)
     }
 }
 
+// A particle's shares straight into the global grid (the rare particle whose
+// new base cell left its tile); out of line, so that its registers do not
+// weigh on the kernel's common path.  False when out of range.
+template <int DIM>
+__device__ __noinline__ bool scatter_global(const GridP &g, const float (&rec_v)[P2GFields<DIM>::NF],
+                                            const int (&b)[3], const float (&f)[3], long long *acc) {
+    const GlobalAdd<DIM> ad{acc, g.nodes, g.n[0], (int64_t)g.n[0] * g.n[1],
+                            node_index(g, b[0], b[1], DIM == 3 ? b[2] : 0)};
+    const StressP sp{0.f, 0.f, 0.f, 0.f};
+    uint32_t unused = 0;
+    auto rec = [&](int fi) { return rec_v[fi]; };
+    return scatter_shares<DIM, false, false>(g, rec, f, ad, sp, unused);
+}
+
+// The fused step with one warp per work item (the P2G kernel's shape): each
+// warp owns a velocity halo of its tile, an accumulator halo of the same
+// tile and a double buffer of its lanes' x, m and id, so no block barrier
+// couples the warps.  32 particles a round, a lane gathers its particle at x,
+// writes the new state at the particle's place in bin order (coalesced; the
+// order inside a tile is the input's, so a bank-class interleave written by
+// the sorted G2P carries over) and scatters the new state from its
+// registers: into the warp's halo while the new base cell is still in the
+// tile, else straight into the global grid.
+template <int DIM, int T>
+__global__ void __launch_bounds__(kP2GThreads, 3)
+    k_g2p2g_w(GridP g, PartsF p, PartsF q, const long long *__restrict__ accR, long long *__restrict__ accW,
+              float dtg0, float dtg1, float dtg2, const uint32_t *__restrict__ perm,
+              const uint32_t *__restrict__ slices, const uint32_t *__restrict__ start,
+              uint32_t *__restrict__ status, float dt, float c4) {
+    using Hl = HaloU<DIM, T>;
+    using St = Stencil<DIM>;
+    constexpr int NW = kP2GThreads / 32;
+    constexpr int VW = DIM * Hl::SIZE;     // velocity words per warp
+    constexpr int AW = St::NC * Hl::SIZE;  // accumulator words per warp
+    constexpr int NF = DIM + 2;            // staged: x, m, id
+    __shared__ float svel[NW][VW];
+    __shared__ __align__(16) int32_t sacc[NW][AW];
+    __shared__ float sbuf[NW][2 * NF * 32];
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    float *vw = svel[warp];
+    const VelHalo<DIM, T> sv{vw, vw + Hl::SIZE, DIM == 3 ? vw + 2 * Hl::SIZE : vw, nullptr};
+    int32_t *wh = sacc[warp];
+    float *wb = sbuf[warp];
+    const uint32_t halo = (uint32_t)__cvta_generic_to_shared(wh);
+    const uint32_t nslices = status[MPM_ST_N_SLICES];
+    uint32_t *work = &status[MPM_ST_WORK_G2P];
+    const float dtg[3] = {dtg0, dtg1, dtg2};
+    const StressP sp{0.f, 0.f, dt, 0.f};
+    float smax = 0.f;
+    uint32_t bad = 0, escaped = 0, unused = 0;
+    for (int i = lane; i < AW; i += 32) wh[i] = 0;
+    __syncwarp();
+    auto at = [&](int stage, int f) { return wb + (stage * NF + f) * 32 + lane; };
+    int o[3];
+    auto flush = [&]() {
+        __syncwarp();
+        for (int h = lane; h < Hl::NODES; h += 32) {
+            int hx, hy, hz;
+            Hl::node(h, hx, hy, hz);
+            const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
+            const bool on = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
+            const int64_t node = on ? node_index(g, gx, gy, gz) : 0;
+#pragma unroll
+            for (int c = 0; c < St::NC; ++c) {
+                const int32_t val = wh[c * Hl::SIZE + h];
+                if (val == 0) continue;
+                wh[c * Hl::SIZE + h] = 0;
+                if (on)
+                    atomicAdd(reinterpret_cast<unsigned long long *>(accW + c * g.nodes + node),
+                              (unsigned long long)(long long)val);
+            }
+        }
+        __syncwarp();
+    };
+    uint32_t s = 0;
+    if (lane == 0) s = atomicAdd(work, 1u);
+    s = __shfl_sync(0xFFFFFFFFu, s, 0);
+    while (s < nslices) {
+        const uint32_t ask = lane == 0 ? atomicAdd(work, 1u) : 0u;
+        const uint32_t t = slices[2 * (size_t)s];
+        const uint32_t beg = start[t] + slices[2 * (size_t)s + 1];
+        const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
+        const uint32_t rounds = (cnt + 31) / 32;
+        tile_origin(g, t, o);
+        auto issue = [&](int stage, uint32_t r) {
+            const uint32_t pid = perm[beg + r];
+#pragma unroll
+            for (int f = 0; f < DIM; ++f) cp_async4(at(stage, f), p.x[f] + pid);
+            cp_async4(at(stage, DIM), p.m + pid);
+            if (p.id) cp_async4(at(stage, DIM + 1), p.id + pid);
+            return pid;
+        };
+        uint32_t pid_next = lane < cnt ? issue(0, lane) : 0u;
+        cp_async_commit();
+        // node velocities of the tile's halo, the grid update applied on load
+        for (int h = lane; h < Hl::NODES; h += 32) {
+            int hx, hy, hz;
+            Hl::node(h, hx, hy, hz);
+            const int gi[3] = {o[0] + hx, o[1] + hy, o[2] + hz};
+            float v[3] = {0.f, 0.f, 0.f};
+            if (gi[0] < g.n[0] && gi[1] < g.n[1] && (DIM == 2 || gi[2] < g.n[2])) {
+                const int64_t node = node_index(g, gi[0], gi[1], gi[2]);
+                const float M = __ll2float_rn(accR[node]);
+                if (M != 0.f) {
+#pragma unroll
+                    for (int l = 0; l < DIM; ++l) {
+                        float vl = __fadd_rn(__fdiv_rn(__ll2float_rn(accR[(1 + l) * g.nodes + node]), M), dtg[l]);
+                        if ((gi[l] < g.boundary && vl < 0.f) || (gi[l] > g.n[l] - 1 - g.boundary && vl > 0.f))
+                            vl = 0.f;
+                        v[l] = vl;
+                    }
+                }
+            }
+#pragma unroll
+            for (int l = 0; l < DIM; ++l) vw[l * Hl::SIZE + h] = v[l];
+        }
+        __syncwarp();
+        int stage = 0;
+        for (uint32_t qr = 0; qr < rounds; ++qr) {
+            const uint32_t r = qr * 32 + lane;
+            const uint32_t pid = pid_next;
+            if (qr + 1 < rounds && r + 32 < cnt) pid_next = issue(stage ^ 1, r + 32);
+            cp_async_commit();
+            cp_async_wait<1>();
+            if (r < cnt) {
+                const uint32_t dst = beg + r;  // bin order
+                float x[DIM], f[3] = {0.f, 0.f, 0.f};
+                int b[3] = {0, 0, 0};
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) x[l] = *at(stage, l);
+                const float m = *at(stage, DIM);
+                const_cast<float *>(q.m)[dst] = m;
+                if (q.id) q.id[dst] = __float_as_uint(*at(stage, DIM + 1));
+                float rec_v[P2GFields<DIM>::NF];
+                rec_v[2 * DIM + DIM * DIM] = m;
+                if (!in_box_x<DIM, T>(g, x, o, b, f)) {
+                    // not binned into this tile from these positions: carried as it is
+#pragma unroll
+                    for (int l = 0; l < DIM; ++l) {
+                        rec_v[l] = x[l];
+                        rec_v[DIM + l] = p.v[l][pid];
+                    }
+#pragma unroll
+                    for (int j = 0; j < DIM * DIM; ++j) rec_v[2 * DIM + j] = p.C[j][pid];
+                } else {
+                    float w[3][3], we[3][3];
+#pragma unroll
+                    for (int l = 0; l < DIM; ++l) {
+                        quad_weights(f[l], w[l]);
+#pragma unroll
+                        for (int a = 0; a < 3; ++a) we[l][a] = __fmul_rn(w[l][a], __fsub_rn((float)a, f[l]));
+                    }
+                    const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
+                                            : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
+                    float vn[DIM], Bm[DIM][DIM];
+                    gather_vB<DIM, T>(sv, hb, w, we, vn, Bm);
+                    float sv2 = 0.f, sc2 = 0.f;
+#pragma unroll
+                    for (int k = 0; k < DIM; ++k) {
+                        rec_v[DIM + k] = vn[k];
+                        sv2 = __fadd_rn(sv2, __fmul_rn(vn[k], vn[k]));
+#pragma unroll
+                        for (int l = 0; l < DIM; ++l) {
+                            const float c = __fmul_rn(Bm[k][l], c4);
+                            rec_v[2 * DIM + k * DIM + l] = c;
+                            sc2 = __fadd_rn(sc2, __fmul_rn(c, c));
+                        }
+                    }
+                    smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
+#pragma unroll
+                    for (int l = 0; l < DIM; ++l) rec_v[l] = __fmaf_rn(dt, vn[l], x[l]);
+                }
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) {
+                    q.x[l][dst] = rec_v[l];
+                    q.v[l][dst] = rec_v[DIM + l];
+                }
+#pragma unroll
+                for (int j = 0; j < DIM * DIM; ++j) q.C[j][dst] = rec_v[2 * DIM + j];
+                // the scatter of the new state (the P2G's arithmetic)
+                auto rec = [&](int fi) { return rec_v[fi]; };
+                int b2[3] = {0, 0, 0};
+                float f2v[3] = {0.f, 0.f, 0.f};
+                bool inside = true;
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) inside = inside && base_frac(rec_v[l], g.inv_dx, g.n[l], b2[l], f2v[l]);
+                if (inside) {
+                    bool in_tile = true;
+#pragma unroll
+                    for (int l = 0; l < DIM; ++l) in_tile = in_tile && b2[l] >= o[l] && b2[l] < o[l] + T;
+                    if (in_tile) {
+                        const int hb2 = DIM == 3 ? (b2[0] - o[0]) + (b2[1] - o[1]) * Hl::SY + (b2[2] - o[2]) * Hl::SZ
+                                                 : (b2[0] - o[0]) + (b2[1] - o[1]) * Hl::SY;
+                        const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb2};
+                        if (!scatter_shares<DIM, false, false>(g, rec, f2v, ad, sp, unused)) ++bad;
+                    } else if (scatter_global<DIM>(g, rec_v, b2, f2v, accW)) {
+                        ++escaped;
+                    } else {
+                        ++bad;
+                    }
+                }
+            }
+            stage ^= 1;
+            // int32 accumulators: at most 512 shares below 2^22 reach one entry between two flushes
+            if ((qr + 1) % 16 == 0 && qr + 1 < rounds) flush();
+        }
+        flush();
+        s = __shfl_sync(0xFFFFFFFFu, ask, 0);
+    }
+    cp_async_wait<0>();
+    bad = __reduce_add_sync(0xFFFFFFFFu, bad);
+    escaped = __reduce_add_sync(0xFFFFFFFFu, escaped);
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
+    if (lane == 0) {
+        if (bad) {
+            atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
+            set_flag(status, MPM_E_BOUND);
+        }
+        if (escaped) atomicAdd(&status[MPM_ST_N_ESCAPED], escaped);
+        if (wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
+    }
+}
+
 // Clears the accumulators of the node blocks that the binned tiles' stencils
 // reach (the blocks the grid update visits), every channel.
 template <int DIM, int T>
@@ -320,20 +545,20 @@ void launch_clear_blocks(const GridP &g, long long *acc, const WsView &w, const 
 mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, const WsView &w, void *acc_read,
                         void *acc_write, float dt, const float dtg[3], const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;
-    const int blocks = dev.sms * 2;
+    const int blocks = dev.sms * 4;
     static_assert(MPM_ST_MAX_SPEED == MPM_ST_WORK_G2P + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
     const auto *R = static_cast<const long long *>(acc_read);
     auto *Wr = static_cast<long long *>(acc_write);
     auto *Rc = static_cast<long long *>(acc_read);
     if (g.dim == 3 && g.T == 4) {
-        k_g2p2g<3, 4><<<blocks, kG2PThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm, w.key,
-                                                      w.slices, w.start, w.status, dt, c4);
+        k_g2p2g_w<3, 4><<<blocks, kP2GThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm,
+                                                        w.slices, w.start, w.status, dt, c4);
         launch_copy_rest(g, in, out, w, dev, st);
         launch_clear_blocks(g, Rc, w, dev, st);
     } else if (g.dim == 2 && g.T == 8) {
-        k_g2p2g<2, 8><<<blocks, kG2PThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm, w.key,
-                                                      w.slices, w.start, w.status, dt, c4);
+        k_g2p2g_w<2, 8><<<blocks, kP2GThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm,
+                                                        w.slices, w.start, w.status, dt, c4);
         launch_copy_rest(g, in, out, w, dev, st);
         launch_clear_blocks(g, Rc, w, dev, st);
     } else {

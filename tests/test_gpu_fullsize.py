@@ -224,7 +224,7 @@ def test_blobs_full_size_fused_step():
     sys.step_fused()
     torch.cuda.synchronize()
     st = sys.status()
-    assert st[L.ST_FLAGS] == 0 and st[L.ST_N_ESCAPED] == 0
+    assert st[L.ST_FLAGS] == 0 and 0 < st[L.ST_N_ESCAPED] < n // 20   # tile changes: a few per cent
     assert not sys.acc2.any().item(), "the grid read must be cleared"
     x1, v1, C1 = sys.state()
     ids1 = sys.id.cpu().numpy().astype(np.int64)
