@@ -32,34 +32,28 @@ UNIT = "particles/s"
 WORKLOAD = "blobs3d: 3D quadratic B-spline MPM step, 256^3 nodes, 16,777,216 particles in 64 Gaussian blobs " \
            "(sigma 0.02), int64 fixed point"
 LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2g; grid update; g2p + copy
+# The timed steps write the new state in bin order (mpm_g2p_binned: one warp per work item), and every
+# SORT_PERIOD-th step with mpm_g2p_sorted, which rewrites the bank-class interleave that the binned steps carry
+# over and wear down; every step bins, scatters, updates and gathers every particle.
+SORT_PERIOD = 8
 
 
 # DRAM traffic per particle (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by the
-# particles it processed) from the ncu captures summarised in profiles/p2g_g2p_full_blobs3d_2M.md and (the
-# "_el" stress and "_vc" volume-channel variants) profiles/stress_volume_full_blobs3d_2M.md, taken on the
-# 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
+# particles it processed) from the ncu capture summarised in profiles/p2g_g2p_full_blobs3d_2M.md (P2G and
+# the bin-order G2P of the timed steps), taken on the 2M-particle sample of the workload (same density) and
+# scaled to a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
-    "p2g": {"bytes_per_particle": 82.0, "files": ('p2g.cu', 'common.cuh'),
-            "sha256": "c6dfe51b1f0273472f433146ebc3674e1c64082a7c1e4562caf3dba360d5507c"
-                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
-    "g2p": {"bytes_per_particle": 77.0, "files": ('grid_g2p.cu', 'common.cuh'),
-            "sha256": "651b07b89e4be6450719238e229272fcbb4bfa75c60eb2d9ce821fbc2d668c0b"
-                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
-    "p2g_el": {"bytes_per_particle": 126.3, "files": ('p2g.cu', 'common.cuh', 'stress.cuh'),
-            "sha256": "c6dfe51b1f0273472f433146ebc3674e1c64082a7c1e4562caf3dba360d5507c"
-                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"
+    "p2g": {"bytes_per_particle": 82.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
+            "sha256": "4d85a4db146d1c76c97099163c30654455b97983623695f20db84ccb8b8283bb"
+                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+                      "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "g2p_el": {"bytes_per_particle": 156.5, "files": ('grid_g2p.cu', 'common.cuh', 'stress.cuh'),
-            "sha256": "651b07b89e4be6450719238e229272fcbb4bfa75c60eb2d9ce821fbc2d668c0b"
-                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"
+    "g2p": {"bytes_per_particle": 74.2, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
+            "sha256": "2177b47c8bc4a3a2e61db227705692fe8476dd3bea09184f43c5134003ea0669"
+                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+                      "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "p2g_vc": {"bytes_per_particle": 89.3, "files": ('p2g.cu', 'common.cuh'),
-            "sha256": "c6dfe51b1f0273472f433146ebc3674e1c64082a7c1e4562caf3dba360d5507c"
-                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
-    "g2p_vc": {"bytes_per_particle": 88.1, "files": ('grid_g2p.cu', 'common.cuh'),
-            "sha256": "651b07b89e4be6450719238e229272fcbb4bfa75c60eb2d9ce821fbc2d668c0b"
-                      "3bab5265a273d17696db96c3ed0f42f265d5340e1b4f13c404927db1b2beaf46"},
 }
 
 
@@ -216,7 +210,10 @@ def run_ours(args, rank, world, local):
         e[2].record(stream)
         sys_.grid_update(stream)
         e[3].record(stream)
-        sys_.g2p_sorted(stream)
+        if (k + 1) % SORT_PERIOD == 0:
+            sys_.g2p_sorted(stream)
+        else:
+            sys_.g2p_binned(stream)
         e[4].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -255,12 +252,13 @@ def run_ours(args, rank, world, local):
                 "frac": round((n * 136.0 + touched * 64.0) / (tr_ms * 1e-3) / 1e9 / peak, 4),
                 "bin_ms": round(float(mean_ms[0]), 4)}
 
-    elastic = volume = fused = loop = None
+    elastic = volume = fused = loop = binned = None
     if args.variant_steps > 0:
         elastic = measure_variant(args, cloud, dev, stream, world, peak, elastic=True, volume=False)
         volume = measure_variant(args, cloud, dev, stream, world, peak, elastic=False, volume=True)
         fused = measure_fused(args, cloud, dev, stream, world, peak, touched, float(mean_ms[0]))
         loop = measure_loop(args, cloud, dev, stream, world, peak)
+        binned = measure_binned(args, cloud, dev, stream, world)
 
     # end to end through the host entry point (pinned host SoA, copies inside the timed region)
     e2e = None
@@ -296,7 +294,8 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "f32+i64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "particles": n, "grid": grid["n"], "acc": "int64",
                    "scale_log2": grid["scale_log2"], "tile": grid["tile"], "touched_nodes": touched,
-                   "particle_order": "kept in bin order: each step's G2P writes the new state sorted (ping-pong)",
+                   "particle_order": "kept in bin order: each step's G2P writes the new state in bin order "
+                                     "(ping-pong), every 8th step with the bank-class interleave",
                    "l2": "inputs larger than L2 (1.07 GB of particle state per step)",
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, mean_ms)},
@@ -311,6 +310,7 @@ def run_ours(args, rank, world, local):
         "volume_channel": volume,
         "fused_step": fused,
         "transfer_loop": loop,
+        "binned_step": binned,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
@@ -440,6 +440,45 @@ def measure_fused(args, cloud, dev, stream, world, peak, touched, bin_ms):
                         "frac": round(achieved / peak, 4), "traffic": None}}
     del fs
     torch.cuda.empty_cache()
+    return out
+
+
+def measure_binned(args, cloud, dev, stream, world):
+    """The G2P schedules on the same workload, after sorted steps have written the
+    bank-class interleave: `steps` steps with mpm_step_binned only, with every eighth
+    step a sorted one (the main region's schedule), and with mpm_step_sorted only."""
+    import torch
+    from material_point_particle_gb300 import _lib as L
+    from material_point_particle_gb300.system import MPMSystem
+
+    steps = args.variant_steps
+    n = cloud["x"].shape[1]
+    out = {"unit": UNIT, "steps": steps}
+    for name, period in (("binned", 0), ("sorted_every_8", 8), ("sorted_every_step", 1)):
+        bs = MPMSystem(cloud["grid"], n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted()
+        for _ in range(max(3, args.warmup)):
+            bs.step_sorted(stream)
+        torch.cuda.synchronize()
+        barrier(world, dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for k in range(steps):
+            if period and (k + 1) % period == 0:
+                bs.step_sorted(stream)
+            else:
+                bs.step_binned(stream)
+            ev[k + 1].record(stream)
+        torch.cuda.synchronize()
+        st = bs.status()
+        assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
+        per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+        ms = aggregate_max(ev[0].elapsed_time(ev[steps]) / steps, world, dev)
+        q = max(1, steps // 10)
+        out[name] = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1),
+                     "first_tenth_ms": round(float(np.mean(per[:q])), 4),
+                     "last_tenth_ms": round(float(np.mean(per[-q:])), 4)}
+        del bs
+        torch.cuda.empty_cache()
     return out
 
 

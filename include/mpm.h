@@ -288,6 +288,20 @@ mpm_status mpm_g2p_sorted(const mpm_grid_desc *desc, const float *grid_vel, cons
                           mpm_particles *out, mpm_bins *bins, float dt, void *stream);
 
 /*
+ * mpm_g2p_binned -- mpm_g2p_sorted without the bank-class interleave: the
+ * in-domain particles are written in bin order, out[j] = the new state of
+ * in[perm[j]] for j below MPM_ST_N_VALID, the others copied as by
+ * mpm_g2p_sorted; the same bits per particle.  One warp per work item and no
+ * block barrier, so it is faster than mpm_g2p_sorted; the order inside a tile
+ * is the input's, so an interleave written by an earlier mpm_g2p_sorted
+ * carries over and wears down slowly as particles change cells (the next
+ * P2G's shared-memory bank conflicts grow with it; an occasional
+ * mpm_g2p_sorted restores it).  `in` and `out` must not overlap.
+ */
+mpm_status mpm_g2p_binned(const mpm_grid_desc *desc, const float *grid_vel, const mpm_particles *in,
+                          mpm_particles *out, mpm_bins *bins, float dt, void *stream);
+
+/*
  * mpm_step -- mpm_bin, mpm_p2g, mpm_grid_update and mpm_g2p in sequence on one
  * stream (device pointers throughout; particles keep their index).
  */
@@ -299,6 +313,13 @@ mpm_status mpm_step(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *b
  * mpm_g2p_sorted from `in` into `out` (the caller swaps the two between steps).
  */
 mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
+                           void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream);
+
+/*
+ * mpm_step_binned -- mpm_bin, mpm_p2g and mpm_grid_update on `in`, then
+ * mpm_g2p_binned from `in` into `out` (the caller swaps the two).
+ */
+mpm_status mpm_step_binned(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
                            void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream);
 
 /*

@@ -86,12 +86,15 @@ def library() -> ct.CDLL:
             L.mpm_step_fused.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
                                          P(ct.c_float), VP]
             L.mpm_iterate.argtypes = [P(GridDesc), P(Particles), P(Bins), VP, VP, ct.c_int, VP]
+            L.mpm_g2p_binned.argtypes = [P(GridDesc), VP, P(Particles), P(Particles), P(Bins), ct.c_float, VP]
+            L.mpm_step_binned.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
+                                          P(ct.c_float), VP]
             L.mpm_permute.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP]
             L.mpm_read_status.argtypes = [P(Bins), VP, VP]
             L.mpm_bin_static.argtypes = [P(GridDesc), P(Particles), ct.c_int, P(Bins), VP]
             for name in ("mpm_bins_init", "mpm_bin", "mpm_p2g", "mpm_grid_update", "mpm_g2p", "mpm_step",
                          "mpm_g2p_sorted", "mpm_step_sorted", "mpm_step_host", "mpm_permute", "mpm_read_status",
-                         "mpm_bin_static", "mpm_step_fused", "mpm_iterate"):
+                         "mpm_bin_static", "mpm_step_fused", "mpm_iterate", "mpm_g2p_binned", "mpm_step_binned"):
                 getattr(L, name).restype = ct.c_int
             _L = L
     return _L
@@ -242,6 +245,19 @@ def mpm_iterate(desc: GridDesc, parts: Particles, bins: Bins, acc_a: torch.Tenso
                 iterations: int, stream=None):
     _check(library().mpm_iterate(ct.byref(desc), ct.byref(parts), ct.byref(bins), ct.c_void_p(acc_a.data_ptr()),
                                  ct.c_void_p(acc_b.data_ptr()), int(iterations), _stream(stream)), "mpm_iterate")
+
+
+def mpm_g2p_binned(desc: GridDesc, grid_vel: torch.Tensor, src: Particles, dst: Particles, bins: Bins, dt: float,
+                   stream=None):
+    _check(library().mpm_g2p_binned(ct.byref(desc), ct.c_void_p(grid_vel.data_ptr()), ct.byref(src), ct.byref(dst),
+                                    ct.byref(bins), ct.c_float(dt), _stream(stream)), "mpm_g2p_binned")
+
+
+def mpm_step_binned(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, grid_acc: torch.Tensor,
+                    grid_vel: torch.Tensor, dt: float, dtg, stream=None):
+    _check(library().mpm_step_binned(ct.byref(desc), ct.byref(src), ct.byref(dst), ct.byref(bins),
+                                     ct.c_void_p(grid_acc.data_ptr()), ct.c_void_p(grid_vel.data_ptr()),
+                                     ct.c_float(dt), _f3(dtg), _stream(stream)), "mpm_step_binned")
 
 
 def mpm_step_sorted(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, grid_acc: torch.Tensor,

@@ -383,6 +383,29 @@ mpm_status mpm_g2p_sorted(const mpm_grid_desc *desc, const float *grid_vel, cons
     return launch_g2p_sorted(g, grid_vel, pi, po, view_of(g, *bins), dt, dev, static_cast<cudaStream_t>(stream));
 }
 
+mpm_status mpm_g2p_binned(const mpm_grid_desc *desc, const float *grid_vel, const mpm_particles *in,
+                          mpm_particles *out, mpm_bins *bins, float dt, void *stream) {
+    GridP g;
+    MPM_TRY(make_grid(desc, g));
+    if (g.acc_mode == MPM_ACC_EXACT_INT || !grid_vel) return MPM_E_ARG;
+    PartsF pi, po;
+    MPM_TRY(parts_f(g, in, true, pi));
+    MPM_TRY(parts_f(g, out, true, po));
+    if (pi.n != po.n || (!pi.id) != (!po.id) || (!pi.F[0]) != (!po.F[0])) return MPM_E_ARG;
+    MPM_TRY(check_bins(g, bins, pi.n));
+    DeviceInfo dev;
+    MPM_TRY(device_info(dev));
+    return launch_g2p_binned(g, grid_vel, pi, po, view_of(g, *bins), dt, dev, static_cast<cudaStream_t>(stream));
+}
+
+mpm_status mpm_step_binned(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
+                           void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream) {
+    MPM_TRY(mpm_bin(desc, in, bins, 0, stream));
+    MPM_TRY(mpm_p2g(desc, in, bins, grid_acc, dt, stream));
+    MPM_TRY(mpm_grid_update(desc, grid_acc, grid_vel, dtg, bins, stream));
+    return mpm_g2p_binned(desc, grid_vel, in, out, bins, dt, stream);
+}
+
 mpm_status mpm_step_sorted(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,
                            void *grid_acc, float *grid_vel, float dt, const float dtg[3], void *stream) {
     MPM_TRY(mpm_bin(desc, in, bins, 0, stream));

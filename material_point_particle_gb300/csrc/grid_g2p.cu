@@ -336,6 +336,85 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
     if (lane == 0 && wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
 }
 
+// The sorted G2P without the bank-class interleave: out[j] = the new state of
+// in[perm[j]] (bin order), one warp per work item (the P2G kernel's shape).
+// Each warp stages its tile's velocity halo and, 32 particles a round, its
+// lanes' x, m and id, and each lane gathers its particle (gather_one, the
+// same arithmetic) and writes it at its bin-order place: consecutive lanes,
+// consecutive places, no block barrier.
+template <int DIM, int T, bool EL, bool VC>
+__global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
+                                                       const uint32_t *__restrict__ perm,
+                                                       const uint32_t *__restrict__ slices,
+                                                       const uint32_t *__restrict__ start,
+                                                       uint32_t *__restrict__ status, float dt, float c4) {
+    using Hl = HaloU<DIM, T>;
+    constexpr int NW = kP2GThreads / 32;
+    constexpr int NCH = DIM + (VC ? 1 : 0);
+    constexpr int NF = DIM + 2;  // staged: x, m, id
+    __shared__ float svel[NW][NCH * Hl::SIZE];
+    __shared__ float sbuf[NW][2 * NF * 32];
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    float *vw = svel[warp];
+    const VelHalo<DIM, T> sv{vw, vw + Hl::SIZE, DIM == 3 ? vw + 2 * Hl::SIZE : vw, VC ? vw + DIM * Hl::SIZE : vw};
+    float *wb = sbuf[warp];
+    const uint32_t nslices = status[MPM_ST_N_SLICES];
+    uint32_t *work = &status[MPM_ST_WORK_G2P];
+    float smax = 0.f;
+    auto at = [&](int stage, int f) { return wb + (stage * NF + f) * 32 + lane; };
+    uint32_t s = 0;
+    if (lane == 0) s = atomicAdd(work, 1u);
+    s = __shfl_sync(0xFFFFFFFFu, s, 0);
+    while (s < nslices) {
+        const uint32_t ask = lane == 0 ? atomicAdd(work, 1u) : 0u;
+        const uint32_t t = slices[2 * (size_t)s];
+        const uint32_t beg = start[t] + slices[2 * (size_t)s + 1];
+        const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
+        int o[3];
+        tile_origin(g, t, o);
+        auto issue = [&](int stage, uint32_t r) {
+            const uint32_t pid = perm[beg + r];
+#pragma unroll
+            for (int f = 0; f < DIM; ++f) cp_async4(at(stage, f), p.x[f] + pid);
+            cp_async4(at(stage, DIM), p.m + pid);
+            if (p.id) cp_async4(at(stage, DIM + 1), p.id + pid);
+            return pid;
+        };
+        uint32_t pid_next = lane < cnt ? issue(0, lane) : 0u;
+        cp_async_commit();
+        for (int h = lane; h < Hl::NODES; h += 32) {
+            int hx, hy, hz;
+            Hl::node(h, hx, hy, hz);
+            const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
+            const bool in = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
+            const int64_t node = in ? node_index(g, gx, gy, gz) : 0;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) vw[c * Hl::SIZE + h] = in ? vel[c * g.nodes + node] : 0.f;
+        }
+        __syncwarp();
+        const uint32_t rounds = (cnt + 31) / 32;
+        int stage = 0;
+        for (uint32_t qr = 0; qr < rounds; ++qr) {
+            const uint32_t r = qr * 32 + lane;
+            const uint32_t pid = pid_next;
+            if (qr + 1 < rounds && r + 32 < cnt) pid_next = issue(stage ^ 1, r + 32);
+            cp_async_commit();
+            cp_async_wait<1>();
+            if (r < cnt) {
+                const int st = stage;
+                auto rec = [&](int f) { return *at(st, f); };
+                gather_one<DIM, T, true, EL, VC>(g, p, q, pid, beg + r, rec, o, sv, dt, c4, smax);
+            }
+            stage ^= 1;
+        }
+        __syncwarp();
+        s = __shfl_sync(0xFFFFFFFFu, ask, 0);
+    }
+    cp_async_wait<0>();
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
+    if (lane == 0 && wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
+}
+
 // Particles past the sorted in-domain part (outside the domain): copied.
 template <int DIM>
 __global__ void k_copy_rest(PartsF p, PartsF q, const uint32_t *__restrict__ perm, const uint32_t *__restrict__ status) {
@@ -385,6 +464,39 @@ mpm_status launch_g2p_any(const GridP &g, const float *vel, const PartsF &in, co
         launch_g2p_dt<3, 4, SORTED>(g, vel, in, out, w, dt, dev, st);
     else if (g.dim == 2 && g.T == 8)
         launch_g2p_dt<2, 8, SORTED>(g, vel, in, out, w, dt, dev, st);
+    else
+        return MPM_E_ARG;
+    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+}
+
+template <int DIM, int T>
+void launch_g2p_binned_dt(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
+                          float dt, const DeviceInfo &dev, cudaStream_t st) {
+    const float c4 = 4.0f * g.inv_dx;
+    const int blocks = dev.sms * 4;
+    const bool el = in.F[0] != nullptr;
+#define MPM_G2P_W(EL_, VC_)                                                                                    \
+    k_g2p_w<DIM, T, EL_, VC_><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.slices, w.start, w.status, \
+                                                            dt, c4)
+    if (el && g.vc)
+        MPM_G2P_W(true, true);
+    else if (el)
+        MPM_G2P_W(true, false);
+    else if (g.vc)
+        MPM_G2P_W(false, true);
+    else
+        MPM_G2P_W(false, false);
+#undef MPM_G2P_W
+    k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+}
+
+mpm_status launch_g2p_binned(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
+                             float dt, const DeviceInfo &dev, cudaStream_t st) {
+    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
+    if (g.dim == 3 && g.T == 4)
+        launch_g2p_binned_dt<3, 4>(g, vel, in, out, w, dt, dev, st);
+    else if (g.dim == 2 && g.T == 8)
+        launch_g2p_binned_dt<2, 8>(g, vel, in, out, w, dt, dev, st);
     else
         return MPM_E_ARG;
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;

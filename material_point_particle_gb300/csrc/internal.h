@@ -54,6 +54,8 @@ mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, con
 void launch_clear_blocks(const GridP &g, long long *acc, const WsView &w, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_iterate(const GridP &g, const PartsF &p, const WsView &w, void *acc_a, void *acc_b,
                           int iterations, const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_g2p_binned(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
+                             float dt, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
                           const DeviceInfo &dev, cudaStream_t st);
 

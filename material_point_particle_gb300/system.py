@@ -154,6 +154,15 @@ class MPMSystem:
         L.mpm_g2p_sorted(self.desc, self.vel, self.parts, self.parts2, self.bins, self.dt, stream)
         self.swap()
 
+    def g2p_binned(self, stream=None):
+        L.mpm_g2p_binned(self.desc, self.vel, self.parts, self.parts2, self.bins, self.dt, stream)
+        self.swap()
+
+    def step_binned(self, stream=None):
+        L.mpm_step_binned(self.desc, self.parts, self.parts2, self.bins, self.acc, self.vel, self.dt, self.dtg,
+                          stream)
+        self.swap()
+
     def step_sorted(self, stream=None):
         L.mpm_step_sorted(self.desc, self.parts, self.parts2, self.bins, self.acc, self.vel, self.dt, self.dtg,
                           stream)
