@@ -4,7 +4,8 @@
   output compared with the oracle (bit for bit in int64 mode, within the float
   tolerance in float-atomic mode).
 - The clustered blobs (16,777,216 particles, 256^3 nodes) in the launch
-  configuration the benchmark times (steady state after three sorted steps),
+  configuration the benchmark times (three sorted warm-up steps, then
+  bin-order steps with a sorted one every eighth: one of each checked),
   and the sphere (67,108,864 particles, 512^3 nodes) from its generated order:
   one step checked piece by piece: the whole permutation against the oracle's
   binning; the P2G grid through the exact conservation identities and, on
@@ -86,9 +87,10 @@ def _quantities(grid, x, v, m):
     return Q
 
 
-def _check_step(sys, grid, n, n_tiles_sampled=6):
-    """One sorted step of `sys`, checked piece by piece against the oracle
-    (with the stress fold and the F update when the particles are elastic)."""
+def _check_step(sys, grid, n, n_tiles_sampled=6, binned=False):
+    """One sorted (or, with `binned`, bin-order) step of `sys`, checked piece by
+    piece against the oracle (with the stress fold and the F update when the
+    particles are elastic)."""
     x0, v0, C0 = sys.state()
     m0 = sys.m.cpu().numpy()
     ids0 = sys.id.cpu().numpy().astype(np.int64)
@@ -142,13 +144,18 @@ def _check_step(sys, grid, n, n_tiles_sampled=6):
     del acc, ovel
     assert not sys.acc.any().item(), "grid update must leave the accumulators zero"
 
-    # sorted G2P: sampled in-domain particles, found through their ids
-    sys.g2p_sorted()
+    # sorted (or binned) G2P: sampled in-domain particles, found through their ids
+    if binned:
+        sys.g2p_binned()
+    else:
+        sys.g2p_sorted()
     x1, v1, C1 = sys.state()
     ids1 = sys.id.cpu().numpy().astype(np.int64)
     # the advective step bound: the largest term over the moved particles (all in the domain)
     speed = np.array([sys.status()[L.ST_MAX_SPEED]], np.uint32).view(np.float32)[0]
     assert speed == O.advective_speed(grid["dim"], grid["dx"], v1[:, :valid], C1[:, :valid])
+    if binned:   # bin order: out[j] = in[perm[j]]
+        assert np.array_equal(ids1, ids0[perm.astype(np.int64)])
     where = np.empty(n, dtype=np.int64)
     where[ids1] = np.arange(n)
     samp = inside[(W.Stream(32, 32).bits(20000) % np.uint64(inside.size)).astype(np.int64)]
@@ -166,15 +173,21 @@ def _check_step(sys, grid, n, n_tiles_sampled=6):
 
 
 def test_blobs_full_size_bench_configuration():
+    """The benchmark's schedule: three sorted warm-up steps, then bin-order steps
+    with a sorted one every eighth; a binned step and a sorted step checked."""
     cloud = W.blobs3d()
     grid = cloud["grid"]
     n = cloud["x"].shape[1]
     assert n == 16777216 and grid["n"][0] == 256
     sys = _system(cloud).enable_sorted()
     del cloud
-    for _ in range(3):                       # steady state, as the benchmark times it
+    for _ in range(3):                       # the warm-up steps
         sys.step_sorted()
-    _check_step(sys, grid, n)
+    for _ in range(5):
+        sys.step_binned()
+    _check_step(sys, grid, n, n_tiles_sampled=3, binned=True)
+    sys.step_binned()
+    _check_step(sys, grid, n, n_tiles_sampled=3)
 
 
 def test_sphere_full_size_step():
