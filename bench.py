@@ -39,9 +39,10 @@ SORT_PERIOD = 8
 
 
 # DRAM traffic per particle (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by the
-# particles it processed) from the ncu capture summarised in profiles/p2g_g2p_full_blobs3d_2M.md (P2G and
-# the bin-order G2P of the timed steps), taken on the 2M-particle sample of the workload (same density) and
-# scaled to a full launch by the particle count.
+# particles it processed) from the ncu captures summarised in profiles/p2g_g2p_full_blobs3d_2M.md (P2G and
+# the bin-order G2P of the timed steps) and profiles/stress_volume_full_blobs3d_2M.md (their "_el" stress and
+# "_vc" volume-channel variants), taken on the 2M-particle sample of the workload (same density) and scaled to
+# a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
     "p2g": {"bytes_per_particle": 82.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
@@ -50,6 +51,26 @@ MEASURED_TRAFFIC = {
                       "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
     "g2p": {"bytes_per_particle": 74.2, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
+            "sha256": "2177b47c8bc4a3a2e61db227705692fe8476dd3bea09184f43c5134003ea0669"
+                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+                      "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
+                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
+    "p2g_el": {"bytes_per_particle": 126.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
+            "sha256": "4d85a4db146d1c76c97099163c30654455b97983623695f20db84ccb8b8283bb"
+                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+                      "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
+                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
+    "g2p_el": {"bytes_per_particle": 166.0, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
+            "sha256": "2177b47c8bc4a3a2e61db227705692fe8476dd3bea09184f43c5134003ea0669"
+                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+                      "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
+                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
+    "p2g_vc": {"bytes_per_particle": 89.1, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
+            "sha256": "4d85a4db146d1c76c97099163c30654455b97983623695f20db84ccb8b8283bb"
+                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+                      "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
+                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
+    "g2p_vc": {"bytes_per_particle": 89.9, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
             "sha256": "2177b47c8bc4a3a2e61db227705692fe8476dd3bea09184f43c5134003ea0669"
                       "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
                       "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
@@ -324,8 +345,8 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     """The same workload with the elastic state (F = I + N(0, 0.05), V0 = dx^3,
     Neo-Hookean mu = lambda = 1e9: the stress folded into P2G's affine matrix,
     F advanced in G2P) and/or the grid-recovered volume channel (rest volume
-    V0 = dx^3 scattered and gathered back).  Timed like the main region, in the
-    steady state, per phase."""
+    V0 = dx^3 scattered and gathered back).  Timed like the main region (the same
+    G2P schedule), in the steady state, per phase."""
     import torch
     from material_point_particle_gb300 import _lib as L
     from material_point_particle_gb300 import workloads as W
@@ -360,7 +381,10 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
         e[2].record(stream)
         es.grid_update(stream)
         e[3].record(stream)
-        es.g2p_sorted(stream)
+        if (k + 1) % SORT_PERIOD == 0:
+            es.g2p_sorted(stream)
+        else:
+            es.g2p_binned(stream)
         e[4].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
