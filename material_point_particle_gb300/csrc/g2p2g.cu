@@ -2,287 +2,29 @@
 //
 // Implementation guide ("Implementation -- GPU Optimization & Reference
 // Codebases"), section 2.1, the worked shape of "sort + tile + stage in shared
-// memory": the whole transfer is one kernel, one thread block per slice of a
-// tile; the block loads the tile's nodes and their halo applying the grid
-// update as it loads (so the read is the grid pass), each thread gathers its
-// particle, updates it and scatters it into shared-memory accumulators, and
-// the block adds them to the global grid once.
+// memory": the whole transfer is one kernel per step; it loads a tile's nodes
+// and their halo applying the grid update as it loads (so the read is the
+// grid pass), gathers each particle, updates it and scatters it into a
+// shared-memory accumulator that is added to the global grid once.
 //
 // In the guide's position-based solver the particles do not move inside the
-// loop, so gather and scatter share one halo.  Here, in the velocity form,
+// loop, so gather and scatter share one tile.  Here, in the velocity form,
 // the gather reads the accumulators R of the P2G at the binned positions x,
 // and the scatter writes the next accumulators W at the advected positions
-// x' = fma(dt, v', x).  A particle moves less than a cell per step under the
-// advective bound (section 3.3.2, rule 6), so the block's scatter accumulator
-// covers base cells [o - 1, o + T] of the tile at origin o: (T + 4)^dim nodes.
-// A particle that moved further is scattered straight into the global grid,
-// with the same shares.  Shares, velocities and the new state are bit for
-// bit those of mpm_bin + mpm_p2g + mpm_grid_update + mpm_g2p_sorted, then
-// mpm_p2g on the new state.  R is only read (several blocks read each halo
-// node); a second kernel clears it afterwards, so that it can be the next
-// step's W (the guide's rotation of grid buffers).
+// x' = fma(dt, v', x).  The scatter uses the same tile's accumulator while a
+// particle's new base cell stays in the tile; a particle that left the tile
+// (a few in ten thousand per step) is scattered straight into the global
+// grid, with the same shares.  Shares, velocities and the new state are bit
+// for bit those of mpm_bin + mpm_p2g + mpm_grid_update + mpm_g2p_binned, then
+// mpm_p2g on the new state.  R is only read (several work items read each
+// halo node); a second kernel clears it afterwards, so that it can be the
+// next step's W (the guide's rotation of grid buffers).
 #include "common.cuh"
 #include "gather.cuh"
 #include "internal.h"
 #include "scatter.cuh"
 
 namespace mpm {
-
-// The scatter accumulator: base cells [o - 1, o + T] of a tile, (T + 4)^dim
-// nodes, with row and plane pitches congruent to those of the compact halo
-// (T + 2 and (T + 2)^2) modulo 32 banks, so that a cell's bank is its
-// interleave class plus a constant: 38 = 6 and 324 = 36 (mod 32) for 4^3
-// tiles, 42 = 10 (mod 32) for 8^2 tiles.
-template <int DIM, int T>
-struct HaloX {
-    static constexpr int H = T + 4;
-    static constexpr int SY = DIM == 3 ? 38 : 42;
-    static constexpr int SZ = DIM == 3 ? 324 : 0;
-    static_assert(SY >= H && (DIM == 2 || SZ >= H * SY), "pitches hold a row and a plane");
-    static_assert(SY % 32 == (T + 2) % 32 && (DIM == 2 || SZ % 32 == ((T + 2) * (T + 2)) % 32), "bank classes");
-    static constexpr int NODES = DIM == 3 ? H * H * H : H * H;
-    static constexpr int SIZE = DIM == 3 ? (H - 1) * SZ + (H - 1) * SY + H : (H - 1) * SY + H;
-    __device__ static constexpr int off(int a) {
-        return DIM == 3 ? (a / 9) + (a / 3 % 3) * SY + (a % 3) * SZ : (a / 3) + (a % 3) * SY;
-    }
-    __device__ static void node(int h, int &hx, int &hy, int &hz, int &idx) {
-        hx = h % H;
-        hy = (h / H) % H;
-        hz = DIM == 3 ? h / (H * H) : 0;
-        idx = hx + hy * SY + hz * SZ;
-    }
-};
-
-template <int DIM, int T>
-__global__ void __launch_bounds__(kG2PThreads, 2)
-    k_g2p2g(GridP g, PartsF p, PartsF q, const long long *__restrict__ accR, long long *__restrict__ accW,
-            float dtg0, float dtg1, float dtg2, const uint32_t *__restrict__ perm, const uint32_t *__restrict__ key,
-            const uint32_t *__restrict__ slices, const uint32_t *__restrict__ start, uint32_t *__restrict__ status,
-            float dt, float c4) {
-    using Hl = HaloU<DIM, T>;      // gather: base cells [o, o + T)
-    using Hx = HaloX<DIM, T>;      // scatter: base cells [o - 1, o + T + 1)
-    using St = Stencil<DIM>;
-    constexpr int NQ = kSliceParticles / kG2PThreads;
-    constexpr int NF = DIM + 2;                 // staged: x, m, id
-    constexpr int XW = St::NC * Hx::SIZE;       // scatter accumulator words
-    __shared__ float sv_x[Hl::SIZE], sv_y[Hl::SIZE], sv_z[DIM == 3 ? Hl::SIZE : 1];
-    const VelHalo<DIM, T> sv{sv_x, sv_y, sv_z, nullptr};
-    __shared__ float sbuf[NF * kSliceParticles];
-    __shared__ uint32_t hist[32 * 33];
-    __shared__ uint32_t cstart[32];
-    __shared__ uint32_t order[kSliceParticles + kSliceParticles / 32];
-    __shared__ __align__(16) int32_t sacc[XW];
-    __shared__ uint32_t item_sh;
-    const uint32_t lane = lane_id();
-    const uint32_t nslices = status[MPM_ST_N_SLICES];
-    const uint32_t halo = (uint32_t)__cvta_generic_to_shared(sacc);
-    const float dtg[3] = {dtg0, dtg1, dtg2};
-    const StressP sp{0.f, 0.f, dt, 0.f};
-    float smax = 0.f;
-    uint32_t bad = 0, escaped = 0, unused = 0;
-    for (int i = threadIdx.x; i < XW; i += blockDim.x) sacc[i] = 0;
-    int o[3], ox[3];
-    // every nonzero scatter-accumulator entry added to W once, and cleared
-    auto flush = [&]() {
-        for (int h = threadIdx.x; h < Hx::NODES; h += blockDim.x) {
-            int hx, hy, hz, idx;
-            Hx::node(h, hx, hy, hz, idx);
-            const int gx = ox[0] + hx, gy = ox[1] + hy, gz = ox[2] + hz;
-            const bool on = gx >= 0 && gy >= 0 && gz >= 0 && gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
-            const int64_t node = on ? node_index(g, gx, gy, gz) : 0;
-#pragma unroll
-            for (int c = 0; c < St::NC; ++c) {
-                const int32_t val = sacc[c * Hx::SIZE + idx];
-                if (val == 0) continue;
-                sacc[c * Hx::SIZE + idx] = 0;
-                if (on)
-                    atomicAdd(reinterpret_cast<unsigned long long *>(accW + c * g.nodes + node),
-                              (unsigned long long)(long long)val);
-            }
-        }
-    };
-    uint32_t next = 0;
-    for (uint32_t s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
-        next = ask_item(&status[MPM_ST_WORK_G2P]);
-        const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
-        const uint32_t beg = start[t] + first;
-        const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
-        tile_origin(g, t, o);
-#pragma unroll
-        for (int l = 0; l < 3; ++l) ox[l] = l < DIM ? o[l] - 1 : 0;
-        uint32_t pids[NQ];
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-            const uint32_t r = threadIdx.x + qi * kG2PThreads;
-            pids[qi] = r < cnt ? perm[beg + r] : 0u;
-        }
-        // the slice's x, m, id in bin order
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-            const uint32_t r = threadIdx.x + qi * kG2PThreads;
-            if (r < cnt) {
-#pragma unroll
-                for (int f = 0; f < DIM; ++f) cp_async4(&sbuf[f * kSliceParticles + r], p.x[f] + pids[qi]);
-                cp_async4(&sbuf[DIM * kSliceParticles + r], p.m + pids[qi]);
-                if (p.id) cp_async4(&sbuf[(DIM + 1) * kSliceParticles + r], p.id + pids[qi]);
-            }
-        }
-        cp_async_commit();
-        // node velocities of the tile's halo, the grid update applied on load
-        for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
-            int hx, hy, hz;
-            Hl::node(h, hx, hy, hz);
-            const int gi[3] = {o[0] + hx, o[1] + hy, o[2] + hz};
-            float v[3] = {0.f, 0.f, 0.f};
-            if (gi[0] < g.n[0] && gi[1] < g.n[1] && (DIM == 2 || gi[2] < g.n[2])) {
-                const int64_t node = node_index(g, gi[0], gi[1], gi[2]);
-                const float M = __ll2float_rn(accR[node]);
-                if (M != 0.f) {
-#pragma unroll
-                    for (int l = 0; l < DIM; ++l) {
-                        float vl = __fadd_rn(__fdiv_rn(__ll2float_rn(accR[(1 + l) * g.nodes + node]), M), dtg[l]);
-                        if ((gi[l] < g.boundary && vl < 0.f) || (gi[l] > g.n[l] - 1 - g.boundary && vl > 0.f))
-                            vl = 0.f;
-                        v[l] = vl;
-                    }
-                }
-            }
-            sv_x[h] = v[0];
-            sv_y[h] = v[1];
-            if (DIM == 3) sv_z[h] = v[2];
-        }
-        if (cnt > 32u) class_order<DIM, T, kG2PThreads>(key, pids, cnt, hist, cstart, order);
-        cp_async_wait<0>();
-        __syncthreads();
-        // one particle: gathered at x, its new state written to the output
-        auto gather_pass = [&](uint32_t pos) {
-            {
-                uint32_t r = pos;  // a slice of at most 32 particles keeps bin order
-                if (cnt > 32u) {
-                    const uint32_t e = interleave_entry(pos, cnt);
-                    r = order[e + (e >> 5)];
-                }
-                const uint32_t pid = perm[beg + r], dst = beg + pos;
-                float x[DIM], f[3] = {0.f, 0.f, 0.f};
-                int b[3] = {0, 0, 0};
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) x[l] = sbuf[l * kSliceParticles + r];
-                const float m = sbuf[DIM * kSliceParticles + r];
-                if (!in_box_x<DIM, T>(g, x, o, b, f)) {
-                    // not binned into this tile from these positions: carried as it is
-#pragma unroll
-                    for (int l = 0; l < DIM; ++l) {
-                        q.x[l][dst] = p.x[l][pid];
-                        q.v[l][dst] = p.v[l][pid];
-                    }
-#pragma unroll
-                    for (int j = 0; j < DIM * DIM; ++j) q.C[j][dst] = p.C[j][pid];
-                    const_cast<float *>(q.m)[dst] = m;
-                    if (q.id) q.id[dst] = __float_as_uint(sbuf[(DIM + 1) * kSliceParticles + r]);
-                    return;
-                }
-                // gather (the G2P's arithmetic)
-                float w[3][3], we[3][3];
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) {
-                    quad_weights(f[l], w[l]);
-#pragma unroll
-                    for (int a = 0; a < 3; ++a) we[l][a] = __fmul_rn(w[l][a], __fsub_rn((float)a, f[l]));
-                }
-                const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
-                                        : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
-                float vn[DIM], Bm[DIM][DIM];
-                gather_vB<DIM, T>(sv, hb, w, we, vn, Bm);
-                // the new state
-                float sv2 = 0.f, sc2 = 0.f;
-#pragma unroll
-                for (int k = 0; k < DIM; ++k) {
-                    q.v[k][dst] = vn[k];
-                    sv2 = __fadd_rn(sv2, __fmul_rn(vn[k], vn[k]));
-#pragma unroll
-                    for (int l = 0; l < DIM; ++l) {
-                        const float c = __fmul_rn(Bm[k][l], c4);
-                        q.C[k * DIM + l][dst] = c;
-                        sc2 = __fadd_rn(sc2, __fmul_rn(c, c));
-                    }
-                }
-                smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) q.x[l][dst] = __fmaf_rn(dt, vn[l], x[l]);
-                const_cast<float *>(q.m)[dst] = m;
-                if (q.id) q.id[dst] = __float_as_uint(sbuf[(DIM + 1) * kSliceParticles + r]);
-            }
-        };
-        // one particle of the new state (written by this thread in the gather
-        // pass, read back from the cache): scattered at x' (the P2G's arithmetic)
-        auto scatter_pass = [&](uint32_t pos) {
-            {
-                const uint32_t dst = beg + pos;
-                float rec_v[P2GFields<DIM>::NF];
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) {
-                    rec_v[l] = q.x[l][dst];
-                    rec_v[DIM + l] = q.v[l][dst];
-                }
-#pragma unroll
-                for (int j = 0; j < DIM * DIM; ++j) rec_v[2 * DIM + j] = q.C[j][dst];
-                rec_v[2 * DIM + DIM * DIM] = q.m[dst];
-                auto rec = [&](int fi) { return rec_v[fi]; };
-                int b2[3] = {0, 0, 0};
-                float f2v[3] = {0.f, 0.f, 0.f};
-                bool inside = true;
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) inside = inside && base_frac(rec_v[l], g.inv_dx, g.n[l], b2[l], f2v[l]);
-                if (!inside) return;  // outside the domain: the next binning counts it, nothing is scattered
-                bool in_box = true;
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) in_box = in_box && b2[l] >= ox[l] && b2[l] < ox[l] + T + 2;
-                if (in_box) {
-                    const int hb2 = DIM == 3 ? (b2[0] - ox[0]) + (b2[1] - ox[1]) * Hx::SY + (b2[2] - ox[2]) * Hx::SZ
-                                             : (b2[0] - ox[0]) + (b2[1] - ox[1]) * Hx::SY;
-                    const SharedAdd<Hx> ad{halo + 4u * (uint32_t)hb2};
-                    if (!scatter_shares<DIM, false, false>(g, rec, f2v, ad, sp, unused)) ++bad;
-                } else {
-                    const GlobalAdd<DIM> ad{accW, g.nodes, g.n[0], (int64_t)g.n[0] * g.n[1],
-                                            node_index(g, b2[0], b2[1], DIM == 3 ? b2[2] : 0)};
-                    if (scatter_shares<DIM, false, false>(g, rec, f2v, ad, sp, unused))
-                        ++escaped;
-                    else
-                        ++bad;
-                }
-            }
-        };
-#pragma unroll 1
-        for (int qi = 0; qi < NQ; ++qi) {
-            const uint32_t pos = threadIdx.x + qi * kG2PThreads;
-            if (pos < cnt) gather_pass(pos);
-        }
-#pragma unroll 1
-        for (int qi = 0; qi < NQ; ++qi) {
-            const uint32_t pos = threadIdx.x + qi * kG2PThreads;
-            if (pos < cnt) scatter_pass(pos);
-            // int32 accumulators: at most 512 shares below 2^22 reach one entry between two flushes
-            if (qi == 1 && cnt > 2u * kG2PThreads) {
-                __syncthreads();
-                flush();
-                __syncthreads();
-            }
-        }
-        __syncthreads();
-        flush();
-    }
-    bad = __reduce_add_sync(0xFFFFFFFFu, bad);
-    escaped = __reduce_add_sync(0xFFFFFFFFu, escaped);
-    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
-    if (lane == 0) {
-        if (bad) {
-            atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
-            set_flag(status, MPM_E_BOUND);
-        }
-        if (escaped) atomicAdd(&status[MPM_ST_N_ESCAPED], escaped);
-        if (wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
-    }
-}
 
 // A particle's shares straight into the global grid (the rare particle whose
 // new base cell left its tile); out of line, so that its registers do not
