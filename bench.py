@@ -31,48 +31,52 @@ METRIC = "P2G+G2P particles/sec (3D 256^3, 16M clustered); % of HBM roofline"
 UNIT = "particles/s"
 WORKLOAD = "blobs3d: 3D quadratic B-spline MPM step, 256^3 nodes, 16,777,216 particles in 64 Gaussian blobs " \
            "(sigma 0.02), int64 fixed point"
-LAUNCHES_PER_STEP = 12  # bin: keys, 3 scans, scatter, 3 in-tile order tiers; p2g; grid update; g2p + copy
-# The timed steps write the new state in bin order (mpm_g2p_binned: one warp per work item), and every
-# SORT_PERIOD-th step with mpm_g2p_sorted, which rewrites the bank-class interleave that the binned steps carry
-# over and wear down; every step bins, scatters, updates and gathers every particle.
+# kernels per step: bin (keys, 3 scans, scatter, 3 in-tile order tiers), P2G, grid update, G2P; the sorted
+# G2P adds the copy of the particles outside the domain
+LAUNCHES_PER_STEP = 11
+# The timed steps gather in place (mpm_g2p: one warp per work item), and every SORT_PERIOD-th step with
+# mpm_g2p_sorted, which moves the particles into bin order and rewrites the bank-class interleave that the
+# in-place steps keep and wear down; every step bins, scatters, updates and gathers every particle.
 SORT_PERIOD = 8
 
 
 # DRAM traffic per particle (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by the
 # particles it processed) from the ncu captures summarised in profiles/p2g_g2p_full_blobs3d_2M.md (P2G and
-# the bin-order G2P of the timed steps) and profiles/stress_volume_full_blobs3d_2M.md (their "_el" stress and
+# the in-place G2P of the timed steps) and profiles/stress_volume_full_blobs3d_2M.md (their "_el" stress and
 # "_vc" volume-channel variants), taken on the 2M-particle sample of the workload (same density) and scaled to
-# a full launch by the particle count.
+# a full launch by the particle count.  The G2P figures are lower bounds on the write side: the sample's
+# output (60 B per particle, 126 MB) is about the size of L2, and what is still dirty in L2 when the kernel
+# ends is not counted.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
-    "p2g": {"bytes_per_particle": 82.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
-            "sha256": "4d85a4db146d1c76c97099163c30654455b97983623695f20db84ccb8b8283bb"
-                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+    "p2g": {"bytes_per_particle": 82.0, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
+            "sha256": "527770cd9816f122c60c21d9eaa081fea12200a94e13ae6d45acaa022bf6cb21"
+                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
                       "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "g2p": {"bytes_per_particle": 74.2, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
-            "sha256": "2177b47c8bc4a3a2e61db227705692fe8476dd3bea09184f43c5134003ea0669"
-                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+    "g2p": {"bytes_per_particle": 56.2, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
+            "sha256": "1935305f617fcd1d0d44150057a9bf6634ca569b6b19efb1587b985ce68aabe7"
+                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
                       "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "p2g_el": {"bytes_per_particle": 126.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
-            "sha256": "4d85a4db146d1c76c97099163c30654455b97983623695f20db84ccb8b8283bb"
-                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+    "p2g_el": {"bytes_per_particle": 126.1, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
+            "sha256": "527770cd9816f122c60c21d9eaa081fea12200a94e13ae6d45acaa022bf6cb21"
+                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
                       "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "g2p_el": {"bytes_per_particle": 166.0, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
-            "sha256": "2177b47c8bc4a3a2e61db227705692fe8476dd3bea09184f43c5134003ea0669"
-                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+    "g2p_el": {"bytes_per_particle": 131.9, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
+            "sha256": "1935305f617fcd1d0d44150057a9bf6634ca569b6b19efb1587b985ce68aabe7"
+                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
                       "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "p2g_vc": {"bytes_per_particle": 89.1, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
-            "sha256": "4d85a4db146d1c76c97099163c30654455b97983623695f20db84ccb8b8283bb"
-                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+    "p2g_vc": {"bytes_per_particle": 88.9, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
+            "sha256": "527770cd9816f122c60c21d9eaa081fea12200a94e13ae6d45acaa022bf6cb21"
+                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
                       "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "g2p_vc": {"bytes_per_particle": 89.9, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
-            "sha256": "2177b47c8bc4a3a2e61db227705692fe8476dd3bea09184f43c5134003ea0669"
-                      "cbeadc6e86f7b993ef096879ff6b3792f4d3b7c43375fb38a8a84d41d3afef19"
+    "g2p_vc": {"bytes_per_particle": 62.6, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
+            "sha256": "1935305f617fcd1d0d44150057a9bf6634ca569b6b19efb1587b985ce68aabe7"
+                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
                       "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
 }
@@ -234,7 +238,7 @@ def run_ours(args, rank, world, local):
         if (k + 1) % SORT_PERIOD == 0:
             sys_.g2p_sorted(stream)
         else:
-            sys_.g2p_binned(stream)
+            sys_.g2p(stream)
         e[4].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -273,13 +277,13 @@ def run_ours(args, rank, world, local):
                 "frac": round((n * 136.0 + touched * 64.0) / (tr_ms * 1e-3) / 1e9 / peak, 4),
                 "bin_ms": round(float(mean_ms[0]), 4)}
 
-    elastic = volume = fused = loop = binned = None
+    elastic = volume = fused = loop = schedules = None
     if args.variant_steps > 0:
         elastic = measure_variant(args, cloud, dev, stream, world, peak, elastic=True, volume=False)
         volume = measure_variant(args, cloud, dev, stream, world, peak, elastic=False, volume=True)
         fused = measure_fused(args, cloud, dev, stream, world, peak, touched, float(mean_ms[0]))
         loop = measure_loop(args, cloud, dev, stream, world, peak)
-        binned = measure_binned(args, cloud, dev, stream, world)
+        schedules = measure_schedules(args, cloud, dev, stream, world)
 
     # end to end through the host entry point (pinned host SoA, copies inside the timed region)
     e2e = None
@@ -315,8 +319,9 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "f32+i64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "particles": n, "grid": grid["n"], "acc": "int64",
                    "scale_log2": grid["scale_log2"], "tile": grid["tile"], "touched_nodes": touched,
-                   "particle_order": "kept in bin order: each step's G2P writes the new state in bin order "
-                                     "(ping-pong), every 8th step with the bank-class interleave",
+                   "particle_order": "in place between sorted steps: every 8th step's G2P moves the particles "
+                                     "into bin order with the bank-class interleave (ping-pong), the others "
+                                     "gather in place",
                    "l2": "inputs larger than L2 (1.07 GB of particle state per step)",
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, mean_ms)},
@@ -324,14 +329,14 @@ def run_ours(args, rank, world, local):
         "cold_step_ms": round(cold_ms, 4) if cold_ms is not None else None,
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps + args.steps // SORT_PERIOD,
         "clocks": clk,
         "advective_step_bound": advective,
         "mls_stress": elastic,
         "volume_channel": volume,
         "fused_step": fused,
         "transfer_loop": loop,
-        "binned_step": binned,
+        "g2p_schedules": schedules,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
@@ -384,7 +389,7 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
         if (k + 1) % SORT_PERIOD == 0:
             es.g2p_sorted(stream)
         else:
-            es.g2p_binned(stream)
+            es.g2p(stream)
         e[4].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -467,10 +472,11 @@ def measure_fused(args, cloud, dev, stream, world, peak, touched, bin_ms):
     return out
 
 
-def measure_binned(args, cloud, dev, stream, world):
+def measure_schedules(args, cloud, dev, stream, world):
     """The G2P schedules on the same workload, after sorted steps have written the
-    bank-class interleave: `steps` steps with mpm_step_binned only, with every eighth
-    step a sorted one (the main region's schedule), and with mpm_step_sorted only."""
+    bank-class interleave, `steps` steps each: in place with every 4th, 8th (the main
+    region's schedule) or 16th step sorted, in place only, in bin order (mpm_step_binned)
+    with every 8th step sorted, in bin order only, and sorted only."""
     import torch
     from material_point_particle_gb300 import _lib as L
     from material_point_particle_gb300.system import MPMSystem
@@ -478,7 +484,11 @@ def measure_binned(args, cloud, dev, stream, world):
     steps = args.variant_steps
     n = cloud["x"].shape[1]
     out = {"unit": UNIT, "steps": steps}
-    for name, period in (("binned", 0), ("sorted_every_8", 8), ("sorted_every_step", 1)):
+    plans = (("in_place_sorted_every_4", "in_place", 4), ("in_place_sorted_every_8", "in_place", 8),
+             ("in_place_sorted_every_16", "in_place", 16), ("in_place", "in_place", 0),
+             ("bin_order_sorted_every_8", "bin_order", 8), ("bin_order", "bin_order", 0),
+             ("sorted_every_step", "in_place", 1))
+    for name, kind, period in plans:
         bs = MPMSystem(cloud["grid"], n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted()
         for _ in range(max(3, args.warmup)):
             bs.step_sorted(stream)
@@ -489,8 +499,10 @@ def measure_binned(args, cloud, dev, stream, world):
         for k in range(steps):
             if period and (k + 1) % period == 0:
                 bs.step_sorted(stream)
-            else:
+            elif kind == "bin_order":
                 bs.step_binned(stream)
+            else:
+                bs.step(stream)
             ev[k + 1].record(stream)
         torch.cuda.synchronize()
         st = bs.status()

@@ -254,7 +254,11 @@ mpm_status mpm_grid_update(const mpm_grid_desc *desc, void *grid_acc, float *gri
  * compressed; that policy is left to the caller).
  * Elastic particles also get F' = (I + dt C') F, each entry as
  * fma(D_k2, F_2l, fma(D_k1, F_1l, fma(D_k0, F_0l, F_kl))) with D = dt*C'.
- * Particles outside the domain are left unchanged.
+ * Particles outside the domain are left unchanged.  In place, the storage
+ * order is kept: an interleave written by an earlier mpm_g2p_sorted carries
+ * over, and particles that change tiles stay where they are stored, so the
+ * next binning finds more index runs (an occasional mpm_g2p_sorted puts the
+ * particles back in bin order).
  * MPM_ACC_EXACT_INT: `grid` is the int64 accumulator; each on-grid particle's v is set
  * to its cell's momentum over its cell's mass, rounded to nearest (ties to even).
  */

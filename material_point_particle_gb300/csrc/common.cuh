@@ -200,15 +200,6 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Per-thread double buffer in shared memory for the NF fields of one
-// particle: field f of stage s of thread t at buf[(s * NF + f) * NT + t]
-// (consecutive threads, consecutive words).
-template <int NF, int NT>
-struct Prefetch {
-    float *buf;
-    __device__ float *at(int stage, int f) const { return buf + (stage * NF + f) * NT + threadIdx.x; }
-};
-
 // The particle record of P2G: x[dim], v[dim], C[dim*dim], m, then with the
 // elastic state F[dim*dim], and vol when the elastic state or the volume
 // channel needs it.

@@ -145,7 +145,7 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
 // read F (and, sorted, vol) of `pid` from global memory and write F'; with
 // the volume channel (VC) the particle's grid-recovered volume fraction is
 // gathered as v is and written to phi.
-template <int DIM, int T, bool SORTED, bool EL, bool VC, typename Rec>
+template <int DIM, int T, bool MOVED, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
                                            uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
                                            float dt, float c4, float &smax) {
@@ -155,7 +155,7 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
 #pragma unroll
     for (int l = 0; l < DIM; ++l) x[l] = rec(l);
     if (!in_tile_x<DIM>(g, x, o, b, f)) {
-        if constexpr (SORTED) copy_particle<DIM>(p, q, pid, dst);
+        if constexpr (MOVED) copy_particle<DIM>(p, q, pid, dst);
         return;
     }
     [[maybe_unused]] float Fo[EL ? DIM * DIM : 1];
@@ -195,31 +195,26 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
 #pragma unroll
         for (int j = 0; j < DIM * DIM; ++j) q.F[j][dst] = Fn[j];
     }
-    if constexpr (SORTED && (EL || VC)) q.vol[dst] = p.vol[pid];
+    if constexpr (MOVED && (EL || VC)) q.vol[dst] = p.vol[pid];
     if constexpr (VC) q.phi[dst] = gather_phi<DIM, T>(sv, hb, w);
     smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
 #pragma unroll
     for (int l = 0; l < DIM; ++l) q.x[l][dst] = __fmaf_rn(dt, vn[l], x[l]);
-    if constexpr (SORTED) {
+    if constexpr (MOVED) {
         const_cast<float *>(q.m)[dst] = rec(DIM);
         if (q.id) q.id[dst] = __float_as_uint(rec(DIM + 1));
     }
 }
 
 
-// Work item as in P2G: one slice of a tile.  The CTA stages the tile's halo
-// of node velocities in shared memory (padded as the P2G accumulators), then
-// every thread gathers its particles from it.
-//
-// In place: thread t takes slice entries t, t + 256, ...; the next one's
-// fields are copied into shared memory (cp.async) while the current one
-// gathers.  Sorted: the slice's x, m and id are copied into shared memory in
-// bin order, the slice is counting-sorted by bank class, and thread t
-// computes the particles that go to places t, t + 256, ... of the
-// interleaved slice, so that its writes are coalesced and its reads of the
-// velocity halo meet few bank conflicts.  A slice of at most 32 particles is
-// one round and keeps bin order.
-template <int DIM, int T, bool SORTED, bool EL, bool VC>
+// The sorted G2P.  Work item as in P2G: one slice of a tile.  The CTA stages
+// the tile's halo of node velocities in shared memory, the slice's x, m and
+// id in bin order, and counting-sorts the slice by bank class; thread t then
+// computes the particles that go to places t, t + 256, ... of the interleaved
+// slice, so that its writes are coalesced and its reads of the velocity halo
+// meet few bank conflicts.  A slice of at most 32 particles is one round and
+// keeps bin order.
+template <int DIM, int T, bool EL, bool VC>
 __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                      const uint32_t *__restrict__ perm,
                                                      const uint32_t *__restrict__ key,
@@ -230,18 +225,17 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
     constexpr int NQ = kSliceParticles / kG2PThreads;
     constexpr int NWARP = kG2PThreads / 32;
     static_assert(NQ * NWARP == 32, "one warp-scan lane per (round, warp)");
-    // in place: per-thread double buffer of x; sorted: x, m, id of the whole slice
-    constexpr int NF = SORTED ? DIM + 2 : DIM;
-    constexpr int BUF = SORTED ? NF * kSliceParticles : 2 * NF * kG2PThreads;
+    constexpr int NF = DIM + 2;  // x, m, id of the whole slice
+    constexpr int BUF = NF * kSliceParticles;
     __shared__ float sv_x[Hl::SIZE], sv_y[Hl::SIZE], sv_z[DIM == 3 ? Hl::SIZE : 1], sv_phi[VC ? Hl::SIZE : 1];
     const VelHalo<DIM, T> sv{sv_x, sv_y, sv_z, sv_phi};
     __shared__ float sbuf[BUF];
     // [(qi, warp)][class], rows padded to 33 words: the scan reads a column
-    __shared__ uint32_t hist[SORTED ? NQ * NWARP * 33 : 1];
-    __shared__ uint32_t cstart[SORTED ? 32 : 1];
+    __shared__ uint32_t hist[NQ * NWARP * 33];
+    __shared__ uint32_t cstart[32];
     // sorted entry e -> bin-order entry, at e + e / 32: the interleaved reads
     // take entries R apart
-    __shared__ uint32_t order[SORTED ? kSliceParticles + kSliceParticles / 32 : 1];
+    __shared__ uint32_t order[kSliceParticles + kSliceParticles / 32];
     const uint32_t lane = lane_id();
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
@@ -260,20 +254,18 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
             const uint32_t r = threadIdx.x + qi * kG2PThreads;
             pids[qi] = r < cnt ? perm[beg + r] : 0u;
         }
-        if constexpr (SORTED) {
-            // the slice's x, m, id in bin order
+        // the slice's x, m, id in bin order
 #pragma unroll
-            for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t r = threadIdx.x + qi * kG2PThreads;
-                if (r < cnt) {
+        for (int qi = 0; qi < NQ; ++qi) {
+            const uint32_t r = threadIdx.x + qi * kG2PThreads;
+            if (r < cnt) {
 #pragma unroll
-                    for (int f = 0; f < DIM; ++f) cp_async4(&sbuf[f * kSliceParticles + r], p.x[f] + pids[qi]);
-                    cp_async4(&sbuf[DIM * kSliceParticles + r], p.m + pids[qi]);
-                    if (p.id) cp_async4(&sbuf[(DIM + 1) * kSliceParticles + r], p.id + pids[qi]);
-                }
+                for (int f = 0; f < DIM; ++f) cp_async4(&sbuf[f * kSliceParticles + r], p.x[f] + pids[qi]);
+                cp_async4(&sbuf[DIM * kSliceParticles + r], p.m + pids[qi]);
+                if (p.id) cp_async4(&sbuf[(DIM + 1) * kSliceParticles + r], p.id + pids[qi]);
             }
-            cp_async_commit();
         }
+        cp_async_commit();
         for (int h = threadIdx.x; h < Hl::NODES; h += blockDim.x) {
             int hx, hy, hz;
             Hl::node(h, hx, hy, hz);
@@ -285,7 +277,7 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
             if (DIM == 3) sv_z[h] = in ? vel[2 * g.nodes + node] : 0.f;
             if (VC) sv_phi[h] = in ? vel[DIM * g.nodes + node] : 0.f;
         }
-        if (SORTED && cnt <= 32u) {
+        if (cnt <= 32u) {
             // one round: the order inside it does not matter, bin order is kept
             cp_async_wait<0>();
             __syncthreads();
@@ -294,7 +286,7 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
                 auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
                 gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
             }
-        } else if constexpr (SORTED) {
+        } else {
             class_order<DIM, T, kG2PThreads>(key, pids, cnt, hist, cstart, order);
             cp_async_wait<0>();
             __syncthreads();
@@ -308,27 +300,6 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
                     gather_one<DIM, T, true, EL, VC>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax);
                 }
             }
-        } else {
-            const Prefetch<NF, kG2PThreads> pf{sbuf};
-            __syncthreads();
-            auto issue = [&](int stage, uint32_t pid) {
-#pragma unroll
-                for (int f = 0; f < DIM; ++f) cp_async4(pf.at(stage, f), p.x[f] + pid);
-            };
-            if (threadIdx.x < cnt) issue(0, pids[0]);
-            cp_async_commit();
-#pragma unroll
-            for (int qi = 0; qi < NQ; ++qi) {
-                const uint32_t r = threadIdx.x + qi * kG2PThreads;
-                if (qi + 1 < NQ && r + kG2PThreads < cnt) issue((qi + 1) & 1, pids[qi + 1]);
-                cp_async_commit();
-                cp_async_wait<1>();
-                if (r < cnt) {
-                    const int stage = qi & 1;
-                    auto rec = [&](int f) { return *pf.at(stage, f); };
-                    gather_one<DIM, T, false, EL, VC>(g, p, q, pids[qi], pids[qi], rec, o, sv, dt, c4, smax);
-                }
-            }
         }
     }
     // non-negative fp32 values order as their bit patterns
@@ -336,13 +307,14 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
     if (lane == 0 && wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
 }
 
-// The sorted G2P without the bank-class interleave: out[j] = the new state of
-// in[perm[j]] (bin order), one warp per work item (the P2G kernel's shape).
-// Each warp stages its tile's velocity halo and, 32 particles a round, its
-// lanes' x, m and id, and each lane gathers its particle (gather_one, the
-// same arithmetic) and writes it at its bin-order place: consecutive lanes,
-// consecutive places, no block barrier.
-template <int DIM, int T, bool EL, bool VC>
+// G2P with one warp per work item (the P2G kernel's shape), in place or in
+// bin order.  Each warp stages its tile's velocity halo and, 32 particles a
+// round, its lanes' x (and m and id for the bin-order output), and each lane
+// gathers its particle (gather_one, the same arithmetic).  In place, the new
+// state overwrites the particle's own entry (the mpm_g2p contract).  In bin
+// order (BINORDER), out[j] = the new state of in[perm[j]]: consecutive lanes
+// write consecutive places.  No block barrier couples the warps.
+template <int DIM, int T, bool BINORDER, bool EL, bool VC>
 __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                        const uint32_t *__restrict__ perm,
                                                        const uint32_t *__restrict__ slices,
@@ -351,7 +323,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
     using Hl = HaloU<DIM, T>;
     constexpr int NW = kP2GThreads / 32;
     constexpr int NCH = DIM + (VC ? 1 : 0);
-    constexpr int NF = DIM + 2;  // staged: x, m, id
+    constexpr int NF = BINORDER ? DIM + 2 : DIM;  // staged: x (and m, id)
     __shared__ float svel[NW][NCH * Hl::SIZE];
     __shared__ float sbuf[NW][2 * NF * 32];
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -376,8 +348,10 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
             const uint32_t pid = perm[beg + r];
 #pragma unroll
             for (int f = 0; f < DIM; ++f) cp_async4(at(stage, f), p.x[f] + pid);
-            cp_async4(at(stage, DIM), p.m + pid);
-            if (p.id) cp_async4(at(stage, DIM + 1), p.id + pid);
+            if constexpr (BINORDER) {
+                cp_async4(at(stage, DIM), p.m + pid);
+                if (p.id) cp_async4(at(stage, DIM + 1), p.id + pid);
+            }
             return pid;
         };
         uint32_t pid_next = lane < cnt ? issue(0, lane) : 0u;
@@ -403,7 +377,8 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
             if (r < cnt) {
                 const int st = stage;
                 auto rec = [&](int f) { return *at(st, f); };
-                gather_one<DIM, T, true, EL, VC>(g, p, q, pid, beg + r, rec, o, sv, dt, c4, smax);
+                gather_one<DIM, T, BINORDER, EL, VC>(g, p, q, pid, BINORDER ? beg + r : pid, rec, o, sv, dt, c4,
+                                                     smax);
             }
             stage ^= 1;
         }
@@ -431,85 +406,65 @@ void launch_copy_rest(const GridP &g, const PartsF &in, const PartsF &out, const
         k_copy_rest<2><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
 }
 
-template <int DIM, int T, bool SORTED, bool EL, bool VC>
+// Where G2P writes the new state: in place (out = in), in bin order
+// (out[j] = new state of in[perm[j]]), or sorted (bin order with the
+// bank-class interleave inside each slice).
+enum G2POut { kInPlace, kBinOrder, kSorted };
+
+template <int DIM, int T, int OUT, bool EL, bool VC>
 void launch_g2p_t(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w, float dt,
                   const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
-    const int blocks = dev.sms * (1024 / kG2PThreads);
-    k_g2p<DIM, T, SORTED, EL, VC><<<blocks, kG2PThreads, 0, st>>>(g, in, out, vel, w.perm, w.key, w.slices, w.start,
-                                                                   w.status, dt, c4);
-    if constexpr (SORTED) k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
+    if constexpr (OUT == kSorted)
+        k_g2p<DIM, T, EL, VC><<<dev.sms * (1024 / kG2PThreads), kG2PThreads, 0, st>>>(
+            g, in, out, vel, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
+    else
+        k_g2p_w<DIM, T, OUT == kBinOrder, EL, VC><<<dev.sms * 4, kP2GThreads, 0, st>>>(
+            g, in, out, vel, w.perm, w.slices, w.start, w.status, dt, c4);
+    if constexpr (OUT != kInPlace) k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
 }
 
-template <int DIM, int T, bool SORTED>
+template <int DIM, int T, int OUT>
 void launch_g2p_dt(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w, float dt,
                    const DeviceInfo &dev, cudaStream_t st) {
     const bool el = in.F[0] != nullptr;
     if (el && g.vc)
-        launch_g2p_t<DIM, T, SORTED, true, true>(g, vel, in, out, w, dt, dev, st);
+        launch_g2p_t<DIM, T, OUT, true, true>(g, vel, in, out, w, dt, dev, st);
     else if (el)
-        launch_g2p_t<DIM, T, SORTED, true, false>(g, vel, in, out, w, dt, dev, st);
+        launch_g2p_t<DIM, T, OUT, true, false>(g, vel, in, out, w, dt, dev, st);
     else if (g.vc)
-        launch_g2p_t<DIM, T, SORTED, false, true>(g, vel, in, out, w, dt, dev, st);
+        launch_g2p_t<DIM, T, OUT, false, true>(g, vel, in, out, w, dt, dev, st);
     else
-        launch_g2p_t<DIM, T, SORTED, false, false>(g, vel, in, out, w, dt, dev, st);
+        launch_g2p_t<DIM, T, OUT, false, false>(g, vel, in, out, w, dt, dev, st);
 }
 
-template <bool SORTED>
+template <int OUT>
 mpm_status launch_g2p_any(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
                           float dt, const DeviceInfo &dev, cudaStream_t st) {
     static_assert(MPM_ST_MAX_SPEED == MPM_ST_WORK_G2P + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
     if (g.dim == 3 && g.T == 4)
-        launch_g2p_dt<3, 4, SORTED>(g, vel, in, out, w, dt, dev, st);
+        launch_g2p_dt<3, 4, OUT>(g, vel, in, out, w, dt, dev, st);
     else if (g.dim == 2 && g.T == 8)
-        launch_g2p_dt<2, 8, SORTED>(g, vel, in, out, w, dt, dev, st);
+        launch_g2p_dt<2, 8, OUT>(g, vel, in, out, w, dt, dev, st);
     else
         return MPM_E_ARG;
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
-}
-
-template <int DIM, int T>
-void launch_g2p_binned_dt(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
-                          float dt, const DeviceInfo &dev, cudaStream_t st) {
-    const float c4 = 4.0f * g.inv_dx;
-    const int blocks = dev.sms * 4;
-    const bool el = in.F[0] != nullptr;
-#define MPM_G2P_W(EL_, VC_)                                                                                    \
-    k_g2p_w<DIM, T, EL_, VC_><<<blocks, kP2GThreads, 0, st>>>(g, in, out, vel, w.perm, w.slices, w.start, w.status, \
-                                                            dt, c4)
-    if (el && g.vc)
-        MPM_G2P_W(true, true);
-    else if (el)
-        MPM_G2P_W(true, false);
-    else if (g.vc)
-        MPM_G2P_W(false, true);
-    else
-        MPM_G2P_W(false, false);
-#undef MPM_G2P_W
-    k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
 }
 
 mpm_status launch_g2p_binned(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
                              float dt, const DeviceInfo &dev, cudaStream_t st) {
-    cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
-    if (g.dim == 3 && g.T == 4)
-        launch_g2p_binned_dt<3, 4>(g, vel, in, out, w, dt, dev, st);
-    else if (g.dim == 2 && g.T == 8)
-        launch_g2p_binned_dt<2, 8>(g, vel, in, out, w, dt, dev, st);
-    else
-        return MPM_E_ARG;
-    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
+    return launch_g2p_any<kBinOrder>(g, vel, in, out, w, dt, dev, st);
 }
 
 mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,
                       const DeviceInfo &dev, cudaStream_t st) {
-    return launch_g2p_any<false>(g, vel, p, p, w, dt, dev, st);
+    return launch_g2p_any<kInPlace>(g, vel, p, p, w, dt, dev, st);
 }
 
 mpm_status launch_g2p_sorted(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
                              float dt, const DeviceInfo &dev, cudaStream_t st) {
-    return launch_g2p_any<true>(g, vel, in, out, w, dt, dev, st);
+    return launch_g2p_any<kSorted>(g, vel, in, out, w, dt, dev, st);
 }
 
 // --------------------------------------------------------------------------

@@ -172,12 +172,15 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
         };
         uint32_t bad = 0;
         const uint32_t rounds = (cnt + 31) / 32;
+        // perm read one round ahead of its use, so no round waits on it
+        uint32_t pid_next = lane + 32 < cnt ? perm[beg + lane + 32] : 0u;
         if (lane < cnt) issue(0, perm[beg + lane]);
         cp_async_commit();
         int stage = 0;
         for (uint32_t q = 0; q < rounds; ++q) {
             const uint32_t r = q * 32 + lane;
-            if (q + 1 < rounds && r + 32 < cnt) issue(stage ^ 1, perm[beg + r + 32]);
+            if (q + 1 < rounds && r + 32 < cnt) issue(stage ^ 1, pid_next);
+            pid_next = r + 64 < cnt ? perm[beg + r + 64] : 0u;
             cp_async_commit();
             cp_async_wait<1>();
             if (r < cnt) {

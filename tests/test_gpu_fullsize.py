@@ -5,14 +5,15 @@
   tolerance in float-atomic mode).
 - The clustered blobs (16,777,216 particles, 256^3 nodes) in the launch
   configuration the benchmark times (three sorted warm-up steps, then
-  bin-order steps with a sorted one every eighth: one of each checked),
+  in-place steps with a sorted one every eighth: one of each checked, and a
+  bin-order step),
   and the sphere (67,108,864 particles, 512^3 nodes) from its generated order:
   one step checked piece by piece: the whole permutation against the oracle's
   binning; the P2G grid through the exact conservation identities and, on
   sampled tiles, against the oracle's P2G of the particles that reach them;
   the whole velocity grid where there is mass against the oracle's grid update
-  of the GPU's accumulators; and the sorted G2P on sampled particles (found
-  through their ids) against the oracle's G2P.
+  of the GPU's accumulators; and the G2P on sampled particles (found through
+  their ids) against the oracle's G2P.
 - The blobs as the benchmark's elastic row times them (the Neo-Hookean state),
   checked the same way with the stress fold and the F update.
 - The blobs stepped by the fused kernel: the new state on sampled particles,
@@ -87,10 +88,10 @@ def _quantities(grid, x, v, m):
     return Q
 
 
-def _check_step(sys, grid, n, n_tiles_sampled=6, binned=False):
-    """One sorted (or, with `binned`, bin-order) step of `sys`, checked piece by
-    piece against the oracle (with the stress fold and the F update when the
-    particles are elastic)."""
+def _check_step(sys, grid, n, n_tiles_sampled=6, out="sorted"):
+    """One step of `sys` whose G2P writes `out` ("sorted", "bin_order" or
+    "in_place"), checked piece by piece against the oracle (with the stress fold
+    and the F update when the particles are elastic)."""
     x0, v0, C0 = sys.state()
     m0 = sys.m.cpu().numpy()
     ids0 = sys.id.cpu().numpy().astype(np.int64)
@@ -144,18 +145,18 @@ def _check_step(sys, grid, n, n_tiles_sampled=6, binned=False):
     del acc, ovel
     assert not sys.acc.any().item(), "grid update must leave the accumulators zero"
 
-    # sorted (or binned) G2P: sampled in-domain particles, found through their ids
-    if binned:
-        sys.g2p_binned()
-    else:
-        sys.g2p_sorted()
+    # G2P: sampled in-domain particles, found through their ids
+    {"sorted": sys.g2p_sorted, "bin_order": sys.g2p_binned, "in_place": sys.g2p}[out]()
     x1, v1, C1 = sys.state()
     ids1 = sys.id.cpu().numpy().astype(np.int64)
     # the advective step bound: the largest term over the moved particles (all in the domain)
     speed = np.array([sys.status()[L.ST_MAX_SPEED]], np.uint32).view(np.float32)[0]
-    assert speed == O.advective_speed(grid["dim"], grid["dx"], v1[:, :valid], C1[:, :valid])
-    if binned:   # bin order: out[j] = in[perm[j]]
+    mv = inside if out == "in_place" else np.arange(valid)   # where the moved particles now sit
+    assert speed == O.advective_speed(grid["dim"], grid["dx"], v1[:, mv], C1[:, mv])
+    if out == "bin_order":   # out[j] = in[perm[j]]
         assert np.array_equal(ids1, ids0[perm.astype(np.int64)])
+    if out == "in_place":
+        assert np.array_equal(ids1, ids0)
     where = np.empty(n, dtype=np.int64)
     where[ids1] = np.arange(n)
     samp = inside[(W.Stream(32, 32).bits(20000) % np.uint64(inside.size)).astype(np.int64)]
@@ -173,8 +174,9 @@ def _check_step(sys, grid, n, n_tiles_sampled=6, binned=False):
 
 
 def test_blobs_full_size_bench_configuration():
-    """The benchmark's schedule: three sorted warm-up steps, then bin-order steps
-    with a sorted one every eighth; a binned step and a sorted step checked."""
+    """The benchmark's schedule: three sorted warm-up steps, then in-place steps
+    with a sorted one every eighth; an in-place step and a sorted step checked,
+    and a bin-order step between them."""
     cloud = W.blobs3d()
     grid = cloud["grid"]
     n = cloud["x"].shape[1]
@@ -184,9 +186,9 @@ def test_blobs_full_size_bench_configuration():
     for _ in range(3):                       # the warm-up steps
         sys.step_sorted()
     for _ in range(5):
-        sys.step_binned()
-    _check_step(sys, grid, n, n_tiles_sampled=3, binned=True)
-    sys.step_binned()
+        sys.step()
+    _check_step(sys, grid, n, n_tiles_sampled=3, out="in_place")
+    _check_step(sys, grid, n, n_tiles_sampled=2, out="bin_order")
     _check_step(sys, grid, n, n_tiles_sampled=3)
 
 
