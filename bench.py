@@ -184,6 +184,16 @@ def workload(W, n_particles, n_blobs=64):
     return W.blobs3d(n_particles=n_particles, n_blobs=n_blobs)
 
 
+def inputs_sha256(cloud) -> str:
+    """SHA-256 of the generated particle arrays (x, v, C, m as stored fp32, in that order): the inputs the
+    GPU and the oracle are given."""
+    import hashlib
+    h = hashlib.sha256()
+    for k in ("x", "v", "C", "m"):
+        h.update(np.ascontiguousarray(cloud[k]).tobytes())
+    return h.hexdigest()
+
+
 def run_ours(args, rank, world, local):
     import torch
     from material_point_particle_gb300 import _lib as L
@@ -195,6 +205,7 @@ def run_ours(args, rank, world, local):
     cloud = workload(W, args.particles, args.blobs)
     grid = cloud["grid"]
     n = cloud["x"].shape[1]
+    inputs_sha = inputs_sha256(cloud)
     sys_ = MPMSystem(grid, n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted()
     # touched nodes of the initial state (algorithmic grid bytes)
     sys_.bin()
@@ -246,6 +257,7 @@ def run_ours(args, rank, world, local):
     barrier(world, dev)
     total_ms = t_start.elapsed_time(t_end)
     parts_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev])
+    median_ms = aggregate_max(float(np.median(parts_ms.sum(axis=1))), world, dev)
     st = sys_.status()
     assert st[L.ST_FLAGS] == 0, f"status flags after timing {st[:8]}"
     ms_step = aggregate_max(total_ms / args.steps, world, dev)
@@ -309,9 +321,10 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": n * 17 * 4, "d2h_bytes_per_step": n * 17 * 4,
                "ms_per_step": round(e2e_ms, 4)}
 
-    cpu = None
+    cpu = cpu_omp = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cloud, sample=args.cpu_sample)
+        cpu_omp = cpu_baseline_omp(cloud, particles=args.cpu_omp_particles)
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -323,9 +336,11 @@ def run_ours(args, rank, world, local):
                                      "into bin order with the bank-class interleave (ping-pong), the others "
                                      "gather in place",
                    "l2": "inputs larger than L2 (1.07 GB of particle state per step)",
+                   "inputs_sha256": inputs_sha,
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, mean_ms)},
         "transfer": transfer,
+        "median_ms_per_step": round(median_ms, 4),
         "cold_step_ms": round(cold_ms, 4) if cold_ms is not None else None,
         "roofline": roofline,
         "e2e": e2e,
@@ -340,6 +355,7 @@ def run_ours(args, rank, world, local):
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
+        out["cpu_baseline_openmp"] = cpu_omp
     return out
 
 
@@ -590,9 +606,58 @@ def cpu_baseline(cloud, sample: int):
     t0 = time.perf_counter()
     O.step_fixed(grid, x, v, C, m)
     dt = time.perf_counter() - t0
-    return {"value": round(sample / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": round(sample / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
             "sample": f"first {sample} particles (storage order) of the same workload, full 256^3 grid, "
                       f"one full oracle step (bin, P2G, grid update, G2P): {dt:.2f} s"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type) and its core count."""
+    import platform
+    import subprocess
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not name:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    name = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return f"{name or platform.machine()}, {os.cpu_count()} cores"
+
+
+def cpu_baseline_omp(cloud, particles: int):
+    """The multi-core CPU baseline (OpenMP: the oracle's arithmetic, private per-thread int64 grids merged by
+    integer add, outputs in bin order) on all host cores: one warm-up and two timed full steps of the first
+    `particles` particles (all by default) on the full grid."""
+    from oracle import cpu_omp
+    if not cpu_omp.available():
+        return {"unavailable": "the host compiler has no OpenMP"}
+    grid = cloud["grid"]
+    n = cloud["x"].shape[1] if particles <= 0 else min(particles, cloud["x"].shape[1])
+    state = {k: np.ascontiguousarray(cloud[k][..., :n]) for k in ("x", "v", "C", "m")}
+    bufs = [cpu_omp.buffers(grid, n), cpu_omp.buffers(grid, n)]   # ping-pong, as the GPU path
+    times = []
+    for k in range(3):
+        t0 = time.perf_counter()
+        state = cpu_omp.step_fixed(grid, state["x"], state["v"], state["C"], state["m"], out=bufs[k % 2])
+        times.append(time.perf_counter() - t0)
+    dt = min(times[1:])
+    phases = cpu_omp.phase_seconds()
+    return {"value": round(n / dt, 1), "unit": UNIT, "cores": cpu_omp.max_threads(), "kind": "openmp",
+            "cpu": cpu_model(),
+            "sample": f"{n} particles of the same workload, full 256^3 grid, one full step (bin, P2G with "
+                      f"private per-thread int64 grids merged by integer add, grid update, G2P; outputs in bin "
+                      f"order), best of 2 after a warm-up: {dt:.3f} s", "phases_s": phases}
 
 
 def run_reference(args, rank, world):
@@ -633,6 +698,8 @@ def main():
     ap.add_argument("--blobs", type=int, default=64, help="blobs (64 = the workload; fewer keeps the density "
                     "of a smaller sample, for profiling)")
     ap.add_argument("--cpu-sample", type=int, default=2097152)
+    ap.add_argument("--cpu-omp-particles", type=int, default=0,
+                    help="particles of the workload the OpenMP CPU baseline steps (0: all)")
     ap.add_argument("--ref-sample", type=int, default=262144)
     ap.add_argument("--variant-steps", type=int, default=50,
                     help="timed steps of the same workload with the Neo-Hookean stress, and with the "
