@@ -1,119 +1,15 @@
-// grid_g2p.cu -- grid update and grid-to-particle gather.
+// grid_g2p.cu -- grid-to-particle gather.
 //
-// Grid update (implementation guide, section 2.1 item 1 and section 3.3.2):
-// mass-normalise, add gravity (rule 7: a solver parameter), apply the
-// velocity-form boundary sign test; each accumulator is read once and written
-// back to zero (section 2.1, "the grid clear can ride along"; rule 4).  Only
-// node blocks next to a tile that holds particles are visited.
-//
-// G2P (section 1: a gather, every particle writes only itself; section 3.1
+// G2P (implementation guide, section 1: a gather, every particle writes only itself; section 3.1
 // Part 1 and 3.3.2 "gather d and D (= B*4)"): new velocity, APIC affine matrix
 // C = B * 4/dx^2 in cell units, advection x += dt v; for elastic particles
 // also F <- (I + dt C) F (section 3.3.2; stress.cuh).
-#include <type_traits>
-
 #include "common.cuh"
 #include "gather.cuh"
 #include "internal.h"
 #include "stress.cuh"
 
 namespace mpm {
-
-template <typename AccT>
-__device__ __forceinline__ float acc_to_float(AccT v) {
-    if constexpr (sizeof(AccT) == 8)
-        return __ll2float_rn((long long)v);
-    else if constexpr (std::is_same<AccT, float>::value)
-        return v;
-    else
-        return __int2float_rn((int)v);
-}
-
-template <int DIM, int T, typename AccT, bool VC>
-__global__ void k_grid_update(GridP g, AccT *__restrict__ acc, float *__restrict__ vel, float dtg0, float dtg1,
-                              float dtg2, const uint32_t *__restrict__ count) {
-    constexpr int NCH = DIM + 1 + (VC ? 1 : 0);
-    constexpr int NB = DIM == 3 ? T * T * T : T * T;
-    const uint32_t lane = lane_id();
-    const float dtg[3] = {dtg0, dtg1, dtg2};
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < g.nblocks; blk += warps) {
-        const int bx = (int)(blk % g.nb[0]);
-        const int by = (int)((blk / g.nb[0]) % g.nb[1]);
-        const int bz = DIM == 3 ? (int)(blk / ((int64_t)g.nb[0] * g.nb[1])) : 0;
-        // the block's nodes receive shares only from tiles (b - delta), delta in {0,1}^dim
-        bool act = false;
-        if (lane < (1u << DIM)) {
-            const int tx = bx - (int)(lane & 1), ty = by - (int)((lane >> 1) & 1), tz = bz - (int)((lane >> 2) & 1);
-            if (tx >= 0 && ty >= 0 && tz >= 0 && tx < g.nt[0] && ty < g.nt[1] && (DIM == 2 || tz < g.nt[2]))
-                act = count[((int64_t)tz * g.nt[1] + ty) * g.nt[0] + tx] > 0;
-        }
-        if (!__any_sync(0xFFFFFFFFu, act)) continue;
-        for (int r = lane; r < NB; r += 32) {
-            const int gx = bx * T + r % T, gy = by * T + (r / T) % T, gz = DIM == 3 ? bz * T + r / (T * T) : 0;
-            if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
-            const int64_t node = node_index(g, gx, gy, gz);
-            AccT a[NCH];
-            bool any = false;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                a[c] = acc[c * g.nodes + node];
-                any = any || a[c] != (AccT)0;
-            }
-            const int idx[3] = {gx, gy, gz};
-            const float M = acc_to_float(a[0]);
-#pragma unroll
-            for (int l = 0; l < DIM; ++l) {
-                float v = 0.f;
-                if (M != 0.f) {
-                    v = __fadd_rn(__fdiv_rn(acc_to_float(a[1 + l]), M), dtg[l]);
-                    if ((idx[l] < g.boundary && v < 0.f) || (idx[l] > g.n[l] - 1 - g.boundary && v > 0.f)) v = 0.f;
-                }
-                vel[l * g.nodes + node] = v;
-            }
-            // volume fraction: the sum in cells, the fixed-point scale removed
-            if constexpr (VC) vel[DIM * g.nodes + node] = __fmul_rn(acc_to_float(a[DIM + 1]), g.inv_S);
-            if (any) {
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) acc[c * g.nodes + node] = (AccT)0;
-            }
-        }
-    }
-}
-
-template <int DIM, int T, typename AccT>
-void launch_grid_update_t(const GridP &g, void *grid_acc, float *vel, const float dtg[3], const WsView &w, int blocks,
-                          cudaStream_t st) {
-    if (g.vc)
-        k_grid_update<DIM, T, AccT, true><<<blocks, 256, 0, st>>>(g, (AccT *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
-                                                                  w.count);
-    else
-        k_grid_update<DIM, T, AccT, false><<<blocks, 256, 0, st>>>(g, (AccT *)grid_acc, vel, dtg[0], dtg[1], dtg[2],
-                                                                   w.count);
-}
-
-mpm_status launch_grid_update(const GridP &g, void *grid_acc, float *vel, const float dtg[3], const WsView &w,
-                              const DeviceInfo &dev, cudaStream_t st) {
-    const int blocks = dev.sms * 8;
-    if (g.dim == 3 && g.T == 4) {
-        if (g.acc_mode == MPM_ACC_I64)
-            launch_grid_update_t<3, 4, long long>(g, grid_acc, vel, dtg, w, blocks, st);
-        else if (g.acc_mode == MPM_ACC_I32)
-            launch_grid_update_t<3, 4, int>(g, grid_acc, vel, dtg, w, blocks, st);
-        else
-            launch_grid_update_t<3, 4, float>(g, grid_acc, vel, dtg, w, blocks, st);
-    } else if (g.dim == 2 && g.T == 8) {
-        if (g.acc_mode == MPM_ACC_I64)
-            launch_grid_update_t<2, 8, long long>(g, grid_acc, vel, dtg, w, blocks, st);
-        else if (g.acc_mode == MPM_ACC_I32)
-            launch_grid_update_t<2, 8, int>(g, grid_acc, vel, dtg, w, blocks, st);
-        else
-            launch_grid_update_t<2, 8, float>(g, grid_acc, vel, dtg, w, blocks, st);
-    } else {
-        return MPM_E_ARG;
-    }
-    return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
-}
 
 // --------------------------------------------------------------------------
 // Whole-state copy of particle `src` of p to entry `dst` of q.
