@@ -253,23 +253,33 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
 // reach (the blocks the grid update visits), every channel.
 template <int DIM, int T>
 __global__ void k_clear_blocks(GridP g, long long *__restrict__ acc, const uint32_t *__restrict__ count) {
-    constexpr int NB = DIM == 3 ? T * T * T : T * T;
+    constexpr int ROWS = DIM == 3 ? T * T : T;  // grid rows of one block row
     const uint32_t lane = lane_id();
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < g.nblocks; blk += warps) {
-        const int bx = (int)(blk % g.nb[0]);
-        const int by = (int)((blk / g.nb[0]) % g.nb[1]);
-        const int bz = DIM == 3 ? (int)(blk / ((int64_t)g.nb[0] * g.nb[1])) : 0;
+    // work item: a brick of 32 nodes in x (one per lane) by one row of node blocks, as the grid update
+    const uint32_t runs = ((uint32_t)g.n[0] + 31) / 32, nb1 = (uint32_t)g.nb[1];
+    const uint32_t items = runs * nb1 * (DIM == 3 ? (uint32_t)g.nb[2] : 1u);
+    const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+    for (uint32_t it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+        const uint32_t rest = it / runs;
+        const int gx = (int)(it - rest * runs) * 32 + (int)lane;
+        const int by = DIM == 3 ? (int)(rest % nb1) : (int)rest;
+        const int bz = DIM == 3 ? (int)(rest / nb1) : 0;
+        // the node's block received shares only from tiles (block - delta), delta in {0,1}^dim
         bool act = false;
-        if (lane < (1u << DIM)) {
-            const int tx = bx - (int)(lane & 1), ty = by - (int)((lane >> 1) & 1), tz = bz - (int)((lane >> 2) & 1);
-            if (tx >= 0 && ty >= 0 && tz >= 0 && tx < g.nt[0] && ty < g.nt[1] && (DIM == 2 || tz < g.nt[2]))
-                act = count[((int64_t)tz * g.nt[1] + ty) * g.nt[0] + tx] > 0;
+        if (gx < g.n[0]) {
+            const int bx = gx / T;
+#pragma unroll
+            for (int d = 0; d < (1 << DIM); ++d) {
+                const int tx = bx - (d & 1), ty = by - ((d >> 1) & 1), tz = bz - ((d >> 2) & 1);
+                if (tx >= 0 && ty >= 0 && tz >= 0 && tx < g.nt[0] && ty < g.nt[1] && (DIM == 2 || tz < g.nt[2]))
+                    act = act || count[((int64_t)tz * g.nt[1] + ty) * g.nt[0] + tx] > 0;
+            }
         }
-        if (!__any_sync(0xFFFFFFFFu, act)) continue;
-        for (int r = lane; r < NB; r += 32) {
-            const int gx = bx * T + r % T, gy = by * T + (r / T) % T, gz = DIM == 3 ? bz * T + r / (T * T) : 0;
-            if (gx >= g.n[0] || gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
+        if (!act) continue;
+#pragma unroll 4
+        for (int r = 0; r < ROWS; ++r) {
+            const int gy = by * T + r % T, gz = DIM == 3 ? bz * T + r / T : 0;
+            if (gy >= g.n[1] || (DIM == 3 && gz >= g.n[2])) continue;
             const int64_t node = node_index(g, gx, gy, gz);
 #pragma unroll
             for (int c = 0; c <= DIM; ++c) acc[c * g.nodes + node] = 0;
