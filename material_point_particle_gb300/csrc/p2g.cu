@@ -100,14 +100,14 @@ __device__ __forceinline__ SliceMeta slice_meta(const uint32_t *slices, const ui
 
 // One warp per work item (a slice of at most 1024 binned particles of one
 // tile), so no CTA barrier couples the warps: each warp owns a compact halo
-// of the tile's (T+2)^dim nodes x (dim+1) int32 accumulators and a double
-// buffer for its lanes' positions.  Per item: 32 particles a round, the next
-// round's positions copied into shared memory (cp.async) while the current
-// one scatters, and each lane's other fields (v, C, m, ...) loaded into
-// registers at the start of its round: the shared-memory pipe, which the
-// scatter's atomics keep busy, carries only what the stencil needs early
-// (with the elastic state the whole record is staged).
-// Every 512 particles and at the end the warp adds each
+// of the tile's (T+2)^dim nodes x (dim+1) int32 accumulators.  Per item: 32
+// particles a round; each lane loads its next particle's position into
+// registers while the current one scatters, and the rest of the record
+// (v, C, m, ...) at the start of its round, so the shared-memory pipe, which
+// the scatter's atomics keep busy, carries nothing else.  With the elastic
+// state (two blocks per SM) the whole record is copied into a per-warp double
+// buffer in shared memory (cp.async) a round ahead instead.  Every 512
+// particles and at the end the warp adds each
 // nonzero halo entry to the grid with one global atomic and clears it
 // (neighbouring tiles overlap on the halo, so the flush adds).  Particles
 // stored in bank-class interleaved order (the sorted G2P) put the 32 lanes of
@@ -125,10 +125,10 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
     constexpr int NCH = St::NC + (VC ? 1 : 0);  // accumulator channels
     constexpr int HW = NCH * Hl::NODES;         // halo words per warp
     __shared__ __align__(16) int32_t shalo[kP2GWarps][HW];
-    // staged fields: x, or with the elastic state the whole record (at two blocks per SM the
-    // F loads' latency would not hide behind other warps)
-    constexpr int NS = EL ? Fl::NF : DIM;
-    __shared__ float sbuf[kP2GWarps][2 * NS * 32];
+    // with the elastic state the whole record is staged in shared memory (at two blocks per SM
+    // register loads' latency would not hide behind other warps); otherwise nothing is
+    constexpr int NS = EL ? Fl::NF : 1;
+    __shared__ float sbuf[kP2GWarps][EL ? 2 * NS * 32 : 1];
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     int32_t *wh = shalo[warp];
@@ -179,35 +179,54 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
         };
         uint32_t bad = 0;
         const uint32_t rounds = (cnt + 31) / 32;
-        // perm read one round ahead of its use, so no round waits on it
+        // the int32 halo accumulators are flushed every 16 rounds: at most 512
+        // shares of magnitude below 2^22 reach one entry between two flushes
+        // perm is read one round ahead of its use, so no round waits on it
         uint32_t pid = lane < cnt ? perm[beg + lane] : 0u;
         uint32_t pid_next = lane + 32 < cnt ? perm[beg + lane + 32] : 0u;
-        if (lane < cnt) issue(0, pid);
-        cp_async_commit();
-        int stage = 0;
-        for (uint32_t q = 0; q < rounds; ++q) {
-            const uint32_t r = q * 32 + lane;
-            if (q + 1 < rounds && r + 32 < cnt) issue(stage ^ 1, pid_next);
-            const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
-            // the record's other fields, straight into registers
-            float rest[Fl::NF > NS ? Fl::NF - NS : 1];
-            if (r < cnt) {
+        if constexpr (!EL) {
+            // the positions in registers a round ahead, the rest of the record at the start of its round
+            float xc[DIM], xn[DIM];
 #pragma unroll
-                for (int f = NS; f < Fl::NF; ++f) rest[f - NS] = Fl::src(p, f)[pid];
+            for (int l = 0; l < DIM; ++l) xc[l] = lane < cnt ? p.x[l][pid] : 0.f;
+            for (uint32_t q = 0; q < rounds; ++q) {
+                const uint32_t r = q * 32 + lane;
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) xn[l] = r + 32 < cnt ? p.x[l][pid_next] : 0.f;
+                const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
+                if (r < cnt) {
+                    float rest[Fl::NF - DIM];
+#pragma unroll
+                    for (int f = DIM; f < Fl::NF; ++f) rest[f - DIM] = Fl::src(p, f)[pid];
+                    auto rec = [&](int f) { return f < DIM ? xc[f] : rest[f - DIM]; };
+                    if (!scatter_fixed<DIM, T, Hl, EL, VC>(g, rec, o, halo, sp, degenerate)) ++bad;
+                }
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) xc[l] = xn[l];
+                pid = pid_next;
+                pid_next = pid_after;
+                if ((q + 1) % 16 == 0 && q + 1 < rounds) flush();
             }
+        } else {
+            // the whole record copied into shared memory (cp.async) a round ahead
+            if (lane < cnt) issue(0, pid);
             cp_async_commit();
-            cp_async_wait<1>();
-            if (r < cnt) {
-                const int st = stage;
-                auto rec = [&](int f) { return f < NS ? *at(st, f) : rest[f - NS]; };
-                if (!scatter_fixed<DIM, T, Hl, EL, VC>(g, rec, o, halo, sp, degenerate)) ++bad;
+            int stage = 0;
+            for (uint32_t q = 0; q < rounds; ++q) {
+                const uint32_t r = q * 32 + lane;
+                if (q + 1 < rounds && r + 32 < cnt) issue(stage ^ 1, pid_next);
+                const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
+                cp_async_commit();
+                cp_async_wait<1>();
+                if (r < cnt) {
+                    const int st = stage;
+                    auto rec = [&](int f) { return *at(st, f); };
+                    if (!scatter_fixed<DIM, T, Hl, EL, VC>(g, rec, o, halo, sp, degenerate)) ++bad;
+                }
+                stage ^= 1;
+                pid_next = pid_after;
+                if ((q + 1) % 16 == 0 && q + 1 < rounds) flush();
             }
-            stage ^= 1;
-            pid = pid_next;
-            pid_next = pid_after;
-            // int32 halo accumulators: at most 512 shares of magnitude below
-            // 2^22 reach one entry between two flushes
-            if ((q + 1) % 16 == 0 && q + 1 < rounds) flush();
         }
         flush();
         bad = __reduce_add_sync(0xFFFFFFFFu, bad);
