@@ -204,12 +204,15 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
 }
 
 // G2P with one warp per work item (the P2G kernel's shape), in place or in
-// bin order.  Each warp stages its tile's velocity halo and, 32 particles a
-// round, its lanes' x (and m and id for the bin-order output), and each lane
-// gathers its particle (gather_one, the same arithmetic).  In place, the new
-// state overwrites the particle's own entry (the mpm_g2p contract).  In bin
-// order (BINORDER), out[j] = the new state of in[perm[j]]: consecutive lanes
-// write consecutive places.  No block barrier couples the warps.
+// bin order.  Each warp stages its tile's velocity halo in shared memory and
+// takes 32 particles a round; each lane gathers its particle (gather_one, the
+// same arithmetic).  In place, the new state overwrites the particle's own
+// entry (the mpm_g2p contract), and each lane loads its next particle's
+// position into registers while the current one gathers.  In bin order
+// (BINORDER), out[j] = the new state of in[perm[j]]: x, m and id are copied
+// into a per-warp double buffer in shared memory a round ahead, and
+// consecutive lanes write consecutive places.  No block barrier couples the
+// warps.
 template <int DIM, int T, bool BINORDER, bool EL, bool VC>
 __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF q, const float *__restrict__ vel,
                                                        const uint32_t *__restrict__ perm,
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
     constexpr int NCH = DIM + (VC ? 1 : 0);
     constexpr int NF = BINORDER ? DIM + 2 : DIM;  // staged: x (and m, id)
     __shared__ float svel[NW][NCH * Hl::SIZE];
-    __shared__ float sbuf[NW][2 * NF * 32];
+    __shared__ float sbuf[NW][BINORDER ? 2 * NF * 32 : 1];
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     float *vw = svel[warp];
     const VelHalo<DIM, T> sv{vw, vw + Hl::SIZE, DIM == 3 ? vw + 2 * Hl::SIZE : vw, VC ? vw + DIM * Hl::SIZE : vw};
@@ -250,8 +253,11 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
             }
             return pid;
         };
-        uint32_t pid_next = lane < cnt ? issue(0, lane) : 0u;
-        cp_async_commit();
+        uint32_t pid_next = 0u;
+        if constexpr (BINORDER) {
+            pid_next = lane < cnt ? issue(0, lane) : 0u;
+            cp_async_commit();
+        }
         for (int h = lane; h < Hl::NODES; h += 32) {
             int hx, hy, hz;
             Hl::node(h, hx, hy, hz);
@@ -263,20 +269,44 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
         }
         __syncwarp();
         const uint32_t rounds = (cnt + 31) / 32;
-        int stage = 0;
-        for (uint32_t qr = 0; qr < rounds; ++qr) {
-            const uint32_t r = qr * 32 + lane;
-            const uint32_t pid = pid_next;
-            if (qr + 1 < rounds && r + 32 < cnt) pid_next = issue(stage ^ 1, r + 32);
-            cp_async_commit();
-            cp_async_wait<1>();
-            if (r < cnt) {
-                const int st = stage;
-                auto rec = [&](int f) { return *at(st, f); };
-                gather_one<DIM, T, BINORDER, EL, VC>(g, p, q, pid, BINORDER ? beg + r : pid, rec, o, sv, dt, c4,
-                                                     smax);
+        if constexpr (!BINORDER) {
+            // in place: positions in registers a round ahead, perm two rounds ahead
+            uint32_t pid = lane < cnt ? perm[beg + lane] : 0u;
+            pid_next = lane + 32 < cnt ? perm[beg + lane + 32] : 0u;
+            float xc[DIM], xn[DIM];
+#pragma unroll
+            for (int l = 0; l < DIM; ++l) xc[l] = lane < cnt ? p.x[l][pid] : 0.f;
+            for (uint32_t qr = 0; qr < rounds; ++qr) {
+                const uint32_t r = qr * 32 + lane;
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) xn[l] = r + 32 < cnt ? p.x[l][pid_next] : 0.f;
+                const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
+                if (r < cnt) {
+                    auto rec = [&](int f) { return xc[f]; };
+                    gather_one<DIM, T, false, EL, VC>(g, p, q, pid, pid, rec, o, sv, dt, c4, smax);
+                }
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) xc[l] = xn[l];
+                pid = pid_next;
+                pid_next = pid_after;
             }
-            stage ^= 1;
+        } else {
+            // bin order: x, m and id copied into shared memory (cp.async) a round ahead
+            int stage = 0;
+            for (uint32_t qr = 0; qr < rounds; ++qr) {
+                const uint32_t r = qr * 32 + lane;
+                const uint32_t pid = pid_next;
+                if (qr + 1 < rounds && r + 32 < cnt) pid_next = issue(stage ^ 1, r + 32);
+                cp_async_commit();
+                cp_async_wait<1>();
+                if (r < cnt) {
+                    const int st = stage;
+                    auto rec = [&](int f) { return *at(st, f); };
+                    gather_one<DIM, T, BINORDER, EL, VC>(g, p, q, pid, BINORDER ? beg + r : pid, rec, o, sv, dt, c4,
+                                                         smax);
+                }
+                stage ^= 1;
+            }
         }
         __syncwarp();
         s = __shfl_sync(0xFFFFFFFFu, ask, 0);
