@@ -13,9 +13,11 @@
 // tile, the P2G kernel's shape): the warp loads the tile's halo of the
 // accumulators R applying the grid update (mass-normalise and boundary;
 // gravity is not applied inside the loop) into its own shared-memory
-// velocity halo, then, 32 particles a round, each lane gathers its particle's
-// new (d, D), writes it in place and scatters it from its registers at the
-// same position into the warp's own accumulator halo, which the warp adds to
+// velocity halo, then, 32 particles a round (each lane's next position and
+// mass loaded into registers while the current particle is processed), each
+// lane gathers its particle's new (d, D), writes it in place and scatters it
+// from its registers at the same position into the warp's own accumulator
+// halo, which the warp adds to
 // the accumulators W after every 512 particles and at the end.  No block
 // barrier couples the warps.  The last iteration only gathers.  After each
 // iteration a second kernel clears R.  The material projections the page
@@ -27,8 +29,7 @@
 
 namespace mpm {
 
-// Per warp: a velocity halo, an accumulator halo and a double buffer of its
-// lanes' x and m.
+// Per warp: a velocity halo and an accumulator halo.
 template <int DIM, int T, bool SCATTER>
 __global__ void __launch_bounds__(kP2GThreads, 3)
     k_iterate_w(GridP g, PartsF p, const long long *__restrict__ accR, long long *__restrict__ accW,
@@ -39,15 +40,12 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
     constexpr int NW = kP2GThreads / 32;
     constexpr int VW = DIM * Hl::SIZE;                       // velocity words per warp
     constexpr int AW = SCATTER ? St::NC * Hl::SIZE : 1;      // accumulator words per warp
-    constexpr int NF = DIM + 1;                              // staged: x, m
     __shared__ float svel[NW][VW];
     __shared__ __align__(16) int32_t sacc[NW][AW];
-    __shared__ float sbuf[NW][2 * NF * 32];
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     float *vw = svel[warp];
     const VelHalo<DIM, T> sv{vw, vw + Hl::SIZE, DIM == 3 ? vw + 2 * Hl::SIZE : vw, nullptr};
     int32_t *wh = sacc[warp];
-    float *wb = sbuf[warp];
     const uint32_t halo = (uint32_t)__cvta_generic_to_shared(wh);
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     uint32_t *work = &status[MPM_ST_WORK_G2P];
@@ -56,7 +54,6 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
     if constexpr (SCATTER)
         for (int i = lane; i < AW; i += 32) wh[i] = 0;
     __syncwarp();
-    auto at = [&](int stage, int f) { return wb + (stage * NF + f) * 32 + lane; };
     int o[3];
     auto flush = [&]() {
         __syncwarp();
@@ -87,15 +84,13 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
         const uint32_t beg = start[t] + slices[2 * (size_t)s + 1];
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
         tile_origin(g, t, o);
-        auto issue = [&](int stage, uint32_t r) {
-            const uint32_t pid = perm[beg + r];
+        // positions and masses in registers a round ahead, perm two rounds ahead
+        uint32_t pid = lane < cnt ? perm[beg + lane] : 0u;
+        uint32_t pid_next = lane + 32 < cnt ? perm[beg + lane + 32] : 0u;
+        float xc[DIM + 1], xn[DIM + 1];
 #pragma unroll
-            for (int f = 0; f < DIM; ++f) cp_async4(at(stage, f), p.x[f] + pid);
-            cp_async4(at(stage, DIM), p.m + pid);
-            return pid;
-        };
-        uint32_t pid_next = lane < cnt ? issue(0, lane) : 0u;
-        cp_async_commit();
+        for (int l = 0; l < DIM; ++l) xc[l] = lane < cnt ? p.x[l][pid] : 0.f;
+        xc[DIM] = lane < cnt ? p.m[pid] : 0.f;
         // the halo's node values, the grid update (without gravity) applied on load
         for (int h = lane; h < Hl::NODES; h += 32) {
             int hx, hy, hz;
@@ -120,18 +115,17 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
         }
         __syncwarp();
         const uint32_t rounds = (cnt + 31) / 32;
-        int stage = 0;
         for (uint32_t q = 0; q < rounds; ++q) {
             const uint32_t r = q * 32 + lane;
-            const uint32_t pid = pid_next;
-            if (q + 1 < rounds && r + 32 < cnt) pid_next = issue(stage ^ 1, r + 32);
-            cp_async_commit();
-            cp_async_wait<1>();
+#pragma unroll
+            for (int l = 0; l < DIM; ++l) xn[l] = r + 32 < cnt ? p.x[l][pid_next] : 0.f;
+            xn[DIM] = r + 32 < cnt ? p.m[pid_next] : 0.f;
+            const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
             if (r < cnt) {
                 float x[DIM], f[3] = {0.f, 0.f, 0.f};
                 int b[3] = {0, 0, 0};
 #pragma unroll
-                for (int l = 0; l < DIM; ++l) x[l] = *at(stage, l);
+                for (int l = 0; l < DIM; ++l) x[l] = xc[l];
                 if (in_box_x<DIM, T>(g, x, o, b, f)) {
                     float w[3][3], we[3][3];
 #pragma unroll
@@ -159,14 +153,17 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
                     if constexpr (SCATTER) {
 #pragma unroll
                         for (int l = 0; l < DIM; ++l) rec_v[l] = x[l];
-                        rec_v[2 * DIM + DIM * DIM] = *at(stage, DIM);
+                        rec_v[2 * DIM + DIM * DIM] = xc[DIM];
                         auto rec = [&](int fi) { return rec_v[fi]; };
                         const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb};
                         if (!scatter_shares<DIM, false, false>(g, rec, f, ad, sp, unused)) ++bad;
                     }
                 }
             }
-            stage ^= 1;
+#pragma unroll
+            for (int l = 0; l <= DIM; ++l) xc[l] = xn[l];
+            pid = pid_next;
+            pid_next = pid_after;
             // int32 accumulators: at most 512 shares below 2^22 reach one entry between two flushes
             if constexpr (SCATTER)
                 if ((q + 1) % 16 == 0 && q + 1 < rounds) flush();
@@ -175,7 +172,6 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
         __syncwarp();
         s = __shfl_sync(0xFFFFFFFFu, ask, 0);
     }
-    cp_async_wait<0>();
     if constexpr (SCATTER) {
         bad = __reduce_add_sync(0xFFFFFFFFu, bad);
         if (bad && lane == 0) {
