@@ -92,7 +92,7 @@ static int64_t **private_grids(int T, size_t words)
  * xo, vo, Co, mo: the new state in bin order; perm: the order; acc:
  * (dim+1)*nodes int64 and vel: dim*nodes fp32 scratch (the grid of the step,
  * left holding it).  threads <= 0: all cores.  Returns the number of
- * particles moved (in the domain and in range); counts[0], counts[1] as the
+ * particles moved (those in the domain); counts[0], counts[1] as the
  * oracle's P2G.                                                            */
 int64_t orc_omp_step_fixed(const orc_desc *d, float dt, const float *dtg, int64_t np, const float *const *x,
                            const float *const *v, const float *const *C, const float *m, float *const *xo,
@@ -169,18 +169,41 @@ int64_t orc_omp_step_fixed(const orc_desc *d, float dt, const float *dtg, int64_
 
     double t_perm = omp_get_wtime();
 
+    /* the oracle's bound before any scatter: R over every in-domain
+     * particle (the max is order-free), one test for the whole step        */
+    float *Rt = (float *)calloc((size_t)T, sizeof(float));
+#pragma omp parallel num_threads(T)
+    {
+        int t = omp_get_thread_num();
+        int64_t j0 = valid * t / T, j1 = valid * (t + 1) / T;
+        const float *xs[3], *vs[3], *Cs[9];
+        for (int l = 0; l < dim; ++l) {
+            xs[l] = xo[l] + j0;
+            vs[l] = vo[l] + j0;
+        }
+        for (int k = 0; k < dim * dim; ++k)
+            Cs[k] = Co[k] + j0;
+        Rt[t] = orc_scatter_range(d, j1 - j0, xs, vs, Cs, mo + j0, NULL, NULL);
+    }
+    float R = 0.0f;
+    for (int t = 0; t < T; ++t)
+        R = max_nan(R, Rt[t]);
+    free(Rt);
+    int64_t count = d->acc_mode == 0 ? orc_max_cover(d, valid, (const float *const *)xo) : valid;
+    int scatter = orc_bound_ok(d, R, count);
+    counts[1] = scatter ? 0 : valid;
+
     /* P2G: private grids over each thread's slab, merged by integer add */
     int64_t pn = plane_nodes(d), nplanes = num_planes(d);
     int64_t **priv = private_grids(T, (size_t)(dim + 1) * (size_t)nodes);
     int *used = (int *)calloc((size_t)T, sizeof(int));
     plane_range *range = (plane_range *)calloc((size_t)T, sizeof(plane_range));
-    int64_t (*cnt)[2] = (int64_t (*)[2])calloc((size_t)T, sizeof(int64_t[2]));
 #pragma omp parallel num_threads(T)
     {
         int t = omp_get_thread_num();
         int64_t j0 = valid * t / T, j1 = valid * (t + 1) / T;
         range[t].lo = range[t].hi = 0;
-        if (j1 > j0) {
+        if (scatter && j1 > j0) {
             range[t] = planes_of_tiles(d, bucket[perm[j0]], bucket[perm[j1 - 1]]);
             used[t] = 1;
             /* only the slab is cleared and read back */
@@ -194,12 +217,9 @@ int64_t orc_omp_step_fixed(const orc_desc *d, float dt, const float *dtg, int64_
             }
             for (int k = 0; k < dim * dim; ++k)
                 Cs[k] = Co[k] + j0;
-            p2g_fixed_core(d, j1 - j0, xs, vs, Cs, mo + j0, NULL, priv[t], cnt[t]);
+            int64_t outside = 0;
+            scatter_fixed_all(d, j1 - j0, xs, vs, Cs, mo + j0, NULL, priv[t], &outside);
         }
-    }
-    for (int t = 0; t < T; ++t) {
-        counts[0] += cnt[t][0];
-        counts[1] += cnt[t][1];
     }
     counts[0] += np - valid;
     double t_p2g = omp_get_wtime();
@@ -217,7 +237,6 @@ int64_t orc_omp_step_fixed(const orc_desc *d, float dt, const float *dtg, int64_
         }
     free(used);
     free(range);
-    free(cnt);
     double t_merge = omp_get_wtime();
 
     /* grid update: the oracle's node update, planes in parallel */

@@ -201,43 +201,146 @@ int64_t orc_bin(const orc_desc *d, int64_t np, const float *const *x,
 /* Fixed-point P2G.
  * Implementation guide section 2.1 ("fixed-point atomics"): accumulate scaled
  * integers so the scatter is order-independent; section 3.3.1 and rule 1:
- * the encode rounds, it does not truncate.  "particle to grid transfer in
+ * the encode rounds, it does not truncate, and the multiplier is a runtime
+ * precision dial (any S = 2^scale_log2 here).  "particle to grid transfer in
  * checked integer arithmetic", "integers do not care about order": shares
  * are made integers by splitting, so a particle's shares sum to its quantity
  * exactly.  The momentum carried to a node is the APIC/MLS affine momentum
  * m w (v + C (x_i - x_p)) (implementation guide section 3.1, Part 1; the
  * PB-MPM reading in 3.3.2 scatters "momentum(d + D*offset)" with no stress).
  *
- * Range: each non-centre share must satisfy |share| < 2^22.  A particle is in
- * range when, with wmax = 0.75^dim and h = 1.5*dx,
- *     wmax * |Mt|                                          <= 4190208
- *     wmax * (|Mt| * (|v_k| + h*((|C_k0| + |C_k1|) + |C_k2|))) <= 4190208
- * for every k (all in fp32, NaN fails).  Out-of-range particles are not
- * scattered and are counted: the check comes before the particle's shares.  */
+ * Bound (the same page, "the program": the bounds line runs before the loop,
+ * and when it fails the program stops there, before any particle is
+ * scattered).  The page bounds count * max m * max |v| by the int64 range.
+ * Here a particle's quantity is spread over a stencil with an affine term,
+ * so its range is taken per particle, in fp32, in this order:
+ *     r_k = |v_k| + h*((|C_k0| + |C_k1|) + |C_k2|),   h = 1.5*dx
+ *     r   = max(1, r_0, .., r_dim-1)
+ *     R_p = max(|m|*r, |q|)          (q = rest volume in cells, volume channel)
+ * with NaN making R_p NaN.  Since |x_i - x_p| <= 1.5 dx over the stencil and
+ * the weights sum to one up to a few fp32 roundings, the absolute values of a
+ * particle's shares of any channel sum to at most
+ *     S*R_p*(1 + 2^-10) + 28
+ * (26 shares each rounded by at most 1/2; the centre's remainder differs from
+ * its own product by Q's rounding and the weights' and fma's roundings, which
+ * are below 2^-16 relative).  A node's accumulator, and every partial sum on
+ * the way to it, is at most the sum of these over the particles whose stencil
+ * covers the node.  With R = max over the in-domain particles of R_p and
+ * B = S*R*(1 + 2^-10) + 28 in fp64 (no contraction, this order):
+ *     int64 accumulators:  n_in_domain * B <= 2^62
+ *     int32 accumulators:  (most stencils covering one node) * B <= 2^31 - 1024
+ * (the int32 form is the neighbourhood refinement of the global one).  If the
+ * test fails (or R is NaN) nothing is scattered and the status reports the
+ * bound.  The limits keep a margin below the types' maxima that covers the
+ * fp64 rounding of the test itself.                                         */
 
-#define ORC_SHARE_LIMIT 4190208.0f /* 2^22 - 4096 */
+#define ORC_I64_LIMIT 0x1p62
+#define ORC_I32_LIMIT 2147482624.0 /* 2^31 - 1024 */
 
-static int in_range(const orc_desc *d, float Mt, const float *const *v, const float *const *C, int64_t p)
+/* max that keeps NaN: NaN in either operand gives NaN */
+static float max_nan(float a, float b)
+{
+    if (a != a || b != b)
+        return NAN;
+    return a > b ? a : b;
+}
+
+static float cells_of_volume(const orc_desc *d, float V0);
+
+/* R_p of particle p (see above).  vol: rest volumes (volume channel) or NULL. */
+static float particle_range(const orc_desc *d, const float *const *v, const float *const *C, const float *m,
+                            const float *vol, int64_t p)
 {
     int dim = d->dim;
-    float wmax = dim == 3 ? 0.421875f : 0.5625f;
     float h = 1.5f * d->dx;
-    float aM = fabsf(Mt);
-    int ok = (wmax * aM) <= ORC_SHARE_LIMIT;
+    float r = 1.0f;
     for (int k = 0; k < dim; ++k) {
         float sc = fabsf(C[k * dim + 0][p]) + fabsf(C[k * dim + 1][p]);
         if (dim == 3)
             sc = sc + fabsf(C[k * dim + 2][p]);
-        float R = aM * (fabsf(v[k][p]) + h * sc);
-        ok = ok && ((wmax * R) <= ORC_SHARE_LIMIT);
+        r = max_nan(r, fabsf(v[k][p]) + h * sc);
     }
-    return ok;
+    float R = fabsf(m[p]) * r;
+    if (m[p] != m[p])
+        R = NAN;
+    if (vol)
+        R = max_nan(R, fabsf(cells_of_volume(d, vol[p])));
+    return R;
 }
 
+/* R = max of R_p over the in-domain particles (0 when there are none; NaN if
+ * any R_p is NaN); *valid = their number.                                   */
+float orc_scatter_range(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                        const float *const *C, const float *m, const float *vol, int64_t *valid)
+{
+    float R = 0.0f;
+    int64_t nv = 0;
+    for (int64_t p = 0; p < np; ++p) {
+        int b[3];
+        float f[3];
+        if (!base_frac(d, x, p, b, f))
+            continue;
+        nv += 1;
+        R = max_nan(R, particle_range(d, v, C, m, vol, p));
+    }
+    if (valid)
+        *valid = nv;
+    return R;
+}
+
+/* The most in-domain particles whose stencil covers one node: per base cell
+ * the particle count, then per node the sum over the 3^dim base cells whose
+ * stencil reaches it.                                                       */
+int64_t orc_max_cover(const orc_desc *d, int64_t np, const float *const *x)
+{
+    int dim = d->dim;
+    int64_t nodes = nodes_of(d);
+    int64_t *cnt = (int64_t *)calloc((size_t)nodes, sizeof(int64_t)); /* indexed by the base node */
+    for (int64_t p = 0; p < np; ++p) {
+        int b[3];
+        float f[3];
+        if (base_frac(d, x, p, b, f))
+            cnt[node_at(d, b[0], b[1], dim == 3 ? b[2] : 0)] += 1;
+    }
+    int64_t best = 0;
+    int nk = dim == 3 ? d->n[2] : 1;
+    for (int k = 0; k < nk; ++k)
+        for (int j = 0; j < d->n[1]; ++j)
+            for (int i = 0; i < d->n[0]; ++i) {
+                int64_t s = 0;
+                for (int a2 = 0; a2 < (dim == 3 ? 3 : 1); ++a2)
+                    for (int a1 = 0; a1 < 3; ++a1)
+                        for (int a0 = 0; a0 < 3; ++a0) {
+                            int bi = i - a0, bj = j - a1, bk = k - a2;
+                            if (bi < 0 || bj < 0 || bk < 0)
+                                continue;
+                            s += cnt[node_at(d, bi, bj, bk)];
+                        }
+                if (s > best)
+                    best = s;
+            }
+    free(cnt);
+    return best;
+}
+
+/* 1 when the accumulators of this mode hold `count` particles of range R
+ * (count = in-domain particles for int64, orc_max_cover for int32).        */
+int orc_bound_ok(const orc_desc *d, float R, int64_t count)
+{
+    double S = ldexp(1.0, d->scale_log2);
+    double B = S * (double)R;
+    B = B * (1.0 + 0x1p-10);
+    B = B + 28.0;
+    double total = (double)count * B;
+    double limit = d->acc_mode == 0 ? ORC_I32_LIMIT : ORC_I64_LIMIT;
+    return total <= limit;
+}
+
+/* rint of the exact product a*b: the product of two fp32 values is exact in
+ * fp64 (48 significant bits); nearbyint rounds it once, ties to even (the
+ * default rounding mode).  Callers keep |a*b| below 2^62 by the bound.     */
 static int64_t rint_product(float a, float b)
 {
-    /* The product of two fp32 values is exact in fp64; nearbyint rounds it
-     * once, ties to even (default rounding mode). */
     return (int64_t)nearbyint((double)a * (double)b);
 }
 
@@ -246,9 +349,9 @@ static int64_t rint_product(float a, float b)
  * fraction of a cell, 1/ppc for a rest packing, so that a node of a
  * rest-packed region sums to about one; G2P gathers the node values back).
  * The quantity is q = V0 * inv_dx^dim (inv_dx^3 = (inv_dx*inv_dx)*inv_dx),
- * scattered as the mass is: Vt = q*S, share rint(((wx*Vt)*wy)*wz), the centre
- * node takes rint(Vt) minus the other shares, and the particle's range test
- * also requires wmax*|Vt| <= 2^22 - 4096.  It is the last plane of acc.     */
+ * scattered as the mass is: Vt = q*S, share rint(((wx*Vt)*wy)*wz), and the
+ * centre node takes rint(Vt) minus the other shares.  It is the last plane
+ * of acc and enters the bound through R_p.                                  */
 static float cells_of_volume(const orc_desc *d, float V0)
 {
     float c = d->inv_dx * d->inv_dx;
@@ -257,13 +360,20 @@ static float cells_of_volume(const orc_desc *d, float V0)
     return V0 * c;
 }
 
+/* Scatters every in-domain particle, no bound check (the callers check it
+ * first).  counts[0] += out-of-domain particles.                           */
+static void scatter_fixed_all(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                              const float *const *C, const float *m, const float *vol, int64_t *acc,
+                              int64_t *outside);
+
 static uint32_t p2g_fixed_core(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
                                const float *const *C, const float *m, const float *vol, int64_t *acc,
                                int64_t counts[2]);
 
 /* acc: (dim+1) planes of nodes_of(d) int64 values (mass, then momentum per
  * axis), zeroed by the caller.  counts[0] = out-of-domain particles,
- * counts[1] = out-of-range particles.  Returns the status bits.            */
+ * counts[1] = in-domain particles left unscattered because the bound failed
+ * (all of them, or none).  Returns the status bits.                         */
 uint32_t orc_p2g_fixed(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
                        const float *const *C, const float *m, int64_t *acc, int64_t counts[2])
 {
@@ -283,25 +393,37 @@ static uint32_t p2g_fixed_core(const orc_desc *d, int64_t np, const float *const
                                const float *const *C, const float *m, const float *vol, int64_t *acc,
                                int64_t counts[2])
 {
+    int64_t valid = 0;
+    float R = orc_scatter_range(d, np, x, v, C, m, vol, &valid);
+    int64_t count = d->acc_mode == 0 ? orc_max_cover(d, np, x) : valid;
+    counts[0] = np - valid;
+    counts[1] = 0;
+    if (!orc_bound_ok(d, R, count)) {
+        counts[1] = valid;
+        return (counts[0] ? ORC_ST_DOMAIN : 0u) | ORC_ST_BOUND;
+    }
+    int64_t outside = 0;
+    scatter_fixed_all(d, np, x, v, C, m, vol, acc, &outside);
+    return counts[0] ? ORC_ST_DOMAIN : 0u;
+}
+
+static void scatter_fixed_all(const orc_desc *d, int64_t np, const float *const *x, const float *const *v,
+                              const float *const *C, const float *m, const float *vol, int64_t *acc,
+                              int64_t *outside)
+{
     int dim = d->dim;
     int64_t nodes = nodes_of(d);
     float S = ldexpf(1.0f, d->scale_log2);
-    float wmax = dim == 3 ? 0.421875f : 0.5625f;
     int64_t vplane = (int64_t)(dim + 1) * nodes;
-    counts[0] = counts[1] = 0;
     for (int64_t p = 0; p < np; ++p) {
         int b[3];
         float f[3];
         if (!base_frac(d, x, p, b, f)) {
-            counts[0] += 1;
+            *outside += 1;
             continue;
         }
         float Mt = m[p] * S;
         float Vt = vol ? cells_of_volume(d, vol[p]) * S : 0.0f;
-        if (!in_range(d, Mt, v, C, p) || !((wmax * fabsf(Vt)) <= ORC_SHARE_LIMIT)) {
-            counts[1] += 1;
-            continue;
-        }
         float w[3][3], dd[3][3];
         for (int l = 0; l < 3; ++l)
             for (int a = 0; a < 3; ++a) {
@@ -357,7 +479,6 @@ static uint32_t p2g_fixed_core(const orc_desc *d, int64_t np, const float *const
         if (vol)
             acc[vplane + cnode] += vrest;
     }
-    return (counts[0] ? ORC_ST_DOMAIN : 0u) | (counts[1] ? ORC_ST_BOUND : 0u);
 }
 
 /* Float-atomic P2G for comparison (implementation guide section 2.1 caveat:

@@ -75,6 +75,12 @@ def lib():
             L.orc_bin.restype = ct.c_int64
             L.orc_p2g_fixed.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _PP, _PP, _P, _P, _P]
             L.orc_p2g_fixed.restype = ct.c_uint32
+            L.orc_scatter_range.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _PP, _PP, _P, _P, _P]
+            L.orc_scatter_range.restype = ct.c_float
+            L.orc_max_cover.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP]
+            L.orc_max_cover.restype = ct.c_int64
+            L.orc_bound_ok.argtypes = [ct.POINTER(Desc), ct.c_float, ct.c_int64]
+            L.orc_bound_ok.restype = ct.c_int
             L.orc_p2g_float.argtypes = [ct.POINTER(Desc), ct.c_int64, _PP, _PP, _PP, _P, _P, _P]
             L.orc_p2g_float.restype = ct.c_uint32
             L.orc_grid_update_fixed.argtypes = [ct.POINTER(Desc), _P, _P, _P]
@@ -165,9 +171,34 @@ def bin_particles(grid: dict, x: np.ndarray):
     return key, perm, cnt, int(valid)
 
 
+def scatter_range(grid: dict, x, v, C, m, vol=None):
+    """(R, in-domain count): R = max over the in-domain particles of the range R_p the
+    bound is taken on (``mpm_oracle.c``, fixed-point P2G); NaN if any R_p is NaN."""
+    x, v, C, m = _f32(x), _f32(v), _f32(C), _f32(m)
+    d = desc_from(grid)
+    valid = ct.c_int64(0)
+    volp = None if vol is None else _ptr(_f32(vol))
+    R = lib().orc_scatter_range(ct.byref(d), x.shape[1], _rows(x), _rows(v), _rows(C), _ptr(m), volp,
+                                ct.byref(valid))
+    return float(np.float32(R)), int(valid.value)
+
+
+def max_cover(grid: dict, x) -> int:
+    """The most in-domain particles whose stencil covers one node."""
+    x = _f32(x)
+    return int(lib().orc_max_cover(ct.byref(desc_from(grid)), x.shape[1], _rows(x)))
+
+
+def bound_ok(grid: dict, R: float, count: int) -> bool:
+    """The accumulator bound of the grid's mode for ``count`` particles of range R."""
+    return bool(lib().orc_bound_ok(ct.byref(desc_from(grid)), float(R), int(count)))
+
+
 def p2g_fixed(grid: dict, x, v, C, m, vol=None):
     """Fixed-point P2G: returns (acc int64 [(dim+1), nodes], status bits, counts[2]);
-    with rest volumes ``vol`` the volume channel is a last plane (dim+2 planes)."""
+    with rest volumes ``vol`` the volume channel is a last plane (dim+2 planes).
+    counts = (out-of-domain particles, in-domain particles left unscattered because
+    the bound failed: all of them or none)."""
     x, v, C, m = _f32(x), _f32(v), _f32(C), _f32(m)
     d = desc_from(grid)
     nodes = grid_nodes(grid)

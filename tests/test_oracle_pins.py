@@ -122,10 +122,11 @@ def test_bin_is_stable_sort_of_base_cells(dim, n, tile):
 # fixed-point P2G against brute force, conservation and order independence
 
 @pytest.mark.parametrize("dim", [2, 3])
-def test_p2g_fixed_matches_brute_force(dim):
+@pytest.mark.parametrize("scale_log2", [18, 32])
+def test_p2g_fixed_matches_brute_force(dim, scale_log2):
     n = 8
     cloud = W.small_cloud(dim, 48, n, seed=100 + dim, lo=0.2, hi=0.8, vsig=1.0, csig=3.0,
-                          scale_log2=18, mass_lo=0.5, mass_hi=2.0)
+                          scale_log2=scale_log2, mass_lo=0.5, mass_hi=2.0)
     grid = cloud["grid"]
     acc, st, counts = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
     assert st == 0 and counts.sum() == 0
@@ -162,8 +163,9 @@ def test_p2g_float_matches_brute_force(dim):
 
 
 @pytest.mark.parametrize("dim", [2, 3])
-def test_grid_totals_equal_particle_totals(dim):
-    cloud = W.small_cloud(dim, 4000, 32, seed=300 + dim, vsig=2.0, csig=1.0, scale_log2=17,
+@pytest.mark.parametrize("scale_log2", [17, 32])
+def test_grid_totals_equal_particle_totals(dim, scale_log2):
+    cloud = W.small_cloud(dim, 4000, 32, seed=300 + dim, vsig=2.0, csig=1.0, scale_log2=scale_log2,
                           mass_lo=0.25, mass_hi=3.0)
     grid = cloud["grid"]
     acc, st, counts = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
@@ -179,8 +181,9 @@ def test_grid_totals_equal_particle_totals(dim):
 
 
 @pytest.mark.parametrize("dim", [2, 3])
-def test_scrambled_orders_give_identical_grids(dim):
-    cloud = W.small_cloud(dim, 2048, 24, seed=400 + dim, scale_log2=19)
+@pytest.mark.parametrize("scale_log2", [19, 32])
+def test_scrambled_orders_give_identical_grids(dim, scale_log2):
+    cloud = W.small_cloud(dim, 2048, 24, seed=400 + dim, scale_log2=scale_log2)
     grid = cloud["grid"]
     base, _, _ = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
     for a, b in [(97, 13), (1, 13), (1023, 5), (3, 2047)]:
@@ -190,21 +193,133 @@ def test_scrambled_orders_give_identical_grids(dim):
         assert np.array_equal(acc, base)
 
 
-def test_out_of_domain_and_out_of_range_particles_are_counted_not_scattered():
+def test_out_of_domain_particles_are_counted_not_scattered():
     cloud = W.small_cloud(3, 64, 16, seed=501, scale_log2=19)
     grid = cloud["grid"]
     x, v, C, m = cloud["x"].copy(), cloud["v"].copy(), cloud["C"].copy(), cloud["m"].copy()
     x[0, 3] = 0.0            # below the lowest stencil
     x[1, 7] = 1.0            # above the highest
     x[2, 9] = np.nan
-    m[11] = 1e6              # shares would not fit
-    v[1, 12] = np.inf
+    v[1, 7] = np.inf         # outside the domain: its range does not enter the bound
     acc, st, counts = O.p2g_fixed(grid, x, v, C, m)
-    assert st == 3 and counts[0] == 3 and counts[1] == 2
+    assert st == 1 and counts[0] == 3 and counts[1] == 0
     keep = np.ones(64, dtype=bool)
-    keep[[3, 7, 9, 11, 12]] = False
+    keep[[3, 7, 9]] = False
     ref, st2, _ = O.p2g_fixed(grid, x[:, keep], v[:, keep], C[:, keep], m[keep])
     assert st2 == 0 and np.array_equal(acc, ref)
+
+
+# --------------------------------------------------------------------------
+# the bound before any scatter ("particle to grid transfer in checked integer
+# arithmetic", the program: the bounds line runs first; if it fails nothing is
+# scattered)
+
+@pytest.mark.parametrize("dim", [2, 3])
+@pytest.mark.parametrize("scale_log2", [20, 32, 40])
+def test_bound_covers_every_particles_shares(dim, scale_log2):
+    """A particle's shares of each channel sum in absolute value to at most
+    S*R_p*(1 + 2^-10) + 28: each particle scattered alone, its grid holds exactly its
+    shares.  C is large, so the affine term dominates most particles' ranges; the
+    first 20 have C = 0, where the bound is tight on their largest momentum channel."""
+    cloud = W.small_cloud(dim, 200, 10, seed=600 + dim, lo=0.25, hi=0.75, vsig=3.0, csig=40.0,
+                          scale_log2=scale_log2, mass_lo=0.1, mass_hi=4.0)
+    cloud["C"][:, :20] = 0.0
+    grid = cloud["grid"]
+    S = 2.0 ** scale_log2
+    worst = 0.0
+    for p in range(200):
+        sl = slice(p, p + 1)
+        acc, st, _ = O.p2g_fixed(grid, cloud["x"][:, sl], cloud["v"][:, sl], cloud["C"][:, sl],
+                                 cloud["m"][sl])
+        assert st == 0
+        R, valid = O.scatter_range(grid, cloud["x"][:, sl], cloud["v"][:, sl], cloud["C"][:, sl],
+                                   cloud["m"][sl])
+        assert valid == 1
+        bound = S * R * (1 + 2.0 ** -10) + 28
+        for c in range(dim + 1):
+            total = sum(abs(int(t)) for t in acc[c])
+            assert total <= bound
+            worst = max(worst, total / bound)
+    assert worst > 0.99     # the bound is tight for some particle and channel
+
+
+def test_bound_failure_scatters_nothing():
+    cloud = W.small_cloud(3, 64, 16, seed=502, scale_log2=32)
+    grid = cloud["grid"]
+    x, v, C, m = cloud["x"], cloud["v"].copy(), cloud["C"], cloud["m"].copy()
+    acc, st, counts = O.p2g_fixed(grid, x, v, C, m)
+    assert st == 0 and acc.any()
+    for bad in ("inf", "nan", "huge"):
+        v2, m2 = v.copy(), m.copy()
+        if bad == "inf":
+            v2[1, 12] = np.inf
+        elif bad == "nan":
+            m2[30] = np.nan
+        else:
+            m2[11] = 1e15       # 64 * 1e15 * |v| * 2^32 > 2^62
+        acc, st, counts = O.p2g_fixed(grid, x, v2, C, m2)
+        assert st == 2 and counts[0] == 0 and counts[1] == 64
+        assert not acc.any()
+
+
+def test_int64_bound_on_the_integer_pages_magnitudes():
+    """The integer-transfer page's workload magnitudes (256 particles, m <= 1000,
+    |v| <= 1000; its bounds line: 256 * 1000 * 1000 fits int64) carried over to the
+    fp32 path with C = 0: R = max |m| * max(1, |v|) = 10^6 exactly, so the int64 form
+    256 * (S * 10^6 * (1 + 2^-10) + 28) <= 2^62 holds up to S = 2^34 (4.40e18) and
+    fails at 2^35 (8.80e18), by hand."""
+    cfg = W.cic_int()
+    X, mi, vi = cfg["X"], cfg["m"], cfg["v"]
+    x = ((X.astype(np.float64) / 65536.0 + 0.5) / 10.0).astype(np.float32)     # inside a 10-node grid
+    v = vi.astype(np.float32)
+    m = mi.astype(np.float32)
+    v[0, 0], m[0] = 1000.0, 1000.0                   # make the maxima exact
+    C = np.zeros((4, 256), np.float32)
+    for s_log2, ok in [(32, True), (34, True), (35, False)]:
+        grid = W.small_cloud(2, 1, 10, seed=1, scale_log2=s_log2)["grid"]
+        R, valid = O.scatter_range(grid, x, v, C, m)
+        assert R == 1.0e6 and valid == 256
+        total = 256 * (2.0 ** s_log2 * 1.0e6 * (1 + 2.0 ** -10) + 28)
+        assert (total <= 2.0 ** 62) == ok
+        assert O.bound_ok(grid, R, valid) == ok
+        acc, st, counts = O.p2g_fixed(grid, x, v, C, m)
+        assert (st == 0) == ok and acc.any() == ok
+
+
+def test_int32_bound_counts_stencils_per_node():
+    """int32 accumulators use the neighbourhood form: the most stencils covering one
+    node (counted here by brute force over all nodes) times the per-particle bound.
+    Just inside the int32 limit the grid holds the exact sums (checked against the
+    int64 grid); just outside, nothing is scattered."""
+    n = 12
+    cloud = W.small_cloud(2, 300, n, seed=610, lo=0.3, hi=0.45, vsig=0.5, csig=0.2,
+                          acc_mode=W.ACC_I32, scale_log2=20)
+    grid = cloud["grid"]
+    x, v, C, m = cloud["x"], cloud["v"], cloud["C"], cloud["m"]
+    xi = x.astype(np.float64) * grid["inv_dx"]
+    X = node_coords(grid)
+    cover = np.zeros(X.shape[1], dtype=np.int64)
+    for p in range(x.shape[1]):
+        inside = np.ones(X.shape[1], dtype=bool)
+        for l in range(2):
+            b = np.floor(xi[l, p] - 0.5)
+            inside &= (X[l] >= b) & (X[l] <= b + 2)
+        cover += inside
+    assert O.max_cover(grid, x) == cover.max()
+    R, valid = O.scatter_range(grid, x, v, C, m)
+    # the largest scale whose bound fits int32, then one more bit
+    s_fit = max(s for s in range(0, 31)
+                if cover.max() * (2.0 ** s * R * (1 + 2.0 ** -10) + 28) <= 2 ** 31 - 1024)
+    for s_log2, ok in [(s_fit, True), (s_fit + 1, False)]:
+        g32 = dict(grid, scale_log2=s_log2)
+        acc, st, counts = O.p2g_fixed(g32, x, v, C, m)
+        assert (st == 0) == ok
+        if ok:
+            g64 = dict(g32, acc_mode=W.ACC_I64)
+            ref, _, _ = O.p2g_fixed(g64, x, v, C, m)
+            assert np.array_equal(acc, ref) and np.abs(ref).max() < 2 ** 31
+        else:
+            assert not acc.any() and counts[1] == valid
 
 
 # --------------------------------------------------------------------------
