@@ -113,7 +113,9 @@ typedef struct mpm_particles {
 enum {
     MPM_ST_FLAGS = 0,        /* bit (1 << MPM_E_DOMAIN) | (1 << MPM_E_BOUND) | ... */
     MPM_ST_N_OUTSIDE = 1,    /* particles outside the domain */
-    MPM_ST_N_OUT_OF_RANGE = 2, /* particles whose shares would not fit (skipped by P2G) */
+    MPM_ST_N_OUT_OF_RANGE = 2, /* particles found above the range the last P2G's bound was checked with
+                                  (records given by the caller, or a fused step's new state beyond
+                                  22-bit shares): that call's scatter was undone */
     MPM_ST_N_VALID = 3,      /* in-domain particles (length of the sorted part of perm) */
     MPM_ST_N_SLICES = 4,     /* P2G work items */
     MPM_ST_N_ACTIVE = 5,     /* tiles holding at least one particle */
@@ -129,7 +131,15 @@ enum {
                                 |v'| + 1.5 dx |C'|_F; the advective step bound is dt <= dx / it */
     MPM_ST_N_ESCAPED = 14,   /* mpm_step_fused: particles whose base cell left their tile in the step,
                                 scattered straight into the global grid */
-    MPM_STATUS_WORDS = 16
+    MPM_ST_RANGE = 15,       /* fp32 bits of R, the range the last fixed-point P2G checked its bound
+                                with (see mpm_p2g) */
+    MPM_ST_SHARE_PATH = 16,  /* the last fixed-point P2G's shares: 0 below 2^22 (one fp32 fma each),
+                                1 int64 (exact integer product); the bits are the same either way */
+    MPM_ST_P2G_MASS = 20,    /* record: fp32 bits of max |m| over the particles the last P2G scattered */
+    MPM_ST_P2G_VOLUME = 21,  /* record: fp32 bits of max |V0 inv_dx^dim| over the same (volume channel) */
+    MPM_ST_G2P_RANGE = 22,   /* record: fp32 bits of max over the particles the last G2P moved of
+                                max(1, |v'_k| + 1.5 dx sum_l |C'_kl|) */
+    MPM_STATUS_WORDS = 24
 };
 
 /* Binning state: device arrays carved out of one caller workspace by
@@ -148,6 +158,7 @@ typedef struct mpm_bins {
     uint32_t *status;        /* [MPM_STATUS_WORDS] */
     void *scratch;           /* internal */
     size_t scratch_bytes;
+    int32_t range_from_g2p;  /* set by the caller (mpm_bins_init clears it): see mpm_p2g */
 } mpm_bins;
 
 /* Bytes of workspace mpm_bins_init needs for n particles on this grid. */
@@ -174,11 +185,10 @@ enum { MPM_BIN_DEFAULT = 0 };
  * ascending tile order, each tile in particle-index order (the stable counting
  * sort with the tile as bucket), then the out-of-domain particles in index
  * order, so the order is a deterministic function of the keys.  Also builds the active-tile list and
- * the P2G work list, resets the status words, counts out-of-domain particles,
- * and in MPM_ACC_I32 mode checks the accumulator bound before any scatter:
- * every node must be covered by at most 511 particle stencils (511 shares of
- * magnitude below 2^22 fit int32); otherwise MPM_E_BOUND is set and mpm_p2g
- * scatters nothing.
+ * the P2G work list, resets the status words (all but the records
+ * MPM_ST_P2G_MASS .. MPM_ST_G2P_RANGE), counts out-of-domain particles, and in
+ * MPM_ACC_I32 mode counts the most stencils covering one node
+ * (MPM_ST_MAX_NEIGHBOURS), which mpm_p2g's bound uses.
  */
 mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, int flags,
                    void *stream);
@@ -189,15 +199,37 @@ mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
  *   Mt = m*S, Wt(a) = ((wx[a0]*Mt)*wy[a1])*wz[a2],
  *   vel_k(a) = fma(C_k2, d_2, fma(C_k1, d_1, fma(C_k0, d_0, v_k))),  d_l = (a_l - f_l)*dx,
  *   share s_m(a) = rint(Wt(a)), s_k(a) = rint(Wt(a) * vel_k(a)) (exact product,
- *   one rounding, ties to even), and gives the centre node (1,1,1) the
+ *   one rounding, ties to even, at any S), and gives the centre node (1,1,1) the
  *   remainder Q - sum of the others, with Q_m = rint(Mt), Q_k = rint(Mt*v_k),
  * so grid totals equal particle totals exactly ("particle to grid transfer in
  * checked integer arithmetic": split rather than weight; implementation guide
- * 2.1 and 3.3.1: fixed-point atomics, round rather than truncate).  The result
- * is bit-identical for every particle order.  A particle whose shares could
- * reach 2^22 in magnitude (wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) > 2^22 - 4096,
- * wmax = 0.75^dim) is not scattered and is counted in MPM_ST_N_OUT_OF_RANGE.
- * MPM_ACC_F32 adds the fp32 values Wt*vel with float atomics instead.
+ * 2.1 and 3.3.1: fixed-point atomics, round rather than truncate, the
+ * multiplier a runtime precision dial).  The result is bit-identical for
+ * every particle order.
+ * Bound, before any particle is scattered (the same page's bounds line): with
+ * r_k = |v_k| + h*((|C_k0| + |C_k1|) + |C_k2|), h = 1.5*dx, each particle's
+ * range is R_p = max(|m| * max(1, r_0, .., r_dim-1), |V0 inv_dx^dim|) (the
+ * last term with the volume channel; elastic particles use the stress-folded
+ * matrix below; fp32, in this order, NaN propagating), R = max over the
+ * binned particles, and B = S*R*(1 + 2^-10) + 28 (fp64) bounds the absolute
+ * sum of one particle's shares of any channel.  The scatter proceeds when
+ * N_valid * B <= 2^62 (int64 grids) or MPM_ST_MAX_NEIGHBOURS * B <= 2^31 - 1024
+ * (int32 grids); otherwise MPM_E_BOUND is set and nothing is scattered.  R is
+ * found by a pass over v, C and m before the scatter, or -- when the caller
+ * sets bins->range_from_g2p, promising that the particles are those the last
+ * mpm_p2g and mpm_g2p on these bins left (v, C, m unchanged since) -- from the
+ * records those calls wrote (R = max(P2G_MASS * G2P_RANGE, P2G_VOLUME)), which
+ * saves the pass.  With records each particle is verified against R as it is
+ * scattered; a particle above it (the promise broken) makes the call undo its
+ * scatter (the grid is left zero), set MPM_E_BOUND and count the particle in
+ * MPM_ST_N_OUT_OF_RANGE.  Elastic particles always take the pass.
+ * Shares below 2^22 in magnitude (wmax*S*R*(1 + 2^-10) <= 2^22 - 4096,
+ * wmax = 0.75^dim) are formed with one fp32 fma each and summed in 32-bit
+ * shared-memory tile accumulators; larger ones with an exact 24x24-bit integer
+ * product and 64-bit sums (MPM_ST_SHARE_PATH says which ran).  R and the path
+ * are written to MPM_ST_RANGE and MPM_ST_SHARE_PATH; the call also writes the
+ * records MPM_ST_P2G_MASS and MPM_ST_P2G_VOLUME.
+ * MPM_ACC_F32 adds the fp32 values Wt*vel with float atomics instead (no bound).
  * Elastic particles (parts->F[0] != NULL) scatter with C replaced by the
  * MLS-MPM affine matrix C' = C - kappa*tau (implementation guide, section
  * 3.1, Part 2: J = det F, P = mu (F - F^-T) + lambda ln(J) F^-T,
@@ -206,16 +238,15 @@ mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
  * kappa = ((dt*V0)*c4s)/m, c4s = (4*inv_dx)*inv_dx, each step one fp32
  * rounding in the order the oracle states, ln computed by the library's own
  * series (not the CUDA math library) so that it is reproducible.  C' also
- * enters the range test.  A particle whose det F is not a positive normal
+ * enters the range.  A particle whose det F is not a positive normal
  * fp32 number keeps C and is counted in MPM_ST_N_DEGENERATE.  `dt` is only
  * read for elastic particles.
  * With volume_channel = 1 a last accumulator channel receives each
  * particle's rest volume in cells, q = V0 * inv_dx^dim (inv_dx^3 taken as
  * (inv_dx*inv_dx)*inv_dx), as the mass is scattered: Vt = q*S, shares
- * rint(((wx*Vt)*wy)*wz), remainder at the centre, and the range test also
- * requires wmax*|Vt| <= 2^22 - 4096 (implementation guide, section 3.3.2,
- * "grid-recovered volume": 1/ppc per particle, so a rest-packed node sums to
- * about one).  MPM_ACC_F32 adds the fp32 terms ((wx*q)*wy)*wz.
+ * rint(((wx*Vt)*wy)*wz), remainder at the centre (implementation guide,
+ * section 3.3.2, "grid-recovered volume": 1/ppc per particle, so a rest-packed
+ * node sums to about one).  MPM_ACC_F32 adds the fp32 terms ((wx*q)*wy)*wz.
  * MPM_ACC_EXACT_INT (2D or 3D, order 1): integer positions X (1/65,536 cell),
  * int64 m and v; the far node's share of q is q*F/65,536 rounded to nearest
  * (ties to even), the near node gets the rest, split along x then y (then z);
@@ -357,8 +388,15 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
  * warp per work item: a particle's new state is scattered into the warp's
  * tile accumulator while its base cell stays in the tile; a particle whose
  * base cell left the tile is scattered straight into the global grid and
- * counted in MPM_ST_N_ESCAPED; those leaving the domain are not scattered;
- * out-of-range ones are counted in MPM_ST_N_OUT_OF_RANGE as by mpm_p2g.  MPM_ACC_I64 only, without the
+ * counted in MPM_ST_N_ESCAPED; those leaving the domain are not scattered.
+ * The new state is formed in the same kernel that scatters it, so no bound can
+ * run before this scatter: the kernel forms 22-bit shares only and tests each
+ * particle as mpm_p2g's fast path requires (wmax*|m S|*max(1, r_k) within
+ * 2^22 - 4096, with int64 grids no node can then overflow); a particle beyond
+ * it is counted in MPM_ST_N_OUT_OF_RANGE, MPM_E_BOUND is set and the step's
+ * scatter is undone (acc_write left zero; `out` still holds the new state).
+ * Where that happens the separate calls take mpm_p2g's int64 shares instead.
+ * MPM_ACC_I64 only, without the
  * elastic state or the volume channel (MPM_E_ARG otherwise): the int32 mode's
  * bound is checked by the binning of the positions it will scatter, which
  * this scatter runs ahead of.  No velocity grid is written.
@@ -380,7 +418,10 @@ mpm_status mpm_step_fused(const mpm_grid_desc *desc, mpm_particles *in, mpm_part
  * afterwards; x, m and every particle outside the domain are unchanged.  The
  * bits equal `iterations` rounds of mpm_grid_update (dtg = 0) + mpm_g2p
  * (dt = 0) + mpm_p2g.  The material projections the guide runs between the
- * transfers are not part of this call.  MPM_ACC_I64 only, without the elastic
+ * transfers are not part of this call.  Like mpm_step_fused it forms 22-bit
+ * shares only; a round whose state does not fit them counts the particles in
+ * MPM_ST_N_OUT_OF_RANGE and sets MPM_E_BOUND, and the state the call leaves is
+ * then not valid.  MPM_ACC_I64 only, without the elastic
  * state or the volume channel.  iterations >= 1.
  */
 mpm_status mpm_iterate(const mpm_grid_desc *desc, mpm_particles *parts, mpm_bins *bins, void *acc_a, void *acc_b,

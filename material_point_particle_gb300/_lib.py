@@ -22,7 +22,12 @@ ST_BIN_WORDS = 10   # status words 0..9 are written by mpm_bin
 ST_N_DEGENERATE = 10  # elastic particles the last P2G scattered without stress (det F not positive normal)
 ST_MAX_SPEED = 13   # fp32 bits of max |v'| + 1.5 dx |C'|_F over the particles the last G2P moved
 ST_N_ESCAPED = 14   # mpm_step_fused: particles whose base cell left their tile (scattered into the global grid)
-MPM_STATUS_WORDS = 16
+ST_RANGE = 15       # fp32 bits of R, the range the last fixed-point P2G checked its bound with
+ST_SHARE_PATH = 16  # the last fixed-point P2G's shares: 0 below 2^22 (one fma each), 1 int64
+ST_P2G_MASS = 20    # record: fp32 bits of max |m| over the particles the last P2G scattered
+ST_P2G_VOLUME = 21  # record: fp32 bits of max rest volume in cells over the same
+ST_G2P_RANGE = 22   # record: fp32 bits of max over the last G2P's particles of max(1, |v'_k| + 1.5 dx sum|C'_kl|)
+MPM_STATUS_WORDS = 24
 MPM_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -48,7 +53,8 @@ class Bins(ct.Structure):
     _fields_ = [("n", ct.c_int64), ("ntiles", ct.c_int64), ("max_slices", ct.c_int64),
                 ("key", ct.c_void_p), ("perm", ct.c_void_p), ("tile_count", ct.c_void_p),
                 ("tile_start", ct.c_void_p), ("slices", ct.c_void_p), ("active", ct.c_void_p),
-                ("status", ct.c_void_p), ("scratch", ct.c_void_p), ("scratch_bytes", ct.c_size_t)]
+                ("status", ct.c_void_p), ("scratch", ct.c_void_p), ("scratch_bytes", ct.c_size_t),
+                ("range_from_g2p", ct.c_int32)]
 
 
 _lock = threading.Lock()

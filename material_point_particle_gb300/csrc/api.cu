@@ -326,7 +326,8 @@ mpm_status mpm_p2g(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bi
     MPM_TRY(parts_f(g, parts, true, p));
     MPM_TRY(check_bins(g, bins, p.n));
     MPM_TRY(device_info(dev));
-    return launch_p2g(g, p, view_of(g, *bins), grid_acc, dt, dev, static_cast<cudaStream_t>(stream));
+    return launch_p2g(g, p, view_of(g, *bins), grid_acc, dt, bins->range_from_g2p != 0, dev,
+                      static_cast<cudaStream_t>(stream));
 }
 
 mpm_status mpm_grid_update(const mpm_grid_desc *desc, void *grid_acc, float *grid_vel, const float dtg[3],

@@ -37,8 +37,8 @@
 //                   global memory above kSmemRuns)
 //   k_emit          perm, position by position; sorts buckets of at most 32
 //                   runs itself
-//   k_nbr_bound     int32 mode: most stencils covering one node (the
-//                   accumulator bound, checked before any scatter)
+//   k_nbr_bound     int32 mode: most stencils covering one node (for the
+//                   accumulator bound mpm_p2g checks before any scatter)
 #include "common.cuh"
 #include "internal.h"
 
@@ -589,7 +589,8 @@ __global__ void __launch_bounds__(256) k_emit(GridP g, const uint32_t *__restric
 
 // --------------------------------------------------------------------------
 // int32 accumulators: for every node, the number of particles whose stencil
-// covers it is the sum of the counts of the 3^dim base cells below it.
+// covers it is the sum of the counts of the 3^dim base cells below it; the
+// most of them enters mpm_p2g's bound.
 __global__ void k_nbr_bound(GridP g, const uint32_t *__restrict__ cellcount, uint32_t *__restrict__ status) {
     uint32_t best = 0;
     for (int64_t node = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; node < g.nodes;
@@ -610,10 +611,7 @@ __global__ void k_nbr_bound(GridP g, const uint32_t *__restrict__ cellcount, uin
         best = max(best, sum);
     }
     for (int d = 16; d > 0; d >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, d));
-    if (lane_id() == 0 && best > 0) {
-        atomicMax(&status[MPM_ST_MAX_NEIGHBOURS], best);
-        if (best > kI32MaxContributions) atomicOr(&status[MPM_ST_FLAGS], (1u << MPM_E_BOUND) | kFlagNoScatter);
-    }
+    if (lane_id() == 0 && best > 0) atomicMax(&status[MPM_ST_MAX_NEIGHBOURS], best);
 }
 
 // --------------------------------------------------------------------------
@@ -621,7 +619,11 @@ mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const De
                       cudaStream_t st) {
     const int64_t n = p.n;
     const int64_t nb = g.ntiles + 1;
-    cudaMemsetAsync(w.status, 0, MPM_STATUS_WORDS * sizeof(uint32_t), st);
+    // every status word but the records of the last P2G and G2P, which the next bound may use
+    static_assert(MPM_ST_G2P_RANGE == MPM_ST_P2G_MASS + 2, "adjacent records");
+    cudaMemsetAsync(w.status, 0, MPM_ST_P2G_MASS * sizeof(uint32_t), st);
+    cudaMemsetAsync(&w.status[MPM_ST_G2P_RANGE + 1], 0, (MPM_STATUS_WORDS - MPM_ST_G2P_RANGE - 1) * sizeof(uint32_t),
+                    st);
     cudaMemsetAsync(w.count, 0, nb * sizeof(uint32_t), st);
     if (w.cellcount) cudaMemsetAsync(w.cellcount, 0, (size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t), st);
     const int threads = 256;

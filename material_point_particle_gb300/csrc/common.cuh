@@ -25,8 +25,9 @@ constexpr int32_t kMagicBits = 0x4B400000;
 constexpr float kShareLimit = 4190208.0f;  // 2^22 - 4096
 // Status flag set by a check that runs before P2G: P2G then scatters nothing.
 constexpr uint32_t kFlagNoScatter = 1u << 16;
-// int32 accumulators: at most this many stencils may cover one node.
-constexpr uint32_t kI32MaxContributions = 511;
+// Status flag set by a scatter that met a particle above the range its bound
+// was checked with: the scatter is undone (k_rollback).
+constexpr uint32_t kFlagRollback = 1u << 17;
 
 // Everything a kernel needs to know about the grid, derived once on the host.
 struct GridP {

@@ -37,7 +37,7 @@ __device__ __noinline__ bool scatter_global(const GridP &g, const float (&rec_v)
     const StressP sp{0.f, 0.f, 0.f, 0.f};
     uint32_t unused = 0;
     auto rec = [&](int fi) { return rec_v[fi]; };
-    return scatter_shares<DIM, false, false>(g, rec, f, ad, sp, unused);
+    return scatter_shares<DIM, false, false, true>(g, rec, f, ad, sp, unused);
 }
 
 // The fused step with one warp per work item (the P2G kernel's shape): each
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
                         const int hb2 = DIM == 3 ? (b2[0] - o[0]) + (b2[1] - o[1]) * Hl::SY + (b2[2] - o[2]) * Hl::SZ
                                                  : (b2[0] - o[0]) + (b2[1] - o[1]) * Hl::SY;
                         const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb2};
-                        if (!scatter_shares<DIM, false, false>(g, rec, f2v, ad, sp, unused)) ++bad;
+                        if (!scatter_shares<DIM, false, false, true>(g, rec, f2v, ad, sp, unused)) ++bad;
                     } else if (scatter_global<DIM>(g, rec_v, b2, f2v, accW)) {
                         ++escaped;
                     } else {
@@ -240,9 +240,9 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
     escaped = __reduce_add_sync(0xFFFFFFFFu, escaped);
     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
     if (lane == 0) {
-        if (bad) {
+        if (bad) {  // the new state does not fit 22-bit shares: this step's scatter is undone
             atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
-            set_flag(status, MPM_E_BOUND);
+            atomicOr(&status[MPM_ST_FLAGS], (1u << MPM_E_BOUND) | kFlagRollback);
         }
         if (escaped) atomicAdd(&status[MPM_ST_N_ESCAPED], escaped);
         if (wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
@@ -300,22 +300,22 @@ mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, con
     const int blocks = dev.sms * 4;
     static_assert(MPM_ST_MAX_SPEED == MPM_ST_WORK_G2P + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
+    cudaMemsetAsync(&w.status[MPM_ST_N_OUT_OF_RANGE], 0, sizeof(uint32_t), st);
     const auto *R = static_cast<const long long *>(acc_read);
     auto *Wr = static_cast<long long *>(acc_write);
     auto *Rc = static_cast<long long *>(acc_read);
     if (g.dim == 3 && g.T == 4) {
         k_g2p2g_w<3, 4><<<blocks, kP2GThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm,
                                                         w.slices, w.start, w.status, dt, c4);
-        launch_copy_rest(g, in, out, w, dev, st);
-        launch_clear_blocks(g, Rc, w, dev, st);
     } else if (g.dim == 2 && g.T == 8) {
         k_g2p2g_w<2, 8><<<blocks, kP2GThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm,
                                                         w.slices, w.start, w.status, dt, c4);
-        launch_copy_rest(g, in, out, w, dev, st);
-        launch_clear_blocks(g, Rc, w, dev, st);
     } else {
         return MPM_E_ARG;
     }
+    launch_copy_rest(g, in, out, w, dev, st);
+    launch_clear_blocks(g, Rc, w, dev, st);
+    launch_rollback(g, Wr, w.status, dev, st);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }
 

@@ -7,6 +7,7 @@
 #include "common.cuh"
 #include "gather.cuh"
 #include "internal.h"
+#include "range.cuh"
 #include "stress.cuh"
 
 namespace mpm {
@@ -44,7 +45,7 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
 template <int DIM, int T, bool MOVED, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
                                            uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
-                                           float dt, float c4, float &smax) {
+                                           float dt, float c4, float &smax, uint32_t &rmax) {
     using Hl = HaloU<DIM, T>;
     float x[DIM], f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
@@ -94,6 +95,8 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     if constexpr (MOVED && (EL || VC)) q.vol[dst] = p.vol[pid];
     if constexpr (VC) q.phi[dst] = gather_phi<DIM, T>(sv, hb, w);
     smax = fmaxf(smax, __fadd_rn(__fsqrt_rn(sv2), __fmul_rn(__fmul_rn(1.5f, g.dx), __fsqrt_rn(sc2))));
+    // the range the next P2G's bound may take from this record: max(1, |v'_k| + 1.5 dx sum_l |C'_kl|)
+    rmax = max(rmax, range_r_bits<DIM>(vn, Cn, __fmul_rn(1.5f, g.dx)));
 #pragma unroll
     for (int l = 0; l < DIM; ++l) q.x[l][dst] = __fmaf_rn(dt, vn[l], x[l]);
     if constexpr (MOVED) {
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     __shared__ uint32_t item_sh;
     float smax = 0.f;  // the advective bound's largest term among this thread's particles
+    uint32_t rmax = 0;  // the range record's largest term
     uint32_t next = 0;
     for (uint32_t s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
         next = ask_item(&status[MPM_ST_WORK_G2P]);
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
             if (threadIdx.x < cnt) {
                 const uint32_t r = threadIdx.x;
                 auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax);
+                gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax, rmax);
             }
         } else {
             class_order<DIM, T, kG2PThreads>(key, pids, cnt, hist, cstart, order);
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
                     const uint32_t e = interleave_entry(pos, cnt);
                     const uint32_t r = order[e + (e >> 5)];
                     auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                    gather_one<DIM, T, true, EL, VC>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax);
+                    gather_one<DIM, T, true, EL, VC>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax, rmax);
                 }
             }
         }
@@ -201,6 +205,7 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
     // non-negative fp32 values order as their bit patterns
     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
     if (lane == 0 && wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
+    warp_max_to(rmax, &status[MPM_ST_G2P_RANGE]);
 }
 
 // G2P with one warp per work item (the P2G kernel's shape), in place or in
@@ -232,6 +237,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     uint32_t *work = &status[MPM_ST_WORK_G2P];
     float smax = 0.f;
+    uint32_t rmax = 0;
     auto at = [&](int stage, int f) { return wb + (stage * NF + f) * 32 + lane; };
     uint32_t s = 0;
     if (lane == 0) s = atomicAdd(work, 1u);
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
                 const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
                 if (r < cnt) {
                     auto rec = [&](int f) { return xc[f]; };
-                    gather_one<DIM, T, false, EL, VC>(g, p, q, pid, pid, rec, o, sv, dt, c4, smax);
+                    gather_one<DIM, T, false, EL, VC>(g, p, q, pid, pid, rec, o, sv, dt, c4, smax, rmax);
                 }
 #pragma unroll
                 for (int l = 0; l < DIM; ++l) xc[l] = xn[l];
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
                     const int st = stage;
                     auto rec = [&](int f) { return *at(st, f); };
                     gather_one<DIM, T, BINORDER, EL, VC>(g, p, q, pid, BINORDER ? beg + r : pid, rec, o, sv, dt, c4,
-                                                         smax);
+                                                         smax, rmax);
                 }
                 stage ^= 1;
             }
@@ -314,6 +320,7 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
     cp_async_wait<0>();
     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
     if (lane == 0 && wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
+    warp_max_to(rmax, &status[MPM_ST_G2P_RANGE]);
 }
 
 // Particles past the sorted in-domain part (outside the domain): copied.
@@ -369,6 +376,7 @@ mpm_status launch_g2p_any(const GridP &g, const float *vel, const PartsF &in, co
                           float dt, const DeviceInfo &dev, cudaStream_t st) {
     static_assert(MPM_ST_MAX_SPEED == MPM_ST_WORK_G2P + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, 2 * sizeof(uint32_t), st);  // work counter, max speed
+    cudaMemsetAsync(&w.status[MPM_ST_G2P_RANGE], 0, sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4)
         launch_g2p_dt<3, 4, OUT>(g, vel, in, out, w, dt, dev, st);
     else if (g.dim == 2 && g.T == 8)

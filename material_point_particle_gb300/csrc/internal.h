@@ -39,8 +39,10 @@ struct DeviceInfo {
 mpm_status device_info(DeviceInfo &out);
 
 mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const DeviceInfo &dev, cudaStream_t st);
-mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt,
+mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt, bool records,
                       const DeviceInfo &dev, cudaStream_t st);
+void launch_rollback(const GridP &g, void *grid_acc, const uint32_t *status, const DeviceInfo &dev,
+                     cudaStream_t st);
 mpm_status launch_grid_update(const GridP &g, void *grid_acc, float *vel, const float dtg[3], const WsView &w,
                               const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_g2p(const GridP &g, const float *vel, const PartsF &p, const WsView &w, float dt,

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
                         rec_v[2 * DIM + DIM * DIM] = xc[DIM];
                         auto rec = [&](int fi) { return rec_v[fi]; };
                         const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb};
-                        if (!scatter_shares<DIM, false, false>(g, rec, f, ad, sp, unused)) ++bad;
+                        if (!scatter_shares<DIM, false, false, true>(g, rec, f, ad, sp, unused)) ++bad;
                     }
                 }
             }

@@ -18,6 +18,7 @@
 // particles, so no halo sum can overflow.
 #include "common.cuh"
 #include "internal.h"
+#include "range.cuh"
 #include "scatter.cuh"
 #include "stress.cuh"
 
@@ -112,29 +113,47 @@ __device__ __forceinline__ SliceMeta slice_meta(const uint32_t *slices, const ui
 // (neighbouring tiles overlap on the halo, so the flush adds).  Particles
 // stored in bank-class interleaved order (the sorted G2P) put the 32 lanes of
 // a round in different banks.
-constexpr int kP2GWarps = kP2GThreads / 32;
+//
+// Two instances, one per share path; the bound check before the scatter
+// (k_bound) picks one and the other returns at once.  WIDE = false: shares
+// below 2^22 (one fma each).  WIDE = true: 64-bit shares (exact integer
+// product), each split into two int32 halves in two halo planes per channel
+// (twice the shared memory, so four warps per block); a particle whose
+// shares could reach 2^43 adds them straight to the global grid instead.
+// `verify` (the bound was taken from the records of the previous P2G and
+// G2P): a particle above that range is not scattered, and the call's scatter
+// is undone afterwards (k_rollback).
+template <bool WIDE, bool EL>
+struct P2GShape {
+    static constexpr int WARPS = WIDE ? 4 : 8;
+    static constexpr int THREADS = WARPS * 32;
+    static constexpr int MIN_BLOCKS = WIDE ? (EL ? 2 : 3) : (EL ? 2 : 3);
+};
 
-template <int DIM, int T, typename AccT, bool EL, bool VC>
-__global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
+template <int DIM, int T, typename AccT, bool EL, bool VC, bool WIDE>
+__global__ void __launch_bounds__(P2GShape<WIDE, EL>::THREADS, P2GShape<WIDE, EL>::MIN_BLOCKS)
     k_p2g_fixed(GridP g, PartsF p, const uint32_t *__restrict__ perm, const uint32_t *__restrict__ slices,
                 const uint32_t *__restrict__ start, uint32_t *__restrict__ status, AccT *__restrict__ acc,
-                StressP sp) {
-    using St = Stencil<DIM>;
+                StressP sp, int verify) {
     using Hl = HaloU<DIM, T>;
     using Fl = P2GFields<DIM, EL, VC>;
-    constexpr int NCH = St::NC + (VC ? 1 : 0);  // accumulator channels
-    constexpr int HW = NCH * Hl::NODES;         // halo words per warp
-    __shared__ __align__(16) int32_t shalo[kP2GWarps][HW];
+    using Sh = P2GShape<WIDE, EL>;
+    constexpr int NCH = Stencil<DIM>::NC + (VC ? 1 : 0);  // accumulator channels
+    constexpr int HW = (WIDE ? 2 : 1) * NCH * Hl::NODES;  // halo words per warp
+    __shared__ __align__(16) int32_t shalo[Sh::WARPS][HW];
     // with the elastic state the whole record is staged in shared memory (at two blocks per SM
     // register loads' latency would not hide behind other warps); otherwise nothing is
     constexpr int NS = EL ? Fl::NF : 1;
-    __shared__ float sbuf[kP2GWarps][EL ? 2 * NS * 32 : 1];
+    __shared__ float sbuf[Sh::WARPS][EL ? 2 * NS * 32 : 1];
     if (status[MPM_ST_FLAGS] & kFlagNoScatter) return;
+    if (status[MPM_ST_SHARE_PATH] != (WIDE ? 1u : 0u)) return;
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     int32_t *wh = shalo[warp];
     float *wb = sbuf[warp];
     const uint32_t halo = (uint32_t)__cvta_generic_to_shared(wh);
     const uint32_t nslices = status[MPM_ST_N_SLICES];
+    const uint32_t Rrec = status[MPM_ST_RANGE];
+    const float h = __fmul_rn(1.5f, g.dx);
     uint32_t *work = &status[MPM_ST_WORK_P2G];
     for (int i = lane; i < HW; i += 32) wh[i] = 0;
     __syncwarp();
@@ -143,7 +162,7 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
 #pragma unroll
         for (int f = 0; f < NS; ++f) cp_async4(at(stage, f), Fl::src(p, f) + pid);
     };
-    uint32_t s = 0, degenerate = 0;
+    uint32_t s = 0, degenerate = 0, mrec = 0, qrec = 0;
     if (lane == 0) s = atomicAdd(work, 1u);
     s = __shfl_sync(0xFFFFFFFFu, s, 0);
     while (s < nslices) {
@@ -156,31 +175,74 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
         // every nonzero halo entry added to the grid once, and cleared
         auto flush = [&]() {
             __syncwarp();
-            for (int h = lane; h < Hl::NODES; h += 32) {
+            for (int hh = lane; hh < Hl::NODES; hh += 32) {
                 int hx, hy, hz;
-                Hl::node(h, hx, hy, hz);
+                Hl::node(hh, hx, hy, hz);
                 const int gx = o[0] + hx, gy = o[1] + hy, gz = o[2] + hz;
                 const bool on = gx < g.n[0] && gy < g.n[1] && (DIM == 2 || gz < g.n[2]);
                 const int64_t node = node_index(g, gx, gy, gz);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
-                    const int32_t val = wh[c * Hl::NODES + h];
+                    long long val = wh[c * Hl::NODES + hh];
+                    if constexpr (WIDE) val += (long long)wh[(NCH + c) * Hl::NODES + hh] * (1ll << 22);
                     if (val == 0) continue;
-                    wh[c * Hl::NODES + h] = 0;
+                    wh[c * Hl::NODES + hh] = 0;
+                    if constexpr (WIDE) wh[(NCH + c) * Hl::NODES + hh] = 0;
                     if (!on) continue;
                     if constexpr (sizeof(AccT) == 8)
                         atomicAdd(reinterpret_cast<unsigned long long *>(acc + c * g.nodes + node),
-                                  (unsigned long long)(long long)val);
+                                  (unsigned long long)val);
                     else
-                        atomicAdd(reinterpret_cast<int *>(acc + c * g.nodes + node), val);
+                        atomicAdd(reinterpret_cast<int *>(acc + c * g.nodes + node), (int)val);
                 }
             }
             __syncwarp();
         };
+        // one particle: false when it is not scattered (not in this tile's box, or above the
+        // recorded range)
+        auto one = [&](const auto &rec) -> bool {
+            float xs[DIM], f[3] = {0.f, 0.f, 0.f};
+            int b[3] = {0, 0, 0};
+#pragma unroll
+            for (int l = 0; l < DIM; ++l) xs[l] = rec(l);
+            if (!in_box_x<DIM, T>(g, xs, o, b, f)) return false;
+            const float m = rec(2 * DIM + DIM * DIM);
+            [[maybe_unused]] float q = 0.f;
+            if constexpr (VC) q = __fmul_rn(rec(Fl::VOLF), g.vcell);
+            mrec = max_bits(mrec, fabsf(m));
+            if constexpr (VC) qrec = max_bits(qrec, fabsf(q));
+            const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
+                                    : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
+            float v[DIM], C[DIM * DIM];
+#pragma unroll
+            for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
+            if constexpr (!WIDE) {
+                if (verify) {
+#pragma unroll
+                    for (int j = 0; j < DIM * DIM; ++j) C[j] = rec(2 * DIM + j);
+                    if (particle_range_bits<VC>(range_r_bits<DIM>(v, C, h), m, q) > Rrec) return false;
+                }
+                const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb};
+                scatter_shares<DIM, EL, VC, false>(g, rec, f, ad, sp, degenerate);
+            } else {
+                load_affine<DIM, EL, VC>(rec, sp, C, degenerate);
+                const uint32_t Rp = particle_range_bits<VC>(range_r_bits<DIM>(v, C, h), m, q);
+                if (verify && Rp > Rrec) return false;
+                if (__fmul_rn(__uint_as_float(Rp), g.S) <= 0x1p42f) {
+                    const SharedAdd64<Hl, NCH> ad{halo + 4u * (uint32_t)hb};
+                    scatter_shares_wide<DIM, EL, VC>(g, rec, f, ad, v, C);
+                } else {  // shares that could reach 2^43: straight to the grid
+                    const GlobalAdd64<DIM, AccT> ad{acc, g.nodes, g.n[0], (int64_t)g.n[0] * g.n[1],
+                                                    node_index(g, b[0], b[1], DIM == 3 ? b[2] : 0)};
+                    scatter_shares_wide<DIM, EL, VC>(g, rec, f, ad, v, C);
+                }
+            }
+            return true;
+        };
         uint32_t bad = 0;
         const uint32_t rounds = (cnt + 31) / 32;
         // the int32 halo accumulators are flushed every 16 rounds: at most 512
-        // shares of magnitude below 2^22 reach one entry between two flushes
+        // shares reach one entry between two flushes
         // perm is read one round ahead of its use, so no round waits on it
         uint32_t pid = lane < cnt ? perm[beg + lane] : 0u;
         uint32_t pid_next = lane + 32 < cnt ? perm[beg + lane + 32] : 0u;
@@ -189,8 +251,8 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
             float xc[DIM], xn[DIM];
 #pragma unroll
             for (int l = 0; l < DIM; ++l) xc[l] = lane < cnt ? p.x[l][pid] : 0.f;
-            for (uint32_t q = 0; q < rounds; ++q) {
-                const uint32_t r = q * 32 + lane;
+            for (uint32_t qq = 0; qq < rounds; ++qq) {
+                const uint32_t r = qq * 32 + lane;
 #pragma unroll
                 for (int l = 0; l < DIM; ++l) xn[l] = r + 32 < cnt ? p.x[l][pid_next] : 0.f;
                 const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
@@ -199,48 +261,128 @@ __global__ void __launch_bounds__(kP2GThreads, EL ? 2 : 3)
 #pragma unroll
                     for (int f = DIM; f < Fl::NF; ++f) rest[f - DIM] = Fl::src(p, f)[pid];
                     auto rec = [&](int f) { return f < DIM ? xc[f] : rest[f - DIM]; };
-                    if (!scatter_fixed<DIM, T, Hl, EL, VC>(g, rec, o, halo, sp, degenerate)) ++bad;
+                    if (!one(rec)) ++bad;
                 }
 #pragma unroll
                 for (int l = 0; l < DIM; ++l) xc[l] = xn[l];
                 pid = pid_next;
                 pid_next = pid_after;
-                if ((q + 1) % 16 == 0 && q + 1 < rounds) flush();
+                if ((qq + 1) % 16 == 0 && qq + 1 < rounds) flush();
             }
         } else {
             // the whole record copied into shared memory (cp.async) a round ahead
             if (lane < cnt) issue(0, pid);
             cp_async_commit();
             int stage = 0;
-            for (uint32_t q = 0; q < rounds; ++q) {
-                const uint32_t r = q * 32 + lane;
-                if (q + 1 < rounds && r + 32 < cnt) issue(stage ^ 1, pid_next);
+            for (uint32_t qq = 0; qq < rounds; ++qq) {
+                const uint32_t r = qq * 32 + lane;
+                if (qq + 1 < rounds && r + 32 < cnt) issue(stage ^ 1, pid_next);
                 const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
                 cp_async_commit();
                 cp_async_wait<1>();
                 if (r < cnt) {
                     const int st = stage;
                     auto rec = [&](int f) { return *at(st, f); };
-                    if (!scatter_fixed<DIM, T, Hl, EL, VC>(g, rec, o, halo, sp, degenerate)) ++bad;
+                    if (!one(rec)) ++bad;
                 }
                 stage ^= 1;
                 pid_next = pid_after;
-                if ((q + 1) % 16 == 0 && q + 1 < rounds) flush();
+                if ((qq + 1) % 16 == 0 && qq + 1 < rounds) flush();
             }
         }
         flush();
         bad = __reduce_add_sync(0xFFFFFFFFu, bad);
         if (bad && lane == 0) {
             atomicAdd(&status[MPM_ST_N_OUT_OF_RANGE], bad);
-            set_flag(status, MPM_E_BOUND);
+            atomicOr(&status[MPM_ST_FLAGS], (1u << MPM_E_BOUND) | kFlagRollback);
         }
         s = __shfl_sync(0xFFFFFFFFu, ask, 0);
     }
     cp_async_wait<0>();
+    warp_max_to(mrec, &status[MPM_ST_P2G_MASS]);
+    if constexpr (VC) warp_max_to(qrec, &status[MPM_ST_P2G_VOLUME]);
     if constexpr (EL) {
         degenerate = __reduce_add_sync(0xFFFFFFFFu, degenerate);
         if (degenerate && lane == 0) atomicAdd(&status[MPM_ST_N_DEGENERATE], degenerate);
     }
+}
+
+// --------------------------------------------------------------------------
+// The bound before the scatter ("particle to grid transfer in checked integer
+// arithmetic", the program: the bounds line runs first, and if it fails
+// nothing is scattered).
+
+// R = max of R_p over the binned (in-domain) particles, read from the state
+// P2G is about to scatter (elastic particles: the stress-folded matrix).
+template <int DIM, bool EL, bool VC>
+__global__ void __launch_bounds__(256) k_range(GridP g, PartsF p, const uint32_t *__restrict__ key,
+                                               uint32_t *__restrict__ status, StressP sp) {
+    using Fl = P2GFields<DIM, EL, VC>;
+    const float h = __fmul_rn(1.5f, g.dx);
+    uint32_t Rb = 0, unused = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += (int64_t)gridDim.x * blockDim.x) {
+        if (key[i] == kKeyInvalid) continue;
+        auto rec = [&](int f) { return Fl::src(p, f)[i]; };
+        float v[DIM], C[DIM * DIM];
+#pragma unroll
+        for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
+        load_affine<DIM, EL, VC>(rec, sp, C, unused);
+        [[maybe_unused]] float q = 0.f;
+        if constexpr (VC) q = __fmul_rn(rec(Fl::VOLF), g.vcell);
+        Rb = max(Rb, particle_range_bits<VC>(range_r_bits<DIM>(v, C, h), rec(2 * DIM + DIM * DIM), q));
+    }
+    warp_max_to(Rb, &status[MPM_ST_RANGE]);
+}
+
+// One thread: R from the pass above or from the records, then the test the
+// oracle states (fp64, this order): B = S*R*(1 + 2^-10) + 28, count * B within
+// 2^62 (int64) or 2^31 - 1024 (int32, count = most stencils covering a node).
+// Failing, P2G scatters nothing; passing, the share path is chosen.
+__global__ void k_bound(GridP g, uint32_t *__restrict__ status, int from_records) {
+    if (threadIdx.x != 0) return;
+    uint32_t flags = status[MPM_ST_FLAGS] & ~((1u << MPM_E_BOUND) | kFlagNoScatter | kFlagRollback);
+    uint32_t Rb;
+    if (from_records) {
+        const float M = __uint_as_float(status[MPM_ST_P2G_MASS]);
+        const float rG = __uint_as_float(status[MPM_ST_G2P_RANGE]);
+        Rb = __float_as_uint(__fmul_rn(M, rG));
+        if (isnan(M) || isnan(rG)) Rb = 0x7FFFFFFFu;
+        if (g.vc) Rb = max(Rb, status[MPM_ST_P2G_VOLUME]);
+        status[MPM_ST_RANGE] = Rb;
+    } else {
+        Rb = status[MPM_ST_RANGE];
+    }
+    const double R = (double)__uint_as_float(Rb);
+    const double S = (double)g.S;
+    const double B = __dadd_rn(__dmul_rn(__dmul_rn(S, R), 1.0 + 0x1p-10), 28.0);
+    const uint32_t count = g.acc_mode == MPM_ACC_I32 ? status[MPM_ST_MAX_NEIGHBOURS] : status[MPM_ST_N_VALID];
+    const double limit = g.acc_mode == MPM_ACC_I32 ? 2147482624.0 : 0x1p62;
+    if (!(__dmul_rn((double)count, B) <= limit)) {
+        flags |= (1u << MPM_E_BOUND) | kFlagNoScatter;
+    } else {
+        const double fast = __dmul_rn(__dmul_rn(__dmul_rn((double)g.wmax, S), R), 1.0 + 0x1p-10);
+        status[MPM_ST_SHARE_PATH] = fast <= (double)kShareLimit ? 0u : 1u;
+    }
+    status[MPM_ST_FLAGS] = flags;
+}
+
+// Undoes a scatter whose particles broke the range it was checked with: the
+// grid was zero on entry, so it is cleared again.  Returns at once otherwise.
+template <typename AccT>
+__global__ void __launch_bounds__(256) k_rollback(AccT *__restrict__ acc, int64_t words,
+                                                  const uint32_t *__restrict__ status) {
+    if (!(status[MPM_ST_FLAGS] & kFlagRollback)) return;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += (int64_t)gridDim.x * blockDim.x)
+        acc[i] = 0;
+}
+
+void launch_rollback(const GridP &g, void *grid_acc, const uint32_t *status, const DeviceInfo &dev,
+                     cudaStream_t st) {
+    const int64_t words = (int64_t)(g.dim + 1 + g.vc) * g.nodes;
+    if (g.acc_mode == MPM_ACC_I32)
+        k_rollback<int32_t><<<dev.sms * 4, 256, 0, st>>>((int32_t *)grid_acc, words, status);
+    else
+        k_rollback<long long><<<dev.sms * 4, 256, 0, st>>>((long long *)grid_acc, words, status);
 }
 
 // Float-atomic P2G (comparison variant: fp32 adds, order dependent).
@@ -299,45 +441,67 @@ __global__ void __launch_bounds__(kP2GThreads) k_p2g_float(GridP g, PartsF p, co
     }
 }
 
+template <int DIM, int T, typename AccT, bool EL, bool VC>
+void launch_p2g_fixed(const GridP &g, const PartsF &p, const WsView &w, AccT *acc, const StressP &sp, int verify,
+                      const DeviceInfo &dev, cudaStream_t st) {
+    // both share paths; the one k_bound did not pick returns at once
+    k_p2g_fixed<DIM, T, AccT, EL, VC, false><<<dev.sms * 4, P2GShape<false, EL>::THREADS, 0, st>>>(
+        g, p, w.perm, w.slices, w.start, w.status, acc, sp, verify);
+    k_p2g_fixed<DIM, T, AccT, EL, VC, true><<<dev.sms * 8, P2GShape<true, EL>::THREADS, 0, st>>>(
+        g, p, w.perm, w.slices, w.start, w.status, acc, sp, verify);
+}
+
 template <int DIM, int T, bool EL, bool VC>
-void launch_p2g_t(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const StressP &sp, int blocks,
-                  cudaStream_t st) {
+void launch_p2g_t(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const StressP &sp,
+                  bool records, const DeviceInfo &dev, cudaStream_t st) {
+    if (g.acc_mode == MPM_ACC_F32) {
+        k_p2g_float<DIM, T, EL, VC><<<dev.sms * 4, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start,
+                                                                         w.status, (float *)grid_acc, sp);
+        return;
+    }
+    // the bound, before any particle is scattered
+    static_assert(MPM_ST_SHARE_PATH == MPM_ST_RANGE + 1, "adjacent status words");
+    cudaMemsetAsync(&w.status[MPM_ST_RANGE], 0, 2 * sizeof(uint32_t), st);
+    if (!records && p.n > 0) {
+        const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((p.n + 255) / 256, dev.sms * 8));
+        k_range<DIM, EL, VC><<<blocks, 256, 0, st>>>(g, p, w.key, w.status, sp);
+    }
+    k_bound<<<1, 32, 0, st>>>(g, w.status, records ? 1 : 0);
+    // this call's records (the previous ones were read by k_bound)
+    static_assert(MPM_ST_P2G_VOLUME == MPM_ST_P2G_MASS + 1, "adjacent status words");
+    cudaMemsetAsync(&w.status[MPM_ST_P2G_MASS], 0, 2 * sizeof(uint32_t), st);
     if (g.acc_mode == MPM_ACC_I64)
-        k_p2g_fixed<DIM, T, int64_t, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start,
-                                                                            w.status, (int64_t *)grid_acc, sp);
-    else if (g.acc_mode == MPM_ACC_I32)
-        k_p2g_fixed<DIM, T, int32_t, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start,
-                                                                            w.status, (int32_t *)grid_acc, sp);
+        launch_p2g_fixed<DIM, T, long long, EL, VC>(g, p, w, (long long *)grid_acc, sp, records, dev, st);
     else
-        k_p2g_float<DIM, T, EL, VC><<<blocks, kP2GThreads, 0, st>>>(g, p, w.perm, w.slices, w.start, w.status,
-                                                                   (float *)grid_acc, sp);
+        launch_p2g_fixed<DIM, T, int32_t, EL, VC>(g, p, w, (int32_t *)grid_acc, sp, records, dev, st);
+    if (records) launch_rollback(g, grid_acc, w.status, dev, st);
 }
 
 template <int DIM, int T>
-void launch_p2g_dt(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const StressP &sp, int blocks,
-                   cudaStream_t st) {
+void launch_p2g_dt(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, const StressP &sp,
+                   bool records, const DeviceInfo &dev, cudaStream_t st) {
     const bool el = p.F[0] != nullptr;
     if (el && g.vc)
-        launch_p2g_t<DIM, T, true, true>(g, p, w, grid_acc, sp, blocks, st);
+        launch_p2g_t<DIM, T, true, true>(g, p, w, grid_acc, sp, false, dev, st);
     else if (el)
-        launch_p2g_t<DIM, T, true, false>(g, p, w, grid_acc, sp, blocks, st);
+        launch_p2g_t<DIM, T, true, false>(g, p, w, grid_acc, sp, false, dev, st);
     else if (g.vc)
-        launch_p2g_t<DIM, T, false, true>(g, p, w, grid_acc, sp, blocks, st);
+        launch_p2g_t<DIM, T, false, true>(g, p, w, grid_acc, sp, records, dev, st);
     else
-        launch_p2g_t<DIM, T, false, false>(g, p, w, grid_acc, sp, blocks, st);
+        launch_p2g_t<DIM, T, false, false>(g, p, w, grid_acc, sp, records, dev, st);
 }
 
-mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt,
+mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt, bool records,
                       const DeviceInfo &dev, cudaStream_t st) {
-    const int blocks = dev.sms * 4;
     const StressP sp{p.mu, p.lam, dt, (4.0f * g.inv_dx) * g.inv_dx};
-    // degenerate-particle count and work counter
+    // degenerate-particle count, work counter, particles above the range
     static_assert(MPM_ST_WORK_P2G == MPM_ST_N_DEGENERATE + 1, "adjacent status words");
     cudaMemsetAsync(&w.status[MPM_ST_N_DEGENERATE], 0, 2 * sizeof(uint32_t), st);
+    cudaMemsetAsync(&w.status[MPM_ST_N_OUT_OF_RANGE], 0, sizeof(uint32_t), st);
     if (g.dim == 3 && g.T == 4)
-        launch_p2g_dt<3, 4>(g, p, w, grid_acc, sp, blocks, st);
+        launch_p2g_dt<3, 4>(g, p, w, grid_acc, sp, records, dev, st);
     else if (g.dim == 2 && g.T == 8)
-        launch_p2g_dt<2, 8>(g, p, w, grid_acc, sp, blocks, st);
+        launch_p2g_dt<2, 8>(g, p, w, grid_acc, sp, records, dev, st);
     else
         return MPM_E_ARG;
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;

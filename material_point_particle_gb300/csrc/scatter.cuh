@@ -9,6 +9,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "range.cuh"
 #include "stress.cuh"
 
 namespace mpm {
@@ -78,26 +79,12 @@ __device__ __forceinline__ void load_affine(const Rec &rec, const StressP &sp, f
     }
 }
 
-// One particle's fixed-point shares, handed to `ad` as they are formed (the
-// arithmetic the oracle states).  Returns false (and adds nothing) when the
-// particle is out of range.  f: the fractions of its stencil base cell.
-// rec(f) reads field f of the particle (P2GFields: x[dim], v[dim],
-// C[dim*dim], m, then F[dim*dim] for elastic particles, and vol).  With the
-// volume channel (VC) the rest volume in cells, Vt = (vol * inv_dx^dim) * S,
-// is split over the stencil as the mass is, into channel dim + 1.
-template <int DIM, bool EL, bool VC, typename Rec, typename Add>
-__device__ __forceinline__ bool scatter_shares(const GridP &g, const Rec &rec, const float (&f)[3], const Add &ad,
-                                               const StressP &sp, uint32_t &degenerate) {
-    using Fl = P2GFields<DIM, EL, VC>;
-    using St = Stencil<DIM>;
-    float v[DIM], C[DIM * DIM];
-#pragma unroll
-    for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
-    load_affine<DIM, EL, VC>(rec, sp, C, degenerate);
-    const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
-    [[maybe_unused]] float Vt = 0.f;
-    if constexpr (VC) Vt = __fmul_rn(__fmul_rn(rec(Fl::VOLF), g.vcell), g.S);
-    // range: wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) (and wmax*|Vt|) at most 2^22 - 4096
+// True when every share of the particle stays below 2^22 in magnitude:
+// wmax*|Mt| and wmax*|Mt|*(|v_k| + 1.5 dx sum_l |C_kl|) (and wmax*|Vt|) at most
+// 2^22 - 4096, which also keeps the centre's remainder below 2^22.
+template <int DIM, bool VC>
+__device__ __forceinline__ bool shares_fit_22(const GridP &g, const float (&v)[DIM], const float (&C)[DIM * DIM],
+                                              float Mt, float Vt) {
     const float h = __fmul_rn(1.5f, g.dx);
     const float aM = fabsf(Mt);
     bool ok = __fmul_rn(g.wmax, aM) <= kShareLimit;
@@ -109,7 +96,34 @@ __device__ __forceinline__ bool scatter_shares(const GridP &g, const Rec &rec, c
         const float R = __fmul_rn(aM, __fadd_rn(fabsf(v[k]), __fmul_rn(h, sc)));
         ok = ok && (__fmul_rn(g.wmax, R) <= kShareLimit);
     }
-    if (!ok) return false;
+    return ok;
+}
+
+// One particle's fixed-point shares below 2^22, handed to `ad` as they are
+// formed (the arithmetic the oracle states; one fp32 fma against 1.5*2^23
+// leaves rint of the exact product in the low mantissa bits).  The caller
+// guarantees the range (the P2G bound), or asks for the test (CHECK: the
+// fused kernels, whose new state is formed in the same kernel); then the
+// function returns false and adds nothing for a particle out of that range.
+// f: the fractions of its stencil base cell.
+// rec(f) reads field f of the particle (P2GFields: x[dim], v[dim],
+// C[dim*dim], m, then F[dim*dim] for elastic particles, and vol).  With the
+// volume channel (VC) the rest volume in cells, Vt = (vol * inv_dx^dim) * S,
+// is split over the stencil as the mass is, into channel dim + 1.
+template <int DIM, bool EL, bool VC, bool CHECK, typename Rec, typename Add>
+__device__ __forceinline__ bool scatter_shares(const GridP &g, const Rec &rec, const float (&f)[3], const Add &ad,
+                                               const StressP &sp, uint32_t &degenerate) {
+    using Fl = P2GFields<DIM, EL, VC>;
+    using St = Stencil<DIM>;
+    float v[DIM], C[DIM * DIM];
+#pragma unroll
+    for (int k = 0; k < DIM; ++k) v[k] = rec(DIM + k);
+    load_affine<DIM, EL, VC>(rec, sp, C, degenerate);
+    const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
+    [[maybe_unused]] float Vt = 0.f;
+    if constexpr (VC) Vt = __fmul_rn(__fmul_rn(rec(Fl::VOLF), g.vcell), g.S);
+    if constexpr (CHECK)
+        if (!shares_fit_22<DIM, VC>(g, v, C, Mt, Vt)) return false;
     float w[3][3], dd[3][3];
 #pragma unroll
     for (int l = 0; l < DIM; ++l) {
@@ -183,8 +197,9 @@ __device__ __forceinline__ bool scatter_shares(const GridP &g, const Rec &rec, c
 
 // scatter_shares into a shared-memory tile accumulator `halo` (layout Hl)
 // covering the stencils of base cells in the box [o, o + TB) per axis.
-// False when the particle is outside the domain or the box, or out of range.
-template <int DIM, int TB, typename Hl, bool EL, bool VC, typename Rec>
+// False when the particle is outside the domain or the box, or (CHECK) out of
+// the 22-bit range.
+template <int DIM, int TB, typename Hl, bool EL, bool VC, bool CHECK, typename Rec>
 __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo,
                                               const StressP &sp, uint32_t &degenerate) {
     float f[3] = {0.f, 0.f, 0.f};
@@ -196,7 +211,120 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
     const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
                             : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
     const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb};
-    return scatter_shares<DIM, EL, VC>(g, rec, f, ad, sp, degenerate);
+    return scatter_shares<DIM, EL, VC, CHECK>(g, rec, f, ad, sp, degenerate);
+}
+
+// --------------------------------------------------------------------------
+// Shares of any size (up to the bound): the same values as scatter_shares,
+// each the exact product rounded once (rint_prod64), as int64.
+
+// A 64-bit share into the shared-memory tile accumulator: split as
+// s = hi * 2^22 + lo, lo the sign-extended low 22 bits, each half added to its
+// own int32 plane (lo planes at channel c, hi planes at NCH + c).  Between two
+// flushes at most 512 shares reach one entry, so the lo sums stay below 2^30
+// and the hi sums below 2^31 for shares below 2^43.
+template <typename Hl, int NCH>
+struct SharedAdd64 {
+    uint32_t base;
+    template <int C, int A>
+    __device__ __forceinline__ void add(long long s) const {
+        const int32_t lo = ((int32_t)((uint32_t)s << 10)) >> 10;
+        const int32_t hi = (int32_t)((s - lo) >> 22);
+        red_shared_add<4 * (Hl::off(A) + C * Hl::SIZE)>(base, lo);
+        red_shared_add<4 * (Hl::off(A) + (NCH + C) * Hl::SIZE)>(base, hi);
+    }
+};
+
+// A 64-bit share straight into the global grid (int64, or int32 where the
+// bound keeps every node sum in range); node0 = the stencil's first node.
+template <int DIM, typename AccT>
+struct GlobalAdd64 {
+    AccT *acc;
+    int64_t nodes, n0, n01, node0;
+    template <int C, int A>
+    __device__ __forceinline__ void add(long long s) const {
+        constexpr int a0 = DIM == 3 ? A / 9 : A / 3;
+        constexpr int a1 = DIM == 3 ? (A / 3) % 3 : A % 3;
+        constexpr int a2 = DIM == 3 ? A % 3 : 0;
+        AccT *at = acc + C * nodes + node0 + a0 + a1 * n0 + a2 * n01;
+        if constexpr (sizeof(AccT) == 8)
+            atomicAdd(reinterpret_cast<unsigned long long *>(at), (unsigned long long)s);
+        else
+            atomicAdd(reinterpret_cast<int *>(at), (int)s);
+    }
+};
+
+// One particle's shares of any size, handed to `ad` as 64-bit integers:
+// s_m(a) = rint(Wt(a)) and s_k(a) = rint(Wt(a) * vel_k(a)) of the exact
+// product, the centre the remainder, in the same order of fp32 operations as
+// scatter_shares, so the values are the same wherever both apply.
+template <int DIM, bool EL, bool VC, typename Rec, typename Add>
+__device__ __forceinline__ void scatter_shares_wide(const GridP &g, const Rec &rec, const float (&f)[3],
+                                                    const Add &ad, const float (&v)[DIM],
+                                                    const float (&C)[DIM * DIM]) {
+    using Fl = P2GFields<DIM, EL, VC>;
+    using St = Stencil<DIM>;
+    const float Mt = __fmul_rn(rec(2 * DIM + DIM * DIM), g.S);
+    [[maybe_unused]] float Vt = 0.f;
+    if constexpr (VC) Vt = __fmul_rn(__fmul_rn(rec(Fl::VOLF), g.vcell), g.S);
+    float w[3][3], dd[3][3];
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) {
+        quad_weights(f[l], w[l]);
+#pragma unroll
+        for (int a = 0; a < 3; ++a) dd[l][a] = __fmul_rn(__fsub_rn((float)a, f[l]), g.dx);
+    }
+    long long rest[St::NC + 1];
+    rest[0] = __float2ll_rn(Mt);
+    rest[St::NC] = VC ? __float2ll_rn(Vt) : 0ll;
+#pragma unroll
+    for (int k = 0; k < DIM; ++k) rest[1 + k] = __float2ll_rn(__fmul_rn(Mt, v[k]));
+    static_for<3>([&](auto A0) {
+        constexpr int a0 = decltype(A0)::value;
+        const float Wx = __fmul_rn(w[0][a0], Mt);
+        [[maybe_unused]] float Vx = 0.f;
+        if constexpr (VC) Vx = __fmul_rn(w[0][a0], Vt);
+        float h0[DIM];
+#pragma unroll
+        for (int k = 0; k < DIM; ++k) h0[k] = __fmaf_rn(C[k * DIM + 0], dd[0][a0], v[k]);
+        static_for<3>([&](auto A1) {
+            constexpr int a1 = decltype(A1)::value;
+            const float Wxy = __fmul_rn(Wx, w[1][a1]);
+            [[maybe_unused]] float Vxy = 0.f;
+            if constexpr (VC) Vxy = __fmul_rn(Vx, w[1][a1]);
+            float h1[DIM];
+#pragma unroll
+            for (int k = 0; k < DIM; ++k) h1[k] = __fmaf_rn(C[k * DIM + 1], dd[1][a1], h0[k]);
+            static_for<(DIM == 3 ? 3 : 1)>([&](auto A2) {
+                constexpr int a2 = decltype(A2)::value;
+                constexpr int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
+                if constexpr (a != St::CENTRE) {
+                    const float Wt = DIM == 3 ? __fmul_rn(Wxy, w[2][a2]) : Wxy;
+                    const long long sm = __float2ll_rn(Wt);
+                    rest[0] -= sm;
+                    ad.template add<0, a>(sm);
+                    if constexpr (VC) {
+                        const long long sv = __float2ll_rn(DIM == 3 ? __fmul_rn(Vxy, w[2][a2]) : Vxy);
+                        rest[St::NC] -= sv;
+                        ad.template add<DIM + 1, a>(sv);
+                    }
+                    static_for<DIM>([&](auto K) {
+                        constexpr int k = decltype(K)::value;
+                        const float vel = DIM == 3 ? __fmaf_rn(C[k * DIM + 2], dd[2][a2], h1[k]) : h1[k];
+                        const long long sk = rint_prod64(Wt, vel);
+                        rest[1 + k] -= sk;
+                        ad.template add<1 + k, a>(sk);
+                    });
+                }
+            });
+        });
+    });
+    ad.template add<0, St::CENTRE>(rest[0]);
+    static_for<DIM>([&](auto K) {
+        constexpr int k = decltype(K)::value;
+        ad.template add<1 + k, St::CENTRE>(rest[1 + k]);
+    });
+    if constexpr (VC) ad.template add<DIM + 1, St::CENTRE>(rest[St::NC]);
 }
 
 }  // namespace mpm

@@ -102,6 +102,12 @@ class MPMSystem:
         C = self.C.cpu().numpy() if self.C is not None else None
         return self.x.cpu().numpy(), self.v.cpu().numpy(), C
 
+    def use_range_records(self, on: bool = True):
+        """With ``on``, mpm_p2g takes its bound's range from the records the last P2G and
+        G2P on these bins wrote instead of a pass over v, C and m (see mpm_p2g)."""
+        self.bins.range_from_g2p = 1 if on else 0
+        return self
+
     # -- the library calls ----------------------------------------------------
     def bin(self, stream=None):
         L.mpm_bin(self.desc, self.parts, self.bins, 0, stream)

@@ -68,7 +68,7 @@ def test_elastic_step_fixed_bit_exact(dim, mode, scale, n, count):
     assert degenerate == 2
     st = sys.status()
     assert st[L.ST_N_DEGENERATE] == degenerate
-    assert st[L.ST_N_OUT_OF_RANGE] == ocounts[1]
+    assert ocounts[1] == 0 and st[L.ST_N_OUT_OF_RANGE] == 0 and not st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
     assert np.array_equal(acc, oacc)
     sys.grid_update()
     vel = sys.vel.cpu().numpy()

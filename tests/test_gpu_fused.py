@@ -51,7 +51,7 @@ def run_and_check(cloud, steps):
         # the next accumulators: the oracle's P2G of the new state
         nacc, _, counts = O.p2g_fixed(grid, x, v, C, m)
         assert np.array_equal(sys.acc.cpu().numpy(), nacc)
-        assert st[L.ST_N_OUT_OF_RANGE] == counts[1]
+        assert st[L.ST_N_OUT_OF_RANGE] == 0 and counts[1] == 0
         assert not sys.acc2.any().item(), "the accumulators read must be cleared"
         # the order is bin order: out[j] = in[perm[j]] (indices into this step's input, whose ids are prev_ids)
         key, perm, cnt = sys.bins_arrays()
@@ -90,3 +90,27 @@ def test_fused_is_refused_outside_its_scope():
     with pytest.raises(L.MPMError) as e:
         L.mpm_step_fused(sys.desc, sys.parts, sys.parts2, sys.bins, sys.acc, acc2, sys.dt, sys.dtg)
     assert e.value.code == L.MPM_E_ARG
+
+
+def test_fused_step_beyond_22_bit_shares_is_undone():
+    """The fused step forms its new state and scatters it in one kernel, so it can
+    only test each particle as it goes: a particle whose new shares would not fit
+    22 bits (mass 10^5 at S = 2^19) undoes the step's scatter (the written grid is
+    left zero) and sets the bound flag; the gathered state is still the oracle's."""
+    cloud = W.small_cloud(3, 6007, 32, seed=3100, scale_log2=19, lo=0.2, hi=0.8)
+    cloud["m"][123] = 1e5
+    grid = cloud["grid"]
+    sys = fused_system(cloud)
+    st = sys.status()
+    assert st[L.ST_SHARE_PATH] == 1 and not st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
+    sys.step_fused()
+    st = sys.status()
+    assert st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
+    assert st[L.ST_N_OUT_OF_RANGE] == 1
+    assert not sys.acc.any().item() and not sys.acc2.any().item()
+    acc, _, _ = O.p2g_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    x, v, C, _ = O.g2p(grid, O.grid_update_fixed(grid, acc), cloud["x"], cloud["v"], cloud["C"])
+    ids = sys.id.cpu().numpy().astype(np.int64)
+    gx, gv, gC = sys.state()
+    for a, b in ((gx, x), (gv, v), (gC, C)):
+        assert np.array_equal(bits(a), bits(b[:, ids]))

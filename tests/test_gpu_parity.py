@@ -154,11 +154,35 @@ def test_bin_tiny_and_empty():
 # --------------------------------------------------------------------------
 # P2G, grid update, G2P
 
+def expected_path(grid, R):
+    """The share path the bound selects: 0 when wmax*S*R*(1 + 2^-10) <= 2^22 - 4096."""
+    wmax = 0.421875 if grid["dim"] == 3 else 0.5625
+    return 0 if wmax * 2.0 ** grid["scale_log2"] * R * (1 + 2.0 ** -10) <= 4190208.0 else 1
+
+
+def check_bound(sys, cloud, ost, vol=None):
+    """Status of the bound against the oracle's: the flag, and on success R and the path."""
+    st = sys.status()
+    failed = bool(ost & 2)
+    assert bool(st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)) == failed
+    assert st[L.ST_N_OUT_OF_RANGE] == 0
+    if not failed:
+        R, _ = O.scatter_range(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"], vol)
+        assert np.uint32(st[L.ST_RANGE]) == np.array([R], np.float32).view(np.uint32)[0]
+        assert st[L.ST_SHARE_PATH] == expected_path(cloud["grid"], R)
+    return st
+
+
 FIXED_CASES = [
     (2, W.ACC_I32, 20, 64, 6000),
     (2, W.ACC_I64, 20, 48, 3001),
     (3, W.ACC_I64, 19, 32, 6007),
     (3, W.ACC_I32, 19, 24, 2500),
+    # shares past 2^22: the int64 share path
+    (2, W.ACC_I64, 32, 48, 3001),
+    (3, W.ACC_I64, 32, 32, 6007),
+    (3, W.ACC_I64, 40, 24, 2000),
+    (2, W.ACC_I32, 24, 96, 3000),
 ]
 
 
@@ -173,8 +197,8 @@ def test_step_fixed_bit_exact(dim, mode, scale, n, count):
     acc = acc_np(sys)
     oacc, ost, ocounts = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
     assert np.array_equal(acc.astype(np.int64), oacc)
-    st = sys.status()
-    assert st[L.ST_N_OUT_OF_RANGE] == ocounts[1]
+    check_bound(sys, cloud, ost)
+    assert not ost & 2
     sys.grid_update()
     vel = sys.vel.cpu().numpy()
     ovel = O.grid_update_fixed(cloud["grid"], oacc)
@@ -238,7 +262,7 @@ def test_scrambled_input_order_gives_identical_results():
         assert np.array_equal(xb, xa[:, pi]) and np.array_equal(vb, va[:, pi]) and np.array_equal(Cb, Ca[:, pi])
 
 
-def test_dense_single_cell_uses_warp_reduction_and_matches():
+def test_dense_single_cell_matches():
     s = W.Stream(9, 9)
     cnt = 5000
     x = np.full((3, cnt), 0.5 + 0.3 / 16, dtype=np.float64) + 0.2 / 16 * s.uniform24(3 * cnt).reshape(3, cnt)
@@ -269,35 +293,95 @@ def test_full_slice_of_largest_shares():
     assert np.array_equal(acc_np(sys), oacc)
 
 
-def test_out_of_range_particles_are_skipped_and_flagged():
-    cloud = W.small_cloud(3, 3000, 24, seed=401, scale_log2=19)
-    cloud["m"][[5, 77, 2999]] = 1e5
-    cloud["v"][1, 100] = np.nan
+@pytest.mark.parametrize("mode", [W.ACC_I64, W.ACC_I32])
+@pytest.mark.parametrize("bad", ["huge", "nan", "inf"])
+def test_bound_failure_scatters_nothing(mode, bad):
+    """One particle whose range breaks the accumulator bound: nothing at all is
+    scattered (the grid stays zero) and the status reports the bound, as the oracle."""
+    cloud = W.small_cloud(3, 3000, 24, seed=401, scale_log2=19, acc_mode=mode)
+    if bad == "huge":
+        cloud["m"][77] = 1e15
+    elif bad == "nan":
+        cloud["v"][1, 100] = np.nan
+    else:
+        cloud["C"][4, 2999] = np.inf
     sys = make(cloud)
     sys.bin()
     sys.p2g()
     oacc, ost, ocounts = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
-    st = sys.status()
-    assert st[L.ST_N_OUT_OF_RANGE] == 4 == ocounts[1]
-    assert st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
+    assert ost & 2 and ocounts[1] == 3000 and not oacc.any()
+    check_bound(sys, cloud, ost)
+    assert not acc_np(sys).any()
+
+
+def test_one_large_particle_takes_the_wide_path():
+    """At S = 2^19 a particle of mass 10^5 has shares far past 2^22: the bound still
+    holds, the whole launch takes the int64 share path, and the grid is the oracle's."""
+    cloud = W.small_cloud(3, 3000, 24, seed=402, scale_log2=19)
+    cloud["m"][[5, 77, 2999]] = 1e5
+    sys = make(cloud)
+    sys.bin()
+    sys.p2g()
+    oacc, ost, _ = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert ost == 0 and np.abs(oacc).max() > 2 ** 31
+    st = check_bound(sys, cloud, ost)
+    assert st[L.ST_SHARE_PATH] == 1
     assert np.array_equal(acc_np(sys), oacc)
 
 
 def test_int32_accumulator_bound_stops_before_any_scatter():
-    cnt = 600  # 600 stencils over one node > 511
+    """600 stencils over one node: at S = 2^22 the int32 form fails (600 * B > 2^31),
+    at S = 2^10 it holds; both as the oracle decides."""
+    cnt = 600
     s = W.Stream(4, 4)
     x = (0.5 + 0.01 * s.uniform24(2 * cnt)).reshape(2, cnt)
-    cloud = W.small_cloud(2, cnt, 64, seed=1, acc_mode=W.ACC_I32, scale_log2=10)
-    cloud["x"] = x.astype(np.float32)
-    sys = make(cloud)
-    sys.bin()
-    sys.p2g()
-    st = sys.status()
-    assert st[L.ST_MAX_NEIGHBOURS] == cnt
+    for scale, fails in [(22, True), (10, False)]:
+        cloud = W.small_cloud(2, cnt, 64, seed=1, acc_mode=W.ACC_I32, scale_log2=scale)
+        cloud["x"] = x.astype(np.float32)
+        sys = make(cloud)
+        sys.bin()
+        sys.p2g()
+        oacc, ost, _ = O.p2g_fixed(cloud["grid"], cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+        assert bool(ost & 2) == fails
+        st = check_bound(sys, cloud, ost)
+        assert st[L.ST_MAX_NEIGHBOURS] == cnt == O.max_cover(cloud["grid"], cloud["x"])
+        assert np.array_equal(acc_np(sys), oacc)
+
+
+def test_range_records_replace_the_pass():
+    """Steps whose bound takes its range from the previous P2G and G2P (no pass over
+    v, C, m) give the same bits as steps with the pass; breaking the promise (v
+    changed after the G2P) undoes that P2G's scatter and reports the bound."""
+    cloud = W.small_cloud(3, 20000, 32, seed=404, scale_log2=19, lo=0.2, hi=0.8)
+    a = make(cloud)
+    b = make(cloud).use_range_records(False)
+    a.step()
+    b.step()
+    a.use_range_records(True)
+    for _ in range(3):
+        a.bin()
+        a.p2g()
+        b.bin()
+        b.p2g()
+        assert np.array_equal(acc_np(a), acc_np(b))
+        sa, sb = a.status(), b.status()
+        assert sa[L.ST_FLAGS] == sb[L.ST_FLAGS] == 0
+        assert sa[L.ST_RANGE] >= sb[L.ST_RANGE]
+        for s in (a, b):
+            s.grid_update()
+            s.g2p()
+        xa, va, Ca = a.state()
+        xb, vb, Cb = b.state()
+        assert np.array_equal(xa, xb) and np.array_equal(va, vb) and np.array_equal(Ca, Cb)
+    # the promise broken: one particle's velocity raised after the G2P
+    with torch.no_grad():
+        a.v[0, 123] = 1e4
+    a.bin()
+    a.p2g()
+    st = a.status()
     assert st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
-    assert not acc_np(sys).any()
-
-
+    assert st[L.ST_N_OUT_OF_RANGE] == 1
+    assert not acc_np(a).any()
 @pytest.mark.parametrize("name,kw", [
     ("mls2d", {}),
     ("dambreak3d", dict(n_particles=32768)),

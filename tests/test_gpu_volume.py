@@ -65,7 +65,8 @@ def test_volume_step_fixed_bit_exact(dim, mode, scale, n, count, elastic):
         C, _ = O.stress_affine(grid, cloud["material"], cloud["x"], cloud["C"], cloud["F"], cloud["vol"],
                                cloud["m"])
     oacc, _, ocounts = O.p2g_fixed(grid, cloud["x"], cloud["v"], C, cloud["m"], vol=cloud["vol"])
-    assert sys.status()[L.ST_N_OUT_OF_RANGE] == ocounts[1]
+    st = sys.status()
+    assert ocounts[1] == 0 and st[L.ST_N_OUT_OF_RANGE] == 0 and not st[L.ST_FLAGS] & (1 << L.MPM_E_BOUND)
     assert np.array_equal(acc, oacc)
     sys.grid_update()
     vel = sys.vel.cpu().numpy()
