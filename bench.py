@@ -1,11 +1,16 @@
 """Benchmark of the MPM transfer step (bin + P2G + grid update + G2P).
 
 Default workload: 3D quadratic B-spline, 256^3 nodes, 16,777,216 particles in
-64 Gaussian blobs (sigma 0.02), int64 fixed point.  Every step bins the
-particles, scatters, updates the grid and gathers with the sorted G2P, which
-writes the new state in bin order into the second particle buffer (ping-pong),
-so each step starts from the previous step's order (the steady state of a
-simulation that keeps its particles sorted).
+64 Gaussian blobs (sigma 0.02), int64 fixed point.  Every timed step bins the
+particles, checks the accumulator bound (its range taken from the records the
+previous step's P2G and G2P wrote), scatters, updates the grid and gathers;
+seven steps in eight gather in place and every eighth with the sorted G2P,
+which writes the new state in bin order into the second particle buffer
+(ping-pong), so the steps stay in the steady state of a simulation that keeps
+its particles sorted.  The other workloads of the method's configurations (the
+512^3 sphere as a full step, the dam break in int64 and float-atomic modes and
+at S = 2^32, the 2D int32 MLS case, the blobs at S = 2^32) are timed the same
+way as extra rows of the line.
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle on a bounded
 sample of the same workload instead.  Under torchrun (N > 1) every rank runs an
@@ -20,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -31,9 +37,10 @@ METRIC = "P2G+G2P particles/sec (3D 256^3, 16M clustered); % of HBM roofline"
 UNIT = "particles/s"
 WORKLOAD = "blobs3d: 3D quadratic B-spline MPM step, 256^3 nodes, 16,777,216 particles in 64 Gaussian blobs " \
            "(sigma 0.02), int64 fixed point"
-# kernels per step: bin (keys, 3 scans, scatter, 3 in-tile order tiers), P2G, grid update, G2P; the sorted
-# G2P adds the copy of the particles outside the domain
-LAUNCHES_PER_STEP = 11
+# kernels per step: bin (keys, 3 scans, runs, 2 run sorts, emit), the P2G call (the bound, the two share
+# paths of which one returns at once, the undo that returns at once unless a particle broke the recorded
+# range), grid update, G2P; the sorted G2P adds the copy of the particles outside the domain
+LAUNCHES_PER_STEP = 14
 # The timed steps gather in place (mpm_g2p: one warp per work item), and every SORT_PERIOD-th step with
 # mpm_g2p_sorted, which moves the particles into bin order and rewrites the bank-class interleave that the
 # in-place steps keep and wear down; every step bins, scatters, updates and gathers every particle.
@@ -41,10 +48,9 @@ SORT_PERIOD = 8
 
 
 # DRAM traffic per particle (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by the
-# particles it processed) from the ncu captures summarised in profiles/p2g_g2p_full_blobs3d_2M.md (P2G and
-# the in-place G2P of the timed steps) and profiles/stress_volume_full_blobs3d_2M.md (their "_el" stress and
-# "_vc" volume-channel variants), taken on the 2M-particle sample of the workload (same density) and scaled to
-# a full launch by the particle count.  The G2P figures are lower
+# particles it processed) from ncu captures of P2G and the in-place G2P of the timed steps (and of their "_el"
+# stress and "_vc" volume-channel variants), taken on the 2M-particle sample of the workload (same density)
+# and scaled to a full launch by the particle count.  The G2P figures are lower
 # bounds on the write side: the sample's output (60 B per particle, 126 MB) is about the size of L2, and what
 # is still dirty in L2 when the kernel ends is not counted.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
@@ -139,7 +145,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"mpm_bench_clocks_{os.getpid()}_{gpu_index}.csv")
 
     def start(self):
         try:
@@ -174,6 +180,10 @@ class ClockSampler:
             for nm, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
@@ -228,6 +238,8 @@ def run_ours(args, rank, world, local):
             c1.record(stream)
     torch.cuda.synchronize()
     cold_ms = c0.elapsed_time(c1) if args.warmup > 0 else None
+    # from here on the bound takes its range from the records the previous P2G and G2P wrote
+    sys_.use_range_records(True)
     # timed region
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
@@ -260,6 +272,8 @@ def run_ours(args, rank, world, local):
     median_ms = aggregate_max(float(np.median(parts_ms.sum(axis=1))), world, dev)
     st = sys_.status()
     assert st[L.ST_FLAGS] == 0, f"status flags after timing {st[:8]}"
+    share_path = int(st[L.ST_SHARE_PATH])
+    bound_range = float(np.array([st[L.ST_RANGE]], np.uint32).view(np.float32)[0])
     ms_step = aggregate_max(total_ms / args.steps, world, dev)
     value = n * world / (ms_step * 1e-3)
     # the advective step bound of the state the last timed G2P wrote
@@ -321,6 +335,12 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": n * 17 * 4, "d2h_bytes_per_step": n * 17 * 4,
                "ms_per_step": round(e2e_ms, 4)}
 
+    rows = None
+    if args.workload_steps > 0:
+        del sys_
+        torch.cuda.empty_cache()
+        rows = measure_workloads(args, dev, stream, world, peak, rank)
+
     cpu = cpu_omp = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cloud, sample=args.cpu_sample)
@@ -335,6 +355,11 @@ def run_ours(args, rank, world, local):
                    "particle_order": "in place between sorted steps: every 8th step's G2P moves the particles "
                                      "into bin order with the bank-class interleave (ping-pong), the others "
                                      "gather in place",
+                   "bound": {"range_source": "records of the previous step's P2G (max |m|) and G2P "
+                                             "(max(1, |v| + 1.5 dx sum |C|)), verified per particle",
+                             "range": bound_range,
+                             "share_path": "22-bit shares, one fma each" if share_path == 0
+                             else "int64 shares (exact integer product)"},
                    "l2": "inputs larger than L2 (1.07 GB of particle state per step)",
                    "inputs_sha256": inputs_sha,
                    "parallelism": f"replicas x{world}"},
@@ -352,6 +377,7 @@ def run_ours(args, rank, world, local):
         "fused_step": fused,
         "transfer_loop": loop,
         "g2p_schedules": schedules,
+        "workloads": rows,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
@@ -387,6 +413,7 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     del ecloud
     for _ in range(max(3, args.warmup)):
         es.step_sorted(stream)
+    es.use_range_records(True)   # (the elastic state always takes the range pass: its C is stress-folded)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     barrier(world, dev)
@@ -508,6 +535,7 @@ def measure_schedules(args, cloud, dev, stream, world):
         bs = MPMSystem(cloud["grid"], n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted()
         for _ in range(max(3, args.warmup)):
             bs.step_sorted(stream)
+        bs.use_range_records(True)
         torch.cuda.synchronize()
         barrier(world, dev)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
@@ -594,6 +622,141 @@ def measure_loop(args, cloud, dev, stream, world, peak):
     assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
     del ls, acc_b
     torch.cuda.empty_cache()
+    return out
+
+
+def measure_row(args, cloud, dev, stream, world, peak, steps, label):
+    """One workload timed as the main region: three sorted warm-up steps (the first, from the generated
+    order, is the cold step), then `steps` steps binning, checking the bound (range from the records in the
+    fixed-point modes), scattering, updating and gathering, in place with a sorted G2P every SORT_PERIOD-th
+    step.  Per-phase CUDA events; the roofline of the dominant kernel and of the whole step from the
+    algorithmic bytes: bin 24 B (2D 20 B) per particle; P2G 64 B (2D 36 B) per particle plus (dim+1)
+    accumulator words per touched node; grid update (dim+1) words per touched node; G2P 72 B (2D 40 B)."""
+    import torch
+    from material_point_particle_gb300 import _lib as L
+    from material_point_particle_gb300.system import MPMSystem
+
+    grid = cloud["grid"]
+    dim = grid["dim"]
+    n = cloud["x"].shape[1]
+    fixed = grid["acc_mode"] in (L.MPM_ACC_I32, L.MPM_ACC_I64)
+    ws = MPMSystem(grid, n, dev).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"]).enable_sorted()
+    ws.bin(stream)
+    ws.p2g(stream)
+    touched = int((ws.acc[0] != 0).sum().item())
+    ws.grid_update(stream)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in range(max(3, args.warmup)):
+        if k == 0:
+            c0.record(stream)
+        ws.step_sorted(stream)
+        if k == 0:
+            c1.record(stream)
+    torch.cuda.synchronize()
+    cold = c0.elapsed_time(c1)
+    if fixed:
+        ws.use_range_records(True)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        e = ev[k]
+        e[0].record(stream)
+        ws.bin(stream)
+        e[1].record(stream)
+        ws.p2g(stream)
+        e[2].record(stream)
+        ws.grid_update(stream)
+        e[3].record(stream)
+        if (k + 1) % SORT_PERIOD == 0:
+            ws.g2p_sorted(stream)
+        else:
+            ws.g2p(stream)
+        e[4].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    st = ws.status()
+    assert st[L.ST_FLAGS] == 0, f"{label}: status flags {st[:8]}"
+    ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
+    names = ["bin", "p2g", "grid_update", "g2p"]
+    parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev]).mean(axis=0)
+    wacc = 8.0 if grid["acc_mode"] == L.MPM_ACC_I64 else 4.0
+    node = touched * (dim + 1) * wacc
+    alg = {"bin": n * (24.0 if dim == 3 else 20.0), "p2g": n * (64.0 if dim == 3 else 36.0) + node,
+           "grid_update": node, "g2p": n * (72.0 if dim == 3 else 40.0)}
+    dom = names[int(np.argmax(parts))]
+    achieved = alg[dom] / (parts[names.index(dom)] * 1e-3) / 1e9
+    step_bytes = sum(alg.values())
+    out = {"workload": label, "particles": n, "grid": grid["n"][:dim], "touched_nodes": touched,
+           "acc": {L.MPM_ACC_I32: "int32", L.MPM_ACC_I64: "int64", L.MPM_ACC_F32: "fp32 atomics"}[grid["acc_mode"]],
+           "scale_log2": grid["scale_log2"] if fixed else None,
+           "share_path": (("22-bit" if st[L.ST_SHARE_PATH] == 0 else "int64") if fixed else None),
+           "steps": steps, "ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT,
+           "cold_step_ms": round(cold, 4),
+           "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, parts)},
+           "transfer_ms": round(float(parts[1:].sum()), 4),
+           "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4), "traffic": None,
+                        "step_bytes": round(step_bytes), "step_frac": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4)}}
+    del ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def row_cpu_baseline(cloud):
+    """The CPU baseline of one row: the OpenMP build of the oracle's step on all host cores (fixed point),
+    or the oracle itself on one core (float atomics), one step of the whole workload after a warm-up."""
+    from oracle import cpu_omp
+    from oracle import oracle as O
+    grid = cloud["grid"]
+    n = cloud["x"].shape[1]
+    if grid["acc_mode"] != 2 and cpu_omp.available():
+        bufs = cpu_omp.buffers(grid, n)
+        times = []
+        for _ in range(2):
+            t0 = time.perf_counter()
+            cpu_omp.step_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"], out=bufs)
+            times.append(time.perf_counter() - t0)
+        dt = times[-1]
+        return {"value": round(n / dt, 1), "unit": UNIT, "cores": cpu_omp.max_threads(), "kind": "openmp",
+                "sample": f"the whole workload, one step after a warm-up: {dt:.3f} s"}
+    O.build()
+    t0 = time.perf_counter()
+    acc, _, _ = O.p2g_float(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    vel = O.grid_update_float(grid, acc)
+    O.g2p(grid, vel, cloud["x"], cloud["v"], cloud["C"])
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"the whole workload, one oracle step (P2G in fp64 sums, grid update, G2P): {dt:.2f} s"}
+
+
+def measure_workloads(args, dev, stream, world, peak, rank):
+    """The other configurations of the method's workloads, each a row timed like the main region (see
+    measure_row), with its CPU baseline on rank 0: the 512^3 sphere (67,108,864 particles) as a full step
+    with binning; the 128^3 dam break (2,097,152 particles) in int64 (S = 2^21 and S = 2^32, the int64
+    share path) and in float-atomic mode, the comparison the float variant is kept for; the 2D 128^2 MLS
+    case (65,536 particles) with int32 accumulators; the blobs at S = 2^32 (int64 shares)."""
+    from material_point_particle_gb300 import workloads as W
+    steps = args.workload_steps
+    plans = [("sphere3d", lambda: W.sphere3d(), max(10, steps // 2)),
+             ("dambreak3d_int64", lambda: W.dambreak3d(), steps),
+             ("dambreak3d_int64_S2^32", lambda: W.dambreak3d(scale_log2=32), steps),
+             ("dambreak3d_float_atomic", lambda: W.dambreak3d(acc_mode=W.ACC_F32), steps),
+             ("mls2d_int32", lambda: W.mls2d(), steps),
+             ("blobs3d_int64_S2^32", lambda: W.blobs3d(scale_log2=32), steps)]
+    out = {}
+    for label, make, k in plans:
+        cloud = make()
+        row = measure_row(args, cloud, dev, stream, world, peak, k, label)
+        if rank == 0 and not args.no_cpu_baseline and label != "blobs3d_int64_S2^32":
+            row["cpu_baseline"] = row_cpu_baseline(cloud)
+        out[label] = row
+        del cloud
+    sp = out["sphere3d"]
+    sp["note"] = "full step (binning included), the roofline's step bytes 160 B per particle + 64 B per " \
+                 "touched node"
     return out
 
 
@@ -704,6 +867,9 @@ def main():
     ap.add_argument("--variant-steps", type=int, default=50,
                     help="timed steps of the same workload with the Neo-Hookean stress, and with the "
                          "volume channel (0: skip both)")
+    ap.add_argument("--workload-steps", type=int, default=50,
+                    help="timed steps of each other workload row (sphere, dam break, mls2d, blobs at S = 2^32; "
+                         "0: skip them)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -30,6 +30,8 @@ plus the grid parameters.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -73,12 +75,31 @@ class Stream:
 
     CHUNK = 1 << 20
 
+    def _chunks(self, count: int, per: int, fill) -> None:
+        """fill(lo, hi, bits) for each chunk [lo, hi) of `count` outputs, each taking `per` draws per
+        output from its own place in the sequence; chunks run on a thread pool (numpy releases the GIL
+        in these loops), and the counter-based sequence makes the result that of one sequential pass."""
+        base = self.pos
+        spans = [(lo, min(count, lo + self.CHUNK)) for lo in range(0, count, self.CHUNK)]
+
+        def one(span):
+            lo, hi = span
+            fill(lo, hi, splitmix64(self.seed, per * (hi - lo), base + per * lo))
+
+        if len(spans) > 1:
+            with ThreadPoolExecutor(max_workers=min(len(spans), os.cpu_count() or 1)) as ex:
+                list(ex.map(one, spans))
+        elif spans:
+            one(spans[0])
+        self.pos = base + per * count
+
     def _uniform(self, count: int, shift: int, scale: float) -> np.ndarray:
         out = np.empty(count, dtype=np.float64)
-        for lo in range(0, count, self.CHUNK):
-            hi = min(count, lo + self.CHUNK)
-            out[lo:hi] = (self.bits(hi - lo) >> np.uint64(shift)).astype(np.float64)
-        out *= scale
+
+        def fill(lo, hi, b):
+            out[lo:hi] = (b >> np.uint64(shift)).astype(np.float64) * scale
+
+        self._chunks(count, 1, fill)
         return out
 
     def uniform24(self, count: int) -> np.ndarray:
@@ -88,24 +109,24 @@ class Stream:
     def uniform53(self, count: int) -> np.ndarray:
         return self._uniform(count, 11, 2.0 ** -53)
 
-    def normal(self, count: int, sigma: float = 1.0) -> np.ndarray:
+    def normal(self, count: int, sigma: float = 1.0, dtype=np.float64) -> np.ndarray:
         """Box-Muller on consecutive draw pairs (2i, 2i+1): pair i gives r cos(th)
-        at output i and r sin(th) at output half + i."""
+        at output i and r sin(th) at output half + i.  With dtype float32 the fp64
+        values are rounded to fp32 as they are stored."""
         half = (count + 1) // 2
-        z = np.empty(2 * half, dtype=np.float64)
-        for lo in range(0, half, self.CHUNK):
-            hi = min(half, lo + self.CHUNK)
-            k = hi - lo
-            d = (self.bits(2 * k) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        z = np.empty(2 * half, dtype=dtype)
+
+        def fill(lo, hi, b):
+            d = (b >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
             u1 = 1.0 - d[0::2]    # (0, 1]
             u2 = d[1::2]
             r = np.sqrt(-2.0 * np.log(u1))
             th = 2.0 * math.pi * u2
-            z[lo:hi] = r * np.cos(th)
-            z[half + lo:half + hi] = r * np.sin(th)
-        z = z[:count]
-        z *= sigma
-        return z
+            z[lo:hi] = r * np.cos(th) * sigma
+            z[half + lo:half + hi] = r * np.sin(th) * sigma
+
+        self._chunks(half, 2, fill)
+        return z[:count]
 
 
 def scrambled_order(n: int, a: int, b: int) -> np.ndarray:
@@ -156,7 +177,7 @@ def mls2d(n_particles: int = 65536, seed: int = SEED_BASE + 2, n: int = 128):
 
 
 def dambreak3d(n_particles: int = 2097152, seed: int = SEED_BASE + 3, n: int = 128,
-               acc_mode: int = ACC_I64):
+               acc_mode: int = ACC_I64, scale_log2: int = 21):
     """Lattice block: 128^3 particles spaced dx/2 from 0.05 (8 per cell); a
     smaller ``n_particles`` keeps the spacing and takes the leading sub-block."""
     side = max(1, int(round(n_particles ** (1.0 / 3.0))))
@@ -172,7 +193,7 @@ def dambreak3d(n_particles: int = 2097152, seed: int = SEED_BASE + 3, n: int = 1
     m = np.ones(count)
     out = _fp32_particles(x, v, C, m)
     out.update(name="dambreak3d",
-               grid=_grid(3, (n, n, n), 2, acc_mode, 21 if acc_mode != ACC_F32 else 0, 4,
+               grid=_grid(3, (n, n, n), 2, acc_mode, scale_log2 if acc_mode != ACC_F32 else 0, 4,
                           dt=1e-4, g=(0.0, -9.8, 0.0)))
     return out
 
@@ -197,8 +218,8 @@ def blobs3d(n_particles: int = 16777216, seed: int = SEED_BASE + 4, n: int = 256
             bad = np.any((pts < lo) | (pts >= hi), axis=0)
         x[:, pos:pos + cnt] = pts
         pos += cnt
-    v = s.normal(3 * n_particles, 1.0).reshape(3, n_particles)
-    C = s.normal(9 * n_particles, 0.1).reshape(9, n_particles)
+    v = s.normal(3 * n_particles, 1.0, dtype=np.float32).reshape(3, n_particles)
+    C = s.normal(9 * n_particles, 0.1, dtype=np.float32).reshape(9, n_particles)
     m = np.ones(n_particles)
     out = _fp32_particles(x, v, C, m)
     out.update(name="blobs3d", grid=_grid(3, (n, n, n), 2, ACC_I64, scale_log2, 4))
@@ -210,21 +231,45 @@ def sphere3d(n_particles: int = 67108864, seed: int = SEED_BASE + 5, n: int = 51
     """Uniform in a ball (rejection from the cube), rigid rotation about z plus noise."""
     s = Stream(seed, 5)
     c = np.array([0.5, 0.5, 0.5])
-    x = np.empty((3, n_particles))
+    x64 = np.empty((3, n_particles))
+    x = np.empty((3, n_particles), dtype=np.float32)
+    v = np.empty((3, n_particles), dtype=np.float32)
     got = 0
     while got < n_particles:
         want = int((n_particles - got) * 2.0) + 1024
-        p = (s.uniform53(3 * want).reshape(want, 3) * 2.0 - 1.0) * radius
-        keep = p[np.sum(p * p, axis=1) < radius * radius]
-        take = min(len(keep), n_particles - got)
-        x[:, got:got + take] = (keep[:take] + c).T
-        got += take
+        u = s.uniform53(3 * want).reshape(want, 3)
+        # candidates in chunks (threads), the accepted ones kept in candidate order
+        spans = [(lo, min(want, lo + Stream.CHUNK)) for lo in range(0, want, Stream.CHUNK)]
+
+        def accept(span):
+            p = (u[span[0]:span[1]] * 2.0 - 1.0) * radius
+            return p[np.sum(p * p, axis=1) < radius * radius]
+
+        with ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+            keeps = list(ex.map(accept, spans))
+        for keep in keeps:
+            take = min(len(keep), n_particles - got)
+            if take <= 0:
+                break
+            x64[:, got:got + take] = (keep[:take] + c).T
+            got += take
+        del u, keeps
+    noise = s.normal(3 * n_particles, 0.05).reshape(3, n_particles)
     omega = np.array([0.0, 0.0, 2.0])
-    r = x - c[:, None]
-    v = np.cross(omega[None, :], r.T).T + s.normal(3 * n_particles, 0.05).reshape(3, n_particles)
-    C = s.normal(9 * n_particles, 0.1).reshape(9, n_particles)
-    m = np.ones(n_particles)
-    out = _fp32_particles(x, v, C, m)
+    spans = [(lo, min(n_particles, lo + Stream.CHUNK)) for lo in range(0, n_particles, Stream.CHUNK)]
+
+    def rotate(span):
+        lo, hi = span
+        r = x64[:, lo:hi] - c[:, None]
+        v[:, lo:hi] = np.cross(omega[None, :], r.T).T + noise[:, lo:hi]
+        x[:, lo:hi] = x64[:, lo:hi]
+
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        list(ex.map(rotate, spans))
+    del noise, x64
+    C = s.normal(9 * n_particles, 0.1, dtype=np.float32).reshape(9, n_particles)
+    m = np.ones(n_particles, dtype=np.float32)
+    out = dict(x=x, v=v, C=C, m=m)
     out.update(name="sphere3d", grid=_grid(3, (n, n, n), 2, ACC_I64, scale_log2, 4))
     return out
 

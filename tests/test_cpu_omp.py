@@ -48,3 +48,30 @@ def test_omp_step_on_the_blobs_sample():
     for k in ("x", "v", "C"):
         assert np.array_equal(bits(out[k]), bits(ref[k][:, p]))
     assert out["moved"] == cloud["x"].shape[1]
+
+
+def test_omp_step_matches_the_oracle_at_wide_scale():
+    """At S = 2^32 (shares far past 2^22) and S = 2^19 with one heavy particle."""
+    for scale, heavy in [(32, False), (19, True)]:
+        cloud = W.small_cloud(3, 6007, 32, seed=7100 + scale, scale_log2=scale, lo=0.05, hi=0.95,
+                              vsig=1.0, csig=2.0)
+        if heavy:
+            cloud["m"][17] = 1e5
+        grid = cloud["grid"]
+        out = cpu_omp.step_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"], threads=5)
+        ref = O.step_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+        assert np.array_equal(out["acc"], ref["acc"]) and np.abs(ref["acc"]).max() > 2 ** 31
+        assert np.array_equal(bits(out["vel"]), bits(ref["vel"]))
+        p = out["perm"].astype(np.int64)
+        for k in ("x", "v", "C"):
+            assert np.array_equal(bits(out[k]), bits(ref[k][:, p]))
+
+
+def test_omp_step_bound_failure_scatters_nothing():
+    cloud = W.small_cloud(3, 2000, 24, seed=7200, scale_log2=32)
+    cloud["m"][5] = 1e15
+    grid = cloud["grid"]
+    out = cpu_omp.step_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"], threads=4)
+    ref = O.step_fixed(grid, cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    assert not out["acc"].any() and not ref["acc"].any()
+    assert np.array_equal(out["counts"], ref["counts"]) and out["counts"][1] == 2000
