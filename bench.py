@@ -39,8 +39,8 @@ WORKLOAD = "blobs3d: 3D quadratic B-spline MPM step, 256^3 nodes, 16,777,216 par
            "(sigma 0.02), int64 fixed point"
 # kernels per step: bin (keys, 3 scans, runs, 2 run sorts, emit), the P2G call (the bound, the two share
 # paths of which one returns at once, the undo that returns at once unless a particle broke the recorded
-# range), grid update, G2P; the sorted G2P adds the copy of the particles outside the domain
-LAUNCHES_PER_STEP = 14
+# range), G2P with the grid update on load; the sorted G2P adds the copy of the particles outside the domain
+LAUNCHES_PER_STEP = 13
 # The timed steps gather in place (mpm_g2p: one warp per work item), and every SORT_PERIOD-th step with
 # mpm_g2p_sorted, which moves the particles into bin order and rewrites the bank-class interleave that the
 # in-place steps keep and wear down; every step bins, scatters, updates and gathers every particle.
@@ -241,7 +241,7 @@ def run_ours(args, rank, world, local):
     # from here on the bound takes its range from the records the previous P2G and G2P wrote
     sys_.use_range_records(True)
     # timed region
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     barrier(world, dev)
     clocks.start()
@@ -256,19 +256,18 @@ def run_ours(args, rank, world, local):
         e[1].record(stream)
         sys_.p2g(stream)
         e[2].record(stream)
-        sys_.grid_update(stream)
-        e[3].record(stream)
+        # the grid update applied as G2P loads each tile's accumulators (no velocity grid)
         if (k + 1) % SORT_PERIOD == 0:
-            sys_.g2p_sorted(stream)
+            sys_.g2p_sorted_update(stream)
         else:
-            sys_.g2p(stream)
-        e[4].record(stream)
+            sys_.g2p_update(stream)
+        e[3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world, dev)
     total_ms = t_start.elapsed_time(t_end)
-    parts_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev])
+    parts_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev])
     median_ms = aggregate_max(float(np.median(parts_ms.sum(axis=1))), world, dev)
     st = sys_.status()
     assert st[L.ST_FLAGS] == 0, f"status flags after timing {st[:8]}"
@@ -282,12 +281,13 @@ def run_ours(args, rank, world, local):
 
     # roofline of the dominant kernel
     mean_ms = parts_ms.mean(axis=0)
-    names = ["bin", "p2g", "grid_update", "g2p"]
+    names = ["bin", "p2g", "g2p_update"]
     alg_bytes = {
         "bin": n * 24.0,
         "p2g": n * 64.0 + touched * 4 * 8.0,
-        "grid_update": touched * 4 * 8.0,
-        "g2p": n * 72.0,  # read x, write x v C (the m and id copies of the sorted output are extra)
+        # read the accumulators of the touched nodes, read x, write x v C (the clear folded in is not
+        # algorithmic, nor the m and id copies of the sorted output)
+        "g2p_update": n * 72.0 + touched * 4 * 8.0,
     }
     dom = names[int(np.argmax(mean_ms))]
     peak, peak_kind = load_peaks()
@@ -296,7 +296,7 @@ def run_ours(args, rank, world, local):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": measured_traffic(dom, n), "peak_kind": peak_kind,
                 "step_frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4)}
-    # the transfer alone (P2G + grid update + G2P, binning reported apart):
+    # the transfer alone (P2G + the grid update and G2P, binning reported apart):
     # 136 B per particle and 64 B per touched node must move
     tr_ms = aggregate_max(float(mean_ms[1:].sum()), world, dev)
     transfer = {"ms_per_step": round(tr_ms, 4), "value": round(n * world / (tr_ms * 1e-3), 1), "unit": UNIT,
@@ -355,6 +355,9 @@ def run_ours(args, rank, world, local):
                    "particle_order": "in place between sorted steps: every 8th step's G2P moves the particles "
                                      "into bin order with the bank-class interleave (ping-pong), the others "
                                      "gather in place",
+                   "grid_update": "applied as G2P loads each tile's accumulators (mpm_g2p_update, "
+                                  "mpm_g2p_sorted_update); the consumed accumulators cleared as G2P goes; "
+                                  "no velocity grid",
                    "bound": {"range_source": "records of the previous step's P2G (max |m|) and G2P "
                                              "(max(1, |v| + 1.5 dx sum |C|)), verified per particle",
                              "range": bound_range,
@@ -415,7 +418,7 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
         es.step_sorted(stream)
     es.use_range_records(True)   # (the elastic state always takes the range pass: its C is stress-folded)
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     barrier(world, dev)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -427,20 +430,18 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
         e[1].record(stream)
         es.p2g(stream)
         e[2].record(stream)
-        es.grid_update(stream)
-        e[3].record(stream)
         if (k + 1) % SORT_PERIOD == 0:
-            es.g2p_sorted(stream)
+            es.g2p_sorted_update(stream)
         else:
-            es.g2p(stream)
-        e[4].record(stream)
+            es.g2p_update(stream)
+        e[3].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     st = es.status()
     assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
     ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
-    parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev]).mean(axis=0)
-    names = ["bin", "p2g", "grid_update", "g2p"]
+    parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev]).mean(axis=0)
+    names = ["bin", "p2g", "g2p_update"]
     es.bin(stream)
     es.p2g(stream)
     touched = int((es.acc[0] != 0).sum().item())
@@ -450,15 +451,15 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     # 8 B per channel per touched node; G2P reads x (and F) and writes x v C (and F, and phi)
     ch = 4 + (1 if volume else 0)
     alg = {"p2g": n * (64.0 + (36.0 if elastic else 0.0) + 4.0) + touched * 8.0 * ch,
-           "g2p": n * (72.0 + (72.0 if elastic else 0.0) + (4.0 if volume else 0.0))}
-    dom = "p2g" if parts[1] >= parts[3] else "g2p"
+           "g2p_update": n * (72.0 + (72.0 if elastic else 0.0) + (4.0 if volume else 0.0)) + touched * 8.0 * ch}
+    dom = "p2g" if parts[1] >= parts[2] else "g2p_update"
     achieved = alg[dom] / (parts[names.index(dom)] * 1e-3) / 1e9
     out = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
            "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, parts)},
            "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                        "traffic": measured_traffic(f"{dom}_{'el' if elastic else 'vc'}", n)}}
+                        "traffic": None}}
     if elastic:
         out["material"] = {"mu": ELASTIC["mu"], "lambda": ELASTIC["lambda"], "F": "I + N(0, 0.05) per entry",
                            "V0": "dx^3"}
@@ -589,6 +590,7 @@ def measure_loop(args, cloud, dev, stream, world, peak):
     reps = max(1, args.variant_steps // LOOP_ITERATIONS)
 
     def fused():
+        ls.use_range_records(False)
         ls.bin(stream)
         ls.p2g(stream)
         a.record(stream)
@@ -596,8 +598,10 @@ def measure_loop(args, cloud, dev, stream, world, peak):
         b.record(stream)
 
     def separate():
+        ls.use_range_records(False)
         ls.bin(stream)
         ls.p2g(stream)
+        ls.use_range_records(True)   # the later P2G calls take the range from the previous G2P and P2G
         a.record(stream)
         for it in range(LOOP_ITERATIONS):
             ls.grid_update(stream)
@@ -628,8 +632,9 @@ def measure_loop(args, cloud, dev, stream, world, peak):
 def measure_row(args, cloud, dev, stream, world, peak, steps, label):
     """One workload timed as the main region: three sorted warm-up steps (the first, from the generated
     order, is the cold step), then `steps` steps binning, checking the bound (range from the records in the
-    fixed-point modes), scattering, updating and gathering, in place with a sorted G2P every SORT_PERIOD-th
-    step.  Per-phase CUDA events; the roofline of the dominant kernel and of the whole step from the
+    fixed-point modes), scattering, updating and gathering (fixed point: the update applied as G2P loads the
+    accumulators; float atomics: the separate grid update), in place with a sorted G2P every
+    SORT_PERIOD-th step.  Per-phase CUDA events; the roofline of the dominant kernel and of the whole step from the
     algorithmic bytes: bin 24 B (2D 20 B) per particle; P2G 64 B (2D 36 B) per particle plus (dim+1)
     accumulator words per touched node; grid update (dim+1) words per touched node; G2P 72 B (2D 40 B)."""
     import torch
@@ -663,17 +668,19 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
     t0.record(stream)
     for k in range(steps):
         e = ev[k]
+        sort = (k + 1) % SORT_PERIOD == 0
         e[0].record(stream)
         ws.bin(stream)
         e[1].record(stream)
         ws.p2g(stream)
         e[2].record(stream)
-        ws.grid_update(stream)
-        e[3].record(stream)
-        if (k + 1) % SORT_PERIOD == 0:
-            ws.g2p_sorted(stream)
-        else:
-            ws.g2p(stream)
+        if fixed:   # the grid update applied as G2P loads the accumulators
+            e[3].record(stream)
+            ws.g2p_sorted_update(stream) if sort else ws.g2p_update(stream)
+        else:       # float atomics: the separate grid update, then G2P
+            ws.grid_update(stream)
+            e[3].record(stream)
+            ws.g2p_sorted(stream) if sort else ws.g2p(stream)
         e[4].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -684,8 +691,9 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
     parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev]).mean(axis=0)
     wacc = 8.0 if grid["acc_mode"] == L.MPM_ACC_I64 else 4.0
     node = touched * (dim + 1) * wacc
+    # with the update on load the G2P phase also reads the accumulators (and the grid_update phase is empty)
     alg = {"bin": n * (24.0 if dim == 3 else 20.0), "p2g": n * (64.0 if dim == 3 else 36.0) + node,
-           "grid_update": node, "g2p": n * (72.0 if dim == 3 else 40.0)}
+           "grid_update": 0.0 if fixed else node, "g2p": n * (72.0 if dim == 3 else 40.0) + (node if fixed else 0.0)}
     dom = names[int(np.argmax(parts))]
     achieved = alg[dom] / (parts[names.index(dom)] * 1e-3) / 1e9
     step_bytes = sum(alg.values())

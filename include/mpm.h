@@ -337,6 +337,35 @@ mpm_status mpm_g2p_binned(const mpm_grid_desc *desc, const float *grid_vel, cons
                           mpm_particles *out, mpm_bins *bins, float dt, void *stream);
 
 /*
+ * mpm_g2p_update -- mpm_grid_update and mpm_g2p in one pass over the
+ * particles, without a velocity grid (implementation guide, section 2.1, the
+ * worked shape: each tile's nodes are loaded applying the grid update; "the
+ * grid clear can ride along").  `grid_acc` holds mpm_p2g's accumulators at the
+ * positions binned in `bins` (int32 or int64 modes).  Each G2P work item
+ * loads its tile's halo of accumulators and computes every node's velocity as
+ * mpm_grid_update would (v = (float)P / (float)M + dtg, zero where M == 0, the
+ * boundary sign test; the volume fraction with volume_channel), then gathers
+ * exactly as mpm_g2p.  The accumulators are consumed: a node block is read
+ * only by the work items of the 2^dim tiles below it, which count themselves
+ * in a per-block counter of the workspace once their halo is in shared
+ * memory; the one that completes the count clears the block.  So the grid is
+ * zero afterwards, as mpm_grid_update leaves it.  The bits of every particle
+ * are those of mpm_grid_update followed by mpm_g2p.  The status words of
+ * mpm_g2p (MPM_ST_MAX_SPEED, MPM_ST_G2P_RANGE) are written as it writes them.
+ */
+mpm_status mpm_g2p_update(const mpm_grid_desc *desc, void *grid_acc, const float dtg[3], mpm_particles *parts,
+                          mpm_bins *bins, float dt, void *stream);
+
+/*
+ * mpm_g2p_sorted_update -- mpm_grid_update followed by mpm_g2p_sorted, in one
+ * pass as mpm_g2p_update: the new state goes from `in` to `out` in bin order
+ * with the bank-class interleave (see mpm_g2p_sorted), the accumulators are
+ * consumed.  `in` and `out` must not overlap.
+ */
+mpm_status mpm_g2p_sorted_update(const mpm_grid_desc *desc, void *grid_acc, const float dtg[3],
+                                 const mpm_particles *in, mpm_particles *out, mpm_bins *bins, float dt, void *stream);
+
+/*
  * mpm_step -- mpm_bin, mpm_p2g, mpm_grid_update and mpm_g2p in sequence on one
  * stream (device pointers throughout; particles keep their index).
  */

@@ -95,12 +95,16 @@ def library() -> ct.CDLL:
             L.mpm_g2p_binned.argtypes = [P(GridDesc), VP, P(Particles), P(Particles), P(Bins), ct.c_float, VP]
             L.mpm_step_binned.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP, VP, ct.c_float,
                                           P(ct.c_float), VP]
+            L.mpm_g2p_update.argtypes = [P(GridDesc), VP, P(ct.c_float), P(Particles), P(Bins), ct.c_float, VP]
+            L.mpm_g2p_sorted_update.argtypes = [P(GridDesc), VP, P(ct.c_float), P(Particles), P(Particles), P(Bins),
+                                                ct.c_float, VP]
             L.mpm_permute.argtypes = [P(GridDesc), P(Particles), P(Particles), P(Bins), VP]
             L.mpm_read_status.argtypes = [P(Bins), VP, VP]
             L.mpm_bin_static.argtypes = [P(GridDesc), P(Particles), ct.c_int, P(Bins), VP]
             for name in ("mpm_bins_init", "mpm_bin", "mpm_p2g", "mpm_grid_update", "mpm_g2p", "mpm_step",
                          "mpm_g2p_sorted", "mpm_step_sorted", "mpm_step_host", "mpm_permute", "mpm_read_status",
-                         "mpm_bin_static", "mpm_step_fused", "mpm_iterate", "mpm_g2p_binned", "mpm_step_binned"):
+                         "mpm_bin_static", "mpm_step_fused", "mpm_iterate", "mpm_g2p_binned", "mpm_step_binned",
+                         "mpm_g2p_update", "mpm_g2p_sorted_update"):
                 getattr(L, name).restype = ct.c_int
             _L = L
     return _L
@@ -238,6 +242,19 @@ def mpm_g2p_sorted(desc: GridDesc, grid_vel: torch.Tensor, src: Particles, dst: 
                    stream=None):
     _check(library().mpm_g2p_sorted(ct.byref(desc), ct.c_void_p(grid_vel.data_ptr()), ct.byref(src), ct.byref(dst),
                                     ct.byref(bins), ct.c_float(dt), _stream(stream)), "mpm_g2p_sorted")
+
+
+def mpm_g2p_update(desc: GridDesc, grid_acc: torch.Tensor, dtg, parts: Particles, bins: Bins, dt: float,
+                   stream=None):
+    _check(library().mpm_g2p_update(ct.byref(desc), ct.c_void_p(grid_acc.data_ptr()), _f3(dtg), ct.byref(parts),
+                                    ct.byref(bins), ct.c_float(dt), _stream(stream)), "mpm_g2p_update")
+
+
+def mpm_g2p_sorted_update(desc: GridDesc, grid_acc: torch.Tensor, dtg, src: Particles, dst: Particles, bins: Bins,
+                          dt: float, stream=None):
+    _check(library().mpm_g2p_sorted_update(ct.byref(desc), ct.c_void_p(grid_acc.data_ptr()), _f3(dtg),
+                                           ct.byref(src), ct.byref(dst), ct.byref(bins), ct.c_float(dt),
+                                           _stream(stream)), "mpm_g2p_sorted_update")
 
 
 def mpm_step_fused(desc: GridDesc, src: Particles, dst: Particles, bins: Bins, acc_read: torch.Tensor,

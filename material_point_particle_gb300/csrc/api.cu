@@ -79,6 +79,7 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
 
 struct Layout {
     size_t key, perm, heads, tails, count, start, hcnt, tcnt, active, slices, large_list, partial, status, cellcount,
+        readers,
         scratch, total;
     int64_t max_slices;
 };
@@ -113,6 +114,7 @@ Layout layout_of(const GridP &g, int64_t n) {
     L.partial = take(3 * ((nb + 1023) / 1024 + 1) * sizeof(uint32_t));
     L.status = take(MPM_STATUS_WORDS * sizeof(uint32_t));
     L.cellcount = g.acc_mode == MPM_ACC_I32 ? take((size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t)) : 0;
+    L.readers = take((size_t)g.nblocks * sizeof(uint32_t));
     L.scratch = take(2 * sizeof(uint64_t));
     L.total = off;
     return L;
@@ -137,6 +139,7 @@ WsView view_of(const GridP &g, const mpm_bins &b) {
     w.large_list = reinterpret_cast<uint32_t *>(base + L.large_list);
     w.partial = reinterpret_cast<uint32_t *>(base + L.partial);
     w.cellcount = g.acc_mode == MPM_ACC_I32 ? reinterpret_cast<uint32_t *>(base + L.cellcount) : nullptr;
+    w.readers = reinterpret_cast<uint32_t *>(base + L.readers);
     return w;
 }
 
@@ -397,6 +400,36 @@ mpm_status mpm_g2p_binned(const mpm_grid_desc *desc, const float *grid_vel, cons
     DeviceInfo dev;
     MPM_TRY(device_info(dev));
     return launch_g2p_binned(g, grid_vel, pi, po, view_of(g, *bins), dt, dev, static_cast<cudaStream_t>(stream));
+}
+
+mpm_status mpm_g2p_update(const mpm_grid_desc *desc, void *grid_acc, const float dtg[3], mpm_particles *parts,
+                          mpm_bins *bins, float dt, void *stream) {
+    GridP g;
+    MPM_TRY(make_grid(desc, g));
+    if ((g.acc_mode != MPM_ACC_I64 && g.acc_mode != MPM_ACC_I32) || !grid_acc || !dtg) return MPM_E_ARG;
+    PartsF p;
+    MPM_TRY(parts_f(g, parts, true, p));
+    MPM_TRY(check_bins(g, bins, p.n));
+    DeviceInfo dev;
+    MPM_TRY(device_info(dev));
+    return launch_g2p_update(g, grid_acc, dtg, p, p, view_of(g, *bins), dt, false, dev,
+                             static_cast<cudaStream_t>(stream));
+}
+
+mpm_status mpm_g2p_sorted_update(const mpm_grid_desc *desc, void *grid_acc, const float dtg[3],
+                                 const mpm_particles *in, mpm_particles *out, mpm_bins *bins, float dt, void *stream) {
+    GridP g;
+    MPM_TRY(make_grid(desc, g));
+    if ((g.acc_mode != MPM_ACC_I64 && g.acc_mode != MPM_ACC_I32) || !grid_acc || !dtg) return MPM_E_ARG;
+    PartsF pi, po;
+    MPM_TRY(parts_f(g, in, true, pi));
+    MPM_TRY(parts_f(g, out, true, po));
+    if (pi.n != po.n || (!pi.id) != (!po.id) || (!pi.F[0]) != (!po.F[0])) return MPM_E_ARG;
+    MPM_TRY(check_bins(g, bins, pi.n));
+    DeviceInfo dev;
+    MPM_TRY(device_info(dev));
+    return launch_g2p_update(g, grid_acc, dtg, pi, po, view_of(g, *bins), dt, true, dev,
+                             static_cast<cudaStream_t>(stream));
 }
 
 mpm_status mpm_step_binned(const mpm_grid_desc *desc, mpm_particles *in, mpm_particles *out, mpm_bins *bins,

@@ -79,6 +79,17 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+// An accumulator value as fp32, rounded to nearest (the grid update's (float)P, (float)M).
+template <typename AccT>
+__device__ __forceinline__ float acc_to_float(AccT v) {
+    if constexpr (sizeof(AccT) == 8)
+        return __ll2float_rn((long long)v);
+    else if constexpr (std::is_same<AccT, float>::value)
+        return v;
+    else
+        return __int2float_rn((int)v);
+}
+
 // Status word helpers: flags are bit (1 << mpm_status).
 __device__ __forceinline__ void set_flag(uint32_t *status, int code) {
     atomicOr(&status[MPM_ST_FLAGS], 1u << code);

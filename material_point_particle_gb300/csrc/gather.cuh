@@ -229,4 +229,149 @@ __device__ __forceinline__ void class_order(const uint32_t *__restrict__ key, co
     }
 }
 
+// --------------------------------------------------------------------------
+// Where the G2P kernels take node velocities from.  UPD = 0: the velocity
+// grid of mpm_grid_update.  UPD = 1, 2, 3: the accumulators of mpm_p2g
+// (int64, int32, fp32) with the grid update applied to each node as the halo
+// loads (implementation guide, section 2.1, the worked shape: the load is
+// the grid pass), the arithmetic of mpm_grid_update: v = (float)P / (float)M
+// + dt*g (zero where M == 0), then the boundary sign test; with the volume
+// channel phi = (float)V * 2^-scale.
+template <int UPD>
+struct AccOf {
+    using T = float;
+};
+template <>
+struct AccOf<1> {
+    using T = long long;
+};
+template <>
+struct AccOf<2> {
+    using T = int32_t;
+};
+
+// The node values of a tile's halo into shared memory: node h of the compact
+// layout goes to v[c * SIZE + h] for each value c (dim velocities, then phi).
+// Thread `me` of `stride` threads takes nodes me, me + stride, ...; each
+// takes B nodes at a time with every load issued before any value is used,
+// so that the loads of a batch are in flight together.
+template <int DIM, int T, bool VC, int UPD, int B = 4>
+__device__ __forceinline__ void load_halo(const GridP &g, const void *src, const float (&dtg)[3], const int (&o)[3],
+                                          float *v, int me, int stride) {
+    using Hl = HaloU<DIM, T>;
+    constexpr int NV = DIM + (VC ? 1 : 0);
+    constexpr int NL = UPD == 0 ? NV : DIM + 1 + (VC ? 1 : 0);  // values loaded per node
+    using LT = typename AccOf<UPD>::T;
+    const LT *base = static_cast<const LT *>(src);
+    for (int h0 = me; h0 < Hl::NODES; h0 += B * stride) {
+        LT a[B][NL];
+        int gi[B][3];
+        bool in[B];
+#pragma unroll
+        for (int i = 0; i < B; ++i) {
+            const int h = h0 + i * stride;
+            int hx, hy, hz;
+            Hl::node(h < Hl::NODES ? h : 0, hx, hy, hz);
+            gi[i][0] = o[0] + hx;
+            gi[i][1] = o[1] + hy;
+            gi[i][2] = o[2] + hz;
+            in[i] = h < Hl::NODES && gi[i][0] < g.n[0] && gi[i][1] < g.n[1] && (DIM == 2 || gi[i][2] < g.n[2]);
+            const int64_t node = in[i] ? node_index(g, gi[i][0], gi[i][1], DIM == 3 ? gi[i][2] : 0) : 0;
+#pragma unroll
+            for (int c = 0; c < NL; ++c) a[i][c] = in[i] ? base[c * g.nodes + node] : (LT)0;
+        }
+#pragma unroll
+        for (int i = 0; i < B; ++i) {
+            const int h = h0 + i * stride;
+            if (h >= Hl::NODES) break;
+            float out[NV];
+            if constexpr (UPD == 0) {
+#pragma unroll
+                for (int c = 0; c < NV; ++c) out[c] = a[i][c];
+            } else {
+#pragma unroll
+                for (int c = 0; c < NV; ++c) out[c] = 0.f;
+                const float M = acc_to_float(a[i][0]);
+                if (M != 0.f) {
+#pragma unroll
+                    for (int l = 0; l < DIM; ++l) {
+                        float vl = __fadd_rn(__fdiv_rn(acc_to_float(a[i][1 + l]), M), dtg[l]);
+                        if ((gi[i][l] < g.boundary && vl < 0.f) || (gi[i][l] > g.n[l] - 1 - g.boundary && vl > 0.f))
+                            vl = 0.f;
+                        out[l] = vl;
+                    }
+                }
+                if constexpr (VC) out[DIM] = in[i] ? __fmul_rn(acc_to_float(a[i][DIM + 1]), g.inv_S) : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < NV; ++c) v[c * Hl::SIZE + h] = out[c];
+        }
+    }
+}
+
+// The consumed accumulators are cleared as the G2P goes (the guide's "the
+// grid clear can ride along"): node block b (tile^dim nodes) is read only by
+// the work items of the tiles b - delta, delta in {0,1}^dim, each loading its
+// tile's halo once into shared memory.  After it has, a work item of tile t
+// counts itself a reader of each of its blocks t + delta; the reader that
+// completes a block's count (the slices of those tiles, ceil(count / 1024)
+// each) clears the block's accumulators, every channel, and resets the
+// count.  So each touched node is zero after the G2P, as mpm_grid_update
+// leaves it, and no block is cleared before its last reader has loaded it.
+// Called by one whole warp, after the halo loads of its work item are done.
+template <int DIM, int T, typename AccT, int NCH>
+__device__ __forceinline__ void release_blocks(const GridP &g, uint32_t t, uint32_t *readers, const uint32_t *count,
+                                               AccT *acc, uint32_t lane) {
+    constexpr int LOG = T == 4 ? 2 : 3;
+    const int tc[3] = {(int)(t % (uint32_t)g.nt[0]), (int)((t / (uint32_t)g.nt[0]) % (uint32_t)g.nt[1]),
+                       DIM == 3 ? (int)(t / ((uint32_t)g.nt[0] * (uint32_t)g.nt[1])) : 0};
+    int bc[3] = {0, 0, 0};
+    bool done = false;
+    if (lane < (1u << DIM)) {
+        bool valid = true;
+#pragma unroll
+        for (int l = 0; l < DIM; ++l) {
+            bc[l] = tc[l] + (int)((lane >> l) & 1u);
+            valid = valid && bc[l] < g.nb[l];
+        }
+        if (valid) {
+            uint32_t expect = 0;
+#pragma unroll
+            for (int d = 0; d < (1 << DIM); ++d) {
+                int u[3] = {0, 0, 0};
+                bool ok = true;
+#pragma unroll
+                for (int l = 0; l < DIM; ++l) {
+                    u[l] = bc[l] - ((d >> l) & 1);
+                    ok = ok && u[l] >= 0 && u[l] < g.nt[l];
+                }
+                if (ok) {
+                    const uint32_t c = count[((int64_t)u[2] * g.nt[1] + u[1]) * g.nt[0] + u[0]];
+                    expect += (c + kSliceParticles - 1) / kSliceParticles;
+                }
+            }
+            const int64_t blk = ((int64_t)bc[2] * g.nb[1] + bc[1]) * g.nb[0] + bc[0];
+            if (atomicAdd(&readers[blk], 1u) + 1u == expect) {
+                readers[blk] = 0u;
+                done = true;
+            }
+        }
+    }
+    uint32_t todo = __ballot_sync(0xFFFFFFFFu, done);
+    while (todo) {
+        const int j = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const int b0 = __shfl_sync(0xFFFFFFFFu, bc[0], j), b1 = __shfl_sync(0xFFFFFFFFu, bc[1], j);
+        const int b2 = __shfl_sync(0xFFFFFFFFu, bc[2], j);
+        for (int i = (int)lane; i < (DIM == 3 ? T * T * T : T * T); i += 32) {
+            const int x = b0 * T + (i & (T - 1)), y = b1 * T + ((i >> LOG) & (T - 1));
+            const int z = DIM == 3 ? b2 * T + (i >> (2 * LOG)) : 0;
+            if (x >= g.n[0] || y >= g.n[1] || (DIM == 3 && z >= g.n[2])) continue;
+            const int64_t node = node_index(g, x, y, z);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) acc[c * g.nodes + node] = (AccT)0;
+        }
+    }
+}
+
 }  // namespace mpm

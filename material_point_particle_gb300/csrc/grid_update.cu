@@ -12,16 +12,6 @@
 
 namespace mpm {
 
-template <typename AccT>
-__device__ __forceinline__ float acc_to_float(AccT v) {
-    if constexpr (sizeof(AccT) == 8)
-        return __ll2float_rn((long long)v);
-    else if constexpr (std::is_same<AccT, float>::value)
-        return v;
-    else
-        return __int2float_rn((int)v);
-}
-
 // Work item: a brick of 32 nodes in x (one per lane) by one row of node
 // blocks (T rows in y, T planes in z), visited when a tile next to one of its
 // blocks holds particles: each lane reads consecutive nodes of a grid row, so

@@ -29,6 +29,7 @@ struct WsView {
     uint32_t *partial;    // scan block totals, 3 words per 1024 buckets
     uint32_t *status;     // [MPM_STATUS_WORDS]
     uint32_t *cellcount;  // int32 mode only: [ntiles * T^dim], else null
+    uint32_t *readers;    // [nblocks] work items that have read each node block (G2P with the update on load)
 };
 
 struct DeviceInfo {
@@ -56,6 +57,8 @@ mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, con
 void launch_clear_blocks(const GridP &g, long long *acc, const WsView &w, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_iterate(const GridP &g, const PartsF &p, const WsView &w, void *acc_a, void *acc_b,
                           int iterations, const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_g2p_update(const GridP &g, const void *acc, const float dtg[3], const PartsF &in, const PartsF &out,
+                             const WsView &w, float dt, bool sorted, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_g2p_binned(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
                              float dt, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,

@@ -334,12 +334,17 @@ __global__ void __launch_bounds__(256) k_range(GridP g, PartsF p, const uint32_t
     warp_max_to(Rb, &status[MPM_ST_RANGE]);
 }
 
-// One thread: R from the pass above or from the records, then the test the
-// oracle states (fp64, this order): B = S*R*(1 + 2^-10) + 28, count * B within
-// 2^62 (int64) or 2^31 - 1024 (int32, count = most stencils covering a node).
-// Failing, P2G scatters nothing; passing, the share path is chosen.
+// One thread, before the scatter: resets the P2G call's counters, takes R
+// from the pass above or from the records (then clears the records for this
+// call's own), and applies the test the oracle states (fp64, this order):
+// B = S*R*(1 + 2^-10) + 28, count * B within 2^62 (int64) or 2^31 - 1024
+// (int32, count = most stencils covering a node).  Failing, P2G scatters
+// nothing; passing, the share path is chosen.
 __global__ void k_bound(GridP g, uint32_t *__restrict__ status, int from_records) {
     if (threadIdx.x != 0) return;
+    status[MPM_ST_N_DEGENERATE] = 0;
+    status[MPM_ST_WORK_P2G] = 0;
+    status[MPM_ST_N_OUT_OF_RANGE] = 0;
     uint32_t flags = status[MPM_ST_FLAGS] & ~((1u << MPM_E_BOUND) | kFlagNoScatter | kFlagRollback);
     uint32_t Rb;
     if (from_records) {
@@ -352,6 +357,9 @@ __global__ void k_bound(GridP g, uint32_t *__restrict__ status, int from_records
     } else {
         Rb = status[MPM_ST_RANGE];
     }
+    status[MPM_ST_P2G_MASS] = 0;
+    status[MPM_ST_P2G_VOLUME] = 0;
+    status[MPM_ST_SHARE_PATH] = 0;
     const double R = (double)__uint_as_float(Rb);
     const double S = (double)g.S;
     const double B = __dadd_rn(__dmul_rn(__dmul_rn(S, R), 1.0 + 0x1p-10), 28.0);
@@ -380,9 +388,9 @@ void launch_rollback(const GridP &g, void *grid_acc, const uint32_t *status, con
                      cudaStream_t st) {
     const int64_t words = (int64_t)(g.dim + 1 + g.vc) * g.nodes;
     if (g.acc_mode == MPM_ACC_I32)
-        k_rollback<int32_t><<<dev.sms * 4, 256, 0, st>>>((int32_t *)grid_acc, words, status);
+        k_rollback<int32_t><<<dev.sms, 256, 0, st>>>((int32_t *)grid_acc, words, status);
     else
-        k_rollback<long long><<<dev.sms * 4, 256, 0, st>>>((long long *)grid_acc, words, status);
+        k_rollback<long long><<<dev.sms, 256, 0, st>>>((long long *)grid_acc, words, status);
 }
 
 // Float-atomic P2G (comparison variant: fp32 adds, order dependent).
@@ -459,17 +467,15 @@ void launch_p2g_t(const GridP &g, const PartsF &p, const WsView &w, void *grid_a
                                                                          w.status, (float *)grid_acc, sp);
         return;
     }
-    // the bound, before any particle is scattered
-    static_assert(MPM_ST_SHARE_PATH == MPM_ST_RANGE + 1, "adjacent status words");
-    cudaMemsetAsync(&w.status[MPM_ST_RANGE], 0, 2 * sizeof(uint32_t), st);
-    if (!records && p.n > 0) {
-        const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((p.n + 255) / 256, dev.sms * 8));
-        k_range<DIM, EL, VC><<<blocks, 256, 0, st>>>(g, p, w.key, w.status, sp);
+    // the bound, before any particle is scattered: R from a pass over the state, or from the records
+    if (!records) {
+        cudaMemsetAsync(&w.status[MPM_ST_RANGE], 0, sizeof(uint32_t), st);
+        if (p.n > 0) {
+            const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((p.n + 255) / 256, dev.sms * 8));
+            k_range<DIM, EL, VC><<<blocks, 256, 0, st>>>(g, p, w.key, w.status, sp);
+        }
     }
     k_bound<<<1, 32, 0, st>>>(g, w.status, records ? 1 : 0);
-    // this call's records (the previous ones were read by k_bound)
-    static_assert(MPM_ST_P2G_VOLUME == MPM_ST_P2G_MASS + 1, "adjacent status words");
-    cudaMemsetAsync(&w.status[MPM_ST_P2G_MASS], 0, 2 * sizeof(uint32_t), st);
     if (g.acc_mode == MPM_ACC_I64)
         launch_p2g_fixed<DIM, T, long long, EL, VC>(g, p, w, (long long *)grid_acc, sp, records, dev, st);
     else
@@ -494,10 +500,10 @@ void launch_p2g_dt(const GridP &g, const PartsF &p, const WsView &w, void *grid_
 mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt, bool records,
                       const DeviceInfo &dev, cudaStream_t st) {
     const StressP sp{p.mu, p.lam, dt, (4.0f * g.inv_dx) * g.inv_dx};
-    // degenerate-particle count, work counter, particles above the range
-    static_assert(MPM_ST_WORK_P2G == MPM_ST_N_DEGENERATE + 1, "adjacent status words");
-    cudaMemsetAsync(&w.status[MPM_ST_N_DEGENERATE], 0, 2 * sizeof(uint32_t), st);
-    cudaMemsetAsync(&w.status[MPM_ST_N_OUT_OF_RANGE], 0, sizeof(uint32_t), st);
+    if (g.acc_mode == MPM_ACC_F32) {  // the fixed-point modes reset these in k_bound
+        static_assert(MPM_ST_WORK_P2G == MPM_ST_N_DEGENERATE + 1, "adjacent status words");
+        cudaMemsetAsync(&w.status[MPM_ST_N_DEGENERATE], 0, 2 * sizeof(uint32_t), st);
+    }
     if (g.dim == 3 && g.T == 4)
         launch_p2g_dt<3, 4>(g, p, w, grid_acc, sp, records, dev, st);
     else if (g.dim == 2 && g.T == 8)

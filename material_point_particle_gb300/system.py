@@ -122,6 +122,17 @@ class MPMSystem:
         grid = self.acc if self.grid["acc_mode"] == L.MPM_ACC_EXACT_INT else self.vel
         L.mpm_g2p(self.desc, grid, self.parts, self.bins, self.dt, stream)
 
+    def g2p_update(self, stream=None):
+        """The grid update applied as G2P loads each tile's accumulators (mpm_g2p_update): in place, the
+        accumulators consumed, no velocity grid."""
+        L.mpm_g2p_update(self.desc, self.acc, self.dtg, self.parts, self.bins, self.dt, stream)
+
+    def step_update(self, stream=None):
+        """bin, p2g and mpm_g2p_update: a whole step without a velocity grid."""
+        self.bin(stream)
+        self.p2g(stream)
+        self.g2p_update(stream)
+
     def step(self, stream=None):
         L.mpm_step(self.desc, self.parts, self.bins, self.acc, self.vel, self.dt, self.dtg, stream)
 
@@ -159,6 +170,15 @@ class MPMSystem:
     def g2p_sorted(self, stream=None):
         L.mpm_g2p_sorted(self.desc, self.vel, self.parts, self.parts2, self.bins, self.dt, stream)
         self.swap()
+
+    def g2p_sorted_update(self, stream=None):
+        L.mpm_g2p_sorted_update(self.desc, self.acc, self.dtg, self.parts, self.parts2, self.bins, self.dt, stream)
+        self.swap()
+
+    def step_sorted_update(self, stream=None):
+        self.bin(stream)
+        self.p2g(stream)
+        self.g2p_sorted_update(stream)
 
     def g2p_binned(self, stream=None):
         L.mpm_g2p_binned(self.desc, self.vel, self.parts, self.parts2, self.bins, self.dt, stream)
