@@ -412,8 +412,8 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
  * input's, so the bank-class interleave mpm_step_sorted writes carries over
  * (particles drifting between cells wear it down slowly; an occasional
  * sorted step restores it).  It scatters the new state into `acc_write` as
- * mpm_p2g on `out` would (the same integers), and clears `acc_read`; the
- * caller then swaps in/out and the two grids.  One
+ * mpm_p2g on `out` would (the same integers), and clears `acc_read` (a second
+ * kernel, after the reads); the caller then swaps in/out and the two grids.  One
  * warp per work item: a particle's new state is scattered into the warp's
  * tile accumulator while its base cell stays in the tile; a particle whose
  * base cell left the tile is scattered straight into the global grid and

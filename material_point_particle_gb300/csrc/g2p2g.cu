@@ -18,7 +18,10 @@
 // for bit those of mpm_bin + mpm_p2g + mpm_grid_update + mpm_g2p_binned, then
 // mpm_p2g on the new state.  R is only read (several work items read each
 // halo node); a second kernel clears it afterwards, so that it can be the
-// next step's W (the guide's rotation of grid buffers).
+// next step's W (the guide's rotation of grid buffers).  Clearing R inside
+// this kernel by its readers' count, as mpm_g2p_update and the transfer loop
+// do (release_blocks), measured slower here: 1.56 ms per step on the 16.7M
+// blobs against 1.44 ms with the second kernel.
 #include "common.cuh"
 #include "gather.cuh"
 #include "internal.h"
@@ -121,27 +124,7 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
         uint32_t pid_next = lane < cnt ? issue(0, lane) : 0u;
         cp_async_commit();
         // node velocities of the tile's halo, the grid update applied on load
-        for (int h = lane; h < Hl::NODES; h += 32) {
-            int hx, hy, hz;
-            Hl::node(h, hx, hy, hz);
-            const int gi[3] = {o[0] + hx, o[1] + hy, o[2] + hz};
-            float v[3] = {0.f, 0.f, 0.f};
-            if (gi[0] < g.n[0] && gi[1] < g.n[1] && (DIM == 2 || gi[2] < g.n[2])) {
-                const int64_t node = node_index(g, gi[0], gi[1], gi[2]);
-                const float M = __ll2float_rn(accR[node]);
-                if (M != 0.f) {
-#pragma unroll
-                    for (int l = 0; l < DIM; ++l) {
-                        float vl = __fadd_rn(__fdiv_rn(__ll2float_rn(accR[(1 + l) * g.nodes + node]), M), dtg[l]);
-                        if ((gi[l] < g.boundary && vl < 0.f) || (gi[l] > g.n[l] - 1 - g.boundary && vl > 0.f))
-                            vl = 0.f;
-                        v[l] = vl;
-                    }
-                }
-            }
-#pragma unroll
-            for (int l = 0; l < DIM; ++l) vw[l * Hl::SIZE + h] = v[l];
-        }
+        load_halo<DIM, T, false, 1, 2>(g, accR, dtg, o, vw, (int)lane, 32);
         __syncwarp();
         int stage = 0;
         for (uint32_t qr = 0; qr < rounds; ++qr) {
@@ -303,7 +286,6 @@ mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, con
     cudaMemsetAsync(&w.status[MPM_ST_N_OUT_OF_RANGE], 0, sizeof(uint32_t), st);
     const auto *R = static_cast<const long long *>(acc_read);
     auto *Wr = static_cast<long long *>(acc_write);
-    auto *Rc = static_cast<long long *>(acc_read);
     if (g.dim == 3 && g.T == 4) {
         k_g2p2g_w<3, 4><<<blocks, kP2GThreads, 0, st>>>(g, in, out, R, Wr, dtg[0], dtg[1], dtg[2], w.perm,
                                                         w.slices, w.start, w.status, dt, c4);
@@ -314,7 +296,7 @@ mpm_status launch_g2p2g(const GridP &g, const PartsF &in, const PartsF &out, con
         return MPM_E_ARG;
     }
     launch_copy_rest(g, in, out, w, dev, st);
-    launch_clear_blocks(g, Rc, w, dev, st);
+    launch_clear_blocks(g, const_cast<long long *>(R), w, dev, st);
     launch_rollback(g, Wr, w.status, dev, st);
     return cudaGetLastError() == cudaSuccess ? MPM_OK : MPM_E_CUDA;
 }

@@ -19,8 +19,9 @@
 // from its registers at the same position into the warp's own accumulator
 // halo, which the warp adds to
 // the accumulators W after every 512 particles and at the end.  No block
-// barrier couples the warps.  The last iteration only gathers.  After each
-// iteration a second kernel clears R.  The material projections the page
+// barrier couples the warps.  The last iteration only gathers.  R is cleared
+// as the iteration goes by its readers' count (release_blocks: the last work
+// item to load a node block clears it).  The material projections the page
 // runs between the transfers are not part of it.
 #include "common.cuh"
 #include "gather.cuh"
@@ -33,6 +34,7 @@ namespace mpm {
 template <int DIM, int T, bool SCATTER>
 __global__ void __launch_bounds__(kP2GThreads, 3)
     k_iterate_w(GridP g, PartsF p, const long long *__restrict__ accR, long long *__restrict__ accW,
+                uint32_t *__restrict__ readers, const uint32_t *__restrict__ count,
                 const uint32_t *__restrict__ perm, const uint32_t *__restrict__ slices,
                 const uint32_t *__restrict__ start, uint32_t *__restrict__ status, float c4) {
     using Hl = HaloU<DIM, T>;
@@ -50,6 +52,7 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
     const uint32_t nslices = status[MPM_ST_N_SLICES];
     uint32_t *work = &status[MPM_ST_WORK_G2P];
     const StressP sp{0.f, 0.f, 0.f, 0.f};
+    const float kNoGravity[3] = {0.f, 0.f, 0.f};  // the loop adds gravity only at integration
     uint32_t bad = 0, unused = 0;
     if constexpr (SCATTER)
         for (int i = lane; i < AW; i += 32) wh[i] = 0;
@@ -92,28 +95,10 @@ __global__ void __launch_bounds__(kP2GThreads, 3)
         for (int l = 0; l < DIM; ++l) xc[l] = lane < cnt ? p.x[l][pid] : 0.f;
         xc[DIM] = lane < cnt ? p.m[pid] : 0.f;
         // the halo's node values, the grid update (without gravity) applied on load
-        for (int h = lane; h < Hl::NODES; h += 32) {
-            int hx, hy, hz;
-            Hl::node(h, hx, hy, hz);
-            const int gi[3] = {o[0] + hx, o[1] + hy, o[2] + hz};
-            float v[3] = {0.f, 0.f, 0.f};
-            if (gi[0] < g.n[0] && gi[1] < g.n[1] && (DIM == 2 || gi[2] < g.n[2])) {
-                const int64_t node = node_index(g, gi[0], gi[1], gi[2]);
-                const float M = __ll2float_rn(accR[node]);
-                if (M != 0.f) {
-#pragma unroll
-                    for (int l = 0; l < DIM; ++l) {
-                        float vl = __fadd_rn(__fdiv_rn(__ll2float_rn(accR[(1 + l) * g.nodes + node]), M), 0.f);
-                        if ((gi[l] < g.boundary && vl < 0.f) || (gi[l] > g.n[l] - 1 - g.boundary && vl > 0.f))
-                            vl = 0.f;
-                        v[l] = vl;
-                    }
-                }
-            }
-#pragma unroll
-            for (int l = 0; l < DIM; ++l) vw[l * Hl::SIZE + h] = v[l];
-        }
+        load_halo<DIM, T, false, 1, 2>(g, accR, kNoGravity, o, vw, (int)lane, 32);
         __syncwarp();
+        // this work item has read its blocks of R: the last reader of a block clears it
+        release_blocks<DIM, T, long long, DIM + 1>(g, t, readers, count, const_cast<long long *>(accR), lane);
         const uint32_t rounds = (cnt + 31) / 32;
         for (uint32_t q = 0; q < rounds; ++q) {
             const uint32_t r = q * 32 + lane;
@@ -186,15 +171,17 @@ void launch_iterations(const GridP &g, const PartsF &p, const WsView &w, long lo
                        const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;
     const int blocks = dev.sms * 4;
+    // the block reader counts start at zero; each iteration's readers leave them at zero again
+    cudaMemsetAsync(w.readers, 0, (size_t)g.nblocks * sizeof(uint32_t), st);
     for (int it = 0; it < iterations; ++it) {
         cudaMemsetAsync(&w.status[MPM_ST_WORK_G2P], 0, sizeof(uint32_t), st);
+        // R = a is read and cleared as the iteration goes (release_blocks), W = b written
         if (it + 1 < iterations)
-            k_iterate_w<DIM, T, true><<<blocks, kP2GThreads, 0, st>>>(g, p, a, b, w.perm, w.slices, w.start,
-                                                                      w.status, c4);
+            k_iterate_w<DIM, T, true><<<blocks, kP2GThreads, 0, st>>>(g, p, a, b, w.readers, w.count, w.perm,
+                                                                      w.slices, w.start, w.status, c4);
         else
-            k_iterate_w<DIM, T, false><<<blocks, kP2GThreads, 0, st>>>(g, p, a, b, w.perm, w.slices, w.start,
-                                                                       w.status, c4);
-        launch_clear_blocks(g, a, w, dev, st);
+            k_iterate_w<DIM, T, false><<<blocks, kP2GThreads, 0, st>>>(g, p, a, b, w.readers, w.count, w.perm,
+                                                                       w.slices, w.start, w.status, c4);
         std::swap(a, b);
     }
 }
