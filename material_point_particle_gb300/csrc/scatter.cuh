@@ -222,30 +222,33 @@ __device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, co
 // s = hi * 2^22 + lo, lo the sign-extended low 22 bits, each half added to its
 // own int32 plane (lo planes at channel c, hi planes at NCH + c).  Between two
 // flushes at most 512 shares reach one entry, so the lo sums stay below 2^30
-// and the hi sums below 2^31 for shares below 2^43.
+// and the hi sums below 2^31 for shares below 2^43.  The x offset a0 of the
+// stencil node is a run-time value (the wide path keeps its outer loop
+// rolled, see scatter_shares_wide); a1 and a2 are compile-time.
 template <typename Hl, int NCH>
 struct SharedAdd64 {
     uint32_t base;
-    template <int C, int A>
-    __device__ __forceinline__ void add(long long s) const {
+    template <int C, int A12>
+    __device__ __forceinline__ void add(int a0, long long s) const {
         const int32_t lo = ((int32_t)((uint32_t)s << 10)) >> 10;
         const int32_t hi = (int32_t)((s - lo) >> 22);
-        red_shared_add<4 * (Hl::off(A) + C * Hl::SIZE)>(base, lo);
-        red_shared_add<4 * (Hl::off(A) + (NCH + C) * Hl::SIZE)>(base, hi);
+        const uint32_t at = base + 4u * (uint32_t)a0;
+        red_shared_add<4 * (Hl::off(A12) + C * Hl::SIZE)>(at, lo);
+        red_shared_add<4 * (Hl::off(A12) + (NCH + C) * Hl::SIZE)>(at, hi);
     }
 };
 
 // A 64-bit share straight into the global grid (int64, or int32 where the
-// bound keeps every node sum in range); node0 = the stencil's first node.
+// bound keeps every node sum in range); node0 = the stencil's first node,
+// A12 = a1*3 + a2 (3D) or a1 (2D).
 template <int DIM, typename AccT>
 struct GlobalAdd64 {
     AccT *acc;
     int64_t nodes, n0, n01, node0;
-    template <int C, int A>
-    __device__ __forceinline__ void add(long long s) const {
-        constexpr int a0 = DIM == 3 ? A / 9 : A / 3;
-        constexpr int a1 = DIM == 3 ? (A / 3) % 3 : A % 3;
-        constexpr int a2 = DIM == 3 ? A % 3 : 0;
+    template <int C, int A12>
+    __device__ __forceinline__ void add(int a0, long long s) const {
+        constexpr int a1 = DIM == 3 ? A12 / 3 : A12;
+        constexpr int a2 = DIM == 3 ? A12 % 3 : 0;
         AccT *at = acc + C * nodes + node0 + a0 + a1 * n0 + a2 * n01;
         if constexpr (sizeof(AccT) == 8)
             atomicAdd(reinterpret_cast<unsigned long long *>(at), (unsigned long long)s);
@@ -257,7 +260,11 @@ struct GlobalAdd64 {
 // One particle's shares of any size, handed to `ad` as 64-bit integers:
 // s_m(a) = rint(Wt(a)) and s_k(a) = rint(Wt(a) * vel_k(a)) of the exact
 // product, the centre the remainder, in the same order of fp32 operations as
-// scatter_shares, so the values are the same wherever both apply.
+// scatter_shares, so the values are the same wherever both apply.  The loop
+// over a0 stays rolled: fully unrolled, the 27 nodes' integer products made
+// the kernel too large for the instruction cache (its warps stalled mostly
+// waiting for instructions).  Ad::add takes a0 at run time and (a1, a2) as
+// compile-time A12 = a1*3 + a2 (3D) or a1 (2D).
 template <int DIM, bool EL, bool VC, typename Rec, typename Add>
 __device__ __forceinline__ void scatter_shares_wide(const GridP &g, const Rec &rec, const float (&f)[3],
                                                     const Add &ad, const float (&v)[DIM],
@@ -279,14 +286,17 @@ __device__ __forceinline__ void scatter_shares_wide(const GridP &g, const Rec &r
     rest[St::NC] = VC ? __float2ll_rn(Vt) : 0ll;
 #pragma unroll
     for (int k = 0; k < DIM; ++k) rest[1 + k] = __float2ll_rn(__fmul_rn(Mt, v[k]));
-    static_for<3>([&](auto A0) {
-        constexpr int a0 = decltype(A0)::value;
-        const float Wx = __fmul_rn(w[0][a0], Mt);
+    constexpr int A12C = DIM == 3 ? 4 : 1;  // (a1, a2) = (1, 1) (3D) or a1 = 1 (2D): the centre with a0 = 1
+#pragma unroll 1
+    for (int a0 = 0; a0 < 3; ++a0) {
+        const float wx = a0 == 0 ? w[0][0] : (a0 == 1 ? w[0][1] : w[0][2]);
+        const float dx0 = a0 == 0 ? dd[0][0] : (a0 == 1 ? dd[0][1] : dd[0][2]);
+        const float Wx = __fmul_rn(wx, Mt);
         [[maybe_unused]] float Vx = 0.f;
-        if constexpr (VC) Vx = __fmul_rn(w[0][a0], Vt);
+        if constexpr (VC) Vx = __fmul_rn(wx, Vt);
         float h0[DIM];
 #pragma unroll
-        for (int k = 0; k < DIM; ++k) h0[k] = __fmaf_rn(C[k * DIM + 0], dd[0][a0], v[k]);
+        for (int k = 0; k < DIM; ++k) h0[k] = __fmaf_rn(C[k * DIM + 0], dx0, v[k]);
         static_for<3>([&](auto A1) {
             constexpr int a1 = decltype(A1)::value;
             const float Wxy = __fmul_rn(Wx, w[1][a1]);
@@ -297,34 +307,34 @@ __device__ __forceinline__ void scatter_shares_wide(const GridP &g, const Rec &r
             for (int k = 0; k < DIM; ++k) h1[k] = __fmaf_rn(C[k * DIM + 1], dd[1][a1], h0[k]);
             static_for<(DIM == 3 ? 3 : 1)>([&](auto A2) {
                 constexpr int a2 = decltype(A2)::value;
-                constexpr int a = DIM == 3 ? (a0 * 9 + a1 * 3 + a2) : (a0 * 3 + a1);
-                if constexpr (a != St::CENTRE) {
+                constexpr int A12 = DIM == 3 ? a1 * 3 + a2 : a1;
+                if (A12 != A12C || a0 != 1) {
                     const float Wt = DIM == 3 ? __fmul_rn(Wxy, w[2][a2]) : Wxy;
                     const long long sm = __float2ll_rn(Wt);
                     rest[0] -= sm;
-                    ad.template add<0, a>(sm);
+                    ad.template add<0, A12>(a0, sm);
                     if constexpr (VC) {
                         const long long sv = __float2ll_rn(DIM == 3 ? __fmul_rn(Vxy, w[2][a2]) : Vxy);
                         rest[St::NC] -= sv;
-                        ad.template add<DIM + 1, a>(sv);
+                        ad.template add<DIM + 1, A12>(a0, sv);
                     }
                     static_for<DIM>([&](auto K) {
                         constexpr int k = decltype(K)::value;
                         const float vel = DIM == 3 ? __fmaf_rn(C[k * DIM + 2], dd[2][a2], h1[k]) : h1[k];
                         const long long sk = rint_prod64(Wt, vel);
                         rest[1 + k] -= sk;
-                        ad.template add<1 + k, a>(sk);
+                        ad.template add<1 + k, A12>(a0, sk);
                     });
                 }
             });
         });
-    });
-    ad.template add<0, St::CENTRE>(rest[0]);
+    }
+    ad.template add<0, A12C>(1, rest[0]);
     static_for<DIM>([&](auto K) {
         constexpr int k = decltype(K)::value;
-        ad.template add<1 + k, St::CENTRE>(rest[1 + k]);
+        ad.template add<1 + k, A12C>(1, rest[1 + k]);
     });
-    if constexpr (VC) ad.template add<DIM + 1, St::CENTRE>(rest[St::NC]);
+    if constexpr (VC) ad.template add<DIM + 1, A12C>(1, rest[St::NC]);
 }
 
 }  // namespace mpm
