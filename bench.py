@@ -48,43 +48,16 @@ SORT_PERIOD = 8
 
 
 # DRAM traffic per particle (dram__bytes_read.sum + dram__bytes_write.sum of one launch, divided by the
-# particles it processed) from ncu captures of P2G and the in-place G2P of the timed steps (and of their "_el"
-# stress and "_vc" volume-channel variants), taken on the 2M-particle sample of the workload (same density)
-# and scaled to a full launch by the particle count.  The G2P figures are lower
-# bounds on the write side: the sample's output (60 B per particle, 126 MB) is about the size of L2, and what
-# is still dirty in L2 when the kernel ends is not counted.
+# particles it processed) from an ncu capture of the timed steps' P2G (the 22-bit instance), taken on the
+# 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
-    "p2g": {"bytes_per_particle": 82.1, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
-            "sha256": "cefddb79c18767c7898395faef7c8847d4986c85aee4d07baf15bec900c228b5"
-                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
-                      "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
-                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "g2p": {"bytes_per_particle": 55.8, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
-            "sha256": "942a5580779a384d3e09de66522ceeed7c9ed1a0db6a20f7b596e447a3b6fa43"
-                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
-                      "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
-                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "p2g_el": {"bytes_per_particle": 126.0, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
-            "sha256": "cefddb79c18767c7898395faef7c8847d4986c85aee4d07baf15bec900c228b5"
-                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
-                      "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
-                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "g2p_el": {"bytes_per_particle": 132.8, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
-            "sha256": "942a5580779a384d3e09de66522ceeed7c9ed1a0db6a20f7b596e447a3b6fa43"
-                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
-                      "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
-                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "p2g_vc": {"bytes_per_particle": 89.5, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh'),
-            "sha256": "cefddb79c18767c7898395faef7c8847d4986c85aee4d07baf15bec900c228b5"
-                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
-                      "d6fd5d868bb54be501598aec24b839398ff17e807b4b29d955d3a814e2d73c79"
-                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
-    "g2p_vc": {"bytes_per_particle": 62.2, "files": ('grid_g2p.cu', 'common.cuh', 'gather.cuh', 'stress.cuh'),
-            "sha256": "942a5580779a384d3e09de66522ceeed7c9ed1a0db6a20f7b596e447a3b6fa43"
-                      "8e5bd77ad4c3a2f5978e954d672a462b5adbac3ddeaf9c6a32739dd9273f4ca3"
-                      "09d5a0985c85a818aceda2c7de4b991ee091715b3e932b7a743d269c3e4a4105"
-                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"},
+    "p2g": {"bytes_per_particle": 82.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh', 'range.cuh'),
+            "sha256": "dede2e877384adad36c2420bd1dd31b6d3978bb2e627ba5f3cde883e804aed95"
+                      "452a1086524430a56d608e648300eccfc305c13a2339d7898a5718fd941217dc"
+                      "29c6ee5f9c5e38a9e314dd0616fee49a4c72dfd86e3b4f221706ae2ad2345b91"
+                      "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"
+                      "02130a6b5dd5211e01db3ff2aad034b7816abc055a35d45fabd3753f8eeadc19"},
 }
 
 
