@@ -388,12 +388,15 @@ mpm_status mpm_step_binned(const mpm_grid_desc *desc, mpm_particles *in, mpm_par
 
 /*
  * mpm_step_host -- one step from and back to HOST particle arrays: copies the
- * host SoA (`host`: x, v, C, m, and id, F, vol and phi if given; pinned memory
- * gives full copy bandwidth) into the device arrays `dev_in`, runs
- * mpm_step_sorted into `dev_out`, and copies the same arrays of `dev_out`
- * back into `host`, so
- * the host arrays hold the new state in the order mpm_g2p_sorted writes.  Asynchronous on `stream`;
- * the host arrays must stay valid until it completes.
+ * host SoA (`host`: x, v, C, m, and id, F, vol and phi if given) into the
+ * device arrays `dev_in`, runs mpm_step_sorted into `dev_out`, and copies the
+ * same arrays of `dev_out` back into `host`, so the host arrays hold the new
+ * state in the order mpm_g2p_sorted writes.  Asynchronous on `stream`; the
+ * host arrays must stay valid until it completes.  When every host array is
+ * pinned (page-locked, so the device can address it) the copies are made by a
+ * kernel that issues the loads and stores from every SM, which moves data
+ * over the CPU-GPU link faster than the copy engines do; otherwise by one
+ * cudaMemcpyAsync per array.  Either way everything is ordered on `stream`.
  */
 mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_particles *dev_in,
                          mpm_particles *dev_out, mpm_bins *bins, void *grid_acc, float *grid_vel, float dt,
@@ -487,9 +490,10 @@ mpm_status mpm_permute(const mpm_grid_desc *desc, const mpm_particles *in, mpm_p
  *  - Zero state: nothing in the static workspace has to be zero beforehand
  *    (every call clears the counters it uses).  The accumulator grid given to
  *    a later mpm_p2g must still be zero, as always.
- *  - Setup: the first call on each device looks up the array's device
- *    address with that device current (this may load the library's device
- *    code); make that first call before any stream capture begins.
+ *  - Setup: every call looks up the array's device address with the
+ *    current device (so no address outlives a device reset); the first call
+ *    on each device may load the library's device code, so make it before
+ *    any stream capture begins.
  *  - Sharing: there is ONE static workspace per device and process.  A call
  *    overwrites what the previous call left there, so calls (and the P2G,
  *    grid update and G2P calls that read their `out`) must not overlap in

@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmpm_gb300.so")
 SOURCES = ["api.cu", "bin.cu", "p2g.cu", "grid_update.cu", "grid_g2p.cu", "g2p_update.cu", "g2p2g.cu", "iterate.cu",
-           "static_ws.cu"]
+           "static_ws.cu", "host_copy.cu"]
 HEADERS = ["common.cuh", "internal.h", "stress.cuh", "scatter.cuh", "gather.cuh", "range.cuh", "g2p_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2",

@@ -498,35 +498,51 @@ mpm_status mpm_step_host(const mpm_grid_desc *desc, mpm_particles *host, mpm_par
         return MPM_E_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)ph.n * sizeof(float);
-    auto copy = [&](void *dst, const void *src, cudaMemcpyKind kind) {
-        return cudaMemcpyAsync(dst, src, bytes, kind, st) == cudaSuccess;
+    // the (host, device in, device out) arrays of the state, in one list
+    const void *hs[kMaxCopies];
+    void *di[kMaxCopies], *dout[kMaxCopies];
+    int cnt = 0;
+    auto add = [&](const void *h, void *i, void *o) {
+        hs[cnt] = h;
+        di[cnt] = i;
+        dout[cnt] = o;
+        ++cnt;
     };
+    for (int l = 0; l < g.dim; ++l) add(ph.x[l], pa.x[l], pb.x[l]);
+    for (int l = 0; l < g.dim; ++l) add(ph.v[l], pa.v[l], pb.v[l]);
+    for (int j = 0; j < g.dim * g.dim; ++j) add(ph.C[j], pa.C[j], pb.C[j]);
+    add(ph.m, const_cast<float *>(pa.m), const_cast<float *>(pb.m));
+    if (ph.id) add(ph.id, pa.id, pb.id);
+    if (ph.F[0])
+        for (int j = 0; j < g.dim * g.dim; ++j) add(ph.F[j], pa.F[j], pb.F[j]);
+    if (ph.vol) add(ph.vol, pa.vol, pb.vol);
+    if (ph.phi) add(ph.phi, pa.phi, pb.phi);
+    // pinned host arrays are copied by a kernel through their device view; otherwise one copy per array
+    void *hview[kMaxCopies];
+    bool pinned = bytes > 0;
+    for (int a = 0; a < cnt && pinned; ++a) pinned = (hview[a] = device_view_of_host(hs[a])) != nullptr;
+    DeviceInfo dev;
+    MPM_TRY(device_info(dev));
     if (bytes) {
-        bool ok = true;
-        for (int l = 0; l < g.dim; ++l) ok = ok && copy(pa.x[l], ph.x[l], cudaMemcpyHostToDevice);
-        for (int l = 0; l < g.dim; ++l) ok = ok && copy(pa.v[l], ph.v[l], cudaMemcpyHostToDevice);
-        for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(pa.C[j], ph.C[j], cudaMemcpyHostToDevice);
-        ok = ok && copy(const_cast<float *>(pa.m), ph.m, cudaMemcpyHostToDevice);
-        if (ph.id) ok = ok && copy(pa.id, ph.id, cudaMemcpyHostToDevice);
-        if (ph.F[0])
-            for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(pa.F[j], ph.F[j], cudaMemcpyHostToDevice);
-        if (ph.vol) ok = ok && copy(pa.vol, ph.vol, cudaMemcpyHostToDevice);
-        if (ph.phi) ok = ok && copy(pa.phi, ph.phi, cudaMemcpyHostToDevice);
-        if (!ok) return MPM_E_CUDA;
+        if (pinned) {
+            MPM_TRY(launch_copy_table(hview, di, cnt, (int64_t)bytes, dev, st));
+        } else {
+            for (int a = 0; a < cnt; ++a)
+                if (cudaMemcpyAsync(di[a], hs[a], bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return MPM_E_CUDA;
+        }
     }
     MPM_TRY(mpm_step_sorted(desc, dev_in, dev_out, bins, grid_acc, grid_vel, dt, dtg, stream));
     if (bytes) {
-        bool ok = true;
-        for (int l = 0; l < g.dim; ++l) ok = ok && copy(ph.x[l], pb.x[l], cudaMemcpyDeviceToHost);
-        for (int l = 0; l < g.dim; ++l) ok = ok && copy(ph.v[l], pb.v[l], cudaMemcpyDeviceToHost);
-        for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(ph.C[j], pb.C[j], cudaMemcpyDeviceToHost);
-        ok = ok && copy(const_cast<float *>(ph.m), pb.m, cudaMemcpyDeviceToHost);
-        if (ph.id) ok = ok && copy(ph.id, pb.id, cudaMemcpyDeviceToHost);
-        if (ph.F[0])
-            for (int j = 0; j < g.dim * g.dim; ++j) ok = ok && copy(ph.F[j], pb.F[j], cudaMemcpyDeviceToHost);
-        if (ph.vol) ok = ok && copy(ph.vol, pb.vol, cudaMemcpyDeviceToHost);
-        if (ph.phi) ok = ok && copy(ph.phi, pb.phi, cudaMemcpyDeviceToHost);
-        if (!ok) return MPM_E_CUDA;
+        if (pinned) {
+            const void *from[kMaxCopies];
+            for (int a = 0; a < cnt; ++a) from[a] = dout[a];
+            MPM_TRY(launch_copy_table(from, hview, cnt, (int64_t)bytes, dev, st));
+        } else {
+            for (int a = 0; a < cnt; ++a)
+                if (cudaMemcpyAsync(const_cast<void *>(hs[a]), dout[a], bytes, cudaMemcpyDeviceToHost, st) !=
+                    cudaSuccess)
+                    return MPM_E_CUDA;
+        }
     }
     return MPM_OK;
 }

@@ -64,6 +64,14 @@ mpm_status launch_g2p_binned(const GridP &g, const float *vel, const PartsF &in,
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,
                           const DeviceInfo &dev, cudaStream_t st);
 
+// Whole-array copies by a kernel (host_copy.cu): `count` arrays of `bytes`
+// each, src/dst device-addressable (device memory, or pinned host memory
+// through its device view).
+constexpr int kMaxCopies = 32;
+void *device_view_of_host(const void *p);
+mpm_status launch_copy_table(const void *const *src, void *const *dst, int count, int64_t bytes,
+                             const DeviceInfo &dev, cudaStream_t st);
+
 // Integer cloud-in-cell transfer (integer particles, int64 grid).
 struct PartsI {
     const int32_t *X[3];

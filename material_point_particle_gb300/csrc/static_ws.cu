@@ -4,11 +4,12 @@
 //
 // The array is file-scope device memory, created by the CUDA runtime when
 // this file's device code is loaded; the library never calls an allocator
-// for it.  Its device address is looked up once per device, with that device
-// current, and cached.  Everything else is the ordinary mpm_bins_init +
-// mpm_bin on that memory, so the results are the same as mpm_bin's.
+// for it.  Its device address is looked up on every call, with the caller's
+// device current (the lookup is cheap next to the binning), so no address
+// outlives the context it belongs to.  Everything else is the ordinary
+// mpm_bins_init + mpm_bin on that memory, so the results are the same as
+// mpm_bin's.
 #include <cstdint>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -16,36 +17,26 @@
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 // One workspace per device (a __device__ variable has one instance per
 // device context).  Nothing in it must be zero beforehand: mpm_bin clears the
 // counters and status words it uses at the start of every call.
 static __device__ __align__(256) unsigned char g_static_ws[MPM_STATIC_WORKSPACE_BYTES];
 
-std::mutex g_mu;
-void *g_ws_ptr[kMaxDevices] = {};
-
-// Device address of g_static_ws on the current device; the first call per
-// device does the lookup (which may load this file's device code).
+// Device address of g_static_ws on the current device (the first lookup on a
+// device may load this file's device code).
 mpm_status static_ws_ptr(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return MPM_E_NO_DEVICE;
     }
-    if (dev < 0 || dev >= kMaxDevices) return MPM_E_ARG;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_ws_ptr[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
-        if (e != cudaSuccess || !p) {
-            cudaGetLastError();
-            return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? MPM_E_NO_DEVICE : MPM_E_CUDA;
-        }
-        g_ws_ptr[dev] = p;
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? MPM_E_NO_DEVICE : MPM_E_CUDA;
     }
-    *out = g_ws_ptr[dev];
+    *out = p;
     return MPM_OK;
 }
 

@@ -72,6 +72,21 @@ def test_static_bins_equal_workspace_bins_twice():
         _check_one(cloud)
 
 
+def test_static_bins_allocate_no_device_memory():
+    """Repeated calls leave the device's free memory unchanged (measured by the
+    driver, outside any caching allocator): the call uses only the library's
+    file-scope array and the caller's particle arrays."""
+    cloud = W.blobs3d(30000, n=64, n_blobs=4, seed=24)
+    sys = MPMSystem(cloud["grid"], cloud["x"].shape[1]).load(cloud["x"], cloud["v"], cloud["C"], cloud["m"])
+    L.mpm_bin_static(sys.desc, sys.parts, 0)        # the first call may load the library's device code
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        L.mpm_bin_static(sys.desc, sys.parts, 0)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+
+
 def test_static_bins_reject_oversize():
     cloud = W.small_cloud(3, 16, 64, seed=23)
     desc = L.grid_desc(cloud["grid"])
