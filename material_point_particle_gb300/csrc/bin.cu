@@ -60,56 +60,70 @@ __device__ __forceinline__ uint32_t cell_key_t(const GridP &g, const int b[3]) {
     return (tile << (DIM * LOG)) | local;
 }
 
-// Key per particle; tile histogram aggregated over runs of equal buckets
-// among a warp's 32 consecutive particles (one atomic per run: particles
-// kept in bin order come in long runs).
+// Keys of the 32 * kKeysUnroll particles from `base` (FULL: all below n, so
+// no bounds tests); tile histogram aggregated over runs of equal buckets
+// among each 32 consecutive particles (one atomic per run: particles kept in
+// bin order come in long runs).
+template <int DIM, int T, bool FULL>
+__device__ __forceinline__ void keys_span(const GridP &g, const PartsF &p, int64_t n, int64_t base, uint32_t lane,
+                                          uint32_t *__restrict__ key, uint32_t *__restrict__ count,
+                                          uint32_t *__restrict__ cellcount, uint32_t *__restrict__ status) {
+    constexpr int LOG = T == 4 ? 2 : 3;
+    const uint32_t bucket_invalid = (uint32_t)g.ntiles;
+    const float *xs[DIM];
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) xs[l] = p.x[l] + base + lane;
+    uint32_t *ks = key + base + lane;
+    float xv[kKeysUnroll][DIM];
+#pragma unroll
+    for (int u = 0; u < kKeysUnroll; ++u) {
+        const bool in = FULL || base + u * 32 + lane < n;
+#pragma unroll
+        for (int l = 0; l < DIM; ++l) xv[u][l] = in ? xs[l][u * 32] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kKeysUnroll; ++u) {
+        const bool in = FULL || base + u * 32 + lane < n;
+        uint32_t k = kKeyInvalid, bucket = bucket_invalid;
+        if (in) {
+            int b[3] = {0, 0, 0};
+            float f;
+            bool ok = true;
+#pragma unroll
+            for (int l = 0; l < DIM; ++l) ok = base_frac(xv[u][l], g.inv_dx, g.n[l], b[l], f) && ok;
+            if (ok) {
+                k = cell_key_t<DIM, T>(g, b);
+                bucket = k >> (DIM * LOG);
+                if (cellcount) atomicAdd(&cellcount[k], 1u);
+            }
+            ks[u * 32] = k;
+        }
+        // runs of equal buckets: the head lane adds the run's length
+        const uint32_t live = FULL ? 0xFFFFFFFFu : __ballot_sync(0xFFFFFFFFu, in);
+        const uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, bucket, 1);
+        const uint32_t heads = __ballot_sync(0xFFFFFFFFu, in && (lane == 0 || prev != bucket));
+        if ((heads >> lane) & 1u) {
+            const uint32_t later = heads & ~((2u << lane) - 1u);   // heads after this lane (lane 31: none)
+            const uint32_t stop = later ? (uint32_t)(__ffs(later) - 1) : (uint32_t)(32 - __clz(live));
+            atomicAdd(&count[bucket], stop - lane);
+            if (bucket == bucket_invalid) atomicAdd(&status[MPM_ST_N_OUTSIDE], stop - lane);
+        }
+    }
+}
+
+// Key per particle, tile histogram (keys_span), out-of-domain count.
 template <int DIM, int T>
 __global__ void __launch_bounds__(256) k_keys(GridP g, PartsF p, uint32_t *__restrict__ key,
                                               uint32_t *__restrict__ count, uint32_t *__restrict__ cellcount,
                                               uint32_t *__restrict__ status) {
-    constexpr int LOG = T == 4 ? 2 : 3;
     const int64_t n = p.n;
     const uint32_t lane = lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const uint32_t bucket_invalid = (uint32_t)g.ntiles;
     constexpr int64_t kSpan = 32 * kKeysUnroll;
     for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kSpan; base < n;
          base += warps * kSpan) {
-        float xv[kKeysUnroll][DIM];
-#pragma unroll
-        for (int u = 0; u < kKeysUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
-#pragma unroll
-            for (int l = 0; l < DIM; ++l) xv[u][l] = i < n ? p.x[l][i] : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kKeysUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
-            uint32_t k = kKeyInvalid, bucket = bucket_invalid;
-            if (i < n) {
-                int b[3] = {0, 0, 0};
-                float f;
-                bool ok = true;
-#pragma unroll
-                for (int l = 0; l < DIM; ++l) ok = base_frac(xv[u][l], g.inv_dx, g.n[l], b[l], f) && ok;
-                if (ok) {
-                    k = cell_key_t<DIM, T>(g, b);
-                    bucket = k >> (DIM * LOG);
-                    if (cellcount) atomicAdd(&cellcount[k], 1u);
-                }
-                key[i] = k;
-            }
-            // runs of equal buckets: the head lane adds the run's length
-            const uint32_t live = __ballot_sync(0xFFFFFFFFu, i < n);
-            const uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, bucket, 1);
-            const uint32_t heads = __ballot_sync(0xFFFFFFFFu, i < n && (lane == 0 || prev != bucket));
-            if ((heads >> lane) & 1u) {
-                const uint32_t later = heads & ~((2u << lane) - 1u);   // heads after this lane (lane 31: none)
-                const uint32_t stop = later ? (uint32_t)(__ffs(later) - 1) : (uint32_t)(32 - __clz(live));
-                atomicAdd(&count[bucket], stop - lane);
-                if (bucket == bucket_invalid) atomicAdd(&status[MPM_ST_N_OUTSIDE], stop - lane);
-            }
-        }
+        if (base + kSpan <= n) keys_span<DIM, T, true>(g, p, n, base, lane, key, count, cellcount, status);
+        else keys_span<DIM, T, false>(g, p, n, base, lane, key, count, cellcount, status);
     }
 }
 
@@ -233,6 +247,41 @@ __device__ __forceinline__ uint32_t bucket_of(uint32_t k, int cpt_log2, uint32_t
 // Run heads (first index of a run) and tails (last index), each appended to
 // its bucket's range of `heads` / `tails` (a bucket has at most as many runs
 // as particles, so its range [start, start + count) has room).
+template <int DIM, int T, bool FULL>
+__device__ __forceinline__ void runs_span(int64_t n, int64_t base, uint32_t lane, uint32_t binv,
+                                          const uint32_t *__restrict__ key, const uint32_t *__restrict__ start,
+                                          uint32_t *__restrict__ hcnt, uint32_t *__restrict__ tcnt,
+                                          uint32_t *__restrict__ heads, uint32_t *__restrict__ tails) {
+    constexpr int CPT = DIM * (T == 4 ? 2 : 3);
+    constexpr int64_t kSpan = 32 * kKeysUnroll;
+    const uint32_t *ks = key + base + lane;
+    uint32_t bk[kKeysUnroll];
+#pragma unroll
+    for (int u = 0; u < kKeysUnroll; ++u)
+        bk[u] = bucket_of((FULL || base + u * 32 + lane < n) ? ks[u * 32] : kKeyInvalid, CPT, binv);
+    // the buckets just before and just after the span (lane 0 / lane 31 use them)
+    const uint32_t bprev = (lane == 0 && base > 0) ? bucket_of(key[base - 1], CPT, binv) : binv;
+    const uint32_t bnext = (lane == 31 && base + kSpan < n) ? bucket_of(key[base + kSpan], CPT, binv) : binv;
+#pragma unroll
+    for (int u = 0; u < kKeysUnroll; ++u) {
+        const int64_t i = base + u * 32 + lane;
+        const uint32_t up = __shfl_up_sync(0xFFFFFFFFu, bk[u], 1);
+        const uint32_t dn = __shfl_down_sync(0xFFFFFFFFu, bk[u], 1);
+        const uint32_t last_before = u > 0 ? __shfl_sync(0xFFFFFFFFu, bk[u > 0 ? u - 1 : 0], 31) : bprev;
+        const uint32_t first_after =
+            u + 1 < kKeysUnroll ? __shfl_sync(0xFFFFFFFFu, bk[u + 1 < kKeysUnroll ? u + 1 : u], 0) : bnext;
+        const uint32_t bp = lane == 0 ? last_before : up;
+        const uint32_t bn = lane == 31 ? first_after : dn;
+        if (FULL || i < n) {
+            const uint32_t b = bk[u];
+            const bool head = i == 0 || bp != b;
+            const bool tail = i == n - 1 || bn != b;
+            if (head) heads[start[b] + atomicAdd(&hcnt[b], 1u)] = (uint32_t)i;
+            if (tail) tails[start[b] + atomicAdd(&tcnt[b], 1u)] = (uint32_t)i;
+        }
+    }
+}
+
 template <int DIM, int T>
 __global__ void __launch_bounds__(256) k_runs(GridP g, const uint32_t *__restrict__ key, int64_t n,
                                               const uint32_t *__restrict__ start, uint32_t *__restrict__ hcnt,
@@ -244,34 +293,8 @@ __global__ void __launch_bounds__(256) k_runs(GridP g, const uint32_t *__restric
     constexpr int64_t kSpan = 32 * kKeysUnroll;
     for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kSpan; base < n;
          base += warps * kSpan) {
-        uint32_t bk[kKeysUnroll];
-#pragma unroll
-        for (int u = 0; u < kKeysUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
-            bk[u] = bucket_of(i < n ? key[i] : kKeyInvalid, (DIM * (T == 4 ? 2 : 3)), binv);
-        }
-        // the buckets just before and just after the span (lane 0 / lane 31 use them)
-        const uint32_t bprev = (lane == 0 && base > 0) ? bucket_of(key[base - 1], (DIM * (T == 4 ? 2 : 3)), binv) : binv;
-        const uint32_t bnext = (lane == 31 && base + kSpan < n) ? bucket_of(key[base + kSpan], (DIM * (T == 4 ? 2 : 3)), binv)
-                                                                : binv;
-#pragma unroll
-        for (int u = 0; u < kKeysUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
-            const uint32_t up = __shfl_up_sync(0xFFFFFFFFu, bk[u], 1);
-            const uint32_t dn = __shfl_down_sync(0xFFFFFFFFu, bk[u], 1);
-            const uint32_t last_before = u > 0 ? __shfl_sync(0xFFFFFFFFu, bk[u > 0 ? u - 1 : 0], 31) : bprev;
-            const uint32_t first_after =
-                u + 1 < kKeysUnroll ? __shfl_sync(0xFFFFFFFFu, bk[u + 1 < kKeysUnroll ? u + 1 : u], 0) : bnext;
-            const uint32_t bp = lane == 0 ? last_before : up;
-            const uint32_t bn = lane == 31 ? first_after : dn;
-            if (i < n) {
-                const uint32_t b = bk[u];
-                const bool head = i == 0 || bp != b;
-                const bool tail = i == n - 1 || bn != b;
-                if (head) heads[start[b] + atomicAdd(&hcnt[b], 1u)] = (uint32_t)i;
-                if (tail) tails[start[b] + atomicAdd(&tcnt[b], 1u)] = (uint32_t)i;
-            }
-        }
+        if (base + kSpan <= n) runs_span<DIM, T, true>(n, base, lane, binv, key, start, hcnt, tcnt, heads, tails);
+        else runs_span<DIM, T, false>(n, base, lane, binv, key, start, hcnt, tcnt, heads, tails);
     }
 }
 
@@ -517,10 +540,10 @@ __global__ void __launch_bounds__(kLargeThreads) k_sort_runs_large(const uint32_
 // perm, position by position.  Work items: the P2G slices (up to 1024
 // positions of one tile), then the outside bucket in chunks of 1024; one
 // warp per item.  A bucket of at most kEmitRuns runs is sorted here, in
-// registers (lane k holds run k); then for 32 consecutive positions q0 + lane
-// the run is (runs starting before q0) + (run starts in [q0, q]) - 1.  Larger
-// buckets come sorted, with their offsets, and each position binary-searches
-// its run.
+// registers (lane k holds run k), and its runs that meet the item's
+// positions are written one after another, 32 consecutive positions at a
+// time.  Larger buckets come sorted, with their offsets, and each position
+// binary-searches its run.
 __global__ void __launch_bounds__(256) k_emit(GridP g, const uint32_t *__restrict__ start,
                                               const uint32_t *__restrict__ count,
                                               const uint32_t *__restrict__ hcnt,
@@ -533,7 +556,6 @@ __global__ void __launch_bounds__(256) k_emit(GridP g, const uint32_t *__restric
     const uint32_t nout = count[g.ntiles];
     const uint32_t nitems = nslices + (nout + kSliceParticles - 1) / kSliceParticles;
     const uint32_t nw = gridDim.x * (blockDim.x >> 5);
-    const uint32_t le = lane == 31 ? 0xFFFFFFFFu : (2u << lane) - 1u;   // lanes 0..lane
     for (uint32_t it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < nitems; it += nw) {
         uint32_t b, first;
         if (it < nslices) {
@@ -562,16 +584,13 @@ __global__ void __launch_bounds__(256) k_emit(GridP g, const uint32_t *__restric
                 if ((int)lane >= d) inc += x;
             }
             const uint32_t off = inc - len;
-            for (uint32_t q0 = first; q0 < end; q0 += 32) {
-                const bool live = lane < nr;
-                const uint32_t before = __reduce_add_sync(0xFFFFFFFFu, (live && off < q0) ? 1u : 0u);
-                const uint32_t bit = (live && off >= q0 && off - q0 < 32u) ? (1u << (off - q0)) : 0u;
-                const uint32_t starts = __reduce_or_sync(0xFFFFFFFFu, bit);
-                const uint32_t r = before + __popc(starts & le) - 1u;
-                const uint32_t hr = __shfl_sync(0xFFFFFFFFu, h[0], r & 31u);
-                const uint32_t orr = __shfl_sync(0xFFFFFFFFu, off, r & 31u);
-                const uint32_t q = q0 + lane;
-                if (q < end) perm[beg + q] = hr + (q - orr);
+            // run by run: run k fills positions [off_k, off_k + len_k) with h_k, h_k + 1, ...
+            for (uint32_t k = 0; k < nr; ++k) {
+                const uint32_t hk = __shfl_sync(0xFFFFFFFFu, h[0], k);
+                const uint32_t ok = __shfl_sync(0xFFFFFFFFu, off, k);
+                const uint32_t lk = __shfl_sync(0xFFFFFFFFu, len, k);
+                const uint32_t lo = max(ok, first), hi = min(ok + lk, end);
+                for (uint32_t q = lo + lane; q < hi; q += 32) perm[beg + q] = hk + (q - ok);
             }
         } else {
             for (uint32_t q = first + lane; q < end; q += 32) {

@@ -96,12 +96,18 @@ __device__ __forceinline__ void set_flag(uint32_t *status, int code) {
 }
 
 // Stencil base and fraction along one axis; false outside the domain
-// (0.5 <= xi < n - 1.5).  Every operation is one IEEE fp32 rounding.
+// (0.5 <= xi < n - 1.5): b = floor(xi - 0.5), f = xi - b.  Every operation is
+// one IEEE fp32 rounding.  The floor goes through the fp32 adder: for
+// 0 <= y < 2^23 the sum y + 2^23 rounded down is 2^23 + floor(y) exactly, an
+// fp32 number whose bit pattern is that of 2^23 plus floor(y), so b is an
+// integer subtraction and (float)b a subtraction of 2^23 (no conversions;
+// grids have at most 2^20 nodes per axis, so y < 2^23).
 __device__ __forceinline__ bool base_frac(float x, float inv_dx, int n, int &b, float &f) {
-    float xi = __fmul_rn(x, inv_dx);
+    const float xi = __fmul_rn(x, inv_dx);
     if (!(xi >= 0.5f && xi < __fsub_rn((float)n, 1.5f))) return false;
-    b = (int)floorf(__fsub_rn(xi, 0.5f));
-    f = __fsub_rn(xi, (float)b);
+    const float t = __fadd_rd(__fsub_rn(xi, 0.5f), 8388608.0f);
+    b = __float_as_int(t) - 0x4B000000;
+    f = __fsub_rn(xi, __fsub_rn(t, 8388608.0f));
     return true;
 }
 
