@@ -52,9 +52,9 @@ SORT_PERIOD = 8
 # 2M-particle sample of the workload (same density) and scaled to a full launch by the particle count.
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
-    "p2g": {"bytes_per_particle": 82.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh', 'range.cuh'),
+    "p2g": {"bytes_per_particle": 82.1, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh', 'range.cuh'),
             "sha256": "dede2e877384adad36c2420bd1dd31b6d3978bb2e627ba5f3cde883e804aed95"
-                      "452a1086524430a56d608e648300eccfc305c13a2339d7898a5718fd941217dc"
+                      "b6b81e2e49a1ce5cbad7d18fb423b4e41997aa04ffc2225018c8ad8ae8a6a0aa"
                       "29c6ee5f9c5e38a9e314dd0616fee49a4c72dfd86e3b4f221706ae2ad2345b91"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"
                       "02130a6b5dd5211e01db3ff2aad034b7816abc055a35d45fabd3753f8eeadc19"},
@@ -727,6 +727,12 @@ def measure_workloads(args, dev, stream, world, peak, rank):
              ("dambreak3d_float_atomic", lambda: W.dambreak3d(acc_mode=W.ACC_F32), steps),
              ("mls2d_int32", lambda: W.mls2d(), steps),
              ("blobs3d_int64_S2^32", lambda: W.blobs3d(scale_log2=32), steps)]
+    if args.workloads:
+        keep = set(args.workloads.split(","))
+        unknown = keep - {label for label, _, _ in plans}
+        if unknown:
+            raise SystemExit(f"unknown workload rows: {sorted(unknown)}")
+        plans = [pl for pl in plans if pl[0] in keep]
     out = {}
     for label, make, k in plans:
         cloud = make()
@@ -735,9 +741,9 @@ def measure_workloads(args, dev, stream, world, peak, rank):
             row["cpu_baseline"] = row_cpu_baseline(cloud)
         out[label] = row
         del cloud
-    sp = out["sphere3d"]
-    sp["note"] = "full step (binning included), the roofline's step bytes 160 B per particle + 64 B per " \
-                 "touched node"
+    if "sphere3d" in out:
+        out["sphere3d"]["note"] = "full step (binning included), the roofline's step bytes 160 B per particle + " \
+                                  "64 B per touched node"
     return out
 
 
@@ -848,6 +854,8 @@ def main():
     ap.add_argument("--variant-steps", type=int, default=50,
                     help="timed steps of the same workload with the Neo-Hookean stress, and with the "
                          "volume channel (0: skip both)")
+    ap.add_argument("--workloads", default="",
+                    help="comma-separated workload rows to time (default: all of them)")
     ap.add_argument("--workload-steps", type=int, default=50,
                     help="timed steps of each other workload row (sphere, dam break, mls2d, blobs at S = 2^32; "
                          "0: skip them)")
