@@ -17,6 +17,7 @@ constexpr uint32_t kKeyInvalid = 0xFFFFFFFFu;
 // and the threads of the CTAs that process them.
 constexpr int kSliceParticles = 1024;
 constexpr int kP2GThreads = 256;
+constexpr int kG2PThreads = 256;
 // 1.5 * 2^23: adding it to |t| < 2^22 leaves rint(t) in the low mantissa bits.
 constexpr float kMagic = 12582912.0f;
 constexpr int32_t kMagicBits = 0x4B400000;

@@ -1,6 +1,6 @@
-// g2p_kernels.cuh -- the G2P kernel (the gather of one particle, one warp per
-// work item, in place, in bin order or sorted with the bank-class
-// interleave), templated on where the node velocities come from (gather.cuh,
+// g2p_kernels.cuh -- the G2P kernels (the gather of one particle, the sorted
+// kernel with one block per work item, the warp kernel in place or in bin
+// order), templated on where the node velocities come from (gather.cuh,
 // load_halo): the velocity grid, or the accumulators with the grid
 // update applied as the halo loads.  Included by grid_g2p.cu (the velocity
 // grid) and g2p_update.cu (the accumulators), so that the two sets of
@@ -115,101 +115,141 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
 }
 
 
-// Warp-level stable counting sort of a slice of cnt (> 32) binned particles
-// (perm[beg ..]) by the bank class of their base cells: ord[e + e / 32] = the
-// bin-order index of the e-th entry of the class-sorted slice, stable in bin
-// order.  cls: cnt bytes, cbase: 32 words, all the warp's own shared
-// memory.
-template <int DIM, int T>
-__device__ __forceinline__ void warp_class_order(const uint32_t *__restrict__ key, const uint32_t *__restrict__ perm,
-                                                 uint32_t beg, uint32_t cnt, uint8_t *cls, uint32_t *cbase,
-                                                 uint16_t *ord, uint32_t lane) {
-    cbase[lane] = 0;
-    __syncwarp();
-    // classes, and the count of each
-    for (uint32_t r0 = 0; r0 < cnt; r0 += 32) {
-        const uint32_t r = r0 + lane;
-        const bool live = r < cnt;
-        const uint32_t c = live ? cell_class<DIM, T>(key[perm[beg + r]]) : 32u + lane;  // dead lanes: alone
-        if (live) cls[r] = (uint8_t)c;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
-        if (live && (peers & lanemask_lt()) == 0) cbase[c] += (uint32_t)__popc(peers);
-        __syncwarp();
-    }
-    // each class's first place: exclusive scan over the 32 classes
-    const uint32_t v = cbase[lane];
-    uint32_t inc = v;
+// The sorted G2P.  Work item as in P2G: one slice of a tile.  The CTA stages
+// the tile's halo of node velocities in shared memory, the slice's x, m and
+// id in bin order, and counting-sorts the slice by bank class; thread t then
+// computes the particles that go to places t, t + 256, ... of the interleaved
+// slice, so that its writes are coalesced and its reads of the velocity halo
+// meet few bank conflicts.  A slice of at most 32 particles is one round and
+// keeps bin order.
+// UPD (load_halo): node velocities from the velocity grid (0) or from
+// the accumulators with the grid update applied on load (1: int64, 2: int32),
+// the accumulators then cleared as the G2P goes (release_blocks).
+template <int DIM, int T, bool EL, bool VC, int UPD>
+__global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q, const void *__restrict__ src,
+                                                     float dtg0, float dtg1, float dtg2,
+                                                     uint32_t *__restrict__ readers,
+                                                     const uint32_t *__restrict__ count,
+                                                     const uint32_t *__restrict__ perm,
+                                                     const uint32_t *__restrict__ key,
+                                                     const uint32_t *__restrict__ slices,
+                                                     const uint32_t *__restrict__ start,
+                                                     uint32_t *__restrict__ status, float dt, float c4) {
+    using Hl = HaloU<DIM, T>;
+    constexpr int NQ = kSliceParticles / kG2PThreads;
+    constexpr int NWARP = kG2PThreads / 32;
+    static_assert(NQ * NWARP == 32, "one warp-scan lane per (round, warp)");
+    constexpr int NF = DIM + 2;  // x, m, id of the whole slice
+    constexpr int BUF = NF * kSliceParticles;
+    // node velocities (and volume fractions), one plane per value
+    __shared__ float sv_all[(DIM + (VC ? 1 : 0)) * Hl::SIZE];
+    const VelHalo<DIM, T> sv{sv_all, sv_all + Hl::SIZE, DIM == 3 ? sv_all + 2 * Hl::SIZE : sv_all,
+                             VC ? sv_all + DIM * Hl::SIZE : sv_all};
+    __shared__ float sbuf[BUF];
+    // [(qi, warp)][class], rows padded to 33 words: the scan reads a column
+    __shared__ uint32_t hist[NQ * NWARP * 33];
+    __shared__ uint32_t cstart[32];
+    // sorted entry e -> bin-order entry, at e + e / 32: the interleaved reads
+    // take entries R apart
+    __shared__ uint32_t order[kSliceParticles + kSliceParticles / 32];
+    const uint32_t lane = lane_id();
+    const uint32_t nslices = status[MPM_ST_N_SLICES];
+    [[maybe_unused]] const float dtg[3] = {dtg0, dtg1, dtg2};
+    __shared__ uint32_t item_sh;
+    float smax = 0.f;  // the advective bound's largest term among this thread's particles
+    uint32_t rmax = 0;  // the range record's largest term
+    uint32_t next = 0;
+    for (uint32_t s = grab_item(&status[MPM_ST_WORK_G2P], &item_sh); s < nslices; s = publish_item(next, &item_sh)) {
+        next = ask_item(&status[MPM_ST_WORK_G2P]);
+        const uint32_t t = slices[2 * (size_t)s], first = slices[2 * (size_t)s + 1];
+        const uint32_t beg = start[t] + first;
+        const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
+        int o[3];
+        tile_origin(g, t, o);
+        uint32_t pids[NQ];
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-        if ((int)lane >= d) inc += t2;
-    }
-    __syncwarp();
-    cbase[lane] = inc - v;
-    __syncwarp();
-    // places, in bin order within each class
-    for (uint32_t r0 = 0; r0 < cnt; r0 += 32) {
-        const uint32_t r = r0 + lane;
-        const bool live = r < cnt;
-        const uint32_t c = live ? (uint32_t)cls[r] : 32u + lane;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, c);
-        const uint32_t below = (uint32_t)__popc(peers & lanemask_lt());
-        if (live) {
-            const uint32_t e = cbase[c] + below;
-            ord[e + (e >> 5)] = (uint16_t)r;
+        for (int qi = 0; qi < NQ; ++qi) {
+            const uint32_t r = threadIdx.x + qi * kG2PThreads;
+            pids[qi] = r < cnt ? perm[beg + r] : 0u;
         }
-        __syncwarp();
-        if (live && below == 0) cbase[c] += (uint32_t)__popc(peers);
-        __syncwarp();
+        // the slice's x, m, id in bin order
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+            const uint32_t r = threadIdx.x + qi * kG2PThreads;
+            if (r < cnt) {
+#pragma unroll
+                for (int f = 0; f < DIM; ++f) cp_async4(&sbuf[f * kSliceParticles + r], p.x[f] + pids[qi]);
+                cp_async4(&sbuf[DIM * kSliceParticles + r], p.m + pids[qi]);
+                if (p.id) cp_async4(&sbuf[(DIM + 1) * kSliceParticles + r], p.id + pids[qi]);
+            }
+        }
+        cp_async_commit();
+        load_halo<DIM, T, VC, UPD, 1>(g, src, dtg, o, sv_all, (int)threadIdx.x, (int)blockDim.x);
+        if constexpr (UPD != 0) {
+            using AccT = typename AccOf<UPD>::T;
+            __syncthreads();  // every thread's halo loads are done
+            if (threadIdx.x < 32)
+                release_blocks<DIM, T, AccT, DIM + 1 + (VC ? 1 : 0)>(g, t, readers, count,
+                                                                     const_cast<AccT *>(static_cast<const AccT *>(src)),
+                                                                     lane);
+        }
+        if (cnt <= 32u) {
+            // one round: the order inside it does not matter, bin order is kept
+            cp_async_wait<0>();
+            __syncthreads();
+            if (threadIdx.x < cnt) {
+                const uint32_t r = threadIdx.x;
+                auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
+                gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax, rmax);
+            }
+        } else {
+            class_order<DIM, T, kG2PThreads>(key, pids, cnt, hist, cstart, order);
+            cp_async_wait<0>();
+            __syncthreads();
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                const uint32_t pos = threadIdx.x + qi * kG2PThreads;
+                if (pos < cnt) {
+                    const uint32_t e = interleave_entry(pos, cnt);
+                    const uint32_t r = order[e + (e >> 5)];
+                    auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
+                    gather_one<DIM, T, true, EL, VC>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax,
+                                                     rmax);
+                }
+            }
+        }
     }
+    // non-negative fp32 values order as their bit patterns
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(smax));
+    if (lane == 0 && wmax) atomicMax(&status[MPM_ST_MAX_SPEED], wmax);
+    warp_max_to(rmax, &status[MPM_ST_G2P_RANGE]);
 }
 
-// Where the warp G2P writes the new state: in place, in bin order
-// (out[j] = new state of in[perm[j]]), or sorted (bin order with the
-// bank-class interleave inside each slice).
-enum WarpOrder { kWarpInPlace = 0, kWarpBinOrder = 1, kWarpSorted = 2 };
-
-// G2P with one warp per work item (the P2G kernel's shape), in place, in
-// bin order or sorted.  Each warp stages its tile's velocity halo in shared
-// memory and takes 32 particles a round; each lane gathers its particle
-// (gather_one, the same arithmetic).  In place, the new state overwrites the
-// particle's own entry (the mpm_g2p contract), and each lane loads its next
-// particle's position into registers while the current one gathers.  In bin
-// order, place j of the slice takes the particle of bin-order index j; sorted,
-// place j takes the one the interleave puts there (warp_class_order, then
-// interleave_entry; a slice of at most 32 keeps bin order).  Either way x, m
-// and id are copied into a per-warp double buffer in shared memory a round
-// ahead, and consecutive lanes write consecutive places.  No block barrier
-// couples the warps.
-// Threads per block of k_g2p_w: sorted, four warps (each warp's shared
-// memory holds the interleave's order too).
-template <int ORDER>
-__host__ __device__ constexpr int g2p_w_threads() {
-    return ORDER == 2 ? 128 : kP2GThreads;
-}
-
-template <int DIM, int T, int ORDER, bool EL, bool VC, int UPD>
-__global__ void __launch_bounds__(g2p_w_threads<ORDER>()) k_g2p_w(GridP g, PartsF p, PartsF q, const void *__restrict__ src,
+// G2P with one warp per work item (the P2G kernel's shape), in place or in
+// bin order.  Each warp stages its tile's velocity halo in shared memory and
+// takes 32 particles a round; each lane gathers its particle (gather_one, the
+// same arithmetic).  In place, the new state overwrites the particle's own
+// entry (the mpm_g2p contract), and each lane loads its next particle's
+// position into registers while the current one gathers.  In bin order
+// (BINORDER), out[j] = the new state of in[perm[j]]: x, m and id are copied
+// into a per-warp double buffer in shared memory a round ahead, and
+// consecutive lanes write consecutive places.  No block barrier couples the
+// warps.
+template <int DIM, int T, bool BINORDER, bool EL, bool VC, int UPD>
+__global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF q, const void *__restrict__ src,
                                                        float dtg0, float dtg1, float dtg2,
                                                        uint32_t *__restrict__ readers,
                                                        const uint32_t *__restrict__ count,
                                                        const uint32_t *__restrict__ perm,
-                                                       const uint32_t *__restrict__ key,
                                                        const uint32_t *__restrict__ slices,
                                                        const uint32_t *__restrict__ start,
                                                        uint32_t *__restrict__ status, float dt, float c4) {
     using Hl = HaloU<DIM, T>;
-    constexpr bool MOVED = ORDER != kWarpInPlace;
-    constexpr bool SORTED = ORDER == kWarpSorted;
-    constexpr int NW = g2p_w_threads<ORDER>() / 32;
+    constexpr int NW = kP2GThreads / 32;
     constexpr int NCH = DIM + (VC ? 1 : 0);
-    constexpr int NF = MOVED ? DIM + 2 : DIM;  // staged: x (and m, id)
+    constexpr int NF = BINORDER ? DIM + 2 : DIM;  // staged: x (and m, id)
     __shared__ float svel[NW][NCH * Hl::SIZE];
-    __shared__ float sbuf[NW][MOVED ? 2 * NF * 32 : 1];
-    // sorted: the interleave's order, the classes, the class counters
-    __shared__ uint16_t sord[SORTED ? NW : 1][SORTED ? kSliceParticles + kSliceParticles / 32 : 1];
-    __shared__ uint8_t scls[SORTED ? NW : 1][SORTED ? kSliceParticles : 1];
-    __shared__ uint32_t scb[SORTED ? NW : 1][32];
+    __shared__ float sbuf[NW][BINORDER ? 2 * NF * 32 : 1];
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     float *vw = svel[warp];
     const VelHalo<DIM, T> sv{vw, vw + Hl::SIZE, DIM == 3 ? vw + 2 * Hl::SIZE : vw, VC ? vw + DIM * Hl::SIZE : vw};
@@ -230,31 +270,18 @@ __global__ void __launch_bounds__(g2p_w_threads<ORDER>()) k_g2p_w(GridP g, Parts
         const uint32_t cnt = min((uint32_t)kSliceParticles, start[t + 1] - beg);
         int o[3];
         tile_origin(g, t, o);
-        // bin-order index of the particle that goes to place pos of the slice
-        [[maybe_unused]] const bool interleaved = SORTED && cnt > 32u;
-        auto source = [&](uint32_t pos) -> uint32_t {
-            if constexpr (SORTED) {
-                if (interleaved) {
-                    const uint32_t e = interleave_entry(pos, cnt);
-                    return sord[warp][e + (e >> 5)];
-                }
-            }
-            return pos;
-        };
-        auto issue = [&](int stage, uint32_t pos) {
-            const uint32_t pid = perm[beg + source(pos)];
+        auto issue = [&](int stage, uint32_t r) {
+            const uint32_t pid = perm[beg + r];
 #pragma unroll
             for (int f = 0; f < DIM; ++f) cp_async4(at(stage, f), p.x[f] + pid);
-            if constexpr (MOVED) {
+            if constexpr (BINORDER) {
                 cp_async4(at(stage, DIM), p.m + pid);
                 if (p.id) cp_async4(at(stage, DIM + 1), p.id + pid);
             }
             return pid;
         };
-        if constexpr (SORTED)
-            if (interleaved) warp_class_order<DIM, T>(key, perm, beg, cnt, scls[warp], scb[warp], sord[warp], lane);
         uint32_t pid_next = 0u;
-        if constexpr (MOVED) {
+        if constexpr (BINORDER) {
             pid_next = lane < cnt ? issue(0, lane) : 0u;
             cp_async_commit();
         }
@@ -267,7 +294,7 @@ __global__ void __launch_bounds__(g2p_w_threads<ORDER>()) k_g2p_w(GridP g, Parts
                                                                  lane);
         }
         const uint32_t rounds = (cnt + 31) / 32;
-        if constexpr (!MOVED) {
+        if constexpr (!BINORDER) {
             // in place: positions in registers a round ahead, perm two rounds ahead
             uint32_t pid = lane < cnt ? perm[beg + lane] : 0u;
             pid_next = lane + 32 < cnt ? perm[beg + lane + 32] : 0u;
@@ -289,7 +316,7 @@ __global__ void __launch_bounds__(g2p_w_threads<ORDER>()) k_g2p_w(GridP g, Parts
                 pid_next = pid_after;
             }
         } else {
-            // x, m and id copied into shared memory (cp.async) a round ahead
+            // bin order: x, m and id copied into shared memory (cp.async) a round ahead
             int stage = 0;
             for (uint32_t qr = 0; qr < rounds; ++qr) {
                 const uint32_t r = qr * 32 + lane;
@@ -300,7 +327,8 @@ __global__ void __launch_bounds__(g2p_w_threads<ORDER>()) k_g2p_w(GridP g, Parts
                 if (r < cnt) {
                     const int st = stage;
                     auto rec = [&](int f) { return *at(st, f); };
-                    gather_one<DIM, T, true, EL, VC>(g, p, q, pid, beg + r, rec, o, sv, dt, c4, smax, rmax);
+                    gather_one<DIM, T, BINORDER, EL, VC>(g, p, q, pid, BINORDER ? beg + r : pid, rec, o, sv, dt, c4,
+                                                         smax, rmax);
                 }
                 stage ^= 1;
             }

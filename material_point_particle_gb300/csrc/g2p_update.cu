@@ -13,12 +13,15 @@ template <int DIM, int T, bool SORTED, bool EL, bool VC, int UPD>
 void launch_g2p_update_t(const GridP &g, const void *acc, const float dtg[3], const PartsF &in, const PartsF &out,
                          const WsView &w, float dt, const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
-    constexpr int ORDER = SORTED ? kWarpSorted : kWarpInPlace;
-    constexpr int NT = g2p_w_threads<ORDER>();
-    k_g2p_w<DIM, T, ORDER, EL, VC, UPD><<<dev.sms * (1024 / NT), NT, 0, st>>>(
-        g, in, out, acc, dtg[0], dtg[1], dtg[2], w.readers, w.count, w.perm, w.key, w.slices, w.start, w.status, dt,
-        c4);
-    if constexpr (SORTED) launch_copy_rest(g, in, out, w, dev, st);
+    if constexpr (SORTED) {
+        k_g2p<DIM, T, EL, VC, UPD><<<dev.sms * (1024 / kG2PThreads), kG2PThreads, 0, st>>>(
+            g, in, out, acc, dtg[0], dtg[1], dtg[2], w.readers, w.count, w.perm, w.key, w.slices, w.start, w.status,
+            dt, c4);
+        launch_copy_rest(g, in, out, w, dev, st);
+    } else {
+        k_g2p_w<DIM, T, false, EL, VC, UPD><<<dev.sms * 4, kP2GThreads, 0, st>>>(
+            g, in, out, acc, dtg[0], dtg[1], dtg[2], w.readers, w.count, w.perm, w.slices, w.start, w.status, dt, c4);
+    }
 }
 
 template <int DIM, int T, bool SORTED, int UPD>

@@ -167,6 +167,68 @@ __device__ __forceinline__ uint32_t interleave_entry(uint32_t pos, uint32_t cnt)
     return l * R - (l > L ? l - L : 0u) + rho;
 }
 
+// Stable counting sort of a slice of cnt binned particles by bank class
+// (cell_class of each particle's key): order[e + e / 32] = the bin-order
+// index of the e-th entry of the class-sorted slice.  Counts per (round,
+// warp, class), scanned class-major.  pids[qi] = perm entry of bin-order
+// index threadIdx.x + qi * NT.  All NT threads of the block call it; it
+// synchronises the block.  hist: NQ * NWARP * 33 words (rows padded to 33:
+// the scan reads a column); cstart: 32 words.
+template <int DIM, int T, int NT>
+__device__ __forceinline__ void class_order(const uint32_t *__restrict__ key, const uint32_t (&pids)[kSliceParticles / NT],
+                                            uint32_t cnt, uint32_t *hist, uint32_t *cstart, uint32_t *order) {
+    constexpr int NQ = kSliceParticles / NT;
+    constexpr int NWARP = NT / 32;
+    static_assert(NQ * NWARP == 32, "one warp-scan lane per (round, warp)");
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    uint32_t cls[NQ], below[NQ];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+        const uint32_t r = threadIdx.x + qi * NT;
+        cls[qi] = r < cnt ? cell_class<DIM, T>(key[pids[qi]]) : 32u;
+    }
+    for (int i = threadIdx.x; i < NQ * NWARP * 33; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, cls[qi]);
+        below[qi] = (uint32_t)__popc(peers & lanemask_lt());
+        if (cls[qi] < 32u && below[qi] == 0) hist[(qi * NWARP + warp) * 33 + cls[qi]] = (uint32_t)__popc(peers);
+    }
+    __syncthreads();
+    for (uint32_t c = warp; c < 32; c += NWARP) {
+        const uint32_t v = hist[lane * 33 + c];
+        uint32_t inc = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if ((int)lane >= d) inc += t2;
+        }
+        hist[lane * 33 + c] = inc - v;
+        if (lane == 31) cstart[c] = inc;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t v = cstart[lane];
+        uint32_t inc = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if ((int)lane >= d) inc += t2;
+        }
+        cstart[lane] = inc - v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+        const uint32_t r = threadIdx.x + qi * NT;
+        if (cls[qi] < 32u) {
+            const uint32_t e = cstart[cls[qi]] + hist[(qi * NWARP + warp) * 33 + cls[qi]] + below[qi];
+            order[e + (e >> 5)] = r;
+        }
+    }
+}
+
 // --------------------------------------------------------------------------
 // Where the G2P kernels take node velocities from.  UPD = 0: the velocity
 // grid of mpm_grid_update.  UPD = 1, 2, 3: the accumulators of mpm_p2g

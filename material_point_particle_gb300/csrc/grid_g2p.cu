@@ -30,10 +30,12 @@ template <int DIM, int T, int OUT, bool EL, bool VC>
 void launch_g2p_t(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w, float dt,
                   const DeviceInfo &dev, cudaStream_t st) {
     const float c4 = 4.0f * g.inv_dx;  // one fp32 rounding, as the oracle
-    constexpr int ORDER = OUT == kSorted ? kWarpSorted : (OUT == kBinOrder ? kWarpBinOrder : kWarpInPlace);
-    constexpr int NT = g2p_w_threads<ORDER>();
-    k_g2p_w<DIM, T, ORDER, EL, VC, 0><<<dev.sms * (1024 / NT), NT, 0, st>>>(
-        g, in, out, vel, 0.f, 0.f, 0.f, nullptr, w.count, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
+    if constexpr (OUT == kSorted)
+        k_g2p<DIM, T, EL, VC, 0><<<dev.sms * (1024 / kG2PThreads), kG2PThreads, 0, st>>>(
+            g, in, out, vel, 0.f, 0.f, 0.f, nullptr, w.count, w.perm, w.key, w.slices, w.start, w.status, dt, c4);
+    else
+        k_g2p_w<DIM, T, OUT == kBinOrder, EL, VC, 0><<<dev.sms * 4, kP2GThreads, 0, st>>>(
+            g, in, out, vel, 0.f, 0.f, 0.f, nullptr, w.count, w.perm, w.slices, w.start, w.status, dt, c4);
     if constexpr (OUT != kInPlace) k_copy_rest<DIM><<<dev.sms, 256, 0, st>>>(in, out, w.perm, w.status);
 }
 
