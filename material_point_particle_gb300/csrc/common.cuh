@@ -100,13 +100,15 @@ __device__ __forceinline__ void set_flag(uint32_t *status, int code) {
 // one IEEE fp32 rounding.  The floor goes through the fp32 adder: for
 // 0 <= y < 2^23 the sum y + 2^23 rounded down is 2^23 + floor(y) exactly, an
 // fp32 number whose bit pattern is that of 2^23 plus floor(y), so b is an
-// integer subtraction and (float)b a subtraction of 2^23 (no conversions;
-// grids have at most 2^20 nodes per axis, so y < 2^23).
+// integer subtraction and (float)b a subtraction of 2^23 (no conversions).
+// The domain test is then 0 <= b <= n - 3: grids have at most 2^20 nodes per
+// axis, so y = xi - 0.5 is exact wherever it can pass, and a y below 0, at or
+// above 2^23, infinite or NaN leaves a b outside that range.
 __device__ __forceinline__ bool base_frac(float x, float inv_dx, int n, int &b, float &f) {
     const float xi = __fmul_rn(x, inv_dx);
-    if (!(xi >= 0.5f && xi < __fsub_rn((float)n, 1.5f))) return false;
     const float t = __fadd_rd(__fsub_rn(xi, 0.5f), 8388608.0f);
     b = __float_as_int(t) - 0x4B000000;
+    if ((uint32_t)b > (uint32_t)(n - 3)) return false;
     f = __fsub_rn(xi, __fsub_rn(t, 8388608.0f));
     return true;
 }
