@@ -49,7 +49,9 @@ def with_outliers(cloud, k=11):
 # --------------------------------------------------------------------------
 # binning
 
-@pytest.mark.parametrize("dim,n,count", [(2, 64, 5003), (3, 40, 4099), (3, 24, 257), (2, 130, 31)])
+@pytest.mark.parametrize("dim,n,count", [(2, 64, 5003), (3, 40, 4099), (3, 24, 257), (2, 130, 31),
+                                         # whole spans of 128 keys only, and one key either side of a span
+                                         (3, 32, 4096), (3, 32, 128), (3, 32, 127), (2, 64, 129)])
 def test_bin_matches_oracle(dim, n, count):
     cloud = with_outliers(W.small_cloud(dim, count, n, seed=10 * dim + n, lo=0.02, hi=0.98))
     sys = make(cloud)
