@@ -53,9 +53,9 @@ SORT_PERIOD = 8
 # Each figure holds only while the kernel's sources are the ones it was measured on (sha256 of the files).
 MEASURED_TRAFFIC = {
     "p2g": {"bytes_per_particle": 82.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh', 'range.cuh'),
-            "sha256": "dede2e877384adad36c2420bd1dd31b6d3978bb2e627ba5f3cde883e804aed95"
+            "sha256": "edefb99ca279822bf7d50777c3f5979f02f56619c303ded74ec937898b9c4b16"
                       "c6cc35908d2c2d4dad606721b9323d2d91e3647b83e12b82580fbe3b7a077cfd"
-                      "29c6ee5f9c5e38a9e314dd0616fee49a4c72dfd86e3b4f221706ae2ad2345b91"
+                      "dd28ea0fe9334290303e9b5c221100014b52c7cea975b1d29b3d662a3330f405"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"
                       "02130a6b5dd5211e01db3ff2aad034b7816abc055a35d45fabd3753f8eeadc19"},
 }

@@ -82,23 +82,6 @@ __device__ __forceinline__ void scatter_float(const GridP &g, const Rec &rec, co
     }
 }
 
-// Work item: up to kSliceParticles consecutive binned particles of one tile.
-// The CTA zeroes the tile's halo accumulators, every thread scatters its
-// particles with shared atomics, and the CTA adds each nonzero node to the
-// grid once (neighbouring tiles overlap on the halo, so the flush adds).
-// Where one work item's particles sit in perm.
-struct SliceMeta {
-    uint32_t tile, beg, cnt;
-};
-
-__device__ __forceinline__ SliceMeta slice_meta(const uint32_t *slices, const uint32_t *start, uint32_t s) {
-    SliceMeta m;
-    m.tile = slices[2 * (size_t)s];
-    m.beg = start[m.tile] + slices[2 * (size_t)s + 1];
-    m.cnt = min((uint32_t)kSliceParticles, start[m.tile + 1] - m.beg);
-    return m;
-}
-
 // One warp per work item (a slice of at most 1024 binned particles of one
 // tile), so no CTA barrier couples the warps: each warp owns a compact halo
 // of the tile's (T+2)^dim nodes x (dim+1) int32 accumulators.  Per item: 32

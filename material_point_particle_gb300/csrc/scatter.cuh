@@ -195,25 +195,6 @@ __device__ __forceinline__ bool scatter_shares(const GridP &g, const Rec &rec, c
     return true;
 }
 
-// scatter_shares into a shared-memory tile accumulator `halo` (layout Hl)
-// covering the stencils of base cells in the box [o, o + TB) per axis.
-// False when the particle is outside the domain or the box, or (CHECK) out of
-// the 22-bit range.
-template <int DIM, int TB, typename Hl, bool EL, bool VC, bool CHECK, typename Rec>
-__device__ __forceinline__ bool scatter_fixed(const GridP &g, const Rec &rec, const int o[3], uint32_t halo,
-                                              const StressP &sp, uint32_t &degenerate) {
-    float f[3] = {0.f, 0.f, 0.f};
-    int b[3] = {0, 0, 0};
-    float xs[DIM];
-#pragma unroll
-    for (int l = 0; l < DIM; ++l) xs[l] = rec(l);
-    if (!in_box_x<DIM, TB>(g, xs, o, b, f)) return false;
-    const int hb = DIM == 3 ? (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY + (b[2] - o[2]) * Hl::SZ
-                            : (b[0] - o[0]) + (b[1] - o[1]) * Hl::SY;
-    const SharedAdd<Hl> ad{halo + 4u * (uint32_t)hb};
-    return scatter_shares<DIM, EL, VC, CHECK>(g, rec, f, ad, sp, degenerate);
-}
-
 // --------------------------------------------------------------------------
 // Shares of any size (up to the bound): the same values as scatter_shares,
 // each the exact product rounded once (rint_prod64), as int64.
