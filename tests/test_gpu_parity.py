@@ -524,14 +524,20 @@ def test_g2p_sorted_moves_particles_into_bin_order():
     assert speed == O.advective_speed(3, cloud["grid"]["dx"], ov[:, p], oC[:, p])
 
 
-def test_step_host_equals_device_sorted_step():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_step_host_equals_device_sorted_step(pinned):
+    """From and back to host arrays: page-locked ones (copied by a kernel through their device view) and
+    ordinary ones (one copy per array)."""
     cloud = W.small_cloud(3, 20000, 32, seed=501, scale_log2=19)
     a = make(cloud).enable_sorted()
     a.step_sorted()
     xa, va, Ca = a.state()
     ida = a.id.cpu().numpy()
     b = make(cloud).enable_sorted()
-    pin = lambda arr: torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
+    if pinned:
+        pin = lambda arr: torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
+    else:
+        pin = lambda arr: torch.from_numpy(np.array(arr, copy=True, order="C"))
     hx, hv, hC, hm = pin(cloud["x"]), pin(cloud["v"]), pin(cloud["C"]), pin(cloud["m"])
     hid = pin(np.arange(20000, dtype=np.int32))
     b.x.zero_()
