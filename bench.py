@@ -244,7 +244,7 @@ def run_ours(args, rank, world, local):
     eager_ms = aggregate_max(total_ms / args.steps, world, dev)
     # the same schedule again, as a CUDA graph replayed (the headline); the eager region above gives the
     # per-phase times, which a replay does not expose
-    graph = measure_graph(args, sys_, stream, world, dev)
+    graph = measure_graph(args.steps, bench_schedule(sys_), stream, world, dev)
     clk = clocks.stop()
     st = sys_.status()
     assert st[L.ST_FLAGS] == 0, f"status flags after timing {st[:8]}"
@@ -374,25 +374,15 @@ def run_ours(args, rank, world, local):
 ELASTIC = {"fsig": 0.05, "ppc": 1.0, "mu": 1.0e9, "lambda": 1.0e9}
 
 
-def measure_graph(args, sys_, stream, world, dev):
-    """The bench's schedule captured as one CUDA graph and replayed: a period of 2 * SORT_PERIOD steps (bin,
-    P2G, G2P with the update on load; the sorted G2P on every SORT_PERIOD-th step, so the ping-pong particle
-    buffers are back where they started at the end of the period), captured once on a side stream (capture
-    runs nothing), then replayed steps // period times and the steps left over run eagerly, all timed
-    together with CUDA events.  Every call's launches are the eager ones; only the launch overhead between
-    them goes."""
+def measure_graph(steps, run, stream, world, dev):
+    """A schedule captured as one CUDA graph and replayed.  run(count, s) issues `count` steps on stream s
+    (None: the current stream) starting at the first step of a period of 2 * SORT_PERIOD steps, after which the
+    ping-pong particle buffers are back where they started (two sorted G2P steps).  One period is captured on a
+    side stream (capture runs nothing), then replayed steps // period times and the steps left over run
+    eagerly, all timed together with CUDA events.  Every call's launches are the eager ones; only the launch
+    overhead between them goes."""
     import torch
     period = 2 * SORT_PERIOD
-
-    def run(count, s):
-        for k in range(count):
-            sys_.bin(s)
-            sys_.p2g(s)
-            if (k + 1) % SORT_PERIOD == 0:
-                sys_.g2p_sorted_update(s)
-            else:
-                sys_.g2p_update(s)
-
     try:
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
@@ -402,7 +392,7 @@ def measure_graph(args, sys_, stream, world, dev):
         torch.cuda.synchronize()
     except Exception as exc:       # report the eager numbers instead
         return {"error": f"capture failed: {type(exc).__name__}: {exc}"}
-    reps, rest = divmod(args.steps, period)
+    reps, rest = divmod(steps, period)
     barrier(world, dev)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -414,8 +404,24 @@ def measure_graph(args, sys_, stream, world, dev):
         t1.record(stream)
     torch.cuda.synchronize()
     barrier(world, dev)
-    ms = aggregate_max(t0.elapsed_time(t1) / args.steps, world, dev)
+    ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
     return {"ms_per_step": round(ms, 4), "period_steps": period, "replays": reps, "eager_steps": rest}
+
+
+def bench_schedule(sys_, fixed: bool = True):
+    """The bench's step schedule on sys_ as run(count, stream): bin, P2G, and G2P with the update on load
+    (fixed point; float atomics: the separate grid update, then G2P), sorted every SORT_PERIOD-th step."""
+    def run(count, s):
+        for k in range(count):
+            sort = (k + 1) % SORT_PERIOD == 0
+            sys_.bin(s)
+            sys_.p2g(s)
+            if fixed:
+                sys_.g2p_sorted_update(s) if sort else sys_.g2p_update(s)
+            else:
+                sys_.grid_update(s)
+                sys_.g2p_sorted(s) if sort else sys_.g2p(s)
+    return run
 
 
 def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume: bool):
@@ -661,8 +667,9 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
     order, is the cold step), then `steps` steps binning, checking the bound (range from the records in the
     fixed-point modes), scattering, updating and gathering (fixed point: the update applied as G2P loads the
     accumulators; float atomics: the separate grid update), in place with a sorted G2P every
-    SORT_PERIOD-th step.  Per-phase CUDA events; the roofline of the dominant kernel and of the whole step from the
-    algorithmic bytes: bin 24 B (2D 20 B) per particle; P2G 64 B (2D 36 B) per particle plus (dim+1)
+    SORT_PERIOD-th step.  Per-phase CUDA events; then the same schedule as a CUDA graph replayed
+    (measure_graph), whose step time is the row's.  The roofline of the dominant kernel and of the whole step
+    from the algorithmic bytes: bin 24 B (2D 20 B) per particle; P2G 64 B (2D 36 B) per particle plus (dim+1)
     accumulator words per touched node; grid update (dim+1) words per touched node; G2P 72 B (2D 40 B)."""
     import torch
     from material_point_particle_gb300 import _lib as L
@@ -711,9 +718,13 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
         e[4].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    eager_ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
+    # the same schedule replayed as a CUDA graph (the row's step time; the eager region gives the phases)
+    graph = measure_graph(steps, bench_schedule(ws, fixed), stream, world, dev)
+    graph["eager_ms_per_step"] = round(eager_ms, 4)
     st = ws.status()
     assert st[L.ST_FLAGS] == 0, f"{label}: status flags {st[:8]}"
-    ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
+    ms = graph.get("ms_per_step", eager_ms)
     names = ["bin", "p2g", "grid_update", "g2p"]
     parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev]).mean(axis=0)
     wacc = 8.0 if grid["acc_mode"] == L.MPM_ACC_I64 else 4.0
@@ -729,6 +740,7 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
            "scale_log2": grid["scale_log2"] if fixed else None,
            "share_path": (("22-bit" if st[L.ST_SHARE_PATH] == 0 else "int64") if fixed else None),
            "steps": steps, "ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT,
+           "cuda_graph": graph,
            "cold_step_ms": round(cold, 4),
            "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, parts)},
            "transfer_ms": round(float(parts[1:].sum()), 4),
