@@ -429,7 +429,7 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     Neo-Hookean mu = lambda = 1e9: the stress folded into P2G's affine matrix,
     F advanced in G2P) and/or the grid-recovered volume channel (rest volume
     V0 = dx^3 scattered and gathered back).  Timed like the main region (the same
-    G2P schedule), in the steady state, per phase."""
+    G2P schedule), in the steady state, per phase; then replayed as a CUDA graph (the step time)."""
     import torch
     from material_point_particle_gb300 import _lib as L
     from material_point_particle_gb300 import workloads as W
@@ -470,9 +470,13 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
         e[3].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    eager_ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
+    # the same schedule replayed as a CUDA graph (the row's step time; the eager region gives the phases)
+    graph = measure_graph(steps, bench_schedule(es), stream, world, dev)
+    graph["eager_ms_per_step"] = round(eager_ms, 4)
+    ms = graph.get("ms_per_step", eager_ms)
     st = es.status()
     assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
-    ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
     parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev]).mean(axis=0)
     names = ["bin", "p2g", "g2p_update"]
     es.bin(stream)
@@ -488,6 +492,7 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     dom = "p2g" if parts[1] >= parts[2] else "g2p_update"
     achieved = alg[dom] / (parts[names.index(dom)] * 1e-3) / 1e9
     out = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+           "cuda_graph": graph,
            "breakdown_ms": {k: round(float(v), 4) for k, v in zip(names, parts)},
            "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
@@ -509,7 +514,8 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
 def measure_fused(args, cloud, dev, stream, world, peak, touched, bin_ms):
     """The same workload stepped by mpm_step_fused (bin, then one kernel for the grid
     update, G2P and the next P2G, then the clear of the grid it read), after sorted
-    steps have written the bank-class interleave; `steps` fused steps in a row."""
+    steps have written the bank-class interleave; `steps` fused steps in a row, then as many replayed as a
+    CUDA graph (the step time)."""
     import torch
     from material_point_particle_gb300 import _lib as L
     from material_point_particle_gb300.system import MPMSystem
@@ -529,16 +535,25 @@ def measure_fused(args, cloud, dev, stream, world, peak, touched, bin_ms):
         fs.step_fused(stream)
         ev[k + 1].record(stream)
     torch.cuda.synchronize()
+    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    eager_ms = aggregate_max(ev[0].elapsed_time(ev[steps]) / steps, world, dev)
+
+    def run(count, s):   # every fused step swaps both buffer pairs: a period of 16 ends where it began
+        for _ in range(count):
+            fs.step_fused(s)
+
+    graph = measure_graph(steps, run, stream, world, dev)
+    graph["eager_ms_per_step"] = round(eager_ms, 4)
+    ms = graph.get("ms_per_step", eager_ms)
     st = fs.status()
     assert st[L.ST_FLAGS] == 0, f"status flags {st[:8]}"
-    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
-    ms = aggregate_max(ev[0].elapsed_time(ev[steps]) / steps, world, dev)
     # algorithmic bytes of the fused kernel: read x, m, id (20 B) and write x, v, C, m, id (68 B) per
     # particle; read the accumulators R and write W (32 B each per touched node)
     kern_ms = ms - bin_ms
     achieved = (n * 88.0 + touched * 64.0) / (kern_ms * 1e-3) / 1e9
     q = max(1, steps // 10)
     out = {"ms_per_step": round(ms, 4), "value": round(n * world / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+           "cuda_graph": graph,
            "first_tenth_ms": round(float(np.mean(per[:q])), 4), "last_tenth_ms": round(float(np.mean(per[-q:])), 4),
            "escaped": int(st[L.ST_N_ESCAPED]), "out_of_range": int(st[L.ST_N_OUT_OF_RANGE]),
            "roofline": {"bound": "hbm", "kernel": "g2p2g + clear (step minus the main region's bin time)",
