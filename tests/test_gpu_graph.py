@@ -71,3 +71,31 @@ def test_graph_replay_matches_eager_steps(dim, n, count):
     assert sa[L.ST_FLAGS] == sb[L.ST_FLAGS] == 0
     for w in (L.ST_N_VALID, L.ST_MAX_SPEED, L.ST_G2P_RANGE, L.ST_RANGE, L.ST_SHARE_PATH):
         assert sa[w] == sb[w], w
+
+
+def test_graph_replay_of_fused_steps_matches_eager():
+    """mpm_step_fused (bin, the fused gather-scatter kernel, the clear) captured for 16 steps (both buffer
+    pairs back in place) and replayed twice, against 32 eager fused steps."""
+    cloud = W.small_cloud(3, 20000, 32, seed=7200, scale_log2=19, lo=0.1, hi=0.9, vsig=1.0, csig=2.0)
+    cloud["grid"]["g"] = [0.0, -9.8, 0.0]
+    a, b = make(cloud), make(cloud)
+    a.enable_fused()
+    b.enable_fused()
+    for _ in range(2 * PERIOD):
+        a.step_fused()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(PERIOD):
+            b.step_fused()
+    torch.cuda.synchronize()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    xa, va, Ca = a.state()
+    xb, vb, Cb = b.state()
+    for u, w in ((xa, xb), (va, vb), (Ca, Cb)):
+        assert np.array_equal(bits(u), bits(w))
+    assert a.status()[L.ST_FLAGS] == b.status()[L.ST_FLAGS] == 0
