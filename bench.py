@@ -211,8 +211,10 @@ def run_ours(args, rank, world, local):
             c1.record(stream)
     torch.cuda.synchronize()
     cold_ms = c0.elapsed_time(c1) if args.warmup > 0 else None
-    # from here on the bound takes its range from the records the previous P2G and G2P wrote
+    # from here on the bound takes its range from the records the previous P2G and G2P wrote, and each
+    # in-place G2P writes the next step's keys and tile histogram, which that step's binning takes
     sys_.use_range_records(True)
+    sys_.use_next_keys(True)
     # timed region
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
@@ -225,7 +227,7 @@ def run_ours(args, rank, world, local):
     for k in range(args.steps):
         e = ev[k]
         e[0].record(stream)
-        sys_.bin(stream)
+        sys_.bin(stream, keys_from_g2p=k % SORT_PERIOD != 0)   # the steps after an in-place G2P
         e[1].record(stream)
         sys_.p2g(stream)
         e[2].record(stream)
@@ -244,7 +246,7 @@ def run_ours(args, rank, world, local):
     eager_ms = aggregate_max(total_ms / args.steps, world, dev)
     # the same schedule again, as a CUDA graph replayed (the headline); the eager region above gives the
     # per-phase times, which a replay does not expose
-    graph = measure_graph(args.steps, bench_schedule(sys_), stream, world, dev)
+    graph = measure_graph(args.steps, bench_schedule(sys_, next_keys=True), stream, world, dev)
     clk = clocks.stop()
     st = sys_.status()
     assert st[L.ST_FLAGS] == 0, f"status flags after timing {st[:8]}"
@@ -408,13 +410,15 @@ def measure_graph(steps, run, stream, world, dev):
     return {"ms_per_step": round(ms, 4), "period_steps": period, "replays": reps, "eager_steps": rest}
 
 
-def bench_schedule(sys_, fixed: bool = True):
+def bench_schedule(sys_, fixed: bool = True, next_keys: bool = False):
     """The bench's step schedule on sys_ as run(count, stream): bin, P2G, and G2P with the update on load
-    (fixed point; float atomics: the separate grid update, then G2P), sorted every SORT_PERIOD-th step."""
+    (fixed point; float atomics: the separate grid update, then G2P), sorted every SORT_PERIOD-th step.
+    next_keys (int64, sys_.use_next_keys set): each binning after an in-place G2P takes the keys that G2P
+    wrote (MPM_BIN_KEYS_FROM_G2P); the first step of a period follows a sorted G2P and computes them."""
     def run(count, s):
         for k in range(count):
             sort = (k + 1) % SORT_PERIOD == 0
-            sys_.bin(s)
+            sys_.bin(s, keys_from_g2p=next_keys and k % SORT_PERIOD != 0)
             sys_.p2g(s)
             if fixed:
                 sys_.g2p_sorted_update(s) if sort else sys_.g2p_update(s)
@@ -450,6 +454,8 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     for _ in range(max(3, args.warmup)):
         es.step_sorted(stream)
     es.use_range_records(True)   # (the elastic state always takes the range pass: its C is stress-folded)
+    nk = not elastic   # the next keys from G2P (measured slower with the elastic state's G2P)
+    es.use_next_keys(nk)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     barrier(world, dev)
@@ -459,7 +465,7 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     for k in range(steps):
         e = ev[k]
         e[0].record(stream)
-        es.bin(stream)
+        es.bin(stream, keys_from_g2p=nk and k % SORT_PERIOD != 0)
         e[1].record(stream)
         es.p2g(stream)
         e[2].record(stream)
@@ -472,7 +478,7 @@ def measure_variant(args, cloud, dev, stream, world, peak, elastic: bool, volume
     torch.cuda.synchronize()
     eager_ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
     # the same schedule replayed as a CUDA graph (the row's step time; the eager region gives the phases)
-    graph = measure_graph(steps, bench_schedule(es), stream, world, dev)
+    graph = measure_graph(steps, bench_schedule(es, next_keys=nk), stream, world, dev)
     graph["eager_ms_per_step"] = round(eager_ms, 4)
     ms = graph.get("ms_per_step", eager_ms)
     st = es.status()
@@ -708,8 +714,11 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
             c1.record(stream)
     torch.cuda.synchronize()
     cold = c0.elapsed_time(c1)
+    nk = grid["acc_mode"] == L.MPM_ACC_I64   # the in-place G2P writes the next keys (int64 only)
     if fixed:
         ws.use_range_records(True)
+    if nk:
+        ws.use_next_keys(True)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     barrier(world, dev)
     torch.cuda.synchronize()
@@ -719,7 +728,7 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
         e = ev[k]
         sort = (k + 1) % SORT_PERIOD == 0
         e[0].record(stream)
-        ws.bin(stream)
+        ws.bin(stream, keys_from_g2p=nk and k % SORT_PERIOD != 0)
         e[1].record(stream)
         ws.p2g(stream)
         e[2].record(stream)
@@ -735,7 +744,7 @@ def measure_row(args, cloud, dev, stream, world, peak, steps, label):
     torch.cuda.synchronize()
     eager_ms = aggregate_max(t0.elapsed_time(t1) / steps, world, dev)
     # the same schedule replayed as a CUDA graph (the row's step time; the eager region gives the phases)
-    graph = measure_graph(steps, bench_schedule(ws, fixed), stream, world, dev)
+    graph = measure_graph(steps, bench_schedule(ws, fixed, nk), stream, world, dev)
     graph["eager_ms_per_step"] = round(eager_ms, 4)
     st = ws.status()
     assert st[L.ST_FLAGS] == 0, f"{label}: status flags {st[:8]}"

@@ -159,6 +159,7 @@ typedef struct mpm_bins {
     void *scratch;           /* internal */
     size_t scratch_bytes;
     int32_t range_from_g2p;  /* set by the caller (mpm_bins_init clears it): see mpm_p2g */
+    int32_t next_keys;       /* set by the caller (mpm_bins_init clears it): see mpm_g2p_update */
 } mpm_bins;
 
 /* Bytes of workspace mpm_bins_init needs for n particles on this grid. */
@@ -173,8 +174,10 @@ mpm_status mpm_bins_init(const mpm_grid_desc *desc, int64_t n, void *ws, size_t 
 size_t mpm_grid_acc_bytes(const mpm_grid_desc *desc);
 size_t mpm_grid_vel_bytes(const mpm_grid_desc *desc);
 
-/* Flags of mpm_bin. */
-enum { MPM_BIN_DEFAULT = 0 };
+/* Flags of mpm_bin.  MPM_BIN_KEYS_FROM_G2P: take the keys and the tile
+ * histogram the last mpm_g2p_update on these bins wrote with bins->next_keys
+ * set, instead of computing them (MPM_ACC_I64 only; see mpm_g2p_update). */
+enum { MPM_BIN_DEFAULT = 0, MPM_BIN_KEYS_FROM_G2P = 1 };
 
 /*
  * mpm_bin -- cell keys and a stable counting sort of the particles into tiles.
@@ -352,6 +355,17 @@ mpm_status mpm_g2p_binned(const mpm_grid_desc *desc, const float *grid_vel, cons
  * zero afterwards, as mpm_grid_update leaves it.  The bits of every particle
  * are those of mpm_grid_update followed by mpm_g2p.  The status words of
  * mpm_g2p (MPM_ST_MAX_SPEED, MPM_ST_G2P_RANGE) are written as it writes them.
+ *
+ * With bins->next_keys set (MPM_ACC_I64), the call also writes each moved
+ * particle's key of its new position into bins->key and the tile histogram of
+ * all the particles' next keys into the workspace (the particles outside the
+ * domain keep their key and their count), which the next mpm_bin takes with
+ * MPM_BIN_KEYS_FROM_G2P instead of computing them: the same keys and counts,
+ * the key pass skipped.  The caller promises that the positions are those the
+ * call wrote when it passes the flag; a particle whose position has left its
+ * key's tile since is found by mpm_p2g's box test and counted as one above the
+ * range (MPM_E_BOUND).  bins->key then holds the next keys, not those of the
+ * binning the call gathered with.
  */
 mpm_status mpm_g2p_update(const mpm_grid_desc *desc, void *grid_acc, const float dtg[3], mpm_particles *parts,
                           mpm_bins *bins, float dt, void *stream);

@@ -24,6 +24,7 @@ ST_MAX_SPEED = 13   # fp32 bits of max |v'| + 1.5 dx |C'|_F over the particles t
 ST_N_ESCAPED = 14   # mpm_step_fused: particles whose base cell left their tile (scattered into the global grid)
 ST_RANGE = 15       # fp32 bits of R, the range the last fixed-point P2G checked its bound with
 ST_SHARE_PATH = 16  # the last fixed-point P2G's shares: 0 below 2^22 (one fma each), 1 int64
+MPM_BIN_KEYS_FROM_G2P = 1  # mpm_bin flag: the keys and histogram the last mpm_g2p_update wrote
 ST_P2G_MASS = 20    # record: fp32 bits of max |m| over the particles the last P2G scattered
 ST_P2G_VOLUME = 21  # record: fp32 bits of max rest volume in cells over the same
 ST_G2P_RANGE = 22   # record: fp32 bits of max over the last G2P's particles of max(1, |v'_k| + 1.5 dx sum|C'_kl|)
@@ -54,7 +55,8 @@ class Bins(ct.Structure):
                 ("key", ct.c_void_p), ("perm", ct.c_void_p), ("tile_count", ct.c_void_p),
                 ("tile_start", ct.c_void_p), ("slices", ct.c_void_p), ("active", ct.c_void_p),
                 ("status", ct.c_void_p), ("scratch", ct.c_void_p), ("scratch_bytes", ct.c_size_t),
-                ("range_from_g2p", ct.c_int32)]
+                ("range_from_g2p", ct.c_int32),
+                ("next_keys", ct.c_int32)]
 
 
 _lock = threading.Lock()

@@ -79,7 +79,7 @@ mpm_status make_grid(const mpm_grid_desc *d, GridP &g) {
 
 struct Layout {
     size_t key, perm, heads, tails, count, start, hcnt, tcnt, active, slices, large_list, partial, status, cellcount,
-        readers,
+        readers, count_next,
         scratch, total;
     int64_t max_slices;
 };
@@ -115,6 +115,7 @@ Layout layout_of(const GridP &g, int64_t n) {
     L.status = take(MPM_STATUS_WORDS * sizeof(uint32_t));
     L.cellcount = g.acc_mode == MPM_ACC_I32 ? take((size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t)) : 0;
     L.readers = take((size_t)g.nblocks * sizeof(uint32_t));
+    L.count_next = take(nb * sizeof(uint32_t));
     L.scratch = take(2 * sizeof(uint64_t));
     L.total = off;
     return L;
@@ -140,6 +141,7 @@ WsView view_of(const GridP &g, const mpm_bins &b) {
     w.partial = reinterpret_cast<uint32_t *>(base + L.partial);
     w.cellcount = g.acc_mode == MPM_ACC_I32 ? reinterpret_cast<uint32_t *>(base + L.cellcount) : nullptr;
     w.readers = reinterpret_cast<uint32_t *>(base + L.readers);
+    w.count_next = reinterpret_cast<uint32_t *>(base + L.count_next);
     return w;
 }
 
@@ -299,13 +301,15 @@ size_t mpm_grid_vel_bytes(const mpm_grid_desc *desc) {
 mpm_status mpm_bin(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, int flags, void *stream) {
     GridP g;
     MPM_TRY(make_grid(desc, g));
-    if (g.acc_mode == MPM_ACC_EXACT_INT || flags != 0) return MPM_E_ARG;
+    if (g.acc_mode == MPM_ACC_EXACT_INT || (flags & ~MPM_BIN_KEYS_FROM_G2P) != 0) return MPM_E_ARG;
+    const bool from_g2p = (flags & MPM_BIN_KEYS_FROM_G2P) != 0;
+    if (from_g2p && g.acc_mode != MPM_ACC_I64) return MPM_E_ARG;
     PartsF p;
     MPM_TRY(parts_f(g, parts, false, p));
     MPM_TRY(check_bins(g, bins, p.n));
     DeviceInfo dev;
     MPM_TRY(device_info(dev));
-    return launch_bin(g, p, view_of(g, *bins), dev, static_cast<cudaStream_t>(stream));
+    return launch_bin(g, p, view_of(g, *bins), from_g2p, dev, static_cast<cudaStream_t>(stream));
 }
 
 mpm_status mpm_p2g(const mpm_grid_desc *desc, const mpm_particles *parts, mpm_bins *bins, void *grid_acc,
@@ -412,7 +416,8 @@ mpm_status mpm_g2p_update(const mpm_grid_desc *desc, void *grid_acc, const float
     MPM_TRY(check_bins(g, bins, p.n));
     DeviceInfo dev;
     MPM_TRY(device_info(dev));
-    return launch_g2p_update(g, grid_acc, dtg, p, p, view_of(g, *bins), dt, false, dev,
+    if (bins->next_keys && g.acc_mode != MPM_ACC_I64) return MPM_E_ARG;
+    return launch_g2p_update(g, grid_acc, dtg, p, p, view_of(g, *bins), dt, false, bins->next_keys != 0, dev,
                              static_cast<cudaStream_t>(stream));
 }
 
@@ -428,7 +433,7 @@ mpm_status mpm_g2p_sorted_update(const mpm_grid_desc *desc, void *grid_acc, cons
     MPM_TRY(check_bins(g, bins, pi.n));
     DeviceInfo dev;
     MPM_TRY(device_info(dev));
-    return launch_g2p_update(g, grid_acc, dtg, pi, po, view_of(g, *bins), dt, true, dev,
+    return launch_g2p_update(g, grid_acc, dtg, pi, po, view_of(g, *bins), dt, true, false, dev,
                              static_cast<cudaStream_t>(stream));
 }
 

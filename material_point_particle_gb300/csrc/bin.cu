@@ -24,8 +24,9 @@
 // the same code sorts indices.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
-//   k_keys          key per particle, tile histogram aggregated over runs,
-//                   out-of-domain count (int32 mode: per-cell counts)
+//   k_keys          key per particle, tile histogram aggregated over runs
+//                   (int32 mode: per-cell counts); skipped when the last G2P
+//                   wrote both (MPM_BIN_KEYS_FROM_G2P)
 //   k_scan_reduce / k_scan_top / k_scan_final
 //                   exclusive scans of (count, P2G slices, active flag) over
 //                   the buckets; active-tile list, P2G work list; clears the
@@ -45,20 +46,6 @@
 namespace mpm {
 
 constexpr int kKeysUnroll = 4;   // particles per lane per iteration (loads in flight)
-
-// --------------------------------------------------------------------------
-// Tile-major cell key with the tile shape known at compile time.
-template <int DIM, int T>
-__device__ __forceinline__ uint32_t cell_key_t(const GridP &g, const int b[3]) {
-    constexpr int LOG = T == 4 ? 2 : 3;
-    uint32_t tile = 0, local = 0;
-#pragma unroll
-    for (int l = DIM - 1; l >= 0; --l) {
-        tile = tile * (uint32_t)g.nt[l] + ((uint32_t)b[l] >> LOG);
-        local = (local << LOG) | ((uint32_t)b[l] & (T - 1));
-    }
-    return (tile << (DIM * LOG)) | local;
-}
 
 // Keys of the 32 * kKeysUnroll particles from `base` (FULL: all below n, so
 // no bounds tests); tile histogram aggregated over runs of equal buckets
@@ -106,12 +93,11 @@ __device__ __forceinline__ void keys_span(const GridP &g, const PartsF &p, int64
             const uint32_t later = heads & ~((2u << lane) - 1u);   // heads after this lane (lane 31: none)
             const uint32_t stop = later ? (uint32_t)(__ffs(later) - 1) : (uint32_t)(32 - __clz(live));
             atomicAdd(&count[bucket], stop - lane);
-            if (bucket == bucket_invalid) atomicAdd(&status[MPM_ST_N_OUTSIDE], stop - lane);
         }
     }
 }
 
-// Key per particle, tile histogram (keys_span), out-of-domain count.
+// Key per particle and tile histogram (keys_span).
 template <int DIM, int T>
 __global__ void __launch_bounds__(256) k_keys(GridP g, PartsF p, uint32_t *__restrict__ key,
                                               uint32_t *__restrict__ count, uint32_t *__restrict__ cellcount,
@@ -190,7 +176,8 @@ __global__ void k_scan_reduce(const uint32_t *__restrict__ count, int64_t nb, To
     if (threadIdx.x == 0) partial[blockIdx.x] = tot;
 }
 
-// One block: exclusive scan of the block totals (in place) and the grand totals.
+// One block: exclusive scan of the block totals (in place) and the grand totals (with the
+// in-domain and outside counts).
 __global__ void k_scan_top(Tot3 *__restrict__ partial, int64_t nblocks, const uint32_t *__restrict__ count,
                            int64_t nb, uint32_t *__restrict__ status) {
     Tot3 carry = tot_zero();
@@ -203,6 +190,7 @@ __global__ void k_scan_top(Tot3 *__restrict__ partial, int64_t nblocks, const ui
         carry = tot_add(carry, tot);
     }
     if (threadIdx.x == 0) {
+        status[MPM_ST_N_OUTSIDE] = count[nb - 1];
         status[MPM_ST_N_VALID] = carry.v[0] - count[nb - 1];
         status[MPM_ST_N_SLICES] = carry.v[1];
         status[MPM_ST_N_ACTIVE] = carry.v[2];
@@ -634,7 +622,7 @@ __global__ void k_nbr_bound(GridP g, const uint32_t *__restrict__ cellcount, uin
 }
 
 // --------------------------------------------------------------------------
-mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const DeviceInfo &dev,
+mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, bool keys_from_g2p, const DeviceInfo &dev,
                       cudaStream_t st) {
     const int64_t n = p.n;
     const int64_t nb = g.ntiles + 1;
@@ -643,12 +631,17 @@ mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const De
     cudaMemsetAsync(w.status, 0, MPM_ST_P2G_MASS * sizeof(uint32_t), st);
     cudaMemsetAsync(&w.status[MPM_ST_G2P_RANGE + 1], 0, (MPM_STATUS_WORDS - MPM_ST_G2P_RANGE - 1) * sizeof(uint32_t),
                     st);
-    cudaMemsetAsync(w.count, 0, nb * sizeof(uint32_t), st);
-    if (w.cellcount) cudaMemsetAsync(w.cellcount, 0, (size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t), st);
     const int threads = 256;
     const int64_t span = (int64_t)threads * kKeysUnroll;
     const int grid_p = (int)std::max<int64_t>(1, std::min<int64_t>((n + span - 1) / span, dev.sms * 8));
-    if (n > 0) {
+    if (keys_from_g2p) {
+        // the keys (in place) and their histogram, written by the last G2P at the positions it wrote
+        cudaMemcpyAsync(w.count, w.count_next, nb * sizeof(uint32_t), cudaMemcpyDeviceToDevice, st);
+    } else {
+        cudaMemsetAsync(w.count, 0, nb * sizeof(uint32_t), st);
+        if (w.cellcount) cudaMemsetAsync(w.cellcount, 0, (size_t)(g.ntiles << g.cpt_log2) * sizeof(uint32_t), st);
+    }
+    if (n > 0 && !keys_from_g2p) {
         if (g.dim == 3)
             k_keys<3, 4><<<grid_p, threads, 0, st>>>(g, p, w.key, w.count, w.cellcount, w.status);
         else

@@ -113,6 +113,30 @@ __device__ __forceinline__ bool base_frac(float x, float inv_dx, int n, int &b, 
     return true;
 }
 
+// Tile-major cell key with the tile shape known at compile time.
+template <int DIM, int T>
+__device__ __forceinline__ uint32_t cell_key_t(const GridP &g, const int b[3]) {
+    constexpr int LOG = T == 4 ? 2 : 3;
+    uint32_t tile = 0, local = 0;
+#pragma unroll
+    for (int l = DIM - 1; l >= 0; --l) {
+        tile = tile * (uint32_t)g.nt[l] + ((uint32_t)b[l] >> LOG);
+        local = (local << LOG) | ((uint32_t)b[l] & (T - 1));
+    }
+    return (tile << (DIM * LOG)) | local;
+}
+
+// The key of position x (kKeyInvalid outside the domain), as the binning computes it.
+template <int DIM, int T>
+__device__ __forceinline__ uint32_t key_of_x(const GridP &g, const float (&x)[DIM]) {
+    int b[3] = {0, 0, 0};
+    float f;
+    bool ok = true;
+#pragma unroll
+    for (int l = 0; l < DIM; ++l) ok = base_frac(x[l], g.inv_dx, g.n[l], b[l], f) && ok;
+    return ok ? cell_key_t<DIM, T>(g, b) : kKeyInvalid;
+}
+
 // Quadratic B-spline weights at distances f, f-1, f-2 from the stencil's
 // first node (f in [0.5, 1.5)).
 __device__ __forceinline__ void quad_weights(float f, float w[3]) {

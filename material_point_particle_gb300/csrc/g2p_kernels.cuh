@@ -50,16 +50,17 @@ __device__ __forceinline__ void copy_particle(const PartsF &p, const PartsF &q, 
 // rounds each lane exactly as the scalar operation.  Elastic particles (EL)
 // read F (and, sorted, vol) of `pid` from global memory and write F'; with
 // the volume channel (VC) the particle's grid-recovered volume fraction is
-// gathered as v is and written to phi.
+// gathered as v is and written to phi.  xo: the particle's position after the
+// call (the new one when it moved).
 template <int DIM, int T, bool MOVED, bool EL, bool VC, typename Rec>
 __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, const PartsF &q, uint32_t pid,
                                            uint32_t dst, const Rec &rec, const int o[3], const VelHalo<DIM, T> &sv,
-                                           float dt, float c4, float &smax, uint32_t &rmax) {
+                                           float dt, float c4, float &smax, uint32_t &rmax, float (&xo)[DIM]) {
     using Hl = HaloU<DIM, T>;
     float x[DIM], f[3] = {0.f, 0.f, 0.f};
     int b[3] = {0, 0, 0};
 #pragma unroll
-    for (int l = 0; l < DIM; ++l) x[l] = rec(l);
+    for (int l = 0; l < DIM; ++l) xo[l] = x[l] = rec(l);
     if (!in_tile_x<DIM>(g, x, o, b, f)) {
         if constexpr (MOVED) copy_particle<DIM>(p, q, pid, dst);
         return;
@@ -107,7 +108,7 @@ __device__ __forceinline__ void gather_one(const GridP &g, const PartsF &p, cons
     // the range the next P2G's bound may take from this record: max(1, |v'_k| + 1.5 dx sum_l |C'_kl|)
     rmax = max(rmax, range_r_bits<DIM>(vn, Cn, __fmul_rn(1.5f, g.dx)));
 #pragma unroll
-    for (int l = 0; l < DIM; ++l) q.x[l][dst] = __fmaf_rn(dt, vn[l], x[l]);
+    for (int l = 0; l < DIM; ++l) q.x[l][dst] = xo[l] = __fmaf_rn(dt, vn[l], x[l]);
     if constexpr (MOVED) {
         const_cast<float *>(q.m)[dst] = rec(DIM);
         if (q.id) q.id[dst] = __float_as_uint(rec(DIM + 1));
@@ -200,7 +201,8 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
             if (threadIdx.x < cnt) {
                 const uint32_t r = threadIdx.x;
                 auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
-                gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax, rmax);
+                float xo[DIM];
+                gather_one<DIM, T, true, EL, VC>(g, p, q, pids[0], beg + r, rec, o, sv, dt, c4, smax, rmax, xo);
             }
         } else {
             class_order<DIM, T, kG2PThreads>(key, pids, cnt, hist, cstart, order);
@@ -213,8 +215,9 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
                     const uint32_t e = interleave_entry(pos, cnt);
                     const uint32_t r = order[e + (e >> 5)];
                     auto rec = [&](int f) { return sbuf[f * kSliceParticles + r]; };
+                    float xo[DIM];
                     gather_one<DIM, T, true, EL, VC>(g, p, q, perm[beg + r], beg + pos, rec, o, sv, dt, c4, smax,
-                                                     rmax);
+                                                     rmax, xo);
                 }
             }
         }
@@ -234,8 +237,10 @@ __global__ void __launch_bounds__(kG2PThreads) k_g2p(GridP g, PartsF p, PartsF q
 // (BINORDER), out[j] = the new state of in[perm[j]]: x, m and id are copied
 // into a per-warp double buffer in shared memory a round ahead, and
 // consecutive lanes write consecutive places.  No block barrier couples the
-// warps.
-template <int DIM, int T, bool BINORDER, bool EL, bool VC, int UPD>
+// warps.  NK (in place): each lane also writes the key of its particle's new
+// position to next_key and adds it to the tile histogram count_next (the
+// binning of the next step takes both, MPM_BIN_KEYS_FROM_G2P).
+template <int DIM, int T, bool BINORDER, bool EL, bool VC, int UPD, bool NK = false>
 __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF q, const void *__restrict__ src,
                                                        float dtg0, float dtg1, float dtg2,
                                                        uint32_t *__restrict__ readers,
@@ -243,7 +248,9 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
                                                        const uint32_t *__restrict__ perm,
                                                        const uint32_t *__restrict__ slices,
                                                        const uint32_t *__restrict__ start,
-                                                       uint32_t *__restrict__ status, float dt, float c4) {
+                                                       uint32_t *__restrict__ status, float dt, float c4,
+                                                       uint32_t *__restrict__ next_key = nullptr,
+                                                       uint32_t *__restrict__ count_next = nullptr) {
     using Hl = HaloU<DIM, T>;
     constexpr int NW = kP2GThreads / 32;
     constexpr int NCH = DIM + (VC ? 1 : 0);
@@ -306,9 +313,23 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
 #pragma unroll
                 for (int l = 0; l < DIM; ++l) xn[l] = r + 32 < cnt ? p.x[l][pid_next] : 0.f;
                 const uint32_t pid_after = r + 64 < cnt ? perm[beg + r + 64] : 0u;
+                float xo[DIM];
                 if (r < cnt) {
                     auto rec = [&](int f) { return xc[f]; };
-                    gather_one<DIM, T, false, EL, VC>(g, p, q, pid, pid, rec, o, sv, dt, c4, smax, rmax);
+                    gather_one<DIM, T, false, EL, VC>(g, p, q, pid, pid, rec, o, sv, dt, c4, smax, rmax, xo);
+                }
+                if constexpr (NK) {
+                    // the key of the position just written, and its tile's count (one add per tile a round)
+                    constexpr int LOG = T == 4 ? 2 : 3;
+                    const bool live = r < cnt;
+                    uint32_t bk = 0xFFFFFFFFu;
+                    if (live) {
+                        const uint32_t k = key_of_x<DIM, T>(g, xo);
+                        next_key[pid] = k;
+                        bk = k == kKeyInvalid ? (uint32_t)g.ntiles : k >> (DIM * LOG);
+                    }
+                    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bk);
+                    if (live && (peers & lanemask_lt()) == 0) atomicAdd(&count_next[bk], (uint32_t)__popc(peers));
                 }
 #pragma unroll
                 for (int l = 0; l < DIM; ++l) xc[l] = xn[l];
@@ -327,8 +348,9 @@ __global__ void __launch_bounds__(kP2GThreads) k_g2p_w(GridP g, PartsF p, PartsF
                 if (r < cnt) {
                     const int st = stage;
                     auto rec = [&](int f) { return *at(st, f); };
+                    float xo[DIM];
                     gather_one<DIM, T, BINORDER, EL, VC>(g, p, q, pid, BINORDER ? beg + r : pid, rec, o, sv, dt, c4,
-                                                         smax, rmax);
+                                                         smax, rmax, xo);
                 }
                 stage ^= 1;
             }

@@ -30,6 +30,7 @@ struct WsView {
     uint32_t *status;     // [MPM_STATUS_WORDS]
     uint32_t *cellcount;  // int32 mode only: [ntiles * T^dim], else null
     uint32_t *readers;    // [nblocks] work items that have read each node block (G2P with the update on load)
+    uint32_t *count_next; // [ntiles + 1] the histogram of the next keys a G2P wrote (MPM_BIN_KEYS_FROM_G2P)
 };
 
 struct DeviceInfo {
@@ -39,7 +40,8 @@ struct DeviceInfo {
 
 mpm_status device_info(DeviceInfo &out);
 
-mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, const DeviceInfo &dev, cudaStream_t st);
+mpm_status launch_bin(const GridP &g, const PartsF &p, const WsView &w, bool keys_from_g2p, const DeviceInfo &dev,
+                      cudaStream_t st);
 mpm_status launch_p2g(const GridP &g, const PartsF &p, const WsView &w, void *grid_acc, float dt, bool records,
                       const DeviceInfo &dev, cudaStream_t st);
 void launch_rollback(const GridP &g, void *grid_acc, const uint32_t *status, const DeviceInfo &dev,
@@ -58,7 +60,8 @@ void launch_clear_blocks(const GridP &g, long long *acc, const WsView &w, const 
 mpm_status launch_iterate(const GridP &g, const PartsF &p, const WsView &w, void *acc_a, void *acc_b,
                           int iterations, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_g2p_update(const GridP &g, const void *acc, const float dtg[3], const PartsF &in, const PartsF &out,
-                             const WsView &w, float dt, bool sorted, const DeviceInfo &dev, cudaStream_t st);
+                             const WsView &w, float dt, bool sorted, bool next_keys, const DeviceInfo &dev,
+                             cudaStream_t st);
 mpm_status launch_g2p_binned(const GridP &g, const float *vel, const PartsF &in, const PartsF &out, const WsView &w,
                              float dt, const DeviceInfo &dev, cudaStream_t st);
 mpm_status launch_permute(const GridP &g, const PartsF &in, const PartsF &out, const uint32_t *perm,

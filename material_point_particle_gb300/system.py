@@ -108,9 +108,15 @@ class MPMSystem:
         self.bins.range_from_g2p = 1 if on else 0
         return self
 
+    def use_next_keys(self, on: bool = True):
+        """With ``on``, mpm_g2p_update (in place, int64) also writes the keys of the particles' new
+        positions and their tile histogram, which bin(keys_from_g2p=True) then takes (see mpm_g2p_update)."""
+        self.bins.next_keys = 1 if on else 0
+        return self
+
     # -- the library calls ----------------------------------------------------
-    def bin(self, stream=None):
-        L.mpm_bin(self.desc, self.parts, self.bins, 0, stream)
+    def bin(self, stream=None, keys_from_g2p: bool = False):
+        L.mpm_bin(self.desc, self.parts, self.bins, L.MPM_BIN_KEYS_FROM_G2P if keys_from_g2p else 0, stream)
 
     def p2g(self, stream=None):
         L.mpm_p2g(self.desc, self.parts, self.bins, self.acc, self.dt, stream)

@@ -154,3 +154,40 @@ def test_g2p_update_rejects_float_mode():
     a.p2g()
     with pytest.raises(L.MPMError):
         a.g2p_update()
+
+
+@pytest.mark.parametrize("state", ["plain", "elastic", "volume"])
+def test_bin_with_keys_from_g2p_equals_computed_bin(state):
+    """In-place steps whose G2P writes the next keys and their histogram (bins.next_keys) and whose binning
+    takes them (MPM_BIN_KEYS_FROM_G2P) give, step after step, the keys, permutation, tile counts, status
+    words and particle state of steps that compute them (particles outside the domain included)."""
+    cloud = cloud_for(3, W.ACC_I64, 32, 6007, seed=9500, state=state)
+    a, b = make(cloud), make(cloud)
+    b.use_next_keys(True)
+    for step in range(4):
+        a.bin()
+        b.bin(keys_from_g2p=step > 0)
+        torch.cuda.synchronize()
+        ka, pa, ca = a.bins_arrays()
+        kb, pb, cb = b.bins_arrays()
+        assert np.array_equal(ka, kb) and np.array_equal(pa, pb) and np.array_equal(ca, cb), step
+        sa, sb = a.status(), b.status()
+        for w in range(L.ST_BIN_WORDS):
+            assert sa[w] == sb[w], (step, w)
+        a.p2g()
+        b.p2g()
+        a.g2p_update()
+        b.g2p_update()
+        torch.cuda.synchronize()
+        same_state(a, b)
+
+
+def test_next_keys_refused_outside_int64():
+    cloud = cloud_for(3, W.ACC_I32, 24, 2500, seed=9600)
+    a = make(cloud).use_next_keys(True)
+    a.bin()
+    a.p2g()
+    with pytest.raises(L.MPMError):
+        a.g2p_update()
+    with pytest.raises(L.MPMError):
+        a.bin(keys_from_g2p=True)
