@@ -54,7 +54,7 @@ SORT_PERIOD = 8
 MEASURED_TRAFFIC = {
     "p2g": {"bytes_per_particle": 82.2, "files": ('p2g.cu', 'common.cuh', 'scatter.cuh', 'stress.cuh', 'range.cuh'),
             "sha256": "edefb99ca279822bf7d50777c3f5979f02f56619c303ded74ec937898b9c4b16"
-                      "c6cc35908d2c2d4dad606721b9323d2d91e3647b83e12b82580fbe3b7a077cfd"
+                      "4b1028dc922c926810222c631f1419edb36b336f9f5cae2e932a541931a000b7"
                       "dd28ea0fe9334290303e9b5c221100014b52c7cea975b1d29b3d662a3330f405"
                       "0c768a7fc62f6362d0285363fbfdcf0a3b8aa8e57edfd3d35d19bd9133d859f2"
                       "02130a6b5dd5211e01db3ff2aad034b7816abc055a35d45fabd3753f8eeadc19"},
