@@ -389,7 +389,8 @@ def measure_graph(steps, run, stream, world, dev):
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=side):
+        # thread_local: CUDA calls of other threads (a process group's watchdog) do not void the capture
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
             run(period, None)      # None: the capturing stream
         torch.cuda.synchronize()
     except Exception as exc:       # report the eager numbers instead
